@@ -1,0 +1,170 @@
+/*
+ * qmoe.h -- C ABI of the QMoE layer forward on one GB300 (sm_103a).
+ *
+ * The operator is the quantized Mixture-of-Experts layer of the ONNX Runtime
+ * QMoE contrib op as described in the microsoft/onnxruntime pull requests
+ * "Document and test packed token inputs for MoE and QMoE" (#32522),
+ * "[CUDA] Add INT4 and INT3 QMoE CPU/GPU offload support" (#33575, with the
+ * merged texts of #33622, #33629, #33731 and #33624) and "[CUDA] Add MoEPacked
+ * CPU/GPU hybrid offload ..." (#33973). For packed token-major input it computes
+ *
+ *   route   per token t: the top_k largest raw router logits, ties to the lower
+ *           expert index, listed by descending logit; weights w[t,j] = softmax
+ *           over those top_k logits (#32522: QMoE takes raw logits and applies
+ *           top-k then normalisation; reference = softmax over the top-k);
+ *   group   the T*top_k routes r = t*top_k + j sorted by expert, stable in r;
+ *   fc1     gu = W1_e x_t with W1_e = dequant(fc1_q[e]) of shape [2*inter, hidden],
+ *           rows interleaved: row 2i is gate_i, row 2i+1 is up_i (#33575 review:
+ *           the producer interleaves gate/up rows and their scales);
+ *   swiglu  h_i = silu(gate_i) * up_i, silu(z) = z / (1 + exp(-z))
+ *           (activation_type "swiglu", swiglu_fusion = 1; #33624 fixture update);
+ *   fc2     y = W2_e h with W2_e = dequant(fc2_q[e]) of shape [hidden, inter];
+ *   combine out[t] = round_once( sum_j w[t,j] * y[t*top_k + j] ), j ascending,
+ *           FP32 sum, one rounding to the output type, NaN kept NaN, routes with
+ *           w == 0 skipped (#33973 key change 4 and review fixes).
+ *
+ * Dequantisation (#33575 description and #33624 text: unsigned codes, "INT3
+ * zero-point code 4", raw layout weights_prepacked = 0, block_size in
+ * {32, 64, 128}; #33624 review: scales [N, K/32] row-major):
+ *   W[n][kk] = (code[n][kk] - zp[n][kk / block]) * scale[n][kk / block].
+ *
+ * Layouts (all row-major, all buffers caller-owned device memory):
+ *   x            [T][hidden]                        dtype
+ *   router_logits[T][num_experts]                   dtype (raw logits)
+ *   fc1_q        [E][2*inter][hidden*bits/8]        uint8 packed codes
+ *   fc1_scales   [E][2*inter][hidden/block_size]    dtype
+ *   fc1_zp       [E][2*inter][hidden/block_size]    uint8, one code per byte, or NULL
+ *   fc2_q        [E][hidden][inter*bits/8]          uint8 packed codes
+ *   fc2_scales   [E][hidden][inter/block_size]      dtype
+ *   fc2_zp       [E][hidden][inter/block_size]      uint8 or NULL
+ *   out          [T][hidden]                        dtype
+ * Codes are packed least-significant bits first along K as one continuous bit
+ * stream: INT4 code 2c is the low nibble of byte c, INT2 has four codes per byte,
+ * INT3 eight codes per 3-byte little-endian group (code i at bits 3i..3i+2).
+ * A NULL zero-point pointer means the zero point 2^(bits-1) (8, 4 or 2).
+ *
+ * Precision. Routing compares raw logits exactly; weights use FP32 expf. The
+ * expert matmuls run on tensor cores with FP16 operands and FP32 accumulation:
+ * dequantised weights (code - zp) * scale are exact in FP16 for BF16 scales in
+ * [2^-14, 2^12] and round once for FP16 scales; each token's activations are
+ * scaled by a power of two so that their largest magnitude lies in [1, 2)
+ * before the FP16 conversion, and the SwiGLU output is stored in FP16 with the
+ * square of that power of two. The combine sums in FP32 and rounds once.
+ *
+ * Threading and ordering. Every call only enqueues kernels on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and returns; it never
+ * synchronises and never copies device to host. The library allocates no
+ * memory and keeps no state between calls: all scratch lives in the caller's
+ * workspace. Concurrent calls on different streams need distinct workspaces.
+ *
+ * Errors are returned before any launch, for: null problem or required
+ * pointer, T < 0, num_experts <= 0, top_k <= 0, top_k > num_experts, hidden or
+ * inter <= 0 (QMOE_ERR_INVALID_ARGUMENT; #33575: validate positive expert and
+ * feature dimensions before any arithmetic); bits not in {2,3,4}, block_size
+ * not in {32,64,128}, block_size not dividing hidden and inter, hidden or inter
+ * not a multiple of 32, num_experts > 512, top_k > 32, unsupported dtype or path
+ * (QMOE_ERR_UNSUPPORTED); a pointer that is not 16-byte aligned
+ * (QMOE_ERR_MISALIGNED); a workspace smaller than qmoe_workspace_bytes()
+ * (QMOE_ERR_WORKSPACE_TOO_SMALL). T == 0 returns QMOE_OK with no launch (#33973:
+ * empty input is handled). A failed launch returns QMOE_ERR_CUDA.
+ */
+#ifndef QMOE_H
+#define QMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { QMOE_BF16 = 0, QMOE_FP16 = 1 } qmoe_dtype;
+
+typedef enum {
+  QMOE_OK = 0,
+  QMOE_ERR_INVALID_ARGUMENT = 1,
+  QMOE_ERR_UNSUPPORTED = 2,
+  QMOE_ERR_MISALIGNED = 3,
+  QMOE_ERR_WORKSPACE_TOO_SMALL = 4,
+  QMOE_ERR_CUDA = 5
+} qmoe_status;
+
+/*
+ * Execution path. AUTO takes DECODE for T <= 8 and GROUPED otherwise.
+ * DECODE: split-K dequant-GEMV kernels bound by HBM bandwidth; needs T <= 8.
+ * GROUPED: per-expert dequant-GEMM tiles on tcgen05 tensor cores with TMEM
+ * accumulators; needs hidden and inter to be multiples of 64 (bits 2 and 4)
+ * or 128 (bits 3). A path whose condition fails returns QMOE_ERR_UNSUPPORTED.
+ */
+typedef enum { QMOE_PATH_AUTO = 0, QMOE_PATH_DECODE = 1, QMOE_PATH_GROUPED = 2 } qmoe_path;
+
+typedef struct {
+  int64_t T;           /* packed tokens (rows of x) */
+  int32_t hidden;      /* H */
+  int32_t inter;       /* I: SwiGLU width; fc1 has 2*I rows */
+  int32_t num_experts; /* E */
+  int32_t top_k;       /* k */
+  int32_t bits;        /* 2, 3 or 4 */
+  int32_t block_size;  /* 32, 64 or 128 weights per scale along K */
+  int32_t dtype;       /* qmoe_dtype of x, logits, scales and out */
+  int32_t path;        /* qmoe_path */
+} qmoe_problem;
+
+/* Bytes of device workspace that qmoe_forward / qmoe_route need for *p
+ * (0 if *p is invalid). The same value serves both calls. */
+size_t qmoe_workspace_bytes(const qmoe_problem* p);
+
+/* The QMoE layer forward: out = QMoE(x, router_logits, fc1, fc2). */
+qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* router_logits,
+                         const uint8_t* fc1_q, const void* fc1_scales, const uint8_t* fc1_zp,
+                         const uint8_t* fc2_q, const void* fc2_scales, const uint8_t* fc2_zp,
+                         void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Stages of qmoe_forward: ROUTE (top-k routing, grouping by expert and the
+ * activations' FP16 conversion), FC1 (fc1 dequant-matmul with the SwiGLU
+ * epilogue), FC2 (fc2 dequant-matmul, weighted by the routing weight) and
+ * COMBINE (sum over each token's routes, rounded once).
+ */
+typedef enum {
+  QMOE_STAGE_ROUTE = 0,
+  QMOE_STAGE_FC1 = 1,
+  QMOE_STAGE_FC2 = 2,
+  QMOE_STAGE_COMBINE = 3
+} qmoe_stage;
+
+/*
+ * Run stages first_stage..last_stage of qmoe_forward (both inclusive). The
+ * stages of one forward must be enqueued in order, on one stream, with the same
+ * arguments and the same workspace, which carries the intermediate results
+ * (routing, grouped activations, SwiGLU output, per-route fc2 output) from one
+ * call to the next. qmoe_forward is qmoe_forward_stages(ROUTE, COMBINE). Used
+ * to time the stages separately with events between the calls. Returns
+ * QMOE_ERR_INVALID_ARGUMENT for a stage range outside ROUTE..COMBINE or with
+ * first_stage > last_stage; otherwise the same checks as qmoe_forward.
+ */
+qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last_stage,
+                                const void* x, const void* router_logits, const uint8_t* fc1_q,
+                                const void* fc1_scales, const uint8_t* fc1_zp,
+                                const uint8_t* fc2_q, const void* fc2_scales,
+                                const uint8_t* fc2_zp, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * Routing and grouping only (the first two steps of qmoe_forward), for
+ * inspection and tests: topk_idx int32 [T][k] (descending logit, ties to the
+ * lower index), topk_w fp32 [T][k], expert_offsets int32 [E+1] (exclusive
+ * prefix of the per-expert route counts), sorted_route int32 [T*k] (route ids
+ * t*k+j in expert order, stable in the route id). Any output may be NULL.
+ */
+qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t* topk_idx,
+                       float* topk_w, int32_t* expert_offsets, int32_t* sorted_route,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* qmoe_status_string(qmoe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMOE_H */

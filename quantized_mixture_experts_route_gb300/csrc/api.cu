@@ -1,0 +1,200 @@
+// api.cu -- the C ABI of include/qmoe.h: argument checks, workspace layout and
+// the launch sequence of one QMoE layer forward.
+//
+// Every check happens on the host before any launch (the pages validate
+// positive expert and feature dimensions before any arithmetic, "[CUDA] Add
+// INT4 and INT3 QMoE CPU/GPU offload support" #33575; empty input is a no-op,
+// #33973). The call enqueues work on the caller's stream and returns; it never
+// synchronises, allocates or copies device to host.
+#include <cstring>
+
+#include "qmoe_internal.cuh"
+
+namespace qmoe {
+
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+int resolve_path(const qmoe_problem& p) {
+  if (p.path == QMOE_PATH_AUTO) return p.T <= kDecodeMaxT ? QMOE_PATH_DECODE : QMOE_PATH_GROUPED;
+  return p.path;
+}
+
+// Shape and attribute checks shared by every entry point.
+qmoe_status check_problem(const qmoe_problem* p) {
+  if (!p) return QMOE_ERR_INVALID_ARGUMENT;
+  if (p->T < 0 || p->num_experts <= 0 || p->top_k <= 0 || p->top_k > p->num_experts ||
+      p->hidden <= 0 || p->inter <= 0)
+    return QMOE_ERR_INVALID_ARGUMENT;
+  if (p->bits != 2 && p->bits != 3 && p->bits != 4) return QMOE_ERR_UNSUPPORTED;
+  if (p->block_size != 32 && p->block_size != 64 && p->block_size != 128) return QMOE_ERR_UNSUPPORTED;
+  if (p->hidden % p->block_size || p->inter % p->block_size) return QMOE_ERR_UNSUPPORTED;
+  if (p->hidden % 32 || p->inter % 32) return QMOE_ERR_UNSUPPORTED;
+  if (p->num_experts > kMaxExperts || p->top_k > kMaxTopK) return QMOE_ERR_UNSUPPORTED;
+  if (p->dtype != QMOE_BF16 && p->dtype != QMOE_FP16) return QMOE_ERR_UNSUPPORTED;
+  if (p->path < QMOE_PATH_AUTO || p->path > QMOE_PATH_GROUPED) return QMOE_ERR_UNSUPPORTED;
+  if ((int64_t)p->T * p->top_k > (int64_t)INT32_MAX / 2) return QMOE_ERR_UNSUPPORTED;
+  const int path = resolve_path(*p);
+  if (path == QMOE_PATH_DECODE) {
+    if (p->T > kDecodeMaxT) return QMOE_ERR_UNSUPPORTED;
+    if (p->hidden > 8192 || p->inter > 8192) return QMOE_ERR_UNSUPPORTED;
+  } else {
+    const int m = p->bits == 3 ? 128 : 64;
+    if (p->hidden % m || p->inter % m) return QMOE_ERR_UNSUPPORTED;
+  }
+  return QMOE_OK;
+}
+
+Problem to_internal(const qmoe_problem& q) {
+  Problem p;
+  p.T = q.T;
+  p.H = q.hidden;
+  p.I = q.inter;
+  p.E = q.num_experts;
+  p.k = q.top_k;
+  p.bits = q.bits;
+  p.block = q.block_size;
+  p.dtype = q.dtype;
+  p.path = resolve_path(q);
+  return p;
+}
+
+}  // namespace
+
+size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* ws) {
+  size_t off = 0;
+  char* b = static_cast<char*>(base);
+  auto take = [&](size_t bytes) -> void* {
+    const size_t o = off;
+    off += align_up(bytes ? bytes : 1, 256);
+    return b ? b + o : nullptr;
+  };
+  const int64_t R = p.R();
+  Workspace w{};
+  w.topk_idx = static_cast<int32_t*>(take(sizeof(int32_t) * R));
+  w.topk_w = static_cast<float*>(take(sizeof(float) * R));
+  w.tok_scale = static_cast<float*>(take(sizeof(float) * p.T));
+  w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * p.T * p.H));
+  w.offsets = static_cast<int32_t*>(take(sizeof(int32_t) * (p.E + 1)));
+  w.sorted_route = static_cast<int32_t*>(take(sizeof(int32_t) * R));
+  w.active = static_cast<int32_t*>(take(sizeof(int32_t) * p.E));
+  w.counters = static_cast<int32_t*>(take(sizeof(int32_t) * 4));
+  w.max_tiles = (R + kTileM - 1) / kTileM + p.E;
+  w.tiles = static_cast<int32_t*>(take(sizeof(int32_t) * 2 * w.max_tiles));
+  w.nchunks = (R + kPermuteChunk - 1) / kPermuteChunk;
+  w.chunk_hist = static_cast<int32_t*>(take(sizeof(int32_t) * w.nchunks * p.E));
+  w.x16s = grouped ? static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.H)) : nullptr;
+  w.h16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.I));
+  w.y = static_cast<float*>(take(sizeof(float) * R * p.H));
+  if (ws) *ws = w;
+  return off;
+}
+
+}  // namespace qmoe
+
+using namespace qmoe;
+
+extern "C" {
+
+size_t qmoe_workspace_bytes(const qmoe_problem* p) {
+  if (check_problem(p) != QMOE_OK) return 0;
+  const Problem ip = to_internal(*p);
+  return workspace_layout(ip, ip.path == QMOE_PATH_GROUPED, nullptr, nullptr);
+}
+
+qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last_stage,
+                                const void* x, const void* router_logits, const uint8_t* fc1_q,
+                                const void* fc1_scales, const uint8_t* fc1_zp,
+                                const uint8_t* fc2_q, const void* fc2_scales,
+                                const uint8_t* fc2_zp, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (first_stage < QMOE_STAGE_ROUTE || last_stage > QMOE_STAGE_COMBINE || first_stage > last_stage)
+    return QMOE_ERR_INVALID_ARGUMENT;
+  const qmoe_status st = check_problem(p);
+  if (st != QMOE_OK) return st;
+  if (p->T == 0) return QMOE_OK;
+  if (!x || !router_logits || !fc1_q || !fc1_scales || !fc2_q || !fc2_scales || !out || !workspace)
+    return QMOE_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {x, router_logits, fc1_q, fc1_scales, fc2_q, fc2_scales, out, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return QMOE_ERR_MISALIGNED;
+  if ((fc1_zp && !aligned16(fc1_zp)) || (fc2_zp && !aligned16(fc2_zp))) return QMOE_ERR_MISALIGNED;
+  const Problem ip = to_internal(*p);
+  const bool grouped = ip.path == QMOE_PATH_GROUPED;
+  Workspace ws;
+  if (workspace_layout(ip, grouped, workspace, &ws) > workspace_bytes)
+    return QMOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto in_range = [&](int stage) { return first_stage <= stage && stage <= last_stage; };
+  cudaError_t err = cudaSuccess;
+  if (in_range(QMOE_STAGE_ROUTE)) {
+    err = launch_route(ip, x, router_logits, ws, true, s);
+    if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
+    if (err == cudaSuccess && grouped) err = launch_gather(ip, ws, s);
+  }
+  if (err == cudaSuccess && in_range(QMOE_STAGE_FC1))
+    err = grouped ? launch_grouped(ip, true, fc1_q, fc1_scales, fc1_zp, ws, s)
+                  : launch_decode(ip, true, fc1_q, fc1_scales, fc1_zp, ws, s);
+  if (err == cudaSuccess && in_range(QMOE_STAGE_FC2))
+    err = grouped ? launch_grouped(ip, false, fc2_q, fc2_scales, fc2_zp, ws, s)
+                  : launch_decode(ip, false, fc2_q, fc2_scales, fc2_zp, ws, s);
+  if (err == cudaSuccess && in_range(QMOE_STAGE_COMBINE)) err = launch_combine(ip, ws, out, s);
+  if (err == cudaErrorNotSupported) return QMOE_ERR_UNSUPPORTED;
+  return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* router_logits,
+                         const uint8_t* fc1_q, const void* fc1_scales, const uint8_t* fc1_zp,
+                         const uint8_t* fc2_q, const void* fc2_scales, const uint8_t* fc2_zp,
+                         void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return qmoe_forward_stages(p, QMOE_STAGE_ROUTE, QMOE_STAGE_COMBINE, x, router_logits, fc1_q,
+                             fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace,
+                             workspace_bytes, stream);
+}
+
+qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t* topk_idx,
+                       float* topk_w, int32_t* expert_offsets, int32_t* sorted_route,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  const qmoe_status st = check_problem(p);
+  if (st != QMOE_OK) return st;
+  if (p->T == 0) return QMOE_OK;
+  if (!router_logits || !workspace) return QMOE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(router_logits) || !aligned16(workspace)) return QMOE_ERR_MISALIGNED;
+  const Problem ip = to_internal(*p);
+  const bool grouped = ip.path == QMOE_PATH_GROUPED;
+  Workspace ws;
+  if (workspace_layout(ip, grouped, workspace, &ws) > workspace_bytes)
+    return QMOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = launch_route(ip, nullptr, router_logits, ws, false, s);
+  if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
+  const int64_t R = ip.R();
+  if (err == cudaSuccess && topk_idx)
+    err = cudaMemcpyAsync(topk_idx, ws.topk_idx, sizeof(int32_t) * R, cudaMemcpyDeviceToDevice, s);
+  if (err == cudaSuccess && topk_w)
+    err = cudaMemcpyAsync(topk_w, ws.topk_w, sizeof(float) * R, cudaMemcpyDeviceToDevice, s);
+  if (err == cudaSuccess && expert_offsets)
+    err = cudaMemcpyAsync(expert_offsets, ws.offsets, sizeof(int32_t) * (ip.E + 1),
+                          cudaMemcpyDeviceToDevice, s);
+  if (err == cudaSuccess && sorted_route)
+    err = cudaMemcpyAsync(sorted_route, ws.sorted_route, sizeof(int32_t) * R,
+                          cudaMemcpyDeviceToDevice, s);
+  return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+const char* qmoe_status_string(qmoe_status s) {
+  switch (s) {
+    case QMOE_OK: return "ok";
+    case QMOE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case QMOE_ERR_UNSUPPORTED: return "unsupported problem";
+    case QMOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case QMOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case QMOE_ERR_CUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

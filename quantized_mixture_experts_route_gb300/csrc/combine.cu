@@ -1,0 +1,55 @@
+// combine.cu -- routing-weighted combine, one FP32 sum rounded once (sm_103a).
+//
+// out[t, :] = round(sum_{j<k} y_w[t*k + j, :]) where y_w already carries the
+// routing weight (multiplied in the fc2 epilogue). The sum runs in FP32 in
+// ascending j, is rounded to BF16/FP16 exactly once with round-to-nearest-even,
+// and NaN stays NaN ("[CUDA] Add MoEPacked CPU/GPU hybrid offload ..." #33973:
+// the partial sum stays in FP32 and is rounded once, as the GPU-only finalize
+// does; "Keep NaN as NaN when rounding to BF16"). Routes whose weight is exactly
+// zero are skipped ("skip zero-scale routes in the prefill finalizer", same PR).
+// Memory bound: each thread reads k x 32 bytes and writes 16 bytes.
+#include "qmoe_internal.cuh"
+
+namespace qmoe {
+namespace {
+
+__global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
+                                                      uint16_t* __restrict__ out) {
+  const int per_row = p.H / 8;
+  const int64_t total = p.T * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / per_row;
+    const int h0 = (int)(i % per_row) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < p.k; ++j) {
+      const int64_t r = t * p.k + j;
+      if (ws.topk_w[r] == 0.0f) continue;
+      const float4* src = reinterpret_cast<const float4*>(ws.y + r * p.H + h0);
+      const float4 a = src[0], b = src[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    uint4 o;
+    o.x = float_to_half_bits(acc[0], p.dtype) | ((uint32_t)float_to_half_bits(acc[1], p.dtype) << 16);
+    o.y = float_to_half_bits(acc[2], p.dtype) | ((uint32_t)float_to_half_bits(acc[3], p.dtype) << 16);
+    o.z = float_to_half_bits(acc[4], p.dtype) | ((uint32_t)float_to_half_bits(acc[5], p.dtype) << 16);
+    o.w = float_to_half_bits(acc[6], p.dtype) | ((uint32_t)float_to_half_bits(acc[7], p.dtype) << 16);
+    *reinterpret_cast<uint4*>(out + t * p.H + h0) = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cudaStream_t s) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t total = p.T * (p.H / 8);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  combine_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, ws, static_cast<uint16_t*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -1,0 +1,89 @@
+// qmoe_internal.cuh -- shared declarations of the QMoE CUDA path (sm_103a).
+//
+// Layout of the caller's workspace, launcher declarations and small device
+// helpers used by more than one kernel file.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qmoe.h"
+
+namespace qmoe {
+
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 32;
+constexpr int kDecodeMaxT = 8;        // decode GEMV: at most 8 routes per expert (one MMA N-fragment)
+constexpr int kPermuteChunk = 512;    // routes per block in the grouping kernels
+constexpr int kTileM = 128;           // rows (routes) per grouped-GEMM tile
+
+// ---------------------------------------------------------------------------
+// Workspace: every scratch buffer of one forward call, carved from the
+// caller's allocation at 256-byte aligned offsets.
+// ---------------------------------------------------------------------------
+struct Workspace {
+  int32_t* topk_idx;      // [R]      expert of route r = t*k + j
+  float* topk_w;          // [R]      routing weight of route r
+  float* tok_scale;       // [T]      power of two that brings max|x_t| into [1, 2)
+  uint16_t* x16;          // [T][H]   FP16 bits of x_t * tok_scale[t], K-order permuted
+  int32_t* offsets;       // [E+1]    exclusive prefix of per-expert route counts
+  int32_t* sorted_route;  // [R]      route ids grouped by expert, stable
+  int32_t* active;        // [E]      experts with at least one route, ascending
+  int32_t* counters;      // [4]      [0] active experts, [1] grouped tiles
+  int32_t* tiles;         // [2*max_tiles] (expert, first sorted row) of each 128-row tile
+  int32_t* chunk_hist;    // [nchunks][E] per-chunk expert counts, then chunk bases
+  uint16_t* x16s;         // [R][H]   x16 rows gathered into sorted-route order (grouped)
+  uint16_t* h16;          // [R][I]   SwiGLU output, FP16, sorted-route order, K-order permuted
+  float* y;               // [R][H]   weighted fc2 output per route id (FP32)
+  int64_t max_tiles;
+  int64_t nchunks;
+};
+
+struct Problem {
+  int64_t T;
+  int H, I, E, k, bits, block, dtype, path;
+  __host__ __device__ int64_t R() const { return T * (int64_t)k; }
+};
+
+// Byte size of the workspace for problem p and the pointers inside `base`
+// (base may be null when only the size is wanted).
+size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* ws);
+
+// K-order permutation group: positions 2i and 2i+1 of each group hold elements
+// i and i + G/2. G = 8 for 4-bit codes and 16 for 2- and 3-bit codes. It lets
+// the dequantisers produce FP16 pairs straight from the packed words.
+__host__ __device__ inline int perm_group(int bits) { return bits == 4 ? 8 : 16; }
+
+// ---------------------------------------------------------------------------
+// launchers (return the launch error, never synchronise)
+// ---------------------------------------------------------------------------
+cudaError_t launch_route(const Problem& p, const void* x, const void* logits, const Workspace& ws,
+                         bool want_x16, cudaStream_t s);
+cudaError_t launch_group(const Problem& p, const Workspace& ws, bool want_tiles, cudaStream_t s);
+cudaError_t launch_gather(const Problem& p, const Workspace& ws, cudaStream_t s);
+// One expert matmul stage: fc1 (with SwiGLU) when fc1 is true, else fc2.
+cudaError_t launch_decode(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
+                          const uint8_t* zp, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_grouped(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
+                           const uint8_t* zp, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float half_bits_to_float(uint16_t b, int dtype) {
+  if (dtype == QMOE_BF16) return __uint_as_float((uint32_t)b << 16);
+  return __half2float(__ushort_as_half(b));
+}
+
+// Round to nearest even; NaN stays NaN (the CUDA conversion intrinsics).
+__device__ __forceinline__ uint16_t float_to_half_bits(float v, int dtype) {
+  if (dtype == QMOE_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace qmoe

@@ -1,0 +1,411 @@
+// route.cu -- per-token top-k routing and token->expert grouping (sm_103a).
+//
+// route_topk_softmax: one warp per token. The k largest raw router logits are
+// selected by k rounds of a warp-wide maximum over (order key, expert) pairs,
+// so ties go to the lower expert index, and the weights are the softmax over
+// the selected logits ("Document and test packed token inputs for MoE and
+// QMoE" #32522: QMoE receives raw logits; the kernel applies top-k and then
+// normalises, the reference being a softmax over the top-k logits). The same
+// warp also converts its token's activations for the tensor-core matmuls.
+//
+// expert_histogram_scan_permute: a stable counting sort of the T*k route ids by
+// expert (the sorted expert map / expert_first_token_offset that the pages'
+// grouped kernels consume, "[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload
+// ..." #33731 items 1-2). Per-chunk histograms, one scan, and a scatter that
+// ranks equal experts by route id with warp match masks, so the result is the
+// unique stable order, bit for bit, whatever the scheduling.
+#include "qmoe_internal.cuh"
+
+namespace qmoe {
+namespace {
+
+constexpr int kGroupThreads = 512;
+static_assert(kPermuteChunk % kGroupThreads == 0, "chunk must be a multiple of the block");
+
+// Order key of a logit: larger logit -> larger key; +0 and -0 equal; NaN lowest.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v != v) return 0u;
+  if (v == 0.0f) return 0x80000000u;
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = o > v ? o : v;
+  }
+  return v;
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// Top-k + softmax of token t (whole warp), and optionally its FP16 activations.
+template <int PER_LANE>
+__device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
+                            const uint16_t* __restrict__ logits, const Workspace& ws, int64_t t,
+                            bool want_x16) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.E, k = p.k;
+  const uint16_t* lrow = logits + t * E;
+  uint64_t cand[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int e = lane + 32 * i;
+    cand[i] = 0;
+    if (e < E) {
+      const float v = half_bits_to_float(lrow[e], p.dtype);
+      cand[i] = ((uint64_t)order_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+    }
+  }
+  int my_e = 0;
+  float my_l = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = 0;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) best = cand[i] > best ? cand[i] : best;
+    best = warp_max_u64(best);
+    const int e = (int)(0xFFFFFFFFu - (uint32_t)best);
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i)
+      if (lane + 32 * i == e) cand[i] = 0;
+    if (lane == j) {
+      my_e = e;
+      my_l = half_bits_to_float(lrow[e], p.dtype);
+    }
+  }
+  // softmax over the selected logits, shifted by the largest (j = 0)
+  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+  float denom = 0.0f;
+  for (int j = 0; j < k; ++j) denom += expf(__shfl_sync(0xffffffffu, my_l, j) - l0);
+  if (lane < k) {
+    ws.topk_idx[t * k + lane] = my_e;
+    ws.topk_w[t * k + lane] = expf(my_l - l0) / denom;
+  }
+  if (!want_x16) return;
+
+  // Activations: scale by a power of two so that max|x_t| lies in [1, 2), round
+  // to FP16, and store in the K-order permutation of the dequantisers.
+  const int H = p.H;
+  const uint16_t* xrow = x + t * (int64_t)H;
+  float m = 0.0f;
+  for (int base = lane * 16; base < H; base += 32 * 16) {
+    const uint4 a = *reinterpret_cast<const uint4*>(xrow + base);
+    const uint4 b = *reinterpret_cast<const uint4*>(xrow + base + 8);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      m = fmaxf(m, fabsf(half_bits_to_float((uint16_t)(w[i] & 0xFFFF), p.dtype)));
+      m = fmaxf(m, fabsf(half_bits_to_float((uint16_t)(w[i] >> 16), p.dtype)));
+    }
+  }
+  m = warp_max_f(m);
+  float sigma = 1.0f;
+  if (m > 0.0f && m <= 3.4e38f) {
+    int ex;
+    frexpf(m, &ex);                   // m = f * 2^ex, f in [0.5, 1)
+    int sh = 1 - ex;                  // m * 2^sh in [1, 2)
+    sh = sh > 60 ? 60 : (sh < -60 ? -60 : sh);
+    sigma = ldexpf(1.0f, sh);
+  }
+  if (lane == 0) ws.tok_scale[t] = sigma;
+  const int G = perm_group(p.bits);
+  uint16_t* orow = ws.x16 + t * (int64_t)H;
+  for (int base = lane * 16; base < H; base += 32 * 16) {
+    const uint4 a = *reinterpret_cast<const uint4*>(xrow + base);
+    const uint4 b = *reinterpret_cast<const uint4*>(xrow + base + 8);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint16_t in[16], out[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      in[2 * i] = __half_as_ushort(__float2half_rn(half_bits_to_float((uint16_t)(w[i] & 0xFFFF), p.dtype) * sigma));
+      in[2 * i + 1] = __half_as_ushort(__float2half_rn(half_bits_to_float((uint16_t)(w[i] >> 16), p.dtype) * sigma));
+    }
+    if (G == 8) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          out[8 * g + 2 * i] = in[8 * g + i];
+          out[8 * g + 2 * i + 1] = in[8 * g + i + 4];
+        }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        out[2 * i] = in[i];
+        out[2 * i + 1] = in[i + 8];
+      }
+    }
+    uint4 o0, o1;
+    o0.x = out[0] | ((uint32_t)out[1] << 16);
+    o0.y = out[2] | ((uint32_t)out[3] << 16);
+    o0.z = out[4] | ((uint32_t)out[5] << 16);
+    o0.w = out[6] | ((uint32_t)out[7] << 16);
+    o1.x = out[8] | ((uint32_t)out[9] << 16);
+    o1.y = out[10] | ((uint32_t)out[11] << 16);
+    o1.z = out[12] | ((uint32_t)out[13] << 16);
+    o1.w = out[14] | ((uint32_t)out[15] << 16);
+    *reinterpret_cast<uint4*>(orow + base) = o0;
+    *reinterpret_cast<uint4*>(orow + base + 8) = o1;
+  }
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) route_kernel(Problem p, const uint16_t* __restrict__ x,
+                                                    const uint16_t* __restrict__ logits,
+                                                    Workspace ws, int want_x16) {
+  const int warps = blockDim.x >> 5;
+  for (int64_t t = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); t < p.T;
+       t += (int64_t)gridDim.x * warps)
+    route_token<PER_LANE>(p, x, logits, ws, t, want_x16 != 0);
+}
+
+// ---------------------------------------------------------------------------
+// grouping
+// ---------------------------------------------------------------------------
+
+// Exclusive scan of one int per thread over a block of kGroupThreads threads.
+__device__ int block_exclusive_scan(int v, int* sh /* >= 32 ints */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int s = lane < nw ? sh[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += o;
+    }
+    if (lane < nw) sh[lane] = s;  // inclusive per-warp totals
+  }
+  __syncthreads();
+  const int warp_base = warp ? sh[warp - 1] : 0;
+  const int result = warp_base + incl - v;
+  if (total) *total = sh[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return result;
+}
+
+// Count of routes per expert in routes [r0, r1) into shared hist (pre-zeroed).
+__device__ void count_routes(const int32_t* __restrict__ idx, int64_t r0, int64_t r1, int* hist) {
+  for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) atomicAdd(&hist[idx[r]], 1);
+}
+
+// Stable scatter of routes [r0, r1): position = base[e] + (routes of e before r
+// in this range). base is in shared memory and is advanced past the range.
+// warp_cnt holds (blockDim/32) * E ints of shared scratch.
+__device__ void scatter_routes(const int32_t* __restrict__ idx, int64_t r0, int64_t r1, int E,
+                               int* base, int* warp_cnt, int32_t* __restrict__ sorted_route) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int64_t round0 = r0; round0 < r1; round0 += blockDim.x) {
+    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) warp_cnt[i] = 0;
+    __syncthreads();
+    const int64_t r = round0 + threadIdx.x;
+    const bool valid = r < r1;
+    const int e = valid ? idx[r] : -1 - lane;  // invalid lanes never match a real expert
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) warp_cnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += warp_cnt[w * E + e];
+      sorted_route[base[e] + before + rank] = (int32_t)r;
+    }
+    __syncthreads();
+    // advance the bases past this round
+    for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
+      int n = 0;
+      for (int w = 0; w < nw; ++w) n += warp_cnt[w * E + ee];
+      base[ee] += n;
+    }
+    __syncthreads();
+  }
+}
+
+// Offsets, active-expert list and 128-row tile list from per-expert totals held
+// one per thread (thread e < E holds total[e]).
+__device__ void finish_groups(int E, int total_e, const Workspace& ws, bool want_tiles, int* sh,
+                              int* expert_base_out) {
+  const int e = threadIdx.x;
+  const int v = e < E ? total_e : 0;
+  int R_total;
+  const int off = block_exclusive_scan(v, sh, &R_total);
+  if (e < E) ws.offsets[e] = off;
+  if (e == 0) ws.offsets[E] = R_total;
+  if (expert_base_out && e < E) expert_base_out[e] = off;
+  int n_active;
+  const int apos = block_exclusive_scan(v > 0 ? 1 : 0, sh, &n_active);
+  if (e < E && v > 0) ws.active[apos] = e;
+  if (e == 0) ws.counters[0] = n_active;
+  if (want_tiles) {
+    const int nt = (v + kTileM - 1) / kTileM;
+    int n_tiles;
+    const int tpos = block_exclusive_scan(nt, sh, &n_tiles);
+    for (int i = 0; i < nt; ++i) {
+      ws.tiles[2 * (tpos + i)] = e;
+      ws.tiles[2 * (tpos + i) + 1] = off + i * kTileM;
+    }
+    if (e == 0) ws.counters[1] = n_tiles;
+  }
+}
+
+__global__ void __launch_bounds__(kGroupThreads) group_count_kernel(Problem p, Workspace ws) {
+  extern __shared__ int smem[];
+  int* hist = smem;
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int64_t R = p.R();
+  const int64_t r0 = (int64_t)blockIdx.x * kPermuteChunk;
+  const int64_t r1 = r0 + kPermuteChunk < R ? r0 + kPermuteChunk : R;
+  count_routes(ws.topk_idx, r0, r1, hist);
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x)
+    ws.chunk_hist[(int64_t)blockIdx.x * p.E + i] = hist[i];
+}
+
+__global__ void __launch_bounds__(kGroupThreads) group_scan_kernel(Problem p, Workspace ws,
+                                                                   int want_tiles) {
+  __shared__ int sh[32];
+  const int e = threadIdx.x;
+  const int E = p.E;
+  int total = 0;
+  if (e < E) {
+    // per-expert exclusive prefix over chunks
+    for (int64_t c = 0; c < ws.nchunks; ++c) {
+      const int64_t i = c * E + e;
+      const int v = ws.chunk_hist[i];
+      ws.chunk_hist[i] = total;
+      total += v;
+    }
+  }
+  __shared__ int expert_base[kMaxExperts];
+  finish_groups(E, total, ws, want_tiles != 0, sh, expert_base);
+  __syncthreads();
+  if (e < E)
+    for (int64_t c = 0; c < ws.nchunks; ++c) ws.chunk_hist[c * E + e] += expert_base[e];
+}
+
+__global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(Problem p, Workspace ws) {
+  extern __shared__ int smem[];
+  int* base = smem;                 // [E]
+  int* warp_cnt = smem + p.E;       // [16][E]
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x)
+    base[i] = ws.chunk_hist[(int64_t)blockIdx.x * p.E + i];
+  __syncthreads();
+  const int64_t R = p.R();
+  const int64_t r0 = (int64_t)blockIdx.x * kPermuteChunk;
+  const int64_t r1 = r0 + kPermuteChunk < R ? r0 + kPermuteChunk : R;
+  scatter_routes(ws.topk_idx, r0, r1, p.E, base, warp_cnt, ws.sorted_route);
+}
+
+// Routing and grouping of a small batch (R <= kPermuteChunk) in one block.
+template <int PER_LANE>
+__global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
+    Problem p, const uint16_t* __restrict__ x, const uint16_t* __restrict__ logits, Workspace ws,
+    int want_x16, int want_tiles) {
+  extern __shared__ int smem[];
+  int* hist = smem;                  // [E]
+  int* warp_cnt = smem + p.E;        // [16][E]
+  __shared__ int sh[32];
+  const int warps = blockDim.x >> 5;
+  for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps)
+    route_token<PER_LANE>(p, x, logits, ws, t, want_x16 != 0);
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int64_t R = p.R();
+  count_routes(ws.topk_idx, 0, R, hist);
+  __syncthreads();
+  const int total = threadIdx.x < p.E ? hist[threadIdx.x] : 0;
+  __syncthreads();
+  finish_groups(p.E, total, ws, want_tiles != 0, sh, hist);  // hist now holds the bases
+  __syncthreads();
+  scatter_routes(ws.topk_idx, 0, R, p.E, hist, warp_cnt, ws.sorted_route);
+}
+
+__global__ void __launch_bounds__(256) gather_kernel(Problem p, Workspace ws) {
+  // x16s[pos] = x16[token of sorted route pos]; one warp per row, 16 bytes per lane
+  const int warps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t R = p.R();
+  const int chunks = p.H / 8;
+  for (int64_t pos = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); pos < R;
+       pos += (int64_t)gridDim.x * warps) {
+    const int64_t t = ws.sorted_route[pos] / p.k;
+    const uint4* src = reinterpret_cast<const uint4*>(ws.x16 + t * p.H);
+    uint4* dst = reinterpret_cast<uint4*>(ws.x16s + pos * p.H);
+    for (int c = lane; c < chunks; c += 32) dst[c] = src[c];
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_route(const Problem& p, const void* x, const void* logits, const Workspace& ws,
+                         bool want_x16, cudaStream_t s) {
+  const int64_t R = p.R();
+  const bool small = R <= kPermuteChunk;
+  const bool want_tiles = p.path == QMOE_PATH_GROUPED;
+  const auto* xx = static_cast<const uint16_t*>(x);
+  const auto* lg = static_cast<const uint16_t*>(logits);
+  if (small) {
+    const size_t smem = sizeof(int) * (size_t)p.E * (1 + kGroupThreads / 32);
+    if (p.E <= 128)
+      route_group_small_kernel<4><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, want_x16, want_tiles);
+    else
+      route_group_small_kernel<16><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, want_x16, want_tiles);
+    return cudaGetLastError();
+  }
+  const int warps = 8;
+  int64_t blocks = (p.T + warps - 1) / warps;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (p.E <= 128)
+    route_kernel<4><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, want_x16);
+  else
+    route_kernel<16><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, want_x16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group(const Problem& p, const Workspace& ws, bool want_tiles, cudaStream_t s) {
+  if (p.R() <= kPermuteChunk) return cudaSuccess;  // done by route_group_small_kernel
+  const unsigned nchunks = (unsigned)ws.nchunks;
+  group_count_kernel<<<nchunks, kGroupThreads, sizeof(int) * p.E, s>>>(p, ws);
+  group_scan_kernel<<<1, kGroupThreads, 0, s>>>(p, ws, want_tiles ? 1 : 0);
+  const size_t smem = sizeof(int) * (size_t)p.E * (1 + kGroupThreads / 32);
+  group_scatter_kernel<<<nchunks, kGroupThreads, smem, s>>>(p, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const Problem& p, const Workspace& ws, cudaStream_t s) {
+  const int warps = 8;
+  int64_t blocks = (p.R() + warps - 1) / warps;
+  const int64_t cap = (int64_t)num_sms() * 16;
+  if (blocks > cap) blocks = cap;
+  gather_kernel<<<(unsigned)blocks, 32 * warps, 0, s>>>(p, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe

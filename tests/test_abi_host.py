@@ -1,0 +1,133 @@
+"""The C ABI library without a GPU: it loads, exports every symbol the header
+declares, and rejects bad arguments on the host before any CUDA call. CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+qm = pytest.importorskip("quantized_mixture_experts_route_gb300")
+from quantized_mixture_experts_route_gb300 import build as qbuild  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return qm.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "qmoe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmoe_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_header_symbol(L):
+    names = header_functions()
+    assert names == sorted(qm.EXPORTED)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert qm.qmoe_status_string(s)
+    assert "unknown" in qm.qmoe_status_string(99)
+
+
+def P(**kw):
+    base = dict(T=8, hidden=2048, inter=768, num_experts=128, top_k=8, bits=4, block_size=32,
+                dtype=qm.QMOE_BF16, path=qm.QMOE_PATH_AUTO)
+    base.update(kw)
+    return qm.problem(**base)
+
+
+BAD = [
+    (dict(num_experts=0), qm.QMOE_ERR_INVALID_ARGUMENT),
+    (dict(top_k=0), qm.QMOE_ERR_INVALID_ARGUMENT),
+    (dict(top_k=129), qm.QMOE_ERR_INVALID_ARGUMENT),
+    (dict(hidden=0), qm.QMOE_ERR_INVALID_ARGUMENT),
+    (dict(inter=-32), qm.QMOE_ERR_INVALID_ARGUMENT),
+    (dict(T=-1), qm.QMOE_ERR_INVALID_ARGUMENT),
+    (dict(bits=5), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(bits=8), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(block_size=16), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(block_size=128, inter=704), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(hidden=2056), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(num_experts=1024, top_k=8), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(num_experts=64, top_k=33), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(dtype=2), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=3), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=qm.QMOE_PATH_DECODE, T=9), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=qm.QMOE_PATH_GROUPED, bits=3, block_size=64, hidden=2048, inter=704), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(T=9, hidden=96, inter=64), qm.QMOE_ERR_UNSUPPORTED),
+]
+
+FAKE = 1 << 20  # an aligned address that is never dereferenced: every call below fails its checks first
+
+
+def call_forward(L, p, ptrs=None, ws_bytes=1 << 40, misalign=None):
+    args = [FAKE] * 10 if ptrs is None else ptrs
+    if misalign is not None:
+        args[misalign] += 2
+    return L.qmoe_forward(ctypes.byref(p), *args[:9], args[9], ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", BAD, ids=[str(b[0]) for b in BAD])
+def test_invalid_problem_rejected(L, kw, status):
+    p = P(**kw)
+    assert call_forward(L, p) == status
+    assert L.qmoe_route(ctypes.byref(p), FAKE, None, None, None, None, FAKE, 1 << 40, None) == status
+    assert L.qmoe_workspace_bytes(ctypes.byref(p)) == 0
+
+
+def test_null_problem(L):
+    assert L.qmoe_forward(None, *([FAKE] * 10), 1 << 40, None) == qm.QMOE_ERR_INVALID_ARGUMENT
+    assert L.qmoe_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("which", [0, 1, 2, 3, 5, 6, 8, 9])
+def test_null_required_pointer(L, which):
+    args = [FAKE] * 10
+    args[which] = None
+    assert call_forward(L, P(), args) == qm.QMOE_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("which", range(10))
+def test_misaligned_pointer(L, which):
+    assert call_forward(L, P(), misalign=which) == qm.QMOE_ERR_MISALIGNED
+
+
+def test_workspace_too_small(L):
+    p = P()
+    need = L.qmoe_workspace_bytes(ctypes.byref(p))
+    assert need > 0
+    assert call_forward(L, p, ws_bytes=need - 1) == qm.QMOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.qmoe_route(ctypes.byref(p), FAKE, None, None, None, None, FAKE, need - 1, None) == \
+        qm.QMOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_empty_input_is_noop(L):
+    # T == 0: OK with no launch, even with null buffers
+    p = P(T=0)
+    assert L.qmoe_forward(ctypes.byref(p), *([None] * 10), 0, None) == qm.QMOE_OK
+    assert L.qmoe_route(ctypes.byref(p), None, None, None, None, None, None, 0, None) == qm.QMOE_OK
+
+
+def test_workspace_sizes_grow_with_T(L):
+    small = L.qmoe_workspace_bytes(ctypes.byref(P(T=1)))
+    dec = L.qmoe_workspace_bytes(ctypes.byref(P(T=8)))
+    pre = L.qmoe_workspace_bytes(ctypes.byref(P(T=8192)))
+    assert 0 < small < dec < pre
+    # the grouped layout at 8K: x16 + gathered x16 + h16 + FP32 y dominate
+    R = 8192 * 8
+    assert pre >= R * (2048 * 2 + 768 * 2 + 2048 * 4)
+
+
+@pytest.mark.parametrize("first,last", [(-1, 3), (0, 4), (2, 1)])
+def test_bad_stage_range(L, first, last):
+    p = P()
+    assert L.qmoe_forward_stages(ctypes.byref(p), first, last, *([FAKE] * 10), 1 << 40, None) == \
+        qm.QMOE_ERR_INVALID_ARGUMENT
