@@ -10,10 +10,14 @@
 // eight routes of a T <= 8 batch fit one MMA N-fragment, so every weight byte is
 // read exactly once per call and the tensor core does the multiply-adds.
 //
-// Work split. A CTA owns 16 weight rows of one active expert and splits K over
-// KSPLIT warps; the partial tiles are added in a fixed warp order (no atomics),
-// so results are bit-reproducible. A quad of lanes covers 128 consecutive K of
-// two rows (g, g+8) per chunk: lane c takes codes [32c, 32c+32) of the chunk.
+// Work split. A warp owns a group of 16 weight rows of one active expert (one
+// MMA M-fragment) and a range of 128-wide K chunks; a quad of lanes covers the
+// 128 K of two rows (g, g+8) per chunk, lane c taking codes [32c, 32c+32). The
+// weight loads are issued before the activation rows are staged, and each lane
+// keeps kDepth chunks in flight in a register ring while it computes. A CTA of 8
+// warps holds rg whole row groups with K split ks = 8/rg ways, rg as large as
+// the batch allows while keeping two CTAs per SM busy; split-K partials are
+// added in a fixed warp order (no atomics), so results are bit-reproducible.
 //
 // Numerics. A weight is (code - zp) * scale: with the code placed in the
 // mantissa of FP16 1024.0, one exact FP16 subtraction gives (code - zp) and one
@@ -30,30 +34,67 @@
 namespace qmoe {
 namespace {
 
-constexpr int kRowsPerCta = 16;
-constexpr int kMaxKsplit = 8;
-constexpr int kChunkK = 128;      // K covered by one quad of lanes per step
-constexpr int kChunksPerBatch = 2;
+constexpr int kRowsPerGroup = 16;  // rows of one MMA M-fragment
+constexpr int kWarps = 8;
+constexpr int kChunkK = 128;       // K covered by one quad of lanes per chunk
+constexpr int kDepth = 4;          // chunks in flight per lane (register ring)
+constexpr int kSlices = 8;         // fixed K slices (the largest K split)
 
+// Streaming 128-bit / 64-bit / 32-bit loads of read-once weight codes: no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];\n" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// 32 codes of one weight row (one lane's share of a chunk) plus the FP16 pair
+// constants of its block: 1024 + zero point, and the scale.
 template <int BITS>
-struct Codes {
-  uint32_t w[BITS];  // 32 codes of one row: 4 words (INT4), 3 (INT3), 2 (INT2)
+struct RowChunk {
+  uint32_t w[BITS];
+  uint32_t z2, s2;
 };
 
+__device__ __forceinline__ uint32_t scale_half2(uint16_t bits, int dtype) {
+  uint16_t h = bits;
+  if (dtype == QMOE_BF16) h = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)bits << 16)));
+  return (uint32_t)h | ((uint32_t)h << 16);
+}
+
 template <int BITS>
-__device__ __forceinline__ Codes<BITS> load_codes(const uint8_t* p) {
-  Codes<BITS> c;
-  if constexpr (BITS == 4) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-    c.w[0] = v.x; c.w[1] = v.y; c.w[2] = v.z; c.w[3] = v.w;
-  } else if constexpr (BITS == 2) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-    c.w[0] = v.x; c.w[1] = v.y;
-  } else {
-    const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
-    c.w[0] = __ldg(q); c.w[1] = __ldg(q + 1); c.w[2] = __ldg(q + 2);
+__device__ __forceinline__ void load_row_chunk(RowChunk<BITS>& r, const uint8_t* codes,
+                                               const uint16_t* scale, const uint8_t* zp, bool valid,
+                                               int dtype) {
+  if (!valid) {
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) r.w[i] = 0u;
+    r.z2 = 0x64006400u;
+    r.s2 = 0u;  // zero scale: the lane contributes exact zeros
+    return;
   }
-  return c;
+  if constexpr (BITS == 4) {
+    const uint4 v = ld_stream_v4(codes);
+    r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+  } else if constexpr (BITS == 2) {
+    const uint2 v = ld_stream_v2(codes);
+    r.w[0] = v.x; r.w[1] = v.y;
+  } else {
+    r.w[0] = ld_stream_u32(codes); r.w[1] = ld_stream_u32(codes + 4); r.w[2] = ld_stream_u32(codes + 8);
+  }
+  r.s2 = scale_half2(__ldg(scale), dtype);
+  const uint32_t z = zp ? (uint32_t)__ldg(zp) : (1u << (BITS - 1));
+  r.z2 = (0x6400u + z) * 0x00010001u;
 }
 
 __device__ __forceinline__ uint32_t h2_sub_mul(uint32_t biased, uint32_t zp2, uint32_t s2) {
@@ -63,43 +104,44 @@ __device__ __forceinline__ uint32_t h2_sub_mul(uint32_t biased, uint32_t zp2, ui
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// The 16 FP16 pairs of a lane's 32 codes, in the K-order permutation of the
-// activations (pair p holds stored positions 2p and 2p+1).
+// Words from which the FP16 pairs are cut. INT4 and INT2: the packed words. INT3:
+// byte permutes that put two 8-code groups' bits into the two 16-bit halves
+// (groups G0 = bytes 0-2, G1 = 3-5, G2 = 6-8, G3 = 9-11).
 template <int BITS>
-__device__ __forceinline__ void dequant_pairs(const Codes<BITS>& c, uint32_t zp2, uint32_t s2,
-                                              uint32_t* pr) {
-  constexpr uint32_t kMagic = 0x64006400u;  // FP16 1024.0 in both halves
-  if constexpr (BITS == 4) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        pr[4 * i + m] = h2_sub_mul(((c.w[i] >> (4 * m)) & 0x000F000Fu) | kMagic, zp2, s2);
-  } else if constexpr (BITS == 2) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int m = 0; m < 8; ++m)
-        pr[8 * i + m] = h2_sub_mul(((c.w[i] >> (2 * m)) & 0x00030003u) | kMagic, zp2, s2);
+struct PairWords {
+  uint32_t v[BITS == 3 ? 4 : BITS];
+};
+
+template <int BITS>
+__device__ __forceinline__ PairWords<BITS> pair_words(const RowChunk<BITS>& r) {
+  PairWords<BITS> o;
+  if constexpr (BITS == 3) {
+    o.v[0] = __byte_perm(r.w[0], r.w[1], 0x4310);  // G0 bits 0-15  | G1 bits 0-15
+    o.v[1] = __byte_perm(r.w[0], r.w[1], 0x5421);  // G0 bits 8-23  | G1 bits 8-23
+    o.v[2] = __byte_perm(r.w[1], r.w[2], 0x6532);  // G2 bits 0-15  | G3 bits 0-15
+    o.v[3] = __byte_perm(r.w[1], r.w[2], 0x7643);  // G2 bits 8-23  | G3 bits 8-23
   } else {
-    // groups of eight 3-bit codes: G0 = bytes 0-2, G1 = 3-5, G2 = 6-8, G3 = 9-11.
-    // Pair (G0_m, G1_m) and (G2_m, G3_m) need the two groups' bits in the two
-    // 16-bit halves: gather them with byte permutes.
-    const uint32_t lo0 = __byte_perm(c.w[0], c.w[1], 0x4310);  // G0 bits 0-15 | G1 bits 0-15
-    const uint32_t hi0 = __byte_perm(c.w[0], c.w[1], 0x5421);  // G0 bits 8-23 | G1 bits 8-23
-    const uint32_t lo1 = __byte_perm(c.w[1], c.w[2], 0x6532);  // G2 bits 0-15 | G3 bits 0-15
-    const uint32_t hi1 = __byte_perm(c.w[1], c.w[2], 0x7643);  // G2 bits 8-23 | G3 bits 8-23
 #pragma unroll
-    for (int m = 0; m < 5; ++m) {
-      pr[m] = h2_sub_mul(((lo0 >> (3 * m)) & 0x00070007u) | kMagic, zp2, s2);
-      pr[8 + m] = h2_sub_mul(((lo1 >> (3 * m)) & 0x00070007u) | kMagic, zp2, s2);
-    }
-#pragma unroll
-    for (int m = 5; m < 8; ++m) {
-      pr[m] = h2_sub_mul(((hi0 >> (3 * m - 8)) & 0x00070007u) | kMagic, zp2, s2);
-      pr[8 + m] = h2_sub_mul(((hi1 >> (3 * m - 8)) & 0x00070007u) | kMagic, zp2, s2);
-    }
+    for (int i = 0; i < BITS; ++i) o.v[i] = r.w[i];
   }
+  return o;
+}
+
+// Dequantised FP16 pair p (0..15) of a lane's 32 codes, in the activations'
+// K-order permutation: pair p holds stored K positions 2p and 2p+1.
+template <int BITS>
+__device__ __forceinline__ uint32_t dq_pair(const PairWords<BITS>& w, int p, uint32_t z2, uint32_t s2) {
+  constexpr uint32_t kMagic = 0x64006400u;  // FP16 1024.0 in both halves
+  uint32_t bits;
+  if constexpr (BITS == 4) {
+    bits = (w.v[p >> 2] >> (4 * (p & 3))) & 0x000F000Fu;   // codes (8i+m, 8i+m+4)
+  } else if constexpr (BITS == 2) {
+    bits = (w.v[p >> 3] >> (2 * (p & 7))) & 0x00030003u;   // codes (16i+m, 16i+m+8)
+  } else {
+    const int g = p >> 3, m = p & 7;                        // codes (16g+m, 16g+m+8)
+    bits = m < 5 ? (w.v[2 * g] >> (3 * m)) & 0x00070007u : (w.v[2 * g + 1] >> (3 * m - 8)) & 0x00070007u;
+  }
+  return h2_sub_mul(bits | kMagic, z2, s2);
 }
 
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
@@ -111,25 +153,13 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t scale_half2(uint16_t bits, int dtype) {
-  uint16_t h = bits;
-  if (dtype == QMOE_BF16) h = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)bits << 16)));
-  return (uint32_t)h | ((uint32_t)h << 16);
-}
-
-__device__ __forceinline__ uint32_t zp_half2(const uint8_t* zp, int64_t idx, int bits) {
-  const uint32_t z = zp ? (uint32_t)zp[idx] : (1u << (bits - 1));
-  const uint32_t h = 0x6400u + z;  // FP16 1024 + z
-  return h | (h << 16);
-}
-
 struct DecodeArgs {
   const uint8_t* q;        // [E][N][K*bits/8]
   const uint16_t* s;       // [E][N][K/block]
   const uint8_t* zp;       // [E][N][K/block] or null
   const uint16_t* act;     // FC1: x16 [T][K] by token; FC2: h16 [R][K] by sorted position
   int N, K;
-  int ksplit;
+  int ks;                  // warps per team (K split of one item), 1, 2, 4 or 8
   Problem p;
   Workspace ws;
 };
@@ -140,150 +170,260 @@ __device__ __forceinline__ int permuted_pos(int j, int G) {
   return base + (i < G / 2 ? 2 * i : 2 * (i - G / 2) + 1);
 }
 
-template <int BITS, bool FC1>
-__global__ void __launch_bounds__(32 * kMaxKsplit) decode_gemv_kernel(DecodeArgs a) {
-  const Problem& p = a.p;
-  const Workspace& ws = a.ws;
-  const int n_active = ws.counters[0];
-  if ((int)blockIdx.y >= n_active) return;
-  const int e = ws.active[blockIdx.y];
-  const int begin = ws.offsets[e];
-  const int n_e = ws.offsets[e + 1] - begin;  // <= 8 on this path
-  const int K = a.K, N = a.N;
-  const int nq = (K + kChunkK - 1) / kChunkK;
-  const int row0 = blockIdx.x * kRowsPerCta;
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));  // (a & mask) | orv
+  return d;
+}
 
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint4* xs = reinterpret_cast<uint4*>(smem);  // [nq][4][32] x 16 bytes
-  float* red = reinterpret_cast<float*>(smem + (size_t)nq * 4 * 32 * 16);  // [ksplit][32][4]
-  float* tile = red + a.ksplit * 32 * 4;                                   // [16][8]
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  const __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&c));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 
-  // Activation rows of this expert's routes, in MMA B-fragment order.
-  for (int P = threadIdx.x; P < nq * 128; P += blockDim.x) {
-    const int q = P >> 7, i = (P >> 5) & 3, L = P & 31;
-    const int n = L >> 2, c = L & 3;
-    const int kk = q * kChunkK + 32 * c + 8 * i;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (n < n_e && kk < K) {
-      const int pos = begin + n;
-      const int64_t row = FC1 ? (int64_t)(ws.sorted_route[pos] / p.k) : (int64_t)pos;
-      v = *reinterpret_cast<const uint4*>(a.act + row * K + kk);
-    }
-    xs[P] = v;
+// INT4: the 16 FP16 pairs of 32 codes. Nibbles at bits 0-3 become 1024 + c in the
+// FP16 mantissa (one AND/OR); nibbles at bits 4-7 become 1024 + 16c, which one
+// FMA by 1/16 turns into 64 + c exactly; a single shift by 8 serves the other
+// two nibble positions. (c - zp) is exact, and so is (c - zp) * scale for BF16
+// scales in the FP16 normal range.
+__device__ __forceinline__ void dequant_int4(const uint32_t* w, uint32_t z1, uint32_t z16, uint32_t s2,
+                                             uint32_t* pr) {
+  constexpr uint32_t kMagic = 0x64006400u;     // 1024.0 | 1024.0
+  constexpr uint32_t kSixteenth = 0x2C002C00u; // 0.0625 | 0.0625
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = w[i], v8 = w[i] >> 8;
+    pr[4 * i + 0] = h2_mul(h2_sub(lop3_and_or(v, 0x000F000Fu, kMagic), z1), s2);
+    pr[4 * i + 1] = h2_mul(h2_fma(lop3_and_or(v, 0x00F000F0u, kMagic), kSixteenth, z16), s2);
+    pr[4 * i + 2] = h2_mul(h2_sub(lop3_and_or(v8, 0x000F000Fu, kMagic), z1), s2);
+    pr[4 * i + 3] = h2_mul(h2_fma(lop3_and_or(v8, 0x00F000F0u, kMagic), kSixteenth, z16), s2);
   }
-  __syncthreads();
+}
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int64_t rowA = (int64_t)e * N + row0 + g;
-  const int64_t rowB = rowA + 8;
-  const int64_t pitch = (int64_t)K * BITS / 8;
-  const int nblk = K / p.block;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-
-  for (int q0 = warp; warp < a.ksplit && q0 < nq; q0 += a.ksplit * kChunksPerBatch) {
-    Codes<BITS> ca[kChunksPerBatch], cb[kChunksPerBatch];
-    uint32_t sa[kChunksPerBatch], sb[kChunksPerBatch], za[kChunksPerBatch], zb[kChunksPerBatch];
-    bool live[kChunksPerBatch];
-#pragma unroll
-    for (int u = 0; u < kChunksPerBatch; ++u) {
-      const int q = q0 + u * a.ksplit;
-      const int kk = q * kChunkK + 32 * c;
-      live[u] = q < nq && kk < K;
-      if (live[u]) {
-        ca[u] = load_codes<BITS>(a.q + rowA * pitch + (int64_t)kk * BITS / 8);
-        cb[u] = load_codes<BITS>(a.q + rowB * pitch + (int64_t)kk * BITS / 8);
-        const int b = kk / p.block;
-        sa[u] = scale_half2(__ldg(a.s + rowA * nblk + b), p.dtype);
-        sb[u] = scale_half2(__ldg(a.s + rowB * nblk + b), p.dtype);
-        za[u] = zp_half2(a.zp, rowA * nblk + b, BITS);
-        zb[u] = zp_half2(a.zp, rowB * nblk + b, BITS);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kChunksPerBatch; ++u) {
-      const int q = q0 + u * a.ksplit;
-      if (q >= nq) break;
-      uint32_t pa[16], pb[16];
-      if (live[u]) {
-        dequant_pairs<BITS>(ca[u], za[u], sa[u], pa);
-        dequant_pairs<BITS>(cb[u], zb[u], sb[u], pb);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pa[i] = pb[i] = 0u;
-      }
-      const uint4* xq = xs + q * 128;
-      uint32_t bw[16];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = xq[i * 32 + lane];
-        bw[4 * i] = v.x; bw[4 * i + 1] = v.y; bw[4 * i + 2] = v.z; bw[4 * i + 3] = v.w;
-      }
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-        mma16816(acc, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
-    }
-  }
-
-  // fixed-order reduction of the split-K partial tiles
-  if (warp < a.ksplit) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) red[(warp * 32 + lane) * 4 + r] = acc[r];
-  }
-  __syncthreads();
-  if (threadIdx.x < 128) {
-    const int L = threadIdx.x >> 2, r = threadIdx.x & 3;
-    float v = 0.f;
-    for (int w = 0; w < a.ksplit; ++w) v += red[(w * 32 + L) * 4 + r];
-    const int gg = L >> 2, cc = L & 3;
-    const int row = gg + ((r & 2) ? 8 : 0);
-    const int n = 2 * cc + (r & 1);
-    tile[row * 8 + n] = v;
-  }
-  __syncthreads();
-
-  if constexpr (FC1) {
-    if (threadIdx.x < 64) {
-      const int j = threadIdx.x >> 3, n = threadIdx.x & 7;
-      if (n < n_e) {
-        const int pos = begin + n;
-        const int t = ws.sorted_route[pos] / p.k;
-        const float sigma = ws.tok_scale[t];
-        const float inv = 1.0f / sigma;
-        const float gt = tile[(2 * j) * 8 + n] * inv;
-        const float ut = tile[(2 * j + 1) * 8 + n] * inv;
-        const float h = silu(gt) * ut * sigma * sigma;
-        const int jg = row0 / 2 + j;
-        ws.h16[(int64_t)pos * p.I + permuted_pos(jg, perm_group(p.bits))] =
-            __half_as_ushort(__float2half_rn(h));
-      }
-    }
+template <int BITS>
+__device__ __forceinline__ void dequant_chunk(const RowChunk<BITS>& r, uint32_t* pr) {
+  if constexpr (BITS == 4) {
+    // z2 holds 1024 + zp; -(64 + zp) = -(z - 960) for the 1/16-scaled nibbles
+    const __half2 z = *reinterpret_cast<const __half2*>(&r.z2);
+    const __half2 z16h = __hneg2(__hsub2(z, __float2half2_rn(960.0f)));
+    dequant_int4(r.w, r.z2, *reinterpret_cast<const uint32_t*>(&z16h), r.s2, pr);
   } else {
-    if (threadIdx.x < 128) {
-      const int row = threadIdx.x & 15, n = threadIdx.x >> 4;
-      if (n < n_e) {
-        const int pos = begin + n;
-        const int r = ws.sorted_route[pos];
-        const int t = r / p.k;
-        const float inv = 1.0f / ws.tok_scale[t];
-        ws.y[(int64_t)r * p.H + row0 + row] = tile[row * 8 + n] * inv * inv * ws.topk_w[r];
-      }
-    }
+    const PairWords<BITS> pw = pair_words<BITS>(r);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) pr[q] = dq_pair<BITS>(pw, q, r.z2, r.s2);
   }
 }
 
 template <int BITS, bool FC1>
-cudaError_t launch_one(const DecodeArgs& a, int active_max, cudaStream_t s) {
-  const int nq = (a.K + kChunkK - 1) / kChunkK;
-  const size_t smem = (size_t)nq * 4 * 32 * 16 + (size_t)a.ksplit * 32 * 4 * 4 + 16 * 8 * 4;
-  if (smem > 48 * 1024) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_gemv_kernel<BITS, FC1>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
+__global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs a) {
+  const Problem& p = a.p;
+  const Workspace& ws = a.ws;
+  const int K = a.K, N = a.N;
+  const int nq = (K + kChunkK - 1) / kChunkK;
+  const int rgroups = N / kRowsPerGroup;
+  const int items = ws.counters[0] * rgroups;   // (active expert, 16-row group) pairs
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int ks = a.ks;
+  const int team = warp / ks, ksi = warp % ks;
+  const int teams_per_block = kWarps / ks;
+  const int team_global = blockIdx.x * teams_per_block + team;
+  const int teams_total = gridDim.x * teams_per_block;
+  // this warp's K range: fixed slices [sl0, sl1) = chunks [cb, ce)
+  const int sl0 = kSlices * ksi / ks, sl1 = kSlices * (ksi + 1) / ks;
+  const int cb = nq * sl0 / kSlices, ce = nq * sl1 / kSlices;
+  const int cpi = ce - cb;                       // chunks per item for this warp
+  const int my_items = team_global < items ? (items - team_global + teams_total - 1) / teams_total : 0;
+  const int total = my_items * cpi;
+  const int64_t pitch = (int64_t)K * BITS / 8;
+  const int nblk = K / p.block;
+
+  // chunk f of this warp -> (item, chunk) without divisions: walk counters
+  int pf_item = team_global, pf_cc = 0;          // prefetch cursor
+  auto load = [&](RowChunk<BITS>& ra, RowChunk<BITS>& rb) {
+    const int slot = pf_item / rgroups, rg = pf_item - slot * rgroups;
+    const int e = ws.active[slot];
+    const int64_t rowA = (int64_t)e * N + rg * kRowsPerGroup + g;
+    const int kk = (cb + pf_cc) * kChunkK + 32 * c;
+    const bool valid = kk < K;
+    const int b = valid ? kk / p.block : 0;
+    load_row_chunk<BITS>(ra, a.q + rowA * pitch + (int64_t)kk * BITS / 8, a.s + rowA * nblk + b,
+                         a.zp ? a.zp + rowA * nblk + b : nullptr, valid, p.dtype);
+    load_row_chunk<BITS>(rb, a.q + (rowA + 8) * pitch + (int64_t)kk * BITS / 8, a.s + (rowA + 8) * nblk + b,
+                         a.zp ? a.zp + (rowA + 8) * nblk + b : nullptr, valid, p.dtype);
+    if (++pf_cc == cpi) { pf_cc = 0; pf_item += teams_total; }
+  };
+
+  RowChunk<BITS> ring_a[kDepth], ring_b[kDepth];
+#pragma unroll
+  for (int u = 0; u < kDepth; ++u)
+    if (u < total) load(ring_a[u], ring_b[u]);
+
+  extern __shared__ __align__(16) float red[];   // [teams][kSlices][32][4] when ks > 1
+  float* tred = red + (size_t)team * kSlices * 32 * 4;
+
+  int item = team_global, cc = 0;
+  int e = 0, begin = 0, n_e = 0, row0 = 0;
+  const uint16_t* brow = nullptr;                // this lane's activation row (route slot g)
+  float acc0[4], acc1[4], tot[4];
+  int slice = sl0;
+  auto close_slices_until = [&](int gq) {
+    while (slice < sl1 && nq * (slice + 1) / kSlices <= gq) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float v = acc0[r] + acc1[r];
+        if (ks == 1)
+          tot[r] = slice == 0 ? v : tot[r] + v;
+        else
+          tred[(slice * 32 + lane) * 4 + r] = v;
+        acc0[r] = acc1[r] = 0.f;
+      }
+      ++slice;
+    }
+  };
+
+  for (int f0 = 0; f0 < total; f0 += kDepth) {
+#pragma unroll
+    for (int u = 0; u < kDepth; ++u) {
+      if (f0 + u >= total) break;
+      if (cc == 0) {  // a new item: expert, routes, this lane's activation row
+        const int slot = item / rgroups;
+        row0 = (item - slot * rgroups) * kRowsPerGroup;
+        e = ws.active[slot];
+        begin = ws.offsets[e];
+        n_e = ws.offsets[e + 1] - begin;
+        brow = nullptr;
+        if (g < n_e) {
+          const int pos = begin + g;
+          brow = a.act + (FC1 ? (int64_t)(ws.sorted_route[pos] / p.k) : (int64_t)pos) * K;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc0[r] = acc1[r] = 0.f;
+        slice = sl0;
+      }
+      const int q = cb + cc;
+      close_slices_until(q);
+      uint32_t pa[16], pb[16];
+      dequant_chunk<BITS>(ring_a[u], pa);
+      dequant_chunk<BITS>(ring_b[u], pb);
+      if (f0 + u + kDepth < total) load(ring_a[u], ring_b[u]);
+      uint32_t bw[16];
+      const int kk = q * kChunkK + 32 * c;
+      if (brow != nullptr && kk < K) {
+        const uint4* src = reinterpret_cast<const uint4*>(brow + kk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 v = __ldg(src + j);
+          bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) bw[j] = 0u;
+      }
+#pragma unroll
+      for (int s = 0; s < 8; s += 2) {
+        mma16816(acc0, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
+        mma16816(acc1, pa[2 * s + 2], pb[2 * s + 2], pa[2 * s + 3], pb[2 * s + 3], bw[2 * s + 2], bw[2 * s + 3]);
+      }
+      if (++cc < cpi) continue;
+
+      // ---- item finished: close its slices, reduce split K in slice order, epilogue
+      cc = 0;
+      item += teams_total;
+      close_slices_until(nq);
+      if (ks > 1) {
+        asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
+        if (ksi == 0) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            float v = tred[lane * 4 + r];
+            for (int sl = 1; sl < kSlices; ++sl) v += tred[(sl * 32 + lane) * 4 + r];
+            tot[r] = v;
+          }
+        }
+      }
+      if (ksi == 0) {
+        const int n0 = 2 * c, n1 = 2 * c + 1;
+        if constexpr (FC1) {
+          // gate rows are even, up rows odd: lane g+1 (lane + 4) holds the up rows of lane g
+          float up[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) up[r] = __shfl_down_sync(0xffffffffu, tot[r], 4);
+          if ((g & 1) == 0) {
+            const int G = perm_group(p.bits);
+            const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int n = (r & 1) ? n1 : n0;
+              if (n < n_e) {
+                const int pos = begin + n;
+                const float sigma = ws.tok_scale[ws.sorted_route[pos] / p.k];
+                const float inv = 1.0f / sigma;
+                const float h = silu(tot[r] * inv) * (up[r] * inv) * sigma * sigma;
+                const int j = (r & 2) ? j_hi : j_lo;
+                ws.h16[(int64_t)pos * p.I + permuted_pos(j, G)] = __half_as_ushort(__float2half_rn(h));
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int n = (r & 1) ? n1 : n0;
+            if (n < n_e) {
+              const int rid = ws.sorted_route[begin + n];
+              const float inv = 1.0f / ws.tok_scale[rid / p.k];
+              const int row = row0 + g + ((r & 2) ? 8 : 0);
+              ws.y[(int64_t)rid * p.H + row] = tot[r] * inv * inv * ws.topk_w[rid];
+            }
+          }
+        }
+      }
+      if (ks > 1) asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
+    }
   }
-  dim3 grid(a.N / kRowsPerCta, active_max);
-  const int warps = a.ksplit > 4 ? a.ksplit : 4;  // >= 128 threads for the epilogue
-  decode_gemv_kernel<BITS, FC1><<<grid, 32 * warps, smem, s>>>(a);
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+constexpr int kBlocksPerSm = 2;
+
+template <int BITS, bool FC1>
+cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
+  const int rgroups = a.N / kRowsPerGroup;
+  const int64_t items = (int64_t)active_max * rgroups;
+  const int64_t warps = (int64_t)sm_count() * kBlocksPerSm * kWarps;
+  // the smallest K split that gives every warp several items' worth of chunks
+  // Every warp of a team must own at least one K chunk (so that all of them reach
+  // the team barriers once per item): ks <= number of 128-wide chunks.
+  const int nq = (a.K + kChunkK - 1) / kChunkK;
+  int ks = 1;
+  while (ks < kWarps && 2 * ks <= nq && items * ks < 4 * warps) ks <<= 1;
+  a.ks = ks;
+  const int64_t teams_needed = items;
+  int64_t blocks = (teams_needed + (kWarps / ks) - 1) / (kWarps / ks);
+  const int64_t cap = (int64_t)sm_count() * kBlocksPerSm;
+  if (blocks > cap) blocks = cap;
+  const size_t smem = ks > 1 ? (size_t)(kWarps / ks) * kSlices * 32 * 4 * sizeof(float) : 0;
+  decode_gemv_kernel<BITS, FC1><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -293,9 +433,7 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
   const int64_t R = p.R();
   const int active_max = (int)(R < p.E ? R : p.E);
   DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
-               fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 0, p, ws};
-  const int nq = (a.K + kChunkK - 1) / kChunkK;
-  a.ksplit = nq < kMaxKsplit ? nq : kMaxKsplit;
+               fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
   return fc1 ? launch_one<BITS, true>(a, active_max, s) : launch_one<BITS, false>(a, active_max, s);
 }
 

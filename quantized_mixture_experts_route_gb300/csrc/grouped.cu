@@ -1,11 +1,545 @@
-// grouped.cu -- grouped per-expert dequant-GEMM path (tcgen05, sm_103a).
+// grouped.cu -- grouped per-expert dequant-GEMM path on tcgen05 (sm_103a).
+//
+// For T > 8 the routes are grouped by expert (sorted order) and cut into tiles
+// of 128 consecutive sorted rows that all belong to one expert, the grouped
+// prefill scheme of the pages (BuildInt3ExpertTilesKernel / sorted expert map
+// feeding the grouped GEMMs, "[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload
+// ..." #33731; CUTLASS MoeFCGemm for INT4 prefill). One CTA computes a
+// 128 x BN tile of  D = A * W_e^T  for one expert e:
+//
+//   warp 0      TMA producer: A tile (FP16 activations, 128B-swizzled) and the
+//               packed code tile of W_e (raw bytes) per K step, into a ring of
+//               shared-memory stages (cp.async.bulk.tensor + mbarrier tx counts);
+//   warp 1      allocates the TMEM accumulator; one lane issues tcgen05.mma
+//               (kind::f16, M=128, N=BN, K=16 per instruction) and commits each
+//               stage back to the producer with tcgen05.commit;
+//   warps 2..5  dequantise the code tile to FP16 in registers ((code - zp) * s,
+//               exact for BF16 scales) and store it in the 128B-swizzled K-major
+//               layout that the MMA descriptor names; after the K loop they read
+//               the accumulator with tcgen05.ld and run the epilogue.
+//
+// Operands are FP16 (not BF16): (code - zp) * scale needs up to 11 significant
+// bits, which FP16 holds exactly and BF16 does not; FP16 and BF16 run at the
+// same tensor rate. fc1 epilogue: SwiGLU of the interleaved gate/up columns,
+// FP16 store in the K-order permutation of the fc2 operand. fc2 epilogue: FP32
+// rows scaled by the routing weight, stored per route id for the combine.
+//
+// Every mbarrier wait gives up after a bounded number of polls: the CTA then
+// records an error code in the workspace, drains, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "qmoe_internal.cuh"
 
 namespace qmoe {
+namespace {
 
-cudaError_t launch_grouped(const Problem&, bool, const uint8_t*, const void*, const uint8_t*,
-                           const Workspace&, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kBM = 128;
+constexpr int kStages = 3;
+constexpr int kThreads = 192;          // 6 warps
+constexpr int kDequantThreads = 128;   // warps 2..5
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
+constexpr int kErrTimeout = 1;
+
+template <int BITS>
+struct Cfg {
+  static constexpr int BK = BITS == 3 ? 128 : 64;     // K per stage
+  static constexpr int BN = BITS == 3 ? 128 : 256;    // weight rows per tile
+  static constexpr int SUB = BK / 64;                 // 64-wide swizzle atoms per stage
+  static constexpr int A_BYTES = kBM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int CODE_ROW = BK * BITS / 8;      // bytes of codes per weight row per stage
+  static constexpr int C_BYTES = BN * CODE_ROW;
+  static constexpr int UNIT_BYTES = 4 * BITS;         // 32 codes
+  static constexpr int UNITS_PER_ROW = BK / 32;
+  static constexpr int UNITS = BN * UNITS_PER_ROW;
+  static constexpr int UNITS_PER_THREAD = UNITS / kDequantThreads;
+  static constexpr int A_OFF = 0;
+  static constexpr int B_OFF = A_OFF + kStages * A_BYTES;
+  static constexpr int C_OFF = B_OFF + kStages * B_BYTES;
+  static constexpr int BAR_OFF = C_OFF + kStages * C_BYTES;
+  static constexpr int SMEM = BAR_OFF + 128 + 1024;   // barriers + TMEM address + alignment slack
+  static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+
+// Bounded wait that ignores the abort flags (used to drain work in flight).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kDrainLimitNs) return false;
+  }
+}
+
+// Bounded wait. Returns false if this CTA or another CTA of the launch gave up,
+// or if the phase does not complete within kWaitLimitNs; in the last case the
+// CTA's abort flag and the launch-wide error flag in the workspace are set.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          volatile int* launch_err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((i & 255u) == 0) {
+      if (*launch_err) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        *launch_err = kErrTimeout;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
+// layout (8 rows x 128 bytes per swizzle atom, atoms 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);        // start address
+  d |= (uint64_t)1 << 16;                          // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                          // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                          // swizzle mode: 128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulator, FP16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+        "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+        "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+// ------------------------------------------------------------------ dequantisation
+
+__device__ __forceinline__ uint32_t h2_sub_mul(uint32_t biased, uint32_t zp2, uint32_t s2) {
+  const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&biased),
+                                    *reinterpret_cast<const __half2*>(&zp2)),
+                            *reinterpret_cast<const __half2*>(&s2));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// The 16 FP16 pairs of 32 packed codes in the activations' K-order permutation
+// (pair p holds stored K positions 2p and 2p+1; see perm_group).
+template <int BITS>
+__device__ __forceinline__ void dequant_unit(const uint32_t* w, uint32_t z2, uint32_t s2, uint32_t* pr) {
+  constexpr uint32_t kMagic = 0x64006400u;  // FP16 1024.0 in both halves
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        pr[4 * i + m] = h2_sub_mul(((w[i] >> (4 * m)) & 0x000F000Fu) | kMagic, z2, s2);
+  } else if constexpr (BITS == 2) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        pr[8 * i + m] = h2_sub_mul(((w[i] >> (2 * m)) & 0x00030003u) | kMagic, z2, s2);
+  } else {
+    const uint32_t v0 = __byte_perm(w[0], w[1], 0x4310), v1 = __byte_perm(w[0], w[1], 0x5421);
+    const uint32_t v2 = __byte_perm(w[1], w[2], 0x6532), v3 = __byte_perm(w[1], w[2], 0x7643);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const uint32_t lo = m < 5 ? (v0 >> (3 * m)) : (v1 >> (3 * m - 8));
+      const uint32_t hi = m < 5 ? (v2 >> (3 * m)) : (v3 >> (3 * m - 8));
+      pr[m] = h2_sub_mul((lo & 0x00070007u) | kMagic, z2, s2);
+      pr[8 + m] = h2_sub_mul((hi & 0x00070007u) | kMagic, z2, s2);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t scale_half2(uint16_t bits, int dtype) {
+  uint16_t h = bits;
+  if (dtype == QMOE_BF16) h = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)bits << 16)));
+  return (uint32_t)h * 0x00010001u;
+}
+
+__device__ __forceinline__ int permuted_pos(int j, int G) {
+  const int base = j - j % G, i = j % G;
+  return base + (i < G / 2 ? 2 * i : 2 * (i - G / 2) + 1);
+}
+
+struct GemmArgs {
+  const uint16_t* scales;  // [E][N][K/block]
+  const uint8_t* zp;       // [E][N][K/block] or null
+  int N, K;
+  Problem p;
+  Workspace ws;
+};
+
+template <int BITS, bool FC1>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_q, GemmArgs g) {
+  using C = Cfg<BITS>;
+  const Workspace& ws = g.ws;
+  const Problem& p = g.p;
+  const int tile = blockIdx.y;
+  volatile int* launch_err = ws.counters + 2;   // set by a CTA whose wait timed out
+  if (tile >= ws.counters[1] || *launch_err) return;
+  const int e = ws.tiles[2 * tile];
+  const int row0 = ws.tiles[2 * tile + 1];     // first sorted row of the tile
+  const int rows = min(kBM, ws.offsets[e + 1] - row0);
+  const int n0 = blockIdx.x * C::BN;
+  const int K = g.K, N = g.N;
+  const int ksteps = K / C::BK;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  // bars[0..S): TMA full; [S..2S): B dequantised; [2S..3S): stage free; [3S]: accumulator ready
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar_full = [&](int s) { return bar0 + 8u * s; };
+  auto bar_bready = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+  const uint32_t bar_accum = bar0 + 8u * (3 * kStages);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * kStages + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * kStages + 1) + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_bready(s), kDequantThreads);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_accum, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     smem_u32((const void*)tmem_slot)),
+                 "r"(C::BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < ksteps; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!mbar_wait(bar_empty(s), ph ^ 1u, abort_flag, launch_err)) break;
+        ++issued;
+        mbar_expect_tx(bar_full(s), C::A_BYTES + C::C_BYTES);
+        const int k0 = i * C::BK;
+#pragma unroll
+        for (int sub = 0; sub < C::SUB; ++sub)
+          tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128), &tmap_a, bar_full(s),
+                      k0 + 64 * sub, row0);
+        tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8,
+                    e * N + n0);
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA exits
+        for (int i = issued - kStages > 0 ? issued - kStages : 0; i < issued; ++i)
+          mbar_wait_drain(bar_full(i % kStages), (uint32_t)(i / kStages) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(kBM, C::BN);
+      for (int i = 0; i < ksteps; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) break;
+        if (!mbar_wait(bar_bready(s), ph, abort_flag, launch_err)) break;
+        tc_fence_after();
+        const uint32_t a_base = sbase + C::A_OFF + s * C::A_BYTES;
+        const uint32_t b_base = sbase + C::B_OFF + s * C::B_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk) {
+          const int sub = kk / 4, off = (kk % 4) * 32;
+          tc_mma(tmem, sw128_desc(a_base + sub * (kBM * 128) + off),
+                 sw128_desc(b_base + sub * (C::BN * 128) + off), idesc, (i | kk) != 0);
+        }
+        tc_commit(bar_empty(s));
+      }
+      tc_commit(bar_accum);
+      if (*abort_flag) mbar_wait_drain(bar_accum, 0);  // MMAs in flight finish before TMEM is freed
+    }
+  } else {
+    // ---------------- dequantisation (warps 2..5), then the epilogue
+    const int t = threadIdx.x - 64;
+    const int nblk = K / p.block;
+    const int64_t wrow_base = (int64_t)e * N + n0;
+    const int64_t wrow_end = (int64_t)p.E * N;
+    uint32_t s2[C::UNITS_PER_THREAD], z2[C::UNITS_PER_THREAD];
+    auto load_scales = [&](int i) {
+#pragma unroll
+      for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
+        const int unit = t + kDequantThreads * u;
+        const int r = unit / C::UNITS_PER_ROW, j = unit % C::UNITS_PER_ROW;
+        const int64_t wr = wrow_base + r;
+        const int b = (i * C::BK + 32 * j) / p.block;
+        if (wr < wrow_end) {
+          s2[u] = scale_half2(__ldg(g.scales + wr * nblk + b), p.dtype);
+          const uint32_t z = g.zp ? (uint32_t)__ldg(g.zp + wr * nblk + b) : (1u << (BITS - 1));
+          z2[u] = (0x6400u + z) * 0x00010001u;
+        } else {
+          s2[u] = 0u;
+          z2[u] = 0x64006400u;
+        }
+      }
+    };
+    if (ksteps > 0) load_scales(0);
+    for (int i = 0; i < ksteps; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      uint32_t cs2[C::UNITS_PER_THREAD], cz2[C::UNITS_PER_THREAD];
+#pragma unroll
+      for (int u = 0; u < C::UNITS_PER_THREAD; ++u) { cs2[u] = s2[u]; cz2[u] = z2[u]; }
+      if (i + 1 < ksteps) load_scales(i + 1);   // next stage's scales in flight
+      if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) break;
+      const uint8_t* codes = smem + C::C_OFF + s * C::C_BYTES;
+      uint8_t* bt = smem + C::B_OFF + s * C::B_BYTES;
+#pragma unroll
+      for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
+        const int unit = t + kDequantThreads * u;
+        const int r = unit / C::UNITS_PER_ROW, j = unit % C::UNITS_PER_ROW;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + r * C::CODE_ROW + j * C::UNIT_BYTES);
+        uint32_t w[BITS];
+#pragma unroll
+        for (int q = 0; q < BITS; ++q) w[q] = src[q];
+        uint32_t pr[16];
+        dequant_unit<BITS>(w, cz2[u], cs2[u], pr);
+        uint8_t* rowp = bt + (j >> 1) * (C::BN * 128) + r * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = (j & 1) * 4 + c;
+          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(pr[4 * c], pr[4 * c + 1], pr[4 * c + 2], pr[4 * c + 3]);
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(bar_bready(s));
+    }
+
+    // ---------------- epilogue: TMEM -> registers -> global
+    const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+    const int m = quarter * 32 + lane;            // tile row
+    const bool ok = mbar_wait(bar_accum, 0, abort_flag, launch_err);
+    tc_fence_after();
+    if (ok) {
+      const bool row_ok = m < rows;
+      const int pos = row0 + m;
+      const int rid = row_ok ? ws.sorted_route[pos] : 0;
+      const float sigma = row_ok ? ws.tok_scale[rid / p.k] : 1.0f;
+      const float inv = 1.0f / sigma;
+      for (int c0 = 0; c0 < C::BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+        if (!row_ok || n0 + c0 >= N) continue;
+        if constexpr (FC1) {
+          // columns are W1 rows n0 + c0 .. +31: gate/up pairs -> 16 outputs h_j
+          const int j0 = (n0 + c0) / 2;
+          constexpr int G = BITS == 4 ? 8 : 16;
+          uint16_t hv[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float gt = __uint_as_float(v[2 * q]) * inv;
+            const float ut = __uint_as_float(v[2 * q + 1]) * inv;
+            hv[q] = __half_as_ushort(__float2half_rn(silu(gt) * ut * sigma * sigma));
+          }
+          uint16_t ov[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) ov[permuted_pos(q, G)] = hv[q];
+          uint4* dst = reinterpret_cast<uint4*>(ws.h16 + (int64_t)pos * p.I + j0);
+          dst[0] = make_uint4(ov[0] | ((uint32_t)ov[1] << 16), ov[2] | ((uint32_t)ov[3] << 16),
+                              ov[4] | ((uint32_t)ov[5] << 16), ov[6] | ((uint32_t)ov[7] << 16));
+          dst[1] = make_uint4(ov[8] | ((uint32_t)ov[9] << 16), ov[10] | ((uint32_t)ov[11] << 16),
+                              ov[12] | ((uint32_t)ov[13] << 16), ov[14] | ((uint32_t)ov[15] << 16));
+        } else {
+          const float wr = ws.topk_w[rid];
+          const float f = inv * inv;
+          float4* dst = reinterpret_cast<float4*>(ws.y + (int64_t)rid * p.H + n0 + c0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * f * wr, __uint_as_float(v[4 * q + 1]) * f * wr,
+                                 __uint_as_float(v[4 * q + 2]) * f * wr,
+                                 __uint_as_float(v[4 * q + 3]) * f * wr);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::BN)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner,
+                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle) {
+  auto fn = encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BITS, bool FC1>
+cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
+                        const Workspace& ws, cudaStream_t s) {
+  using C = Cfg<BITS>;
+  const int N = FC1 ? 2 * p.I : p.H;
+  const int K = FC1 ? p.H : p.I;
+  const int64_t R = p.R();
+  const uint16_t* A = FC1 ? ws.x16s : ws.h16;
+  CUtensorMap ta, tq;
+  if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2,
+                   64, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const uint64_t row_bytes = (uint64_t)K * BITS / 8;
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, row_bytes, (uint64_t)p.E * N, row_bytes,
+                   C::CODE_ROW, C::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BITS, FC1>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  GemmArgs g{static_cast<const uint16_t*>(scales), zp, N, K, p, ws};
+  if (ws.max_tiles > 65535) return cudaErrorNotSupported;  // grid.y limit: T * top_k < ~8.3M routes
+  dim3 grid((N + C::BN - 1) / C::BN, (unsigned)ws.max_tiles);
+  grouped_gemm_kernel<BITS, FC1><<<grid, kThreads, C::SMEM, s>>>(ta, tq, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
+                           const uint8_t* zp, const Workspace& ws, cudaStream_t s) {
+  switch (p.bits) {
+    case 4: return fc1 ? launch_gemm<4, true>(p, q, scales, zp, ws, s) : launch_gemm<4, false>(p, q, scales, zp, ws, s);
+    case 3: return fc1 ? launch_gemm<3, true>(p, q, scales, zp, ws, s) : launch_gemm<3, false>(p, q, scales, zp, ws, s);
+    case 2: return fc1 ? launch_gemm<2, true>(p, q, scales, zp, ws, s) : launch_gemm<2, false>(p, q, scales, zp, ws, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qmoe

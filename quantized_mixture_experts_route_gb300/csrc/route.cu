@@ -249,7 +249,10 @@ __device__ void finish_groups(int E, int total_e, const Workspace& ws, bool want
   int n_active;
   const int apos = block_exclusive_scan(v > 0 ? 1 : 0, sh, &n_active);
   if (e < E && v > 0) ws.active[apos] = e;
-  if (e == 0) ws.counters[0] = n_active;
+  if (e == 0) {
+    ws.counters[0] = n_active;
+    ws.counters[2] = 0;  // error flag of the grouped GEMM (set on a timed-out wait)
+  }
   if (want_tiles) {
     const int nt = (v + kTileM - 1) / kTileM;
     int n_tiles;

@@ -197,3 +197,66 @@ def test_empty_batch():
     p = qm.problem(0, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block, shape.dtype)
     qm.qmoe_forward(p, None, None, None, None, None, None, None, None, None, None)
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ grouped (tcgen05) path
+
+GROUPED_CASES = {
+    # name: (shape, recipe, seed); several 128-row tiles per expert, ragged M and N tails
+    "g_int4_bf16": (Shape(T=700, H=256, inter=192, E=8, k=2, bits=4, block=32, dtype=BF16),
+                    Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 51),
+    "g_int4_fp16_zp": (Shape(T=333, H=512, inter=128, E=6, k=3, bits=4, block=64, dtype=FP16),
+                       Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, explicit_zp=True), 52),
+    "g_int2_fp16": (Shape(T=400, H=320, inter=256, E=5, k=2, bits=2, block=32, dtype=FP16),
+                    Recipe(logit_std=1.0, scale_lo=0.01, scale_hi=0.04), 53),
+    "g_int3_b64": (Shape(T=500, H=384, inter=256, E=7, k=2, bits=3, block=64, dtype=BF16),
+                   Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 54),
+    "g_int3_b128_zp": (Shape(T=300, H=256, inter=384, E=4, k=2, bits=3, block=128, dtype=BF16),
+                       Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, explicit_zp=True), 55),
+    "g_small_T_forced": (Shape(T=5, H=256, inter=128, E=4, k=2, bits=4, block=32, dtype=BF16),
+                         Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 56),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GROUPED_CASES))
+def test_forward_parity_grouped(name):
+    shape, recipe, seed = GROUPED_CASES[name]
+    inp = synthetic.make_numpy(shape, recipe, seed)
+    got = gu.gpu_forward(shape, inp, path=2)
+    ref, _ = oracle.forward(oproblem(shape), inp)
+    gu.assert_parity(got, ref, shape.dtype, name)
+
+
+def test_grouped_matches_decode_on_small_batch():
+    shape, recipe, seed = synthetic.decode_layer(8)
+    inp = synthetic.make_numpy(shape, recipe, seed)
+    a = gu.to_f64(gu.gpu_forward(shape, inp, path=1), shape.dtype)
+    b = gu.to_f64(gu.gpu_forward(shape, inp, path=2), shape.dtype)
+    assert np.linalg.norm(a - b) / np.linalg.norm(a) < 1e-3
+
+
+def _sampled(shape, recipe, seed, n_sample, big_weights=True):
+    inp = synthetic.make_numpy(shape, recipe, seed)
+    got = gu.gpu_forward(shape, inp)
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(shape.T, size=n_sample, replace=False))
+    toks = np.unique(np.concatenate([toks, [0, shape.T - 1]]))
+    ref, _ = oracle.forward(oproblem(shape), inp, tokens=toks)
+    return got[toks], ref
+
+
+@pytest.mark.parametrize("which", ["prefill_8k", "int2_32k", "int3_b64_T512", "int3_b128_T512", "decode_T64"])
+def test_full_size_sampled(which):
+    """Full-size workloads in the launch configuration the benchmark times, checked
+    on sampled tokens that the oracle computes one by one."""
+    if which == "prefill_8k":
+        shape, recipe, seed = synthetic.prefill_8k()
+    elif which == "int2_32k":
+        shape, recipe, seed = synthetic.int2_prefill_32k()
+    elif which == "decode_T64":
+        shape, recipe, seed = synthetic.decode_layer(64)
+    else:
+        b = int(which.split("_b")[1].split("_")[0])
+        shape, recipe, seed = synthetic.int3_zipf(512, b)
+    got, ref = _sampled(shape, recipe, seed, 48)
+    gu.assert_parity(got, ref, shape.dtype, which)
