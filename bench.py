@@ -245,6 +245,18 @@ def run_reference(args):
 
 # --------------------------------------------------------------------------- GPU
 
+def p_path(shape):
+    return "decode" if shape.T <= 8 else "grouped"
+
+
+def launches_per_layer(path, shape):
+    """Kernels one qmoe_forward call launches (see csrc/api.cu and csrc/route.cu)."""
+    small = shape.T * shape.k <= 512
+    route = 1 if small else 4            # fused route+group, or route, count, scan, scatter
+    if path == "decode":
+        return route + 3                 # fc1, fc2, combine
+    return route + 1 + 3                 # gather, fc1, fc2, combine
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -425,7 +437,7 @@ def run_ours(args):
         "e2e": {"value": round(tokens_per_step / e2e_s, 1), "unit": "layer-tokens/s",
                 "h2d_bytes_per_step": int(x_pin.numel() * 2 + lg_pin.numel() * 2),
                 "d2h_bytes_per_step": int(out_pin.numel() * 2)},
-        "gpu_launches": int(4 * layers * args.steps),
+        "gpu_launches": int(launches_per_layer(p_path(shape), shape) * layers * args.steps),
         "clocks": clocks.summary(),
         **extra,
     }

@@ -223,6 +223,16 @@ __device__ __forceinline__ void dequant_chunk(const RowChunk<BITS>& r, uint32_t*
   }
 }
 
+// Per-lane cursor over the weight rows of one item: code and scale pointers of
+// rows g and g+8 at the lane's current chunk, advanced by constant strides.
+template <int BITS>
+struct RowCursor {
+  const uint8_t* qa;
+  const uint16_t* sa;
+  const uint8_t* za;
+  int kk;                 // K position of the lane's 32 codes in the current chunk
+};
+
 template <int BITS, bool FC1>
 __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs a) {
   const Problem& p = a.p;
@@ -242,25 +252,39 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   // this warp's K range: fixed slices [sl0, sl1) = chunks [cb, ce)
   const int sl0 = kSlices * ksi / ks, sl1 = kSlices * (ksi + 1) / ks;
   const int cb = nq * sl0 / kSlices, ce = nq * sl1 / kSlices;
-  const int cpi = ce - cb;                       // chunks per item for this warp
+  const int cpi = ce - cb;                       // chunks per item for this warp (>= 1)
   const int my_items = team_global < items ? (items - team_global + teams_total - 1) / teams_total : 0;
   const int total = my_items * cpi;
   const int64_t pitch = (int64_t)K * BITS / 8;
   const int nblk = K / p.block;
+  const int lb = 31 - __clz(p.block);            // block is a power of two
+  const int64_t row8_codes = 8 * pitch;          // row g+8 relative to row g
+  const int row8_scales = 8 * nblk;
+  constexpr int kChunkBytes = kChunkK * BITS / 8;
+  const int chunk_scales = kChunkK >> lb;        // scale entries per 128-wide chunk (1, 2 or 4)
 
-  // chunk f of this warp -> (item, chunk) without divisions: walk counters
-  int pf_item = team_global, pf_cc = 0;          // prefetch cursor
-  auto load = [&](RowChunk<BITS>& ra, RowChunk<BITS>& rb) {
-    const int slot = pf_item / rgroups, rg = pf_item - slot * rgroups;
+  // prefetch cursor: (item, chunk) of the next chunk to load, and its row pointers
+  int pf_item = team_global, pf_cc = 0;
+  RowCursor<BITS> pc;
+  auto seek = [&](int it) {
+    const int slot = it / rgroups;
     const int e = ws.active[slot];
-    const int64_t rowA = (int64_t)e * N + rg * kRowsPerGroup + g;
-    const int kk = (cb + pf_cc) * kChunkK + 32 * c;
-    const bool valid = kk < K;
-    const int b = valid ? kk / p.block : 0;
-    load_row_chunk<BITS>(ra, a.q + rowA * pitch + (int64_t)kk * BITS / 8, a.s + rowA * nblk + b,
-                         a.zp ? a.zp + rowA * nblk + b : nullptr, valid, p.dtype);
-    load_row_chunk<BITS>(rb, a.q + (rowA + 8) * pitch + (int64_t)kk * BITS / 8, a.s + (rowA + 8) * nblk + b,
-                         a.zp ? a.zp + (rowA + 8) * nblk + b : nullptr, valid, p.dtype);
+    const int64_t row = (int64_t)e * N + (it - slot * rgroups) * kRowsPerGroup + g;
+    pc.kk = cb * kChunkK + 32 * c;
+    pc.qa = a.q + row * pitch + (int64_t)pc.kk * BITS / 8;
+    pc.sa = a.s + row * nblk + (pc.kk >> lb);
+    pc.za = a.zp ? a.zp + row * nblk + (pc.kk >> lb) : nullptr;
+  };
+  auto load = [&](RowChunk<BITS>& ra, RowChunk<BITS>& rb) {
+    if (pf_cc == 0) seek(pf_item);
+    const bool valid = pc.kk < K;
+    load_row_chunk<BITS>(ra, pc.qa, pc.sa, pc.za, valid, p.dtype);
+    load_row_chunk<BITS>(rb, pc.qa + row8_codes, pc.sa + row8_scales, pc.za ? pc.za + row8_scales : nullptr,
+                         valid, p.dtype);
+    pc.qa += kChunkBytes;
+    pc.sa += chunk_scales;
+    if (pc.za) pc.za += chunk_scales;
+    pc.kk += kChunkK;
     if (++pf_cc == cpi) { pf_cc = 0; pf_item += teams_total; }
   };
 
@@ -305,7 +329,8 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
         brow = nullptr;
         if (g < n_e) {
           const int pos = begin + g;
-          brow = a.act + (FC1 ? (int64_t)(ws.sorted_route[pos] / p.k) : (int64_t)pos) * K;
+          brow = a.act + (FC1 ? (int64_t)(ws.sorted_route[pos] / p.k) : (int64_t)pos) * K +
+                 cb * kChunkK + 32 * c;
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc0[r] = acc1[r] = 0.f;
@@ -313,14 +338,9 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
       }
       const int q = cb + cc;
       close_slices_until(q);
-      uint32_t pa[16], pb[16];
-      dequant_chunk<BITS>(ring_a[u], pa);
-      dequant_chunk<BITS>(ring_b[u], pb);
-      if (f0 + u + kDepth < total) load(ring_a[u], ring_b[u]);
       uint32_t bw[16];
-      const int kk = q * kChunkK + 32 * c;
-      if (brow != nullptr && kk < K) {
-        const uint4* src = reinterpret_cast<const uint4*>(brow + kk);
+      if (brow != nullptr && q * kChunkK + 32 * c < K) {
+        const uint4* src = reinterpret_cast<const uint4*>(brow + cc * kChunkK);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint4 v = __ldg(src + j);
@@ -330,6 +350,10 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
 #pragma unroll
         for (int j = 0; j < 16; ++j) bw[j] = 0u;
       }
+      uint32_t pa[16], pb[16];
+      dequant_chunk<BITS>(ring_a[u], pa);
+      dequant_chunk<BITS>(ring_b[u], pb);
+      if (f0 + u + kDepth < total) load(ring_a[u], ring_b[u]);
 #pragma unroll
       for (int s = 0; s < 8; s += 2) {
         mma16816(acc0, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
