@@ -10,14 +10,17 @@
 // eight routes of a T <= 8 batch fit one MMA N-fragment, so every weight byte is
 // read exactly once per call and the tensor core does the multiply-adds.
 //
-// Work split. A warp owns a group of 16 weight rows of one active expert (one
-// MMA M-fragment) and a range of 128-wide K chunks; a quad of lanes covers the
-// 128 K of two rows (g, g+8) per chunk, lane c taking codes [32c, 32c+32). The
-// weight loads are issued before the activation rows are staged, and each lane
-// keeps kDepth chunks in flight in a register ring while it computes. A CTA of 8
-// warps holds rg whole row groups with K split ks = 8/rg ways, rg as large as
-// the batch allows while keeping two CTAs per SM busy; split-K partials are
-// added in a fixed warp order (no atomics), so results are bit-reproducible.
+// Work split. An item is (active expert, group of 16 weight rows = one MMA
+// M-fragment). Teams of ks warps (ks = 1..8, the K split) walk a static
+// round-robin list of items over a persistent grid of two CTAs per SM; a quad of
+// lanes covers 128 consecutive K of two rows (g, g+8) per chunk, lane c taking
+// codes [32c, 32c+32). Codes stream through a per-warp shared-memory ring of
+// kRing chunks filled by cp.async, so that eight chunks per warp are in flight
+// without holding registers; the next chunk's activations are prefetched into
+// registers; the expert of the next item comes from a decode table written by
+// the routing kernel, so no load waits on another load. K is cut into 8 fixed
+// slices whose FP32 sums are added left to right whatever ks is, so results are
+// bit-reproducible and do not depend on the batch size.
 //
 // Numerics. A weight is (code - zp) * scale: with the code placed in the
 // mantissa of FP16 1024.0, one exact FP16 subtraction gives (code - zp) and one
@@ -37,26 +40,7 @@ namespace {
 constexpr int kRowsPerGroup = 16;  // rows of one MMA M-fragment
 constexpr int kWarps = 8;
 constexpr int kChunkK = 128;       // K covered by one quad of lanes per chunk
-constexpr int kDepth = 4;          // chunks in flight per lane (register ring)
 constexpr int kSlices = 8;         // fixed K slices (the largest K split)
-
-// Streaming 128-bit / 64-bit / 32-bit loads of read-once weight codes: no L1 allocation.
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];\n" : "=r"(v) : "l"(p));
-  return v;
-}
 
 // 32 codes of one weight row (one lane's share of a chunk) plus the FP16 pair
 // constants of its block: 1024 + zero point, and the scale.
@@ -70,31 +54,6 @@ __device__ __forceinline__ uint32_t scale_half2(uint16_t bits, int dtype) {
   uint16_t h = bits;
   if (dtype == QMOE_BF16) h = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)bits << 16)));
   return (uint32_t)h | ((uint32_t)h << 16);
-}
-
-template <int BITS>
-__device__ __forceinline__ void load_row_chunk(RowChunk<BITS>& r, const uint8_t* codes,
-                                               const uint16_t* scale, const uint8_t* zp, bool valid,
-                                               int dtype) {
-  if (!valid) {
-#pragma unroll
-    for (int i = 0; i < BITS; ++i) r.w[i] = 0u;
-    r.z2 = 0x64006400u;
-    r.s2 = 0u;  // zero scale: the lane contributes exact zeros
-    return;
-  }
-  if constexpr (BITS == 4) {
-    const uint4 v = ld_stream_v4(codes);
-    r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
-  } else if constexpr (BITS == 2) {
-    const uint2 v = ld_stream_v2(codes);
-    r.w[0] = v.x; r.w[1] = v.y;
-  } else {
-    r.w[0] = ld_stream_u32(codes); r.w[1] = ld_stream_u32(codes + 4); r.w[2] = ld_stream_u32(codes + 8);
-  }
-  r.s2 = scale_half2(__ldg(scale), dtype);
-  const uint32_t z = zp ? (uint32_t)__ldg(zp) : (1u << (BITS - 1));
-  r.z2 = (0x6400u + z) * 0x00010001u;
 }
 
 __device__ __forceinline__ uint32_t h2_sub_mul(uint32_t biased, uint32_t zp2, uint32_t s2) {
@@ -223,14 +182,40 @@ __device__ __forceinline__ void dequant_chunk(const RowChunk<BITS>& r, uint32_t*
   }
 }
 
-// Per-lane cursor over the weight rows of one item: code and scale pointers of
-// rows g and g+8 at the lane's current chunk, advanced by constant strides.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Copy one lane's 32 codes of one row (4*BITS bytes) into its shared slot.
 template <int BITS>
-struct RowCursor {
-  const uint8_t* qa;
-  const uint16_t* sa;
-  const uint8_t* za;
-  int kk;                 // K position of the lane's 32 codes in the current chunk
+__device__ __forceinline__ void copy_codes(uint32_t dst, const uint8_t* src) {
+  if constexpr (BITS == 4) {
+    cp_async16(dst, src);
+  } else if constexpr (BITS == 2) {
+    cp_async8(dst, src);
+  } else {
+    cp_async4(dst, src);
+    cp_async4(dst + 4, src + 4);
+    cp_async4(dst + 8, src + 8);
+  }
+}
+
+constexpr int kRing = 8;        // chunks in flight per warp (shared-memory ring)
+
+// Per-item data of the decode table entry of one active expert.
+struct ItemMeta {
+  int e, begin, n_e, tok;       // tok: token of route slot g (this lane's activation row)
 };
 
 template <int BITS, bool FC1>
@@ -249,7 +234,6 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   const int teams_per_block = kWarps / ks;
   const int team_global = blockIdx.x * teams_per_block + team;
   const int teams_total = gridDim.x * teams_per_block;
-  // this warp's K range: fixed slices [sl0, sl1) = chunks [cb, ce)
   const int sl0 = kSlices * ksi / ks, sl1 = kSlices * (ksi + 1) / ks;
   const int cb = nq * sl0 / kSlices, ce = nq * sl1 / kSlices;
   const int cpi = ce - cb;                       // chunks per item for this warp (>= 1)
@@ -257,50 +241,100 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   const int total = my_items * cpi;
   const int64_t pitch = (int64_t)K * BITS / 8;
   const int nblk = K / p.block;
-  const int lb = 31 - __clz(p.block);            // block is a power of two
-  const int64_t row8_codes = 8 * pitch;          // row g+8 relative to row g
-  const int row8_scales = 8 * nblk;
+  const int lb = 31 - __clz(p.block);
   constexpr int kChunkBytes = kChunkK * BITS / 8;
-  const int chunk_scales = kChunkK >> lb;        // scale entries per 128-wide chunk (1, 2 or 4)
+  const int chunk_scales = kChunkK >> lb;
 
-  // prefetch cursor: (item, chunk) of the next chunk to load, and its row pointers
-  int pf_item = team_global, pf_cc = 0;
-  RowCursor<BITS> pc;
-  auto seek = [&](int it) {
-    const int slot = it / rgroups;
-    const int e = ws.active[slot];
-    const int64_t row = (int64_t)e * N + (it - slot * rgroups) * kRowsPerGroup + g;
-    pc.kk = cb * kChunkK + 32 * c;
-    pc.qa = a.q + row * pitch + (int64_t)pc.kk * BITS / 8;
-    pc.sa = a.s + row * nblk + (pc.kk >> lb);
-    pc.za = a.zp ? a.zp + row * nblk + (pc.kk >> lb) : nullptr;
+  extern __shared__ __align__(16) uint8_t smem[];
+  // per warp: [kRing][2 rows][32 lanes][16 B] of codes; then the split-K buffers
+  const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(smem) + warp * (kRing * 2 * 32 * 16);
+  float* red = reinterpret_cast<float*>(smem + kWarps * kRing * 2 * 32 * 16);
+  float* tred = red + (size_t)team * kSlices * 32 * 4;
+
+  auto meta_of = [&](int it) {
+    ItemMeta m{0, 0, 0, 0};
+    if (it < items) {
+      const int32_t* d = ws.dtab + (it / rgroups) * kDtabInts;
+      m.e = d[0];
+      m.begin = d[1];
+      m.n_e = d[2];
+      m.tok = d[4 + g];
+    }
+    return m;
   };
-  auto load = [&](RowChunk<BITS>& ra, RowChunk<BITS>& rb) {
-    if (pf_cc == 0) seek(pf_item);
-    const bool valid = pc.kk < K;
-    load_row_chunk<BITS>(ra, pc.qa, pc.sa, pc.za, valid, p.dtype);
-    load_row_chunk<BITS>(rb, pc.qa + row8_codes, pc.sa + row8_scales, pc.za ? pc.za + row8_scales : nullptr,
-                         valid, p.dtype);
-    pc.qa += kChunkBytes;
-    pc.sa += chunk_scales;
-    if (pc.za) pc.za += chunk_scales;
-    pc.kk += kChunkK;
+
+  // ---- issue side: code rows of (pf_item, pf_cc) -> ring slot; scales -> register ring
+  int pf_item = team_global, pf_cc = 0;
+  ItemMeta pf_next = meta_of(pf_item);
+  const uint8_t* pq = nullptr;
+  const uint16_t* ps = nullptr;
+  const uint8_t* pz = nullptr;
+  int pkk = 0;
+  uint32_t sring[kRing], zring[kRing];
+  auto issue = [&](int slot_u) {
+    if (pf_cc == 0) {
+      const ItemMeta m = pf_next;
+      pf_next = meta_of(pf_item + teams_total);
+      const int slot = pf_item / rgroups;
+      const int64_t row = (int64_t)m.e * N + (pf_item - slot * rgroups) * kRowsPerGroup + g;
+      pkk = cb * kChunkK + 32 * c;
+      pq = a.q + row * pitch + (int64_t)pkk * BITS / 8;
+      ps = a.s + row * nblk + (pkk >> lb);
+      pz = a.zp ? a.zp + row * nblk + (pkk >> lb) : nullptr;
+    }
+    const uint32_t dst = ring_base + slot_u * (2 * 32 * 16) + lane * 16;
+    if (pkk < K) {
+      copy_codes<BITS>(dst, pq);
+      copy_codes<BITS>(dst + 32 * 16, pq + 8 * pitch);
+      sring[slot_u] = (uint32_t)__ldg(ps) | ((uint32_t)__ldg(ps + 8 * nblk) << 16);
+      zring[slot_u] = pz ? ((uint32_t)__ldg(pz) | ((uint32_t)__ldg(pz + 8 * nblk) << 16))
+                         : ((1u << (BITS - 1)) * 0x00010001u);
+    } else {
+      sring[slot_u] = 0u;   // zero scale: stale codes in the slot contribute exact zeros
+      zring[slot_u] = 0u;
+    }
+    cp_async_commit();
+    pq += kChunkBytes;
+    ps += chunk_scales;
+    if (pz) pz += chunk_scales;
+    pkk += kChunkK;
     if (++pf_cc == cpi) { pf_cc = 0; pf_item += teams_total; }
   };
 
-  RowChunk<BITS> ring_a[kDepth], ring_b[kDepth];
 #pragma unroll
-  for (int u = 0; u < kDepth; ++u)
-    if (u < total) load(ring_a[u], ring_b[u]);
+  for (int u = 0; u < kRing - 1; ++u) {
+    if (u < total) issue(u);
+    else cp_async_commit();
+  }
 
-  extern __shared__ __align__(16) float red[];   // [teams][kSlices][32][4] when ks > 1
-  float* tred = red + (size_t)team * kSlices * 32 * 4;
-
+  // ---- compute side
   int item = team_global, cc = 0;
-  int e = 0, begin = 0, n_e = 0, row0 = 0;
-  const uint16_t* brow = nullptr;                // this lane's activation row (route slot g)
-  float acc0[4], acc1[4], tot[4];
+  ItemMeta cur = meta_of(item), nxt = meta_of(item + teams_total);
+  auto brow_of = [&](const ItemMeta& m) -> const uint16_t* {
+    if (g >= m.n_e) return nullptr;
+    const int64_t row = FC1 ? (int64_t)m.tok : (int64_t)(m.begin + g);
+    return a.act + row * K + cb * kChunkK + 32 * c;
+  };
+  const uint16_t* brow = brow_of(cur);
+  uint32_t bnext[16];
+  auto load_b = [&](const uint16_t* src, int q) {
+    if (src != nullptr && q * kChunkK + 32 * c < K) {
+      const uint4* v4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = __ldg(v4 + j);
+        bnext[4 * j] = v.x; bnext[4 * j + 1] = v.y; bnext[4 * j + 2] = v.z; bnext[4 * j + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) bnext[j] = 0u;
+    }
+  };
+  if (total > 0) load_b(brow, cb);
+
+  float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f}, tot[4] = {0.f, 0.f, 0.f, 0.f};
   int slice = sl0;
+  int row0 = (item % (rgroups > 0 ? rgroups : 1)) * kRowsPerGroup;
   auto close_slices_until = [&](int gq) {
     while (slice < sl1 && nq * (slice + 1) / kSlices <= gq) {
 #pragma unroll
@@ -316,44 +350,52 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
     }
   };
 
-  for (int f0 = 0; f0 < total; f0 += kDepth) {
+  for (int f0 = 0; f0 < total; f0 += kRing) {
 #pragma unroll
-    for (int u = 0; u < kDepth; ++u) {
-      if (f0 + u >= total) break;
-      if (cc == 0) {  // a new item: expert, routes, this lane's activation row
-        const int slot = item / rgroups;
-        row0 = (item - slot * rgroups) * kRowsPerGroup;
-        e = ws.active[slot];
-        begin = ws.offsets[e];
-        n_e = ws.offsets[e + 1] - begin;
-        brow = nullptr;
-        if (g < n_e) {
-          const int pos = begin + g;
-          brow = a.act + (FC1 ? (int64_t)(ws.sorted_route[pos] / p.k) : (int64_t)pos) * K +
-                 cb * kChunkK + 32 * c;
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc0[r] = acc1[r] = 0.f;
-        slice = sl0;
-      }
+    for (int u = 0; u < kRing; ++u) {
+      const int f = f0 + u;
+      if (f >= total) break;
+      // keep kRing chunks in flight: issue f + kRing - 1 into the slot freed last iteration
+      if (f + kRing - 1 < total) issue((u + kRing - 1) % kRing);
+      else cp_async_commit();
+      cp_async_wait<kRing - 1>();   // chunk f has landed
+
       const int q = cb + cc;
       close_slices_until(q);
       uint32_t bw[16];
-      if (brow != nullptr && q * kChunkK + 32 * c < K) {
-        const uint4* src = reinterpret_cast<const uint4*>(brow + cc * kChunkK);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 v = __ldg(src + j);
-          bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
-        }
+      for (int j = 0; j < 16; ++j) bw[j] = bnext[j];
+      // next chunk's activations (same item, or the next item's first chunk)
+      if (cc + 1 < cpi) load_b(brow ? brow + (cc + 1) * kChunkK : nullptr, q + 1);
+      else load_b(brow_of(nxt), cb);
+
+      RowChunk<BITS> ra, rb;
+      const uint8_t* slotp = smem + warp * (kRing * 2 * 32 * 16) + u * (2 * 32 * 16) + lane * 16;
+      if constexpr (BITS == 4) {
+        const uint4 va = *reinterpret_cast<const uint4*>(slotp);
+        const uint4 vb = *reinterpret_cast<const uint4*>(slotp + 32 * 16);
+        ra.w[0] = va.x; ra.w[1] = va.y; ra.w[2] = va.z; ra.w[3] = va.w;
+        rb.w[0] = vb.x; rb.w[1] = vb.y; rb.w[2] = vb.z; rb.w[3] = vb.w;
+      } else if constexpr (BITS == 2) {
+        const uint2 va = *reinterpret_cast<const uint2*>(slotp);
+        const uint2 vb = *reinterpret_cast<const uint2*>(slotp + 32 * 16);
+        ra.w[0] = va.x; ra.w[1] = va.y;
+        rb.w[0] = vb.x; rb.w[1] = vb.y;
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) bw[j] = 0u;
+        for (int i = 0; i < 3; ++i) {
+          ra.w[i] = reinterpret_cast<const uint32_t*>(slotp)[i];
+          rb.w[i] = reinterpret_cast<const uint32_t*>(slotp + 32 * 16)[i];
+        }
       }
+      const uint32_t sp = sring[u], zp2 = zring[u];
+      ra.s2 = scale_half2((uint16_t)(sp & 0xFFFFu), p.dtype);
+      rb.s2 = scale_half2((uint16_t)(sp >> 16), p.dtype);
+      ra.z2 = (0x6400u + (zp2 & 0xFFFFu)) * 0x00010001u;
+      rb.z2 = (0x6400u + (zp2 >> 16)) * 0x00010001u;
       uint32_t pa[16], pb[16];
-      dequant_chunk<BITS>(ring_a[u], pa);
-      dequant_chunk<BITS>(ring_b[u], pb);
-      if (f0 + u + kDepth < total) load(ring_a[u], ring_b[u]);
+      dequant_chunk<BITS>(ra, pa);
+      dequant_chunk<BITS>(rb, pb);
 #pragma unroll
       for (int s = 0; s < 8; s += 2) {
         mma16816(acc0, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
@@ -362,8 +404,6 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
       if (++cc < cpi) continue;
 
       // ---- item finished: close its slices, reduce split K in slice order, epilogue
-      cc = 0;
-      item += teams_total;
       close_slices_until(nq);
       if (ks > 1) {
         asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
@@ -378,6 +418,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
       }
       if (ksi == 0) {
         const int n0 = 2 * c, n1 = 2 * c + 1;
+        const int begin = cur.begin, n_e = cur.n_e;
         if constexpr (FC1) {
           // gate rows are even, up rows odd: lane g+1 (lane + 4) holds the up rows of lane g
           float up[4];
@@ -386,16 +427,16 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
           if ((g & 1) == 0) {
             const int G = perm_group(p.bits);
             const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+            const int32_t* d = ws.dtab + (item / rgroups) * kDtabInts;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
               const int n = (r & 1) ? n1 : n0;
               if (n < n_e) {
-                const int pos = begin + n;
-                const float sigma = ws.tok_scale[ws.sorted_route[pos] / p.k];
+                const float sigma = ws.tok_scale[d[4 + n]];
                 const float inv = 1.0f / sigma;
                 const float h = silu(tot[r] * inv) * (up[r] * inv) * sigma * sigma;
                 const int j = (r & 2) ? j_hi : j_lo;
-                ws.h16[(int64_t)pos * p.I + permuted_pos(j, G)] = __half_as_ushort(__float2half_rn(h));
+                ws.h16[(int64_t)(begin + n) * p.I + permuted_pos(j, G)] = __half_as_ushort(__float2half_rn(h));
               }
             }
           }
@@ -413,8 +454,19 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
         }
       }
       if (ks > 1) asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
+      // next item
+      cc = 0;
+      item += teams_total;
+      cur = nxt;
+      nxt = meta_of(item + teams_total);
+      brow = brow_of(cur);
+      row0 = (item % rgroups) * kRowsPerGroup;
+      slice = sl0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc0[r] = acc1[r] = 0.f;
     }
   }
+  cp_async_wait<0>();
 }
 
 int sm_count() {
@@ -446,7 +498,15 @@ cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
   int64_t blocks = (teams_needed + (kWarps / ks) - 1) / (kWarps / ks);
   const int64_t cap = (int64_t)sm_count() * kBlocksPerSm;
   if (blocks > cap) blocks = cap;
-  const size_t smem = ks > 1 ? (size_t)(kWarps / ks) * kSlices * 32 * 4 * sizeof(float) : 0;
+  const size_t smem = (size_t)kWarps * kRing * 2 * 32 * 16 +
+                      (ks > 1 ? (size_t)(kWarps / ks) * kSlices * 32 * 4 * sizeof(float) : 0);
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t err = cudaFuncSetAttribute(decode_gemv_kernel<BITS, FC1>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
   decode_gemv_kernel<BITS, FC1><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -34,18 +34,21 @@
 namespace qmoe {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kStages = 3;
-constexpr int kThreads = 192;          // 6 warps
-constexpr int kDequantThreads = 128;   // warps 2..5
+constexpr int kSubM = 128;             // rows per MMA / TMEM accumulator
+constexpr int kBM = 2 * kSubM;         // rows per tile: two accumulators share each B stage
+constexpr int kDequantWarps = 8;       // warps 2..9
+constexpr int kDequantThreads = 32 * kDequantWarps;
+constexpr int kThreads = 64 + kDequantThreads;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
 constexpr int kErrTimeout = 1;
+static_assert(kBM == kTileM, "the grouping kernels cut tiles of kTileM sorted rows");
 
 template <int BITS>
 struct Cfg {
   static constexpr int BK = BITS == 3 ? 128 : 64;     // K per stage
-  static constexpr int BN = BITS == 3 ? 128 : 256;    // weight rows per tile
+  static constexpr int BN = BITS == 3 ? 128 : 256;    // weight rows per tile (MMA N)
+  static constexpr int STAGES = BITS == 3 ? 2 : 3;
   static constexpr int SUB = BK / 64;                 // 64-wide swizzle atoms per stage
   static constexpr int A_BYTES = kBM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
@@ -55,11 +58,14 @@ struct Cfg {
   static constexpr int UNITS_PER_ROW = BK / 32;
   static constexpr int UNITS = BN * UNITS_PER_ROW;
   static constexpr int UNITS_PER_THREAD = UNITS / kDequantThreads;
+  static constexpr int S_BYTES = UNITS * 4;           // per unit: FP16 scale | zero point << 16
   static constexpr int A_OFF = 0;
-  static constexpr int B_OFF = A_OFF + kStages * A_BYTES;
-  static constexpr int C_OFF = B_OFF + kStages * B_BYTES;
-  static constexpr int BAR_OFF = C_OFF + kStages * C_BYTES;
+  static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
+  static constexpr int C_OFF = B_OFF + STAGES * B_BYTES;
+  static constexpr int S_OFF = C_OFF + STAGES * C_BYTES;
+  static constexpr int BAR_OFF = S_OFF + STAGES * S_BYTES;
   static constexpr int SMEM = BAR_OFF + 128 + 1024;   // barriers + TMEM address + alignment slack
+  static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
   static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -236,11 +242,6 @@ __device__ __forceinline__ void dequant_unit(const uint32_t* w, uint32_t z2, uin
   }
 }
 
-__device__ __forceinline__ uint32_t scale_half2(uint16_t bits, int dtype) {
-  uint16_t h = bits;
-  if (dtype == QMOE_BF16) h = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)bits << 16)));
-  return (uint32_t)h * 0x00010001u;
-}
 
 __device__ __forceinline__ int permuted_pos(int j, int G) {
   const int base = j - j % G, i = j % G;
@@ -255,11 +256,57 @@ struct GemmArgs {
   Workspace ws;
 };
 
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));  // (a & mask) | orv
+  return d;
+}
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  const __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&c));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 32 codes -> 16 FP16 pairs in the activations' K-order permutation. INT4 uses
+// the in-place nibble decode (bits 4-7 read as 1024 + 16c and rescaled exactly by
+// one FMA with 1/16); INT2/INT3 cut each pair with a shift and a mask.
+template <int BITS>
+__device__ __forceinline__ void dequant_unit_fast(const uint32_t* w, uint32_t zp, uint32_t s2, uint32_t* pr) {
+  constexpr uint32_t kMagic = 0x64006400u;
+  const uint32_t z1 = (0x6400u + zp) * 0x00010001u;  // 1024 + zp
+  if constexpr (BITS == 4) {
+    // -(64 + zp), exactly representable for zp in 0..15
+    const __half2 nz = __float2half2_rn(-(64.0f + (float)zp));
+    const uint32_t z16v = *reinterpret_cast<const uint32_t*>(&nz);
+    constexpr uint32_t kSixteenth = 0x2C002C00u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t v = w[i], v8 = w[i] >> 8;
+      pr[4 * i + 0] = h2_mul(h2_sub(lop3_and_or(v, 0x000F000Fu, kMagic), z1), s2);
+      pr[4 * i + 1] = h2_mul(h2_fma(lop3_and_or(v, 0x00F000F0u, kMagic), kSixteenth, z16v), s2);
+      pr[4 * i + 2] = h2_mul(h2_sub(lop3_and_or(v8, 0x000F000Fu, kMagic), z1), s2);
+      pr[4 * i + 3] = h2_mul(h2_fma(lop3_and_or(v8, 0x00F000F0u, kMagic), kSixteenth, z16v), s2);
+    }
+  } else {
+    dequant_unit<BITS>(w, z1, s2, pr);
+  }
+}
+
+
 template <int BITS, bool FC1>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_q, GemmArgs g) {
   using C = Cfg<BITS>;
+  constexpr int S = C::STAGES;
   const Workspace& ws = g.ws;
   const Problem& p = g.p;
   const int tile = blockIdx.y;
@@ -275,20 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  // bars[0..S): TMA full; [S..2S): B dequantised; [2S..3S): stage free; [3S]: accumulator ready
-  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  // [0, S): TMA + scales landed; [S, 2S): B dequantised; [2S, 3S): stage free; [3S]: accumulators ready
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
-  auto bar_bready = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto bar_empty = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
-  const uint32_t bar_accum = bar0 + 8u * (3 * kStages);
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * kStages + 1));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * kStages + 1) + 4);
+  auto bar_bready = [&](int s) { return bar0 + 8u * (S + s); };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  const uint32_t bar_accum = bar0 + 8u * (3 * S);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * S + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * S + 1) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full(s), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full(s), 1 + 32);   // the TMA issue (with its byte count) + 32 scale writers
       mbar_init(bar_bready(s), kDequantThreads);
       mbar_init(bar_empty(s), 1);
     }
@@ -301,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                      smem_u32((const void*)tmem_slot)),
-                 "r"(C::BN)
+                 "r"(C::TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
@@ -309,38 +355,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int nblk = K / p.block;
 
   if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < ksteps; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(bar_empty(s), ph ^ 1u, abort_flag, launch_err)) break;
-        ++issued;
+    // ---------------- producer: TMA (lane 0) and the stage's scales (all lanes)
+    int issued = 0;
+    const int64_t wrow_base = (int64_t)e * N + n0;
+    const int64_t wrow_end = (int64_t)p.E * N;
+    for (int i = 0; i < ksteps; ++i) {
+      const int s = i % S;
+      const uint32_t ph = (uint32_t)(i / S) & 1u;
+      bool go = true;
+      if (lane == 0) go = mbar_wait(bar_empty(s), ph ^ 1u, abort_flag, launch_err);
+      go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+      if (!go) break;
+      ++issued;
+      const int k0 = i * C::BK;
+      if (lane == 0) {
         mbar_expect_tx(bar_full(s), C::A_BYTES + C::C_BYTES);
-        const int k0 = i * C::BK;
 #pragma unroll
         for (int sub = 0; sub < C::SUB; ++sub)
-          tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128), &tmap_a, bar_full(s),
-                      k0 + 64 * sub, row0);
-        tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8,
-                    e * N + n0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
+                        bar_full(s), k0 + 64 * sub, row0 + h * kSubM);
+        tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8, e * N + n0);
       }
-      if (*abort_flag) {
-        // let the copies already issued land before the CTA exits
-        for (int i = issued - kStages > 0 ? issued - kStages : 0; i < issued; ++i)
-          mbar_wait_drain(bar_full(i % kStages), (uint32_t)(i / kStages) & 1u);
+      uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
+      for (int u = lane; u < C::UNITS; u += 32) {
+        const int r = u / C::UNITS_PER_ROW, j = u % C::UNITS_PER_ROW;
+        const int64_t wr = wrow_base + r;
+        uint32_t v = 0u;                       // zero scale outside the weight array
+        if (wr < wrow_end) {
+          const int b = (k0 + 32 * j) / p.block;
+          const uint16_t sb = __ldg(g.scales + wr * nblk + b);
+          const uint16_t sh = p.dtype == QMOE_BF16
+                                  ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sb << 16)))
+                                  : sb;
+          const uint32_t z = g.zp ? (uint32_t)__ldg(g.zp + wr * nblk + b) : (1u << (BITS - 1));
+          v = (uint32_t)sh | (z << 16);
+        }
+        st[u] = v;
       }
+      mbar_arrive(bar_full(s));
+    }
+    if (lane == 0 && *abort_flag) {
+      // let the copies already issued land before the CTA exits
+      for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i)
+        mbar_wait_drain(bar_full(i % S), (uint32_t)(i / S) & 1u);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: two 128-row accumulators share each B stage
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(kBM, C::BN);
+      constexpr uint32_t idesc = idesc_f16(kSubM, C::BN);
       for (int i = 0; i < ksteps; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        const int s = i % S;
+        const uint32_t ph = (uint32_t)(i / S) & 1u;
         if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) break;
         if (!mbar_wait(bar_bready(s), ph, abort_flag, launch_err)) break;
         tc_fence_after();
@@ -349,8 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           const int sub = kk / 4, off = (kk % 4) * 32;
-          tc_mma(tmem, sw128_desc(a_base + sub * (kBM * 128) + off),
-                 sw128_desc(b_base + sub * (C::BN * 128) + off), idesc, (i | kk) != 0);
+          const uint64_t bdesc = sw128_desc(b_base + sub * (C::BN * 128) + off);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tc_mma(tmem + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
+                   idesc, (i | kk) != 0);
         }
         tc_commit(bar_empty(s));
       }
@@ -358,50 +431,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) mbar_wait_drain(bar_accum, 0);  // MMAs in flight finish before TMEM is freed
     }
   } else {
-    // ---------------- dequantisation (warps 2..5), then the epilogue
+    // ---------------- dequantisation (warps 2..9), then the epilogue
     const int t = threadIdx.x - 64;
-    const int nblk = K / p.block;
-    const int64_t wrow_base = (int64_t)e * N + n0;
-    const int64_t wrow_end = (int64_t)p.E * N;
-    uint32_t s2[C::UNITS_PER_THREAD], z2[C::UNITS_PER_THREAD];
-    auto load_scales = [&](int i) {
-#pragma unroll
-      for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
-        const int unit = t + kDequantThreads * u;
-        const int r = unit / C::UNITS_PER_ROW, j = unit % C::UNITS_PER_ROW;
-        const int64_t wr = wrow_base + r;
-        const int b = (i * C::BK + 32 * j) / p.block;
-        if (wr < wrow_end) {
-          s2[u] = scale_half2(__ldg(g.scales + wr * nblk + b), p.dtype);
-          const uint32_t z = g.zp ? (uint32_t)__ldg(g.zp + wr * nblk + b) : (1u << (BITS - 1));
-          z2[u] = (0x6400u + z) * 0x00010001u;
-        } else {
-          s2[u] = 0u;
-          z2[u] = 0x64006400u;
-        }
-      }
-    };
-    if (ksteps > 0) load_scales(0);
     for (int i = 0; i < ksteps; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-      uint32_t cs2[C::UNITS_PER_THREAD], cz2[C::UNITS_PER_THREAD];
-#pragma unroll
-      for (int u = 0; u < C::UNITS_PER_THREAD; ++u) { cs2[u] = s2[u]; cz2[u] = z2[u]; }
-      if (i + 1 < ksteps) load_scales(i + 1);   // next stage's scales in flight
+      const int s = i % S;
+      const uint32_t ph = (uint32_t)(i / S) & 1u;
       if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) break;
       const uint8_t* codes = smem + C::C_OFF + s * C::C_BYTES;
+      const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
       uint8_t* bt = smem + C::B_OFF + s * C::B_BYTES;
 #pragma unroll
       for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
         const int unit = t + kDequantThreads * u;
         const int r = unit / C::UNITS_PER_ROW, j = unit % C::UNITS_PER_ROW;
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + r * C::CODE_ROW + j * C::UNIT_BYTES);
+        const uint8_t* src = codes + r * C::CODE_ROW + j * C::UNIT_BYTES;
         uint32_t w[BITS];
+        if constexpr (BITS == 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        } else if constexpr (BITS == 2) {
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          w[0] = v.x; w[1] = v.y;
+        } else {
 #pragma unroll
-        for (int q = 0; q < BITS; ++q) w[q] = src[q];
+          for (int q = 0; q < 3; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
+        }
+        const uint32_t sz = st[unit];
+        const uint32_t s2 = (sz & 0xFFFFu) * 0x00010001u;
         uint32_t pr[16];
-        dequant_unit<BITS>(w, cz2[u], cs2[u], pr);
+        dequant_unit_fast<BITS>(w, sz >> 16, s2, pr);
         uint8_t* rowp = bt + (j >> 1) * (C::BN * 128) + r * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -415,8 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- epilogue: TMEM -> registers -> global
+    const int dw = warp - 2;
+    const int half = dw >> 2;                     // accumulator: tile rows 128*half ..
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
-    const int m = quarter * 32 + lane;            // tile row
+    const int m = half * kSubM + quarter * 32 + lane;
     const bool ok = mbar_wait(bar_accum, 0, abort_flag, launch_err);
     tc_fence_after();
     if (ok) {
@@ -425,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rid = row_ok ? ws.sorted_route[pos] : 0;
       const float sigma = row_ok ? ws.tok_scale[rid / p.k] : 1.0f;
       const float inv = 1.0f / sigma;
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
       for (int c0 = 0; c0 < C::BN; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+        tmem_ld32(tbase + (uint32_t)c0, v);
         if (!row_ok || n0 + c0 >= N) continue;
         if constexpr (FC1) {
           // columns are W1 rows n0 + c0 .. +31: gate/up pairs -> 16 outputs h_j
@@ -466,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::BN)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::TMEM_COLS)
                  : "memory");
   }
 }
@@ -510,7 +571,7 @@ cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, 
   const uint16_t* A = FC1 ? ws.x16s : ws.h16;
   CUtensorMap ta, tq;
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2,
-                   64, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+                   64, kSubM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const uint64_t row_bytes = (uint64_t)K * BITS / 8;
   if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, row_bytes, (uint64_t)p.E * N, row_bytes,

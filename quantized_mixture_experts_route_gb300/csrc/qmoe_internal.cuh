@@ -17,7 +17,8 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 constexpr int kDecodeMaxT = 8;        // decode GEMV: at most 8 routes per expert (one MMA N-fragment)
 constexpr int kPermuteChunk = 512;    // routes per block in the grouping kernels
-constexpr int kTileM = 128;           // rows (routes) per grouped-GEMM tile
+constexpr int kTileM = 256;           // rows (routes) per grouped-GEMM tile
+constexpr int kDtabInts = 12;         // ints per decode-table entry
 
 // ---------------------------------------------------------------------------
 // Workspace: every scratch buffer of one forward call, carved from the
@@ -32,8 +33,10 @@ struct Workspace {
   int32_t* sorted_route;  // [R]      route ids grouped by expert, stable
   int32_t* active;        // [E]      experts with at least one route, ascending
   int32_t* counters;      // [4]      [0] active experts, [1] grouped tiles
-  int32_t* tiles;         // [2*max_tiles] (expert, first sorted row) of each 128-row tile
+  int32_t* tiles;         // [2*max_tiles] (expert, first sorted row) of each kTileM-row tile
   int32_t* chunk_hist;    // [nchunks][E] per-chunk expert counts, then chunk bases
+  int32_t* dtab;          // [E][kDtabInts] decode table per active slot: expert, first sorted
+                          //   row, route count, 0, token of each of its <= 8 routes
   uint16_t* x16s;         // [R][H]   x16 rows gathered into sorted-route order (grouped)
   uint16_t* h16;          // [R][I]   SwiGLU output, FP16, sorted-route order, K-order permuted
   float* y;               // [R][H]   weighted fc2 output per route id (FP32)

@@ -336,6 +336,19 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   finish_groups(p.E, total, ws, want_tiles != 0, sh, hist);  // hist now holds the bases
   __syncthreads();
   scatter_routes(ws.topk_idx, 0, R, p.E, hist, warp_cnt, ws.sorted_route);
+  // decode table: one entry per active expert, so that the decode kernels reach an
+  // expert's rows and its routes' tokens with one independent load
+  const int n_active = ws.counters[0];
+  for (int a = threadIdx.x; a < n_active; a += blockDim.x) {
+    const int e = ws.active[a];
+    const int begin = ws.offsets[e], n_e = ws.offsets[e + 1] - begin;
+    int32_t* d = ws.dtab + a * kDtabInts;
+    d[0] = e;
+    d[1] = begin;
+    d[2] = n_e;
+    d[3] = 0;
+    for (int n = 0; n < 8; ++n) d[4 + n] = n < n_e ? ws.sorted_route[begin + n] / p.k : 0;
+  }
 }
 
 __global__ void __launch_bounds__(256) gather_kernel(Problem p, Workspace ws) {
