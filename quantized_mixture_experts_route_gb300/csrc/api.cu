@@ -132,7 +132,8 @@ qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last
   auto in_range = [&](int stage) { return first_stage <= stage && stage <= last_stage; };
   cudaError_t err = cudaSuccess;
   if (in_range(QMOE_STAGE_ROUTE)) {
-    err = launch_route(ip, x, router_logits, ws, true, s);
+    err = launch_route(ip, x, router_logits, ws,
+                       decode_int4_blockscaled(ip) ? kX16OddSixteenth : kX16Plain, s);
     if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
     if (err == cudaSuccess && grouped) err = launch_gather(ip, ws, s);
   }
@@ -170,7 +171,7 @@ qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t
   if (workspace_layout(ip, grouped, workspace, &ws) > workspace_bytes)
     return QMOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t err = launch_route(ip, nullptr, router_logits, ws, false, s);
+  cudaError_t err = launch_route(ip, nullptr, router_logits, ws, kX16None, s);
   if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
   const int64_t R = ip.R();
   if (err == cudaSuccess && topk_idx)

@@ -469,6 +469,290 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   cp_async_wait<0>();
 }
 
+int sm_count();
+constexpr int kBlocksPerSm = 2;
+
+// ---------------------------------------------------------------------------
+// INT4, block 32: block scales applied after the MMA
+//
+// Per weight the kernel only places the code in an FP16 mantissa: (v & 0x000F000F)
+// | 1024.0 gives 1024 + c for the nibbles at bits 0-3, and (v & 0x00F000F0) |
+// 1024.0 gives 1024 + 16c for the nibbles at bits 4-7 (the odd K positions of the
+// activations' layout). The activations carry 1/16 at odd K positions, so every
+// product is (1024 + c) * x exactly. A second MMA per step with the constant
+// operand -(1024 + zp) (even positions) / -(1024 + 16 zp) (odd positions) removes
+// the bias and the zero point, leaving sum_k (c_k - zp) x_k in FP32.
+//
+// That sum must be taken per 32-wide block, since each block has its own scale:
+// the B operand is laid out so that D column n = 4t + b only receives the K
+// positions of block b of the chunk (lane c of a quad owns block c, and only the
+// lanes with groupID % 4 == c supply a token's activations). The FP32 block sums
+// are then scaled by their block's scale with one FMA each and accumulated per
+// column; the four block columns of a token are added at the end. Two tokens
+// share one MMA; larger expert batches take several.
+// ---------------------------------------------------------------------------
+constexpr int kRingB = 6;                          // chunks in flight per warp
+constexpr int kSlotCode = 2 * 32 * 16;             // [2 rows][32 lanes][16 B]
+constexpr int kSlotScale = 2 * 32 * 4;             // [2 rows][32 lanes][2 scales]
+constexpr int kSlotZp = 2 * 32 * 4;                // [2 rows][32 lanes][4 zero points]
+constexpr int kSlotBytes = kSlotCode + kSlotScale + kSlotZp;
+
+__device__ __forceinline__ float scale_to_float(uint32_t bits16, int dtype) {
+  return dtype == QMOE_BF16 ? __uint_as_float(bits16 << 16) : __half2float(__ushort_as_half((uint16_t)bits16));
+}
+
+template <bool FC1, int NP>
+__global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeArgs a) {
+  const Problem& p = a.p;
+  const Workspace& ws = a.ws;
+  const int K = a.K, N = a.N;
+  const int nq = K / kChunkK;                    // K is a multiple of 128 here
+  const int rgroups = N / kRowsPerGroup;
+  const int items = ws.counters[0] * rgroups;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int ks = a.ks;
+  const int team = warp / ks, ksi = warp % ks;
+  const int teams_per_block = kWarps / ks;
+  const int team_global = blockIdx.x * teams_per_block + team;
+  const int teams_total = gridDim.x * teams_per_block;
+  const int cb = nq * ksi / ks, ce = nq * (ksi + 1) / ks;
+  const int cpi = ce - cb;                       // >= 1 (ks <= nq)
+  const int my_items = team_global < items ? (items - team_global + teams_total - 1) / teams_total : 0;
+  const int total = my_items * cpi;
+  const int64_t pitch = K / 2;                   // bytes of codes per row
+  const int nblk = K / 32;
+  const int b0 = 2 * (c & 1);                    // blocks of this lane's D columns: b0, b0 + 1
+  const bool owner = (g & 3) == c;               // supplies activations for column g
+
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* ring = smem + warp * (kRingB * kSlotBytes);
+  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+  float* red = reinterpret_cast<float*>(smem + kWarps * kRingB * kSlotBytes);  // [8 warps][NP][32][4]
+
+  // ---- issue side
+  int pf_item = team_global, pf_cc = 0;
+  const uint8_t* pq = nullptr;
+  const uint16_t* ps = nullptr;
+  const uint8_t* pz = nullptr;
+  int next_e = team_global < items ? ws.dtab[(team_global / rgroups) * kDtabInts] : 0;
+  auto issue = [&](int slot) {
+    if (pf_cc == 0) {
+      const int e = next_e;
+      const int nx = pf_item + teams_total;
+      next_e = nx < items ? ws.dtab[(nx / rgroups) * kDtabInts] : 0;
+      const int64_t row = (int64_t)e * N + (pf_item % rgroups) * kRowsPerGroup + g;
+      pq = a.q + row * pitch + (cb * kChunkK + 32 * c) / 2;
+      ps = a.s + row * nblk + cb * 4 + b0;
+      pz = a.zp ? a.zp + row * nblk + cb * 4 : nullptr;
+    }
+    const uint32_t d = ring_s + slot * kSlotBytes;
+    cp_async16(d + lane * 16, pq);
+    cp_async16(d + 512 + lane * 16, pq + 8 * pitch);
+    cp_async4(d + kSlotCode + lane * 4, ps);
+    cp_async4(d + kSlotCode + 128 + lane * 4, ps + 8 * nblk);
+    if (pz) {
+      cp_async4(d + kSlotCode + kSlotScale + lane * 4, pz);
+      cp_async4(d + kSlotCode + kSlotScale + 128 + lane * 4, pz + 8 * nblk);
+    }
+    cp_async_commit();
+    pq += kChunkK / 2;
+    ps += 4;
+    if (pz) pz += 4;
+    if (++pf_cc == cpi) { pf_cc = 0; pf_item += teams_total; }
+  };
+  for (int u = 0; u < kRingB - 1; ++u) {
+    if (u < total) issue(u);
+    else cp_async_commit();
+  }
+
+  // ---- compute side
+  int item = team_global, cc = 0;
+  float acc[NP][4];
+#pragma unroll
+  for (int tp = 0; tp < NP; ++tp)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[tp][r] = 0.f;
+  ItemMeta cur{0, 0, 0, 0};
+  const int32_t* dcur = nullptr;
+  int n_pairs = 0;
+  auto open_item = [&]() {
+    dcur = ws.dtab + (item / rgroups) * kDtabInts;
+    cur.e = dcur[0];
+    cur.begin = dcur[1];
+    cur.n_e = dcur[2];
+    n_pairs = (cur.n_e + 1) / 2;
+  };
+  if (total > 0) open_item();
+
+  int slot = 0;
+  for (int f = 0; f < total; ++f) {
+    if (f + kRingB - 1 < total) issue((slot + kRingB - 1) % kRingB);
+    else cp_async_commit();
+    cp_async_wait<kRingB - 1>();
+    const int q = cb + cc;
+    const uint8_t* sl = ring + slot * kSlotBytes;
+    const uint4 ca = *reinterpret_cast<const uint4*>(sl + lane * 16);
+    const uint4 cbv = *reinterpret_cast<const uint4*>(sl + 512 + lane * 16);
+    const uint32_t swa = *reinterpret_cast<const uint32_t*>(sl + kSlotCode + lane * 4);
+    const uint32_t swb = *reinterpret_cast<const uint32_t*>(sl + kSlotCode + 128 + lane * 4);
+    uint32_t za = 8u, zb = 8u;
+    if (a.zp) {
+      za = (*reinterpret_cast<const uint32_t*>(sl + kSlotCode + kSlotScale + lane * 4) >> (8 * c)) & 0xFFu;
+      zb = (*reinterpret_cast<const uint32_t*>(sl + kSlotCode + kSlotScale + 128 + lane * 4) >> (8 * c)) & 0xFFu;
+    }
+    slot = slot + 1 == kRingB ? 0 : slot + 1;
+
+    // A operands: codes in the FP16 mantissa, no arithmetic
+    constexpr uint32_t kMagic = 0x64006400u;
+    const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+    const uint32_t wb[4] = {cbv.x, cbv.y, cbv.z, cbv.w};
+    uint32_t pa[16], pb[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t va8 = wa[i] >> 8, vb8 = wb[i] >> 8;
+      pa[4 * i + 0] = lop3_and_or(wa[i], 0x000F000Fu, kMagic);
+      pa[4 * i + 1] = lop3_and_or(wa[i], 0x00F000F0u, kMagic);
+      pa[4 * i + 2] = lop3_and_or(va8, 0x000F000Fu, kMagic);
+      pa[4 * i + 3] = lop3_and_or(va8, 0x00F000F0u, kMagic);
+      pb[4 * i + 0] = lop3_and_or(wb[i], 0x000F000Fu, kMagic);
+      pb[4 * i + 1] = lop3_and_or(wb[i], 0x00F000F0u, kMagic);
+      pb[4 * i + 2] = lop3_and_or(vb8, 0x000F000Fu, kMagic);
+      pb[4 * i + 3] = lop3_and_or(vb8, 0x00F000F0u, kMagic);
+    }
+    // constant operands removing bias and zero point of this lane's block
+    const __half2 nea = __float2half2_rn(-(1024.0f + (float)za)), nob = __float2half2_rn(-(1024.0f + 16.0f * (float)zb));
+    const __half2 neb = __float2half2_rn(-(1024.0f + (float)zb)), noa = __float2half2_rn(-(1024.0f + 16.0f * (float)za));
+    const uint32_t ne_a = *reinterpret_cast<const uint32_t*>(&nea), ne_b = *reinterpret_cast<const uint32_t*>(&neb);
+    const uint32_t no_a = *reinterpret_cast<const uint32_t*>(&noa), no_b = *reinterpret_cast<const uint32_t*>(&nob);
+    const float s_a0 = scale_to_float(swa & 0xFFFFu, p.dtype), s_a1 = scale_to_float(swa >> 16, p.dtype);
+    const float s_b0 = scale_to_float(swb & 0xFFFFu, p.dtype), s_b1 = scale_to_float(swb >> 16, p.dtype);
+
+#pragma unroll
+    for (int tp = 0; tp < NP; ++tp) {
+      if (tp >= n_pairs) break;
+      // activations of token 2tp + g/4, block c of chunk q (owner lanes only)
+      uint32_t bw[16];
+      const int n = 2 * tp + (g >> 2);
+      if (owner && n < cur.n_e) {
+        const int64_t row = FC1 ? (int64_t)dcur[4 + n] : (int64_t)(cur.begin + n);
+        const uint4* src = reinterpret_cast<const uint4*>(a.act + row * K + q * kChunkK + 32 * c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 v = __ldg(src + j);
+          bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) bw[j] = 0u;
+      }
+      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        mma16816(t0, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
+        mma16816(t1, ne_a, ne_b, no_a, no_b, bw[2 * s], bw[2 * s + 1]);
+      }
+      acc[tp][0] = fmaf(s_a0, t0[0] + t1[0], acc[tp][0]);
+      acc[tp][1] = fmaf(s_a1, t0[1] + t1[1], acc[tp][1]);
+      acc[tp][2] = fmaf(s_b0, t0[2] + t1[2], acc[tp][2]);
+      acc[tp][3] = fmaf(s_b1, t0[3] + t1[3], acc[tp][3]);
+    }
+    if (++cc < cpi) continue;
+
+    // ---- item finished: add the K split in warp order, then the epilogue
+    if (ks > 1) {
+      float* mine = red + (size_t)warp * NP * 128;
+#pragma unroll
+      for (int tp = 0; tp < NP; ++tp)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) mine[(tp * 32 + lane) * 4 + r] = acc[tp][r];
+      asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
+      if (ksi == 0) {
+#pragma unroll
+        for (int tp = 0; tp < NP; ++tp)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            float v = acc[tp][r];
+            for (int k2 = 1; k2 < ks; ++k2) v += red[((size_t)(warp + k2) * NP * 32 + tp * 32 + lane) * 4 + r];
+            acc[tp][r] = v;
+          }
+      }
+    }
+    if (ksi == 0) {
+      const int row0 = (item % rgroups) * kRowsPerGroup;
+#pragma unroll
+      for (int tp = 0; tp < NP; ++tp) {
+        if (tp >= n_pairs) break;
+        // token sum over its four block columns: lanes c and c^1 hold two each
+        float v_lo = acc[tp][0] + acc[tp][1];
+        float v_hi = acc[tp][2] + acc[tp][3];
+        v_lo += __shfl_xor_sync(0xffffffffu, v_lo, 1);
+        v_hi += __shfl_xor_sync(0xffffffffu, v_hi, 1);
+        const int n = 2 * tp + (c >> 1);       // route slot of this lane's columns
+        if constexpr (FC1) {
+          const float up_lo = __shfl_down_sync(0xffffffffu, v_lo, 4);
+          const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
+          if ((g & 1) == 0 && (c & 1) == 0 && n < cur.n_e) {
+            const int pos = cur.begin + n;
+            const float sigma = ws.tok_scale[dcur[4 + n]];
+            const float inv = 1.0f / sigma;
+            const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+            const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
+            const float h_hi = silu(v_hi * inv) * (up_hi * inv) * sigma * sigma;
+            // fc2 reads these as activations: odd K positions carry 1/16
+            ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
+                __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
+            ws.h16[(int64_t)pos * p.I + permuted_pos(j_hi, 8)] =
+                __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * 0.0625f : h_hi));
+          }
+        } else {
+          if ((c & 1) == 0 && n < cur.n_e) {
+            const int rid = ws.sorted_route[cur.begin + n];
+            const float inv = 1.0f / ws.tok_scale[rid / p.k];
+            const float f = inv * inv * ws.topk_w[rid];
+            ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * f;
+            ws.y[(int64_t)rid * p.H + row0 + g + 8] = v_hi * f;
+          }
+        }
+      }
+    }
+    if (ks > 1) asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
+    cc = 0;
+    item += teams_total;
+#pragma unroll
+    for (int tp = 0; tp < NP; ++tp)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[tp][r] = 0.f;
+    if (f + 1 < total) open_item();
+  }
+  cp_async_wait<0>();
+}
+
+template <bool FC1, int NP>
+cudaError_t launch_int4_bs(DecodeArgs a, int active_max, cudaStream_t s) {
+  const int nq = a.K / kChunkK;
+  const int rgroups = a.N / kRowsPerGroup;
+  const int64_t items = (int64_t)active_max * rgroups;
+  const int64_t warps = (int64_t)sm_count() * kBlocksPerSm * kWarps;
+  int ks = 1;
+  while (ks < kWarps && 2 * ks <= nq && items * ks < 4 * warps) ks <<= 1;
+  a.ks = ks;
+  int64_t blocks = (items + (kWarps / ks) - 1) / (kWarps / ks);
+  const int64_t cap = (int64_t)sm_count() * kBlocksPerSm;
+  if (blocks > cap) blocks = cap;
+  const size_t smem = (size_t)kWarps * kRingB * kSlotBytes + (ks > 1 ? (size_t)kWarps * NP * 128 * sizeof(float) : 0);
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t err = cudaFuncSetAttribute(decode_int4_bs_kernel<FC1, NP>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 112 * 1024);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  decode_int4_bs_kernel<FC1, NP><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -479,8 +763,6 @@ int sm_count() {
   }
   return n;
 }
-
-constexpr int kBlocksPerSm = 2;
 
 template <int BITS, bool FC1>
 cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
@@ -516,6 +798,14 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
                         const uint8_t* zp, const Workspace& ws, cudaStream_t s) {
   const int64_t R = p.R();
   const int active_max = (int)(R < p.E ? R : p.E);
+  if (BITS == 4 && decode_int4_blockscaled(p)) {
+    DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
+                 fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
+    const int pairs = ((p.T < 8 ? (int)p.T : 8) + 1) / 2;   // <= T routes per expert
+    if (pairs <= 1) return fc1 ? launch_int4_bs<true, 1>(a, active_max, s) : launch_int4_bs<false, 1>(a, active_max, s);
+    if (pairs <= 2) return fc1 ? launch_int4_bs<true, 2>(a, active_max, s) : launch_int4_bs<false, 2>(a, active_max, s);
+    return fc1 ? launch_int4_bs<true, 4>(a, active_max, s) : launch_int4_bs<false, 4>(a, active_max, s);
+  }
   DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
   return fc1 ? launch_one<BITS, true>(a, active_max, s) : launch_one<BITS, false>(a, active_max, s);

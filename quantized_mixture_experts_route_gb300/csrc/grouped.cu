@@ -382,20 +382,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8, e * N + n0);
       }
       uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
-      for (int u = lane; u < C::UNITS; u += 32) {
+      // all loads first (independent, no branches), then convert and store
+      constexpr int PER_LANE = C::UNITS / 32;
+      uint16_t sv[PER_LANE];
+      uint8_t zv[PER_LANE];
+#pragma unroll
+      for (int q = 0; q < PER_LANE; ++q) {
+        const int u = lane + 32 * q;
         const int r = u / C::UNITS_PER_ROW, j = u % C::UNITS_PER_ROW;
-        const int64_t wr = wrow_base + r;
-        uint32_t v = 0u;                       // zero scale outside the weight array
-        if (wr < wrow_end) {
-          const int b = (k0 + 32 * j) / p.block;
-          const uint16_t sb = __ldg(g.scales + wr * nblk + b);
-          const uint16_t sh = p.dtype == QMOE_BF16
-                                  ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sb << 16)))
-                                  : sb;
-          const uint32_t z = g.zp ? (uint32_t)__ldg(g.zp + wr * nblk + b) : (1u << (BITS - 1));
-          v = (uint32_t)sh | (z << 16);
-        }
-        st[u] = v;
+        const int64_t wr = min(wrow_base + r, wrow_end - 1);   // rows past the array: masked below
+        const int64_t idx = wr * nblk + (k0 + 32 * j) / p.block;
+        sv[q] = __ldg(g.scales + idx);
+        zv[q] = g.zp ? __ldg(g.zp + idx) : (uint8_t)(1u << (BITS - 1));
+      }
+#pragma unroll
+      for (int q = 0; q < PER_LANE; ++q) {
+        const int u = lane + 32 * q;
+        const int r = u / C::UNITS_PER_ROW;
+        const uint16_t sh = p.dtype == QMOE_BF16
+                                ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sv[q] << 16)))
+                                : sv[q];
+        st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
       }
       mbar_arrive(bar_full(s));
     }

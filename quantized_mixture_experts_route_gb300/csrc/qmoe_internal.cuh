@@ -59,11 +59,22 @@ size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* w
 // the dequantisers produce FP16 pairs straight from the packed words.
 __host__ __device__ inline int perm_group(int bits) { return bits == 4 ? 8 : 16; }
 
+// The INT4 decode kernel with per-block scales applied after the MMA (block 32,
+// K a multiple of 128 for both matmuls). It reads activations whose odd K
+// positions are pre-divided by 16 (see decode.cu).
+__host__ __device__ inline bool decode_int4_blockscaled(const Problem& p) {
+  return p.path == QMOE_PATH_DECODE && p.bits == 4 && p.block == 32 && p.H % 128 == 0 && p.I % 128 == 0;
+}
+
+// How the routing kernel writes x16: not at all, plain, or with the odd K
+// positions divided by 16 (for decode_int4_blockscaled).
+enum X16Mode { kX16None = 0, kX16Plain = 1, kX16OddSixteenth = 2 };
+
 // ---------------------------------------------------------------------------
 // launchers (return the launch error, never synchronise)
 // ---------------------------------------------------------------------------
 cudaError_t launch_route(const Problem& p, const void* x, const void* logits, const Workspace& ws,
-                         bool want_x16, cudaStream_t s);
+                         int x16_mode, cudaStream_t s);
 cudaError_t launch_group(const Problem& p, const Workspace& ws, bool want_tiles, cudaStream_t s);
 cudaError_t launch_gather(const Problem& p, const Workspace& ws, cudaStream_t s);
 // One expert matmul stage: fc1 (with SwiGLU) when fc1 is true, else fc2.

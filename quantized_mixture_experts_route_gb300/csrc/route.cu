@@ -49,7 +49,7 @@ __device__ __forceinline__ float warp_max_f(float v) {
 template <int PER_LANE>
 __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
                             const uint16_t* __restrict__ logits, const Workspace& ws, int64_t t,
-                            bool want_x16) {
+                            int x16_mode) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   const uint16_t* lrow = logits + t * E;
@@ -87,7 +87,7 @@ __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
     ws.topk_idx[t * k + lane] = my_e;
     ws.topk_w[t * k + lane] = expf(my_l - l0) / denom;
   }
-  if (!want_x16) return;
+  if (x16_mode == kX16None) return;
 
   // Activations: scale by a power of two so that max|x_t| lies in [1, 2), round
   // to FP16, and store in the K-order permutation of the dequantisers.
@@ -121,10 +121,12 @@ __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
     const uint4 b = *reinterpret_cast<const uint4*>(xrow + base + 8);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint16_t in[16], out[16];
+    // odd K positions carry 1/16 in the block-scaled INT4 decode layout
+    const float odd = x16_mode == kX16OddSixteenth ? sigma * 0.0625f : sigma;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       in[2 * i] = __half_as_ushort(__float2half_rn(half_bits_to_float((uint16_t)(w[i] & 0xFFFF), p.dtype) * sigma));
-      in[2 * i + 1] = __half_as_ushort(__float2half_rn(half_bits_to_float((uint16_t)(w[i] >> 16), p.dtype) * sigma));
+      in[2 * i + 1] = __half_as_ushort(__float2half_rn(half_bits_to_float((uint16_t)(w[i] >> 16), p.dtype) * odd));
     }
     if (G == 8) {
 #pragma unroll
@@ -158,11 +160,11 @@ __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
 template <int PER_LANE>
 __global__ void __launch_bounds__(256) route_kernel(Problem p, const uint16_t* __restrict__ x,
                                                     const uint16_t* __restrict__ logits,
-                                                    Workspace ws, int want_x16) {
+                                                    Workspace ws, int x16_mode) {
   const int warps = blockDim.x >> 5;
   for (int64_t t = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); t < p.T;
        t += (int64_t)gridDim.x * warps)
-    route_token<PER_LANE>(p, x, logits, ws, t, want_x16 != 0);
+    route_token<PER_LANE>(p, x, logits, ws, t, x16_mode);
 }
 
 // ---------------------------------------------------------------------------
@@ -318,14 +320,14 @@ __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(Problem p,
 template <int PER_LANE>
 __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
     Problem p, const uint16_t* __restrict__ x, const uint16_t* __restrict__ logits, Workspace ws,
-    int want_x16, int want_tiles) {
+    int x16_mode, int want_tiles) {
   extern __shared__ int smem[];
   int* hist = smem;                  // [E]
   int* warp_cnt = smem + p.E;        // [16][E]
   __shared__ int sh[32];
   const int warps = blockDim.x >> 5;
   for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps)
-    route_token<PER_LANE>(p, x, logits, ws, t, want_x16 != 0);
+    route_token<PER_LANE>(p, x, logits, ws, t, x16_mode);
   for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int64_t R = p.R();
@@ -380,7 +382,7 @@ int num_sms() {
 }  // namespace
 
 cudaError_t launch_route(const Problem& p, const void* x, const void* logits, const Workspace& ws,
-                         bool want_x16, cudaStream_t s) {
+                         int x16_mode, cudaStream_t s) {
   const int64_t R = p.R();
   const bool small = R <= kPermuteChunk;
   const bool want_tiles = p.path == QMOE_PATH_GROUPED;
@@ -389,9 +391,9 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* logits, co
   if (small) {
     const size_t smem = sizeof(int) * (size_t)p.E * (1 + kGroupThreads / 32);
     if (p.E <= 128)
-      route_group_small_kernel<4><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, want_x16, want_tiles);
+      route_group_small_kernel<4><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, x16_mode, want_tiles);
     else
-      route_group_small_kernel<16><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, want_x16, want_tiles);
+      route_group_small_kernel<16><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, x16_mode, want_tiles);
     return cudaGetLastError();
   }
   const int warps = 8;
@@ -399,9 +401,9 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* logits, co
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
   if (p.E <= 128)
-    route_kernel<4><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, want_x16);
+    route_kernel<4><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, x16_mode);
   else
-    route_kernel<16><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, want_x16);
+    route_kernel<16><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, x16_mode);
   return cudaGetLastError();
 }
 
