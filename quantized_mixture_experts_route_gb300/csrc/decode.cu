@@ -497,11 +497,8 @@ constexpr int kSlotScale = 2 * 32 * 4;             // [2 rows][32 lanes][2 scale
 constexpr int kSlotZp = 2 * 32 * 4;                // [2 rows][32 lanes][4 zero points]
 constexpr int kSlotBytes = kSlotCode + kSlotScale + kSlotZp;
 
-__device__ __forceinline__ float scale_to_float(uint32_t bits16, int dtype) {
-  return dtype == QMOE_BF16 ? __uint_as_float(bits16 << 16) : __half2float(__ushort_as_half((uint16_t)bits16));
-}
 
-template <bool FC1, int NP>
+template <bool FC1, int NP, bool BF16S, bool HAS_ZP>
 __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeArgs a) {
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
@@ -545,27 +542,32 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
       const int64_t row = (int64_t)e * N + (pf_item % rgroups) * kRowsPerGroup + g;
       pq = a.q + row * pitch + (cb * kChunkK + 32 * c) / 2;
       ps = a.s + row * nblk + cb * 4 + b0;
-      pz = a.zp ? a.zp + row * nblk + cb * 4 : nullptr;
+      if constexpr (HAS_ZP) pz = a.zp + row * nblk + cb * 4;
     }
     const uint32_t d = ring_s + slot * kSlotBytes;
     cp_async16(d + lane * 16, pq);
     cp_async16(d + 512 + lane * 16, pq + 8 * pitch);
     cp_async4(d + kSlotCode + lane * 4, ps);
     cp_async4(d + kSlotCode + 128 + lane * 4, ps + 8 * nblk);
-    if (pz) {
+    if constexpr (HAS_ZP) {
       cp_async4(d + kSlotCode + kSlotScale + lane * 4, pz);
       cp_async4(d + kSlotCode + kSlotScale + 128 + lane * 4, pz + 8 * nblk);
+      pz += 4;
     }
     cp_async_commit();
     pq += kChunkK / 2;
     ps += 4;
-    if (pz) pz += 4;
     if (++pf_cc == cpi) { pf_cc = 0; pf_item += teams_total; }
   };
   for (int u = 0; u < kRingB - 1; ++u) {
     if (u < total) issue(u);
     else cp_async_commit();
   }
+
+  // constant operands removing the bias and the default zero point 8
+  const __half2 ne_d = __float2half2_rn(-(1024.0f + 8.0f)), no_d = __float2half2_rn(-(1024.0f + 128.0f));
+  const uint32_t ne_def = *reinterpret_cast<const uint32_t*>(&ne_d);
+  const uint32_t no_def = *reinterpret_cast<const uint32_t*>(&no_d);
 
   // ---- compute side
   int item = team_global, cc = 0;
@@ -574,33 +576,49 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
   for (int tp = 0; tp < NP; ++tp)
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[tp][r] = 0.f;
-  ItemMeta cur{0, 0, 0, 0};
+  int begin = 0, n_e = 0, n_pairs = 0;
   const int32_t* dcur = nullptr;
-  int n_pairs = 0;
+  int bsrc[NP];                                  // owner lanes: element offset of their token's row, or -1
   auto open_item = [&]() {
     dcur = ws.dtab + (item / rgroups) * kDtabInts;
-    cur.e = dcur[0];
-    cur.begin = dcur[1];
-    cur.n_e = dcur[2];
-    n_pairs = (cur.n_e + 1) / 2;
+    begin = dcur[1];
+    n_e = dcur[2];
+    n_pairs = (n_e + 1) / 2;
+#pragma unroll
+    for (int tp = 0; tp < NP; ++tp) {
+      const int n = 2 * tp + (g >> 2);
+      bsrc[tp] = -1;
+      if (owner && n < n_e) {
+        const int row = FC1 ? dcur[4 + n] : begin + n;
+        bsrc[tp] = row * K + cb * kChunkK + 32 * c;
+      }
+    }
   };
   if (total > 0) open_item();
+  uint32_t bw[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) bw[j] = 0u;       // non-owner lanes keep zeros for good
 
   int slot = 0;
   for (int f = 0; f < total; ++f) {
     if (f + kRingB - 1 < total) issue((slot + kRingB - 1) % kRingB);
     else cp_async_commit();
     cp_async_wait<kRingB - 1>();
-    const int q = cb + cc;
     const uint8_t* sl = ring + slot * kSlotBytes;
     const uint4 ca = *reinterpret_cast<const uint4*>(sl + lane * 16);
     const uint4 cbv = *reinterpret_cast<const uint4*>(sl + 512 + lane * 16);
     const uint32_t swa = *reinterpret_cast<const uint32_t*>(sl + kSlotCode + lane * 4);
     const uint32_t swb = *reinterpret_cast<const uint32_t*>(sl + kSlotCode + 128 + lane * 4);
-    uint32_t za = 8u, zb = 8u;
-    if (a.zp) {
-      za = (*reinterpret_cast<const uint32_t*>(sl + kSlotCode + kSlotScale + lane * 4) >> (8 * c)) & 0xFFu;
-      zb = (*reinterpret_cast<const uint32_t*>(sl + kSlotCode + kSlotScale + 128 + lane * 4) >> (8 * c)) & 0xFFu;
+    uint32_t ne_a = ne_def, ne_b = ne_def, no_a = no_def, no_b = no_def;
+    if constexpr (HAS_ZP) {
+      const uint32_t za = (*reinterpret_cast<const uint32_t*>(sl + kSlotCode + kSlotScale + lane * 4) >> (8 * c)) & 0xFFu;
+      const uint32_t zb = (*reinterpret_cast<const uint32_t*>(sl + kSlotCode + kSlotScale + 128 + lane * 4) >> (8 * c)) & 0xFFu;
+      const __half2 h1 = __float2half2_rn(-(1024.0f + (float)za)), h2 = __float2half2_rn(-(1024.0f + 16.0f * (float)za));
+      const __half2 h3 = __float2half2_rn(-(1024.0f + (float)zb)), h4 = __float2half2_rn(-(1024.0f + 16.0f * (float)zb));
+      ne_a = *reinterpret_cast<const uint32_t*>(&h1);
+      no_a = *reinterpret_cast<const uint32_t*>(&h2);
+      ne_b = *reinterpret_cast<const uint32_t*>(&h3);
+      no_b = *reinterpret_cast<const uint32_t*>(&h4);
     }
     slot = slot + 1 == kRingB ? 0 : slot + 1;
 
@@ -621,37 +639,38 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
       pb[4 * i + 2] = lop3_and_or(vb8, 0x000F000Fu, kMagic);
       pb[4 * i + 3] = lop3_and_or(vb8, 0x00F000F0u, kMagic);
     }
-    // constant operands removing bias and zero point of this lane's block
-    const __half2 nea = __float2half2_rn(-(1024.0f + (float)za)), nob = __float2half2_rn(-(1024.0f + 16.0f * (float)zb));
-    const __half2 neb = __float2half2_rn(-(1024.0f + (float)zb)), noa = __float2half2_rn(-(1024.0f + 16.0f * (float)za));
-    const uint32_t ne_a = *reinterpret_cast<const uint32_t*>(&nea), ne_b = *reinterpret_cast<const uint32_t*>(&neb);
-    const uint32_t no_a = *reinterpret_cast<const uint32_t*>(&noa), no_b = *reinterpret_cast<const uint32_t*>(&nob);
-    const float s_a0 = scale_to_float(swa & 0xFFFFu, p.dtype), s_a1 = scale_to_float(swa >> 16, p.dtype);
-    const float s_b0 = scale_to_float(swb & 0xFFFFu, p.dtype), s_b1 = scale_to_float(swb >> 16, p.dtype);
+    float s_a0, s_a1, s_b0, s_b1;
+    if constexpr (BF16S) {
+      s_a0 = __uint_as_float(swa << 16); s_a1 = __uint_as_float(swa & 0xFFFF0000u);
+      s_b0 = __uint_as_float(swb << 16); s_b1 = __uint_as_float(swb & 0xFFFF0000u);
+    } else {
+      s_a0 = __half2float(__ushort_as_half((uint16_t)(swa & 0xFFFFu))); s_a1 = __half2float(__ushort_as_half((uint16_t)(swa >> 16)));
+      s_b0 = __half2float(__ushort_as_half((uint16_t)(swb & 0xFFFFu))); s_b1 = __half2float(__ushort_as_half((uint16_t)(swb >> 16)));
+    }
+    const int coff = cc * kChunkK;
 
 #pragma unroll
     for (int tp = 0; tp < NP; ++tp) {
       if (tp >= n_pairs) break;
-      // activations of token 2tp + g/4, block c of chunk q (owner lanes only)
-      uint32_t bw[16];
-      const int n = 2 * tp + (g >> 2);
-      if (owner && n < cur.n_e) {
-        const int64_t row = FC1 ? (int64_t)dcur[4 + n] : (int64_t)(cur.begin + n);
-        const uint4* src = reinterpret_cast<const uint4*>(a.act + row * K + q * kChunkK + 32 * c);
+      if (bsrc[tp] >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.act + bsrc[tp] + coff);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint4 v = __ldg(src + j);
           bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
         }
-      } else {
+      } else if (owner) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) bw[j] = 0u;
       }
+      // two chains (even / odd steps), each with the raw and the bias MMA
       float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
+      for (int s = 0; s < 8; s += 2) {
         mma16816(t0, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
-        mma16816(t1, ne_a, ne_b, no_a, no_b, bw[2 * s], bw[2 * s + 1]);
+        mma16816(t1, pa[2 * s + 2], pb[2 * s + 2], pa[2 * s + 3], pb[2 * s + 3], bw[2 * s + 2], bw[2 * s + 3]);
+        mma16816(t0, ne_a, ne_b, no_a, no_b, bw[2 * s], bw[2 * s + 1]);
+        mma16816(t1, ne_a, ne_b, no_a, no_b, bw[2 * s + 2], bw[2 * s + 3]);
       }
       acc[tp][0] = fmaf(s_a0, t0[0] + t1[0], acc[tp][0]);
       acc[tp][1] = fmaf(s_a1, t0[1] + t1[1], acc[tp][1]);
@@ -666,7 +685,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
 #pragma unroll
       for (int tp = 0; tp < NP; ++tp)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) mine[(tp * 32 + lane) * 4 + r] = acc[tp][r];
+        for (int r = 0; r < 4; ++r) mine[(tp * 4 + r) * 32 + lane] = acc[tp][r];
       asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
       if (ksi == 0) {
 #pragma unroll
@@ -674,7 +693,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             float v = acc[tp][r];
-            for (int k2 = 1; k2 < ks; ++k2) v += red[((size_t)(warp + k2) * NP * 32 + tp * 32 + lane) * 4 + r];
+            for (int k2 = 1; k2 < ks; ++k2) v += red[(size_t)(warp + k2) * NP * 128 + (tp * 4 + r) * 32 + lane];
             acc[tp][r] = v;
           }
       }
@@ -693,8 +712,8 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
         if constexpr (FC1) {
           const float up_lo = __shfl_down_sync(0xffffffffu, v_lo, 4);
           const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
-          if ((g & 1) == 0 && (c & 1) == 0 && n < cur.n_e) {
-            const int pos = cur.begin + n;
+          if ((g & 1) == 0 && (c & 1) == 0 && n < n_e) {
+            const int pos = begin + n;
             const float sigma = ws.tok_scale[dcur[4 + n]];
             const float inv = 1.0f / sigma;
             const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
@@ -707,8 +726,8 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
                 __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * 0.0625f : h_hi));
           }
         } else {
-          if ((c & 1) == 0 && n < cur.n_e) {
-            const int rid = ws.sorted_route[cur.begin + n];
+          if ((c & 1) == 0 && n < n_e) {
+            const int rid = ws.sorted_route[begin + n];
             const float inv = 1.0f / ws.tok_scale[rid / p.k];
             const float f = inv * inv * ws.topk_w[rid];
             ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * f;
@@ -729,6 +748,19 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
   cp_async_wait<0>();
 }
 
+template <bool FC1, int NP, bool BF16S, bool HAS_ZP>
+cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t err = cudaFuncSetAttribute(decode_int4_bs_kernel<FC1, NP, BF16S, HAS_ZP>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 112 * 1024);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  decode_int4_bs_kernel<FC1, NP, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <bool FC1, int NP>
 cudaError_t launch_int4_bs(DecodeArgs a, int active_max, cudaStream_t s) {
   const int nq = a.K / kChunkK;
@@ -742,15 +774,11 @@ cudaError_t launch_int4_bs(DecodeArgs a, int active_max, cudaStream_t s) {
   const int64_t cap = (int64_t)sm_count() * kBlocksPerSm;
   if (blocks > cap) blocks = cap;
   const size_t smem = (size_t)kWarps * kRingB * kSlotBytes + (ks > 1 ? (size_t)kWarps * NP * 128 * sizeof(float) : 0);
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_int4_bs_kernel<FC1, NP>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 112 * 1024);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
-  decode_int4_bs_kernel<FC1, NP><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
-  return cudaGetLastError();
+  const bool bf16 = a.p.dtype == QMOE_BF16, zp = a.zp != nullptr;
+  if (bf16) return zp ? launch_int4_bs_t<FC1, NP, true, true>(a, blocks, smem, s)
+                      : launch_int4_bs_t<FC1, NP, true, false>(a, blocks, smem, s);
+  return zp ? launch_int4_bs_t<FC1, NP, false, true>(a, blocks, smem, s)
+            : launch_int4_bs_t<FC1, NP, false, false>(a, blocks, smem, s);
 }
 
 int sm_count() {
