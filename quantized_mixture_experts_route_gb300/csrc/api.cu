@@ -86,7 +86,7 @@ size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* w
   w.tiles = static_cast<int32_t*>(take(sizeof(int32_t) * 2 * w.max_tiles));
   w.nchunks = (R + kPermuteChunk - 1) / kPermuteChunk;
   w.chunk_hist = static_cast<int32_t*>(take(sizeof(int32_t) * w.nchunks * p.E));
-  w.dtab = static_cast<int32_t*>(take(sizeof(int32_t) * kDtabInts * p.E));
+  w.dtab = static_cast<int32_t*>(take(sizeof(int32_t) * kDtabInts * kDtabMax));
   w.x16s = grouped ? static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.H)) : nullptr;
   w.h16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.I));
   w.y = static_cast<float*>(take(sizeof(float) * R * p.H));

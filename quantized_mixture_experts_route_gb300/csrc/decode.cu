@@ -254,11 +254,10 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   auto meta_of = [&](int it) {
     ItemMeta m{0, 0, 0, 0};
     if (it < items) {
-      const int32_t* d = ws.dtab + (it / rgroups) * kDtabInts;
-      m.e = d[0];
-      m.begin = d[1];
-      m.n_e = d[2];
-      m.tok = d[4 + g];
+      m.e = ws.active[it / rgroups];
+      m.begin = ws.offsets[m.e];
+      m.n_e = ws.offsets[m.e + 1] - m.begin;
+      m.tok = g < m.n_e ? ws.sorted_route[m.begin + g] / p.k : 0;
     }
     return m;
   };
@@ -427,12 +426,11 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
           if ((g & 1) == 0) {
             const int G = perm_group(p.bits);
             const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
-            const int32_t* d = ws.dtab + (item / rgroups) * kDtabInts;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
               const int n = (r & 1) ? n1 : n0;
               if (n < n_e) {
-                const float sigma = ws.tok_scale[d[4 + n]];
+                const float sigma = ws.tok_scale[ws.sorted_route[begin + n] / p.k];
                 const float inv = 1.0f / sigma;
                 const float h = silu(tot[r] * inv) * (up[r] * inv) * sigma * sigma;
                 const int j = (r & 2) ? j_hi : j_lo;
@@ -491,21 +489,28 @@ constexpr int kBlocksPerSm = 2;
 // column; the four block columns of a token are added at the end. Two tokens
 // share one MMA; larger expert batches take several.
 // ---------------------------------------------------------------------------
-constexpr int kRingB = 6;                          // chunks in flight per warp
+constexpr int kRingB = 4;                          // chunks in flight per warp
 constexpr int kSlotCode = 2 * 32 * 16;             // [2 rows][32 lanes][16 B]
 constexpr int kSlotScale = 2 * 32 * 4;             // [2 rows][32 lanes][2 scales]
 constexpr int kSlotZp = 2 * 32 * 4;                // [2 rows][32 lanes][4 zero points]
 constexpr int kSlotBytes = kSlotCode + kSlotScale + kSlotZp;
 
 
-template <bool FC1, int NP, bool BF16S, bool HAS_ZP>
-__global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeArgs a) {
+constexpr int kBlocksPerSmB = 3;
+
+// Work unit: (decode-table entry = active expert and a pair of its routes,
+// 16-row group). One accumulator set per unit. An expert with more than two
+// routes has several entries; their units read the same weight rows, which the
+// round-robin order hands to neighbouring teams in the same round, so the
+// repeated reads are served by L2.
+template <bool FC1, bool BF16S, bool HAS_ZP>
+__global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_kernel(DecodeArgs a) {
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
   const int K = a.K, N = a.N;
   const int nq = K / kChunkK;                    // K is a multiple of 128 here
   const int rgroups = N / kRowsPerGroup;
-  const int items = ws.counters[0] * rgroups;
+  const int items = ws.counters[3] * rgroups;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -526,7 +531,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* ring = smem + warp * (kRingB * kSlotBytes);
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
-  float* red = reinterpret_cast<float*>(smem + kWarps * kRingB * kSlotBytes);  // [8 warps][NP][32][4]
+  float* red = reinterpret_cast<float*>(smem + kWarps * kRingB * kSlotBytes);  // [2][8 warps][4][32]
 
   // ---- issue side
   int pf_item = team_global, pf_cc = 0;
@@ -571,35 +576,23 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
 
   // ---- compute side
   int item = team_global, cc = 0;
-  float acc[NP][4];
-#pragma unroll
-  for (int tp = 0; tp < NP; ++tp)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) acc[tp][r] = 0.f;
-  int begin = 0, n_e = 0, n_pairs = 0;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int pos0 = 0, cnt = 0, boff = -1;
   const int32_t* dcur = nullptr;
-  int bsrc[NP];                                  // owner lanes: element offset of their token's row, or -1
   auto open_item = [&]() {
     dcur = ws.dtab + (item / rgroups) * kDtabInts;
-    begin = dcur[1];
-    n_e = dcur[2];
-    n_pairs = (n_e + 1) / 2;
-#pragma unroll
-    for (int tp = 0; tp < NP; ++tp) {
-      const int n = 2 * tp + (g >> 2);
-      bsrc[tp] = -1;
-      if (owner && n < n_e) {
-        const int row = FC1 ? dcur[4 + n] : begin + n;
-        bsrc[tp] = row * K + cb * kChunkK + 32 * c;
-      }
-    }
+    pos0 = dcur[1];
+    cnt = dcur[2];
+    const int n = g >> 2;                        // this lane's column's route within the pair
+    boff = -1;
+    if (owner && n < cnt) boff = (FC1 ? dcur[4 + n] : pos0 + n) * K + cb * kChunkK + 32 * c;
   };
   if (total > 0) open_item();
   uint32_t bw[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) bw[j] = 0u;       // non-owner lanes keep zeros for good
 
-  int slot = 0;
+  int slot = 0, item_parity = 0;
   for (int f = 0; f < total; ++f) {
     if (f + kRingB - 1 < total) issue((slot + kRingB - 1) % kRingB);
     else cp_async_commit();
@@ -621,23 +614,13 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
       no_b = *reinterpret_cast<const uint32_t*>(&h4);
     }
     slot = slot + 1 == kRingB ? 0 : slot + 1;
-
-    // A operands: codes in the FP16 mantissa, no arithmetic
-    constexpr uint32_t kMagic = 0x64006400u;
-    const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-    const uint32_t wb[4] = {cbv.x, cbv.y, cbv.z, cbv.w};
-    uint32_t pa[16], pb[16];
+    if (boff >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.act + boff + cc * kChunkK);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t va8 = wa[i] >> 8, vb8 = wb[i] >> 8;
-      pa[4 * i + 0] = lop3_and_or(wa[i], 0x000F000Fu, kMagic);
-      pa[4 * i + 1] = lop3_and_or(wa[i], 0x00F000F0u, kMagic);
-      pa[4 * i + 2] = lop3_and_or(va8, 0x000F000Fu, kMagic);
-      pa[4 * i + 3] = lop3_and_or(va8, 0x00F000F0u, kMagic);
-      pb[4 * i + 0] = lop3_and_or(wb[i], 0x000F000Fu, kMagic);
-      pb[4 * i + 1] = lop3_and_or(wb[i], 0x00F000F0u, kMagic);
-      pb[4 * i + 2] = lop3_and_or(vb8, 0x000F000Fu, kMagic);
-      pb[4 * i + 3] = lop3_and_or(vb8, 0x00F000F0u, kMagic);
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = __ldg(src + j);
+        bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
+      }
     }
     float s_a0, s_a1, s_b0, s_b1;
     if constexpr (BF16S) {
@@ -647,138 +630,124 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_int4_bs_kernel(DecodeAr
       s_a0 = __half2float(__ushort_as_half((uint16_t)(swa & 0xFFFFu))); s_a1 = __half2float(__ushort_as_half((uint16_t)(swa >> 16)));
       s_b0 = __half2float(__ushort_as_half((uint16_t)(swb & 0xFFFFu))); s_b1 = __half2float(__ushort_as_half((uint16_t)(swb >> 16)));
     }
-    const int coff = cc * kChunkK;
-
+    // Two chains (even / odd steps), each with the raw and the bias MMA. The A
+    // operands are the codes placed in the FP16 mantissa, cut per step: step
+    // 2i uses nibbles 0,4 / 1,5 of word i, step 2i+1 nibbles 2,6 / 3,7.
+    constexpr uint32_t kMagic = 0x64006400u;
+    const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+    const uint32_t wb[4] = {cbv.x, cbv.y, cbv.z, cbv.w};
+    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int tp = 0; tp < NP; ++tp) {
-      if (tp >= n_pairs) break;
-      if (bsrc[tp] >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.act + bsrc[tp] + coff);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 v = __ldg(src + j);
-          bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
-        }
-      } else if (owner) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) bw[j] = 0u;
-      }
-      // two chains (even / odd steps), each with the raw and the bias MMA
-      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int s = 0; s < 8; s += 2) {
-        mma16816(t0, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
-        mma16816(t1, pa[2 * s + 2], pb[2 * s + 2], pa[2 * s + 3], pb[2 * s + 3], bw[2 * s + 2], bw[2 * s + 3]);
-        mma16816(t0, ne_a, ne_b, no_a, no_b, bw[2 * s], bw[2 * s + 1]);
-        mma16816(t1, ne_a, ne_b, no_a, no_b, bw[2 * s + 2], bw[2 * s + 3]);
-      }
-      acc[tp][0] = fmaf(s_a0, t0[0] + t1[0], acc[tp][0]);
-      acc[tp][1] = fmaf(s_a1, t0[1] + t1[1], acc[tp][1]);
-      acc[tp][2] = fmaf(s_b0, t0[2] + t1[2], acc[tp][2]);
-      acc[tp][3] = fmaf(s_b1, t0[3] + t1[3], acc[tp][3]);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t va8 = wa[i] >> 8, vb8 = wb[i] >> 8;
+      mma16816(t0, lop3_and_or(wa[i], 0x000F000Fu, kMagic), lop3_and_or(wb[i], 0x000F000Fu, kMagic),
+               lop3_and_or(wa[i], 0x00F000F0u, kMagic), lop3_and_or(wb[i], 0x00F000F0u, kMagic),
+               bw[4 * i], bw[4 * i + 1]);
+      mma16816(t1, lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
+               lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
+               bw[4 * i + 2], bw[4 * i + 3]);
+      mma16816(t0, ne_a, ne_b, no_a, no_b, bw[4 * i], bw[4 * i + 1]);
+      mma16816(t1, ne_a, ne_b, no_a, no_b, bw[4 * i + 2], bw[4 * i + 3]);
     }
+    acc[0] = fmaf(s_a0, t0[0] + t1[0], acc[0]);
+    acc[1] = fmaf(s_a1, t0[1] + t1[1], acc[1]);
+    acc[2] = fmaf(s_b0, t0[2] + t1[2], acc[2]);
+    acc[3] = fmaf(s_b1, t0[3] + t1[3], acc[3]);
     if (++cc < cpi) continue;
 
-    // ---- item finished: add the K split in warp order, then the epilogue
+    // ---- unit finished: add the K split in warp order, then the epilogue
     if (ks > 1) {
-      float* mine = red + (size_t)warp * NP * 128;
+      // double-buffered by unit parity: one barrier per unit suffices, since a
+      // buffer is rewritten only after the next unit's barrier
+      float* buf = red + (size_t)(item_parity * kWarps) * 128;
+      float* mine = buf + (size_t)warp * 128;
 #pragma unroll
-      for (int tp = 0; tp < NP; ++tp)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) mine[(tp * 4 + r) * 32 + lane] = acc[tp][r];
+      for (int r = 0; r < 4; ++r) mine[r * 32 + lane] = acc[r];
       asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
       if (ksi == 0) {
 #pragma unroll
-        for (int tp = 0; tp < NP; ++tp)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            float v = acc[tp][r];
-            for (int k2 = 1; k2 < ks; ++k2) v += red[(size_t)(warp + k2) * NP * 128 + (tp * 4 + r) * 32 + lane];
-            acc[tp][r] = v;
-          }
+        for (int r = 0; r < 4; ++r) {
+          float v = acc[r];
+          for (int k2 = 1; k2 < ks; ++k2) v += buf[(size_t)(warp + k2) * 128 + r * 32 + lane];
+          acc[r] = v;
+        }
       }
+      item_parity ^= 1;
     }
     if (ksi == 0) {
       const int row0 = (item % rgroups) * kRowsPerGroup;
-#pragma unroll
-      for (int tp = 0; tp < NP; ++tp) {
-        if (tp >= n_pairs) break;
-        // token sum over its four block columns: lanes c and c^1 hold two each
-        float v_lo = acc[tp][0] + acc[tp][1];
-        float v_hi = acc[tp][2] + acc[tp][3];
-        v_lo += __shfl_xor_sync(0xffffffffu, v_lo, 1);
-        v_hi += __shfl_xor_sync(0xffffffffu, v_hi, 1);
-        const int n = 2 * tp + (c >> 1);       // route slot of this lane's columns
-        if constexpr (FC1) {
-          const float up_lo = __shfl_down_sync(0xffffffffu, v_lo, 4);
-          const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
-          if ((g & 1) == 0 && (c & 1) == 0 && n < n_e) {
-            const int pos = begin + n;
-            const float sigma = ws.tok_scale[dcur[4 + n]];
-            const float inv = 1.0f / sigma;
-            const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
-            const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
-            const float h_hi = silu(v_hi * inv) * (up_hi * inv) * sigma * sigma;
-            // fc2 reads these as activations: odd K positions carry 1/16
-            ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
-                __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
-            ws.h16[(int64_t)pos * p.I + permuted_pos(j_hi, 8)] =
-                __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * 0.0625f : h_hi));
-          }
-        } else {
-          if ((c & 1) == 0 && n < n_e) {
-            const int rid = ws.sorted_route[begin + n];
-            const float inv = 1.0f / ws.tok_scale[rid / p.k];
-            const float f = inv * inv * ws.topk_w[rid];
-            ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * f;
-            ws.y[(int64_t)rid * p.H + row0 + g + 8] = v_hi * f;
-          }
+      // route sum over its four block columns: lanes c and c^1 hold two each
+      float v_lo = acc[0] + acc[1];
+      float v_hi = acc[2] + acc[3];
+      v_lo += __shfl_xor_sync(0xffffffffu, v_lo, 1);
+      v_hi += __shfl_xor_sync(0xffffffffu, v_hi, 1);
+      const int n = c >> 1;                      // route within the pair of this lane's columns
+      if constexpr (FC1) {
+        const float up_lo = __shfl_down_sync(0xffffffffu, v_lo, 4);
+        const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
+        if ((g & 1) == 0 && (c & 1) == 0 && n < cnt) {
+          const int pos = pos0 + n;
+          const float sigma = ws.tok_scale[dcur[4 + n]];
+          const float inv = 1.0f / sigma;
+          const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+          const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
+          const float h_hi = silu(v_hi * inv) * (up_hi * inv) * sigma * sigma;
+          // fc2 reads these as activations: odd K positions carry 1/16
+          ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
+              __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
+          ws.h16[(int64_t)pos * p.I + permuted_pos(j_hi, 8)] =
+              __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * 0.0625f : h_hi));
+        }
+      } else {
+        if ((c & 1) == 0 && n < cnt) {
+          const int rid = ws.sorted_route[pos0 + n];
+          const float inv = 1.0f / ws.tok_scale[rid / p.k];
+          const float fct = inv * inv * ws.topk_w[rid];
+          ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * fct;
+          ws.y[(int64_t)rid * p.H + row0 + g + 8] = v_hi * fct;
         }
       }
     }
-    if (ks > 1) asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
     cc = 0;
     item += teams_total;
 #pragma unroll
-    for (int tp = 0; tp < NP; ++tp)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[tp][r] = 0.f;
+    for (int r = 0; r < 4; ++r) acc[r] = 0.f;
     if (f + 1 < total) open_item();
   }
   cp_async_wait<0>();
 }
 
-template <bool FC1, int NP, bool BF16S, bool HAS_ZP>
+template <bool FC1, bool BF16S, bool HAS_ZP>
 cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_int4_bs_kernel<FC1, NP, BF16S, HAS_ZP>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 112 * 1024);
+    const cudaError_t err = cudaFuncSetAttribute(decode_int4_bs_kernel<FC1, BF16S, HAS_ZP>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 75 * 1024);
     if (err != cudaSuccess) return err;
     attr = true;
   }
-  decode_int4_bs_kernel<FC1, NP, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
+  decode_int4_bs_kernel<FC1, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-template <bool FC1, int NP>
-cudaError_t launch_int4_bs(DecodeArgs a, int active_max, cudaStream_t s) {
+template <bool FC1>
+cudaError_t launch_int4_bs(DecodeArgs a, int units_max, cudaStream_t s) {
   const int nq = a.K / kChunkK;
   const int rgroups = a.N / kRowsPerGroup;
-  const int64_t items = (int64_t)active_max * rgroups;
-  const int64_t warps = (int64_t)sm_count() * kBlocksPerSm * kWarps;
+  const int64_t items = (int64_t)units_max * rgroups;
+  const int64_t warps = (int64_t)sm_count() * kBlocksPerSmB * kWarps;
   int ks = 1;
   while (ks < kWarps && 2 * ks <= nq && items * ks < 4 * warps) ks <<= 1;
   a.ks = ks;
   int64_t blocks = (items + (kWarps / ks) - 1) / (kWarps / ks);
-  const int64_t cap = (int64_t)sm_count() * kBlocksPerSm;
+  const int64_t cap = (int64_t)sm_count() * kBlocksPerSmB;
   if (blocks > cap) blocks = cap;
-  const size_t smem = (size_t)kWarps * kRingB * kSlotBytes + (ks > 1 ? (size_t)kWarps * NP * 128 * sizeof(float) : 0);
+  const size_t smem = (size_t)kWarps * kRingB * kSlotBytes + (ks > 1 ? (size_t)2 * kWarps * 128 * sizeof(float) : 0);
   const bool bf16 = a.p.dtype == QMOE_BF16, zp = a.zp != nullptr;
-  if (bf16) return zp ? launch_int4_bs_t<FC1, NP, true, true>(a, blocks, smem, s)
-                      : launch_int4_bs_t<FC1, NP, true, false>(a, blocks, smem, s);
-  return zp ? launch_int4_bs_t<FC1, NP, false, true>(a, blocks, smem, s)
-            : launch_int4_bs_t<FC1, NP, false, false>(a, blocks, smem, s);
+  if (bf16) return zp ? launch_int4_bs_t<FC1, true, true>(a, blocks, smem, s)
+                      : launch_int4_bs_t<FC1, true, false>(a, blocks, smem, s);
+  return zp ? launch_int4_bs_t<FC1, false, true>(a, blocks, smem, s)
+            : launch_int4_bs_t<FC1, false, false>(a, blocks, smem, s);
 }
 
 int sm_count() {
@@ -829,10 +798,11 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
   if (BITS == 4 && decode_int4_blockscaled(p)) {
     DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                  fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
-    const int pairs = ((p.T < 8 ? (int)p.T : 8) + 1) / 2;   // <= T routes per expert
-    if (pairs <= 1) return fc1 ? launch_int4_bs<true, 1>(a, active_max, s) : launch_int4_bs<false, 1>(a, active_max, s);
-    if (pairs <= 2) return fc1 ? launch_int4_bs<true, 2>(a, active_max, s) : launch_int4_bs<false, 2>(a, active_max, s);
-    return fc1 ? launch_int4_bs<true, 4>(a, active_max, s) : launch_int4_bs<false, 4>(a, active_max, s);
+    // decode-table entries: at most one per expert per pair of routes (<= R, <= E * ceil(T/2))
+    const int64_t per_expert = (p.T + 1) / 2;
+    int64_t units = (int64_t)p.E * per_expert;
+    if (units > R) units = R;
+    return fc1 ? launch_int4_bs<true>(a, (int)units, s) : launch_int4_bs<false>(a, (int)units, s);
   }
   DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};

@@ -18,7 +18,8 @@ constexpr int kMaxTopK = 32;
 constexpr int kDecodeMaxT = 8;        // decode GEMV: at most 8 routes per expert (one MMA N-fragment)
 constexpr int kPermuteChunk = 512;    // routes per block in the grouping kernels
 constexpr int kTileM = 256;           // rows (routes) per grouped-GEMM tile
-constexpr int kDtabInts = 12;         // ints per decode-table entry
+constexpr int kDtabInts = 8;          // ints per decode-table entry
+constexpr int kDtabMax = kDecodeMaxT * kMaxTopK;  // entries: at most one per route
 
 // ---------------------------------------------------------------------------
 // Workspace: every scratch buffer of one forward call, carved from the
@@ -32,11 +33,13 @@ struct Workspace {
   int32_t* offsets;       // [E+1]    exclusive prefix of per-expert route counts
   int32_t* sorted_route;  // [R]      route ids grouped by expert, stable
   int32_t* active;        // [E]      experts with at least one route, ascending
-  int32_t* counters;      // [4]      [0] active experts, [1] grouped tiles
+  int32_t* counters;      // [4]      [0] active experts, [1] grouped tiles, [2] error flag,
+                          //          [3] decode-table entries
   int32_t* tiles;         // [2*max_tiles] (expert, first sorted row) of each kTileM-row tile
   int32_t* chunk_hist;    // [nchunks][E] per-chunk expert counts, then chunk bases
-  int32_t* dtab;          // [E][kDtabInts] decode table per active slot: expert, first sorted
-                          //   row, route count, 0, token of each of its <= 8 routes
+  int32_t* dtab;          // [kDtabMax][kDtabInts] decode table: one entry per (active expert,
+                          //   pair of its routes): expert, first sorted row of the pair, routes in
+                          //   the pair (1 or 2), 0, token of each route; counters[3] entries
   uint16_t* x16s;         // [R][H]   x16 rows gathered into sorted-route order (grouped)
   uint16_t* h16;          // [R][I]   SwiGLU output, FP16, sorted-route order, K-order permuted
   float* y;               // [R][H]   weighted fc2 output per route id (FP32)

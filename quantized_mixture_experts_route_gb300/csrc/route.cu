@@ -338,19 +338,33 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   finish_groups(p.E, total, ws, want_tiles != 0, sh, hist);  // hist now holds the bases
   __syncthreads();
   scatter_routes(ws.topk_idx, 0, R, p.E, hist, warp_cnt, ws.sorted_route);
-  // decode table: one entry per active expert, so that the decode kernels reach an
-  // expert's rows and its routes' tokens with one independent load
+  // decode table: one entry per (active expert, pair of its routes), so that a
+  // decode work unit reaches its expert's rows and its tokens with one
+  // independent load and always multiplies exactly one MMA column pair
+  if (p.path != QMOE_PATH_DECODE) return;    // (block-uniform) R <= kDtabMax on this path
+  __syncthreads();
   const int n_active = ws.counters[0];
-  for (int a = threadIdx.x; a < n_active; a += blockDim.x) {
-    const int e = ws.active[a];
-    const int begin = ws.offsets[e], n_e = ws.offsets[e + 1] - begin;
-    int32_t* d = ws.dtab + a * kDtabInts;
-    d[0] = e;
-    d[1] = begin;
-    d[2] = n_e;
-    d[3] = 0;
-    for (int n = 0; n < 8; ++n) d[4 + n] = n < n_e ? ws.sorted_route[begin + n] / p.k : 0;
+  int e = 0, begin = 0, n_e = 0;
+  if ((int)threadIdx.x < n_active) {
+    e = ws.active[threadIdx.x];
+    begin = ws.offsets[e];
+    n_e = ws.offsets[e + 1] - begin;
   }
+  int n_entries;
+  const int first = block_exclusive_scan((n_e + 1) / 2, sh, &n_entries);
+  for (int q = 0; 2 * q < n_e; ++q) {
+    int32_t* d = ws.dtab + (first + q) * kDtabInts;
+    const int cnt = n_e - 2 * q < 2 ? n_e - 2 * q : 2;
+    d[0] = e;
+    d[1] = begin + 2 * q;
+    d[2] = cnt;
+    d[3] = 0;
+    d[4] = ws.sorted_route[begin + 2 * q] / p.k;
+    d[5] = cnt > 1 ? ws.sorted_route[begin + 2 * q + 1] / p.k : 0;
+    d[6] = 0;
+    d[7] = 0;
+  }
+  if (threadIdx.x == 0) ws.counters[3] = n_entries;
 }
 
 __global__ void __launch_bounds__(256) gather_kernel(Problem p, Workspace ws) {
