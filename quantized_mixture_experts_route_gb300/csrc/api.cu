@@ -87,6 +87,11 @@ size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* w
   w.nchunks = (R + kPermuteChunk - 1) / kPermuteChunk;
   w.chunk_hist = static_cast<int32_t*>(take(sizeof(int32_t) * w.nchunks * p.E));
   w.dtab = static_cast<int32_t*>(take(sizeof(int32_t) * kDtabInts * kDtabMax));
+  const bool dec = p.path == QMOE_PATH_DECODE;
+  w.dunits_max = dec ? decode_units_max(p) : 0;
+  w.dsplit_items = dec ? decode_split_items_max(p) : 0;
+  w.dticket = static_cast<int32_t*>(take(sizeof(int32_t) * w.dunits_max));
+  w.dsplit = static_cast<float*>(take(sizeof(float) * 128 * w.dsplit_items));
   w.x16s = grouped ? static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.H)) : nullptr;
   w.h16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.I));
   w.y = static_cast<float*>(take(sizeof(float) * R * p.H));

@@ -493,15 +493,20 @@ constexpr int kRingB = 4;                          // chunks in flight per warp
 constexpr int kSlotCode = 2 * 32 * 16;             // [2 rows][32 lanes][16 B]
 constexpr int kSlotScale = 2 * 32 * 4;             // [2 rows][32 lanes][2 scales]
 constexpr int kSlotZp = 2 * 32 * 4;                // [2 rows][32 lanes][4 zero points]
-constexpr int kSlotBytes = kSlotCode + kSlotScale + kSlotZp;
-
-
+constexpr int kSlotAct = 8 * 64;                   // [8 owner lanes][32 activations]
+constexpr int kSlotBytes = kSlotCode + kSlotScale + kSlotZp + kSlotAct;
 constexpr int kBlocksPerSmB = 3;
 
-// Work unit: (decode-table entry = active expert and a pair of its routes,
-// 16-row group). One accumulator set per unit. An expert with more than two
-// routes has several entries; their units read the same weight rows, which the
-// round-robin order hands to neighbouring teams in the same round, so the
+int choose_ks_bs(int64_t items, int nq);
+
+// Work item: (unit, K slice). A unit is (decode-table entry = active expert and
+// a pair of its routes, 16-row group); its K range is split into ks slices
+// handled by independent warps. Warps take work items round-robin over a
+// persistent grid, with no barriers: each writes its slice's FP32 partial tile
+// to a scratch buffer and takes a ticket; the last arriver adds the ks partials
+// in slice order (deterministic) and runs the epilogue. An expert with more than
+// two routes has several entries whose units read the same weight rows; the
+// round-robin order hands them to neighbouring warps in the same round, so the
 // repeated reads are served by L2.
 template <bool FC1, bool BF16S, bool HAS_ZP>
 __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_kernel(DecodeArgs a) {
@@ -511,43 +516,46 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
   const int nq = K / kChunkK;                    // K is a multiple of 128 here
   const int rgroups = N / kRowsPerGroup;
   const int items = ws.counters[3] * rgroups;
+  const int lks = 31 - __clz(a.ks);              // ks is a power of two
+  const int ks = a.ks;
+  const int works = items << lks;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int ks = a.ks;
-  const int team = warp / ks, ksi = warp % ks;
-  const int teams_per_block = kWarps / ks;
-  const int team_global = blockIdx.x * teams_per_block + team;
-  const int teams_total = gridDim.x * teams_per_block;
-  const int cb = nq * ksi / ks, ce = nq * (ksi + 1) / ks;
-  const int cpi = ce - cb;                       // >= 1 (ks <= nq)
-  const int my_items = team_global < items ? (items - team_global + teams_total - 1) / teams_total : 0;
-  const int total = my_items * cpi;
+  const int wg = blockIdx.x * kWarps + warp;
+  const int nwarps = gridDim.x * kWarps;
   const int64_t pitch = K / 2;                   // bytes of codes per row
   const int nblk = K / 32;
   const int b0 = 2 * (c & 1);                    // blocks of this lane's D columns: b0, b0 + 1
   const bool owner = (g & 3) == c;               // supplies activations for column g
+  const int oid = (g >> 2) * 4 + c;              // owner slot in the activation area
+  const int on = g >> 2;                         // owner lane's route within the pair
 
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* ring = smem + warp * (kRingB * kSlotBytes);
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
-  float* red = reinterpret_cast<float*>(smem + kWarps * kRingB * kSlotBytes);  // [2][8 warps][4][32]
 
-  // ---- issue side
-  int pf_item = team_global, pf_cc = 0;
+  // ---- issue side: walks this warp's work items, kRingB - 1 chunks ahead
+  int pw = wg, pcc = 0, pce = 0;
   const uint8_t* pq = nullptr;
   const uint16_t* ps = nullptr;
   const uint8_t* pz = nullptr;
-  int next_e = team_global < items ? ws.dtab[(team_global / rgroups) * kDtabInts] : 0;
+  int pboff = -1;
   auto issue = [&](int slot) {
-    if (pf_cc == 0) {
-      const int e = next_e;
-      const int nx = pf_item + teams_total;
-      next_e = nx < items ? ws.dtab[(nx / rgroups) * kDtabInts] : 0;
-      const int64_t row = (int64_t)e * N + (pf_item % rgroups) * kRowsPerGroup + g;
+    if (pcc == pce) {                            // start the next work item
+      if (pcc != 0) pw += nwarps;
+      const int item = pw >> lks, ksi = pw & (ks - 1);
+      const int cb = (nq * ksi) >> lks;
+      pce = ((nq * (ksi + 1)) >> lks) - cb;
+      pcc = 0;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts + 4));
+      const int64_t row = (int64_t)d0.x * N + (item % rgroups) * kRowsPerGroup + g;
       pq = a.q + row * pitch + (cb * kChunkK + 32 * c) / 2;
       ps = a.s + row * nblk + cb * 4 + b0;
       if constexpr (HAS_ZP) pz = a.zp + row * nblk + cb * 4;
+      pboff = -1;
+      if (owner && on < d0.z) pboff = (FC1 ? (on ? d1.y : d1.x) : d0.y + on) * K + cb * kChunkK + 32 * c;
     }
     const uint32_t d = ring_s + slot * kSlotBytes;
     cp_async16(d + lane * 16, pq);
@@ -559,11 +567,26 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
       cp_async4(d + kSlotCode + kSlotScale + 128 + lane * 4, pz + 8 * nblk);
       pz += 4;
     }
+    if (pboff >= 0) {
+      const uint16_t* src = a.act + pboff + pcc * kChunkK;
+      const uint32_t da = d + kSlotCode + kSlotScale + kSlotZp + oid * 64;
+      cp_async16(da, src);
+      cp_async16(da + 16, src + 8);
+      cp_async16(da + 32, src + 16);
+      cp_async16(da + 48, src + 24);
+    }
     cp_async_commit();
     pq += kChunkK / 2;
     ps += 4;
-    if (++pf_cc == cpi) { pf_cc = 0; pf_item += teams_total; }
+    ++pcc;
   };
+
+  // the number of chunks this warp streams
+  int total = 0;
+  for (int w = wg; w < works; w += nwarps) {
+    const int ksi = w & (ks - 1);
+    total += ((nq * (ksi + 1)) >> lks) - ((nq * ksi) >> lks);
+  }
   for (int u = 0; u < kRingB - 1; ++u) {
     if (u < total) issue(u);
     else cp_async_commit();
@@ -575,27 +598,30 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
   const uint32_t no_def = *reinterpret_cast<const uint32_t*>(&no_d);
 
   // ---- compute side
-  int item = team_global, cc = 0;
+  int w = wg, cc = 0, ce_n = 0, cnt = 0, pos0 = 0, tok0 = 0, tok1 = 0;
+  bool bvalid = false;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int pos0 = 0, cnt = 0, boff = -1;
-  const int32_t* dcur = nullptr;
-  auto open_item = [&]() {
-    dcur = ws.dtab + (item / rgroups) * kDtabInts;
-    pos0 = dcur[1];
-    cnt = dcur[2];
-    const int n = g >> 2;                        // this lane's column's route within the pair
-    boff = -1;
-    if (owner && n < cnt) boff = (FC1 ? dcur[4 + n] : pos0 + n) * K + cb * kChunkK + 32 * c;
-  };
-  if (total > 0) open_item();
   uint32_t bw[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) bw[j] = 0u;       // non-owner lanes keep zeros for good
-
-  int slot = 0, item_parity = 0;
+  int slot = 0;
   for (int f = 0; f < total; ++f) {
     if (f + kRingB - 1 < total) issue((slot + kRingB - 1) % kRingB);
     else cp_async_commit();
+    if (cc == ce_n) {                            // start of a work item (compute side)
+      if (f != 0) w += nwarps;
+      const int ksi = w & (ks - 1);
+      ce_n = ((nq * (ksi + 1)) >> lks) - ((nq * ksi) >> lks);
+      cc = 0;
+      const int item = w >> lks;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts + 4));
+      pos0 = d0.y;
+      cnt = d0.z;
+      tok0 = d1.x;
+      tok1 = d1.y;
+      bvalid = owner && on < cnt;
+    }
     cp_async_wait<kRingB - 1>();
     const uint8_t* sl = ring + slot * kSlotBytes;
     const uint4 ca = *reinterpret_cast<const uint4*>(sl + lane * 16);
@@ -613,15 +639,20 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
       ne_b = *reinterpret_cast<const uint32_t*>(&h3);
       no_b = *reinterpret_cast<const uint32_t*>(&h4);
     }
-    slot = slot + 1 == kRingB ? 0 : slot + 1;
-    if (boff >= 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.act + boff + cc * kChunkK);
+    if (owner) {
+      if (bvalid) {
+        const uint4* src = reinterpret_cast<const uint4*>(sl + kSlotCode + kSlotScale + kSlotZp + oid * 64);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 v = __ldg(src + j);
-        bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
+        for (int j = 0; j < 4; ++j) {
+          const uint4 v = src[j];
+          bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) bw[j] = 0u;
       }
     }
+    slot = slot + 1 == kRingB ? 0 : slot + 1;
     float s_a0, s_a1, s_b0, s_b1;
     if constexpr (BF16S) {
       s_a0 = __uint_as_float(swa << 16); s_a1 = __uint_as_float(swa & 0xFFFF0000u);
@@ -653,28 +684,37 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
     acc[1] = fmaf(s_a1, t0[1] + t1[1], acc[1]);
     acc[2] = fmaf(s_b0, t0[2] + t1[2], acc[2]);
     acc[3] = fmaf(s_b1, t0[3] + t1[3], acc[3]);
-    if (++cc < cpi) continue;
+    if (++cc < ce_n) continue;
 
-    // ---- unit finished: add the K split in warp order, then the epilogue
+    // ---- work item finished
+    const int item = w >> lks, ksi = w & (ks - 1);
+    bool last = true;
     if (ks > 1) {
-      // double-buffered by unit parity: one barrier per unit suffices, since a
-      // buffer is rewritten only after the next unit's barrier
-      float* buf = red + (size_t)(item_parity * kWarps) * 128;
-      float* mine = buf + (size_t)warp * 128;
+      float* part = ws.dsplit + (size_t)w * 128;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) mine[r * 32 + lane] = acc[r];
-      asm volatile("bar.sync %0, %1;\n" ::"r"(team + 1), "r"(32 * ks) : "memory");
-      if (ksi == 0) {
+      for (int r = 0; r < 4; ++r) part[r * 32 + lane] = acc[r];
+      __threadfence();
+      int old = 0;
+      if (lane == 0) old = atomicAdd(&ws.dticket[item], 1);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      last = old == ks - 1;
+      if (last) {
+        // every slice has arrived: the ticket is free again (for fc2, and the next call)
+        if (lane == 0) ws.dticket[item] = 0;
+        __threadfence();
+        // the K slices' partials added in slice order
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          float v = acc[r];
-          for (int k2 = 1; k2 < ks; ++k2) v += buf[(size_t)(warp + k2) * 128 + r * 32 + lane];
+          float v = 0.f;
+          for (int k2 = 0; k2 < ks; ++k2) {
+            const float pk = k2 == ksi ? acc[r] : __ldcg(ws.dsplit + ((size_t)(item << lks) + k2) * 128 + r * 32 + lane);
+            v = k2 == 0 ? pk : v + pk;
+          }
           acc[r] = v;
         }
       }
-      item_parity ^= 1;
     }
-    if (ksi == 0) {
+    if (last) {
       const int row0 = (item % rgroups) * kRowsPerGroup;
       // route sum over its four block columns: lanes c and c^1 hold two each
       float v_lo = acc[0] + acc[1];
@@ -687,7 +727,7 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
         const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
         if ((g & 1) == 0 && (c & 1) == 0 && n < cnt) {
           const int pos = pos0 + n;
-          const float sigma = ws.tok_scale[dcur[4 + n]];
+          const float sigma = ws.tok_scale[n ? tok1 : tok0];
           const float inv = 1.0f / sigma;
           const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
           const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
@@ -708,11 +748,8 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
         }
       }
     }
-    cc = 0;
-    item += teams_total;
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[r] = 0.f;
-    if (f + 1 < total) open_item();
   }
   cp_async_wait<0>();
 }
@@ -731,23 +768,29 @@ cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStre
 }
 
 template <bool FC1>
-cudaError_t launch_int4_bs(DecodeArgs a, int units_max, cudaStream_t s) {
+cudaError_t launch_int4_bs(DecodeArgs a, int64_t units_max, cudaStream_t s) {
   const int nq = a.K / kChunkK;
-  const int rgroups = a.N / kRowsPerGroup;
-  const int64_t items = (int64_t)units_max * rgroups;
-  const int64_t warps = (int64_t)sm_count() * kBlocksPerSmB * kWarps;
-  int ks = 1;
-  while (ks < kWarps && 2 * ks <= nq && items * ks < 4 * warps) ks <<= 1;
-  a.ks = ks;
-  int64_t blocks = (items + (kWarps / ks) - 1) / (kWarps / ks);
+  const int64_t items = units_max * (a.N / kRowsPerGroup);
+  a.ks = choose_ks_bs(items, nq);
+  int64_t blocks = (items * a.ks + kWarps - 1) / kWarps;
   const int64_t cap = (int64_t)sm_count() * kBlocksPerSmB;
   if (blocks > cap) blocks = cap;
-  const size_t smem = (size_t)kWarps * kRingB * kSlotBytes + (ks > 1 ? (size_t)2 * kWarps * 128 * sizeof(float) : 0);
+  if (blocks < 1) blocks = 1;
+  const size_t smem = (size_t)kWarps * kRingB * kSlotBytes;
   const bool bf16 = a.p.dtype == QMOE_BF16, zp = a.zp != nullptr;
   if (bf16) return zp ? launch_int4_bs_t<FC1, true, true>(a, blocks, smem, s)
                       : launch_int4_bs_t<FC1, true, false>(a, blocks, smem, s);
   return zp ? launch_int4_bs_t<FC1, false, true>(a, blocks, smem, s)
             : launch_int4_bs_t<FC1, false, false>(a, blocks, smem, s);
+}
+
+// The smallest K split (power of two, <= 8, <= chunks) that gives every warp of
+// the persistent grid several work items.
+int choose_ks_bs(int64_t items, int nq) {
+  const int64_t warps = (int64_t)sm_count() * kBlocksPerSmB * kWarps;
+  int ks = 1;
+  while (ks < kWarps && 2 * ks <= nq && items * ks < 4 * warps) ks <<= 1;
+  return ks;
 }
 
 int sm_count() {
@@ -798,11 +841,8 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
   if (BITS == 4 && decode_int4_blockscaled(p)) {
     DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                  fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
-    // decode-table entries: at most one per expert per pair of routes (<= R, <= E * ceil(T/2))
-    const int64_t per_expert = (p.T + 1) / 2;
-    int64_t units = (int64_t)p.E * per_expert;
-    if (units > R) units = R;
-    return fc1 ? launch_int4_bs<true>(a, (int)units, s) : launch_int4_bs<false>(a, (int)units, s);
+    const int64_t entries = decode_units_max(p) / ((2 * p.I > p.H ? 2 * p.I : p.H) / kRowsPerGroup);
+    return fc1 ? launch_int4_bs<true>(a, entries, s) : launch_int4_bs<false>(a, entries, s);
   }
   DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
@@ -810,6 +850,21 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
 }
 
 }  // namespace
+
+int64_t decode_units_max(const Problem& p) {
+  // decode-table entries: at most one per expert per pair of routes (<= R, <= E * ceil(T/2))
+  int64_t entries = (int64_t)p.E * ((p.T + 1) / 2);
+  if (entries > p.R()) entries = p.R();
+  return entries * ((2 * p.I > p.H ? 2 * p.I : p.H) / kRowsPerGroup);
+}
+
+int64_t decode_split_items_max(const Problem& p) {
+  if (!decode_int4_blockscaled(p)) return 0;
+  const int64_t entries = decode_units_max(p) / ((2 * p.I > p.H ? 2 * p.I : p.H) / kRowsPerGroup);
+  const int64_t i1 = entries * (2 * p.I / kRowsPerGroup), i2 = entries * (p.H / kRowsPerGroup);
+  const int64_t w1 = i1 * choose_ks_bs(i1, p.H / kChunkK), w2 = i2 * choose_ks_bs(i2, p.I / kChunkK);
+  return w1 > w2 ? w1 : w2;
+}
 
 cudaError_t launch_decode(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
                           const uint8_t* zp, const Workspace& ws, cudaStream_t s) {

@@ -43,6 +43,10 @@ struct Workspace {
   uint16_t* x16s;         // [R][H]   x16 rows gathered into sorted-route order (grouped)
   uint16_t* h16;          // [R][I]   SwiGLU output, FP16, sorted-route order, K-order permuted
   float* y;               // [R][H]   weighted fc2 output per route id (FP32)
+  float* dsplit;           // decode split-K partials [work items][4][32] (FP32)
+  int32_t* dticket;        // [decode units] arrival counters of the split-K partials
+  int64_t dunits_max;      // capacity of dticket
+  int64_t dsplit_items;    // capacity of dsplit in work items
   int64_t max_tiles;
   int64_t nchunks;
 };
@@ -52,6 +56,11 @@ struct Problem {
   int H, I, E, k, bits, block, dtype, path;
   __host__ __device__ int64_t R() const { return T * (int64_t)k; }
 };
+
+// Decode work units (decode-table entries x 16-row groups of the larger matmul)
+// and split-K work items the workspace is sized for.
+int64_t decode_units_max(const Problem& p);
+int64_t decode_split_items_max(const Problem& p);
 
 // Byte size of the workspace for problem p and the pointers inside `base`
 // (base may be null when only the size is wanted).

@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   // decode work unit reaches its expert's rows and its tokens with one
   // independent load and always multiplies exactly one MMA column pair
   if (p.path != QMOE_PATH_DECODE) return;    // (block-uniform) R <= kDtabMax on this path
+  for (int64_t i = threadIdx.x; i < ws.dunits_max; i += blockDim.x) ws.dticket[i] = 0;
   __syncthreads();
   const int n_active = ws.counters[0];
   int e = 0, begin = 0, n_e = 0;
