@@ -468,6 +468,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
 }
 
 int sm_count();
+int64_t decode_grid_blocks();
 constexpr int kBlocksPerSm = 2;
 
 // ---------------------------------------------------------------------------
@@ -497,17 +498,21 @@ constexpr int kSlotAct = 8 * 64;                   // [8 owner lanes][32 activat
 constexpr int kSlotBytes = kSlotCode + kSlotScale + kSlotZp + kSlotAct;
 constexpr int kBlocksPerSmB = 3;
 
-int choose_ks_bs(int64_t items, int nq);
+// Stream-K work split. Units are (decode-table entry = active expert and a pair
+// of its routes, 16-row group); their 128-wide K chunks, laid end to end, form
+// one flat range that is cut into nw equal contiguous pieces, one per warp of a
+// persistent grid. A warp streams its piece through the cp.async ring; a unit that
+// lies wholly inside the piece ends in the warp's epilogue, and the (at most two)
+// units cut at the piece's ends leave an FP32 partial tile in scratch and take a
+// ticket: the last of a unit's parts adds them in chunk order (deterministic)
+// and runs the epilogue. An expert with more than two routes has several
+// entries whose units read the same weight rows; neighbouring entries stream at
+// the same time, so the repeated reads are served by L2.
+__device__ __forceinline__ int chunk_owner(int64_t x, int nw, int64_t total) {
+  // the warp whose piece [floor(w*total/nw), floor((w+1)*total/nw)) holds chunk x
+  return (int)(((x + 1) * nw - 1) / total);
+}
 
-// Work item: (unit, K slice). A unit is (decode-table entry = active expert and
-// a pair of its routes, 16-row group); its K range is split into ks slices
-// handled by independent warps. Warps take work items round-robin over a
-// persistent grid, with no barriers: each writes its slice's FP32 partial tile
-// to a scratch buffer and takes a ticket; the last arriver adds the ks partials
-// in slice order (deterministic) and runs the epilogue. An expert with more than
-// two routes has several entries whose units read the same weight rows; the
-// round-robin order hands them to neighbouring warps in the same round, so the
-// repeated reads are served by L2.
 template <bool FC1, bool BF16S, bool HAS_ZP>
 __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_kernel(DecodeArgs a) {
   const Problem& p = a.p;
@@ -516,14 +521,16 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
   const int nq = K / kChunkK;                    // K is a multiple of 128 here
   const int rgroups = N / kRowsPerGroup;
   const int items = ws.counters[3] * rgroups;
-  const int lks = 31 - __clz(a.ks);              // ks is a power of two
-  const int ks = a.ks;
-  const int works = items << lks;
+  const int64_t cfull = (int64_t)items * nq;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int wg = blockIdx.x * kWarps + warp;
-  const int nwarps = gridDim.x * kWarps;
+  // pieces over at most one warp per chunk, so that no piece is empty (the
+  // tickets count one part per warp between a unit's first and last chunk)
+  const int nw = (int)((int64_t)gridDim.x * kWarps < cfull ? (int64_t)gridDim.x * kWarps : cfull);
+  const int64_t x_begin = wg < nw ? cfull * wg / nw : 0, x_end = wg < nw ? cfull * (wg + 1) / nw : 0;
+  const int total = (int)(x_end - x_begin);
   const int64_t pitch = K / 2;                   // bytes of codes per row
   const int nblk = K / 32;
   const int b0 = 2 * (c & 1);                    // blocks of this lane's D columns: b0, b0 + 1
@@ -535,27 +542,27 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
   uint8_t* ring = smem + warp * (kRingB * kSlotBytes);
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
 
-  // ---- issue side: walks this warp's work items, kRingB - 1 chunks ahead
-  int pw = wg, pcc = 0, pce = 0;
+  const int item0 = total > 0 ? (int)(x_begin / nq) : 0;
+  const int cic0 = total > 0 ? (int)(x_begin - (int64_t)item0 * nq) : 0;
+
+  // ---- issue side: walks the piece kRingB - 1 chunks ahead
+  int p_item = item0, p_cic = cic0;              // unit and chunk within it
+  bool p_new = true;
   const uint8_t* pq = nullptr;
   const uint16_t* ps = nullptr;
   const uint8_t* pz = nullptr;
   int pboff = -1;
   auto issue = [&](int slot) {
-    if (pcc == pce) {                            // start the next work item
-      if (pcc != 0) pw += nwarps;
-      const int item = pw >> lks, ksi = pw & (ks - 1);
-      const int cb = (nq * ksi) >> lks;
-      pce = ((nq * (ksi + 1)) >> lks) - cb;
-      pcc = 0;
-      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts));
-      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts + 4));
-      const int64_t row = (int64_t)d0.x * N + (item % rgroups) * kRowsPerGroup + g;
-      pq = a.q + row * pitch + (cb * kChunkK + 32 * c) / 2;
-      ps = a.s + row * nblk + cb * 4 + b0;
-      if constexpr (HAS_ZP) pz = a.zp + row * nblk + cb * 4;
+    if (p_new) {
+      p_new = false;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (p_item / rgroups) * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (p_item / rgroups) * kDtabInts + 4));
+      const int64_t row = (int64_t)d0.x * N + (p_item % rgroups) * kRowsPerGroup + g;
+      pq = a.q + row * pitch + (p_cic * kChunkK + 32 * c) / 2;
+      ps = a.s + row * nblk + p_cic * 4 + b0;
+      if constexpr (HAS_ZP) pz = a.zp + row * nblk + p_cic * 4;
       pboff = -1;
-      if (owner && on < d0.z) pboff = (FC1 ? (on ? d1.y : d1.x) : d0.y + on) * K + cb * kChunkK + 32 * c;
+      if (owner && on < d0.z) pboff = (FC1 ? (on ? d1.y : d1.x) : d0.y + on) * K + p_cic * kChunkK + 32 * c;
     }
     const uint32_t d = ring_s + slot * kSlotBytes;
     cp_async16(d + lane * 16, pq);
@@ -568,25 +575,19 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
       pz += 4;
     }
     if (pboff >= 0) {
-      const uint16_t* src = a.act + pboff + pcc * kChunkK;
+      const uint16_t* src = a.act + pboff;
       const uint32_t da = d + kSlotCode + kSlotScale + kSlotZp + oid * 64;
       cp_async16(da, src);
       cp_async16(da + 16, src + 8);
       cp_async16(da + 32, src + 16);
       cp_async16(da + 48, src + 24);
+      pboff += kChunkK;
     }
     cp_async_commit();
     pq += kChunkK / 2;
     ps += 4;
-    ++pcc;
+    if (++p_cic == nq) { p_cic = 0; ++p_item; p_new = true; }
   };
-
-  // the number of chunks this warp streams
-  int total = 0;
-  for (int w = wg; w < works; w += nwarps) {
-    const int ksi = w & (ks - 1);
-    total += ((nq * (ksi + 1)) >> lks) - ((nq * ksi) >> lks);
-  }
   for (int u = 0; u < kRingB - 1; ++u) {
     if (u < total) issue(u);
     else cp_async_commit();
@@ -598,8 +599,10 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
   const uint32_t no_def = *reinterpret_cast<const uint32_t*>(&no_d);
 
   // ---- compute side
-  int w = wg, cc = 0, ce_n = 0, cnt = 0, pos0 = 0, tok0 = 0, tok1 = 0;
-  bool bvalid = false;
+  int item = item0, cic = cic0;
+  int first_cic = cic;                           // where this warp's part of the unit began
+  int cnt = 0, pos0 = 0, tok0 = 0, tok1 = 0;
+  bool bvalid = false, fresh = true;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   uint32_t bw[16];
 #pragma unroll
@@ -608,12 +611,8 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
   for (int f = 0; f < total; ++f) {
     if (f + kRingB - 1 < total) issue((slot + kRingB - 1) % kRingB);
     else cp_async_commit();
-    if (cc == ce_n) {                            // start of a work item (compute side)
-      if (f != 0) w += nwarps;
-      const int ksi = w & (ks - 1);
-      ce_n = ((nq * (ksi + 1)) >> lks) - ((nq * ksi) >> lks);
-      cc = 0;
-      const int item = w >> lks;
+    if (fresh) {
+      fresh = false;
       const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts));
       const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts + 4));
       pos0 = d0.y;
@@ -684,31 +683,41 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
     acc[1] = fmaf(s_a1, t0[1] + t1[1], acc[1]);
     acc[2] = fmaf(s_b0, t0[2] + t1[2], acc[2]);
     acc[3] = fmaf(s_b1, t0[3] + t1[3], acc[3]);
-    if (++cc < ce_n) continue;
+    ++cic;
+    if (cic < nq && f + 1 < total) continue;
 
-    // ---- work item finished
-    const int item = w >> lks, ksi = w & (ks - 1);
+    // ---- this warp's part of the unit is done
+    const bool whole = first_cic == 0 && cic == nq;
     bool last = true;
-    if (ks > 1) {
-      float* part = ws.dsplit + (size_t)w * 128;
+    if (!whole) {
+      // parts of this unit: the warps owning its first and last chunk, and those between
+      const int64_t ux = (int64_t)item * nq;
+      const int w0 = chunk_owner(ux, nw, cfull), w1 = chunk_owner(ux + nq - 1, nw, cfull);
+      // partial slot 0: the piece's first unit; slot 1: its last unit
+      float* part = ws.dsplit + ((size_t)wg * 2 + (item == item0 ? 0 : 1)) * 128;
 #pragma unroll
       for (int r = 0; r < 4; ++r) part[r * 32 + lane] = acc[r];
-      __threadfence();
+      __syncwarp();
       int old = 0;
-      if (lane == 0) old = atomicAdd(&ws.dticket[item], 1);
+      if (lane == 0) {
+        // release: the warp's partial tile is visible before the ticket moves;
+        // acquire: the other parts' tiles are visible to the last arriver
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(ws.dticket + item) : "memory");
+      }
       old = __shfl_sync(0xffffffffu, old, 0);
-      last = old == ks - 1;
+      last = old == w1 - w0;
       if (last) {
-        // every slice has arrived: the ticket is free again (for fc2, and the next call)
-        if (lane == 0) ws.dticket[item] = 0;
-        __threadfence();
-        // the K slices' partials added in slice order
+        if (lane == 0) ws.dticket[item] = 0;    // free again for fc2 and the next call
+        __syncwarp();
+        // parts added in chunk order: warps w0 .. w1
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           float v = 0.f;
-          for (int k2 = 0; k2 < ks; ++k2) {
-            const float pk = k2 == ksi ? acc[r] : __ldcg(ws.dsplit + ((size_t)(item << lks) + k2) * 128 + r * 32 + lane);
-            v = k2 == 0 ? pk : v + pk;
+          for (int wk = w0; wk <= w1; ++wk) {
+            const int64_t wk_begin = cfull * wk / nw;
+            const int hs = (wk_begin / nq == item) ? 0 : 1;   // the unit is warp wk's first one?
+            const float pk = wk == wg ? acc[r] : __ldcg(ws.dsplit + ((size_t)wk * 2 + hs) * 128 + r * 32 + lane);
+            v = wk == w0 ? pk : v + pk;
           }
           acc[r] = v;
         }
@@ -750,6 +759,9 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[r] = 0.f;
+    if (cic == nq) { cic = 0; ++item; }
+    first_cic = cic;
+    fresh = true;
   }
   cp_async_wait<0>();
 }
@@ -767,30 +779,17 @@ cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStre
   return cudaGetLastError();
 }
 
+int64_t decode_grid_blocks() { return (int64_t)sm_count() * kBlocksPerSmB; }
+
 template <bool FC1>
-cudaError_t launch_int4_bs(DecodeArgs a, int64_t units_max, cudaStream_t s) {
-  const int nq = a.K / kChunkK;
-  const int64_t items = units_max * (a.N / kRowsPerGroup);
-  a.ks = choose_ks_bs(items, nq);
-  int64_t blocks = (items * a.ks + kWarps - 1) / kWarps;
-  const int64_t cap = (int64_t)sm_count() * kBlocksPerSmB;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
+cudaError_t launch_int4_bs(DecodeArgs a, cudaStream_t s) {
+  const int64_t blocks = decode_grid_blocks();
   const size_t smem = (size_t)kWarps * kRingB * kSlotBytes;
   const bool bf16 = a.p.dtype == QMOE_BF16, zp = a.zp != nullptr;
   if (bf16) return zp ? launch_int4_bs_t<FC1, true, true>(a, blocks, smem, s)
                       : launch_int4_bs_t<FC1, true, false>(a, blocks, smem, s);
   return zp ? launch_int4_bs_t<FC1, false, true>(a, blocks, smem, s)
             : launch_int4_bs_t<FC1, false, false>(a, blocks, smem, s);
-}
-
-// The smallest K split (power of two, <= 8, <= chunks) that gives every warp of
-// the persistent grid several work items.
-int choose_ks_bs(int64_t items, int nq) {
-  const int64_t warps = (int64_t)sm_count() * kBlocksPerSmB * kWarps;
-  int ks = 1;
-  while (ks < kWarps && 2 * ks <= nq && items * ks < 4 * warps) ks <<= 1;
-  return ks;
 }
 
 int sm_count() {
@@ -841,8 +840,7 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
   if (BITS == 4 && decode_int4_blockscaled(p)) {
     DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                  fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
-    const int64_t entries = decode_units_max(p) / ((2 * p.I > p.H ? 2 * p.I : p.H) / kRowsPerGroup);
-    return fc1 ? launch_int4_bs<true>(a, entries, s) : launch_int4_bs<false>(a, entries, s);
+    return fc1 ? launch_int4_bs<true>(a, s) : launch_int4_bs<false>(a, s);
   }
   DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
@@ -859,11 +857,9 @@ int64_t decode_units_max(const Problem& p) {
 }
 
 int64_t decode_split_items_max(const Problem& p) {
+  // two partial tiles (the piece's first and last unit) per warp of the grid
   if (!decode_int4_blockscaled(p)) return 0;
-  const int64_t entries = decode_units_max(p) / ((2 * p.I > p.H ? 2 * p.I : p.H) / kRowsPerGroup);
-  const int64_t i1 = entries * (2 * p.I / kRowsPerGroup), i2 = entries * (p.H / kRowsPerGroup);
-  const int64_t w1 = i1 * choose_ks_bs(i1, p.H / kChunkK), w2 = i2 * choose_ks_bs(i2, p.I / kChunkK);
-  return w1 > w2 ? w1 : w2;
+  return decode_grid_blocks() * kWarps * 2;
 }
 
 cudaError_t launch_decode(const Problem& p, bool fc1, const uint8_t* q, const void* scales,

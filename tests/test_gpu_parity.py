@@ -96,6 +96,15 @@ def case(name):
     if name == "dense_E1_k1":
         return (Shape(T=3, H=128, inter=64, E=1, k=1, bits=4, block=32, dtype=BF16),
                 Recipe(scale_lo=0.01, scale_hi=0.03), 44)
+    if name == "bs_small":
+        return (Shape(T=1, H=256, inter=128, E=4, k=2, bits=4, block=32, dtype=BF16),
+                Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 46)
+    if name == "bs_zp_fp16":
+        return (Shape(T=6, H=512, inter=256, E=5, k=3, bits=4, block=32, dtype=FP16),
+                Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, explicit_zp=True), 47)
+    if name == "bs_crowded":
+        return (Shape(T=8, H=384, inter=256, E=3, k=3, bits=4, block=32, dtype=BF16),
+                Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 48)
     if name == "wide_k":
         return (Shape(T=2, H=256, inter=128, E=64, k=32, bits=4, block=128, dtype=BF16),
                 Recipe(logit_std=0.5, scale_lo=0.005, scale_hi=0.02), 45)
@@ -104,7 +113,7 @@ def case(name):
 
 DECODE_CASES = ["tiny", "decode_T1", "decode_T2", "decode_T4", "decode_T8", "int3_b64_T1",
                 "int3_b64_T8", "int3_b128_T8", "int2_T8", "int4_zp_fp16", "int3_zp_small",
-                "int2_zp_small", "dense_E1_k1", "wide_k"]
+                "int2_zp_small", "dense_E1_k1", "wide_k", "bs_small", "bs_zp_fp16", "bs_crowded"]
 
 
 @pytest.mark.parametrize("name", DECODE_CASES)
