@@ -497,6 +497,7 @@ constexpr int kSlotZp = 2 * 32 * 4;                // [2 rows][32 lanes][4 zero 
 constexpr int kSlotAct = 8 * 64;                   // [8 owner lanes][32 activations]
 constexpr int kSlotBytes = kSlotCode + kSlotScale + kSlotZp + kSlotAct;
 constexpr int kBlocksPerSmB = 3;
+constexpr int kMinPiece = 8;                       // chunks per warp at least (small batches)
 
 // Stream-K work split. Units are (decode-table entry = active expert and a pair
 // of its routes, 16-row group); their 128-wide K chunks, laid end to end, form
@@ -526,9 +527,10 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int wg = blockIdx.x * kWarps + warp;
-  // pieces over at most one warp per chunk, so that no piece is empty (the
-  // tickets count one part per warp between a unit's first and last chunk)
-  const int nw = (int)((int64_t)gridDim.x * kWarps < cfull ? (int64_t)gridDim.x * kWarps : cfull);
+  // pieces of at least kMinPiece chunks (and so never empty: the tickets count
+  // one part per warp between a unit's first and last chunk)
+  const int64_t nw_cap = (cfull + kMinPiece - 1) / kMinPiece;
+  const int nw = (int)((int64_t)gridDim.x * kWarps < nw_cap ? (int64_t)gridDim.x * kWarps : nw_cap);
   const int64_t x_begin = wg < nw ? cfull * wg / nw : 0, x_end = wg < nw ? cfull * (wg + 1) / nw : 0;
   const int total = (int)(x_end - x_begin);
   const int64_t pitch = K / 2;                   // bytes of codes per row
@@ -576,11 +578,11 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
     }
     if (pboff >= 0) {
       const uint16_t* src = a.act + pboff;
-      const uint32_t da = d + kSlotCode + kSlotScale + kSlotZp + oid * 64;
+      const uint32_t da = d + kSlotCode + kSlotScale + kSlotZp + oid * 16;   // [4][8 owners][16 B]
       cp_async16(da, src);
-      cp_async16(da + 16, src + 8);
-      cp_async16(da + 32, src + 16);
-      cp_async16(da + 48, src + 24);
+      cp_async16(da + 128, src + 8);
+      cp_async16(da + 256, src + 16);
+      cp_async16(da + 384, src + 24);
       pboff += kChunkK;
     }
     cp_async_commit();
@@ -640,10 +642,10 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
     }
     if (owner) {
       if (bvalid) {
-        const uint4* src = reinterpret_cast<const uint4*>(sl + kSlotCode + kSlotScale + kSlotZp + oid * 64);
+        const uint4* src = reinterpret_cast<const uint4*>(sl + kSlotCode + kSlotScale + kSlotZp + oid * 16);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 v = src[j];
+          const uint4 v = src[j * 8];
           bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
         }
       } else {
@@ -709,13 +711,15 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
       if (last) {
         if (lane == 0) ws.dticket[item] = 0;    // free again for fc2 and the next call
         __syncwarp();
-        // parts added in chunk order: warps w0 .. w1
+        // parts added in chunk order: warps w0 .. w1. Warp w0's piece may begin
+        // before the unit (the unit is then its last, slot 1); every later
+        // warp's piece begins inside it (slot 0).
+        const int hs0 = cfull * w0 / nw < ux ? 1 : 0;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           float v = 0.f;
           for (int wk = w0; wk <= w1; ++wk) {
-            const int64_t wk_begin = cfull * wk / nw;
-            const int hs = (wk_begin / nq == item) ? 0 : 1;   // the unit is warp wk's first one?
+            const int hs = wk == w0 ? hs0 : 0;
             const float pk = wk == wg ? acc[r] : __ldcg(ws.dsplit + ((size_t)wk * 2 + hs) * 128 + r * 32 + lane);
             v = wk == w0 ? pk : v + pk;
           }
