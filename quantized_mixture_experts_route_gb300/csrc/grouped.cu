@@ -65,6 +65,7 @@ struct Cfg {
   static constexpr int S_OFF = C_OFF + STAGES * C_BYTES;
   static constexpr int BAR_OFF = S_OFF + STAGES * S_BYTES;
   static constexpr int SMEM = BAR_OFF + 128 + 1024;   // barriers + TMEM address + alignment slack
+  static_assert(8 * (3 * STAGES + 2) + 8 <= 128, "barrier area");
   static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
   static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -309,27 +310,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int S = C::STAGES;
   const Workspace& ws = g.ws;
   const Problem& p = g.p;
-  const int tile = blockIdx.y;
   volatile int* launch_err = ws.counters + 2;   // set by a CTA whose wait timed out
-  if (tile >= ws.counters[1] || *launch_err) return;
-  const int e = ws.tiles[2 * tile];
-  const int row0 = ws.tiles[2 * tile + 1];     // first sorted row of the tile
-  const int rows = min(kBM, ws.offsets[e + 1] - row0);
-  const int n0 = blockIdx.x * C::BN;
   const int K = g.K, N = g.N;
   const int ksteps = K / C::BK;
+  const int n_tiles_n = (N + C::BN - 1) / C::BN;
+  // work tiles, m-tile major so that the n-tiles of one activation tile run together
+  const int works = ws.counters[1] * n_tiles_n;
+  if (blockIdx.x >= works || *launch_err) return;
+  const int my_works = (works - blockIdx.x + gridDim.x - 1) / gridDim.x;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::BAR_OFF;
-  // [0, S): TMA + scales landed; [S, 2S): B dequantised; [2S, 3S): stage free; [3S]: accumulators ready
+  // [0, S): TMA + scales landed; [S, 2S): B dequantised; [2S, 3S): stage free;
+  // [3S]: accumulators ready; [3S+1]: accumulators drained by the epilogue
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
   auto bar_bready = [&](int s) { return bar0 + 8u * (S + s); };
   auto bar_empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
   const uint32_t bar_accum = bar0 + 8u * (3 * S);
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * S + 1));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * S + 1) + 4);
+  const uint32_t bar_drained = bar0 + 8u * (3 * S + 1);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * S + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * S + 2) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -339,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_accum, 1);
+    mbar_init(bar_drained, kDequantThreads);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
@@ -356,55 +359,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nblk = K / p.block;
+  auto tile_of = [&](int j, int& e, int& row0, int& n0) {
+    const int w = blockIdx.x + j * gridDim.x;
+    const int mt = w / n_tiles_n;
+    e = ws.tiles[2 * mt];
+    row0 = ws.tiles[2 * mt + 1];
+    n0 = (w - mt * n_tiles_n) * C::BN;
+  };
 
   if (warp == 0) {
-    // ---------------- producer: TMA (lane 0) and the stage's scales (all lanes)
+    // ---------------- producer: TMA (lane 0) and each stage's scales (all lanes)
     int issued = 0;
-    const int64_t wrow_base = (int64_t)e * N + n0;
-    const int64_t wrow_end = (int64_t)p.E * N;
-    for (int i = 0; i < ksteps; ++i) {
-      const int s = i % S;
-      const uint32_t ph = (uint32_t)(i / S) & 1u;
-      bool go = true;
-      if (lane == 0) go = mbar_wait(bar_empty(s), ph ^ 1u, abort_flag, launch_err);
-      go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-      if (!go) break;
-      ++issued;
-      const int k0 = i * C::BK;
-      if (lane == 0) {
-        mbar_expect_tx(bar_full(s), C::A_BYTES + C::C_BYTES);
+    bool go = true;
+    for (int j = 0; j < my_works && go; ++j) {
+      int e, row0, n0;
+      tile_of(j, e, row0, n0);
+      const int64_t wrow_base = (int64_t)e * N + n0;
+      const int64_t wrow_end = (int64_t)p.E * N;
+      for (int i = 0; i < ksteps; ++i) {
+        const int it = j * ksteps + i;           // stage sequence number across tiles
+        const int s = it % S;
+        const uint32_t ph = (uint32_t)(it / S) & 1u;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(bar_empty(s), ph ^ 1u, abort_flag, launch_err) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, ok, 0) == 0) { go = false; break; }
+        ++issued;
+        const int k0 = i * C::BK;
+        if (lane == 0) {
+          mbar_expect_tx(bar_full(s), C::A_BYTES + C::C_BYTES);
 #pragma unroll
-        for (int sub = 0; sub < C::SUB; ++sub)
+          for (int sub = 0; sub < C::SUB; ++sub)
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
-                        bar_full(s), k0 + 64 * sub, row0 + h * kSubM);
-        tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8, e * N + n0);
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
+                          bar_full(s), k0 + 64 * sub, row0 + h * kSubM);
+          tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8, e * N + n0);
+        }
+        uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
+        // all loads first (independent, no branches), then convert and store
+        constexpr int PER_LANE = C::UNITS / 32;
+        uint16_t sv[PER_LANE];
+        uint8_t zv[PER_LANE];
+#pragma unroll
+        for (int q = 0; q < PER_LANE; ++q) {
+          const int u = lane + 32 * q;
+          const int r = u / C::UNITS_PER_ROW, jj = u % C::UNITS_PER_ROW;
+          const int64_t wr = min(wrow_base + r, wrow_end - 1);   // rows past the array: masked below
+          const int64_t idx = wr * nblk + (k0 + 32 * jj) / p.block;
+          sv[q] = __ldg(g.scales + idx);
+          zv[q] = g.zp ? __ldg(g.zp + idx) : (uint8_t)(1u << (BITS - 1));
+        }
+#pragma unroll
+        for (int q = 0; q < PER_LANE; ++q) {
+          const int u = lane + 32 * q;
+          const int r = u / C::UNITS_PER_ROW;
+          const uint16_t sh = p.dtype == QMOE_BF16
+                                  ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sv[q] << 16)))
+                                  : sv[q];
+          st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
+        }
+        mbar_arrive(bar_full(s));
       }
-      uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
-      // all loads first (independent, no branches), then convert and store
-      constexpr int PER_LANE = C::UNITS / 32;
-      uint16_t sv[PER_LANE];
-      uint8_t zv[PER_LANE];
-#pragma unroll
-      for (int q = 0; q < PER_LANE; ++q) {
-        const int u = lane + 32 * q;
-        const int r = u / C::UNITS_PER_ROW, j = u % C::UNITS_PER_ROW;
-        const int64_t wr = min(wrow_base + r, wrow_end - 1);   // rows past the array: masked below
-        const int64_t idx = wr * nblk + (k0 + 32 * j) / p.block;
-        sv[q] = __ldg(g.scales + idx);
-        zv[q] = g.zp ? __ldg(g.zp + idx) : (uint8_t)(1u << (BITS - 1));
-      }
-#pragma unroll
-      for (int q = 0; q < PER_LANE; ++q) {
-        const int u = lane + 32 * q;
-        const int r = u / C::UNITS_PER_ROW;
-        const uint16_t sh = p.dtype == QMOE_BF16
-                                ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sv[q] << 16)))
-                                : sv[q];
-        st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
-      }
-      mbar_arrive(bar_full(s));
     }
     if (lane == 0 && *abort_flag) {
       // let the copies already issued land before the CTA exits
@@ -415,84 +430,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer: two 128-row accumulators share each B stage
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(kSubM, C::BN);
-      for (int i = 0; i < ksteps; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) break;
-        if (!mbar_wait(bar_bready(s), ph, abort_flag, launch_err)) break;
+      bool go = true;
+      int committed = 0;
+      for (int j = 0; j < my_works && go; ++j) {
+        // the epilogue of the previous tile has read the accumulators
+        if (j > 0 && !mbar_wait(bar_drained, (uint32_t)(j - 1) & 1u, abort_flag, launch_err)) break;
         tc_fence_after();
-        const uint32_t a_base = sbase + C::A_OFF + s * C::A_BYTES;
-        const uint32_t b_base = sbase + C::B_OFF + s * C::B_BYTES;
+        for (int i = 0; i < ksteps; ++i) {
+          const int it = j * ksteps + i;
+          const int s = it % S;
+          const uint32_t ph = (uint32_t)(it / S) & 1u;
+          if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err) ||
+              !mbar_wait(bar_bready(s), ph, abort_flag, launch_err)) { go = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = sbase + C::A_OFF + s * C::A_BYTES;
+          const uint32_t b_base = sbase + C::B_OFF + s * C::B_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk) {
-          const int sub = kk / 4, off = (kk % 4) * 32;
-          const uint64_t bdesc = sw128_desc(b_base + sub * (C::BN * 128) + off);
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const int sub = kk / 4, off = (kk % 4) * 32;
+            const uint64_t bdesc = sw128_desc(b_base + sub * (C::BN * 128) + off);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tc_mma(tmem + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
-                   idesc, (i | kk) != 0);
+            for (int h = 0; h < 2; ++h)
+              tc_mma(tmem + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
+                     idesc, (i | kk) != 0);
+          }
+          tc_commit(bar_empty(s));
         }
-        tc_commit(bar_empty(s));
+        tc_commit(bar_accum);
+        ++committed;
       }
-      tc_commit(bar_accum);
-      if (*abort_flag) mbar_wait_drain(bar_accum, 0);  // MMAs in flight finish before TMEM is freed
+      // MMAs in flight finish before TMEM is freed
+      if (*abort_flag && committed > 0) mbar_wait_drain(bar_accum, (uint32_t)(committed - 1) & 1u);
     }
   } else {
-    // ---------------- dequantisation (warps 2..9), then the epilogue
+    // ---------------- dequantisation (warps 2..9) and the epilogue of each tile
     const int t = threadIdx.x - 64;
-    for (int i = 0; i < ksteps; ++i) {
-      const int s = i % S;
-      const uint32_t ph = (uint32_t)(i / S) & 1u;
-      if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) break;
-      const uint8_t* codes = smem + C::C_OFF + s * C::C_BYTES;
-      const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
-      uint8_t* bt = smem + C::B_OFF + s * C::B_BYTES;
-#pragma unroll
-      for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
-        const int unit = t + kDequantThreads * u;
-        const int r = unit / C::UNITS_PER_ROW, j = unit % C::UNITS_PER_ROW;
-        const uint8_t* src = codes + r * C::CODE_ROW + j * C::UNIT_BYTES;
-        uint32_t w[BITS];
-        if constexpr (BITS == 4) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src);
-          w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-        } else if constexpr (BITS == 2) {
-          const uint2 v = *reinterpret_cast<const uint2*>(src);
-          w[0] = v.x; w[1] = v.y;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 3; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
-        }
-        const uint32_t sz = st[unit];
-        const uint32_t s2 = (sz & 0xFFFFu) * 0x00010001u;
-        uint32_t pr[16];
-        dequant_unit_fast<BITS>(w, sz >> 16, s2, pr);
-        uint8_t* rowp = bt + (j >> 1) * (C::BN * 128) + r * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int chunk = (j & 1) * 4 + c;
-          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(pr[4 * c], pr[4 * c + 1], pr[4 * c + 2], pr[4 * c + 3]);
-        }
-      }
-      fence_proxy_async();
-      mbar_arrive(bar_bready(s));
-    }
-
-    // ---------------- epilogue: TMEM -> registers -> global
     const int dw = warp - 2;
     const int half = dw >> 2;                     // accumulator: tile rows 128*half ..
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
     const int m = half * kSubM + quarter * 32 + lane;
-    const bool ok = mbar_wait(bar_accum, 0, abort_flag, launch_err);
-    tc_fence_after();
-    if (ok) {
+    const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
+    bool go = true;
+    for (int j = 0; j < my_works && go; ++j) {
+      int e, row0, n0;
+      tile_of(j, e, row0, n0);
+      // this thread's epilogue row: metadata loaded now, used after the K loop
+      const int rows = min(kBM, ws.offsets[e + 1] - row0);
       const bool row_ok = m < rows;
       const int pos = row0 + m;
       const int rid = row_ok ? ws.sorted_route[pos] : 0;
       const float sigma = row_ok ? ws.tok_scale[rid / p.k] : 1.0f;
+      const float wr = FC1 ? 0.f : (row_ok ? ws.topk_w[rid] : 0.f);
+      for (int i = 0; i < ksteps; ++i) {
+        const int it = j * ksteps + i;
+        const int s = it % S;
+        const uint32_t ph = (uint32_t)(it / S) & 1u;
+        if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) { go = false; break; }
+        const uint8_t* codes = smem + C::C_OFF + s * C::C_BYTES;
+        const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
+        uint8_t* bt = smem + C::B_OFF + s * C::B_BYTES;
+#pragma unroll
+        for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
+          const int unit = t + kDequantThreads * u;
+          const int r = unit / C::UNITS_PER_ROW, jj = unit % C::UNITS_PER_ROW;
+          const uint8_t* src = codes + r * C::CODE_ROW + jj * C::UNIT_BYTES;
+          uint32_t w[BITS];
+          if constexpr (BITS == 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+          } else if constexpr (BITS == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(src);
+            w[0] = v.x; w[1] = v.y;
+          } else {
+#pragma unroll
+            for (int q = 0; q < 3; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
+          }
+          const uint32_t sz = st[unit];
+          const uint32_t s2 = (sz & 0xFFFFu) * 0x00010001u;
+          uint32_t pr[16];
+          dequant_unit_fast<BITS>(w, sz >> 16, s2, pr);
+          uint8_t* rowp = bt + (jj >> 1) * (C::BN * 128) + r * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int chunk = (jj & 1) * 4 + c;
+            *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) =
+                make_uint4(pr[4 * c], pr[4 * c + 1], pr[4 * c + 2], pr[4 * c + 3]);
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(bar_bready(s));
+      }
+      if (!go) break;
+
+      // ---------------- epilogue: TMEM -> registers -> global
+      if (!mbar_wait(bar_accum, (uint32_t)j & 1u, abort_flag, launch_err)) break;
+      tc_fence_after();
       const float inv = 1.0f / sigma;
-      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
       for (int c0 = 0; c0 < C::BN; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)c0, v);
@@ -501,12 +534,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // columns are W1 rows n0 + c0 .. +31: gate/up pairs -> 16 outputs h_j
           const int j0 = (n0 + c0) / 2;
           constexpr int G = BITS == 4 ? 8 : 16;
+          const float ss = sigma * sigma;
           uint16_t hv[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const float gt = __uint_as_float(v[2 * q]) * inv;
             const float ut = __uint_as_float(v[2 * q + 1]) * inv;
-            hv[q] = __half_as_ushort(__float2half_rn(silu(gt) * ut * sigma * sigma));
+            // SwiGLU with CUDA's fast exp and divide; the result is rounded to FP16
+            const float sl = __fdividef(gt, 1.0f + __expf(-gt));
+            hv[q] = __half_as_ushort(__float2half_rn(sl * ut * ss));
           }
           uint16_t ov[16];
 #pragma unroll
@@ -517,18 +553,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[1] = make_uint4(ov[8] | ((uint32_t)ov[9] << 16), ov[10] | ((uint32_t)ov[11] << 16),
                               ov[12] | ((uint32_t)ov[13] << 16), ov[14] | ((uint32_t)ov[15] << 16));
         } else {
-          const float wr = ws.topk_w[rid];
-          const float f = inv * inv;
+          const float f = inv * inv * wr;
           float4* dst = reinterpret_cast<float4*>(ws.y + (int64_t)rid * p.H + n0 + c0);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * f * wr, __uint_as_float(v[4 * q + 1]) * f * wr,
-                                 __uint_as_float(v[4 * q + 2]) * f * wr,
-                                 __uint_as_float(v[4 * q + 3]) * f * wr);
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * f, __uint_as_float(v[4 * q + 1]) * f,
+                                 __uint_as_float(v[4 * q + 2]) * f, __uint_as_float(v[4 * q + 3]) * f);
         }
       }
+      tc_fence_before();
+      mbar_arrive(bar_drained);                  // the accumulators may be overwritten
     }
-    tc_fence_before();
   }
 
   __syncthreads();
@@ -592,8 +627,12 @@ cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, 
     attr_set = true;
   }
   GemmArgs g{static_cast<const uint16_t*>(scales), zp, N, K, p, ws};
-  if (ws.max_tiles > 65535) return cudaErrorNotSupported;  // grid.y limit: T * top_k < ~8.3M routes
-  dim3 grid((N + C::BN - 1) / C::BN, (unsigned)ws.max_tiles);
+  // persistent: one CTA per SM, each walking its share of the (m-tile, n-tile) list
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t works_max = ws.max_tiles * ((N + C::BN - 1) / C::BN);
+  dim3 grid((unsigned)(works_max < sms ? works_max : sms));
   grouped_gemm_kernel<BITS, FC1><<<grid, kThreads, C::SMEM, s>>>(ta, tq, g);
   return cudaGetLastError();
 }
