@@ -150,6 +150,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 32-byte global store (one full sector), 32-byte aligned address.
+__device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t e, uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+               "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
@@ -547,18 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint16_t ov[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q) ov[permuted_pos(q, G)] = hv[q];
-          uint4* dst = reinterpret_cast<uint4*>(ws.h16 + (int64_t)pos * p.I + j0);
-          dst[0] = make_uint4(ov[0] | ((uint32_t)ov[1] << 16), ov[2] | ((uint32_t)ov[3] << 16),
-                              ov[4] | ((uint32_t)ov[5] << 16), ov[6] | ((uint32_t)ov[7] << 16));
-          dst[1] = make_uint4(ov[8] | ((uint32_t)ov[9] << 16), ov[10] | ((uint32_t)ov[11] << 16),
-                              ov[12] | ((uint32_t)ov[13] << 16), ov[14] | ((uint32_t)ov[15] << 16));
+          // one 32-byte store: a whole sector per lane
+          st_global_v8(ws.h16 + (int64_t)pos * p.I + j0,
+                       ov[0] | ((uint32_t)ov[1] << 16), ov[2] | ((uint32_t)ov[3] << 16),
+                       ov[4] | ((uint32_t)ov[5] << 16), ov[6] | ((uint32_t)ov[7] << 16),
+                       ov[8] | ((uint32_t)ov[9] << 16), ov[10] | ((uint32_t)ov[11] << 16),
+                       ov[12] | ((uint32_t)ov[13] << 16), ov[14] | ((uint32_t)ov[15] << 16));
         } else {
           const float f = inv * inv * wr;
-          float4* dst = reinterpret_cast<float4*>(ws.y + (int64_t)rid * p.H + n0 + c0);
+          float* dst = ws.y + (int64_t)rid * p.H + n0 + c0;
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * f, __uint_as_float(v[4 * q + 1]) * f,
-                                 __uint_as_float(v[4 * q + 2]) * f, __uint_as_float(v[4 * q + 3]) * f);
+          for (int q = 0; q < 4; ++q)
+            st_global_v8(dst + 8 * q, __float_as_uint(__uint_as_float(v[8 * q]) * f),
+                         __float_as_uint(__uint_as_float(v[8 * q + 1]) * f),
+                         __float_as_uint(__uint_as_float(v[8 * q + 2]) * f),
+                         __float_as_uint(__uint_as_float(v[8 * q + 3]) * f),
+                         __float_as_uint(__uint_as_float(v[8 * q + 4]) * f),
+                         __float_as_uint(__uint_as_float(v[8 * q + 5]) * f),
+                         __float_as_uint(__uint_as_float(v[8 * q + 6]) * f),
+                         __float_as_uint(__uint_as_float(v[8 * q + 7]) * f));
         }
       }
       tc_fence_before();
