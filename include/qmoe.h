@@ -164,6 +164,37 @@ qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t
 /* Static, human-readable name of a status code. */
 const char* qmoe_status_string(qmoe_status s);
 
+/*
+ * The mixture-of-experts pages have no counterpart of this call: it serves
+ * callers that cannot allocate device memory.
+ *
+ * qmoe_forward on the decode path (T <= 8: path QMOE_PATH_DECODE, or
+ * QMOE_PATH_AUTO with T <= 8) with the same arguments, layouts and results,
+ * except that the workspace is a fixed device array inside this library of
+ * QMOE_STATIC_WORKSPACE_BYTES (8 MiB), which every GPU that loads the library
+ * holds until the process exits. The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine); the caller still passes the inputs
+ * and `out`. Returns QMOE_ERR_WORKSPACE_TOO_SMALL when qmoe_workspace_bytes(p)
+ * exceeds QMOE_STATIC_WORKSPACE_BYTES and QMOE_ERR_UNSUPPORTED when *p resolves
+ * to the grouped path; other errors as qmoe_forward. Both checks happen on the
+ * host before any CUDA call.
+ *
+ * The work runs on the calling thread's current device, to which `stream` must
+ * belong. The first call on each device looks up the array's device address
+ * there (cudaGetSymbolAddress) and caches it: make that first call before any
+ * stream capture on that device. All calls on a device share the array, which
+ * keeps the previous call's contents; each call first clears, on `stream`, the
+ * parts that must start at zero. Calls whose GPU work overlaps (different
+ * streams or threads without ordering between them) race on the array and give
+ * undefined results.
+ */
+#define QMOE_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
+qmoe_status qmoe_forward_decode_static(const qmoe_problem* p, const void* x,
+                                       const void* router_logits, const uint8_t* fc1_q,
+                                       const void* fc1_scales, const uint8_t* fc1_zp,
+                                       const uint8_t* fc2_q, const void* fc2_scales,
+                                       const uint8_t* fc2_zp, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,7 +42,9 @@ QMOE_PATH_GROUPED = 2
 
 # every symbol the header declares
 EXPORTED = ("qmoe_workspace_bytes", "qmoe_forward", "qmoe_forward_stages", "qmoe_route",
-            "qmoe_status_string")
+            "qmoe_status_string", "qmoe_forward_decode_static")
+
+QMOE_STATIC_WORKSPACE_BYTES = 8 << 20
 
 QMOE_STAGE_ROUTE = 0
 QMOE_STAGE_FC1 = 1
@@ -90,6 +92,8 @@ def lib():
         L.qmoe_forward_stages.restype = ctypes.c_int
         L.qmoe_route.argtypes = [P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.qmoe_route.restype = ctypes.c_int
+        L.qmoe_forward_decode_static.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.qmoe_forward_decode_static.restype = ctypes.c_int
         L.qmoe_status_string.argtypes = [ctypes.c_int]
         L.qmoe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -140,6 +144,17 @@ def qmoe_forward(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, f
                             _nbytes(workspace) if workspace is not None else 0, _stream(stream))
     if st != QMOE_OK:
         raise QMoEError(st, "qmoe_forward")
+
+
+def qmoe_forward_decode_static(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, fc2_q,
+                               fc2_scales, fc2_zp, out, stream=None) -> None:
+    """qmoe_forward on the decode path with the library's own fixed device workspace."""
+    st = lib().qmoe_forward_decode_static(ctypes.byref(p), _addr(x), _addr(router_logits),
+                                          _addr(fc1_q), _addr(fc1_scales), _addr(fc1_zp),
+                                          _addr(fc2_q), _addr(fc2_scales), _addr(fc2_zp),
+                                          _addr(out), _stream(stream))
+    if st != QMOE_OK:
+        raise QMoEError(st, "qmoe_forward_decode_static")
 
 
 def qmoe_forward_stages(p: qmoe_problem, first_stage: int, last_stage: int, x, router_logits, fc1_q,
