@@ -22,13 +22,25 @@ __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
     const int64_t t = i / per_row;
     const int h0 = (int)(i % per_row) * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < p.k; ++j) {
-      const int64_t r = t * p.k + j;
-      if (ws.topk_w[r] == 0.0f) continue;
-      const float4* src = reinterpret_cast<const float4*>(ws.y + r * p.H + h0);
-      const float4 a = src[0], b = src[1];
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    // routes in batches of 8: every load of a batch is issued before the first add
+    for (int j0 = 0; j0 < p.k; j0 += 8) {
+      float w[8];
+      float4 a[8], b[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = j0 + j < p.k ? ws.topk_w[t * p.k + j0 + j] : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t r = t * p.k + (j0 + j < p.k ? j0 + j : j0);
+        const float4* src = reinterpret_cast<const float4*>(ws.y + r * p.H + h0);
+        a[j] = src[0];
+        b[j] = src[1];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (w[j] == 0.0f) continue;   // also the batch's padding past k
+        acc[0] += a[j].x; acc[1] += a[j].y; acc[2] += a[j].z; acc[3] += a[j].w;
+        acc[4] += b[j].x; acc[5] += b[j].y; acc[6] += b[j].z; acc[7] += b[j].w;
+      }
     }
     uint4 o;
     o.x = float_to_half_bits(acc[0], p.dtype) | ((uint32_t)float_to_half_bits(acc[1], p.dtype) << 16);

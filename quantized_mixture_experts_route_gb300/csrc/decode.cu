@@ -32,7 +32,7 @@
 // (activation_type "swiglu", swiglu_fusion = 1), stored in FP16 with the
 // token's power of two squared. fc2 epilogue: y = (W2 h) / scale^2 * w_route in
 // FP32, stored per route id for the combine.
-#include "qmoe_internal.cuh"
+#include "tma.cuh"
 
 namespace qmoe {
 namespace {
@@ -785,6 +785,338 @@ cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStre
 
 int64_t decode_grid_blocks() { return (int64_t)sm_count() * kBlocksPerSmB; }
 
+// ---------------------------------------------------------------------------
+// INT4, block 32, K a multiple of 256: the same per-chunk arithmetic as above,
+// with the operands brought in by the tensor-memory-access unit. Lane 0 of each
+// warp issues, per 256-wide K chunk of a unit, four or five bulk tensor copies
+// (codes as two [16 rows][64 B] boxes, the [16 rows][8] block scales, the
+// chunk's activations of one or two tokens, the zero points when present) into
+// the warp's ring slot, completing on the slot's mbarrier; the other lanes only
+// wait on the barrier and read shared memory. Lanes that supply no activations
+// read a zero area instead of branching. Work split, tickets and epilogues are
+// those of the kernel above, with 256-wide chunks.
+// ---------------------------------------------------------------------------
+constexpr int kTWarps = 8;
+constexpr int kTRing = 3;                          // chunks per warp: two in flight, one in use
+constexpr int kTChunkK = 256;
+constexpr int kTBlocksPerSm = 2;
+constexpr int kTMinPiece = 4;
+constexpr int kTCode = 0;                          // [2 sub-chunks][16 rows][64 B]
+constexpr int kTScale = 2048;                      // [16 rows][8 scales]
+constexpr int kTZp = 2304;                         // [16 rows][16 zero points]
+constexpr int kTAct0 = 2560;                       // [256] FP16, first route's token
+constexpr int kTAct1 = 3072;                       // [256] FP16, second route's token
+constexpr int kTSlot = 3584;                       // every part 128-byte aligned
+constexpr int kTZero = 512;                        // zero bytes read by non-supplying lanes
+constexpr size_t kTSmem = (size_t)kTWarps * kTRing * kTSlot + kTZero + kTWarps * kTRing * 8 + 128;
+constexpr uint64_t kTWaitNs = 1000000000ull;      // 1 s: far beyond any legitimate wait
+constexpr uint64_t kTDrainNs = 100000000ull;
+constexpr int kErrDecodeTimeout = 2;
+
+struct TmaDecodeArgs {
+  int N, K;
+  Problem p;
+  Workspace ws;
+};
+
+template <bool FC1, bool BF16S, bool HAS_ZP>
+__global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ts,
+    const __grid_constant__ CUtensorMap tz, const __grid_constant__ CUtensorMap ta, TmaDecodeArgs a) {
+  const Problem& p = a.p;
+  const Workspace& ws = a.ws;
+  const int K = a.K, N = a.N;
+  const int nq = K / kTChunkK;
+  const int rgroups = N / kRowsPerGroup;
+  const int items = ws.counters[3] * rgroups;
+  const int64_t cfull = (int64_t)items * nq;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int wg = blockIdx.x * kTWarps + warp;
+  const int64_t nw_cap = (cfull + kTMinPiece - 1) / kTMinPiece;
+  const int nw = (int)((int64_t)gridDim.x * kTWarps < nw_cap ? (int64_t)gridDim.x * kTWarps : nw_cap);
+  const int64_t x_begin = wg < nw ? cfull * wg / nw : 0, x_end = wg < nw ? cfull * (wg + 1) / nw : 0;
+  const int total = (int)(x_end - x_begin);
+  const bool owner = (g & 3) == c;               // supplies activations for column g
+  const int on = g >> 2;                         // owner lane's route within the pair
+
+  extern __shared__ __align__(16) uint8_t smem[];
+  // bulk tensor copies land on 128-byte boundaries
+  uint8_t* base = smem + ((128u - (smem_u32(smem) & 127u)) & 127u);
+  const uint32_t ring_s = smem_u32(base) + warp * (kTRing * kTSlot);
+  const uint32_t zero_s = smem_u32(base) + kTWarps * kTRing * kTSlot;
+  const uint32_t bar_s = zero_s + kTZero + warp * (kTRing * 8);
+  if (threadIdx.x < kTZero / 4) reinterpret_cast<uint32_t*>(base + kTWarps * kTRing * kTSlot)[threadIdx.x] = 0u;
+  if (lane == 0)
+    for (int s = 0; s < kTRing; ++s) mbar_init(bar_s + 8 * s, 1);
+  mbar_init_fence();
+  __syncthreads();
+  if (total == 0) return;
+
+  const int item0 = (int)(x_begin / nq);
+  const int cic0 = (int)(x_begin - (int64_t)item0 * nq);
+
+  // ---- issue side: lane 0 copies chunk f of the piece into slot f % kTRing
+  int p_item = item0, p_cic = cic0, p_row = 0, p_t0 = 0, p_t1 = 0, p_cnt = 0;
+  bool p_new = true;
+  int p_slot = 0;
+  auto issue = [&]() {
+    if (p_new) {
+      p_new = false;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (p_item / rgroups) * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (p_item / rgroups) * kDtabInts + 4));
+      p_row = d0.x * N + (p_item % rgroups) * kRowsPerGroup;
+      p_cnt = d0.z;
+      p_t0 = FC1 ? d1.x : d0.y;
+      p_t1 = FC1 ? d1.y : d0.y + 1;
+    }
+    if (lane == 0) {
+      const uint32_t d = ring_s + p_slot * kTSlot, bar = bar_s + 8 * p_slot;
+      const int kx = p_cic * kTChunkK;
+      mbar_expect_tx(bar, 2048 + 256 + (HAS_ZP ? 256 : 0) + (p_cnt > 1 ? 1024 : 512));
+      tma_load_2d(d + kTCode, &tq, bar, kx / 2, p_row);
+      tma_load_2d(d + kTCode + 1024, &tq, bar, kx / 2 + 64, p_row);
+      tma_load_2d(d + kTScale, &ts, bar, kx / 32, p_row);
+      if constexpr (HAS_ZP) tma_load_2d(d + kTZp, &tz, bar, (kx / 32) & ~15, p_row);
+      tma_load_2d(d + kTAct0, &ta, bar, kx, p_t0);
+      if (p_cnt > 1) tma_load_2d(d + kTAct1, &ta, bar, kx, p_t1);
+    }
+    p_slot = p_slot + 1 == kTRing ? 0 : p_slot + 1;
+    if (++p_cic == nq) { p_cic = 0; ++p_item; p_new = true; }
+  };
+  const int pre = total < kTRing - 1 ? total : kTRing - 1;
+  for (int u = 0; u < pre; ++u) issue();
+
+  const __half2 ne_d = __float2half2_rn(-(1024.0f + 8.0f)), no_d = __float2half2_rn(-(1024.0f + 128.0f));
+  const uint32_t ne_def = *reinterpret_cast<const uint32_t*>(&ne_d);
+  const uint32_t no_def = *reinterpret_cast<const uint32_t*>(&no_d);
+  // activation words: owners read their token's tile, the other lanes the zero area
+  const uint32_t act_base = owner ? ring_s + (on ? kTAct1 : kTAct0) + 64 * c : zero_s;
+  const uint32_t act_slot_stride = owner ? kTSlot : 0;
+
+  // ---- compute side
+  int item = item0, cic = cic0;
+  int first_cic = cic;
+  int cnt = 0, pos0 = 0, tok0 = 0, tok1 = 0;
+  bool fresh = true;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int f = 0; f < total; ++f) {
+    __syncwarp();                                // every lane is done with the slot refilled next
+    if (f + kTRing - 1 < total) issue();
+    if (fresh) {
+      fresh = false;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts + 4));
+      pos0 = d0.y;
+      cnt = d0.z;
+      tok0 = d1.x;
+      tok1 = d1.y;
+    }
+    if (!mbar_wait_for(bar_s + 8 * slot, phase, kTWaitNs)) {
+      // record the failure, let this warp's copies in flight land, and stop
+      if (lane == 0) atomicExch(ws.counters + 2, kErrDecodeTimeout);
+      int s2 = slot;
+      uint32_t ph2 = phase;
+      const int inflight = total - f < kTRing ? total - f : kTRing;   // chunks f .. f + kTRing - 1
+      for (int u = 0; u < inflight; ++u) {
+        mbar_wait_for(bar_s + 8 * s2, ph2, kTDrainNs);
+        if (++s2 == kTRing) { s2 = 0; ph2 ^= 1u; }
+      }
+      return;
+    }
+    const uint32_t sb = ring_s + slot * kTSlot;
+    const uint32_t ab = act_base + slot * act_slot_stride;
+    const uint32_t srow = sb + kTScale + g * 16 + 4 * (c & 1);
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      uint4 ca, cbv;
+      uint32_t swa, swb;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                   : "=r"(ca.x), "=r"(ca.y), "=r"(ca.z), "=r"(ca.w) : "r"(sb + sub * 1024 + lane * 16));
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                   : "=r"(cbv.x), "=r"(cbv.y), "=r"(cbv.z), "=r"(cbv.w) : "r"(sb + sub * 1024 + 512 + lane * 16));
+      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(swa) : "r"(srow + 8 * sub));
+      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(swb) : "r"(srow + 128 + 8 * sub));
+      uint32_t bw[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(bw[4 * j]), "=r"(bw[4 * j + 1]), "=r"(bw[4 * j + 2]), "=r"(bw[4 * j + 3])
+                     : "r"(ab + sub * 256 + 16 * j));
+      uint32_t ne_a = ne_def, ne_b = ne_def, no_a = no_def, no_b = no_def;
+      if constexpr (HAS_ZP) {
+        uint32_t zwa, zwb;
+        const uint32_t zrow = sb + kTZp + g * 16 + (cic & 1) * 8 + 4 * sub;
+        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(zwa) : "r"(zrow));
+        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(zwb) : "r"(zrow + 128));
+        const uint32_t za = (zwa >> (8 * c)) & 0xFFu, zb = (zwb >> (8 * c)) & 0xFFu;
+        const __half2 h1 = __float2half2_rn(-(1024.0f + (float)za)), h2 = __float2half2_rn(-(1024.0f + 16.0f * (float)za));
+        const __half2 h3 = __float2half2_rn(-(1024.0f + (float)zb)), h4 = __float2half2_rn(-(1024.0f + 16.0f * (float)zb));
+        ne_a = *reinterpret_cast<const uint32_t*>(&h1);
+        no_a = *reinterpret_cast<const uint32_t*>(&h2);
+        ne_b = *reinterpret_cast<const uint32_t*>(&h3);
+        no_b = *reinterpret_cast<const uint32_t*>(&h4);
+      }
+      float s_a0, s_a1, s_b0, s_b1;
+      if constexpr (BF16S) {
+        s_a0 = __uint_as_float(swa << 16); s_a1 = __uint_as_float(swa & 0xFFFF0000u);
+        s_b0 = __uint_as_float(swb << 16); s_b1 = __uint_as_float(swb & 0xFFFF0000u);
+      } else {
+        s_a0 = __half2float(__ushort_as_half((uint16_t)(swa & 0xFFFFu))); s_a1 = __half2float(__ushort_as_half((uint16_t)(swa >> 16)));
+        s_b0 = __half2float(__ushort_as_half((uint16_t)(swb & 0xFFFFu))); s_b1 = __half2float(__ushort_as_half((uint16_t)(swb >> 16)));
+      }
+      constexpr uint32_t kMagic = 0x64006400u;
+      const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+      const uint32_t wb[4] = {cbv.x, cbv.y, cbv.z, cbv.w};
+      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t va8 = wa[i] >> 8, vb8 = wb[i] >> 8;
+        mma16816(t0, lop3_and_or(wa[i], 0x000F000Fu, kMagic), lop3_and_or(wb[i], 0x000F000Fu, kMagic),
+                 lop3_and_or(wa[i], 0x00F000F0u, kMagic), lop3_and_or(wb[i], 0x00F000F0u, kMagic),
+                 bw[4 * i], bw[4 * i + 1]);
+        mma16816(t1, lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
+                 lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
+                 bw[4 * i + 2], bw[4 * i + 3]);
+        mma16816(t0, ne_a, ne_b, no_a, no_b, bw[4 * i], bw[4 * i + 1]);
+        mma16816(t1, ne_a, ne_b, no_a, no_b, bw[4 * i + 2], bw[4 * i + 3]);
+      }
+      acc[0] = fmaf(s_a0, t0[0] + t1[0], acc[0]);
+      acc[1] = fmaf(s_a1, t0[1] + t1[1], acc[1]);
+      acc[2] = fmaf(s_b0, t0[2] + t1[2], acc[2]);
+      acc[3] = fmaf(s_b1, t0[3] + t1[3], acc[3]);
+    }
+    if (++slot == kTRing) { slot = 0; phase ^= 1u; }
+    ++cic;
+    if (cic < nq && f + 1 < total) continue;
+
+    // ---- this warp's part of the unit is done
+    const bool whole = first_cic == 0 && cic == nq;
+    bool last = true;
+    if (!whole) {
+      const int64_t ux = (int64_t)item * nq;
+      const int w0 = chunk_owner(ux, nw, cfull), w1 = chunk_owner(ux + nq - 1, nw, cfull);
+      float* part = ws.dsplit + ((size_t)wg * 2 + (item == item0 ? 0 : 1)) * 128;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) part[r * 32 + lane] = acc[r];
+      __syncwarp();
+      int old = 0;
+      if (lane == 0)
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(ws.dticket + item) : "memory");
+      old = __shfl_sync(0xffffffffu, old, 0);
+      last = old == w1 - w0;
+      if (last) {
+        if (lane == 0) ws.dticket[item] = 0;
+        __syncwarp();
+        const int hs0 = cfull * w0 / nw < ux ? 1 : 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          float v = 0.f;
+          for (int wk = w0; wk <= w1; ++wk) {
+            const int hs = wk == w0 ? hs0 : 0;
+            const float pk = wk == wg ? acc[r] : __ldcg(ws.dsplit + ((size_t)wk * 2 + hs) * 128 + r * 32 + lane);
+            v = wk == w0 ? pk : v + pk;
+          }
+          acc[r] = v;
+        }
+      }
+    }
+    if (last) {
+      const int row0 = (item % rgroups) * kRowsPerGroup;
+      float v_lo = acc[0] + acc[1];
+      float v_hi = acc[2] + acc[3];
+      v_lo += __shfl_xor_sync(0xffffffffu, v_lo, 1);
+      v_hi += __shfl_xor_sync(0xffffffffu, v_hi, 1);
+      const int n = c >> 1;
+      if constexpr (FC1) {
+        const float up_lo = __shfl_down_sync(0xffffffffu, v_lo, 4);
+        const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
+        if ((g & 1) == 0 && (c & 1) == 0 && n < cnt) {
+          const int pos = pos0 + n;
+          const float sigma = ws.tok_scale[n ? tok1 : tok0];
+          const float inv = 1.0f / sigma;
+          const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+          const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
+          const float h_hi = silu(v_hi * inv) * (up_hi * inv) * sigma * sigma;
+          ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
+              __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
+          ws.h16[(int64_t)pos * p.I + permuted_pos(j_hi, 8)] =
+              __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * 0.0625f : h_hi));
+        }
+      } else {
+        if ((c & 1) == 0 && n < cnt) {
+          const int rid = ws.sorted_route[pos0 + n];
+          const float inv = 1.0f / ws.tok_scale[rid / p.k];
+          const float fct = inv * inv * ws.topk_w[rid];
+          ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * fct;
+          ws.y[(int64_t)rid * p.H + row0 + g + 8] = v_hi * fct;
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[r] = 0.f;
+    if (cic == nq) { cic = 0; ++item; }
+    first_cic = cic;
+    fresh = true;
+  }
+}
+
+template <bool FC1, bool BF16S, bool HAS_ZP>
+cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, const CUtensorMap& tz,
+                              const CUtensorMap& ta, TmaDecodeArgs a, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t err = cudaFuncSetAttribute(decode_int4_tma_kernel<FC1, BF16S, HAS_ZP>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTSmem);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  const int64_t blocks = (int64_t)sm_count() * kTBlocksPerSm;
+  decode_int4_tma_kernel<FC1, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kTWarps, kTSmem, s>>>(tq, ts, tz, ta, a);
+  return cudaGetLastError();
+}
+
+// The tensor-copy variant applies when both matmuls' K are multiples of 256 and
+// the zero-point rows (if any) are a multiple of 16 bytes long.
+bool decode_tma_applies(const Problem& p, bool has_zp) {
+  if (!decode_int4_blockscaled(p) || p.H % kTChunkK || p.I % kTChunkK) return false;
+  return !has_zp || ((p.H / 32) % 16 == 0 && (p.I / 32) % 16 == 0);
+}
+
+template <bool FC1>
+cudaError_t launch_int4_tma(const uint8_t* q, const uint16_t* scales, const uint8_t* zp, const Problem& p,
+                            const Workspace& ws, cudaStream_t s) {
+  const int N = FC1 ? 2 * p.I : p.H, K = FC1 ? p.H : p.I;
+  const uint64_t rows = (uint64_t)p.E * N;
+  const uint16_t* act = FC1 ? ws.x16 : ws.h16;
+  const uint64_t arows = FC1 ? (uint64_t)p.T : (uint64_t)p.R();
+  CUtensorMap tq, ts, tz, ta;
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K / 2, rows, (uint64_t)K / 2, 64,
+                   kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)K / 32, rows, (uint64_t)K / 16, 8,
+                   kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT16, act, (uint64_t)K, arows, (uint64_t)K * 2, kTChunkK, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (zp) {
+    if (!make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT8, zp, (uint64_t)K / 32, rows, (uint64_t)K / 32, 16,
+                     kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    tz = ts;                                     // not read
+  }
+  TmaDecodeArgs a{N, K, p, ws};
+  const bool bf16 = p.dtype == QMOE_BF16;
+  if (bf16) return zp ? launch_int4_tma_t<FC1, true, true>(tq, ts, tz, ta, a, s)
+                      : launch_int4_tma_t<FC1, true, false>(tq, ts, tz, ta, a, s);
+  return zp ? launch_int4_tma_t<FC1, false, true>(tq, ts, tz, ta, a, s)
+            : launch_int4_tma_t<FC1, false, false>(tq, ts, tz, ta, a, s);
+}
+
+
 template <bool FC1>
 cudaError_t launch_int4_bs(DecodeArgs a, cudaStream_t s) {
   const int64_t blocks = decode_grid_blocks();
@@ -841,6 +1173,9 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
                         const uint8_t* zp, const Workspace& ws, cudaStream_t s) {
   const int64_t R = p.R();
   const int active_max = (int)(R < p.E ? R : p.E);
+  if (BITS == 4 && decode_tma_applies(p, zp != nullptr))
+    return fc1 ? launch_int4_tma<true>(q, static_cast<const uint16_t*>(scales), zp, p, ws, s)
+               : launch_int4_tma<false>(q, static_cast<const uint16_t*>(scales), zp, p, ws, s);
   if (BITS == 4 && decode_int4_blockscaled(p)) {
     DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
                  fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};

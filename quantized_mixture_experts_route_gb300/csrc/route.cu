@@ -49,7 +49,7 @@ __device__ __forceinline__ float warp_max_f(float v) {
 template <int PER_LANE>
 __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
                             const uint16_t* __restrict__ logits, const Workspace& ws, int64_t t,
-                            int x16_mode) {
+                            int x16_mode, int* s_idx = nullptr) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   const uint16_t* lrow = logits + t * E;
@@ -86,6 +86,7 @@ __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
   if (lane < k) {
     ws.topk_idx[t * k + lane] = my_e;
     ws.topk_w[t * k + lane] = expf(my_l - l0) / denom;
+    if (s_idx) s_idx[t * k + lane] = my_e;
   }
   if (x16_mode == kX16None) return;
 
@@ -316,7 +317,9 @@ __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(Problem p,
   scatter_routes(ws.topk_idx, r0, r1, p.E, base, warp_cnt, ws.sorted_route);
 }
 
-// Routing and grouping of a small batch (R <= kPermuteChunk) in one block.
+// Routing and grouping of a small batch (R <= kPermuteChunk) in one block. The
+// intermediate results (expert of each route, offsets, sorted order) stay in
+// shared memory, so no step waits on a global round trip of an earlier one.
 template <int PER_LANE>
 __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
     Problem p, const uint16_t* __restrict__ x, const uint16_t* __restrict__ logits, Workspace ws,
@@ -325,43 +328,42 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   int* hist = smem;                  // [E]
   int* warp_cnt = smem + p.E;        // [16][E]
   __shared__ int sh[32];
+  __shared__ int s_idx[kPermuteChunk];
+  __shared__ int s_sorted[kPermuteChunk];
   const int warps = blockDim.x >> 5;
   for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps)
-    route_token<PER_LANE>(p, x, logits, ws, t, x16_mode);
+    route_token<PER_LANE>(p, x, logits, ws, t, x16_mode, s_idx);
   for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int64_t R = p.R();
-  count_routes(ws.topk_idx, 0, R, hist);
+  const int R = (int)p.R();
+  count_routes(s_idx, 0, R, hist);
   __syncthreads();
   const int total = threadIdx.x < p.E ? hist[threadIdx.x] : 0;
   __syncthreads();
   finish_groups(p.E, total, ws, want_tiles != 0, sh, hist);  // hist now holds the bases
   __syncthreads();
-  scatter_routes(ws.topk_idx, 0, R, p.E, hist, warp_cnt, ws.sorted_route);
+  const int begin = threadIdx.x < p.E ? hist[threadIdx.x] : 0;
+  scatter_routes(s_idx, 0, R, p.E, hist, warp_cnt, s_sorted);   // ends with a block barrier
+  for (int i = threadIdx.x; i < R; i += blockDim.x) ws.sorted_route[i] = s_sorted[i];
   // decode table: one entry per (active expert, pair of its routes), so that a
   // decode work unit reaches its expert's rows and its tokens with one
   // independent load and always multiplies exactly one MMA column pair
   if (p.path != QMOE_PATH_DECODE) return;    // (block-uniform) R <= kDtabMax on this path
   for (int64_t i = threadIdx.x; i < ws.dunits_max; i += blockDim.x) ws.dticket[i] = 0;
-  __syncthreads();
-  const int n_active = ws.counters[0];
-  int e = 0, begin = 0, n_e = 0;
-  if ((int)threadIdx.x < n_active) {
-    e = ws.active[threadIdx.x];
-    begin = ws.offsets[e];
-    n_e = ws.offsets[e + 1] - begin;
-  }
+  // entries in ascending expert order (the order of the active-expert list)
+  const int n_e = total;
   int n_entries;
   const int first = block_exclusive_scan((n_e + 1) / 2, sh, &n_entries);
   for (int q = 0; 2 * q < n_e; ++q) {
     int32_t* d = ws.dtab + (first + q) * kDtabInts;
     const int cnt = n_e - 2 * q < 2 ? n_e - 2 * q : 2;
+    const int e = threadIdx.x;
     d[0] = e;
     d[1] = begin + 2 * q;
     d[2] = cnt;
     d[3] = 0;
-    d[4] = ws.sorted_route[begin + 2 * q] / p.k;
-    d[5] = cnt > 1 ? ws.sorted_route[begin + 2 * q + 1] / p.k : 0;
+    d[4] = s_sorted[begin + 2 * q] / p.k;
+    d[5] = cnt > 1 ? s_sorted[begin + 2 * q + 1] / p.k : 0;
     d[6] = 0;
     d[7] = 0;
   }

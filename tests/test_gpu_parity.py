@@ -105,6 +105,19 @@ def case(name):
     if name == "bs_crowded":
         return (Shape(T=8, H=384, inter=256, E=3, k=3, bits=4, block=32, dtype=BF16),
                 Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 48)
+    # tensor-copy decode kernel (K of both matmuls a multiple of 256)
+    if name == "tma_zp_fp16":
+        return (Shape(T=6, H=512, inter=512, E=5, k=3, bits=4, block=32, dtype=FP16),
+                Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, explicit_zp=True), 49)
+    if name == "tma_zp_bf16":
+        return (Shape(T=7, H=1024, inter=512, E=9, k=4, bits=4, block=32, dtype=BF16),
+                Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, explicit_zp=True), 50)
+    if name == "tma_small":
+        return (Shape(T=3, H=256, inter=256, E=4, k=2, bits=4, block=32, dtype=BF16),
+                Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 51)
+    if name == "tma_crowded_fp16":
+        return (Shape(T=8, H=768, inter=512, E=3, k=3, bits=4, block=32, dtype=FP16),
+                Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 52)
     if name == "wide_k":
         return (Shape(T=2, H=256, inter=128, E=64, k=32, bits=4, block=128, dtype=BF16),
                 Recipe(logit_std=0.5, scale_lo=0.005, scale_hi=0.02), 45)
@@ -113,7 +126,8 @@ def case(name):
 
 DECODE_CASES = ["tiny", "decode_T1", "decode_T2", "decode_T4", "decode_T8", "int3_b64_T1",
                 "int3_b64_T8", "int3_b128_T8", "int2_T8", "int4_zp_fp16", "int3_zp_small",
-                "int2_zp_small", "dense_E1_k1", "wide_k", "bs_small", "bs_zp_fp16", "bs_crowded"]
+                "int2_zp_small", "dense_E1_k1", "wide_k", "bs_small", "bs_zp_fp16", "bs_crowded",
+                "tma_zp_fp16", "tma_zp_bf16", "tma_small", "tma_crowded_fp16"]
 
 
 @pytest.mark.parametrize("name", DECODE_CASES)
