@@ -105,7 +105,7 @@ __device__ __forceinline__ uint32_t dq_pair(const PairWords<BITS>& w, int p, uin
 
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -800,7 +800,7 @@ constexpr int kTWarps = 8;
 constexpr int kTRing = 3;                          // chunks per warp: two in flight, one in use
 constexpr int kTChunkK = 256;
 constexpr int kTBlocksPerSm = 2;
-constexpr int kTMinPiece = 4;
+constexpr int kTMinPiece = 4;                      // chunks per warp at least
 constexpr int kTCode = 0;                          // [2 sub-chunks][16 rows][64 B]
 constexpr int kTScale = 2048;                      // [16 rows][8 scales]
 constexpr int kTZp = 2304;                         // [16 rows][16 zero points]
@@ -826,20 +826,23 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
   const int K = a.K, N = a.N;
-  const int nq = K / kTChunkK;
+  const int nq = K / kTChunkK;                   // chunks per unit
   const int rgroups = N / kRowsPerGroup;
-  const int items = ws.counters[3] * rgroups;
-  const int64_t cfull = (int64_t)items * nq;
+  const int cfull = ws.counters[3] * rgroups * nq;   // < 2^31: <= 256 entries x 1024 groups x 32 chunks
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
+  const int gw = gridDim.x * kTWarps;
   const int wg = blockIdx.x * kTWarps + warp;
-  const int64_t nw_cap = (cfull + kTMinPiece - 1) / kTMinPiece;
-  const int nw = (int)((int64_t)gridDim.x * kTWarps < nw_cap ? (int64_t)gridDim.x * kTWarps : nw_cap);
-  const int64_t x_begin = wg < nw ? cfull * wg / nw : 0, x_end = wg < nw ? cfull * (wg + 1) / nw : 0;
-  const int total = (int)(x_end - x_begin);
+  // equal pieces of L chunks (the last one shorter, none empty)
+  int L = (cfull + gw - 1) / gw;
+  if (L < kTMinPiece) L = kTMinPiece;
+  const int nw = (cfull + L - 1) / L;
+  const int x_begin = wg < nw ? wg * L : 0;
+  const int total = wg < nw ? min(x_begin + L, cfull) - x_begin : 0;
   const bool owner = (g & 3) == c;               // supplies activations for column g
   const int on = g >> 2;                         // owner lane's route within the pair
+  const int n = c >> 1;                          // route within the pair of this lane's D columns
 
   extern __shared__ __align__(16) uint8_t smem[];
   // bulk tensor copies land on 128-byte boundaries
@@ -854,52 +857,60 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   __syncthreads();
   if (total == 0) return;
 
-  const int item0 = (int)(x_begin / nq);
-  const int cic0 = (int)(x_begin - (int64_t)item0 * nq);
+  // unit = (decode-table entry ei, 16-row group rg); walked without divisions
+  const int item0 = x_begin / nq;
+  const int cic0 = x_begin - item0 * nq;
+  const int ei0 = item0 / rgroups, rg0 = item0 - ei0 * rgroups;
 
   // ---- issue side: lane 0 copies chunk f of the piece into slot f % kTRing
-  int p_item = item0, p_cic = cic0, p_row = 0, p_t0 = 0, p_t1 = 0, p_cnt = 0;
+  int p_ei = ei0, p_rg = rg0, p_cic = cic0, p_row = 0, p_t0 = 0, p_t1 = 0, p_cnt = 0;
   bool p_new = true;
-  int p_slot = 0;
+  uint32_t p_slot_s = ring_s, p_bar = bar_s;
   auto issue = [&]() {
     if (p_new) {
       p_new = false;
-      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (p_item / rgroups) * kDtabInts));
-      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (p_item / rgroups) * kDtabInts + 4));
-      p_row = d0.x * N + (p_item % rgroups) * kRowsPerGroup;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + p_ei * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + p_ei * kDtabInts + 4));
+      p_row = d0.x * N + p_rg * kRowsPerGroup;
       p_cnt = d0.z;
       p_t0 = FC1 ? d1.x : d0.y;
       p_t1 = FC1 ? d1.y : d0.y + 1;
     }
     if (lane == 0) {
-      const uint32_t d = ring_s + p_slot * kTSlot, bar = bar_s + 8 * p_slot;
       const int kx = p_cic * kTChunkK;
-      mbar_expect_tx(bar, 2048 + 256 + (HAS_ZP ? 256 : 0) + (p_cnt > 1 ? 1024 : 512));
-      tma_load_2d(d + kTCode, &tq, bar, kx / 2, p_row);
-      tma_load_2d(d + kTCode + 1024, &tq, bar, kx / 2 + 64, p_row);
-      tma_load_2d(d + kTScale, &ts, bar, kx / 32, p_row);
-      if constexpr (HAS_ZP) tma_load_2d(d + kTZp, &tz, bar, (kx / 32) & ~15, p_row);
-      tma_load_2d(d + kTAct0, &ta, bar, kx, p_t0);
-      if (p_cnt > 1) tma_load_2d(d + kTAct1, &ta, bar, kx, p_t1);
+      mbar_expect_tx(p_bar, 2048 + 256 + (HAS_ZP ? 256 : 0) + (p_cnt > 1 ? 1024 : 512));
+      tma_load_2d(p_slot_s + kTCode, &tq, p_bar, kx / 2, p_row);
+      tma_load_2d(p_slot_s + kTCode + 1024, &tq, p_bar, kx / 2 + 64, p_row);
+      tma_load_2d(p_slot_s + kTScale, &ts, p_bar, kx / 32, p_row);
+      if constexpr (HAS_ZP) tma_load_2d(p_slot_s + kTZp, &tz, p_bar, (kx / 32) & ~15, p_row);
+      tma_load_2d(p_slot_s + kTAct0, &ta, p_bar, kx, p_t0);
+      if (p_cnt > 1) tma_load_2d(p_slot_s + kTAct1, &ta, p_bar, kx, p_t1);
     }
-    p_slot = p_slot + 1 == kTRing ? 0 : p_slot + 1;
-    if (++p_cic == nq) { p_cic = 0; ++p_item; p_new = true; }
+    if (p_bar == bar_s + 8 * (kTRing - 1)) { p_bar = bar_s; p_slot_s = ring_s; }
+    else { p_bar += 8; p_slot_s += kTSlot; }
+    if (++p_cic == nq) {
+      p_cic = 0;
+      p_new = true;
+      if (++p_rg == rgroups) { p_rg = 0; ++p_ei; }
+    }
   };
-  const int pre = total < kTRing - 1 ? total : kTRing - 1;
-  for (int u = 0; u < pre; ++u) issue();
+  for (int u = 0; u < kTRing - 1 && u < total; ++u) issue();
 
   const __half2 ne_d = __float2half2_rn(-(1024.0f + 8.0f)), no_d = __float2half2_rn(-(1024.0f + 128.0f));
   const uint32_t ne_def = *reinterpret_cast<const uint32_t*>(&ne_d);
   const uint32_t no_def = *reinterpret_cast<const uint32_t*>(&no_d);
+  // per-lane shared-memory offsets within a slot (the rest are immediates)
+  const uint32_t code_off = lane * 16;
+  const uint32_t scale_off = kTScale + g * 16 + 4 * (c & 1);
   // activation words: owners read their token's tile, the other lanes the zero area
   const uint32_t act_base = owner ? ring_s + (on ? kTAct1 : kTAct0) + 64 * c : zero_s;
   const uint32_t act_slot_stride = owner ? kTSlot : 0;
 
   // ---- compute side
-  int item = item0, cic = cic0;
-  int first_cic = cic;
-  int cnt = 0, pos0 = 0, tok0 = 0, tok1 = 0;
-  bool fresh = true;
+  int ei = ei0, rg = rg0, cic = cic0, first_cic = cic0;
+  bool first_unit = true, fresh = true;
+  int cnt = 0, pos0 = 0, e_rid = 0;
+  float e_scale = 1.0f, e_w = 0.0f;              // epilogue operands of route n, loaded early
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   int slot = 0;
   uint32_t phase = 0;
@@ -908,14 +919,22 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
     if (f + kTRing - 1 < total) issue();
     if (fresh) {
       fresh = false;
-      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts));
-      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + (item / rgroups) * kDtabInts + 4));
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + ei * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + ei * kDtabInts + 4));
       pos0 = d0.y;
       cnt = d0.z;
-      tok0 = d1.x;
-      tok1 = d1.y;
+      if (n < cnt) {
+        if constexpr (FC1) {
+          e_scale = __ldg(ws.tok_scale + (n ? d1.y : d1.x));
+        } else {
+          e_rid = __ldg(ws.sorted_route + pos0 + n);
+          e_scale = __ldg(ws.tok_scale + e_rid / p.k);
+          e_w = __ldg(ws.topk_w + e_rid);
+        }
+      }
     }
-    if (!mbar_wait_for(bar_s + 8 * slot, phase, kTWaitNs)) {
+    const uint32_t bar = bar_s + 8 * slot;
+    if (!mbar_wait_for(bar, phase, kTWaitNs)) {
       // record the failure, let this warp's copies in flight land, and stop
       if (lane == 0) atomicExch(ws.counters + 2, kErrDecodeTimeout);
       int s2 = slot;
@@ -928,39 +947,88 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       return;
     }
     const uint32_t sb = ring_s + slot * kTSlot;
+    const uint32_t cb_ = sb + code_off, sr = sb + scale_off;
     const uint32_t ab = act_base + slot * act_slot_stride;
-    const uint32_t srow = sb + kTScale + g * 16 + 4 * (c & 1);
+    // both sub-chunks' operands first; then their MMAs as four independent
+    // accumulation chains (sub-chunk x even/odd step), interleaved
+    uint4 cw[2][2];
+    uint32_t sw[2][2];
+    uint32_t bw[2][16];
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(cw[0][0].x), "=r"(cw[0][0].y), "=r"(cw[0][0].z), "=r"(cw[0][0].w) : "r"(cb_));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+512];\n"
+                 : "=r"(cw[0][1].x), "=r"(cw[0][1].y), "=r"(cw[0][1].z), "=r"(cw[0][1].w) : "r"(cb_));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1024];\n"
+                 : "=r"(cw[1][0].x), "=r"(cw[1][0].y), "=r"(cw[1][0].z), "=r"(cw[1][0].w) : "r"(cb_));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1536];\n"
+                 : "=r"(cw[1][1].x), "=r"(cw[1][1].y), "=r"(cw[1][1].z), "=r"(cw[1][1].w) : "r"(cb_));
+    asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sw[0][0]) : "r"(sr));
+    asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(sw[0][1]) : "r"(sr));
+    asm volatile("ld.shared.u32 %0, [%1+8];\n" : "=r"(sw[1][0]) : "r"(sr));
+    asm volatile("ld.shared.u32 %0, [%1+136];\n" : "=r"(sw[1][1]) : "r"(sr));
+#define QMOE_LDS_ACT(SUB, J, OFF)                                                                  \
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+" #OFF "];\n"                                 \
+               : "=r"(bw[SUB][4 * J]), "=r"(bw[SUB][4 * J + 1]), "=r"(bw[SUB][4 * J + 2]),         \
+                 "=r"(bw[SUB][4 * J + 3])                                                          \
+               : "r"(ab))
+    QMOE_LDS_ACT(0, 0, 0);
+    QMOE_LDS_ACT(0, 1, 16);
+    QMOE_LDS_ACT(0, 2, 32);
+    QMOE_LDS_ACT(0, 3, 48);
+    QMOE_LDS_ACT(1, 0, 256);
+    QMOE_LDS_ACT(1, 1, 272);
+    QMOE_LDS_ACT(1, 2, 288);
+    QMOE_LDS_ACT(1, 3, 304);
+#undef QMOE_LDS_ACT
+    uint32_t ne_a[2], ne_b[2], no_a[2], no_b[2];
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {
-      uint4 ca, cbv;
-      uint32_t swa, swb;
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                   : "=r"(ca.x), "=r"(ca.y), "=r"(ca.z), "=r"(ca.w) : "r"(sb + sub * 1024 + lane * 16));
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                   : "=r"(cbv.x), "=r"(cbv.y), "=r"(cbv.z), "=r"(cbv.w) : "r"(sb + sub * 1024 + 512 + lane * 16));
-      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(swa) : "r"(srow + 8 * sub));
-      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(swb) : "r"(srow + 128 + 8 * sub));
-      uint32_t bw[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(bw[4 * j]), "=r"(bw[4 * j + 1]), "=r"(bw[4 * j + 2]), "=r"(bw[4 * j + 3])
-                     : "r"(ab + sub * 256 + 16 * j));
-      uint32_t ne_a = ne_def, ne_b = ne_def, no_a = no_def, no_b = no_def;
+      ne_a[sub] = ne_def; ne_b[sub] = ne_def; no_a[sub] = no_def; no_b[sub] = no_def;
       if constexpr (HAS_ZP) {
         uint32_t zwa, zwb;
         const uint32_t zrow = sb + kTZp + g * 16 + (cic & 1) * 8 + 4 * sub;
         asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(zwa) : "r"(zrow));
-        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(zwb) : "r"(zrow + 128));
+        asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(zwb) : "r"(zrow));
         const uint32_t za = (zwa >> (8 * c)) & 0xFFu, zb = (zwb >> (8 * c)) & 0xFFu;
         const __half2 h1 = __float2half2_rn(-(1024.0f + (float)za)), h2 = __float2half2_rn(-(1024.0f + 16.0f * (float)za));
         const __half2 h3 = __float2half2_rn(-(1024.0f + (float)zb)), h4 = __float2half2_rn(-(1024.0f + 16.0f * (float)zb));
-        ne_a = *reinterpret_cast<const uint32_t*>(&h1);
-        no_a = *reinterpret_cast<const uint32_t*>(&h2);
-        ne_b = *reinterpret_cast<const uint32_t*>(&h3);
-        no_b = *reinterpret_cast<const uint32_t*>(&h4);
+        ne_a[sub] = *reinterpret_cast<const uint32_t*>(&h1);
+        no_a[sub] = *reinterpret_cast<const uint32_t*>(&h2);
+        ne_b[sub] = *reinterpret_cast<const uint32_t*>(&h3);
+        no_b[sub] = *reinterpret_cast<const uint32_t*>(&h4);
       }
+    }
+    constexpr uint32_t kMagic = 0x64006400u;
+    float t[2][2][4];
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) t[sub][q][e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const uint32_t wa = (&cw[sub][0].x)[i], wb = (&cw[sub][1].x)[i];
+        const uint32_t va8 = wa >> 8, vb8 = wb >> 8;
+        mma16816(t[sub][0], lop3_and_or(wa, 0x000F000Fu, kMagic), lop3_and_or(wb, 0x000F000Fu, kMagic),
+                 lop3_and_or(wa, 0x00F000F0u, kMagic), lop3_and_or(wb, 0x00F000F0u, kMagic),
+                 bw[sub][4 * i], bw[sub][4 * i + 1]);
+        mma16816(t[sub][1], lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
+                 lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
+                 bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+      }
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        mma16816(t[sub][0], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i], bw[sub][4 * i + 1]);
+        mma16816(t[sub][1], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+      }
+    }
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
       float s_a0, s_a1, s_b0, s_b1;
+      const uint32_t swa = sw[sub][0], swb = sw[sub][1];
       if constexpr (BF16S) {
         s_a0 = __uint_as_float(swa << 16); s_a1 = __uint_as_float(swa & 0xFFFF0000u);
         s_b0 = __uint_as_float(swb << 16); s_b1 = __uint_as_float(swb & 0xFFFF0000u);
@@ -968,50 +1036,42 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
         s_a0 = __half2float(__ushort_as_half((uint16_t)(swa & 0xFFFFu))); s_a1 = __half2float(__ushort_as_half((uint16_t)(swa >> 16)));
         s_b0 = __half2float(__ushort_as_half((uint16_t)(swb & 0xFFFFu))); s_b1 = __half2float(__ushort_as_half((uint16_t)(swb >> 16)));
       }
-      constexpr uint32_t kMagic = 0x64006400u;
-      const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-      const uint32_t wb[4] = {cbv.x, cbv.y, cbv.z, cbv.w};
-      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t va8 = wa[i] >> 8, vb8 = wb[i] >> 8;
-        mma16816(t0, lop3_and_or(wa[i], 0x000F000Fu, kMagic), lop3_and_or(wb[i], 0x000F000Fu, kMagic),
-                 lop3_and_or(wa[i], 0x00F000F0u, kMagic), lop3_and_or(wb[i], 0x00F000F0u, kMagic),
-                 bw[4 * i], bw[4 * i + 1]);
-        mma16816(t1, lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
-                 lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
-                 bw[4 * i + 2], bw[4 * i + 3]);
-        mma16816(t0, ne_a, ne_b, no_a, no_b, bw[4 * i], bw[4 * i + 1]);
-        mma16816(t1, ne_a, ne_b, no_a, no_b, bw[4 * i + 2], bw[4 * i + 3]);
-      }
-      acc[0] = fmaf(s_a0, t0[0] + t1[0], acc[0]);
-      acc[1] = fmaf(s_a1, t0[1] + t1[1], acc[1]);
-      acc[2] = fmaf(s_b0, t0[2] + t1[2], acc[2]);
-      acc[3] = fmaf(s_b1, t0[3] + t1[3], acc[3]);
+      acc[0] = fmaf(s_a0, t[sub][0][0] + t[sub][1][0], acc[0]);
+      acc[1] = fmaf(s_a1, t[sub][0][1] + t[sub][1][1], acc[1]);
+      acc[2] = fmaf(s_b0, t[sub][0][2] + t[sub][1][2], acc[2]);
+      acc[3] = fmaf(s_b1, t[sub][0][3] + t[sub][1][3], acc[3]);
     }
     if (++slot == kTRing) { slot = 0; phase ^= 1u; }
-    ++cic;
-    if (cic < nq && f + 1 < total) continue;
+    if (++cic < nq && f + 1 < total) continue;
 
     // ---- this warp's part of the unit is done
     const bool whole = first_cic == 0 && cic == nq;
     bool last = true;
     if (!whole) {
-      const int64_t ux = (int64_t)item * nq;
-      const int w0 = chunk_owner(ux, nw, cfull), w1 = chunk_owner(ux + nq - 1, nw, cfull);
-      float* part = ws.dsplit + ((size_t)wg * 2 + (item == item0 ? 0 : 1)) * 128;
+      // parts of this unit: the warps owning its first and last chunk, and those between
+      const int item = ei * rgroups + rg;
+      const int ux = item * nq;
+      const int w0 = ux / L, w1 = (ux + nq - 1) / L;
+      // partial slot 0: the piece's first unit; slot 1: its last unit
+      float* part = ws.dsplit + ((size_t)wg * 2 + (first_unit ? 0 : 1)) * 128;
 #pragma unroll
       for (int r = 0; r < 4; ++r) part[r * 32 + lane] = acc[r];
       __syncwarp();
       int old = 0;
-      if (lane == 0)
+      if (lane == 0) {
+        // release: the warp's partial tile is visible before the ticket moves;
+        // acquire: the other parts' tiles are visible to the last arriver
         asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(ws.dticket + item) : "memory");
+      }
       old = __shfl_sync(0xffffffffu, old, 0);
       last = old == w1 - w0;
       if (last) {
-        if (lane == 0) ws.dticket[item] = 0;
+        if (lane == 0) ws.dticket[item] = 0;    // free again for fc2 and the next call
         __syncwarp();
-        const int hs0 = cfull * w0 / nw < ux ? 1 : 0;
+        // parts added in chunk order: warps w0 .. w1. Warp w0's piece may begin
+        // before the unit (the unit is then its last, slot 1); every later
+        // warp's piece begins inside it (slot 0).
+        const int hs0 = w0 * L < ux ? 1 : 0;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           float v = 0.f;
@@ -1025,22 +1085,22 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       }
     }
     if (last) {
-      const int row0 = (item % rgroups) * kRowsPerGroup;
+      const int row0 = rg * kRowsPerGroup;
       float v_lo = acc[0] + acc[1];
       float v_hi = acc[2] + acc[3];
       v_lo += __shfl_xor_sync(0xffffffffu, v_lo, 1);
       v_hi += __shfl_xor_sync(0xffffffffu, v_hi, 1);
-      const int n = c >> 1;
       if constexpr (FC1) {
         const float up_lo = __shfl_down_sync(0xffffffffu, v_lo, 4);
         const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
         if ((g & 1) == 0 && (c & 1) == 0 && n < cnt) {
           const int pos = pos0 + n;
-          const float sigma = ws.tok_scale[n ? tok1 : tok0];
+          const float sigma = e_scale;
           const float inv = 1.0f / sigma;
           const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
           const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
           const float h_hi = silu(v_hi * inv) * (up_hi * inv) * sigma * sigma;
+          // fc2 reads these as activations: odd K positions carry 1/16
           ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
               __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
           ws.h16[(int64_t)pos * p.I + permuted_pos(j_hi, 8)] =
@@ -1048,18 +1108,21 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
         }
       } else {
         if ((c & 1) == 0 && n < cnt) {
-          const int rid = ws.sorted_route[pos0 + n];
-          const float inv = 1.0f / ws.tok_scale[rid / p.k];
-          const float fct = inv * inv * ws.topk_w[rid];
-          ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * fct;
-          ws.y[(int64_t)rid * p.H + row0 + g + 8] = v_hi * fct;
+          const float inv = 1.0f / e_scale;
+          const float fct = inv * inv * e_w;
+          ws.y[(int64_t)e_rid * p.H + row0 + g] = v_lo * fct;
+          ws.y[(int64_t)e_rid * p.H + row0 + g + 8] = v_hi * fct;
         }
       }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[r] = 0.f;
-    if (cic == nq) { cic = 0; ++item; }
+    if (cic == nq) {
+      cic = 0;
+      if (++rg == rgroups) { rg = 0; ++ei; }
+    }
     first_cic = cic;
+    first_unit = false;
     fresh = true;
   }
 }
