@@ -789,7 +789,7 @@ int64_t decode_grid_blocks() { return (int64_t)sm_count() * kBlocksPerSmB; }
 // INT4, block 32, K a multiple of 256: the same per-chunk arithmetic as above,
 // with the operands brought in by the tensor-memory-access unit. Lane 0 of each
 // warp issues, per 256-wide K chunk of a unit, four or five bulk tensor copies
-// (codes as two [16 rows][64 B] boxes, the [16 rows][8] block scales, the
+// (codes as one [16 rows][128 B] box, the [16 rows][8] block scales, the
 // chunk's activations of one or two tokens, the zero points when present) into
 // the warp's ring slot, completing on the slot's mbarrier; the other lanes only
 // wait on the barrier and read shared memory. Lanes that supply no activations
@@ -801,7 +801,7 @@ constexpr int kTRing = 3;                          // chunks per warp: two in fl
 constexpr int kTChunkK = 256;
 constexpr int kTBlocksPerSm = 2;
 constexpr int kTMinPiece = 4;                      // chunks per warp at least
-constexpr int kTCode = 0;                          // [2 sub-chunks][16 rows][64 B]
+constexpr int kTCode = 0;                          // [16 rows][128 B]: sub-chunk s at byte 64 s
 constexpr int kTScale = 2048;                      // [16 rows][8 scales]
 constexpr int kTZp = 2304;                         // [16 rows][16 zero points]
 constexpr int kTAct0 = 2560;                       // [256] FP16, first route's token
@@ -880,7 +880,6 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       const int kx = p_cic * kTChunkK;
       mbar_expect_tx(p_bar, 2048 + 256 + (HAS_ZP ? 256 : 0) + (p_cnt > 1 ? 1024 : 512));
       tma_load_2d(p_slot_s + kTCode, &tq, p_bar, kx / 2, p_row);
-      tma_load_2d(p_slot_s + kTCode + 1024, &tq, p_bar, kx / 2 + 64, p_row);
       tma_load_2d(p_slot_s + kTScale, &ts, p_bar, kx / 32, p_row);
       if constexpr (HAS_ZP) tma_load_2d(p_slot_s + kTZp, &tz, p_bar, (kx / 32) & ~15, p_row);
       tma_load_2d(p_slot_s + kTAct0, &ta, p_bar, kx, p_t0);
@@ -900,7 +899,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   const uint32_t ne_def = *reinterpret_cast<const uint32_t*>(&ne_d);
   const uint32_t no_def = *reinterpret_cast<const uint32_t*>(&no_d);
   // per-lane shared-memory offsets within a slot (the rest are immediates)
-  const uint32_t code_off = lane * 16;
+  const uint32_t code_off = g * 128 + c * 16;   // row g of the [16][128 B] code tile
   const uint32_t scale_off = kTScale + g * 16 + 4 * (c & 1);
   // activation words: owners read their token's tile, the other lanes the zero area
   const uint32_t act_base = owner ? ring_s + (on ? kTAct1 : kTAct0) + 64 * c : zero_s;
@@ -956,11 +955,11 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
     uint32_t bw[2][16];
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(cw[0][0].x), "=r"(cw[0][0].y), "=r"(cw[0][0].z), "=r"(cw[0][0].w) : "r"(cb_));
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+512];\n"
-                 : "=r"(cw[0][1].x), "=r"(cw[0][1].y), "=r"(cw[0][1].z), "=r"(cw[0][1].w) : "r"(cb_));
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1024];\n"
+                 : "=r"(cw[0][1].x), "=r"(cw[0][1].y), "=r"(cw[0][1].z), "=r"(cw[0][1].w) : "r"(cb_));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+64];\n"
                  : "=r"(cw[1][0].x), "=r"(cw[1][0].y), "=r"(cw[1][0].z), "=r"(cw[1][0].w) : "r"(cb_));
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1536];\n"
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1088];\n"
                  : "=r"(cw[1][1].x), "=r"(cw[1][1].y), "=r"(cw[1][1].z), "=r"(cw[1][1].w) : "r"(cb_));
     asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sw[0][0]) : "r"(sr));
     asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(sw[0][1]) : "r"(sr));
@@ -1157,7 +1156,7 @@ cudaError_t launch_int4_tma(const uint8_t* q, const uint16_t* scales, const uint
   const uint16_t* act = FC1 ? ws.x16 : ws.h16;
   const uint64_t arows = FC1 ? (uint64_t)p.T : (uint64_t)p.R();
   CUtensorMap tq, ts, tz, ta;
-  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K / 2, rows, (uint64_t)K / 2, 64,
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K / 2, rows, (uint64_t)K / 2, 128,
                    kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)K / 32, rows, (uint64_t)K / 16, 8,
                    kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE) ||
