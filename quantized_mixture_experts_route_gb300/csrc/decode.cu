@@ -797,21 +797,34 @@ int64_t decode_grid_blocks() { return (int64_t)sm_count() * kBlocksPerSmB; }
 // those of the kernel above, with 256-wide chunks.
 // ---------------------------------------------------------------------------
 constexpr int kTWarps = 8;
-constexpr int kTRing = 3;                          // chunks per warp: two in flight, one in use
 constexpr int kTChunkK = 256;
 constexpr int kTBlocksPerSm = 2;
 constexpr int kTMinPiece = 4;                      // chunks per warp at least
-constexpr int kTCode = 0;                          // [16 rows][128 B]: sub-chunk s at byte 64 s
-constexpr int kTScale = 2048;                      // [16 rows][8 scales]
-constexpr int kTZp = 2304;                         // [16 rows][16 zero points]
-constexpr int kTAct0 = 2560;                       // [256] FP16, first route's token
-constexpr int kTAct1 = 3072;                       // [256] FP16, second route's token
-constexpr int kTSlot = 3584;                       // every part 128-byte aligned
 constexpr int kTZero = 512;                        // zero bytes read by non-supplying lanes
-constexpr size_t kTSmem = (size_t)kTWarps * kTRing * kTSlot + kTZero + kTWarps * kTRing * 8 + 128;
 constexpr uint64_t kTWaitNs = 1000000000ull;      // 1 s: far beyond any legitimate wait
 constexpr uint64_t kTDrainNs = 100000000ull;
 constexpr int kErrDecodeTimeout = 2;
+
+// Unit height: 16 rows (one MMA M-fragment) or 32 rows (two, sharing each
+// chunk's activations: fewer instructions per weight byte, but longer units and
+// a shallower ring in the same shared memory). Slot layout, every part 128-byte
+// aligned: codes [ROWS][128 B] (sub-chunk s at byte 64 s), scales [ROWS][8],
+// zero points [ROWS][16], activations of the pair's two tokens [256] FP16 each.
+template <int ROWS>
+struct TCfg {
+  static constexpr int kRows = ROWS;
+  static constexpr int kHalves = ROWS / 16;
+  static constexpr int kRing = ROWS == 32 ? 2 : 3;   // chunks per warp: kRing - 1 in flight, one in use
+  static constexpr int kCode = 0;
+  static constexpr int kScale = ROWS * 128;
+  static constexpr int kZp = kScale + ROWS * 16;
+  static constexpr int kAct0 = kZp + ROWS * 16;
+  static constexpr int kAct1 = kAct0 + 512;
+  static constexpr int kSlot = kAct1 + 512;
+  static constexpr int kPart = kHalves * 4 * 32;      // FP32 partial tile of one unit
+  static constexpr size_t kSmem = (size_t)kTWarps * kRing * kSlot + kTZero + kTWarps * kRing * 8 + 128;
+};
+constexpr int kTPartMax = TCfg<32>::kPart;
 
 struct TmaDecodeArgs {
   int N, K;
@@ -819,16 +832,17 @@ struct TmaDecodeArgs {
   Workspace ws;
 };
 
-template <bool FC1, bool BF16S, bool HAS_ZP>
+template <int ROWS, bool FC1, bool BF16S, bool HAS_ZP>
 __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ts,
     const __grid_constant__ CUtensorMap tz, const __grid_constant__ CUtensorMap ta, TmaDecodeArgs a) {
+  using C = TCfg<ROWS>;
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
   const int K = a.K, N = a.N;
   const int nq = K / kTChunkK;                   // chunks per unit
-  const int rgroups = N / kRowsPerGroup;
-  const int cfull = ws.counters[3] * rgroups * nq;   // < 2^31: <= 256 entries x 1024 groups x 32 chunks
+  const int rgroups = N / C::kRows;
+  const int cfull = ws.counters[3] * rgroups * nq;   // < 2^31: <= 256 entries x 512 groups x 32 chunks
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -847,22 +861,22 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   extern __shared__ __align__(16) uint8_t smem[];
   // bulk tensor copies land on 128-byte boundaries
   uint8_t* base = smem + ((128u - (smem_u32(smem) & 127u)) & 127u);
-  const uint32_t ring_s = smem_u32(base) + warp * (kTRing * kTSlot);
-  const uint32_t zero_s = smem_u32(base) + kTWarps * kTRing * kTSlot;
-  const uint32_t bar_s = zero_s + kTZero + warp * (kTRing * 8);
-  if (threadIdx.x < kTZero / 4) reinterpret_cast<uint32_t*>(base + kTWarps * kTRing * kTSlot)[threadIdx.x] = 0u;
+  const uint32_t ring_s = smem_u32(base) + warp * (C::kRing * C::kSlot);
+  const uint32_t zero_s = smem_u32(base) + kTWarps * C::kRing * C::kSlot;
+  const uint32_t bar_s = zero_s + kTZero + warp * (C::kRing * 8);
+  if (threadIdx.x < kTZero / 4) reinterpret_cast<uint32_t*>(base + kTWarps * C::kRing * C::kSlot)[threadIdx.x] = 0u;
   if (lane == 0)
-    for (int s = 0; s < kTRing; ++s) mbar_init(bar_s + 8 * s, 1);
+    for (int s = 0; s < C::kRing; ++s) mbar_init(bar_s + 8 * s, 1);
   mbar_init_fence();
   __syncthreads();
   if (total == 0) return;
 
-  // unit = (decode-table entry ei, 16-row group rg); walked without divisions
+  // unit = (decode-table entry ei, 32-row group rg); walked without divisions
   const int item0 = x_begin / nq;
   const int cic0 = x_begin - item0 * nq;
   const int ei0 = item0 / rgroups, rg0 = item0 - ei0 * rgroups;
 
-  // ---- issue side: lane 0 copies chunk f of the piece into slot f % kTRing
+  // ---- issue side: lane 0 copies chunk f of the piece into slot f % C::kRing
   int p_ei = ei0, p_rg = rg0, p_cic = cic0, p_row = 0, p_t0 = 0, p_t1 = 0, p_cnt = 0;
   bool p_new = true;
   uint32_t p_slot_s = ring_s, p_bar = bar_s;
@@ -871,51 +885,55 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       p_new = false;
       const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + p_ei * kDtabInts));
       const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + p_ei * kDtabInts + 4));
-      p_row = d0.x * N + p_rg * kRowsPerGroup;
+      p_row = d0.x * N + p_rg * C::kRows;
       p_cnt = d0.z;
       p_t0 = FC1 ? d1.x : d0.y;
       p_t1 = FC1 ? d1.y : d0.y + 1;
     }
     if (lane == 0) {
       const int kx = p_cic * kTChunkK;
-      mbar_expect_tx(p_bar, 2048 + 256 + (HAS_ZP ? 256 : 0) + (p_cnt > 1 ? 1024 : 512));
-      tma_load_2d(p_slot_s + kTCode, &tq, p_bar, kx / 2, p_row);
-      tma_load_2d(p_slot_s + kTScale, &ts, p_bar, kx / 32, p_row);
-      if constexpr (HAS_ZP) tma_load_2d(p_slot_s + kTZp, &tz, p_bar, (kx / 32) & ~15, p_row);
-      tma_load_2d(p_slot_s + kTAct0, &ta, p_bar, kx, p_t0);
-      if (p_cnt > 1) tma_load_2d(p_slot_s + kTAct1, &ta, p_bar, kx, p_t1);
+      mbar_expect_tx(p_bar, ROWS * 128 + ROWS * 16 + (HAS_ZP ? ROWS * 16 : 0) + (p_cnt > 1 ? 1024 : 512));
+      tma_load_2d(p_slot_s + C::kCode, &tq, p_bar, kx / 2, p_row);
+      tma_load_2d(p_slot_s + C::kScale, &ts, p_bar, kx / 32, p_row);
+      if constexpr (HAS_ZP) tma_load_2d(p_slot_s + C::kZp, &tz, p_bar, (kx / 32) & ~15, p_row);
+      tma_load_2d(p_slot_s + C::kAct0, &ta, p_bar, kx, p_t0);
+      if (p_cnt > 1) tma_load_2d(p_slot_s + C::kAct1, &ta, p_bar, kx, p_t1);
     }
-    if (p_bar == bar_s + 8 * (kTRing - 1)) { p_bar = bar_s; p_slot_s = ring_s; }
-    else { p_bar += 8; p_slot_s += kTSlot; }
+    if (p_bar == bar_s + 8 * (C::kRing - 1)) { p_bar = bar_s; p_slot_s = ring_s; }
+    else { p_bar += 8; p_slot_s += C::kSlot; }
     if (++p_cic == nq) {
       p_cic = 0;
       p_new = true;
       if (++p_rg == rgroups) { p_rg = 0; ++p_ei; }
     }
   };
-  for (int u = 0; u < kTRing - 1 && u < total; ++u) issue();
+  for (int u = 0; u < C::kRing - 1 && u < total; ++u) issue();
 
   const __half2 ne_d = __float2half2_rn(-(1024.0f + 8.0f)), no_d = __float2half2_rn(-(1024.0f + 128.0f));
   const uint32_t ne_def = *reinterpret_cast<const uint32_t*>(&ne_d);
   const uint32_t no_def = *reinterpret_cast<const uint32_t*>(&no_d);
   // per-lane shared-memory offsets within a slot (the rest are immediates)
   const uint32_t code_off = g * 128 + c * 16;   // row g of the [16][128 B] code tile
-  const uint32_t scale_off = kTScale + g * 16 + 4 * (c & 1);
+  const uint32_t scale_off = C::kScale + g * 16 + 4 * (c & 1);
   // activation words: owners read their token's tile, the other lanes the zero area
-  const uint32_t act_base = owner ? ring_s + (on ? kTAct1 : kTAct0) + 64 * c : zero_s;
-  const uint32_t act_slot_stride = owner ? kTSlot : 0;
+  const uint32_t act_base = owner ? ring_s + (on ? C::kAct1 : C::kAct0) + 64 * c : zero_s;
+  const uint32_t act_slot_stride = owner ? C::kSlot : 0;
 
   // ---- compute side
   int ei = ei0, rg = rg0, cic = cic0, first_cic = cic0;
   bool first_unit = true, fresh = true;
   int cnt = 0, pos0 = 0, e_rid = 0;
   float e_scale = 1.0f, e_w = 0.0f;              // epilogue operands of route n, loaded early
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[C::kHalves][4];                    // [row half][D fragment]
+#pragma unroll
+  for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[rh][r] = 0.f;
   int slot = 0;
   uint32_t phase = 0;
   for (int f = 0; f < total; ++f) {
     __syncwarp();                                // every lane is done with the slot refilled next
-    if (f + kTRing - 1 < total) issue();
+    if (f + C::kRing - 1 < total) issue();
     if (fresh) {
       fresh = false;
       const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + ei * kDtabInts));
@@ -938,33 +956,17 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       if (lane == 0) atomicExch(ws.counters + 2, kErrDecodeTimeout);
       int s2 = slot;
       uint32_t ph2 = phase;
-      const int inflight = total - f < kTRing ? total - f : kTRing;   // chunks f .. f + kTRing - 1
+      const int inflight = total - f < C::kRing ? total - f : C::kRing;   // chunks f .. f + C::kRing - 1
       for (int u = 0; u < inflight; ++u) {
         mbar_wait_for(bar_s + 8 * s2, ph2, kTDrainNs);
-        if (++s2 == kTRing) { s2 = 0; ph2 ^= 1u; }
+        if (++s2 == C::kRing) { s2 = 0; ph2 ^= 1u; }
       }
       return;
     }
-    const uint32_t sb = ring_s + slot * kTSlot;
-    const uint32_t cb_ = sb + code_off, sr = sb + scale_off;
+    const uint32_t sb = ring_s + slot * C::kSlot;
     const uint32_t ab = act_base + slot * act_slot_stride;
-    // both sub-chunks' operands first; then their MMAs as four independent
-    // accumulation chains (sub-chunk x even/odd step), interleaved
-    uint4 cw[2][2];
-    uint32_t sw[2][2];
+    // the activations (B fragments) of both sub-chunks serve both 16-row halves
     uint32_t bw[2][16];
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(cw[0][0].x), "=r"(cw[0][0].y), "=r"(cw[0][0].z), "=r"(cw[0][0].w) : "r"(cb_));
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1024];\n"
-                 : "=r"(cw[0][1].x), "=r"(cw[0][1].y), "=r"(cw[0][1].z), "=r"(cw[0][1].w) : "r"(cb_));
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+64];\n"
-                 : "=r"(cw[1][0].x), "=r"(cw[1][0].y), "=r"(cw[1][0].z), "=r"(cw[1][0].w) : "r"(cb_));
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1088];\n"
-                 : "=r"(cw[1][1].x), "=r"(cw[1][1].y), "=r"(cw[1][1].z), "=r"(cw[1][1].w) : "r"(cb_));
-    asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sw[0][0]) : "r"(sr));
-    asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(sw[0][1]) : "r"(sr));
-    asm volatile("ld.shared.u32 %0, [%1+8];\n" : "=r"(sw[1][0]) : "r"(sr));
-    asm volatile("ld.shared.u32 %0, [%1+136];\n" : "=r"(sw[1][1]) : "r"(sr));
 #define QMOE_LDS_ACT(SUB, J, OFF)                                                                  \
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+" #OFF "];\n"                                 \
                : "=r"(bw[SUB][4 * J]), "=r"(bw[SUB][4 * J + 1]), "=r"(bw[SUB][4 * J + 2]),         \
@@ -979,68 +981,86 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
     QMOE_LDS_ACT(1, 2, 288);
     QMOE_LDS_ACT(1, 3, 304);
 #undef QMOE_LDS_ACT
-    uint32_t ne_a[2], ne_b[2], no_a[2], no_b[2];
 #pragma unroll
-    for (int sub = 0; sub < 2; ++sub) {
-      ne_a[sub] = ne_def; ne_b[sub] = ne_def; no_a[sub] = no_def; no_b[sub] = no_def;
-      if constexpr (HAS_ZP) {
-        uint32_t zwa, zwb;
-        const uint32_t zrow = sb + kTZp + g * 16 + (cic & 1) * 8 + 4 * sub;
-        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(zwa) : "r"(zrow));
-        asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(zwb) : "r"(zrow));
-        const uint32_t za = (zwa >> (8 * c)) & 0xFFu, zb = (zwb >> (8 * c)) & 0xFFu;
-        const __half2 h1 = __float2half2_rn(-(1024.0f + (float)za)), h2 = __float2half2_rn(-(1024.0f + 16.0f * (float)za));
-        const __half2 h3 = __float2half2_rn(-(1024.0f + (float)zb)), h4 = __float2half2_rn(-(1024.0f + 16.0f * (float)zb));
-        ne_a[sub] = *reinterpret_cast<const uint32_t*>(&h1);
-        no_a[sub] = *reinterpret_cast<const uint32_t*>(&h2);
-        ne_b[sub] = *reinterpret_cast<const uint32_t*>(&h3);
-        no_b[sub] = *reinterpret_cast<const uint32_t*>(&h4);
-      }
-    }
-    constexpr uint32_t kMagic = 0x64006400u;
-    float t[2][2][4];
-#pragma unroll
-    for (int sub = 0; sub < 2; ++sub)
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) t[sub][q][e] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int rh = 0; rh < C::kHalves; ++rh) {
+      const uint32_t cb_ = sb + code_off + rh * 2048, sr = sb + scale_off + rh * 256;   // rows 16 rh ..
+      uint4 cw[2][2];
+      uint32_t sw[2][2];
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                   : "=r"(cw[0][0].x), "=r"(cw[0][0].y), "=r"(cw[0][0].z), "=r"(cw[0][0].w) : "r"(cb_));
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1024];\n"
+                   : "=r"(cw[0][1].x), "=r"(cw[0][1].y), "=r"(cw[0][1].z), "=r"(cw[0][1].w) : "r"(cb_));
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+64];\n"
+                   : "=r"(cw[1][0].x), "=r"(cw[1][0].y), "=r"(cw[1][0].z), "=r"(cw[1][0].w) : "r"(cb_));
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1088];\n"
+                   : "=r"(cw[1][1].x), "=r"(cw[1][1].y), "=r"(cw[1][1].z), "=r"(cw[1][1].w) : "r"(cb_));
+      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sw[0][0]) : "r"(sr));
+      asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(sw[0][1]) : "r"(sr));
+      asm volatile("ld.shared.u32 %0, [%1+8];\n" : "=r"(sw[1][0]) : "r"(sr));
+      asm volatile("ld.shared.u32 %0, [%1+136];\n" : "=r"(sw[1][1]) : "r"(sr));
+      uint32_t ne_a[2], ne_b[2], no_a[2], no_b[2];
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
-        const uint32_t wa = (&cw[sub][0].x)[i], wb = (&cw[sub][1].x)[i];
-        const uint32_t va8 = wa >> 8, vb8 = wb >> 8;
-        mma16816(t[sub][0], lop3_and_or(wa, 0x000F000Fu, kMagic), lop3_and_or(wb, 0x000F000Fu, kMagic),
-                 lop3_and_or(wa, 0x00F000F0u, kMagic), lop3_and_or(wb, 0x00F000F0u, kMagic),
-                 bw[sub][4 * i], bw[sub][4 * i + 1]);
-        mma16816(t[sub][1], lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
-                 lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
-                 bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+        ne_a[sub] = ne_def; ne_b[sub] = ne_def; no_a[sub] = no_def; no_b[sub] = no_def;
+        if constexpr (HAS_ZP) {
+          uint32_t zwa, zwb;
+          const uint32_t zrow = sb + C::kZp + (rh * 16 + g) * 16 + (cic & 1) * 8 + 4 * sub;
+          asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(zwa) : "r"(zrow));
+          asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(zwb) : "r"(zrow));
+          const uint32_t za = (zwa >> (8 * c)) & 0xFFu, zb = (zwb >> (8 * c)) & 0xFFu;
+          const __half2 h1 = __float2half2_rn(-(1024.0f + (float)za)), h2 = __float2half2_rn(-(1024.0f + 16.0f * (float)za));
+          const __half2 h3 = __float2half2_rn(-(1024.0f + (float)zb)), h4 = __float2half2_rn(-(1024.0f + 16.0f * (float)zb));
+          ne_a[sub] = *reinterpret_cast<const uint32_t*>(&h1);
+          no_a[sub] = *reinterpret_cast<const uint32_t*>(&h2);
+          ne_b[sub] = *reinterpret_cast<const uint32_t*>(&h3);
+          no_b[sub] = *reinterpret_cast<const uint32_t*>(&h4);
+        }
+      }
+      constexpr uint32_t kMagic = 0x64006400u;
+      float t[2][2][4];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) t[sub][q][e] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const uint32_t wa = (&cw[sub][0].x)[i], wb = (&cw[sub][1].x)[i];
+          const uint32_t va8 = wa >> 8, vb8 = wb >> 8;
+          mma16816(t[sub][0], lop3_and_or(wa, 0x000F000Fu, kMagic), lop3_and_or(wb, 0x000F000Fu, kMagic),
+                   lop3_and_or(wa, 0x00F000F0u, kMagic), lop3_and_or(wb, 0x00F000F0u, kMagic),
+                   bw[sub][4 * i], bw[sub][4 * i + 1]);
+          mma16816(t[sub][1], lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
+                   lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
+                   bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+        }
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          mma16816(t[sub][0], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i], bw[sub][4 * i + 1]);
+          mma16816(t[sub][1], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+        }
       }
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
-        mma16816(t[sub][0], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i], bw[sub][4 * i + 1]);
-        mma16816(t[sub][1], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+        float s_a0, s_a1, s_b0, s_b1;
+        const uint32_t swa = sw[sub][0], swb = sw[sub][1];
+        if constexpr (BF16S) {
+          s_a0 = __uint_as_float(swa << 16); s_a1 = __uint_as_float(swa & 0xFFFF0000u);
+          s_b0 = __uint_as_float(swb << 16); s_b1 = __uint_as_float(swb & 0xFFFF0000u);
+        } else {
+          s_a0 = __half2float(__ushort_as_half((uint16_t)(swa & 0xFFFFu))); s_a1 = __half2float(__ushort_as_half((uint16_t)(swa >> 16)));
+          s_b0 = __half2float(__ushort_as_half((uint16_t)(swb & 0xFFFFu))); s_b1 = __half2float(__ushort_as_half((uint16_t)(swb >> 16)));
+        }
+        acc[rh][0] = fmaf(s_a0, t[sub][0][0] + t[sub][1][0], acc[rh][0]);
+        acc[rh][1] = fmaf(s_a1, t[sub][0][1] + t[sub][1][1], acc[rh][1]);
+        acc[rh][2] = fmaf(s_b0, t[sub][0][2] + t[sub][1][2], acc[rh][2]);
+        acc[rh][3] = fmaf(s_b1, t[sub][0][3] + t[sub][1][3], acc[rh][3]);
       }
     }
-#pragma unroll
-    for (int sub = 0; sub < 2; ++sub) {
-      float s_a0, s_a1, s_b0, s_b1;
-      const uint32_t swa = sw[sub][0], swb = sw[sub][1];
-      if constexpr (BF16S) {
-        s_a0 = __uint_as_float(swa << 16); s_a1 = __uint_as_float(swa & 0xFFFF0000u);
-        s_b0 = __uint_as_float(swb << 16); s_b1 = __uint_as_float(swb & 0xFFFF0000u);
-      } else {
-        s_a0 = __half2float(__ushort_as_half((uint16_t)(swa & 0xFFFFu))); s_a1 = __half2float(__ushort_as_half((uint16_t)(swa >> 16)));
-        s_b0 = __half2float(__ushort_as_half((uint16_t)(swb & 0xFFFFu))); s_b1 = __half2float(__ushort_as_half((uint16_t)(swb >> 16)));
-      }
-      acc[0] = fmaf(s_a0, t[sub][0][0] + t[sub][1][0], acc[0]);
-      acc[1] = fmaf(s_a1, t[sub][0][1] + t[sub][1][1], acc[1]);
-      acc[2] = fmaf(s_b0, t[sub][0][2] + t[sub][1][2], acc[2]);
-      acc[3] = fmaf(s_b1, t[sub][0][3] + t[sub][1][3], acc[3]);
-    }
-    if (++slot == kTRing) { slot = 0; phase ^= 1u; }
+    if (++slot == C::kRing) { slot = 0; phase ^= 1u; }
     if (++cic < nq && f + 1 < total) continue;
 
     // ---- this warp's part of the unit is done
@@ -1052,9 +1072,11 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       const int ux = item * nq;
       const int w0 = ux / L, w1 = (ux + nq - 1) / L;
       // partial slot 0: the piece's first unit; slot 1: its last unit
-      float* part = ws.dsplit + ((size_t)wg * 2 + (first_unit ? 0 : 1)) * 128;
+      float* part = ws.dsplit + ((size_t)wg * 2 + (first_unit ? 0 : 1)) * C::kPart;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) part[r * 32 + lane] = acc[r];
+      for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) part[(rh * 4 + r) * 32 + lane] = acc[rh][r];
       __syncwarp();
       int old = 0;
       if (lane == 0) {
@@ -1072,21 +1094,26 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
         // warp's piece begins inside it (slot 0).
         const int hs0 = w0 * L < ux ? 1 : 0;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          float v = 0.f;
-          for (int wk = w0; wk <= w1; ++wk) {
-            const int hs = wk == w0 ? hs0 : 0;
-            const float pk = wk == wg ? acc[r] : __ldcg(ws.dsplit + ((size_t)wk * 2 + hs) * 128 + r * 32 + lane);
-            v = wk == w0 ? pk : v + pk;
+        for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            float v = 0.f;
+            for (int wk = w0; wk <= w1; ++wk) {
+              const int hs = wk == w0 ? hs0 : 0;
+              const float pk = wk == wg ? acc[rh][r]
+                                        : __ldcg(ws.dsplit + ((size_t)wk * 2 + hs) * C::kPart + (rh * 4 + r) * 32 + lane);
+              v = wk == w0 ? pk : v + pk;
+            }
+            acc[rh][r] = v;
           }
-          acc[r] = v;
-        }
       }
     }
     if (last) {
-      const int row0 = rg * kRowsPerGroup;
-      float v_lo = acc[0] + acc[1];
-      float v_hi = acc[2] + acc[3];
+#pragma unroll
+      for (int rh = 0; rh < C::kHalves; ++rh) {
+      const int row0 = rg * C::kRows + rh * kRowsPerGroup;
+      float v_lo = acc[rh][0] + acc[rh][1];
+      float v_hi = acc[rh][2] + acc[rh][3];
       v_lo += __shfl_xor_sync(0xffffffffu, v_lo, 1);
       v_hi += __shfl_xor_sync(0xffffffffu, v_hi, 1);
       if constexpr (FC1) {
@@ -1113,9 +1140,12 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
           ws.y[(int64_t)e_rid * p.H + row0 + g + 8] = v_hi * fct;
         }
       }
+      }
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) acc[r] = 0.f;
+    for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[rh][r] = 0.f;
     if (cic == nq) {
       cic = 0;
       if (++rg == rgroups) { rg = 0; ++ei; }
@@ -1126,18 +1156,19 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   }
 }
 
-template <bool FC1, bool BF16S, bool HAS_ZP>
+template <int ROWS, bool FC1, bool BF16S, bool HAS_ZP>
 cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, const CUtensorMap& tz,
                               const CUtensorMap& ta, TmaDecodeArgs a, cudaStream_t s) {
+  using C = TCfg<ROWS>;
   static bool attr = false;
   if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_int4_tma_kernel<FC1, BF16S, HAS_ZP>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTSmem);
+    const cudaError_t err = cudaFuncSetAttribute(decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (err != cudaSuccess) return err;
     attr = true;
   }
   const int64_t blocks = (int64_t)sm_count() * kTBlocksPerSm;
-  decode_int4_tma_kernel<FC1, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kTWarps, kTSmem, s>>>(tq, ts, tz, ta, a);
+  decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kTWarps, C::kSmem, s>>>(tq, ts, tz, ta, a);
   return cudaGetLastError();
 }
 
@@ -1148,34 +1179,44 @@ bool decode_tma_applies(const Problem& p, bool has_zp) {
   return !has_zp || ((p.H / 32) % 16 == 0 && (p.I / 32) % 16 == 0);
 }
 
-template <bool FC1>
-cudaError_t launch_int4_tma(const uint8_t* q, const uint16_t* scales, const uint8_t* zp, const Problem& p,
-                            const Workspace& ws, cudaStream_t s) {
+template <int ROWS, bool FC1>
+cudaError_t launch_int4_tma_rows(const uint8_t* q, const uint16_t* scales, const uint8_t* zp, const Problem& p,
+                                 const Workspace& ws, cudaStream_t s) {
   const int N = FC1 ? 2 * p.I : p.H, K = FC1 ? p.H : p.I;
   const uint64_t rows = (uint64_t)p.E * N;
   const uint16_t* act = FC1 ? ws.x16 : ws.h16;
   const uint64_t arows = FC1 ? (uint64_t)p.T : (uint64_t)p.R();
   CUtensorMap tq, ts, tz, ta;
   if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K / 2, rows, (uint64_t)K / 2, 128,
-                   kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)K / 32, rows, (uint64_t)K / 16, 8,
-                   kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT16, act, (uint64_t)K, arows, (uint64_t)K * 2, kTChunkK, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (zp) {
     if (!make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT8, zp, (uint64_t)K / 32, rows, (uint64_t)K / 32, 16,
-                     kRowsPerGroup, CU_TENSOR_MAP_SWIZZLE_NONE))
+                     ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   } else {
     tz = ts;                                     // not read
   }
   TmaDecodeArgs a{N, K, p, ws};
   const bool bf16 = p.dtype == QMOE_BF16;
-  if (bf16) return zp ? launch_int4_tma_t<FC1, true, true>(tq, ts, tz, ta, a, s)
-                      : launch_int4_tma_t<FC1, true, false>(tq, ts, tz, ta, a, s);
-  return zp ? launch_int4_tma_t<FC1, false, true>(tq, ts, tz, ta, a, s)
-            : launch_int4_tma_t<FC1, false, false>(tq, ts, tz, ta, a, s);
+  if (bf16) return zp ? launch_int4_tma_t<ROWS, FC1, true, true>(tq, ts, tz, ta, a, s)
+                      : launch_int4_tma_t<ROWS, FC1, true, false>(tq, ts, tz, ta, a, s);
+  return zp ? launch_int4_tma_t<ROWS, FC1, false, true>(tq, ts, tz, ta, a, s)
+            : launch_int4_tma_t<ROWS, FC1, false, false>(tq, ts, tz, ta, a, s);
+}
+
+// 32-row units where a unit has at least four chunks (long enough that few of
+// them are cut between warps), 16-row units otherwise.
+template <bool FC1>
+cudaError_t launch_int4_tma(const uint8_t* q, const uint16_t* scales, const uint8_t* zp, const Problem& p,
+                            const Workspace& ws, cudaStream_t s) {
+  const int K = FC1 ? p.H : p.I, N = FC1 ? 2 * p.I : p.H;
+  if (K / kTChunkK >= 4 && N % 32 == 0) return launch_int4_tma_rows<32, FC1>(q, scales, zp, p, ws, s);
+  return launch_int4_tma_rows<16, FC1>(q, scales, zp, p, ws, s);
 }
 
 
@@ -1258,9 +1299,13 @@ int64_t decode_units_max(const Problem& p) {
 }
 
 int64_t decode_split_items_max(const Problem& p) {
-  // two partial tiles (the piece's first and last unit) per warp of the grid
+  // two partial tiles (the piece's first and last unit) per warp of the grid, in
+  // items of 128 floats: one per warp of the cp.async kernel, two (32 rows) per
+  // warp of the tensor-copy kernel
   if (!decode_int4_blockscaled(p)) return 0;
-  return decode_grid_blocks() * kWarps * 2;
+  const int64_t bs = decode_grid_blocks() * kWarps * 2;
+  const int64_t tma = (int64_t)sm_count() * kTBlocksPerSm * kTWarps * 2 * (kTPartMax / 128);
+  return bs > tma ? bs : tma;
 }
 
 cudaError_t launch_decode(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
