@@ -245,6 +245,21 @@ def run_reference(args):
 
 # --------------------------------------------------------------------------- GPU
 
+def kernel_traffic(key):
+    """DRAM bytes per launch of a roofline kernel from the committed ncu summary,
+    or None when the kernel's sources changed since that capture."""
+    import hashlib
+    try:
+        data = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        ent = data[key]
+        h = hashlib.sha256()
+        for f in ent["sources"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+    except (OSError, ValueError, KeyError):
+        return None
+    return int(ent["dram_bytes_per_launch"]) if h.hexdigest() == ent["source_sha256"] else None
+
+
 def p_path(shape):
     return "decode" if shape.T <= 8 else "grouped"
 
@@ -411,7 +426,7 @@ def run_ours(args):
                 "frac": round(achieved / (hbm if hbm else 6800.0), 4),
                 "peak_source": "measured" if hbm else "fallback",
                 "algorithmic_bytes_per_launch": int(bytes_fc1),
-                "traffic": None}
+                "traffic": kernel_traffic("decode_fc1"), "traffic_unit": "bytes per launch (ncu)"}
         extra = {"distinct_experts_per_layer_mean": float(np.mean(nact)),
                  "fc2_GBps": round(float(nact[-1]) * fc2_b / (stage_ms[2] / 1e3) / 1e9, 1),
                  "layer_GBps": round(float(np.mean(nact)) * (fc1_b + fc2_b) / (ms / layers / 1e3) / 1e9, 1)}
@@ -423,7 +438,7 @@ def run_ours(args):
                 "achieved": round(achieved, 1), "peak": tf if tf else 1900.0, "unit": "TFLOP/s",
                 "frac": round(achieved / (tf if tf else 1900.0), 4),
                 "peak_source": "measured" if tf else "fallback", "algorithmic_flops_per_launch": flops,
-                "traffic": None}
+                "traffic": kernel_traffic("prefill_fc1"), "traffic_unit": "bytes per launch (ncu)"}
         extra = {}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "layer-tokens/s", "n_gpus": world,
