@@ -45,6 +45,9 @@ __device__ __forceinline__ float warp_max_f(float v) {
   return v;
 }
 
+__device__ void convert_token(const Problem& p, const uint16_t* __restrict__ x, const Workspace& ws,
+                              int64_t t, int x16_mode);
+
 // Top-k + softmax of token t (whole warp), and optionally its FP16 activations.
 template <int PER_LANE>
 __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
@@ -89,9 +92,15 @@ __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
     if (s_idx) s_idx[t * k + lane] = my_e;
   }
   if (x16_mode == kX16None) return;
+  convert_token(p, x, ws, t, x16_mode);
+}
 
-  // Activations: scale by a power of two so that max|x_t| lies in [1, 2), round
-  // to FP16, and store in the K-order permutation of the dequantisers.
+// Activations of token t (whole warp): scale by a power of two so that max|x_t|
+// lies in [1, 2), round to FP16, and store in the K-order permutation of the
+// dequantisers.
+__device__ void convert_token(const Problem& p, const uint16_t* __restrict__ x, const Workspace& ws,
+                              int64_t t, int x16_mode) {
+  const int lane = threadIdx.x & 31;
   const int H = p.H;
   const uint16_t* xrow = x + t * (int64_t)H;
   float m = 0.0f;
@@ -289,12 +298,18 @@ __global__ void __launch_bounds__(kGroupThreads) group_scan_kernel(Problem p, Wo
   const int E = p.E;
   int total = 0;
   if (e < E) {
-    // per-expert exclusive prefix over chunks
-    for (int64_t c = 0; c < ws.nchunks; ++c) {
-      const int64_t i = c * E + e;
-      const int v = ws.chunk_hist[i];
-      ws.chunk_hist[i] = total;
-      total += v;
+    // per-expert exclusive prefix over chunks, eight independent loads at a time
+    int32_t* __restrict__ h = ws.chunk_hist;
+    const int64_t nc = ws.nchunks;
+    for (int64_t c0 = 0; c0 < nc; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = c0 + u < nc ? h[(c0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < nc) h[(c0 + u) * E + e] = total;
+        total += v[u];
+      }
     }
   }
   __shared__ int expert_base[kMaxExperts];
@@ -331,8 +346,15 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   __shared__ int s_idx[kPermuteChunk];
   __shared__ int s_sorted[kPermuteChunk];
   const int warps = blockDim.x >> 5;
-  for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps)
-    route_token<PER_LANE>(p, x, logits, ws, t, x16_mode, s_idx);
+  if (x16_mode != kX16None && 2 * p.T <= warps) {
+    // warps 0 .. T-1 route, warps T .. 2T-1 convert the activations at the same time
+    const int w = threadIdx.x >> 5;
+    if (w < p.T) route_token<PER_LANE>(p, x, logits, ws, w, kX16None, s_idx);
+    else if (w < 2 * p.T) convert_token(p, x, ws, w - p.T, x16_mode);
+  } else {
+    for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps)
+      route_token<PER_LANE>(p, x, logits, ws, t, x16_mode, s_idx);
+  }
   for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int R = (int)p.R();
