@@ -15,6 +15,8 @@ namespace {
 
 __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
                                                       uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int per_row = p.H / 8;
   const int64_t total = p.T * per_row;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -60,7 +62,10 @@ cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cud
   const int64_t total = p.T * (p.H / 8);
   int64_t blocks = (total + 255) / 256;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-  combine_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, ws, static_cast<uint16_t*>(out));
+  {
+    const cudaError_t e_ = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p, ws, static_cast<uint16_t*>(out));
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

@@ -220,6 +220,8 @@ struct ItemMeta {
 
 template <int BITS, bool FC1>
 __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
   const int K = a.K, N = a.N;
@@ -516,6 +518,8 @@ __device__ __forceinline__ int chunk_owner(int64_t x, int nw, int64_t total) {
 
 template <bool FC1, bool BF16S, bool HAS_ZP>
 __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_kernel(DecodeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
   const int K = a.K, N = a.N;
@@ -779,7 +783,10 @@ cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStre
     if (err != cudaSuccess) return err;
     attr = true;
   }
-  decode_int4_bs_kernel<FC1, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
+  {
+    const cudaError_t e_ = launch_pdl(decode_int4_bs_kernel<FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
@@ -837,6 +844,16 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ts,
     const __grid_constant__ CUtensorMap tz, const __grid_constant__ CUtensorMap ta, TmaDecodeArgs a) {
   using C = TCfg<ROWS>;
+  // fc1 needs the routing kernel's results at once. fc2 reads only the routing
+  // results (complete: fc1 let fc2 be scheduled only after waiting for routing)
+  // and its own weights before it waits for fc1, so its first weight copies
+  // overlap the end of fc1.
+  if constexpr (FC1) {
+    pdl_wait();
+    pdl_trigger();
+  } else {
+    pdl_trigger();
+  }
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
   const int K = a.K, N = a.N;
@@ -869,18 +886,33 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
     for (int s = 0; s < C::kRing; ++s) mbar_init(bar_s + 8 * s, 1);
   mbar_init_fence();
   __syncthreads();
-  if (total == 0) return;
+  if (total == 0) {
+    if constexpr (!FC1) pdl_wait();
+    return;
+  }
 
   // unit = (decode-table entry ei, 32-row group rg); walked without divisions
   const int item0 = x_begin / nq;
   const int cic0 = x_begin - item0 * nq;
   const int ei0 = item0 / rgroups, rg0 = item0 - ei0 * rgroups;
 
-  // ---- issue side: lane 0 copies chunk f of the piece into slot f % C::kRing
+  // ---- issue side: lane 0 copies chunk f of the piece into slot f % C::kRing:
+  // the weights (codes, scales, zero points; announced without arriving) and the
+  // activations of the entry's tokens (announced with the arrival)
   int p_ei = ei0, p_rg = rg0, p_cic = cic0, p_row = 0, p_t0 = 0, p_t1 = 0, p_cnt = 0;
   bool p_new = true;
   uint32_t p_slot_s = ring_s, p_bar = bar_s;
-  auto issue = [&]() {
+  auto issue_act = [&](uint32_t slot_s, uint32_t bar, int kx, int t0, int t1, int cnt) {
+    if (lane == 0) {
+      mbar_expect_tx(bar, cnt > 1 ? 1024 : 512);
+      tma_load_2d(slot_s + C::kAct0, &ta, bar, kx, t0);
+      if (cnt > 1) tma_load_2d(slot_s + C::kAct1, &ta, bar, kx, t1);
+    }
+  };
+  // deferred activation copies of the first slots (fc2: issued after the wait)
+  uint32_t q_slot[C::kRing - 1], q_bar[C::kRing - 1];
+  int q_kx[C::kRing - 1], q_t0[C::kRing - 1], q_t1[C::kRing - 1], q_cnt[C::kRing - 1];
+  auto issue = [&](bool with_act, int q) {
     if (p_new) {
       p_new = false;
       const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + p_ei * kDtabInts));
@@ -890,14 +922,17 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       p_t0 = FC1 ? d1.x : d0.y;
       p_t1 = FC1 ? d1.y : d0.y + 1;
     }
+    const int kx = p_cic * kTChunkK;
     if (lane == 0) {
-      const int kx = p_cic * kTChunkK;
-      mbar_expect_tx(p_bar, ROWS * 128 + ROWS * 16 + (HAS_ZP ? ROWS * 16 : 0) + (p_cnt > 1 ? 1024 : 512));
+      mbar_expect_tx_only(p_bar, ROWS * 128 + ROWS * 16 + (HAS_ZP ? ROWS * 16 : 0));
       tma_load_2d(p_slot_s + C::kCode, &tq, p_bar, kx / 2, p_row);
       tma_load_2d(p_slot_s + C::kScale, &ts, p_bar, kx / 32, p_row);
       if constexpr (HAS_ZP) tma_load_2d(p_slot_s + C::kZp, &tz, p_bar, (kx / 32) & ~15, p_row);
-      tma_load_2d(p_slot_s + C::kAct0, &ta, p_bar, kx, p_t0);
-      if (p_cnt > 1) tma_load_2d(p_slot_s + C::kAct1, &ta, p_bar, kx, p_t1);
+    }
+    if (with_act) {
+      issue_act(p_slot_s, p_bar, kx, p_t0, p_t1, p_cnt);
+    } else {
+      q_slot[q] = p_slot_s; q_bar[q] = p_bar; q_kx[q] = kx; q_t0[q] = p_t0; q_t1[q] = p_t1; q_cnt[q] = p_cnt;
     }
     if (p_bar == bar_s + 8 * (C::kRing - 1)) { p_bar = bar_s; p_slot_s = ring_s; }
     else { p_bar += 8; p_slot_s += C::kSlot; }
@@ -907,7 +942,16 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       if (++p_rg == rgroups) { p_rg = 0; ++p_ei; }
     }
   };
-  for (int u = 0; u < C::kRing - 1 && u < total; ++u) issue();
+  const int pre = total < C::kRing - 1 ? total : C::kRing - 1;
+#pragma unroll
+  for (int u = 0; u < C::kRing - 1; ++u)
+    if (u < pre) issue(FC1, u);
+  if constexpr (!FC1) {
+    pdl_wait();                                  // h16 (fc1's output) is complete from here on
+#pragma unroll
+    for (int u = 0; u < C::kRing - 1; ++u)
+      if (u < pre) issue_act(q_slot[u], q_bar[u], q_kx[u], q_t0[u], q_t1[u], q_cnt[u]);
+  }
 
   const __half2 ne_d = __float2half2_rn(-(1024.0f + 8.0f)), no_d = __float2half2_rn(-(1024.0f + 128.0f));
   const uint32_t ne_def = *reinterpret_cast<const uint32_t*>(&ne_d);
@@ -933,7 +977,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   uint32_t phase = 0;
   for (int f = 0; f < total; ++f) {
     __syncwarp();                                // every lane is done with the slot refilled next
-    if (f + C::kRing - 1 < total) issue();
+    if (f + C::kRing - 1 < total) issue(true, 0);
     if (fresh) {
       fresh = false;
       const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + ei * kDtabInts));
@@ -1168,7 +1212,10 @@ cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, cons
     attr = true;
   }
   const int64_t blocks = (int64_t)sm_count() * kTBlocksPerSm;
-  decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP><<<(unsigned)blocks, 32 * kTWarps, C::kSmem, s>>>(tq, ts, tz, ta, a);
+  {
+    const cudaError_t e_ = launch_pdl(decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem, s, tq, ts, tz, ta, a);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
@@ -1267,7 +1314,10 @@ cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     attr = true;
   }
-  decode_gemv_kernel<BITS, FC1><<<(unsigned)blocks, 32 * kWarps, smem, s>>>(a);
+  {
+    const cudaError_t e_ = launch_pdl(decode_gemv_kernel<BITS, FC1>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

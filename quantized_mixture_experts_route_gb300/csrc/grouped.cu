@@ -264,6 +264,8 @@ template <int BITS, bool FC1>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_q, GemmArgs g) {
+  pdl_wait();
+  pdl_trigger();
   using C = Cfg<BITS>;
   constexpr int S = C::STAGES;
   const Workspace& ws = g.ws;
@@ -571,7 +573,10 @@ cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t works_max = ws.max_tiles * ((N + C::BN - 1) / C::BN);
   dim3 grid((unsigned)(works_max < sms ? works_max : sms));
-  grouped_gemm_kernel<BITS, FC1><<<grid, kThreads, C::SMEM, s>>>(ta, tq, g);
+  {
+    const cudaError_t e_ = launch_pdl(grouped_gemm_kernel<BITS, FC1>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tq, g);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/qmoe.h"
 
 namespace qmoe {
@@ -108,6 +110,35 @@ __device__ __forceinline__ float half_bits_to_float(uint16_t b, int dtype) {
 __device__ __forceinline__ uint16_t float_to_half_bits(float v, int dtype) {
   if (dtype == QMOE_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
   return __half_as_ushort(__float2half_rn(v));
+}
+
+// Programmatic dependent launch. Every kernel of the path is launched so that it
+// may be scheduled while the previous kernel on the stream is still running.
+// pdl_wait() returns once the previous kernel has completed and its writes are
+// visible; a kernel touches nothing that kernel writes, nor memory that it
+// reads, before pdl_wait(). pdl_trigger() lets the next kernel be scheduled
+// (once every block of this one has called it or exited); a kernel calls it
+// only after pdl_wait(), except the fc2 and combine kernels, whose dependents
+// wait for them before touching anything. The results do not change.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }

@@ -52,7 +52,7 @@ __device__ void convert_token(const Problem& p, const uint16_t* __restrict__ x, 
 template <int PER_LANE>
 __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
                             const uint16_t* __restrict__ logits, const Workspace& ws, int64_t t,
-                            int x16_mode, int* s_idx = nullptr) {
+                            int x16_mode, int* s_idx = nullptr, float* s_w = nullptr) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   const uint16_t* lrow = logits + t * E;
@@ -87,9 +87,15 @@ __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
   float denom = 0.0f;
   for (int j = 0; j < k; ++j) denom += expf(__shfl_sync(0xffffffffu, my_l, j) - l0);
   if (lane < k) {
-    ws.topk_idx[t * k + lane] = my_e;
-    ws.topk_w[t * k + lane] = expf(my_l - l0) / denom;
-    if (s_idx) s_idx[t * k + lane] = my_e;
+    const float w = expf(my_l - l0) / denom;
+    if (s_w) {                                   // shared memory only; written out later
+      s_idx[t * k + lane] = my_e;
+      s_w[t * k + lane] = w;
+    } else {
+      ws.topk_idx[t * k + lane] = my_e;
+      ws.topk_w[t * k + lane] = w;
+      if (s_idx) s_idx[t * k + lane] = my_e;
+    }
   }
   if (x16_mode == kX16None) return;
   convert_token(p, x, ws, t, x16_mode);
@@ -171,6 +177,8 @@ template <int PER_LANE>
 __global__ void __launch_bounds__(256) route_kernel(Problem p, const uint16_t* __restrict__ x,
                                                     const uint16_t* __restrict__ logits,
                                                     Workspace ws, int x16_mode) {
+  pdl_wait();
+  pdl_trigger();
   const int warps = blockDim.x >> 5;
   for (int64_t t = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); t < p.T;
        t += (int64_t)gridDim.x * warps)
@@ -278,6 +286,8 @@ __device__ void finish_groups(int E, int total_e, const Workspace& ws, bool want
 }
 
 __global__ void __launch_bounds__(kGroupThreads) group_count_kernel(Problem p, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   int* hist = smem;
   for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
@@ -293,6 +303,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_count_kernel(Problem p, W
 
 __global__ void __launch_bounds__(kGroupThreads) group_scan_kernel(Problem p, Workspace ws,
                                                                    int want_tiles) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int sh[32];
   const int e = threadIdx.x;
   const int E = p.E;
@@ -320,6 +332,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_scan_kernel(Problem p, Wo
 }
 
 __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(Problem p, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   int* base = smem;                 // [E]
   int* warp_cnt = smem + p.E;       // [16][E]
@@ -332,9 +346,12 @@ __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(Problem p,
   scatter_routes(ws.topk_idx, r0, r1, p.E, base, warp_cnt, ws.sorted_route);
 }
 
-// Routing and grouping of a small batch (R <= kPermuteChunk) in one block. The
-// intermediate results (expert of each route, offsets, sorted order) stay in
-// shared memory, so no step waits on a global round trip of an earlier one.
+// Routing and grouping of a small batch (R <= kPermuteChunk) in one block. All of
+// it is computed in shared memory from the router logits alone, before the
+// previous kernel on the stream has finished (programmatic dependent launch);
+// then the kernel waits for it and writes the results, the decode table and the
+// FP16 activations (which read x, the previous kernel's output).
+// Dynamic shared memory: hist [E], warp_cnt [16][E], decode table [dtab_max][8].
 template <int PER_LANE>
 __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
     Problem p, const uint16_t* __restrict__ x, const uint16_t* __restrict__ logits, Workspace ws,
@@ -342,57 +359,89 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   extern __shared__ int smem[];
   int* hist = smem;                  // [E]
   int* warp_cnt = smem + p.E;        // [16][E]
+  int* s_dtab = warp_cnt + (kGroupThreads / 32) * p.E;   // [entries][kDtabInts] (decode path)
   __shared__ int sh[32];
   __shared__ int s_idx[kPermuteChunk];
+  __shared__ float s_w[kPermuteChunk];
   __shared__ int s_sorted[kPermuteChunk];
+  __shared__ int s_act[kMaxExperts];
   const int warps = blockDim.x >> 5;
-  if (x16_mode != kX16None && 2 * p.T <= warps) {
-    // warps 0 .. T-1 route, warps T .. 2T-1 convert the activations at the same time
-    const int w = threadIdx.x >> 5;
-    if (w < p.T) route_token<PER_LANE>(p, x, logits, ws, w, kX16None, s_idx);
-    else if (w < 2 * p.T) convert_token(p, x, ws, w - p.T, x16_mode);
-  } else {
-    for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps)
-      route_token<PER_LANE>(p, x, logits, ws, t, x16_mode, s_idx);
-  }
+  const int R = (int)p.R();
+  const int e = threadIdx.x;
+  for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps)
+    route_token<PER_LANE>(p, x, logits, ws, t, kX16None, s_idx, s_w);
   for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int R = (int)p.R();
   count_routes(s_idx, 0, R, hist);
   __syncthreads();
-  const int total = threadIdx.x < p.E ? hist[threadIdx.x] : 0;
+  const int total = e < p.E ? hist[e] : 0;
   __syncthreads();
-  finish_groups(p.E, total, ws, want_tiles != 0, sh, hist);  // hist now holds the bases
-  __syncthreads();
-  const int begin = threadIdx.x < p.E ? hist[threadIdx.x] : 0;
-  scatter_routes(s_idx, 0, R, p.E, hist, warp_cnt, s_sorted);   // ends with a block barrier
-  for (int i = threadIdx.x; i < R; i += blockDim.x) ws.sorted_route[i] = s_sorted[i];
-  // decode table: one entry per (active expert, pair of its routes), so that a
-  // decode work unit reaches its expert's rows and its tokens with one
-  // independent load and always multiplies exactly one MMA column pair
-  if (p.path != QMOE_PATH_DECODE) return;    // (block-uniform) R <= kDtabMax on this path
-  for (int64_t i = threadIdx.x; i < ws.dunits_max; i += blockDim.x) ws.dticket[i] = 0;
-  // entries in ascending expert order (the order of the active-expert list)
-  const int n_e = total;
-  int n_entries;
-  const int first = block_exclusive_scan((n_e + 1) / 2, sh, &n_entries);
-  for (int q = 0; 2 * q < n_e; ++q) {
-    int32_t* d = ws.dtab + (first + q) * kDtabInts;
-    const int cnt = n_e - 2 * q < 2 ? n_e - 2 * q : 2;
-    const int e = threadIdx.x;
-    d[0] = e;
-    d[1] = begin + 2 * q;
-    d[2] = cnt;
-    d[3] = 0;
-    d[4] = s_sorted[begin + 2 * q] / p.k;
-    d[5] = cnt > 1 ? s_sorted[begin + 2 * q + 1] / p.k : 0;
-    d[6] = 0;
-    d[7] = 0;
+  int R_total, n_active, n_tiles = 0;
+  const int off = block_exclusive_scan(total, sh, &R_total);
+  const int apos = block_exclusive_scan(total > 0 ? 1 : 0, sh, &n_active);
+  const int nt = (total + kTileM - 1) / kTileM;
+  const int tpos = want_tiles ? block_exclusive_scan(nt, sh, &n_tiles) : 0;
+  if (e < p.E) {
+    hist[e] = off;                   // scatter bases
+    if (total > 0) s_act[apos] = e;
   }
-  if (threadIdx.x == 0) ws.counters[3] = n_entries;
+  __syncthreads();
+  scatter_routes(s_idx, 0, R, p.E, hist, warp_cnt, s_sorted);   // ends with a block barrier
+  // decode table: one entry per (active expert, pair of its routes), in expert
+  // order, so that a decode work unit reaches its expert's rows and its tokens
+  // with one independent load and always multiplies exactly one MMA column pair
+  const bool dec = p.path == QMOE_PATH_DECODE;  // (block-uniform) R <= kDtabMax on this path
+  int n_entries = 0;
+  if (dec) {
+    const int first = block_exclusive_scan((total + 1) / 2, sh, &n_entries);
+    for (int q = 0; 2 * q < total; ++q) {
+      int* d = s_dtab + (first + q) * kDtabInts;
+      const int cnt = total - 2 * q < 2 ? total - 2 * q : 2;
+      d[0] = e;
+      d[1] = off + 2 * q;
+      d[2] = cnt;
+      d[3] = 0;
+      d[4] = s_sorted[off + 2 * q] / p.k;
+      d[5] = cnt > 1 ? s_sorted[off + 2 * q + 1] / p.k : 0;
+      d[6] = 0;
+      d[7] = 0;
+    }
+    __syncthreads();
+  }
+
+  // ---- the previous kernel has finished: write everything out
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    ws.topk_idx[i] = s_idx[i];
+    ws.topk_w[i] = s_w[i];
+    ws.sorted_route[i] = s_sorted[i];
+  }
+  if (e < p.E) ws.offsets[e] = off;
+  if (e == 0) {
+    ws.offsets[p.E] = R_total;
+    ws.counters[0] = n_active;
+    ws.counters[1] = n_tiles;
+    ws.counters[2] = 0;  // error flag of the grouped GEMM / decode kernels (set on a timed-out wait)
+    ws.counters[3] = n_entries;
+  }
+  for (int i = threadIdx.x; i < n_active; i += blockDim.x) ws.active[i] = s_act[i];
+  if (want_tiles && e < p.E)
+    for (int i = 0; i < nt; ++i) {
+      ws.tiles[2 * (tpos + i)] = e;
+      ws.tiles[2 * (tpos + i) + 1] = off + i * kTileM;
+    }
+  if (dec) {
+    for (int64_t i = threadIdx.x; i < ws.dunits_max; i += blockDim.x) ws.dticket[i] = 0;
+    for (int i = threadIdx.x; i < n_entries * kDtabInts; i += blockDim.x) ws.dtab[i] = s_dtab[i];
+  }
+  if (x16_mode != kX16None)
+    for (int64_t t = threadIdx.x >> 5; t < p.T; t += warps) convert_token(p, x, ws, t, x16_mode);
 }
 
 __global__ void __launch_bounds__(256) gather_kernel(Problem p, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
   // x16s[pos] = x16[token of sorted route pos]; one warp per row, 16 bytes per lane
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -428,31 +477,57 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* logits, co
   const auto* xx = static_cast<const uint16_t*>(x);
   const auto* lg = static_cast<const uint16_t*>(logits);
   if (small) {
-    const size_t smem = sizeof(int) * (size_t)p.E * (1 + kGroupThreads / 32);
+    const size_t smem = sizeof(int) * ((size_t)p.E * (1 + kGroupThreads / 32) +
+                                       (p.path == QMOE_PATH_DECODE ? (size_t)kDtabMax * kDtabInts : 0));
+    static bool attr = false;
+    if (!attr) {
+      cudaError_t err = cudaFuncSetAttribute(route_group_small_kernel<4>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(route_group_small_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   96 * 1024);
+      if (err != cudaSuccess) return err;
+      attr = true;
+    }
     if (p.E <= 128)
-      route_group_small_kernel<4><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, x16_mode, want_tiles);
-    else
-      route_group_small_kernel<16><<<1, kGroupThreads, smem, s>>>(p, xx, lg, ws, x16_mode, want_tiles);
-    return cudaGetLastError();
+      return launch_pdl(route_group_small_kernel<4>, dim3(1), dim3(kGroupThreads), smem, s, p, xx, lg, ws,
+                        x16_mode, (int)want_tiles);
+    return launch_pdl(route_group_small_kernel<16>, dim3(1), dim3(kGroupThreads), smem, s, p, xx, lg, ws,
+                      x16_mode, (int)want_tiles);
   }
   const int warps = 8;
   int64_t blocks = (p.T + warps - 1) / warps;
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
   if (p.E <= 128)
-    route_kernel<4><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, x16_mode);
+    {
+      const cudaError_t e_ = launch_pdl(route_kernel<4>, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, xx, lg, ws, x16_mode);
+      if (e_ != cudaSuccess) return e_;
+    }
   else
-    route_kernel<16><<<(unsigned)blocks, 32 * warps, 0, s>>>(p, xx, lg, ws, x16_mode);
+    {
+      const cudaError_t e_ = launch_pdl(route_kernel<16>, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, xx, lg, ws, x16_mode);
+      if (e_ != cudaSuccess) return e_;
+    }
   return cudaGetLastError();
 }
 
 cudaError_t launch_group(const Problem& p, const Workspace& ws, bool want_tiles, cudaStream_t s) {
   if (p.R() <= kPermuteChunk) return cudaSuccess;  // done by route_group_small_kernel
   const unsigned nchunks = (unsigned)ws.nchunks;
-  group_count_kernel<<<nchunks, kGroupThreads, sizeof(int) * p.E, s>>>(p, ws);
-  group_scan_kernel<<<1, kGroupThreads, 0, s>>>(p, ws, want_tiles ? 1 : 0);
+  {
+    const cudaError_t e_ = launch_pdl(group_count_kernel, dim3(nchunks), dim3(kGroupThreads), sizeof(int) * p.E, s, p, ws);
+    if (e_ != cudaSuccess) return e_;
+  }
+  {
+    const cudaError_t e_ = launch_pdl(group_scan_kernel, dim3(1), dim3(kGroupThreads), 0, s, p, ws, want_tiles ? 1 : 0);
+    if (e_ != cudaSuccess) return e_;
+  }
   const size_t smem = sizeof(int) * (size_t)p.E * (1 + kGroupThreads / 32);
-  group_scatter_kernel<<<nchunks, kGroupThreads, smem, s>>>(p, ws);
+  {
+    const cudaError_t e_ = launch_pdl(group_scatter_kernel, dim3(nchunks), dim3(kGroupThreads), smem, s, p, ws);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
@@ -461,7 +536,10 @@ cudaError_t launch_gather(const Problem& p, const Workspace& ws, cudaStream_t s)
   int64_t blocks = (p.R() + warps - 1) / warps;
   const int64_t cap = (int64_t)num_sms() * 16;
   if (blocks > cap) blocks = cap;
-  gather_kernel<<<(unsigned)blocks, 32 * warps, 0, s>>>(p, ws);
+  {
+    const cudaError_t e_ = launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, ws);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
