@@ -1025,6 +1025,24 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
     QMOE_LDS_ACT(1, 2, 288);
     QMOE_LDS_ACT(1, 3, 304);
 #undef QMOE_LDS_ACT
+    // With the implicit zero point every weight row has the same bias operand, so
+    // the bias MMAs are computed once per chunk and start each row half's sums.
+    float tb[2][2][4];
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tb[sub][q][e] = 0.f;
+    if constexpr (!HAS_ZP) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          mma16816(tb[sub][0], ne_def, ne_def, no_def, no_def, bw[sub][4 * i], bw[sub][4 * i + 1]);
+          mma16816(tb[sub][1], ne_def, ne_def, no_def, no_def, bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+        }
+    }
 #pragma unroll
     for (int rh = 0; rh < C::kHalves; ++rh) {
       const uint32_t cb_ = sb + code_off + rh * 2048, sr = sb + scale_off + rh * 256;   // rows 16 rh ..
@@ -1067,7 +1085,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) t[sub][q][e] = 0.f;
+          for (int e = 0; e < 4; ++e) t[sub][q][e] = tb[sub][q][e];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -1081,10 +1099,12 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
                    lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
                    bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
         }
+        if constexpr (HAS_ZP) {
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          mma16816(t[sub][0], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i], bw[sub][4 * i + 1]);
-          mma16816(t[sub][1], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+          for (int sub = 0; sub < 2; ++sub) {
+            mma16816(t[sub][0], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i], bw[sub][4 * i + 1]);
+            mma16816(t[sub][1], ne_a[sub], ne_b[sub], no_a[sub], no_b[sub], bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+          }
         }
       }
 #pragma unroll
