@@ -41,7 +41,11 @@ constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
 constexpr int kErrTimeout = 1;
 static_assert(kBM == kTileM, "the grouping kernels cut tiles of kTileM sorted rows");
 
-template <int BITS>
+// TSC: block scales brought in by bulk tensor copies (no zero points, and rows of
+// scales a multiple of 16 bytes): one [BN rows][8 scales] box covers 8 blocks
+// along K (a "scale span" of 8*block/BK stages) in a ring of two; otherwise the
+// producer warp loads scales and zero points per stage and stores FP16 words.
+template <int BITS, bool TSC = false>
 struct Cfg {
   static constexpr int BK = BITS == 3 ? 128 : 64;     // K per stage
   static constexpr int BN = BITS == 3 ? 128 : 256;    // weight rows per tile (MMA N)
@@ -56,13 +60,14 @@ struct Cfg {
   static constexpr int UNITS = BN * UNITS_PER_ROW;
   static constexpr int UNITS_PER_THREAD = UNITS / kDequantThreads;
   static constexpr int S_BYTES = UNITS * 4;           // per unit: FP16 scale | zero point << 16
+  static constexpr int SC_BYTES = BN * 16;            // one scale box: [BN][8] 16-bit scales
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
   static constexpr int C_OFF = B_OFF + STAGES * B_BYTES;
   static constexpr int S_OFF = C_OFF + STAGES * C_BYTES;
-  static constexpr int BAR_OFF = S_OFF + STAGES * S_BYTES;
+  static constexpr int BAR_OFF = S_OFF + (TSC ? 2 * SC_BYTES : STAGES * S_BYTES);
   static constexpr int SMEM = BAR_OFF + 128 + 1024;   // barriers + TMEM address + alignment slack
-  static_assert(8 * (3 * STAGES + 2) + 8 <= 128, "barrier area");
+  static_assert(8 * (3 * STAGES + 2 + 4) + 8 <= 128, "barrier area");
   static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
   static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -260,13 +265,14 @@ __device__ __forceinline__ void dequant_unit_fast(const uint32_t* w, uint32_t zp
 }
 
 
-template <int BITS, bool FC1>
+template <int BITS, bool FC1, bool TSC>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_q, GemmArgs g) {
+                        const __grid_constant__ CUtensorMap tmap_q,
+                        const __grid_constant__ CUtensorMap tmap_s, GemmArgs g) {
   pdl_wait();
   pdl_trigger();
-  using C = Cfg<BITS>;
+  using C = Cfg<BITS, TSC>;
   constexpr int S = C::STAGES;
   const Workspace& ws = g.ws;
   const Problem& p = g.p;
@@ -290,22 +296,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
   const uint32_t bar_accum = bar0 + 8u * (3 * S);
   const uint32_t bar_drained = bar0 + 8u * (3 * S + 1);
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * S + 2));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * S + 2) + 4);
+  // scale ring (TSC): [3S+2, 3S+4) box landed; [3S+4, 3S+6) box read by the dequantisers
+  auto bar_sfull = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
+  auto bar_sempty = [&](int b) { return bar0 + 8u * (3 * S + 4 + b); };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * S + 6));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * S + 6) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(bar_full(s), 1 + 32);   // the TMA issue (with its byte count) + 32 scale writers
+      mbar_init(bar_full(s), TSC ? 1 : 1 + 32);   // the TMA issue (with its byte count) [+ 32 scale writers]
       mbar_init(bar_bready(s), kDequantThreads);
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_accum, 1);
     mbar_init(bar_drained, kDequantThreads);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_sfull(b), 1);
+      mbar_init(bar_sempty(b), kDequantThreads);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+    if (TSC) asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_s)) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
@@ -319,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nblk = K / p.block;
+  const int span = 8 * p.block / C::BK;          // stages per scale box (TSC)
   auto tile_of = [&](int j, int& e, int& row0, int& n0) {
     const int w = blockIdx.x + j * gridDim.x;
     const int mt = w / n_tiles_n;
@@ -329,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- producer: TMA (lane 0) and each stage's scales (all lanes)
-    int issued = 0;
+    int issued = 0, spans = 0;
     bool go = true;
     for (int j = 0; j < my_works && go; ++j) {
       int e, row0, n0;
@@ -342,9 +357,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)(it / S) & 1u;
         int ok = 1;
         if (lane == 0) ok = mbar_wait(bar_empty(s), ph ^ 1u, abort_flag, launch_err) ? 1 : 0;
+        const int k0 = i * C::BK;
+        if (TSC && i % span == 0) {
+          // next scale box, into the ring slot the dequantisers released
+          const int m = spans++;
+          if (lane == 0 && ok) {
+            if (m >= 2 && !mbar_wait(bar_sempty(m & 1), (uint32_t)((m - 2) >> 1) & 1u, abort_flag, launch_err))
+              ok = 0;
+            else {
+              mbar_expect_tx(bar_sfull(m & 1), C::SC_BYTES);
+              tma_load_2d(sbase + C::S_OFF + (m & 1) * C::SC_BYTES, &tmap_s, bar_sfull(m & 1), k0 / p.block,
+                          e * N + n0);
+            }
+          }
+        }
         if (__shfl_sync(0xffffffffu, ok, 0) == 0) { go = false; break; }
         ++issued;
-        const int k0 = i * C::BK;
         if (lane == 0) {
           mbar_expect_tx(bar_full(s), C::A_BYTES + C::C_BYTES);
 #pragma unroll
@@ -355,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           bar_full(s), k0 + 64 * sub, row0 + h * kSubM);
           tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8, e * N + n0);
         }
+        if constexpr (TSC) continue;
         uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
         // all loads first (independent, no branches), then convert and store
         constexpr int PER_LANE = C::UNITS / 32;
@@ -385,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // let the copies already issued land before the CTA exits
       for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i)
         mbar_wait_drain(bar_full(i % S), (uint32_t)(i / S) & 1u);
+      if (TSC)
+        for (int m = spans - 2 > 0 ? spans - 2 : 0; m < spans; ++m)
+          mbar_wait_drain(bar_sfull(m & 1), (uint32_t)(m >> 1) & 1u);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: two 128-row accumulators share each B stage
@@ -431,6 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = half * kSubM + quarter * 32 + lane;
     const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
     bool go = true;
+    int spans = 0;                               // scale boxes consumed (TSC)
+    const uint32_t zdef = (uint32_t)(1u << (BITS - 1)) << 16;
     for (int j = 0; j < my_works && go; ++j) {
       int e, row0, n0;
       tile_of(j, e, row0, n0);
@@ -446,6 +480,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
         if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) { go = false; break; }
+        const int m_sp = spans;                  // scale box of this stage (TSC)
+        if (TSC && i % span == 0) {
+          ++spans;
+          if (!mbar_wait(bar_sfull(m_sp & 1), (uint32_t)(m_sp >> 1) & 1u, abort_flag, launch_err)) {
+            go = false;
+            break;
+          }
+        }
+        const int m_cur = TSC ? spans - 1 : 0;
+        // [BN rows][8] scales of this box; this stage's first block within it
+        const uint16_t* sbox = reinterpret_cast<const uint16_t*>(smem + C::S_OFF + (m_cur & 1) * C::SC_BYTES);
+        const int b_first = (i % span) * C::BK / p.block;
         const uint8_t* codes = smem + C::C_OFF + s * C::C_BYTES;
         const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
         uint8_t* bt = smem + C::B_OFF + s * C::B_BYTES;
@@ -465,7 +511,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 3; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
           }
-          const uint32_t sz = st[unit];
+          uint32_t sz;
+          if constexpr (TSC) {
+            const uint16_t sb16 = sbox[r * 8 + b_first + (32 * jj) / p.block];
+            const uint16_t sh = p.dtype == QMOE_BF16
+                                    ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sb16 << 16)))
+                                    : sb16;
+            sz = (uint32_t)sh | zdef;
+          } else {
+            sz = st[unit];
+          }
           const uint32_t s2 = (sz & 0xFFFFu) * 0x00010001u;
           uint32_t pr[16];
           dequant_unit_fast<BITS>(w, sz >> 16, s2, pr);
@@ -479,6 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async();
         mbar_arrive(bar_bready(s));
+        // the last stage of a scale box releases the box
+        if (TSC && (i % span == span - 1 || i == ksteps - 1)) mbar_arrive(bar_sempty(m_cur & 1));
       }
       if (!go) break;
 
@@ -543,15 +600,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-template <int BITS, bool FC1>
-cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
-                        const Workspace& ws, cudaStream_t s) {
-  using C = Cfg<BITS>;
+template <int BITS, bool FC1, bool TSC>
+cudaError_t launch_gemm_t(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
+                          const Workspace& ws, cudaStream_t s) {
+  using C = Cfg<BITS, TSC>;
   const int N = FC1 ? 2 * p.I : p.H;
   const int K = FC1 ? p.H : p.I;
   const int64_t R = p.R();
   const uint16_t* A = FC1 ? ws.x16s : ws.h16;
-  CUtensorMap ta, tq;
+  CUtensorMap ta, tq, tsc;
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2,
                    64, kSubM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -559,9 +616,18 @@ cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, 
   if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, row_bytes, (uint64_t)p.E * N, row_bytes,
                    C::CODE_ROW, C::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  if (TSC) {
+    // [E*N rows][K/block] 16-bit scales, boxes of 8 scales x BN rows
+    const uint64_t nb = (uint64_t)K / p.block;
+    if (!make_map_2d(&tsc, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, nb, (uint64_t)p.E * N, nb * 2, 8, C::BN,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    tsc = tq;                                    // not read
+  }
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BITS, FC1>,
+    const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BITS, FC1, TSC>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     attr_set = true;
@@ -573,11 +639,17 @@ cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t works_max = ws.max_tiles * ((N + C::BN - 1) / C::BN);
   dim3 grid((unsigned)(works_max < sms ? works_max : sms));
-  {
-    const cudaError_t e_ = launch_pdl(grouped_gemm_kernel<BITS, FC1>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tq, g);
-    if (e_ != cudaSuccess) return e_;
-  }
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<BITS, FC1, TSC>, grid, dim3(kThreads), C::SMEM, s, ta, tq, tsc, g);
+}
+
+// Scales by bulk tensor copies when there are no zero points and a row of
+// scales is a multiple of 16 bytes; the producer-warp path otherwise.
+template <int BITS, bool FC1>
+cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
+                        const Workspace& ws, cudaStream_t s) {
+  const int K = FC1 ? p.H : p.I;
+  if (!zp && (K / p.block) % 8 == 0) return launch_gemm_t<BITS, FC1, true>(p, q, scales, zp, ws, s);
+  return launch_gemm_t<BITS, FC1, false>(p, q, scales, zp, ws, s);
 }
 
 }  // namespace
