@@ -35,7 +35,9 @@ constexpr int kSubM = 128;             // rows per MMA / TMEM accumulator
 constexpr int kBM = 2 * kSubM;         // rows per tile: two accumulators share each B stage
 constexpr int kDequantWarps = 8;       // warps 2..9
 constexpr int kDequantThreads = 32 * kDequantWarps;
-constexpr int kThreads = 64 + kDequantThreads;
+constexpr int kEpiWarps = 4;           // warps 10..13
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kDequantThreads + kEpiThreads;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
 constexpr int kErrTimeout = 1;
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_accum, 1);
-    mbar_init(bar_drained, kDequantThreads);
+    mbar_init(bar_drained, kEpiThreads);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_sfull(b), 1);
       mbar_init(bar_sempty(b), kDequantThreads);
@@ -454,27 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MMAs in flight finish before TMEM is freed
       if (*abort_flag && committed > 0) mbar_wait_drain(bar_accum, (uint32_t)(committed - 1) & 1u);
     }
-  } else {
-    // ---------------- dequantisation (warps 2..9) and the epilogue of each tile
+  } else if (warp < 2 + kDequantWarps) {
+    // ---------------- dequantisation (warps 2..9): every stage's code tile to FP16 B
     const int t = threadIdx.x - 64;
-    const int dw = warp - 2;
-    const int half = dw >> 2;                     // accumulator: tile rows 128*half ..
-    const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
-    const int m = half * kSubM + quarter * 32 + lane;
-    const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
     bool go = true;
     int spans = 0;                               // scale boxes consumed (TSC)
     const uint32_t zdef = (uint32_t)(1u << (BITS - 1)) << 16;
     for (int j = 0; j < my_works && go; ++j) {
-      int e, row0, n0;
-      tile_of(j, e, row0, n0);
-      // this thread's epilogue row: metadata loaded now, used after the K loop
-      const int rows = min(kBM, ws.offsets[e + 1] - row0);
-      const bool row_ok = m < rows;
-      const int pos = row0 + m;
-      const int rid = row_ok ? ws.sorted_route[pos] : 0;
-      const float sigma = row_ok ? ws.tok_scale[rid / p.k] : 1.0f;
-      const float wr = FC1 ? 0.f : (row_ok ? ws.topk_w[rid] : 0.f);
       for (int i = 0; i < ksteps; ++i) {
         const int it = j * ksteps + i;
         const int s = it % S;
@@ -537,11 +525,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the last stage of a scale box releases the box
         if (TSC && (i % span == span - 1 || i == ksteps - 1)) mbar_arrive(bar_sempty(m_cur & 1));
       }
-      if (!go) break;
-
-      // ---------------- epilogue: TMEM -> registers -> global
+    }
+  } else {
+    // ---------------- epilogue (warps 10..13): warp w reads TMEM lanes 32 (w % 4) ..
+    // of both accumulators, i.e. tile rows q*32 + lane and 128 + q*32 + lane, while
+    // the dequantisers already work on the next tile's stages
+    const int quarter = warp & 3;
+    for (int j = 0; j < my_works; ++j) {
+      int e, row0, n0;
+      tile_of(j, e, row0, n0);
+      const int rows = min(kBM, ws.offsets[e + 1] - row0);
+      int rid_h[2];
+      float sigma_h[2], wr_h[2];
+      bool ok_h[2];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int m = half * kSubM + quarter * 32 + lane;
+        ok_h[half] = m < rows;
+        rid_h[half] = ok_h[half] ? ws.sorted_route[row0 + m] : 0;
+        sigma_h[half] = ok_h[half] ? ws.tok_scale[rid_h[half] / p.k] : 1.0f;
+        wr_h[half] = FC1 ? 0.f : (ok_h[half] ? ws.topk_w[rid_h[half]] : 0.f);
+      }
       if (!mbar_wait(bar_accum, (uint32_t)j & 1u, abort_flag, launch_err)) break;
       tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+      const int pos = row0 + half * kSubM + quarter * 32 + lane;
+      const int rid = rid_h[half];
+      const float sigma = sigma_h[half], wr = wr_h[half];
+      const bool row_ok = ok_h[half];
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
       const float inv = 1.0f / sigma;
       for (int c0 = 0; c0 < C::BN; c0 += 32) {
         uint32_t v[32];
@@ -584,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          __float_as_uint(__uint_as_float(v[8 * q + 6]) * f),
                          __float_as_uint(__uint_as_float(v[8 * q + 7]) * f));
         }
+      }
       }
       tc_fence_before();
       mbar_arrive(bar_drained);                  // the accumulators may be overwritten
