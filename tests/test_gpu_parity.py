@@ -288,3 +288,54 @@ def test_full_size_sampled(which):
         shape, recipe, seed = synthetic.int3_zipf(512, b)
     got, ref = _sampled(shape, recipe, seed, 48)
     gu.assert_parity(got, ref, shape.dtype, which)
+
+
+# ------------------------------------------------------------------ back-to-back calls
+
+def _chain(cases, path, sync_each):
+    """Run the layers in order on one stream, each consuming the previous output,
+    with one shared workspace; return every layer's output bits."""
+    import torch
+    import quantized_mixture_experts_route_gb300 as qm
+
+    shape0 = cases[0][0]
+    p = gu.problem(shape0, path)
+    ws = torch.empty(qm.qmoe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    devs = [gu.device_inputs(inp) for _, inp in cases]
+    outs = [torch.empty((shape0.T, shape0.H), dtype=torch.int16, device="cuda") for _ in cases]
+    x = devs[0]["x"]
+    for (shape, _), d, out in zip(cases, devs, outs):
+        qm.qmoe_forward(p, x, d["logits"], d["fc1_q"], d["fc1_s"], d.get("fc1_zp"), d["fc2_q"], d["fc2_s"],
+                        d.get("fc2_zp"), out, ws)
+        if sync_each:
+            torch.cuda.synchronize()
+        x = out
+    torch.cuda.synchronize()
+    return [o.cpu().numpy().view(np.uint16) for o in outs]
+
+
+@pytest.mark.parametrize("path_name", ["decode", "grouped"])
+def test_back_to_back_layers_match_synchronised_calls(path_name):
+    """Consecutive calls overlap on the GPU (each kernel may start before the
+    previous one ends and waits for it before touching its results). Chained
+    layers launched back to back must give exactly the results of the same calls
+    separated by a device synchronisation, and each layer must match the oracle
+    on the input the GPU actually gave it."""
+    if path_name == "decode":
+        cases = [synthetic.decode_layer(8, l) for l in range(4)]
+        path = 0
+    else:
+        base, recipe, _ = synthetic.decode_layer(8)
+        shape = Shape(**{**base.__dict__, "T": 64})
+        cases = [(shape, recipe, 2000 + l) for l in range(3)]
+        path = 2
+    cases = [(s, synthetic.make_numpy(s, r, seed)) for s, r, seed in cases]
+    fast = _chain(cases, path, sync_each=False)
+    slow = _chain(cases, path, sync_each=True)
+    for l, (a, b) in enumerate(zip(fast, slow)):
+        assert np.array_equal(a, b), f"layer {l}: back-to-back result differs from synchronised calls"
+    prev = cases[0][1]["x"]
+    for l, ((shape, inp), got) in enumerate(zip(cases, fast)):
+        ref, _ = oracle.forward(oproblem(shape), dict(inp, x=prev))
+        gu.assert_parity(got, ref, shape.dtype, f"chained layer {l}")
+        prev = got
