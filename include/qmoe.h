@@ -114,7 +114,19 @@ typedef struct {
  * (0 if *p is invalid). The same value serves both calls. */
 size_t qmoe_workspace_bytes(const qmoe_problem* p);
 
-/* The QMoE layer forward: out = QMoE(x, router_logits, fc1, fc2). */
+/*
+ * The QMoE layer forward: out = QMoE(x, router_logits, fc1, fc2).
+ *
+ * Stream order: the call's kernels are launched with programmatic dependent
+ * launch, so each may start while the previous kernel on `stream` is still
+ * running; every kernel waits for that kernel to complete before it reads
+ * anything the previous kernel writes, except that the routing step reads
+ * `router_logits` early (the logits are an input the layer never writes). A
+ * caller whose own kernel writes `router_logits` directly before this call must
+ * therefore not signal early completion to its dependents (a kernel that does not
+ * use programmatic launch never does). Results are the same as with plain
+ * stream ordering; consecutive calls overlap on the GPU.
+ */
 qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* router_logits,
                          const uint8_t* fc1_q, const void* fc1_scales, const uint8_t* fc1_zp,
                          const uint8_t* fc2_q, const void* fc2_scales, const uint8_t* fc2_zp,
