@@ -53,6 +53,24 @@ def parse():
 
 # --------------------------------------------------------------------------- common
 
+def reduce_max(v, device):
+    """Largest value of v over the ranks of the default process group (the job's
+    time is its slowest rank's); v itself without a process group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(tokens_per_rank_step, world, seconds_per_step):
+    """Whole-job throughput: the tokens of every rank over the slowest rank's step."""
+    return tokens_per_rank_step * world / seconds_per_step
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -363,11 +381,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = t0.elapsed_time(t1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = reduce_max(t0.elapsed_time(t1) / args.steps, device)
 
     # stage durations: CUDA events on the launching stream around `steps` replays of
     # each single-stage graph (every layer's launch of that stage)
@@ -395,11 +409,7 @@ def run_ours(args):
             g.replay()
             out_pin.copy_(final, non_blocking=True)
         s.synchronize()
-    e2e_s = (time.perf_counter() - e2e_t0) / args.steps
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = reduce_max((time.perf_counter() - e2e_t0) / args.steps, device)
 
     if rank != 0:
         if world > 1:
@@ -408,7 +418,7 @@ def run_ours(args):
         return
 
     tokens_per_step = shape.T * layers * world
-    value = tokens_per_step / (ms / 1e3)
+    value = job_rate(shape.T * layers, world, ms / 1e3)
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
