@@ -53,6 +53,15 @@ def parse():
 
 # --------------------------------------------------------------------------- common
 
+def workload_config(args, shape, layers, world):
+    """The `config` object of the bench line (the same for both arms)."""
+    return {"workload": (f"{args.workload}: {layers} QMoE layers H={shape.H} inter={shape.inter} "
+                         f"E={shape.E} k={shape.k} INT{shape.bits} b{shape.block} "
+                         f"{'BF16' if shape.dtype == 0 else 'FP16'} T={shape.T} per rank"),
+            "T": shape.T, "layers": layers, "parallelism": f"replicas x{world}",
+            "l2": "weights 16.3 GB >> L2, no flush" if args.workload == "decode" else "inputs > L2 per step"}
+
+
 def reduce_max(v, device):
     """Largest value of v over the ranks of the default process group (the job's
     time is its slowest rank's); v itself without a process group."""
@@ -249,11 +258,10 @@ def run_reference(args):
     value = statistics.median(per_step)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "layer-tokens/s",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: QMoE H={shape.H} inter={shape.inter} E={shape.E} "
-                               f"k={shape.k} INT{shape.bits} b{shape.block} T={shape.T}"},
+        "config": workload_config(args, shape, layer_count(args), world),
         "cpu_baseline": {**res, "value": value},
         "e2e": {"value": value, "unit": "layer-tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -455,12 +463,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32-acc",
         "data": "synthetic",
-        "config": {"workload": (f"{args.workload}: {layers} QMoE layers H={shape.H} inter={shape.inter} "
-                                f"E={shape.E} k={shape.k} INT{shape.bits} b{shape.block} "
-                                f"{'BF16' if shape.dtype == 0 else 'FP16'} T={shape.T} per rank"),
-                   "T": shape.T, "layers": layers, "parallelism": f"replicas x{world}",
-                   "l2": "weights 16.3 GB >> L2, no flush" if args.workload == "decode" else
-                         "inputs > L2 per step"},
+        "config": workload_config(args, shape, layers, world),
         "roofline": roof,
         "stage_us": {"route_group": round(stage_ms[0] * 1e3, 2), "fc1": round(stage_ms[1] * 1e3, 2),
                      "fc2": round(stage_ms[2] * 1e3, 2), "combine": round(stage_ms[3] * 1e3, 2)},
