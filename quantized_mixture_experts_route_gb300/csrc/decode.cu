@@ -1,32 +1,26 @@
 // decode.cu -- decode path (T <= 8): split-K dequant-GEMV kernels (sm_103a).
 //
 // For each expert that received routes, the selected expert's packed weight
-// rows are streamed from HBM once with wide vector loads (16/12/8 bytes of codes
-// per lane per row), dequantised in registers and multiplied with the <= 8
-// routed activation rows. The pages' decode kernels (MoeGemvTcInt4Kernel,
-// FusedFc1FastVecKernel / Fc2RouteFastVecKernel, "[CUDA] Enable Tensor-Core
-// INT3/INT4 QMoE offload ..." #33731) group <= 8 routes of one expert per CTA and
-// use an m16n8k16 tensor-core step; this kernel keeps that grouping because the
-// eight routes of a T <= 8 batch fit one MMA N-fragment, so every weight byte is
-// read exactly once per call and the tensor core does the multiply-adds.
+// rows are streamed from HBM once, dequantised in registers and multiplied with
+// the <= 8 routed activation rows on the tensor core (m16n8k16 mma.sync). The
+// pages' decode kernels (MoeGemvTcInt4Kernel, FusedFc1FastVecKernel /
+// Fc2RouteFastVecKernel, "[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload ..."
+// #33731) group <= 8 routes of one expert per CTA around an m16n8k16 step; here
+// the decode table pairs the routes of each active expert, so one MMA column pair
+// serves two routes and every weight byte is read exactly once per call.
 //
-// Work split. An item is (active expert, group of 16 weight rows = one MMA
-// M-fragment). Teams of ks warps (ks = 1..8, the K split) walk a static
-// round-robin list of items over a persistent grid of two CTAs per SM; a quad of
-// lanes covers 128 consecutive K of two rows (g, g+8) per chunk, lane c taking
-// codes [32c, 32c+32). Codes stream through a per-warp shared-memory ring of
-// kRing chunks filled by cp.async, so that eight chunks per warp are in flight
-// without holding registers; the next chunk's activations are prefetched into
-// registers; the expert of the next item comes from a decode table written by
-// the routing kernel, so no load waits on another load. K is cut into 8 fixed
-// slices whose FP32 sums are added left to right whatever ks is, so results are
-// bit-reproducible and do not depend on the batch size.
-//
-// Numerics. A weight is (code - zp) * scale: with the code placed in the
-// mantissa of FP16 1024.0, one exact FP16 subtraction gives (code - zp) and one
-// FP16 multiplication by the scale is exact for BF16 scales in the FP16 normal
-// range (at most 11 significant bits). Activations arrive as FP16 scaled by a
-// power of two per token; the MMA accumulates in FP32.
+// Three kernels, by format:
+//   decode_int4_tma_kernel  INT4, block 32, H and I multiples of 256 (the decode
+//       stack's format): units of 16 or 32 weight rows x 256-wide K chunks,
+//       brought into per-warp shared-memory rings by bulk tensor copies; codes
+//       placed in FP16 mantissas and block scales applied in FP32 after the MMA;
+//       stream-K split of the (unit, chunk) range into equal pieces per warp.
+//   decode_int4_bs_kernel   the same arithmetic for other INT4 block-32 shapes
+//       (K a multiple of 128), fed by per-lane cp.async.
+//   decode_gemv_kernel      INT2, INT3 and other block sizes: FP16 dequantised
+//       weights ((code - zp) * scale, exact for BF16 scales in the FP16 normal
+//       range), persistent teams of warps over (expert, 16-row group) items with
+//       K cut into 8 fixed slices added left to right.
 //
 // fc1 epilogue: h_i = silu(gate_i) * up_i from the interleaved rows 2i / 2i+1
 // (activation_type "swiglu", swiglu_fusion = 1), stored in FP16 with the

@@ -1,22 +1,24 @@
 // grouped.cu -- grouped per-expert dequant-GEMM path on tcgen05 (sm_103a).
 //
 // For T > 8 the routes are grouped by expert (sorted order) and cut into tiles
-// of 128 consecutive sorted rows that all belong to one expert, the grouped
+// of 256 consecutive sorted rows that all belong to one expert, the grouped
 // prefill scheme of the pages (BuildInt3ExpertTilesKernel / sorted expert map
 // feeding the grouped GEMMs, "[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload
-// ..." #33731; CUTLASS MoeFCGemm for INT4 prefill). One CTA computes a
-// 128 x BN tile of  D = A * W_e^T  for one expert e:
+// ..." #33731; CUTLASS MoeFCGemm for INT4 prefill). A persistent CTA per SM walks
+// its share of (256-row tile, BN-column tile) works and computes D = A * W_e^T:
 //
-//   warp 0      TMA producer: A tile (FP16 activations, 128B-swizzled) and the
-//               packed code tile of W_e (raw bytes) per K step, into a ring of
-//               shared-memory stages (cp.async.bulk.tensor + mbarrier tx counts);
-//   warp 1      allocates the TMEM accumulator; one lane issues tcgen05.mma
-//               (kind::f16, M=128, N=BN, K=16 per instruction) and commits each
-//               stage back to the producer with tcgen05.commit;
-//   warps 2..5  dequantise the code tile to FP16 in registers ((code - zp) * s,
-//               exact for BF16 scales) and store it in the 128B-swizzled K-major
-//               layout that the MMA descriptor names; after the K loop they read
-//               the accumulator with tcgen05.ld and run the epilogue.
+//   warp 0       TMA producer: per K stage the A tile (FP16 activations,
+//                128B-swizzled), the packed code tile of W_e and, every 8 scale
+//                blocks, a box of block scales (or, with zero points, it loads
+//                scales and zero points itself), into rings of shared-memory
+//                stages (cp.async.bulk.tensor + mbarrier transaction counts);
+//   warp 1       allocates TMEM; one lane issues tcgen05.mma (kind::f16, two
+//                M = 128 accumulators sharing each B stage, N = BN, K = 16) and
+//                commits each stage back to the producer;
+//   warps 2..9   dequantise the code tile to FP16 ((code - zp) * s, exact for
+//                BF16 scales) into the 128B-swizzled K-major B layout;
+//   warps 10..13 after each tile, read the accumulators (tcgen05.ld) and run
+//                the epilogue while warps 2..9 work on the next tile.
 //
 // Operands are FP16 (not BF16): (code - zp) * scale needs up to 11 significant
 // bits, which FP16 holds exactly and BF16 does not; FP16 and BF16 run at the
@@ -24,8 +26,9 @@
 // FP16 store in the K-order permutation of the fc2 operand. fc2 epilogue: FP32
 // rows scaled by the routing weight, stored per route id for the combine.
 //
-// Every mbarrier wait gives up after a bounded number of polls: the CTA then
-// records an error code in the workspace, drains, frees its TMEM and returns.
+// Every mbarrier wait gives up after a bounded time: the CTA then records an
+// error code in the workspace, drains its copies and MMAs in flight, frees its
+// TMEM and returns.
 #include "tma.cuh"
 
 namespace qmoe {

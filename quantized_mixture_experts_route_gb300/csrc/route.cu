@@ -5,8 +5,11 @@
 // so ties go to the lower expert index, and the weights are the softmax over
 // the selected logits ("Document and test packed token inputs for MoE and
 // QMoE" #32522: QMoE receives raw logits; the kernel applies top-k and then
-// normalises, the reference being a softmax over the top-k logits). The same
-// warp also converts its token's activations for the tensor-core matmuls.
+// normalises, the reference being a softmax over the top-k logits). Warps also
+// convert each token's activations to the FP16 operand of the matmuls. For a
+// small batch (at most 512 routes) one block does routing and grouping from the
+// logits alone, in shared memory, while the previous kernel on the stream may
+// still run, and writes the results and converts the activations after it.
 //
 // expert_histogram_scan_permute: a stable counting sort of the T*k route ids by
 // expert (the sorted expert map / expert_first_token_offset that the pages'
