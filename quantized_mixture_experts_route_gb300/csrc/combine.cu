@@ -62,11 +62,7 @@ cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cud
   const int64_t total = p.T * (p.H / 8);
   int64_t blocks = (total + 255) / 256;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-  {
-    const cudaError_t e_ = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p, ws, static_cast<uint16_t*>(out));
-    if (e_ != cudaSuccess) return e_;
-  }
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p, ws, static_cast<uint16_t*>(out));
 }
 
 }  // namespace qmoe

@@ -777,11 +777,7 @@ cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStre
     if (err != cudaSuccess) return err;
     attr = true;
   }
-  {
-    const cudaError_t e_ = launch_pdl(decode_int4_bs_kernel<FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
-    if (e_ != cudaSuccess) return e_;
-  }
-  return cudaGetLastError();
+  return launch_pdl(decode_int4_bs_kernel<FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
 }
 
 int64_t decode_grid_blocks() { return (int64_t)sm_count() * kBlocksPerSmB; }
@@ -1226,11 +1222,7 @@ cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, cons
     attr = true;
   }
   const int64_t blocks = (int64_t)sm_count() * kTBlocksPerSm;
-  {
-    const cudaError_t e_ = launch_pdl(decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem, s, tq, ts, tz, ta, a);
-    if (e_ != cudaSuccess) return e_;
-  }
-  return cudaGetLastError();
+  return launch_pdl(decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem, s, tq, ts, tz, ta, a);
 }
 
 // The tensor-copy variant applies when both matmuls' K are multiples of 256 and
@@ -1328,11 +1320,7 @@ cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     attr = true;
   }
-  {
-    const cudaError_t e_ = launch_pdl(decode_gemv_kernel<BITS, FC1>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
-    if (e_ != cudaSuccess) return e_;
-  }
-  return cudaGetLastError();
+  return launch_pdl(decode_gemv_kernel<BITS, FC1>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
 }
 
 template <int BITS>

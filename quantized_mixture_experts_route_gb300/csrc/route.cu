@@ -503,35 +503,20 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* logits, co
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
   if (p.E <= 128)
-    {
-      const cudaError_t e_ = launch_pdl(route_kernel<4>, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, xx, lg, ws, x16_mode);
-      if (e_ != cudaSuccess) return e_;
-    }
-  else
-    {
-      const cudaError_t e_ = launch_pdl(route_kernel<16>, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, xx, lg, ws, x16_mode);
-      if (e_ != cudaSuccess) return e_;
-    }
-  return cudaGetLastError();
+    return launch_pdl(route_kernel<4>, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, xx, lg, ws, x16_mode);
+  return launch_pdl(route_kernel<16>, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, xx, lg, ws, x16_mode);
 }
 
 cudaError_t launch_group(const Problem& p, const Workspace& ws, bool want_tiles, cudaStream_t s) {
   if (p.R() <= kPermuteChunk) return cudaSuccess;  // done by route_group_small_kernel
   const unsigned nchunks = (unsigned)ws.nchunks;
-  {
-    const cudaError_t e_ = launch_pdl(group_count_kernel, dim3(nchunks), dim3(kGroupThreads), sizeof(int) * p.E, s, p, ws);
-    if (e_ != cudaSuccess) return e_;
-  }
-  {
-    const cudaError_t e_ = launch_pdl(group_scan_kernel, dim3(1), dim3(kGroupThreads), 0, s, p, ws, want_tiles ? 1 : 0);
-    if (e_ != cudaSuccess) return e_;
-  }
+  cudaError_t err =
+      launch_pdl(group_count_kernel, dim3(nchunks), dim3(kGroupThreads), sizeof(int) * p.E, s, p, ws);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(group_scan_kernel, dim3(1), dim3(kGroupThreads), 0, s, p, ws, want_tiles ? 1 : 0);
+  if (err != cudaSuccess) return err;
   const size_t smem = sizeof(int) * (size_t)p.E * (1 + kGroupThreads / 32);
-  {
-    const cudaError_t e_ = launch_pdl(group_scatter_kernel, dim3(nchunks), dim3(kGroupThreads), smem, s, p, ws);
-    if (e_ != cudaSuccess) return e_;
-  }
-  return cudaGetLastError();
+  return launch_pdl(group_scatter_kernel, dim3(nchunks), dim3(kGroupThreads), smem, s, p, ws);
 }
 
 cudaError_t launch_gather(const Problem& p, const Workspace& ws, cudaStream_t s) {
@@ -539,11 +524,7 @@ cudaError_t launch_gather(const Problem& p, const Workspace& ws, cudaStream_t s)
   int64_t blocks = (p.R() + warps - 1) / warps;
   const int64_t cap = (int64_t)num_sms() * 16;
   if (blocks > cap) blocks = cap;
-  {
-    const cudaError_t e_ = launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, ws);
-    if (e_ != cudaSuccess) return e_;
-  }
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(32 * warps), 0, s, p, ws);
 }
 
 }  // namespace qmoe
