@@ -243,6 +243,12 @@ GROUPED_CASES = {
                        Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, explicit_zp=True), 55),
     "g_small_T_forced": (Shape(T=5, H=256, inter=128, E=4, k=2, bits=4, block=32, dtype=BF16),
                          Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 56),
+    # scales by bulk tensor copies with a long scale box (block 128: 16 stages per box)
+    "g_int4_b128_fp16": (Shape(T=300, H=1024, inter=1024, E=4, k=2, bits=4, block=128, dtype=FP16),
+                         Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 57),
+    # ... and a short one (INT3 block 32: 2 stages of K = 128 per box)
+    "g_int3_b32": (Shape(T=260, H=256, inter=256, E=5, k=2, bits=3, block=32, dtype=BF16),
+                   Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 58),
 }
 
 
