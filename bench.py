@@ -43,7 +43,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--workload", choices=["decode", "prefill", "int3", "int2"], default="decode",
+                    help="decode: 48-layer stack; prefill: one 8K layer; int3: one INT3 Zipf layer "
+                         "(--T, --block); int2: one INT2 32K layer")
+    ap.add_argument("--block", type=int, default=64, help="INT3 block size (64 or 128)")
     ap.add_argument("--T", type=int, default=None, help="tokens per step (decode default 8)")
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
@@ -91,6 +94,14 @@ def workload_shape(args):
     if args.workload == "decode":
         T = args.T or 8
         shape, recipe, _ = synthetic.decode_layer(T)
+        return shape, recipe
+    if args.workload == "int3":
+        shape, recipe, _ = synthetic.int3_zipf(args.T or 512, args.block)
+        return shape, recipe
+    if args.workload == "int2":
+        shape, recipe, _ = synthetic.int2_prefill_32k()
+        if args.T:
+            shape.T = args.T
         return shape, recipe
     shape, recipe, _ = synthetic.prefill_8k()
     if args.T:
@@ -238,8 +249,23 @@ def oracle_rate(shape, recipe, args, rank, budget_s):
             done_tokens += len(toks)
             start += batch
         sample = f"{done_tokens} of the {shape.T} prefill tokens of one layer"
+    # the same oracle on one thread, on a small sample: one layer (decode) or 16 tokens
+    if args.workload == "decode":
+        inp1 = dict(weights(0), x=x, logits=logits[0])
+        t0 = time.perf_counter()
+        oracle.forward(op, inp1, nthreads=1)
+        one = shape.T / (time.perf_counter() - t0)
+        one_sample = f"one decode layer x {shape.T} tokens"
+    else:
+        inp1 = dict(weights(0), x=x, logits=logits[0])
+        toks = np.arange(0, min(16, shape.T))
+        t0 = time.perf_counter()
+        oracle.forward(op, inp1, tokens=toks, nthreads=1)
+        one = len(toks) / (time.perf_counter() - t0)
+        one_sample = f"{len(toks)} tokens of one layer"
     return {"value": done_tokens / spent, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
-            "sample": sample, "seconds": round(spent, 2)}
+            "sample": sample, "seconds": round(spent, 2),
+            "single_thread": {"value": one, "sample": one_sample}}
 
 
 def run_reference(args):
@@ -377,19 +403,19 @@ def run_ours(args):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:
         uuid = None
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(uuid) as clocks:
         torch.cuda.synchronize()
         with torch.cuda.stream(s):
-            t0.record()
-            for _ in range(args.steps):
+            marks[0].record()
+            for i in range(args.steps):
                 g.replay()
-            t1.record()
+                marks[i + 1].record()
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = reduce_max(t0.elapsed_time(t1) / args.steps, device)
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
+    ms = reduce_max(marks[0].elapsed_time(marks[-1]) / args.steps, device)
 
     # stage durations: CUDA events on the launching stream around `steps` replays of
     # each single-stage graph (every layer's launch of that stage)
@@ -433,7 +459,8 @@ def run_ours(args):
     except (OSError, ValueError):
         pass
     fc1_b, fc2_b = expert_bytes(shape)
-    if args.workload == "decode":
+    default_kernel = args.workload in ("decode", "prefill")   # the captured kernels' workloads
+    if shape.T <= 8:
         nact = distinct_experts(logits_h, shape.dtype, shape.k)
         # the single-stage graphs run on the routing of the last layer
         bytes_fc1 = float(nact[-1]) * fc1_b
@@ -444,7 +471,8 @@ def run_ours(args):
                 "frac": round(achieved / (hbm if hbm else 6800.0), 4),
                 "peak_source": "measured" if hbm else "fallback",
                 "algorithmic_bytes_per_launch": int(bytes_fc1),
-                "traffic": kernel_traffic("decode_fc1"), "traffic_unit": "bytes per launch (ncu)"}
+                "traffic": kernel_traffic("decode_fc1") if default_kernel else None,
+                "traffic_unit": "bytes per launch (ncu)"}
         extra = {"distinct_experts_per_layer_mean": float(np.mean(nact)),
                  "fc2_GBps": round(float(nact[-1]) * fc2_b / (stage_ms[2] / 1e3) / 1e9, 1),
                  "layer_GBps": round(float(np.mean(nact)) * (fc1_b + fc2_b) / (ms / layers / 1e3) / 1e9, 1)}
@@ -456,11 +484,17 @@ def run_ours(args):
                 "achieved": round(achieved, 1), "peak": tf if tf else 1900.0, "unit": "TFLOP/s",
                 "frac": round(achieved / (tf if tf else 1900.0), 4),
                 "peak_source": "measured" if tf else "fallback", "algorithmic_flops_per_launch": flops,
-                "traffic": kernel_traffic("prefill_fc1"), "traffic_unit": "bytes per launch (ncu)"}
-        extra = {}
+                "traffic": kernel_traffic("prefill_fc1") if default_kernel else None,
+                "traffic_unit": "bytes per launch (ncu)"}
+        # the same launch read as a byte stream: the selected experts' fc1 codes + scales
+        nact = distinct_experts(logits_h, shape.dtype, shape.k)
+        extra = {"fc1_GBps": round(float(nact[-1]) * fc1_b / (stage_ms[1] / 1e3) / 1e9, 1),
+                 "distinct_experts_per_layer_mean": float(np.mean(nact))}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "layer-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "ms_per_step_stats": {"median": round(float(np.median(step_ms)), 4),
+                              "min": round(float(np.min(step_ms)), 4), "max": round(float(np.max(step_ms)), 4)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32-acc",
         "data": "synthetic",
         "config": workload_config(args, shape, layers, world),
