@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(256) route_kernel(Problem p, const uint16_t* _
 // grouping
 // ---------------------------------------------------------------------------
 
-// Exclusive scan of one int per thread over a block of kGroupThreads threads.
+// Exclusive scan of one int per thread over the whole block (up to 1024 threads).
 __device__ int block_exclusive_scan(int v, int* sh /* >= 32 ints */, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -304,34 +304,61 @@ __global__ void __launch_bounds__(kGroupThreads) group_count_kernel(Problem p, W
     ws.chunk_hist[(int64_t)blockIdx.x * p.E + i] = hist[i];
 }
 
-__global__ void __launch_bounds__(kGroupThreads) group_scan_kernel(Problem p, Workspace ws,
-                                                                   int want_tiles) {
+// Per-expert exclusive prefix of the per-chunk counts, plus the expert bases:
+// thread (part, e) sums chunks [nc*part/P, nc*(part+1)/P) of expert e (P parts
+// per expert, coalesced over e), the parts are scanned per expert, and a second
+// pass writes every chunk's base. Loads go eight chunks at a time.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) group_scan_kernel(Problem p, Workspace ws, int want_tiles) {
   pdl_wait();
   pdl_trigger();
   __shared__ int sh[32];
-  const int e = threadIdx.x;
+  __shared__ int part_sum[kScanThreads];
+  __shared__ int expert_base[kMaxExperts];
   const int E = p.E;
-  int total = 0;
-  if (e < E) {
-    // per-expert exclusive prefix over chunks, eight independent loads at a time
-    int32_t* __restrict__ h = ws.chunk_hist;
-    const int64_t nc = ws.nchunks;
-    for (int64_t c0 = 0; c0 < nc; c0 += 8) {
+  int P = 1;
+  while (2 * P * E <= kScanThreads) P *= 2;
+  const int tid = threadIdx.x;
+  const bool active = tid < P * E;
+  const int e = tid % E, part = tid / E;
+  const int64_t nc = ws.nchunks;
+  const int64_t c_lo = nc * part / P, c_hi = nc * (part + 1) / P;
+  int32_t* __restrict__ h = ws.chunk_hist;
+  int sum = 0;
+  if (active)
+    for (int64_t c0 = c_lo; c0 < c_hi; c0 += 8) {
       int v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = c0 + u < nc ? h[(c0 + u) * E + e] : 0;
+      for (int u = 0; u < 8; ++u) v[u] = c0 + u < c_hi ? h[(c0 + u) * E + e] : 0;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (c0 + u < nc) h[(c0 + u) * E + e] = total;
-        total += v[u];
-      }
+      for (int u = 0; u < 8; ++u) sum += v[u];
     }
-  }
-  __shared__ int expert_base[kMaxExperts];
+  part_sum[tid] = active ? sum : 0;
+  __syncthreads();
+  int total = 0;
+  if (tid < E)
+    for (int q = 0; q < P; ++q) {
+      const int v = part_sum[q * E + tid];
+      part_sum[q * E + tid] = total;
+      total += v;
+    }
+  __syncthreads();
   finish_groups(E, total, ws, want_tiles != 0, sh, expert_base);
   __syncthreads();
-  if (e < E)
-    for (int64_t c = 0; c < ws.nchunks; ++c) ws.chunk_hist[c * E + e] += expert_base[e];
+  if (active) {
+    int run = expert_base[e] + part_sum[tid];
+    for (int64_t c0 = c_lo; c0 < c_hi; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = c0 + u < c_hi ? h[(c0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + u < c_hi) {
+          h[(c0 + u) * E + e] = run;
+          run += v[u];
+        }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(Problem p, Workspace ws) {
@@ -445,17 +472,33 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
 __global__ void __launch_bounds__(256) gather_kernel(Problem p, Workspace ws) {
   pdl_wait();
   pdl_trigger();
-  // x16s[pos] = x16[token of sorted route pos]; one warp per row, 16 bytes per lane
+  // x16s[pos] = x16[token of sorted route pos]; one warp per row, 16 bytes per
+  // lane per access. Each lane issues all its loads of a 4-KB piece of the row
+  // before its stores, so eight loads per lane are in flight at once.
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t R = p.R();
   const int chunks = p.H / 8;
+  const uint16_t* __restrict__ x16 = ws.x16;
+  uint16_t* __restrict__ x16s = ws.x16s;
   for (int64_t pos = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); pos < R;
        pos += (int64_t)gridDim.x * warps) {
     const int64_t t = ws.sorted_route[pos] / p.k;
-    const uint4* src = reinterpret_cast<const uint4*>(ws.x16 + t * p.H);
-    uint4* dst = reinterpret_cast<uint4*>(ws.x16s + pos * p.H);
-    for (int c = lane; c < chunks; c += 32) dst[c] = src[c];
+    const uint4* __restrict__ src = reinterpret_cast<const uint4*>(x16 + t * p.H);
+    uint4* __restrict__ dst = reinterpret_cast<uint4*>(x16s + pos * p.H);
+    for (int c0 = 0; c0 < chunks; c0 += 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) v[u] = src[c];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) dst[c] = v[u];
+      }
+    }
   }
 }
 
@@ -513,7 +556,7 @@ cudaError_t launch_group(const Problem& p, const Workspace& ws, bool want_tiles,
   cudaError_t err =
       launch_pdl(group_count_kernel, dim3(nchunks), dim3(kGroupThreads), sizeof(int) * p.E, s, p, ws);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(group_scan_kernel, dim3(1), dim3(kGroupThreads), 0, s, p, ws, want_tiles ? 1 : 0);
+  err = launch_pdl(group_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, p, ws, want_tiles ? 1 : 0);
   if (err != cudaSuccess) return err;
   const size_t smem = sizeof(int) * (size_t)p.E * (1 + kGroupThreads / 32);
   return launch_pdl(group_scatter_kernel, dim3(nchunks), dim3(kGroupThreads), smem, s, p, ws);
