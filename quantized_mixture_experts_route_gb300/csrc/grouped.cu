@@ -7,14 +7,16 @@
 // ..." #33731; CUTLASS MoeFCGemm for INT4 prefill). A persistent CTA per SM walks
 // its share of (256-row tile, BN-column tile) works and computes D = A * W_e^T:
 //
-//   warp 0       TMA producer: per K stage the A tile (FP16 activations,
-//                128B-swizzled), the packed code tile of W_e and, every 8 scale
-//                blocks, a box of block scales (or, with zero points, it loads
-//                scales and zero points itself), into rings of shared-memory
-//                stages (cp.async.bulk.tensor + mbarrier transaction counts);
+//   warp 0       code producer: per K stage the packed code tile of W_e and,
+//                every 8 scale blocks, a box of block scales (or, with zero
+//                points, it loads the stage's scales and zero points itself);
+//   warp 14      activation producer: per K stage the A tile (FP16
+//                activations, 128B-swizzled);
+//                both by cp.async.bulk.tensor into rings of shared-memory slots
+//                with mbarrier transaction counts;
 //   warp 1       allocates TMEM; one lane issues tcgen05.mma (kind::f16, two
 //                M = 128 accumulators sharing each B stage, N = BN, K = 16) and
-//                commits each stage back to the producer;
+//                commits each stage's A and B slots back to their writers;
 //   warps 2..9   dequantise the code tile to FP16 ((code - zp) * s, exact for
 //                BF16 scales) into the 128B-swizzled K-major B layout;
 //   warps 10..13 after each tile, read the accumulators (tcgen05.ld) and run
@@ -40,7 +42,8 @@ constexpr int kDequantWarps = 8;       // warps 2..9
 constexpr int kDequantThreads = 32 * kDequantWarps;
 constexpr int kEpiWarps = 4;           // warps 10..13
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 64 + kDequantThreads + kEpiThreads;
+constexpr int kAProdWarp = 2 + kDequantWarps + kEpiWarps;   // warp 14
+constexpr int kThreads = 32 * (kAProdWarp + 1);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
 constexpr int kErrTimeout = 1;
@@ -54,7 +57,13 @@ template <int BITS, bool TSC = false>
 struct Cfg {
   static constexpr int BK = BITS == 3 ? 128 : 64;     // K per stage
   static constexpr int BN = BITS == 3 ? 128 : 256;    // weight rows per tile (MMA N)
-  static constexpr int STAGES = BITS == 3 ? 2 : 3;
+  // Three rings: activation tiles (read by the MMAs), code tiles (read by the
+  // dequantisers) and dequantised B tiles (written by the dequantisers, read by
+  // the MMAs). The B ring only spans dequantisation to MMA; the two rings fed by
+  // copies are deeper, so that more copies are in flight per SM.
+  static constexpr int SA = BITS == 3 ? 2 : 4;
+  static constexpr int SC = BITS == 3 ? 2 : (BITS == 4 ? 3 : 4);
+  static constexpr int SB = 2;
   static constexpr int SUB = BK / 64;                 // 64-wide swizzle atoms per stage
   static constexpr int A_BYTES = kBM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
@@ -67,12 +76,13 @@ struct Cfg {
   static constexpr int S_BYTES = UNITS * 4;           // per unit: FP16 scale | zero point << 16
   static constexpr int SC_BYTES = BN * 16;            // one scale box: [BN][8] 16-bit scales
   static constexpr int A_OFF = 0;
-  static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
-  static constexpr int C_OFF = B_OFF + STAGES * B_BYTES;
-  static constexpr int S_OFF = C_OFF + STAGES * C_BYTES;
-  static constexpr int BAR_OFF = S_OFF + (TSC ? 2 * SC_BYTES : STAGES * S_BYTES);
-  static constexpr int SMEM = BAR_OFF + 128 + 1024;   // barriers + TMEM address + alignment slack
-  static_assert(8 * (3 * STAGES + 2 + 4) + 8 <= 128, "barrier area");
+  static constexpr int B_OFF = A_OFF + SA * A_BYTES;
+  static constexpr int C_OFF = B_OFF + SB * B_BYTES;
+  static constexpr int S_OFF = C_OFF + SC * C_BYTES;
+  static constexpr int BAR_OFF = S_OFF + (TSC ? 2 * SC_BYTES : SC * S_BYTES);
+  static constexpr int NBARS = 2 * (SA + SC + SB) + 2 + 4;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;   // barriers + TMEM address + alignment slack
+  static_assert(8 * NBARS + 8 <= 256, "barrier area");
   static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
   static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -278,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_trigger();
   using C = Cfg<BITS, TSC>;
-  constexpr int S = C::STAGES;
+  constexpr int SA = C::SA, SB = C::SB, SC = C::SC;
   const Workspace& ws = g.ws;
   const Problem& p = g.p;
   volatile int* launch_err = ws.counters + 2;   // set by a CTA whose wait timed out
@@ -294,25 +304,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::BAR_OFF;
-  // [0, S): TMA + scales landed; [S, 2S): B dequantised; [2S, 3S): stage free;
-  // [3S]: accumulators ready; [3S+1]: accumulators drained by the epilogue
-  auto bar_full = [&](int s) { return bar0 + 8u * s; };
-  auto bar_bready = [&](int s) { return bar0 + 8u * (S + s); };
-  auto bar_empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  const uint32_t bar_accum = bar0 + 8u * (3 * S);
-  const uint32_t bar_drained = bar0 + 8u * (3 * S + 1);
-  // scale ring (TSC): [3S+2, 3S+4) box landed; [3S+4, 3S+6) box read by the dequantisers
-  auto bar_sfull = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-  auto bar_sempty = [&](int b) { return bar0 + 8u * (3 * S + 4 + b); };
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * (3 * S + 6));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * (3 * S + 6) + 4);
+  // activation ring: landed / read by the MMAs; code ring: landed (with the
+  // stage's scales) / read by the dequantisers; B ring: dequantised / read by the
+  // MMAs; then accumulators ready / drained by the epilogue, and the scale-box
+  // ring (TSC): box landed / box read by the dequantisers
+  auto bar_afull = [&](int s) { return bar0 + 8u * s; };
+  auto bar_aempty = [&](int s) { return bar0 + 8u * (SA + s); };
+  auto bar_cfull = [&](int s) { return bar0 + 8u * (2 * SA + s); };
+  auto bar_cempty = [&](int s) { return bar0 + 8u * (2 * SA + SC + s); };
+  auto bar_bready = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SC + s); };
+  auto bar_bempty = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SC + SB + s); };
+  constexpr int kAcc = 2 * (SA + SC + SB);
+  const uint32_t bar_accum = bar0 + 8u * kAcc;
+  const uint32_t bar_drained = bar0 + 8u * (kAcc + 1);
+  auto bar_sfull = [&](int b) { return bar0 + 8u * (kAcc + 2 + b); };
+  auto bar_sempty = [&](int b) { return bar0 + 8u * (kAcc + 4 + b); };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBARS + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(bar_full(s), TSC ? 1 : 1 + 32);   // the TMA issue (with its byte count) [+ 32 scale writers]
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(bar_afull(s), 1);                 // the copy issue (with its byte count)
+      mbar_init(bar_aempty(s), 1);                // MMA commit
+    }
+    for (int s = 0; s < SC; ++s) {
+      mbar_init(bar_cfull(s), TSC ? 1 : 1 + 32);  // the copy issue [+ 32 scale writers]
+      mbar_init(bar_cempty(s), kDequantThreads);
+    }
+    for (int s = 0; s < SB; ++s) {
       mbar_init(bar_bready(s), kDequantThreads);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_bempty(s), 1);                // MMA commit
     }
     mbar_init(bar_accum, 1);
     mbar_init(bar_drained, kEpiThreads);
@@ -348,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    // ---------------- producer: TMA (lane 0) and each stage's scales (all lanes)
+    // ---------------- code producer: per stage the code tile (lane 0) and either a
+    // scale box every `span` stages (lane 0) or the stage's scales (all lanes)
     int issued = 0, spans = 0;
     bool go = true;
     for (int j = 0; j < my_works && go; ++j) {
@@ -358,10 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t wrow_end = (int64_t)p.E * N;
       for (int i = 0; i < ksteps; ++i) {
         const int it = j * ksteps + i;           // stage sequence number across tiles
-        const int s = it % S;
-        const uint32_t ph = (uint32_t)(it / S) & 1u;
+        const int s = it % SC;
+        const uint32_t ph = (uint32_t)(it / SC) & 1u;
         int ok = 1;
-        if (lane == 0) ok = mbar_wait(bar_empty(s), ph ^ 1u, abort_flag, launch_err) ? 1 : 0;
+        if (lane == 0) ok = mbar_wait(bar_cempty(s), ph ^ 1u, abort_flag, launch_err) ? 1 : 0;
         const int k0 = i * C::BK;
         if (TSC && i % span == 0) {
           // next scale box, into the ring slot the dequantisers released
@@ -379,14 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__shfl_sync(0xffffffffu, ok, 0) == 0) { go = false; break; }
         ++issued;
         if (lane == 0) {
-          mbar_expect_tx(bar_full(s), C::A_BYTES + C::C_BYTES);
-#pragma unroll
-          for (int sub = 0; sub < C::SUB; ++sub)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
-                          bar_full(s), k0 + 64 * sub, row0 + h * kSubM);
-          tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_full(s), k0 * BITS / 8, e * N + n0);
+          mbar_expect_tx(bar_cfull(s), C::C_BYTES);
+          tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_cfull(s), k0 * BITS / 8, e * N + n0);
         }
         if constexpr (TSC) continue;
         uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
@@ -412,36 +429,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   : sv[q];
           st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
         }
-        mbar_arrive(bar_full(s));
+        mbar_arrive(bar_cfull(s));
       }
     }
     if (lane == 0 && *abort_flag) {
       // let the copies already issued land before the CTA exits
-      for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i)
-        mbar_wait_drain(bar_full(i % S), (uint32_t)(i / S) & 1u);
+      for (int i = issued - SC > 0 ? issued - SC : 0; i < issued; ++i)
+        mbar_wait_drain(bar_cfull(i % SC), (uint32_t)(i / SC) & 1u);
       if (TSC)
         for (int m = spans - 2 > 0 ? spans - 2 : 0; m < spans; ++m)
           mbar_wait_drain(bar_sfull(m & 1), (uint32_t)(m >> 1) & 1u);
+    }
+  } else if (warp == kAProdWarp) {
+    // ---------------- activation producer (lane 0): per stage the two 128-row halves
+    // of the A tile
+    if (lane == 0) {
+      int issued = 0;
+      bool go = true;
+      for (int j = 0; j < my_works && go; ++j) {
+        int e, row0, n0;
+        tile_of(j, e, row0, n0);
+        for (int i = 0; i < ksteps; ++i) {
+          const int it = j * ksteps + i;
+          const int s = it % SA;
+          const uint32_t ph = (uint32_t)(it / SA) & 1u;
+          if (!mbar_wait(bar_aempty(s), ph ^ 1u, abort_flag, launch_err)) { go = false; break; }
+          ++issued;
+          const int k0 = i * C::BK;
+          mbar_expect_tx(bar_afull(s), C::A_BYTES);
+#pragma unroll
+          for (int sub = 0; sub < C::SUB; ++sub)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
+                          bar_afull(s), k0 + 64 * sub, row0 + h * kSubM);
+        }
+      }
+      if (*abort_flag)
+        for (int i = issued - SA > 0 ? issued - SA : 0; i < issued; ++i)
+          mbar_wait_drain(bar_afull(i % SA), (uint32_t)(i / SA) & 1u);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: two 128-row accumulators share each B stage
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(kSubM, C::BN);
       bool go = true;
-      int committed = 0;
+      int accum_commits = 0;
+      bool pending = false;                      // MMAs issued since the last accumulator commit
       for (int j = 0; j < my_works && go; ++j) {
         // the epilogue of the previous tile has read the accumulators
         if (j > 0 && !mbar_wait(bar_drained, (uint32_t)(j - 1) & 1u, abort_flag, launch_err)) break;
         tc_fence_after();
         for (int i = 0; i < ksteps; ++i) {
           const int it = j * ksteps + i;
-          const int s = it % S;
-          const uint32_t ph = (uint32_t)(it / S) & 1u;
-          if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err) ||
-              !mbar_wait(bar_bready(s), ph, abort_flag, launch_err)) { go = false; break; }
+          const int sa = it % SA, sb = it % SB;
+          if (!mbar_wait(bar_afull(sa), (uint32_t)(it / SA) & 1u, abort_flag, launch_err) ||
+              !mbar_wait(bar_bready(sb), (uint32_t)(it / SB) & 1u, abort_flag, launch_err)) { go = false; break; }
           tc_fence_after();
-          const uint32_t a_base = sbase + C::A_OFF + s * C::A_BYTES;
-          const uint32_t b_base = sbase + C::B_OFF + s * C::B_BYTES;
+          const uint32_t a_base = sbase + C::A_OFF + sa * C::A_BYTES;
+          const uint32_t b_base = sbase + C::B_OFF + sb * C::B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             const int sub = kk / 4, off = (kk % 4) * 32;
@@ -451,13 +497,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma(tmem + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
                      idesc, (i | kk) != 0);
           }
-          tc_commit(bar_empty(s));
+          pending = true;
+          tc_commit(bar_aempty(sa));
+          tc_commit(bar_bempty(sb));
         }
+        if (!go) break;
         tc_commit(bar_accum);
-        ++committed;
+        ++accum_commits;
+        pending = false;
       }
       // MMAs in flight finish before TMEM is freed
-      if (*abort_flag && committed > 0) mbar_wait_drain(bar_accum, (uint32_t)(committed - 1) & 1u);
+      if (*abort_flag) {
+        if (pending) {
+          tc_commit(bar_accum);
+          ++accum_commits;
+        }
+        if (accum_commits > 0) mbar_wait_drain(bar_accum, (uint32_t)(accum_commits - 1) & 1u);
+      }
     }
   } else if (warp < 2 + kDequantWarps) {
     // ---------------- dequantisation (warps 2..9): every stage's code tile to FP16 B
@@ -468,9 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < my_works && go; ++j) {
       for (int i = 0; i < ksteps; ++i) {
         const int it = j * ksteps + i;
-        const int s = it % S;
-        const uint32_t ph = (uint32_t)(it / S) & 1u;
-        if (!mbar_wait(bar_full(s), ph, abort_flag, launch_err)) { go = false; break; }
+        const int cs = it % SC, bs = it % SB;
+        if (!mbar_wait(bar_cfull(cs), (uint32_t)(it / SC) & 1u, abort_flag, launch_err)) { go = false; break; }
         const int m_sp = spans;                  // scale box of this stage (TSC)
         if (TSC && i % span == 0) {
           ++spans;
@@ -479,13 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
+        // the MMAs have finished reading this B slot's previous stage
+        if (!mbar_wait(bar_bempty(bs), ((uint32_t)(it / SB) & 1u) ^ 1u, abort_flag, launch_err)) {
+          go = false;
+          break;
+        }
         const int m_cur = TSC ? spans - 1 : 0;
         // [BN rows][8] scales of this box; this stage's first block within it
         const uint16_t* sbox = reinterpret_cast<const uint16_t*>(smem + C::S_OFF + (m_cur & 1) * C::SC_BYTES);
         const int b_first = (i % span) * C::BK / p.block;
-        const uint8_t* codes = smem + C::C_OFF + s * C::C_BYTES;
-        const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
-        uint8_t* bt = smem + C::B_OFF + s * C::B_BYTES;
+        const uint8_t* codes = smem + C::C_OFF + cs * C::C_BYTES;
+        const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + cs * C::S_BYTES);
+        uint8_t* bt = smem + C::B_OFF + bs * C::B_BYTES;
 #pragma unroll
         for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
           const int unit = t + kDequantThreads * u;
@@ -524,7 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async();
-        mbar_arrive(bar_bready(s));
+        mbar_arrive(bar_bready(bs));
+        mbar_arrive(bar_cempty(cs));
         // the last stage of a scale box releases the box
         if (TSC && (i % span == span - 1 || i == ksteps - 1)) mbar_arrive(bar_sempty(m_cur & 1));
       }
