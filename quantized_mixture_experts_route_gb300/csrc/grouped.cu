@@ -10,17 +10,18 @@
 //   warp 0       code producer: per K stage the packed code tile of W_e and,
 //                every 8 scale blocks, a box of block scales (or, with zero
 //                points, it loads the stage's scales and zero points itself);
-//   warp 14      activation producer: per K stage the A tile (FP16
+//   warp 22      activation producer: per K stage the A tile (FP16
 //                activations, 128B-swizzled);
 //                both by cp.async.bulk.tensor into rings of shared-memory slots
 //                with mbarrier transaction counts;
 //   warp 1       allocates TMEM; one lane issues tcgen05.mma (kind::f16, two
 //                M = 128 accumulators sharing each B stage, N = BN, K = 16) and
 //                commits each stage's A and B slots back to their writers;
-//   warps 2..9   dequantise the code tile to FP16 ((code - zp) * s, exact for
-//                BF16 scales) into the 128B-swizzled K-major B layout;
-//   warps 10..13 after each tile, read the accumulators (tcgen05.ld) and run
-//                the epilogue while warps 2..9 work on the next tile.
+//   warps 2..17  dequantise the code tile to FP16 ((code - zp) * s, exact for
+//                BF16 scales) into the 128B-swizzled K-major B layout, in two
+//                groups of 8 warps that take alternate stages;
+//   warps 18..21 after each tile, read the accumulators (tcgen05.ld) and run
+//                the epilogue while warps 2..17 work on the next tile.
 //
 // Operands are FP16 (not BF16): (code - zp) * scale needs up to 11 significant
 // bits, which FP16 holds exactly and BF16 does not; FP16 and BF16 run at the
@@ -38,11 +39,12 @@ namespace {
 
 constexpr int kSubM = 128;             // rows per MMA / TMEM accumulator
 constexpr int kBM = 2 * kSubM;         // rows per tile: two accumulators share each B stage
-constexpr int kDequantWarps = 8;       // warps 2..9
-constexpr int kDequantThreads = 32 * kDequantWarps;
-constexpr int kEpiWarps = 4;           // warps 10..13
+constexpr int kGroupWarps = 8;         // one dequantisation group
+constexpr int kDequantWarps = 2 * kGroupWarps;   // warps 2..17: two groups taking alternate stages
+constexpr int kDequantThreads = 32 * kGroupWarps;  // threads of one group (one stage)
+constexpr int kEpiWarps = 4;           // warps 18..21: one per TMEM lane quarter
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kAProdWarp = 2 + kDequantWarps + kEpiWarps;   // warp 14
+constexpr int kAProdWarp = 2 + kDequantWarps + kEpiWarps;   // warp 22
 constexpr int kThreads = 32 * (kAProdWarp + 1);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
@@ -61,9 +63,9 @@ struct Cfg {
   // dequantisers) and dequantised B tiles (written by the dequantisers, read by
   // the MMAs). The B ring only spans dequantisation to MMA; the two rings fed by
   // copies are deeper, so that more copies are in flight per SM.
-  static constexpr int SA = BITS == 3 ? 2 : 4;
+  static constexpr int SA = BITS == 3 ? 2 : 3;
   static constexpr int SC = BITS == 3 ? 2 : (BITS == 4 ? 3 : 4);
-  static constexpr int SB = 2;
+  static constexpr int SB = BITS == 3 ? 2 : 3;
   static constexpr int SUB = BK / 64;                 // 64-wide swizzle atoms per stage
   static constexpr int A_BYTES = kBM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_drained, kEpiThreads);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_sfull(b), 1);
-      mbar_init(bar_sempty(b), kDequantThreads);
+      mbar_init(bar_sempty(b), 2 * kDequantThreads);   // both groups (a group alone arrives twice)
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -407,27 +409,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (TSC) continue;
         uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
-        // all loads first (independent, no branches), then convert and store
+        // per batch of 8: all loads first (independent, no branches), then convert and store
         constexpr int PER_LANE = C::UNITS / 32;
-        uint16_t sv[PER_LANE];
-        uint8_t zv[PER_LANE];
+        constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;
+        static_assert(PER_LANE % BATCH == 0, "scale batches");
+#pragma unroll 1
+        for (int q0 = 0; q0 < PER_LANE; q0 += BATCH) {
+          uint16_t sv[BATCH];
+          uint8_t zv[BATCH];
 #pragma unroll
-        for (int q = 0; q < PER_LANE; ++q) {
-          const int u = lane + 32 * q;
-          const int r = u / C::UNITS_PER_ROW, jj = u % C::UNITS_PER_ROW;
-          const int64_t wr = min(wrow_base + r, wrow_end - 1);   // rows past the array: masked below
-          const int64_t idx = wr * nblk + (k0 + 32 * jj) / p.block;
-          sv[q] = __ldg(g.scales + idx);
-          zv[q] = g.zp ? __ldg(g.zp + idx) : (uint8_t)(1u << (BITS - 1));
-        }
+          for (int q = 0; q < BATCH; ++q) {
+            const int u = lane + 32 * (q0 + q);
+            const int r = u / C::UNITS_PER_ROW, jj = u % C::UNITS_PER_ROW;
+            const int64_t wr = min(wrow_base + r, wrow_end - 1);   // rows past the array: masked below
+            const int64_t idx = wr * nblk + (k0 + 32 * jj) / p.block;
+            sv[q] = __ldg(g.scales + idx);
+            zv[q] = g.zp ? __ldg(g.zp + idx) : (uint8_t)(1u << (BITS - 1));
+          }
 #pragma unroll
-        for (int q = 0; q < PER_LANE; ++q) {
-          const int u = lane + 32 * q;
-          const int r = u / C::UNITS_PER_ROW;
-          const uint16_t sh = p.dtype == QMOE_BF16
-                                  ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sv[q] << 16)))
-                                  : sv[q];
-          st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
+          for (int q = 0; q < BATCH; ++q) {
+            const int u = lane + 32 * (q0 + q);
+            const int r = u / C::UNITS_PER_ROW;
+            const uint16_t sh = p.dtype == QMOE_BF16
+                                    ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sv[q] << 16)))
+                                    : sv[q];
+            st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
+          }
         }
         mbar_arrive(bar_cfull(s));
       }
@@ -516,20 +523,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 2 + kDequantWarps) {
-    // ---------------- dequantisation (warps 2..9): every stage's code tile to FP16 B
-    const int t = threadIdx.x - 64;
+    // ---------------- dequantisation (warps 2..17): every stage's code tile to FP16 B.
+    // Two groups of 8 warps take alternate stages (group g the stages whose
+    // sequence number is g mod 2), so that one group's waits overlap the other's work.
+    const int grp = (warp - 2) / kGroupWarps;
+    const int t = threadIdx.x - 64 - grp * kDequantThreads;
     bool go = true;
-    int spans = 0;                               // scale boxes consumed (TSC)
+    int box_seen = -1;                           // last scale box waited for (TSC)
+    const int nbox = (ksteps + span - 1) / span; // scale boxes per tile (TSC)
     const uint32_t zdef = (uint32_t)(1u << (BITS - 1)) << 16;
     for (int j = 0; j < my_works && go; ++j) {
       for (int i = 0; i < ksteps; ++i) {
         const int it = j * ksteps + i;
+        if ((it & 1) != grp) continue;
         const int cs = it % SC, bs = it % SB;
         if (!mbar_wait(bar_cfull(cs), (uint32_t)(it / SC) & 1u, abort_flag, launch_err)) { go = false; break; }
-        const int m_sp = spans;                  // scale box of this stage (TSC)
-        if (TSC && i % span == 0) {
-          ++spans;
-          if (!mbar_wait(bar_sfull(m_sp & 1), (uint32_t)(m_sp >> 1) & 1u, abort_flag, launch_err)) {
+        const int m_cur = j * nbox + i / span;   // scale box of this stage (TSC), in issue order
+        if (TSC && m_cur != box_seen) {
+          box_seen = m_cur;
+          if (!mbar_wait(bar_sfull(m_cur & 1), (uint32_t)(m_cur >> 1) & 1u, abort_flag, launch_err)) {
             go = false;
             break;
           }
@@ -539,7 +551,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           go = false;
           break;
         }
-        const int m_cur = TSC ? spans - 1 : 0;
         // [BN rows][8] scales of this box; this stage's first block within it
         const uint16_t* sbox = reinterpret_cast<const uint16_t*>(smem + C::S_OFF + (m_cur & 1) * C::SC_BYTES);
         const int b_first = (i % span) * C::BK / p.block;
@@ -586,15 +597,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         mbar_arrive(bar_bready(bs));
         mbar_arrive(bar_cempty(cs));
-        // the last stage of a scale box releases the box
-        if (TSC && (i % span == span - 1 || i == ksteps - 1)) mbar_arrive(bar_sempty(m_cur & 1));
+        // a group's last stage in a scale box releases the box for the group; a box
+        // of one stage has one group, which arrives for both
+        if (TSC) {
+          const int box0 = (i / span) * span;
+          const int box_end = min(box0 + span, ksteps);
+          if (i + 2 >= box_end) mbar_arrive_cnt(bar_sempty(m_cur & 1), box_end - box0 >= 2 ? 1u : 2u);
+        }
       }
     }
   } else {
-    // ---------------- epilogue (warps 10..13): warp w reads TMEM lanes 32 (w % 4) ..
+    // ---------------- epilogue (warps 18..21): warp w reads TMEM lanes 32 (w % 4) ..
     // of both accumulators, i.e. tile rows q*32 + lane and 128 + q*32 + lane, while
     // the dequantisers already work on the next tile's stages
     const int quarter = warp & 3;
+    const int cpart = (warp - 2 - kDequantWarps) >> 2;   // with 4k epilogue warps: chunks cpart, cpart + k, ...
     for (int j = 0; j < my_works; ++j) {
       int e, row0, n0;
       tile_of(j, e, row0, n0);
@@ -620,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = ok_h[half];
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
       const float inv = 1.0f / sigma;
-      for (int c0 = 0; c0 < C::BN; c0 += 32) {
+      for (int c0 = 32 * cpart; c0 < C::BN; c0 += 32 * (kEpiWarps / 4)) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)c0, v);
         if (!row_ok || n0 + c0 >= N) continue;
