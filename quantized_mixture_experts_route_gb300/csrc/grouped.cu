@@ -21,7 +21,9 @@
 //                BF16 scales) into the 128B-swizzled K-major B layout, in two
 //                groups of 8 warps that take alternate stages;
 //   warps 18..21 after each tile, read the accumulators (tcgen05.ld) and run
-//                the epilogue while warps 2..17 work on the next tile.
+//                the epilogue while warps 2..17 work on the next tile; with
+//                128-row weight tiles (INT3) the accumulators are double
+//                buffered and the MMAs of the next tile run meanwhile too.
 //
 // Operands are FP16 (not BF16): (code - zp) * scale needs up to 11 significant
 // bits, which FP16 holds exactly and BF16 does not; FP16 and BF16 run at the
@@ -55,10 +57,16 @@ static_assert(kBM == kTileM, "the grouping kernels cut tiles of kTileM sorted ro
 // scales a multiple of 16 bytes): one [BN rows][8 scales] box covers 8 blocks
 // along K (a "scale span" of 8*block/BK stages) in a ring of two; otherwise the
 // producer warp loads scales and zero points per stage and stores FP16 words.
-template <int BITS, bool TSC = false>
+template <int BITS, bool TSC, bool FC1>
 struct Cfg {
   static constexpr int BK = BITS == 3 ? 128 : 64;     // K per stage
-  static constexpr int BN = BITS == 3 ? 128 : 256;    // weight rows per tile (MMA N)
+  // Weight rows per tile (MMA N). With 128 (INT3), a tile's two accumulators
+  // take 256 TMEM columns, so two tiles' accumulators fit (ACC = 2) and the
+  // epilogue of one tile overlaps the MMAs of the next. INT4 / INT2 keep 256 and
+  // one accumulator buffer: 128 there (double-buffered) measured slower for fc2,
+  // as every activation tile then feeds half as many MMAs.
+  static constexpr int BN = BITS == 3 ? 128 : 256;
+  static constexpr int ACC = 4 * BN <= 512 ? 2 : 1;   // accumulator buffers
   // Three rings: activation tiles (read by the MMAs), code tiles (read by the
   // dequantisers) and dequantised B tiles (written by the dequantisers, read by
   // the MMAs). The B ring only spans dequantisation to MMA; the two rings fed by
@@ -82,10 +90,10 @@ struct Cfg {
   static constexpr int C_OFF = B_OFF + SB * B_BYTES;
   static constexpr int S_OFF = C_OFF + SC * C_BYTES;
   static constexpr int BAR_OFF = S_OFF + (TSC ? 2 * SC_BYTES : SC * S_BYTES);
-  static constexpr int NBARS = 2 * (SA + SC + SB) + 2 + 4;
+  static constexpr int NBARS = 2 * (SA + SC + SB) + 2 * ACC + 4;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;   // barriers + TMEM address + alignment slack
   static_assert(8 * NBARS + 8 <= 256, "barrier area");
-  static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
+  static constexpr int TMEM_COLS = 2 * BN * ACC;      // two accumulators per tile
   static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_s, GemmArgs g) {
   pdl_wait();
   pdl_trigger();
-  using C = Cfg<BITS, TSC>;
+  using C = Cfg<BITS, TSC, FC1>;
   constexpr int SA = C::SA, SB = C::SB, SC = C::SC;
   const Workspace& ws = g.ws;
   const Problem& p = g.p;
@@ -317,10 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_bready = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SC + s); };
   auto bar_bempty = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SC + SB + s); };
   constexpr int kAcc = 2 * (SA + SC + SB);
-  const uint32_t bar_accum = bar0 + 8u * kAcc;
-  const uint32_t bar_drained = bar0 + 8u * (kAcc + 1);
-  auto bar_sfull = [&](int b) { return bar0 + 8u * (kAcc + 2 + b); };
-  auto bar_sempty = [&](int b) { return bar0 + 8u * (kAcc + 4 + b); };
+  auto bar_accum = [&](int b) { return bar0 + 8u * (kAcc + b); };
+  auto bar_drained = [&](int b) { return bar0 + 8u * (kAcc + C::ACC + b); };
+  auto bar_sfull = [&](int b) { return bar0 + 8u * (kAcc + 2 * C::ACC + b); };
+  auto bar_sempty = [&](int b) { return bar0 + 8u * (kAcc + 2 * C::ACC + 2 + b); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBARS + 4);
 
@@ -338,8 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_bready(s), kDequantThreads);
       mbar_init(bar_bempty(s), 1);                // MMA commit
     }
-    mbar_init(bar_accum, 1);
-    mbar_init(bar_drained, kEpiThreads);
+    for (int b = 0; b < C::ACC; ++b) {
+      mbar_init(bar_accum(b), 1);
+      mbar_init(bar_drained(b), kEpiThreads);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_sfull(b), 1);
       mbar_init(bar_sempty(b), 2 * kDequantThreads);   // both groups (a group alone arrives twice)
@@ -481,12 +491,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(kSubM, C::BN);
       bool go = true;
-      int accum_commits = 0;
+      int commits0 = 0, commits1 = 0;            // accumulator commits per buffer
+      int buf = 0;
       bool pending = false;                      // MMAs issued since the last accumulator commit
       for (int j = 0; j < my_works && go; ++j) {
-        // the epilogue of the previous tile has read the accumulators
-        if (j > 0 && !mbar_wait(bar_drained, (uint32_t)(j - 1) & 1u, abort_flag, launch_err)) break;
+        buf = j % C::ACC;
+        // the epilogue has read this buffer's previous tile
+        if (j >= C::ACC &&
+            !mbar_wait(bar_drained(buf), (uint32_t)(j / C::ACC - 1) & 1u, abort_flag, launch_err))
+          break;
         tc_fence_after();
+        const uint32_t acc0 = tmem + (uint32_t)(buf * 2 * C::BN);
         for (int i = 0; i < ksteps; ++i) {
           const int it = j * ksteps + i;
           const int sa = it % SA, sb = it % SB;
@@ -501,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = sw128_desc(b_base + sub * (C::BN * 128) + off);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tc_mma(tmem + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
+              tc_mma(acc0 + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
                      idesc, (i | kk) != 0);
           }
           pending = true;
@@ -509,17 +524,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(bar_bempty(sb));
         }
         if (!go) break;
-        tc_commit(bar_accum);
-        ++accum_commits;
+        tc_commit(bar_accum(buf));
+        if (buf == 0) ++commits0; else ++commits1;
         pending = false;
       }
       // MMAs in flight finish before TMEM is freed
       if (*abort_flag) {
         if (pending) {
-          tc_commit(bar_accum);
-          ++accum_commits;
+          tc_commit(bar_accum(buf));
+          if (buf == 0) ++commits0; else ++commits1;
         }
-        if (accum_commits > 0) mbar_wait_drain(bar_accum, (uint32_t)(accum_commits - 1) & 1u);
+        if (commits0 > 0) mbar_wait_drain(bar_accum(0), (uint32_t)(commits0 - 1) & 1u);
+        if (commits1 > 0) mbar_wait_drain(bar_accum(1), (uint32_t)(commits1 - 1) & 1u);
       }
     }
   } else if (warp < 2 + kDequantWarps) {
@@ -627,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sigma_h[half] = ok_h[half] ? ws.tok_scale[rid_h[half] / p.k] : 1.0f;
         wr_h[half] = FC1 ? 0.f : (ok_h[half] ? ws.topk_w[rid_h[half]] : 0.f);
       }
-      if (!mbar_wait(bar_accum, (uint32_t)j & 1u, abort_flag, launch_err)) break;
+      const int buf = j % C::ACC;
+      if (!mbar_wait(bar_accum(buf), (uint32_t)(j / C::ACC) & 1u, abort_flag, launch_err)) break;
       tc_fence_after();
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -635,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rid = rid_h[half];
       const float sigma = sigma_h[half], wr = wr_h[half];
       const bool row_ok = ok_h[half];
-      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * C::BN);
+      const uint32_t tbase =
+          tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * 2 * C::BN + half * C::BN);
       const float inv = 1.0f / sigma;
       for (int c0 = 32 * cpart; c0 < C::BN; c0 += 32 * (kEpiWarps / 4)) {
         uint32_t v[32];
@@ -681,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       }
       tc_fence_before();
-      mbar_arrive(bar_drained);                  // the accumulators may be overwritten
+      mbar_arrive(bar_drained(buf));             // the accumulators may be overwritten
     }
   }
 
@@ -698,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BITS, bool FC1, bool TSC>
 cudaError_t launch_gemm_t(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
                           const Workspace& ws, cudaStream_t s) {
-  using C = Cfg<BITS, TSC>;
+  using C = Cfg<BITS, TSC, FC1>;
   const int N = FC1 ? 2 * p.I : p.H;
   const int K = FC1 ? p.H : p.I;
   const int64_t R = p.R();
