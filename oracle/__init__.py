@@ -44,7 +44,7 @@ def build(force: bool = False) -> str:
 class _Problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("bits", ctypes.c_int32),
-                ("block", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("block", ctypes.c_int32), ("dtype", ctypes.c_int32), ("full_softmax", ctypes.c_int32)]
 
 
 
@@ -67,9 +67,15 @@ def _declare(L):
     L.oracle_expert_ffn.argtypes = [P(_Problem), vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp,
                                     vp, vp]
     L.oracle_expert_ffn.restype = None
+    L.oracle_expert_ffn_bias.argtypes = [P(_Problem), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp,
+                                         vp, vp, vp]
+    L.oracle_expert_ffn_bias.restype = None
     L.oracle_forward.argtypes = [P(_Problem), vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                  ctypes.c_int64, vp, vp, ctypes.c_int]
     L.oracle_forward.restype = ctypes.c_int
+    L.oracle_forward_bias.argtypes = [P(_Problem), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.c_int64, vp, vp, ctypes.c_int]
+    L.oracle_forward_bias.restype = ctypes.c_int
     L.oracle_num_cores.argtypes = []
     L.oracle_num_cores.restype = ctypes.c_int
     return L
@@ -85,9 +91,11 @@ class Problem:
     bits: int
     block: int
     dtype: int
+    full_softmax: int = 0   # 1: normalize_routing_weights = 0 (weights under the softmax over all E)
 
     def c(self) -> _Problem:
-        return _Problem(self.T, self.H, self.inter, self.E, self.k, self.bits, self.block, self.dtype)
+        return _Problem(self.T, self.H, self.inter, self.E, self.k, self.bits, self.block, self.dtype,
+                        self.full_softmax)
 
 
 def _ptr(a):
@@ -101,6 +109,11 @@ def _weights(inp):
     c = lambda a, dt: None if a is None else np.ascontiguousarray(a, dtype=dt)
     return (c(inp["fc1_q"], np.uint8), c(inp["fc1_s"], np.uint16), c(inp.get("fc1_zp"), np.uint8),
             c(inp["fc2_q"], np.uint8), c(inp["fc2_s"], np.uint16), c(inp.get("fc2_zp"), np.uint8))
+
+
+def _biases(inp):
+    c = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.uint16)
+    return c(inp.get("fc1_b")), c(inp.get("fc2_b"))
 
 
 class Oracle:
@@ -155,14 +168,15 @@ class Oracle:
         return offsets, sorted_route, route_slot
 
     def expert_ffn(self, p: Problem, inp: dict, expert: int, x_row: np.ndarray):
-        w = _weights(inp)
+        q1, s1, z1, q2, s2, z2 = _weights(inp)
+        b1, b2 = _biases(inp)
         xr = np.ascontiguousarray(x_row, dtype=np.float64)
         gu = np.zeros(2 * p.inter)
         h = np.zeros(p.inter)
         y = np.zeros(p.H)
         pc = p.c()
-        self.L.oracle_expert_ffn(ctypes.byref(pc), *[_ptr(a) for a in w], expert, _ptr(xr),
-                                 _ptr(gu), _ptr(h), _ptr(y))
+        self.L.oracle_expert_ffn_bias(ctypes.byref(pc), *[_ptr(a) for a in (q1, s1, z1, b1, q2, s2, z2, b2)],
+                                      expert, _ptr(xr), _ptr(gu), _ptr(h), _ptr(y))
         return gu, h, y
 
     def forward(self, p: Problem, inp: dict, tokens=None, nthreads: int = 0, want_acc: bool = False):
@@ -175,8 +189,11 @@ class Oracle:
         out = np.zeros((n, p.H), dtype=np.uint16)
         acc = np.zeros((n, p.H), dtype=np.float64) if want_acc else None
         pc = p.c()
-        if self.L.oracle_forward(ctypes.byref(pc), _ptr(x), _ptr(lg), *[_ptr(a) for a in w],
-                                 _ptr(tok), n, _ptr(out), _ptr(acc), nthreads) != 0:
+        q1, s1, z1, q2, s2, z2 = w
+        b1, b2 = _biases(inp)
+        if self.L.oracle_forward_bias(ctypes.byref(pc), _ptr(x), _ptr(lg),
+                                      *[_ptr(a) for a in (q1, s1, z1, b1, q2, s2, z2, b2)],
+                                      _ptr(tok), n, _ptr(out), _ptr(acc), nthreads) != 0:
             raise ValueError("oracle_forward: invalid arguments")
         return out, acc
 

@@ -21,7 +21,13 @@
  *    scales_are_block_major=false);
  *  - the combine keeps the partial sum unrounded and rounds to BF16/FP16 once,
  *    NaN stays NaN, zero-weight routes add nothing (#33973 key change 4 and
- *    review fixes).
+ *    review fixes);
+ *  - optional FC1 / FC2 biases [E, 2I] and [E, H] in the activation dtype, the
+ *    FC2 bias indexed by the route's expert and added before the one rounding
+ *    (#33575 commit notes: bias validation, "original-expert-indexed FC2 bias
+ *    before FP16/BF16 rounding"); normalize_routing_weights = 0 kept covered by
+ *    the tests (#32522 review), read as the weights being the selected experts'
+ *    probabilities under the softmax over all E logits, not renormalised.
  */
 #define _GNU_SOURCE
 #include "qmoe_oracle.h"
@@ -163,12 +169,17 @@ static void route_token(const oracle_problem* p, const uint16_t* lrow, int32_t* 
     idx[j] = best;
   }
   free(taken);
-  /* softmax over the k selected logits, shifted by the largest one */
+  /* softmax over the k selected logits, shifted by the largest one; with
+   * full_softmax the denominator runs over all E logits instead */
   const double l0 = oracle_bits_to_double(lrow[idx[0]], p->dtype);
   double denom = 0.0;
   for (int j = 0; j < k; ++j) {
     w[j] = exp(oracle_bits_to_double(lrow[idx[j]], p->dtype) - l0);
     denom += w[j];
+  }
+  if (p->full_softmax) {
+    denom = 0.0;
+    for (int e = 0; e < E; ++e) denom += exp(oracle_bits_to_double(lrow[e], p->dtype) - l0);
   }
   for (int j = 0; j < k; ++j) w[j] /= denom;
 }
@@ -179,6 +190,7 @@ static int valid_problem(const oracle_problem* p) {
   if (p->block <= 0 || p->H % p->block || p->inter % p->block) return 0;
   if (p->H % 8 || p->inter % 8) return 0;
   if (p->dtype != ORACLE_BF16 && p->dtype != ORACLE_FP16) return 0;
+  if (p->full_softmax != 0 && p->full_softmax != 1) return 0;
   return 1;
 }
 
@@ -223,6 +235,14 @@ void oracle_expert_ffn(const oracle_problem* p, const uint8_t* fc1_q, const uint
                        const uint8_t* fc1_zp, const uint8_t* fc2_q, const uint16_t* fc2_s,
                        const uint8_t* fc2_zp, int expert, const double* x_row, double* gu,
                        double* h, double* y) {
+  oracle_expert_ffn_bias(p, fc1_q, fc1_s, fc1_zp, NULL, fc2_q, fc2_s, fc2_zp, NULL, expert, x_row, gu,
+                         h, y);
+}
+
+void oracle_expert_ffn_bias(const oracle_problem* p, const uint8_t* fc1_q, const uint16_t* fc1_s,
+                            const uint8_t* fc1_zp, const uint16_t* fc1_b, const uint8_t* fc2_q,
+                            const uint16_t* fc2_s, const uint8_t* fc2_zp, const uint16_t* fc2_b,
+                            int expert, const double* x_row, double* gu, double* h, double* y) {
   const int H = p->H, I = p->inter;
   const int64_t rows1 = 2 * (int64_t)I, rows2 = H;
   double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
@@ -232,6 +252,7 @@ void oracle_expert_ffn(const oracle_problem* p, const uint8_t* fc1_q, const uint
                        (int64_t)expert * rows1 + n, wrow);
     double acc = 0.0;
     for (int kk = 0; kk < H; ++kk) acc += wrow[kk] * x_row[kk];
+    if (fc1_b) acc += oracle_bits_to_double(fc1_b[(int64_t)expert * rows1 + n], p->dtype);
     gu[n] = acc;
   }
   for (int i = 0; i < I; ++i) h[i] = silu(gu[2 * i]) * gu[2 * i + 1];
@@ -241,6 +262,7 @@ void oracle_expert_ffn(const oracle_problem* p, const uint8_t* fc1_q, const uint
                        (int64_t)expert * rows2 + m, wrow);
     double acc = 0.0;
     for (int i = 0; i < I; ++i) acc += wrow[i] * h[i];
+    if (fc2_b) acc += oracle_bits_to_double(fc2_b[(int64_t)expert * rows2 + m], p->dtype);
     y[m] = acc;
   }
   free(wrow);
@@ -248,7 +270,7 @@ void oracle_expert_ffn(const oracle_problem* p, const uint8_t* fc1_q, const uint
 
 typedef struct {
   const oracle_problem* p;
-  const uint16_t *x, *logits, *fc1_s, *fc2_s;
+  const uint16_t *x, *logits, *fc1_s, *fc2_s, *fc1_b, *fc2_b;
   const uint8_t *fc1_q, *fc1_zp, *fc2_q, *fc2_zp;
   const int64_t* tokens;
   int64_t n;
@@ -267,8 +289,8 @@ static void forward_token(const fwd_job* J, int64_t slot, double* xr, double* gu
   for (int m = 0; m < H; ++m) acc[m] = 0.0;
   for (int j = 0; j < p->k; ++j) {
     if (w[j] == 0.0) continue; /* a zero-weight route adds nothing */
-    oracle_expert_ffn(p, J->fc1_q, J->fc1_s, J->fc1_zp, J->fc2_q, J->fc2_s, J->fc2_zp, idx[j], xr,
-                      gu, h, y);
+    oracle_expert_ffn_bias(p, J->fc1_q, J->fc1_s, J->fc1_zp, J->fc1_b, J->fc2_q, J->fc2_s, J->fc2_zp,
+                           J->fc2_b, idx[j], xr, gu, h, y);
     for (int m = 0; m < H; ++m) acc[m] += w[j] * y[m];
   }
   for (int m = 0; m < H; ++m) {
@@ -310,6 +332,15 @@ int oracle_forward(const oracle_problem* p, const uint16_t* x, const uint16_t* l
                    const uint8_t* fc2_q, const uint16_t* fc2_s, const uint8_t* fc2_zp,
                    const int64_t* tokens, int64_t n_tokens, uint16_t* out_bits, double* out_acc,
                    int nthreads) {
+  return oracle_forward_bias(p, x, logits, fc1_q, fc1_s, fc1_zp, NULL, fc2_q, fc2_s, fc2_zp, NULL,
+                             tokens, n_tokens, out_bits, out_acc, nthreads);
+}
+
+int oracle_forward_bias(const oracle_problem* p, const uint16_t* x, const uint16_t* logits,
+                        const uint8_t* fc1_q, const uint16_t* fc1_s, const uint8_t* fc1_zp,
+                        const uint16_t* fc1_b, const uint8_t* fc2_q, const uint16_t* fc2_s,
+                        const uint8_t* fc2_zp, const uint16_t* fc2_b, const int64_t* tokens,
+                        int64_t n_tokens, uint16_t* out_bits, double* out_acc, int nthreads) {
   if (!valid_problem(p) || !out_bits) return -1;
   const int64_t n = tokens ? n_tokens : p->T;
   if (n < 0) return -1;
@@ -318,7 +349,7 @@ int oracle_forward(const oracle_problem* p, const uint16_t* x, const uint16_t* l
       if (tokens[i] < 0 || tokens[i] >= p->T) return -1;
   if (n == 0) return 0;
   if (!x || !logits || !fc1_q || !fc1_s || !fc2_q || !fc2_s) return -1;
-  fwd_job J = {p, x, logits, fc1_s, fc2_s, fc1_q, fc1_zp, fc2_q, fc2_zp, tokens, n,
+  fwd_job J = {p, x, logits, fc1_s, fc2_s, fc1_b, fc2_b, fc1_q, fc1_zp, fc2_q, fc2_zp, tokens, n,
                out_bits, out_acc, 0};
   int nt = nthreads > 0 ? nthreads : oracle_num_cores();
   if (nt > n) nt = (int)n;

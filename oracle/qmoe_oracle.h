@@ -42,6 +42,9 @@ typedef struct {
   int32_t bits;    /* 2, 3 or 4 */
   int32_t block;   /* block size along K */
   int32_t dtype;   /* ORACLE_BF16 / ORACLE_FP16: x, logits, scales, out */
+  int32_t full_softmax; /* 0: weights = softmax over the k selected logits (renormalised);
+                           1: normalize_routing_weights = 0, each selected expert's
+                           probability under the softmax over all E logits */
 } oracle_problem;
 
 /* 16-bit float <-> double. */
@@ -68,6 +71,13 @@ void oracle_expert_ffn(const oracle_problem* p, const uint8_t* fc1_q, const uint
                        const uint8_t* fc2_zp, int expert, const double* x_row, double* gu,
                        double* h, double* y);
 
+/* The same with optional biases in the layer's dtype (NULL: none): fc1_b [E][2I]
+ * is added to gate/up before SwiGLU, fc2_b [E][H] to the expert output. */
+void oracle_expert_ffn_bias(const oracle_problem* p, const uint8_t* fc1_q, const uint16_t* fc1_s,
+                            const uint8_t* fc1_zp, const uint16_t* fc1_b, const uint8_t* fc2_q,
+                            const uint16_t* fc2_s, const uint8_t* fc2_zp, const uint16_t* fc2_b,
+                            int expert, const double* x_row, double* gu, double* h, double* y);
+
 /*
  * The layer forward for the tokens listed in `tokens` (NULL: all T tokens, in
  * order). out_bits [n][H] receives the rounded outputs, out_acc [n][H] (may be
@@ -79,6 +89,13 @@ int oracle_forward(const oracle_problem* p, const uint16_t* x, const uint16_t* l
                    const uint8_t* fc2_q, const uint16_t* fc2_s, const uint8_t* fc2_zp,
                    const int64_t* tokens, int64_t n_tokens, uint16_t* out_bits, double* out_acc,
                    int nthreads);
+
+/* oracle_forward with optional biases fc1_b [E][2I] and fc2_b [E][H] (NULL: none). */
+int oracle_forward_bias(const oracle_problem* p, const uint16_t* x, const uint16_t* logits,
+                        const uint8_t* fc1_q, const uint16_t* fc1_s, const uint8_t* fc1_zp,
+                        const uint16_t* fc1_b, const uint8_t* fc2_q, const uint16_t* fc2_s,
+                        const uint8_t* fc2_zp, const uint16_t* fc2_b, const int64_t* tokens,
+                        int64_t n_tokens, uint16_t* out_bits, double* out_acc, int nthreads);
 
 /* Number of cores in the calling process's affinity mask. */
 int oracle_num_cores(void);

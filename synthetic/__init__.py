@@ -58,6 +58,7 @@ class Recipe:
     scale_hi: float = 0.02
     explicit_zp: bool = False         # False: zero point is the implicit 2^(bits-1)
     seq_lens: list[int] | None = None  # packed sequence lengths (sum == T), for the packing tests
+    bias_std: float | None = None     # FC1 [E, 2I] and FC2 [E, H] biases ~ N(0, bias_std); None: no biases
     extra: dict = field(default_factory=dict)
 
 
@@ -137,8 +138,13 @@ def make_numpy(shape: Shape, recipe: Recipe, seed: int) -> dict:
     fc2_q = codes(E * H, I)
     fc2_s = scales(E * H, I)
     fc2_zp = zps(E * H, I)
+    # biases come last, so that the other inputs do not depend on whether they are drawn
+    fc1_b = fc2_b = None
+    if recipe.bias_std is not None:
+        fc1_b = float_to_bits(rng.standard_normal((E, 2 * I)) * recipe.bias_std, dt)
+        fc2_b = float_to_bits(rng.standard_normal((E, H)) * recipe.bias_std, dt)
     return dict(x=x, logits=logits, fc1_q=fc1_q, fc1_s=fc1_s, fc1_zp=fc1_zp,
-                fc2_q=fc2_q, fc2_s=fc2_s, fc2_zp=fc2_zp)
+                fc2_q=fc2_q, fc2_s=fc2_s, fc2_zp=fc2_zp, fc1_b=fc1_b, fc2_b=fc2_b)
 
 
 def make_torch_weights(shape: Shape, recipe: Recipe, seed: int, device):

@@ -52,7 +52,8 @@ def dequant_matrix(q, s, zp, bits, block, dtype, rows, K) -> np.ndarray:
 
 
 def dense_expert(inp, shape, e, xrow):
-    """gu, h, y of expert e for one input row in torch float64 (matmul + library SiLU)."""
+    """gu, h, y of expert e for one input row in torch float64 (matmul + library SiLU),
+    with the optional biases fc1_b / fc2_b added after each matmul."""
     H, I = shape.H, shape.inter
     W1 = dequant_matrix(inp["fc1_q"][e], inp["fc1_s"][e], None if inp["fc1_zp"] is None else inp["fc1_zp"][e],
                         shape.bits, shape.block, shape.dtype, 2 * I, H)
@@ -62,9 +63,13 @@ def dense_expert(inp, shape, e, xrow):
     W2 = torch.from_numpy(W2)
     x = torch.from_numpy(np.asarray(xrow, dtype=np.float64))
     gu = W1 @ x
+    if inp.get("fc1_b") is not None:
+        gu = gu + torch.from_numpy(bits_to_f64(inp["fc1_b"][e], shape.dtype))
     gate, up = gu[0::2], gu[1::2]
     h = torch.nn.functional.silu(gate) * up
     y = W2 @ h
+    if inp.get("fc2_b") is not None:
+        y = y + torch.from_numpy(bits_to_f64(inp["fc2_b"][e], shape.dtype))
     return gu.numpy(), h.numpy(), y.numpy()
 
 
@@ -257,9 +262,11 @@ def pin_permute(orc):
             fail("route_slot is not the inverse of sorted_route")
 
 
-def _small_inputs(T=5, H=64, I=96, E=6, k=3, bits=4, block=32, dt=BF16, seed=21, explicit_zp=False):
+def _small_inputs(T=5, H=64, I=96, E=6, k=3, bits=4, block=32, dt=BF16, seed=21, explicit_zp=False,
+                  bias_std=None):
     shape = synthetic.Shape(T=T, H=H, inter=I, E=E, k=k, bits=bits, block=block, dtype=dt)
-    rec = synthetic.Recipe(x_std=1.0, logit_std=1.5, scale_lo=0.01, scale_hi=0.05, explicit_zp=explicit_zp)
+    rec = synthetic.Recipe(x_std=1.0, logit_std=1.5, scale_lo=0.01, scale_hi=0.05, explicit_zp=explicit_zp,
+                           bias_std=bias_std)
     return shape, synthetic.make_numpy(shape, rec, seed)
 
 
@@ -371,6 +378,69 @@ def pin_zero_weight_route_skipped(orc):
         fail("single surviving route with weight 1")
 
 
+def pin_full_softmax_routing(orc):
+    """normalize_routing_weights = 0: each selected expert's weight is its
+    probability under the softmax over all E logits (scipy), the selection is
+    unchanged, and with k = E both readings give the full softmax."""
+    rng = np.random.default_rng(8)
+    for dt in (BF16, FP16):
+        T, E, k = 7, 9, 3
+        lv = rng.standard_normal((T, E)) * 2.0
+        lg = _logits_bits(lv, dt)
+        lvq = bits_to_f64(lg, dt)
+        p = oracle_mod.Problem(T, 64, 32, E, k, 4, 32, dt, full_softmax=1)
+        idx, w = orc.route(p, lg)
+        idx_n, w_n = orc.route(oracle_mod.Problem(T, 64, 32, E, k, 4, 32, dt), lg)
+        if not np.array_equal(idx, idx_n):
+            fail("full softmax changes the selection")
+        for t in range(T):
+            full = scipy.special.softmax(lvq[t])
+            if not np.allclose(w[t], full[idx[t]], rtol=1e-12, atol=0):
+                fail(f"full-softmax weights of token {t}")
+        pk = oracle_mod.Problem(T, 64, 32, E, E, 4, 32, dt, full_softmax=1)
+        _, wk = orc.route(pk, lg)
+        _, wk_n = orc.route(oracle_mod.Problem(T, 64, 32, E, E, 4, 32, dt), lg)
+        if not np.allclose(wk, wk_n, rtol=1e-12, atol=0):
+            fail("k = E: full softmax and renormalised weights differ")
+
+
+def pin_biases_dense_over_experts(orc):
+    """FC1 / FC2 biases: every expert for every token with the biases added after
+    each matmul (torch float64), under both routing-weight readings."""
+    for bits, block, dt, full in ((4, 32, BF16, 0), (2, 32, FP16, 1), (3, 64, BF16, 1)):
+        shape, inp = _small_inputs(T=5, H=128, I=64, E=5, k=2, bits=bits, block=block, dt=dt, bias_std=0.5)
+        p = problem_of(shape)
+        p.full_softmax = full
+        _, acc = orc.forward(p, inp, nthreads=2, want_acc=True)
+        x = bits_to_f64(inp["x"], dt)
+        lv = bits_to_f64(inp["logits"], dt)
+        for t in range(shape.T):
+            sel = sorted(range(shape.E), key=lambda e: (-lv[t, e], e))[: shape.k]
+            wsel = scipy.special.softmax(lv[t])[sel] if full else scipy.special.softmax(lv[t, sel])
+            total = np.zeros(shape.H)
+            for e, w in zip(sel, wsel):
+                total += w * dense_expert(inp, shape, e, x[t])[2]
+            if not np.allclose(acc[t], total, rtol=1e-11, atol=1e-12):
+                fail(f"biased layer bits={bits} full_softmax={full} token {t}")
+
+
+def pin_fc2_bias_with_zero_weights(orc):
+    """All weights zero (zero point equal to every code): each route's expert output
+    is its FC2 bias, whatever the FC1 bias, so the layer gives sum_j w_j b2[e_j]."""
+    shape, inp = _small_inputs(T=4, H=64, I=32, E=4, k=2, bits=4, block=32, explicit_zp=True, bias_std=1.0)
+    inp = dict(inp)
+    for name, zpn in (("fc1_q", "fc1_zp"), ("fc2_q", "fc2_zp")):
+        inp[name] = np.full_like(inp[name], 0x33)  # every code 3
+        inp[zpn] = np.full_like(inp[zpn], 3)
+    p = problem_of(shape)
+    idx, w = orc.route(p, inp["logits"])
+    _, acc = orc.forward(p, inp, nthreads=1, want_acc=True)
+    b2 = bits_to_f64(inp["fc2_b"], shape.dtype)
+    want = np.einsum("tj,tjh->th", w, b2[idx])
+    if not np.allclose(acc, want, rtol=1e-14, atol=0):
+        fail("zero weights with biases: output is not the weighted FC2 biases")
+
+
 def pin_nan_propagates(orc):
     shape, inp = _small_inputs(T=2, H=64, I=32, E=4, k=2, dt=BF16)
     inp = dict(inp)
@@ -388,5 +458,6 @@ ALL_PINS = [
     pin_rounding_fp16_exhaustive, pin_rounding_bf16, pin_dequant, pin_golden_routing,
     pin_route_bruteforce, pin_permute, pin_dense_ffn_E1_k1, pin_bruteforce_dense_over_experts,
     pin_one_hot, pin_token_permutation, pin_zero_weights, pin_zero_weight_route_skipped,
-    pin_nan_propagates,
+    pin_nan_propagates, pin_full_softmax_routing, pin_biases_dense_over_experts,
+    pin_fc2_bias_with_zero_weights,
 ]

@@ -23,7 +23,7 @@ MUTANTS = {
     "nibble_order": ("(kk % 2) ? (b >> 4) : (b & 0xF)", "(kk % 2) ? (b & 0xF) : (b >> 4)"),
     "scale_index": ("scales[row * nblk + b]", "scales[row + b]"),
     "silu_sign": ("z / (1.0 + exp(-z))", "z / (1.0 + exp(z))"),
-    "fc1_expert_stride": ("(int64_t)expert * rows1 + n", "(int64_t)expert * rows2 + n"),
+    "fc1_expert_stride": ("(int64_t)expert * rows1 + n, wrow);", "(int64_t)expert * rows2 + n, wrow);"),
     "int3_field_order": ("(group >> (3 * (kk % 8))) & 0x7", "(group >> (3 * (7 - kk % 8))) & 0x7"),
     "int2_field_width": ("(b >> (2 * (kk % 4))) & 0x3", "(b >> (kk % 4)) & 0x3"),
     "ties_away_from_zero": ("rint(a / quantum)", "floor(a / quantum + 0.5)"),
@@ -34,6 +34,12 @@ MUTANTS = {
     "fp16_bias": ("const int bias = dtype == ORACLE_BF16 ? 127 : 15;", "const int bias = dtype == ORACLE_BF16 ? 127 : 16;"),
     "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     "fc2_reads_gate": ("for (int i = 0; i < I; ++i) acc += wrow[i] * h[i];", "for (int i = 0; i < I; ++i) acc += wrow[i] * gu[2 * i];"),
+    "fc1_bias_dropped": ("    if (fc1_b) acc += oracle_bits_to_double(fc1_b[(int64_t)expert * rows1 + n], p->dtype);\n", ""),
+    "fc1_bias_gate_up_swapped": ("fc1_b[(int64_t)expert * rows1 + n]", "fc1_b[(int64_t)expert * rows1 + (n ^ 1)]"),
+    "fc2_bias_dropped": ("    if (fc2_b) acc += oracle_bits_to_double(fc2_b[(int64_t)expert * rows2 + m], p->dtype);\n", ""),
+    "fc2_bias_wrong_expert": ("fc2_b[(int64_t)expert * rows2 + m]", "fc2_b[m]"),
+    "full_softmax_ignored": ("  if (p->full_softmax) {", "  if (0) {"),
+    "full_softmax_last_expert_dropped": ("for (int e = 0; e < E; ++e) denom += exp(", "for (int e = 0; e + 1 < E; ++e) denom += exp("),
     "x_not_read_per_token": ("xr[kk] = oracle_bits_to_double(J->x[t * H + kk], p->dtype);", "xr[kk] = oracle_bits_to_double(J->x[kk], p->dtype);"),
 }
 
