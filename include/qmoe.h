@@ -133,6 +133,44 @@ qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* route
                          void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Options of qmoe_forward_ex. A zero-filled struct gives qmoe_forward.
+ *
+ * full_softmax: 0 -- the routing weights are the softmax over the k selected
+ *   logits (renormalised over the top-k); 1 -- normalize_routing_weights = 0:
+ *   each selected expert's weight is its probability under the softmax over all
+ *   E logits of the token, not renormalised ("[CUDA] Document and test packed
+ *   token inputs for MoE and QMoE" #32522, review: keep normalize_routing_weights
+ *   = 0 covered). A NaN logit anywhere in the row then makes the row's weights NaN.
+ * fc1_bias: [E][2*inter] in dtype, row 2j the gate and 2j+1 the up bias of
+ *   SwiGLU unit j, added to the fc1 output before SwiGLU; NULL: none.
+ * fc2_bias: [E][hidden] in dtype, added to each route's expert output before
+ *   the routing weight and the one final rounding; NULL: none ("[CUDA] Add INT4
+ *   and INT3 QMoE CPU/GPU offload support" #33575, commit notes: biases
+ *   validated as [E, 2*I] and [E, H] in the activation dtype, the FC2 bias
+ *   indexed by the route's original expert and applied before the FP16/BF16
+ *   rounding).
+ * Bias pointers are caller-owned device memory, 16-byte aligned
+ * (QMOE_ERR_MISALIGNED otherwise), and only read.
+ */
+typedef struct {
+  int32_t full_softmax;
+  const void* fc1_bias;
+  const void* fc2_bias;
+} qmoe_options;
+
+/*
+ * qmoe_forward with options (opt may be NULL: the defaults). Extra errors:
+ * QMOE_ERR_INVALID_ARGUMENT if opt->full_softmax is not 0 or 1. The pages
+ * define no separate entry point for these options; this one carries them so
+ * that qmoe_forward keeps its signature.
+ */
+qmoe_status qmoe_forward_ex(const qmoe_problem* p, const qmoe_options* opt, const void* x,
+                            const void* router_logits, const uint8_t* fc1_q, const void* fc1_scales,
+                            const uint8_t* fc1_zp, const uint8_t* fc2_q, const void* fc2_scales,
+                            const uint8_t* fc2_zp, void* out, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * Stages of qmoe_forward: ROUTE (top-k routing, grouping by expert and the
  * activations' FP16 conversion), FC1 (fc1 dequant-matmul with the SwiGLU
  * epilogue), FC2 (fc2 dequant-matmul, weighted by the routing weight) and

@@ -42,7 +42,7 @@ QMOE_PATH_GROUPED = 2
 
 # every symbol the header declares
 EXPORTED = ("qmoe_workspace_bytes", "qmoe_forward", "qmoe_forward_stages", "qmoe_route",
-            "qmoe_status_string", "qmoe_forward_decode_static")
+            "qmoe_status_string", "qmoe_forward_decode_static", "qmoe_forward_ex")
 
 QMOE_STATIC_WORKSPACE_BYTES = 8 << 20
 
@@ -63,6 +63,10 @@ class qmoe_problem(ctypes.Structure):
                 ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("bits", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("path", ctypes.c_int32)]
+
+
+class qmoe_options(ctypes.Structure):
+    _fields_ = [("full_softmax", ctypes.c_int32), ("fc1_bias", ctypes.c_void_p), ("fc2_bias", ctypes.c_void_p)]
 
 
 def problem(T, hidden, inter, num_experts, top_k, bits, block_size, dtype, path=QMOE_PATH_AUTO):
@@ -94,6 +98,9 @@ def lib():
         L.qmoe_route.restype = ctypes.c_int
         L.qmoe_forward_decode_static.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.qmoe_forward_decode_static.restype = ctypes.c_int
+        L.qmoe_forward_ex.argtypes = [P, ctypes.POINTER(qmoe_options), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.c_size_t, vp]
+        L.qmoe_forward_ex.restype = ctypes.c_int
         L.qmoe_status_string.argtypes = [ctypes.c_int]
         L.qmoe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -144,6 +151,17 @@ def qmoe_forward(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, f
                             _nbytes(workspace) if workspace is not None else 0, _stream(stream))
     if st != QMOE_OK:
         raise QMoEError(st, "qmoe_forward")
+
+
+def qmoe_forward_ex(p: qmoe_problem, full_softmax: int, fc1_bias, fc2_bias, x, router_logits, fc1_q,
+                    fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, stream=None) -> None:
+    opt = qmoe_options(int(full_softmax), _addr(fc1_bias), _addr(fc2_bias))
+    st = lib().qmoe_forward_ex(ctypes.byref(p), ctypes.byref(opt), _addr(x), _addr(router_logits),
+                               _addr(fc1_q), _addr(fc1_scales), _addr(fc1_zp), _addr(fc2_q),
+                               _addr(fc2_scales), _addr(fc2_zp), _addr(out), _addr(workspace),
+                               _nbytes(workspace) if workspace is not None else 0, _stream(stream))
+    if st != QMOE_OK:
+        raise QMoEError(st, "qmoe_forward_ex")
 
 
 def qmoe_forward_decode_static(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, fc2_q,

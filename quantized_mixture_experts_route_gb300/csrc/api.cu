@@ -49,7 +49,7 @@ qmoe_status check_problem(const qmoe_problem* p) {
 }
 
 Problem to_internal(const qmoe_problem& q) {
-  Problem p;
+  Problem p{};
   p.T = q.T;
   p.H = q.hidden;
   p.I = q.inter;
@@ -111,16 +111,20 @@ size_t qmoe_workspace_bytes(const qmoe_problem* p) {
   return workspace_layout(ip, ip.path == QMOE_PATH_GROUPED, nullptr, nullptr);
 }
 
-qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last_stage,
-                                const void* x, const void* router_logits, const uint8_t* fc1_q,
-                                const void* fc1_scales, const uint8_t* fc1_zp,
-                                const uint8_t* fc2_q, const void* fc2_scales,
-                                const uint8_t* fc2_zp, void* out, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int first_stage, int last_stage,
+                         const void* x, const void* router_logits, const uint8_t* fc1_q,
+                         const void* fc1_scales, const uint8_t* fc1_zp, const uint8_t* fc2_q,
+                         const void* fc2_scales, const uint8_t* fc2_zp, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   if (first_stage < QMOE_STAGE_ROUTE || last_stage > QMOE_STAGE_COMBINE || first_stage > last_stage)
     return QMOE_ERR_INVALID_ARGUMENT;
   const qmoe_status st = check_problem(p);
   if (st != QMOE_OK) return st;
+  if (opt && opt->full_softmax != 0 && opt->full_softmax != 1) return QMOE_ERR_INVALID_ARGUMENT;
   if (p->T == 0) return QMOE_OK;
   if (!x || !router_logits || !fc1_q || !fc1_scales || !fc2_q || !fc2_scales || !out || !workspace)
     return QMOE_ERR_INVALID_ARGUMENT;
@@ -128,7 +132,14 @@ qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last
   for (const void* q : ptrs)
     if (!aligned16(q)) return QMOE_ERR_MISALIGNED;
   if ((fc1_zp && !aligned16(fc1_zp)) || (fc2_zp && !aligned16(fc2_zp))) return QMOE_ERR_MISALIGNED;
-  const Problem ip = to_internal(*p);
+  if (opt && ((opt->fc1_bias && !aligned16(opt->fc1_bias)) || (opt->fc2_bias && !aligned16(opt->fc2_bias))))
+    return QMOE_ERR_MISALIGNED;
+  Problem ip = to_internal(*p);
+  if (opt) {
+    ip.full_softmax = opt->full_softmax;
+    ip.b1 = static_cast<const uint16_t*>(opt->fc1_bias);
+    ip.b2 = static_cast<const uint16_t*>(opt->fc2_bias);
+  }
   const bool grouped = ip.path == QMOE_PATH_GROUPED;
   Workspace ws;
   if (workspace_layout(ip, grouped, workspace, &ws) > workspace_bytes)
@@ -153,13 +164,36 @@ qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last
   return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last_stage,
+                                const void* x, const void* router_logits, const uint8_t* fc1_q,
+                                const void* fc1_scales, const uint8_t* fc1_zp,
+                                const uint8_t* fc2_q, const void* fc2_scales,
+                                const uint8_t* fc2_zp, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return forward_impl(p, nullptr, first_stage, last_stage, x, router_logits, fc1_q, fc1_scales, fc1_zp,
+                      fc2_q, fc2_scales, fc2_zp, out, workspace, workspace_bytes, stream);
+}
+
 qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* router_logits,
                          const uint8_t* fc1_q, const void* fc1_scales, const uint8_t* fc1_zp,
                          const uint8_t* fc2_q, const void* fc2_scales, const uint8_t* fc2_zp,
                          void* out, void* workspace, size_t workspace_bytes, void* stream) {
-  return qmoe_forward_stages(p, QMOE_STAGE_ROUTE, QMOE_STAGE_COMBINE, x, router_logits, fc1_q,
-                             fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace,
-                             workspace_bytes, stream);
+  return forward_impl(p, nullptr, QMOE_STAGE_ROUTE, QMOE_STAGE_COMBINE, x, router_logits, fc1_q,
+                      fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, workspace_bytes,
+                      stream);
+}
+
+qmoe_status qmoe_forward_ex(const qmoe_problem* p, const qmoe_options* opt, const void* x,
+                            const void* router_logits, const uint8_t* fc1_q, const void* fc1_scales,
+                            const uint8_t* fc1_zp, const uint8_t* fc2_q, const void* fc2_scales,
+                            const uint8_t* fc2_zp, void* out, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return forward_impl(p, opt, QMOE_STAGE_ROUTE, QMOE_STAGE_COMBINE, x, router_logits, fc1_q, fc1_scales,
+                      fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, workspace_bytes, stream);
 }
 
 qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t* topk_idx,

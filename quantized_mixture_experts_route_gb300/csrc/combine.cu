@@ -7,6 +7,10 @@
 // the partial sum stays in FP32 and is rounded once, as the GPU-only finalize
 // does; "Keep NaN as NaN when rounding to BF16"). Routes whose weight is exactly
 // zero are skipped ("skip zero-scale routes in the prefill finalizer", same PR).
+// With an FC2 bias b2 [E][H] the sum adds w_j * b2[expert of route j] next to
+// each route's row (the bias is applied per route, before the weight's sum and
+// the one rounding: "[CUDA] Add INT4 and INT3 QMoE CPU/GPU offload support"
+// #33575, commit notes).
 // Memory bound: each thread reads k x 32 bytes and writes 16 bytes.
 #include "qmoe_internal.cuh"
 
@@ -40,6 +44,22 @@ __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (w[j] == 0.0f) continue;   // also the batch's padding past k
+        if (p.b2) {
+          const int e = ws.topk_idx[t * p.k + j0 + j];
+          const uint4 bb = *reinterpret_cast<const uint4*>(p.b2 + (int64_t)e * p.H + h0);
+          const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+          float bv[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            bv[2 * q] = half_bits_to_float((uint16_t)(bw[q] & 0xFFFFu), p.dtype);
+            bv[2 * q + 1] = half_bits_to_float((uint16_t)(bw[q] >> 16), p.dtype);
+          }
+          acc[0] += a[j].x + w[j] * bv[0]; acc[1] += a[j].y + w[j] * bv[1];
+          acc[2] += a[j].z + w[j] * bv[2]; acc[3] += a[j].w + w[j] * bv[3];
+          acc[4] += b[j].x + w[j] * bv[4]; acc[5] += b[j].y + w[j] * bv[5];
+          acc[6] += b[j].z + w[j] * bv[6]; acc[7] += b[j].w + w[j] * bv[7];
+          continue;
+        }
         acc[0] += a[j].x; acc[1] += a[j].y; acc[2] += a[j].z; acc[3] += a[j].w;
         acc[4] += b[j].x; acc[5] += b[j].y; acc[6] += b[j].z; acc[7] += b[j].w;
       }

@@ -428,8 +428,9 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
               if (n < n_e) {
                 const float sigma = ws.tok_scale[ws.sorted_route[begin + n] / p.k];
                 const float inv = 1.0f / sigma;
-                const float h = silu(tot[r] * inv) * (up[r] * inv) * sigma * sigma;
                 const int j = (r & 2) ? j_hi : j_lo;
+                const float2 bj = fc1_bias_pair(p, cur.e, j);
+                const float h = silu(tot[r] * inv + bj.x) * (up[r] * inv + bj.y) * sigma * sigma;
                 ws.h16[(int64_t)(begin + n) * p.I + permuted_pos(j, G)] = __half_as_ushort(__float2half_rn(h));
               }
             }
@@ -741,8 +742,14 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
           const float sigma = ws.tok_scale[n ? tok1 : tok0];
           const float inv = 1.0f / sigma;
           const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
-          const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
-          const float h_hi = silu(v_hi * inv) * (up_hi * inv) * sigma * sigma;
+          float2 b_lo = make_float2(0.0f, 0.0f), b_hi = b_lo;
+          if (p.b1) {
+            const int ex = __ldg(ws.dtab + (item / rgroups) * kDtabInts);
+            b_lo = fc1_bias_pair(p, ex, j_lo);
+            b_hi = fc1_bias_pair(p, ex, j_hi);
+          }
+          const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * sigma * sigma;
+          const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * sigma * sigma;
           // fc2 reads these as activations: odd K positions carry 1/16
           ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
               __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
@@ -1178,8 +1185,14 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
           const float sigma = e_scale;
           const float inv = 1.0f / sigma;
           const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
-          const float h_lo = silu(v_lo * inv) * (up_lo * inv) * sigma * sigma;
-          const float h_hi = silu(v_hi * inv) * (up_hi * inv) * sigma * sigma;
+          float2 b_lo = make_float2(0.0f, 0.0f), b_hi = b_lo;
+          if (p.b1) {
+            const int ex = __ldg(ws.dtab + ei * kDtabInts);
+            b_lo = fc1_bias_pair(p, ex, j_lo);
+            b_hi = fc1_bias_pair(p, ex, j_hi);
+          }
+          const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * sigma * sigma;
+          const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * sigma * sigma;
           // fc2 reads these as activations: odd K positions carry 1/16
           ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
               __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));

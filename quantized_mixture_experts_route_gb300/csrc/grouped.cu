@@ -665,13 +665,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           constexpr int G = BITS == 4 ? 8 : 16;
           const float ss = sigma * sigma;
           uint16_t hv[16];
+          // SwiGLU with CUDA's fast exp and divide; the result is rounded to FP16
+          if (p.b1) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float gt = __uint_as_float(v[2 * q]) * inv;
-            const float ut = __uint_as_float(v[2 * q + 1]) * inv;
-            // SwiGLU with CUDA's fast exp and divide; the result is rounded to FP16
-            const float sl = __fdividef(gt, 1.0f + __expf(-gt));
-            hv[q] = __half_as_ushort(__float2half_rn(sl * ut * ss));
+            for (int q = 0; q < 16; ++q) {
+              const float2 bq = fc1_bias_pair(p, e, j0 + q);
+              const float gt = __uint_as_float(v[2 * q]) * inv + bq.x;
+              const float ut = __uint_as_float(v[2 * q + 1]) * inv + bq.y;
+              hv[q] = __half_as_ushort(__float2half_rn(__fdividef(gt, 1.0f + __expf(-gt)) * ut * ss));
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float gt = __uint_as_float(v[2 * q]) * inv;
+              const float ut = __uint_as_float(v[2 * q + 1]) * inv;
+              hv[q] = __half_as_ushort(__float2half_rn(__fdividef(gt, 1.0f + __expf(-gt)) * ut * ss));
+            }
           }
           uint16_t ov[16];
 #pragma unroll

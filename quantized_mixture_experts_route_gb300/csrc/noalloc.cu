@@ -64,7 +64,7 @@ extern "C" qmoe_status qmoe_forward_decode_static(const qmoe_problem* p, const v
 
   void* base = nullptr;
   if (static_workspace(&base) != cudaSuccess) return QMOE_ERR_CUDA;
-  Problem ip;
+  Problem ip{};
   ip.T = p->T;
   ip.H = p->hidden;
   ip.I = p->inter;

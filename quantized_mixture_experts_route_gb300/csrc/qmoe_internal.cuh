@@ -56,6 +56,9 @@ struct Workspace {
 struct Problem {
   int64_t T;
   int H, I, E, k, bits, block, dtype, path;
+  int full_softmax;               // routing weights under the softmax over all E logits
+  const uint16_t* b1;             // [E][2I] fc1 bias in dtype, or null
+  const uint16_t* b2;             // [E][H]  fc2 bias in dtype, or null
   __host__ __device__ int64_t R() const { return T * (int64_t)k; }
 };
 
@@ -104,6 +107,15 @@ cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cud
 __device__ __forceinline__ float half_bits_to_float(uint16_t b, int dtype) {
   if (dtype == QMOE_BF16) return __uint_as_float((uint32_t)b << 16);
   return __half2float(__ushort_as_half(b));
+}
+
+// fc1 bias of SwiGLU unit j of expert e: gate (row 2j) and up (row 2j+1), or
+// zeros without a bias.
+__device__ __forceinline__ float2 fc1_bias_pair(const Problem& p, int e, int j) {
+  if (!p.b1) return make_float2(0.0f, 0.0f);
+  const uint32_t v = __ldg(reinterpret_cast<const unsigned int*>(p.b1 + ((int64_t)e * p.I + j) * 2));
+  return make_float2(half_bits_to_float((uint16_t)(v & 0xFFFFu), p.dtype),
+                     half_bits_to_float((uint16_t)(v >> 16), p.dtype));
 }
 
 // Round to nearest even; NaN stays NaN (the CUDA conversion intrinsics).

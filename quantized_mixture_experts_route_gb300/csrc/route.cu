@@ -85,10 +85,17 @@ __device__ void route_token(const Problem& p, const uint16_t* __restrict__ x,
       my_l = half_bits_to_float(lrow[e], p.dtype);
     }
   }
-  // softmax over the selected logits, shifted by the largest (j = 0)
+  // softmax over the selected logits, shifted by the largest (j = 0); with
+  // full_softmax the denominator runs over all E logits of the token
   const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
   float denom = 0.0f;
-  for (int j = 0; j < k; ++j) denom += expf(__shfl_sync(0xffffffffu, my_l, j) - l0);
+  if (p.full_softmax) {
+    for (int e = lane; e < E; e += 32) denom += expf(half_bits_to_float(lrow[e], p.dtype) - l0);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
+  } else {
+    for (int j = 0; j < k; ++j) denom += expf(__shfl_sync(0xffffffffu, my_l, j) - l0);
+  }
   if (lane < k) {
     const float w = expf(my_l - l0) / denom;
     if (s_w) {                                   // shared memory only; written out later

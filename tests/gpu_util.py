@@ -47,6 +47,21 @@ def gpu_forward(shape, inp, path=0, d=None, ws=None, out=None):
     return out.cpu().numpy().view(np.uint16)
 
 
+def gpu_forward_ex(shape, inp, full_softmax, path=0):
+    """qmoe_forward_ex with the inputs' optional biases (fc1_b, fc2_b) and routing option."""
+    import torch
+    import quantized_mixture_experts_route_gb300 as qm
+
+    p = problem(shape, path)
+    d = device_inputs(inp)
+    ws = torch.empty(max(qm.qmoe_workspace_bytes(p), 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+    qm.qmoe_forward_ex(p, full_softmax, d.get("fc1_b"), d.get("fc2_b"), d["x"], d["logits"], d["fc1_q"],
+                       d["fc1_s"], d.get("fc1_zp"), d["fc2_q"], d["fc2_s"], d.get("fc2_zp"), out, ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().view(np.uint16)
+
+
 def gpu_route(shape, logits, path=0):
     import torch
     import quantized_mixture_experts_route_gb300 as qm
