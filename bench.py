@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="CSV file for the nvidia-smi clock samples (default: a file in the temp directory)")
     return ap.parse_args()
 
 
@@ -149,9 +151,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_uuid: str | None):
+    def __init__(self, device_uuid: str | None, path: str | None = None):
+        import tempfile
+
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"qmoe_clocks_{os.getpid()}.csv")
         self.uuid = device_uuid
 
     def __enter__(self):
@@ -404,7 +408,7 @@ def run_ours(args):
     except Exception:
         uuid = None
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    with ClockSampler(uuid) as clocks:
+    with ClockSampler(uuid, args.clock_log) as clocks:
         torch.cuda.synchronize()
         with torch.cuda.stream(s):
             marks[0].record()
