@@ -380,6 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     row0 = ws.tiles[2 * mt + 1];
     n0 = (w - mt * n_tiles_n) * C::BN;
   };
+  // 128-row halves of a tile that hold routes (1 or 2): an expert's last tile
+  // often fills only the first, and its second half is neither copied nor
+  // multiplied nor stored
+  auto halves_of = [&](int e, int row0) { return ws.offsets[e + 1] - row0 > kSubM ? 2 : 1; };
 
   if (warp == 0) {
     // ---------------- code producer: per stage the code tile (lane 0) and either a
@@ -466,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < my_works && go; ++j) {
         int e, row0, n0;
         tile_of(j, e, row0, n0);
+        const int nh = halves_of(e, row0);
         for (int i = 0; i < ksteps; ++i) {
           const int it = j * ksteps + i;
           const int s = it % SA;
@@ -473,13 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_aempty(s), ph ^ 1u, abort_flag, launch_err)) { go = false; break; }
           ++issued;
           const int k0 = i * C::BK;
-          mbar_expect_tx(bar_afull(s), C::A_BYTES);
+          mbar_expect_tx(bar_afull(s), (uint32_t)(C::A_BYTES / 2 * nh));
 #pragma unroll
           for (int sub = 0; sub < C::SUB; ++sub)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
-                          bar_afull(s), k0 + 64 * sub, row0 + h * kSubM);
+              if (h < nh)
+                tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
+                            bar_afull(s), k0 + 64 * sub, row0 + h * kSubM);
         }
       }
       if (*abort_flag)
@@ -502,6 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t acc0 = tmem + (uint32_t)(buf * 2 * C::BN);
+        int e_t, row0_t, n0_t;
+        tile_of(j, e_t, row0_t, n0_t);
+        const int nh = halves_of(e_t, row0_t);
         for (int i = 0; i < ksteps; ++i) {
           const int it = j * ksteps + i;
           const int sa = it % SA, sb = it % SB;
@@ -516,8 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = sw128_desc(b_base + sub * (C::BN * 128) + off);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tc_mma(acc0 + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
-                     idesc, (i | kk) != 0);
+              if (h < nh)
+                tc_mma(acc0 + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
+                       idesc, (i | kk) != 0);
           }
           pending = true;
           tc_commit(bar_aempty(sa));
@@ -646,8 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = j % C::ACC;
       if (!mbar_wait(bar_accum(buf), (uint32_t)(j / C::ACC) & 1u, abort_flag, launch_err)) break;
       tc_fence_after();
+      const int nh = rows > kSubM ? 2 : 1;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
+      if (half >= nh) break;                     // no routes in this half (the same for the warp)
       const int pos = row0 + half * kSubM + quarter * 32 + lane;
       const int rid = rid_h[half];
       const float sigma = sigma_h[half], wr = wr_h[half];
