@@ -74,6 +74,13 @@ def test_misaligned_bias_rejected_on_host(L):
     assert _call(L, p, 1, b2=34) == qm.QMOE_ERR_MISALIGNED
 
 
+def test_empty_batch_with_options(L):
+    p = qm.problem(0, 256, 128, 8, 2, 4, 32, BF16)
+    assert _call(L, p, 1, b1=32, b2=64) == qm.QMOE_OK
+    # a null options pointer means the defaults
+    assert L.qmoe_forward_ex(ctypes.byref(p), None, *([None] * 10), 0, None) == qm.QMOE_OK
+
+
 def test_options_struct_layout():
     # int32 followed by two pointers: the pointers sit at offsets 8 and 16 on LP64 hosts
     assert qm.qmoe_options.fc1_bias.offset == 8 and qm.qmoe_options.fc2_bias.offset == 16
@@ -93,8 +100,21 @@ def test_options_parity(name):
 @pytest.mark.gpu
 @pytest.mark.parametrize("path", [1, 2])
 def test_zero_options_equal_forward(path):
+    import torch
+
     shape = Shape(T=8 if path == 1 else 64, H=512, inter=256, E=8, k=2, bits=4, block=32, dtype=BF16)
     inp = synthetic.make_numpy(shape, Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 79)
     a = gu.gpu_forward(shape, inp, path=path)
     b = gu.gpu_forward_ex(shape, inp, 0, path=path)
     assert np.array_equal(a, b)
+    # a null options pointer: the same call
+    p = gu.problem(shape, path)
+    d = gu.device_inputs(inp)
+    ws = torch.empty(qm.qmoe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+    args = [d["x"], d["logits"], d["fc1_q"], d["fc1_s"], None, d["fc2_q"], d["fc2_s"], None, out, ws]
+    st = qm.lib().qmoe_forward_ex(ctypes.byref(p), None, *[None if t is None else t.data_ptr() for t in args],
+                                  ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == qm.QMOE_OK
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), a)
