@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--options", action="store_true",
+                    help="run qmoe_forward_ex with FC1/FC2 biases and full-softmax routing weights")
     ap.add_argument("--clock-log", default=None,
                     help="CSV file for the nvidia-smi clock samples (default: a file in the temp directory)")
     return ap.parse_args()
@@ -64,7 +66,9 @@ def workload_config(args, shape, layers, world):
                          f"E={shape.E} k={shape.k} INT{shape.bits} b{shape.block} "
                          f"{'BF16' if shape.dtype == 0 else 'FP16'} T={shape.T} per rank"),
             "T": shape.T, "layers": layers, "parallelism": f"replicas x{world}",
-            "l2": "weights 16.3 GB >> L2, no flush" if args.workload == "decode" else "inputs > L2 per step"}
+            "l2": "weights 16.3 GB >> L2, no flush" if args.workload == "decode" else "inputs > L2 per step",
+            **({"options": "fc1/fc2 biases N(0, 0.5), full-softmax routing weights"}
+               if getattr(args, "options", False) else {})}
 
 
 def reduce_max(v, device):
@@ -370,9 +374,22 @@ def run_ours(args):
         w = W[l]
         return (src, lg_d[l], w["fc1_q"], w["fc1_s"], None, w["fc2_q"], w["fc2_s"], None, dst, ws)
 
+    B1 = B2 = None
+    if args.options:
+        gb = torch.Generator(device=device)
+        gb.manual_seed(7)
+        tdt = torch.bfloat16 if shape.dtype == synthetic.BF16 else torch.float16
+        B1 = [(torch.randn((shape.E, 2 * shape.inter), generator=gb, device=device) * 0.5).to(tdt)
+              .view(torch.int16) for _ in range(layers)]
+        B2 = [(torch.randn((shape.E, shape.H), generator=gb, device=device) * 0.5).to(tdt)
+              .view(torch.int16) for _ in range(layers)]
+
     def step():
         for l in range(layers):
-            qm.qmoe_forward(p, *layer_args(l))
+            if args.options:
+                qm.qmoe_forward_ex(p, 1, B1[l], B2[l], *layer_args(l))
+            else:
+                qm.qmoe_forward(p, *layer_args(l))
 
     def stage_only(st):
         # one stage of every layer, back to back: its kernels' own durations, with no
@@ -463,7 +480,8 @@ def run_ours(args):
     except (OSError, ValueError):
         pass
     fc1_b, fc2_b = expert_bytes(shape)
-    default_kernel = args.workload in ("decode", "prefill")   # the captured kernels' workloads
+    # the captured kernels' workloads (traffic figures hold for the plain call only)
+    default_kernel = args.workload in ("decode", "prefill") and not args.options
     if shape.T <= 8:
         nact = distinct_experts(logits_h, shape.dtype, shape.k)
         # the single-stage graphs run on the routing of the last layer
@@ -522,6 +540,8 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.options and args.impl == "reference":
+        raise SystemExit("--options applies to the CUDA arm only")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -441,6 +441,22 @@ def pin_fc2_bias_with_zero_weights(orc):
         fail("zero weights with biases: output is not the weighted FC2 biases")
 
 
+def pin_full_softmax_nan_row(orc):
+    """With full-softmax weights a NaN logit anywhere in a token's row (never
+    selected: NaN ranks lowest) makes that token's weights NaN, as a softmax over
+    the row would; the renormalised weights of the selected logits stay finite."""
+    lv = np.array([[1.0, 0.5, np.nan, -1.0, 2.0], [0.1, 0.2, 0.3, 0.4, 0.5]])
+    lg = _logits_bits(lv, BF16)
+    for full in (0, 1):
+        idx, w = orc.route(oracle_mod.Problem(2, 64, 32, 5, 2, 4, 32, BF16, full_softmax=full), lg)
+        if 2 in idx[0]:
+            fail("a NaN logit was selected")
+        if full and not (np.isnan(w[0]).all() and np.isfinite(w[1]).all()):
+            fail("full softmax: a NaN in the row must give NaN weights for that token only")
+        if not full and not np.isfinite(w).all():
+            fail("renormalised weights of finite selected logits must be finite")
+
+
 def pin_nan_propagates(orc):
     shape, inp = _small_inputs(T=2, H=64, I=32, E=4, k=2, dt=BF16)
     inp = dict(inp)
@@ -459,5 +475,5 @@ ALL_PINS = [
     pin_route_bruteforce, pin_permute, pin_dense_ffn_E1_k1, pin_bruteforce_dense_over_experts,
     pin_one_hot, pin_token_permutation, pin_zero_weights, pin_zero_weight_route_skipped,
     pin_nan_propagates, pin_full_softmax_routing, pin_biases_dense_over_experts,
-    pin_fc2_bias_with_zero_weights,
+    pin_fc2_bias_with_zero_weights, pin_full_softmax_nan_row,
 ]

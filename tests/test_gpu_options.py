@@ -118,3 +118,23 @@ def test_zero_options_equal_forward(path):
     assert st == qm.QMOE_OK
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy().view(np.uint16), a)
+
+
+@pytest.mark.gpu
+def test_full_softmax_nan_logit_row():
+    """A NaN logit (never selected) makes that token's full-softmax weights, and so
+    its output row, NaN on both sides; the other tokens stay within parity."""
+    shape = Shape(T=4, H=256, inter=128, E=8, k=2, bits=4, block=32, dtype=BF16)
+    inp = synthetic.make_numpy(shape, Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 80)
+    lg = inp["logits"].copy()
+    lg[2, 5] = 0x7FC0
+    inp = dict(inp, logits=lg)
+    got = gu.gpu_forward_ex(shape, inp, 1, path=1)
+    ref, _ = oracle.forward(oproblem(shape, 1), inp)
+
+    def nan(b):
+        return ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+
+    assert nan(got[2]).all() and nan(ref[2]).all()
+    keep = [0, 1, 3]
+    gu.assert_parity(got[keep], ref[keep], shape.dtype, "rows without a NaN logit")
