@@ -1,0 +1,191 @@
+"""A host model of the grouped GEMM's shared-memory pipeline protocol.
+
+The tcgen05 kernel in csrc/grouped.cu runs six roles on one CTA that hand
+shared-memory slots to each other through mbarriers: the code producer (code
+tiles and, with scales by tensor copy, a two-box scale ring), the activation
+producer, the MMA issuer, two dequantisation groups taking alternate stages,
+and the epilogue (one or two accumulator buffers). This test replays the same
+slot indices, barrier phase parities and arrival counts as the kernel, with a
+random interleaving of the roles, and checks on every wait that the parity
+test selects exactly the phase the role needs (no phase is skipped or taken
+twice), that no slot is overwritten before its consumer is done with it, and
+that every role finishes (no deadlock). Configurations cover one and several
+tiles, K stage counts below, equal to and above the ring depths, odd stage
+counts (the dequantisation groups swap stages between tiles), scale boxes of
+one stage, and the INT3 ring depths with double-buffered accumulators. The
+model has to follow the kernel: change both together.
+"""
+import random
+
+import pytest
+
+
+class Barrier:
+    def __init__(self, name, count):
+        self.name, self.count, self.arrived, self.completed = name, count, 0, 0
+
+    def arrive(self, n=1):
+        self.arrived += n
+        assert self.arrived <= self.count, f"{self.name}: too many arrivals in one phase"
+        if self.arrived == self.count:
+            self.completed += 1
+            self.arrived = 0
+
+
+def ready(bar, parity, phase_needed):
+    """mbarrier try_wait.parity: true once the phase of that parity has completed.
+    The protocol must make it select exactly completion number `phase_needed`."""
+    ok = (bar.completed & 1) != parity
+    if ok:
+        assert bar.completed == phase_needed, (
+            f"{bar.name}: parity wait passed with {bar.completed} completions, needed {phase_needed}")
+    return ok
+
+
+def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed):
+    rnd = random.Random(seed)
+    afull = [Barrier(f"afull{s}", 1) for s in range(SA)]
+    aempty = [Barrier(f"aempty{s}", 1) for s in range(SA)]
+    cfull = [Barrier(f"cfull{s}", 1) for s in range(SC)]
+    cempty = [Barrier(f"cempty{s}", 1) for s in range(SC)]      # one group's arrival per stage
+    bready = [Barrier(f"bready{s}", 1) for s in range(SB)]
+    bempty = [Barrier(f"bempty{s}", 1) for s in range(SB)]
+    accum = [Barrier(f"accum{b}", 1) for b in range(ACC)]
+    drained = [Barrier(f"drained{b}", 1) for b in range(ACC)]
+    sfull = [Barrier(f"sfull{b}", 1) for b in range(2)]
+    sempty = [Barrier(f"sempty{b}", 2) for b in range(2)]       # both groups, or one group twice
+    a_slot, b_slot, c_slot, s_box, acc_buf = [None] * SA, [None] * SB, [None] * SC, [None] * 2, [None] * ACC
+    a_used, b_used, c_used = [True] * SA, [True] * SB, [True] * SC
+    nbox = (ksteps + span - 1) // span
+    box_left = {}                                               # arrivals still due per scale box
+
+    def wait(bar, parity, need):
+        while not ready(bar, parity, need):
+            yield
+
+    def code_producer():
+        spans = 0
+        for j in range(works):
+            for i in range(ksteps):
+                it = j * ksteps + i
+                s = it % SC
+                yield from wait(cempty[s], ((it // SC) & 1) ^ 1, it // SC)
+                if tsc and i % span == 0:
+                    m = spans
+                    spans += 1
+                    if m >= 2:
+                        yield from wait(sempty[m & 1], ((m - 2) >> 1) & 1, (m - 2) // 2 + 1)
+                        assert box_left[m - 2] == 0, "scale box overwritten before both groups released it"
+                    s_box[m & 1] = m
+                    span_len = min(span, ksteps - i)
+                    box_left[m] = 2 if span_len >= 2 else 1
+                    sfull[m & 1].arrive()
+                assert c_used[s], "code slot overwritten before it was dequantised"
+                c_slot[s], c_used[s] = it, False
+                cfull[s].arrive()
+
+    def act_producer():
+        for j in range(works):
+            for i in range(ksteps):
+                it = j * ksteps + i
+                s = it % SA
+                yield from wait(aempty[s], ((it // SA) & 1) ^ 1, it // SA)
+                assert a_used[s], "activation slot overwritten before the MMAs read it"
+                a_slot[s], a_used[s] = it, False
+                afull[s].arrive()
+
+    def mma():
+        for j in range(works):
+            buf = j % ACC
+            if j >= ACC:
+                yield from wait(drained[buf], (j // ACC - 1) & 1, j // ACC)
+            assert acc_buf[buf] is None, "accumulators overwritten before the epilogue read them"
+            acc_buf[buf] = ("accumulating", j)
+            for i in range(ksteps):
+                it = j * ksteps + i
+                sa, sb = it % SA, it % SB
+                yield from wait(afull[sa], (it // SA) & 1, it // SA + 1)
+                yield from wait(bready[sb], (it // SB) & 1, it // SB + 1)
+                assert a_slot[sa] == it and b_slot[sb] == it, "MMA read the wrong stage"
+                a_used[sa] = b_used[sb] = True
+                aempty[sa].arrive()
+                bempty[sb].arrive()
+            acc_buf[buf] = j
+            accum[buf].arrive()
+
+    def dequant(grp):
+        box_seen = -1
+        for j in range(works):
+            for i in range(ksteps):
+                it = j * ksteps + i
+                if (it & 1) != grp:
+                    continue
+                cs, bs = it % SC, it % SB
+                yield from wait(cfull[cs], (it // SC) & 1, it // SC + 1)
+                assert c_slot[cs] == it, "dequantiser read the wrong code stage"
+                m_cur = j * nbox + i // span
+                if tsc and m_cur != box_seen:
+                    box_seen = m_cur
+                    yield from wait(sfull[m_cur & 1], (m_cur >> 1) & 1, (m_cur >> 1) + 1)
+                    assert s_box[m_cur & 1] == m_cur, "dequantiser read the wrong scale box"
+                yield from wait(bempty[bs], ((it // SB) & 1) ^ 1, it // SB)
+                assert b_used[bs], "B slot overwritten before the MMAs read it"
+                b_slot[bs], b_used[bs] = it, False
+                bready[bs].arrive()
+                c_used[cs] = True
+                cempty[cs].arrive()
+                if tsc:
+                    box0 = (i // span) * span
+                    box_end = min(box0 + span, ksteps)
+                    if i + 2 >= box_end:
+                        box_left[m_cur] -= 1            # this group is done with the box
+                        sempty[m_cur & 1].arrive(1 if box_end - box0 >= 2 else 2)
+
+    def epilogue():
+        for j in range(works):
+            buf = j % ACC
+            yield from wait(accum[buf], (j // ACC) & 1, j // ACC + 1)
+            assert acc_buf[buf] == j, "epilogue read the wrong tile"
+            acc_buf[buf] = None
+            drained[buf].arrive()
+
+    roles = [code_producer(), act_producer(), mma(), dequant(0), dequant(1), epilogue()]
+    live = list(roles)
+    steps = 0
+    last = None
+    while live:
+        steps += 1
+        assert steps < 10_000_000, "model did not finish"
+        r = rnd.choice(live)
+        try:
+            next(r)
+        except StopIteration:
+            live.remove(r)
+            continue
+        # a role that is blocked yields without progress; detect a global deadlock
+        if steps % 20000 == 0:
+            bars = afull + aempty + cfull + cempty + bready + bempty + accum + drained + sfull + sempty
+            snapshot = (len(live), [(b.completed, b.arrived) for b in bars])
+            assert snapshot != last, "deadlock: no role moved in 20000 scheduling steps"
+            last = snapshot
+    assert all(v == 0 for v in box_left.values()), "a scale box was not released by every group"
+
+
+# (ksteps, works, SA, SB, SC, ACC, scales by tensor copy, stages per scale box)
+CONFIGS = [
+    (32, 3, 3, 3, 3, 1, True, 4),     # INT4 block 32, fc1 K = 2048
+    (12, 4, 3, 3, 3, 1, True, 4),     # INT4 block 32, fc2 K = 768
+    (12, 3, 3, 3, 3, 1, True, 16),    # block 128: one box longer than the tile
+    (5, 3, 3, 3, 4, 1, False, 4),     # odd stage count, scales loaded by the producer (INT2 ring)
+    (5, 3, 3, 3, 3, 1, True, 4),      # odd stage count with a one-stage scale box per tile
+    (2, 5, 3, 3, 3, 1, True, 4),      # fewer stages than the B ring
+    (1, 6, 3, 3, 3, 1, True, 4),      # one stage per tile
+    (16, 4, 2, 2, 2, 2, True, 2),     # INT3 block 32 (K stage 128): double-buffered accumulators
+    (3, 5, 2, 2, 2, 2, True, 4),      # INT3, short K
+]
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_pipeline_protocol(cfg):
+    for seed in range(6):
+        simulate(*cfg, seed=seed)
