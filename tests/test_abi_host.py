@@ -31,6 +31,24 @@ def test_exports_every_header_symbol(L):
         assert hasattr(L, n), n
 
 
+def header_signatures():
+    """{function: number of parameters} from the header's declarations."""
+    text = open(os.path.join(ROOT, "include", "qmoe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    sigs = {}
+    for name, params in re.findall(r"\b(qmoe_[a-z_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = params.strip()
+        sigs[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return sigs
+
+
+def test_binding_argument_counts_match_header(L):
+    sigs = header_signatures()
+    assert sorted(sigs) == sorted(qm.EXPORTED)
+    for name, n in sigs.items():
+        assert len(getattr(L, name).argtypes) == n, name
+
+
 def test_status_strings(L):
     for s in range(6):
         assert qm.qmoe_status_string(s)
@@ -68,10 +86,13 @@ BAD = [
 FAKE = 1 << 20  # an aligned address that is never dereferenced: every call below fails its checks first
 
 
-def call_forward(L, p, ptrs=None, ws_bytes=1 << 40, misalign=None):
-    args = [FAKE] * 10 if ptrs is None else ptrs
+def call_forward(L, p, ptrs=None, ws_bytes=1 << 40, misalign=None, ex=False):
+    args = [FAKE] * 10 if ptrs is None else list(ptrs)
     if misalign is not None:
         args[misalign] += 2
+    if ex:   # qmoe_forward_ex with default options makes the same checks
+        opt = qm.qmoe_options(0, None, None)
+        return L.qmoe_forward_ex(ctypes.byref(p), ctypes.byref(opt), *args[:9], args[9], ws_bytes, None)
     return L.qmoe_forward(ctypes.byref(p), *args[:9], args[9], ws_bytes, None)
 
 
@@ -79,6 +100,7 @@ def call_forward(L, p, ptrs=None, ws_bytes=1 << 40, misalign=None):
 def test_invalid_problem_rejected(L, kw, status):
     p = P(**kw)
     assert call_forward(L, p) == status
+    assert call_forward(L, p, ex=True) == status
     assert L.qmoe_route(ctypes.byref(p), FAKE, None, None, None, None, FAKE, 1 << 40, None) == status
     assert L.qmoe_workspace_bytes(ctypes.byref(p)) == 0
 
@@ -93,11 +115,13 @@ def test_null_required_pointer(L, which):
     args = [FAKE] * 10
     args[which] = None
     assert call_forward(L, P(), args) == qm.QMOE_ERR_INVALID_ARGUMENT
+    assert call_forward(L, P(), args, ex=True) == qm.QMOE_ERR_INVALID_ARGUMENT
 
 
 @pytest.mark.parametrize("which", range(10))
 def test_misaligned_pointer(L, which):
     assert call_forward(L, P(), misalign=which) == qm.QMOE_ERR_MISALIGNED
+    assert call_forward(L, P(), misalign=which, ex=True) == qm.QMOE_ERR_MISALIGNED
 
 
 def test_workspace_too_small(L):
@@ -105,6 +129,7 @@ def test_workspace_too_small(L):
     need = L.qmoe_workspace_bytes(ctypes.byref(p))
     assert need > 0
     assert call_forward(L, p, ws_bytes=need - 1) == qm.QMOE_ERR_WORKSPACE_TOO_SMALL
+    assert call_forward(L, p, ws_bytes=need - 1, ex=True) == qm.QMOE_ERR_WORKSPACE_TOO_SMALL
     assert L.qmoe_route(ctypes.byref(p), FAKE, None, None, None, None, FAKE, need - 1, None) == \
         qm.QMOE_ERR_WORKSPACE_TOO_SMALL
 
