@@ -174,7 +174,11 @@ qmoe_status qmoe_forward_ex(const qmoe_problem* p, const qmoe_options* opt, cons
  * Stages of qmoe_forward: ROUTE (top-k routing, grouping by expert and the
  * activations' FP16 conversion), FC1 (fc1 dequant-matmul with the SwiGLU
  * epilogue), FC2 (fc2 dequant-matmul, weighted by the routing weight) and
- * COMBINE (sum over each token's routes, rounded once).
+ * COMBINE (sum over each token's routes, rounded once). On the decode path
+ * with INT4, block 32, no zero points and hidden, inter multiples of 256, a
+ * range that runs FC1 through COMBINE runs them as one kernel (the decode
+ * layer kernel); a range that stops earlier, or starts later, uses the
+ * separate kernels of each stage.
  */
 typedef enum {
   QMOE_STAGE_ROUTE = 0,
@@ -215,6 +219,23 @@ qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t
 const char* qmoe_status_string(qmoe_status s);
 
 /*
+ * Failure of a kernel after its launch. The pages' own kernels have no such
+ * case (they return only argument errors); it exists because every wait inside
+ * this library's kernels is bounded in time (about 1 s). A kernel that gives up
+ * on a wait writes a nonzero code into an int32 word of the workspace, lets its
+ * copies in flight land and returns; the call's last step then writes NaN to
+ * every element of `out`, so a failed call never yields plausible numbers.
+ * This function returns the byte offset of that word inside a workspace laid
+ * out for *p (the same for qmoe_forward, qmoe_forward_ex and the stage calls),
+ * or (size_t)-1 when *p is invalid. The word is 0 after a call that completed
+ * normally and is reset by the routing step of the next call on the same
+ * workspace; read it (for example with cudaMemcpyAsync on the call's stream)
+ * after the call and before the next one. Codes: 1 grouped GEMM, 2 decode
+ * matmul kernel, 3 decode layer kernel.
+ */
+size_t qmoe_workspace_error_offset(const qmoe_problem* p);
+
+/*
  * The mixture-of-experts pages have no counterpart of this call: it serves
  * callers that cannot allocate device memory.
  *
@@ -230,13 +251,14 @@ const char* qmoe_status_string(qmoe_status s);
  * host before any CUDA call.
  *
  * The work runs on the calling thread's current device, to which `stream` must
- * belong. The first call on each device looks up the array's device address
- * there (cudaGetSymbolAddress) and caches it: make that first call before any
- * stream capture on that device. All calls on a device share the array, which
- * keeps the previous call's contents; each call first clears, on `stream`, the
- * parts that must start at zero. Calls whose GPU work overlaps (different
- * streams or threads without ordering between them) race on the array and give
- * undefined results.
+ * belong. The first call with each device and context current looks up the
+ * array's device address there (cudaGetSymbolAddress) and caches it for that
+ * pair: make that first call before any stream capture on that device, and
+ * again after cudaDeviceReset (which creates a new context). All calls on a
+ * device share the array, which keeps the previous call's contents; the parts
+ * that must start at zero are reset by the call's first kernel. Calls whose
+ * GPU work overlaps (different streams or threads without ordering between
+ * them) race on the array and give undefined results.
  */
 #define QMOE_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
 qmoe_status qmoe_forward_decode_static(const qmoe_problem* p, const void* x,

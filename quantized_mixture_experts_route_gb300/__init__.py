@@ -14,6 +14,7 @@ Functions mirror the C names:
 * ``qmoe_route(problem, router_logits, topk_idx, topk_w, expert_offsets,
   sorted_route, workspace, stream=None)``
 * ``qmoe_status_string(status) -> str``
+* ``qmoe_workspace_error_offset(problem) -> int``
 
 Tensor arguments may be torch CUDA tensors or raw integer device addresses;
 ``None`` passes NULL. A non-OK status raises :class:`QMoEError`.
@@ -42,7 +43,8 @@ QMOE_PATH_GROUPED = 2
 
 # every symbol the header declares
 EXPORTED = ("qmoe_workspace_bytes", "qmoe_forward", "qmoe_forward_stages", "qmoe_route",
-            "qmoe_status_string", "qmoe_forward_decode_static", "qmoe_forward_ex")
+            "qmoe_status_string", "qmoe_forward_decode_static", "qmoe_forward_ex",
+            "qmoe_workspace_error_offset")
 
 QMOE_STATIC_WORKSPACE_BYTES = 8 << 20
 
@@ -101,6 +103,8 @@ def lib():
         L.qmoe_forward_ex.argtypes = [P, ctypes.POINTER(qmoe_options), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_size_t, vp]
         L.qmoe_forward_ex.restype = ctypes.c_int
+        L.qmoe_workspace_error_offset.argtypes = [P]
+        L.qmoe_workspace_error_offset.restype = ctypes.c_size_t
         L.qmoe_status_string.argtypes = [ctypes.c_int]
         L.qmoe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -141,6 +145,12 @@ def qmoe_status_string(status: int) -> str:
 
 def qmoe_workspace_bytes(p: qmoe_problem) -> int:
     return int(lib().qmoe_workspace_bytes(ctypes.byref(p)))
+
+
+def qmoe_workspace_error_offset(p: qmoe_problem) -> int:
+    """Byte offset of the workspace's int32 failure word (-1 for an invalid problem)."""
+    v = int(lib().qmoe_workspace_error_offset(ctypes.byref(p)))
+    return -1 if v == (1 << 64) - 1 else v
 
 
 def qmoe_forward(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, fc2_q, fc2_scales,

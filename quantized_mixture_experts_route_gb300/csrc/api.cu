@@ -16,6 +16,10 @@ namespace {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// The decode layer kernel (decode_layer.cu) replaces the separate fc1, fc2 and
+// combine launches once it is the faster of the two on the decode stack.
+constexpr bool kUseDecodeLayerKernel = false;
+
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
 int resolve_path(const qmoe_problem& p) {
@@ -92,6 +96,8 @@ size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* w
   w.dsplit_items = dec ? decode_split_items_max(p) : 0;
   w.dticket = static_cast<int32_t*>(take(sizeof(int32_t) * w.dunits_max));
   w.dsplit = static_cast<float*>(take(sizeof(float) * 128 * w.dsplit_items));
+  w.dsync_ints = dec ? decode_sync_ints(p) : 0;
+  w.dsync = static_cast<int32_t*>(take(sizeof(int32_t) * w.dsync_ints));
   w.x16s = grouped ? static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.H)) : nullptr;
   w.h16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.I));
   w.y = static_cast<float*>(take(sizeof(float) * R * p.H));
@@ -152,6 +158,13 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
                        decode_int4_blockscaled(ip) ? kX16OddSixteenth : kX16Plain, s);
     if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
     if (err == cudaSuccess && grouped) err = launch_gather(ip, ws, s);
+  }
+  // FC1 through COMBINE of the decode path in one kernel where it applies
+  if (err == cudaSuccess && kUseDecodeLayerKernel && in_range(QMOE_STAGE_FC1) &&
+      last_stage == QMOE_STAGE_COMBINE && decode_layer_applies(ip, fc1_zp || fc2_zp)) {
+    err = launch_decode_layer(ip, fc1_q, fc1_scales, fc2_q, fc2_scales, ws, out, s);
+    if (err == cudaErrorNotSupported) return QMOE_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
   }
   if (err == cudaSuccess && in_range(QMOE_STAGE_FC1))
     err = grouped ? launch_grouped(ip, true, fc1_q, fc1_scales, fc1_zp, ws, s)
@@ -224,6 +237,16 @@ qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t
     err = cudaMemcpyAsync(sorted_route, ws.sorted_route, sizeof(int32_t) * R,
                           cudaMemcpyDeviceToDevice, s);
   return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+size_t qmoe_workspace_error_offset(const qmoe_problem* p) {
+  if (check_problem(p) != QMOE_OK) return (size_t)-1;
+  const Problem ip = to_internal(*p);
+  Workspace ws;
+  // laid out from a nominal base address; nothing is dereferenced
+  constexpr uintptr_t kBase = 4096;
+  workspace_layout(ip, ip.path == QMOE_PATH_GROUPED, reinterpret_cast<void*>(kBase), &ws);
+  return (size_t)(reinterpret_cast<uintptr_t>(ws.counters + 2) - kBase);
 }
 
 const char* qmoe_status_string(qmoe_status s) {

@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
   pdl_wait();
   const int per_row = p.H / 8;
   const int64_t total = p.T * per_row;
+  // a matmul kernel of this call gave up on a wait: no plausible numbers
+  const bool failed = *reinterpret_cast<volatile const int*>(ws.counters + 2) != 0;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / per_row;
@@ -64,6 +66,9 @@ __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
         acc[4] += b[j].x; acc[5] += b[j].y; acc[6] += b[j].z; acc[7] += b[j].w;
       }
     }
+    if (failed)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = __int_as_float(0x7FC00000);
     uint4 o;
     o.x = float_to_half_bits(acc[0], p.dtype) | ((uint32_t)float_to_half_bits(acc[1], p.dtype) << 16);
     o.y = float_to_half_bits(acc[2], p.dtype) | ((uint32_t)float_to_half_bits(acc[3], p.dtype) << 16);
@@ -76,9 +81,7 @@ __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
 }  // namespace
 
 cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cudaStream_t s) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   const int64_t total = p.T * (p.H / 8);
   int64_t blocks = (total + 255) / 256;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;

@@ -97,15 +97,6 @@ __device__ __forceinline__ uint32_t dq_pair(const PairWords<BITS>& w, int p, uin
   return h2_sub_mul(bits | kMagic, z2, s2);
 }
 
-__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 struct DecodeArgs {
   const uint8_t* q;        // [E][N][K*bits/8]
   const uint16_t* s;       // [E][N][K/block]
@@ -121,12 +112,6 @@ struct DecodeArgs {
 __device__ __forceinline__ int permuted_pos(int j, int G) {
   const int base = j - j % G, i = j % G;
   return base + (i < G / 2 ? 2 * i : 2 * (i - G / 2) + 1);
-}
-
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));  // (a & mask) | orv
-  return d;
 }
 
 __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
@@ -777,13 +762,8 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
 
 template <bool FC1, bool BF16S, bool HAS_ZP>
 cudaError_t launch_int4_bs_t(DecodeArgs a, int64_t blocks, size_t smem, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_int4_bs_kernel<FC1, BF16S, HAS_ZP>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 75 * 1024);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
+  const cudaError_t err = ensure_smem_optin(decode_int4_bs_kernel<FC1, BF16S, HAS_ZP>, 75 * 1024);
+  if (err != cudaSuccess) return err;
   return launch_pdl(decode_int4_bs_kernel<FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
 }
 
@@ -1227,13 +1207,8 @@ template <int ROWS, bool FC1, bool BF16S, bool HAS_ZP>
 cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, const CUtensorMap& tz,
                               const CUtensorMap& ta, TmaDecodeArgs a, cudaStream_t s) {
   using C = TCfg<ROWS>;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
+  const cudaError_t err = ensure_smem_optin(decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP>, (int)C::kSmem);
+  if (err != cudaSuccess) return err;
   const int64_t blocks = (int64_t)sm_count() * kTBlocksPerSm;
   return launch_pdl(decode_int4_tma_kernel<ROWS, FC1, BF16S, HAS_ZP>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem, s, tq, ts, tz, ta, a);
 }
@@ -1297,16 +1272,7 @@ cudaError_t launch_int4_bs(DecodeArgs a, cudaStream_t s) {
             : launch_int4_bs_t<FC1, false, false>(a, blocks, smem, s);
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count() { return device_sm_count(); }
 
 template <int BITS, bool FC1>
 cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
@@ -1326,13 +1292,8 @@ cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
   if (blocks > cap) blocks = cap;
   const size_t smem = (size_t)kWarps * kRing * 2 * 32 * 16 +
                       (ks > 1 ? (size_t)(kWarps / ks) * kSlices * 32 * 4 * sizeof(float) : 0);
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_gemv_kernel<BITS, FC1>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
+  const cudaError_t err = ensure_smem_optin(decode_gemv_kernel<BITS, FC1>, 100 * 1024);
+  if (err != cudaSuccess) return err;
   return launch_pdl(decode_gemv_kernel<BITS, FC1>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
 }
 

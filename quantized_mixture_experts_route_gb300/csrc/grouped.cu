@@ -92,7 +92,7 @@ struct Cfg {
   static constexpr int BAR_OFF = S_OFF + (TSC ? 2 * SC_BYTES : SC * S_BYTES);
   static constexpr int NBARS = 2 * (SA + SC + SB) + 2 * ACC + 4;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;   // barriers + TMEM address + alignment slack
-  static_assert(8 * NBARS + 8 <= 256, "barrier area");
+  static_assert(8 * NBARS + 8 + 4 * SC <= 256, "barrier area");
   static constexpr int TMEM_COLS = 2 * BN * ACC;      // two accumulators per tile
   static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -119,6 +119,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((i & 255u) == 0) {
+      if (*launch_err) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        *launch_err = kErrTimeout;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait until a shared word equals `want`, with mbar_wait's abort rules.
+__device__ __forceinline__ bool word_wait(const volatile int* word, int want, volatile int* abort_flag,
+                                          volatile int* launch_err) {
+  if (*word == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (*word == want) return true;
     if (*abort_flag) return false;
     if ((i & 255u) == 0) {
       if (*launch_err) {
@@ -245,11 +267,6 @@ struct GemmArgs {
   Workspace ws;
 };
 
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));  // (a & mask) | orv
-  return d;
-}
 __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
   const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -331,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_sempty = [&](int b) { return bar0 + 8u * (kAcc + 2 * C::ACC + 2 + b); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBARS + 4);
+  // per code slot: the stage whose copy the producer issued into it last
+  volatile int* cfill = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -341,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < SC; ++s) {
       mbar_init(bar_cfull(s), TSC ? 1 : 1 + 32);  // the copy issue [+ 32 scale writers]
       mbar_init(bar_cempty(s), kDequantThreads);
+      cfill[s] = -1;
     }
     for (int s = 0; s < SB; ++s) {
       mbar_init(bar_bready(s), kDequantThreads);
@@ -418,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__shfl_sync(0xffffffffu, ok, 0) == 0) { go = false; break; }
         ++issued;
         if (lane == 0) {
+          cfill[s] = it;
           mbar_expect_tx(bar_cfull(s), C::C_BYTES);
           tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_cfull(s), k0 * BITS / 8, e * N + n0);
         }
@@ -563,6 +584,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int it = j * ksteps + i;
         if ((it & 1) != grp) continue;
         const int cs = it % SC, bs = it % SB;
+        // With an odd ring the slot's previous stage belongs to the other group. A
+        // parity wait would also pass while that stage's copy is still open, so wait
+        // first until the producer has issued this stage's copy into the slot: it
+        // does so only after the previous stage was read, i.e. after its copy landed.
+        if (SC % 2 == 1 && !word_wait(cfill + cs, it, abort_flag, launch_err)) { go = false; break; }
         if (!mbar_wait(bar_cfull(cs), (uint32_t)(it / SC) & 1u, abort_flag, launch_err)) { go = false; break; }
         const int m_cur = j * nbox + i / span;   // scale box of this stage (TSC), in issue order
         if (TSC && m_cur != box_seen) {
@@ -759,18 +785,11 @@ cudaError_t launch_gemm_t(const Problem& p, const uint8_t* q, const void* scales
   } else {
     tsc = tq;                                    // not read
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BITS, FC1, TSC>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (err != cudaSuccess) return err;
-    attr_set = true;
-  }
+  const cudaError_t err = ensure_smem_optin(grouped_gemm_kernel<BITS, FC1, TSC>, C::SMEM);
+  if (err != cudaSuccess) return err;
   GemmArgs g{static_cast<const uint16_t*>(scales), zp, N, K, p, ws};
   // persistent: one CTA per SM, each walking its share of the (m-tile, n-tile) list
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   const int64_t works_max = ws.max_tiles * ((N + C::BN - 1) / C::BN);
   dim3 grid((unsigned)(works_max < sms ? works_max : sms));
   return launch_pdl(grouped_gemm_kernel<BITS, FC1, TSC>, grid, dim3(kThreads), C::SMEM, s, ta, tq, tsc, g);

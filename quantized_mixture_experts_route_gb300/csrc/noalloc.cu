@@ -5,40 +5,48 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds QMOE_STATIC_WORKSPACE_BYTES of it until the process exits. In
 // host code its name is only a stand-in: the device address comes from
-// cudaGetSymbolAddress, taken once per device (with that device current) at the
-// first call on that device and cached. All calls on a device share the array
-// and it keeps the previous call's contents, so the counters and the split-K
-// tickets, which must start at zero, are cleared on the stream first. Calls
-// whose work overlaps on the GPU (other streams, other threads) race on the array.
+// cudaGetSymbolAddress, taken on the first call made with a given device and
+// context current, and cached for that pair (a context created after
+// cudaDeviceReset gets its own look-up). All calls on a device share the array
+// and it keeps the previous call's contents. What must start at zero -- the
+// routing counters, the failure word, the split-K tickets and the decode layer
+// kernel's claim and arrival counters -- is reset by the routing kernel at the
+// start of every decode-path call, so nothing is cleared here. Calls whose work
+// overlaps on the GPU (other streams, other threads) race on the array.
 // Nothing here allocates device memory.
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "qmoe_internal.cuh"
 
 namespace qmoe {
 namespace {
 
-constexpr int kMaxStaticDevices = 64;
-
 static __device__ __align__(256) unsigned char g_static_workspace[QMOE_STATIC_WORKSPACE_BYTES];
 
 std::mutex g_static_mu;
-void* g_static_ptr[kMaxStaticDevices] = {};
+std::map<std::pair<int, const void*>, void*> g_static_ptr;   // (device, context) -> address
 
-// Device address of g_static_workspace on the current device (set up on first use).
+// Device address of g_static_workspace on the current device and context (set
+// up on first use there).
 cudaError_t static_workspace(void** out) {
   int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxStaticDevices) return cudaErrorInvalidDevice;
+  const void* ctx = nullptr;
+  if (!current_device_context(&dev, &ctx)) return cudaErrorNoDevice;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* ptr = nullptr;
-    err = cudaGetSymbolAddress(&ptr, g_static_workspace);
-    if (err != cudaSuccess) return err;
-    g_static_ptr[dev] = ptr;
+  auto it = g_static_ptr.find({dev, ctx});
+  if (ctx && it != g_static_ptr.end()) {
+    *out = it->second;
+    return cudaSuccess;
   }
-  *out = g_static_ptr[dev];
+  void* ptr = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&ptr, g_static_workspace);
+  if (err != cudaSuccess) return err;
+  // the look-up makes the device's context current if none was: key the entry by it
+  if (!ctx && !current_device_context(&dev, &ctx)) return cudaErrorNoDevice;
+  g_static_ptr[{dev, ctx}] = ptr;
+  *out = ptr;
   return cudaSuccess;
 }
 
@@ -64,23 +72,6 @@ extern "C" qmoe_status qmoe_forward_decode_static(const qmoe_problem* p, const v
 
   void* base = nullptr;
   if (static_workspace(&base) != cudaSuccess) return QMOE_ERR_CUDA;
-  Problem ip{};
-  ip.T = p->T;
-  ip.H = p->hidden;
-  ip.I = p->inter;
-  ip.E = p->num_experts;
-  ip.k = p->top_k;
-  ip.bits = p->bits;
-  ip.block = p->block_size;
-  ip.dtype = p->dtype;
-  ip.path = QMOE_PATH_DECODE;
-  Workspace ws;
-  workspace_layout(ip, false, base, &ws);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws.counters, 0, sizeof(int32_t) * 4, s) != cudaSuccess) return QMOE_ERR_CUDA;
-  if (ws.dunits_max > 0 &&
-      cudaMemsetAsync(ws.dticket, 0, sizeof(int32_t) * ws.dunits_max, s) != cudaSuccess)
-    return QMOE_ERR_CUDA;
   return qmoe_forward(p, x, router_logits, fc1_q, fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out,
                       base, QMOE_STATIC_WORKSPACE_BYTES, stream);
 }

@@ -41,12 +41,18 @@ struct Workspace {
   int32_t* chunk_hist;    // [nchunks][E] per-chunk expert counts, then chunk bases
   int32_t* dtab;          // [kDtabMax][kDtabInts] decode table: one entry per (active expert,
                           //   pair of its routes): expert, first sorted row of the pair, routes in
-                          //   the pair (1 or 2), 0, token of each route; counters[3] entries
+                          //   the pair (1 or 2), route id of the first, token of each route, route
+                          //   id of the second (0 if none), 0; counters[3] entries
   uint16_t* x16s;         // [R][H]   x16 rows gathered into sorted-route order (grouped)
   uint16_t* h16;          // [R][I]   SwiGLU output, FP16, sorted-route order, K-order permuted
   float* y;               // [R][H]   weighted fc2 output per route id (FP32)
   float* dsplit;           // decode split-K partials [work items][4][32] (FP32)
   int32_t* dticket;        // [decode units] arrival counters of the split-K partials
+  int32_t* dsync;          // decode-layer kernel: [0] unit claims, [1] finished blocks,
+                           //   [kSyncHeader ..] fc1 completions per decode-table entry [kDtabMax],
+                           //   then combine arrivals per (token, 32-row group of H) [T][H/32];
+                           //   zeroed by the routing kernel of every decode-path call
+  int64_t dsync_ints;      // capacity of dsync
   int64_t dunits_max;      // capacity of dticket
   int64_t dsplit_items;    // capacity of dsplit in work items
   int64_t max_tiles;
@@ -66,6 +72,12 @@ struct Problem {
 // and split-K work items the workspace is sized for.
 int64_t decode_units_max(const Problem& p);
 int64_t decode_split_items_max(const Problem& p);
+
+// Synchronisation words of the decode-layer kernel (see Workspace::dsync).
+constexpr int kSyncHeader = 4;
+__host__ __device__ inline int64_t decode_sync_ints(const Problem& p) {
+  return kSyncHeader + kDtabMax + p.T * (int64_t)(p.H / 32);
+}
 
 // Byte size of the workspace for problem p and the pointers inside `base`
 // (base may be null when only the size is wanted).
@@ -100,6 +112,26 @@ cudaError_t launch_decode(const Problem& p, bool fc1, const uint8_t* q, const vo
 cudaError_t launch_grouped(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
                            const uint8_t* zp, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cudaStream_t s);
+// The whole decode layer after routing (fc1 + SwiGLU, fc2, combine) as one
+// persistent kernel; applies to INT4 block 32 without zero points, H and inter
+// multiples of 256 (decode.cu's decode_layer_applies).
+bool decode_layer_applies(const Problem& p, bool has_zp);
+cudaError_t launch_decode_layer(const Problem& p, const uint8_t* fc1_q, const void* fc1_scales,
+                                const uint8_t* fc2_q, const void* fc2_scales, const Workspace& ws,
+                                void* out, cudaStream_t s);
+
+// Per-device launch facts (launch_cache.cu), keyed by device and context and
+// safe to call from several host threads.
+int device_sm_count();
+// The calling thread's device ordinal and current context (null before the
+// runtime has made one current); false when no device is available.
+bool current_device_context(int* dev, const void** ctx);
+// Opt kernel fn into `bytes` of dynamic shared memory on the current device.
+cudaError_t ensure_smem_optin(const void* fn, int bytes);
+template <typename F>
+cudaError_t ensure_smem_optin(F* fn, int bytes) {
+  return ensure_smem_optin(reinterpret_cast<const void*>(fn), bytes);
+}
 
 // ---------------------------------------------------------------------------
 // device helpers
@@ -154,5 +186,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// D += A B on the legacy tensor path: m16n8k16, FP16 operands, FP32 accumulators.
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (a & mask) | orv in one LOP3.
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));
+  return d;
+}
 
 }  // namespace qmoe

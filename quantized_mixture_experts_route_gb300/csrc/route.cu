@@ -437,10 +437,10 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
       d[0] = e;
       d[1] = off + 2 * q;
       d[2] = cnt;
-      d[3] = 0;
+      d[3] = s_sorted[off + 2 * q];
       d[4] = s_sorted[off + 2 * q] / p.k;
       d[5] = cnt > 1 ? s_sorted[off + 2 * q + 1] / p.k : 0;
-      d[6] = 0;
+      d[6] = cnt > 1 ? s_sorted[off + 2 * q + 1] : 0;
       d[7] = 0;
     }
     __syncthreads();
@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
     }
   if (dec) {
     for (int64_t i = threadIdx.x; i < ws.dunits_max; i += blockDim.x) ws.dticket[i] = 0;
+    for (int64_t i = threadIdx.x; i < ws.dsync_ints; i += blockDim.x) ws.dsync[i] = 0;
     for (int i = threadIdx.x; i < n_entries * kDtabInts; i += blockDim.x) ws.dtab[i] = s_dtab[i];
   }
   if (x16_mode != kX16None)
@@ -509,16 +510,7 @@ __global__ void __launch_bounds__(256) gather_kernel(Problem p, Workspace ws) {
   }
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int num_sms() { return device_sm_count(); }
 
 }  // namespace
 
@@ -532,16 +524,9 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* logits, co
   if (small) {
     const size_t smem = sizeof(int) * ((size_t)p.E * (1 + kGroupThreads / 32) +
                                        (p.path == QMOE_PATH_DECODE ? (size_t)kDtabMax * kDtabInts : 0));
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t err = cudaFuncSetAttribute(route_group_small_kernel<4>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-      if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(route_group_small_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   96 * 1024);
-      if (err != cudaSuccess) return err;
-      attr = true;
-    }
+    cudaError_t err = ensure_smem_optin(route_group_small_kernel<4>, 96 * 1024);
+    if (err == cudaSuccess) err = ensure_smem_optin(route_group_small_kernel<16>, 96 * 1024);
+    if (err != cudaSuccess) return err;
     if (p.E <= 128)
       return launch_pdl(route_group_small_kernel<4>, dim3(1), dim3(kGroupThreads), smem, s, p, xx, lg, ws,
                         x16_mode, (int)want_tiles);

@@ -156,3 +156,17 @@ def test_bad_stage_range(L, first, last):
     p = P()
     assert L.qmoe_forward_stages(ctypes.byref(p), first, last, *([FAKE] * 10), 1 << 40, None) == \
         qm.QMOE_ERR_INVALID_ARGUMENT
+
+
+def test_launch_facts_are_per_device():
+    """The shared-memory opt-in and the SM count belong to a device's context:
+    the launchers look them up through one per-(device, context) cache, and no
+    launcher keeps a process-wide flag or count of its own."""
+    csrc = os.path.join(ROOT, "quantized_mixture_experts_route_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh")) or name == "launch_cache.cu":
+            continue
+        code = "\n".join(line.split("//")[0] for line in open(os.path.join(csrc, name)).read().splitlines())
+        assert not re.search(r"\bstatic\s+(bool|int)\s+\w+\s*=", code), f"{name}: process-wide launch state"
+        assert "cudaFuncSetAttribute" not in code, f"{name}: opt-in outside the per-device cache"
+        assert "cudaDevAttrMultiProcessorCount" not in code, f"{name}: SM count outside the per-device cache"

@@ -8,12 +8,22 @@ and the epilogue (one or two accumulator buffers). This test replays the same
 slot indices, barrier phase parities and arrival counts as the kernel, with a
 random interleaving of the roles, and checks on every wait that the parity
 test selects exactly the phase the role needs (no phase is skipped or taken
-twice), that no slot is overwritten before its consumer is done with it, and
-that every role finishes (no deadlock). Configurations cover one and several
-tiles, K stage counts below, equal to and above the ring depths, odd stage
-counts (the dequantisation groups swap stages between tiles), scale boxes of
-one stage, and the INT3 ring depths with double-buffered accumulators. The
-model has to follow the kernel: change both together.
+twice), that no slot is overwritten before its consumer is done with it, that
+a role never reads a slot whose copy has not landed, and that every role
+finishes (no deadlock). Bulk tensor copies land asynchronously: a seventh role,
+the copy engine, completes the copies in flight in random order, so a copy can
+land after later ones. Configurations cover one and several tiles, K stage
+counts below, equal to and above the ring depths, odd stage counts (the
+dequantisation groups swap stages between tiles), scale boxes of one stage, and
+the INT3 ring depths with double-buffered accumulators. The model has to follow
+the kernel: change both together.
+
+With an odd code ring (INT4: three slots) a slot's consecutive stages belong
+to different dequantisation groups, and a parity wait alone would pass while
+the other group's earlier copy into the slot is still in flight; the kernel's
+dequantisers therefore first wait until the producer has issued their stage
+into the slot (`issued_word`). test_odd_code_ring_needs_the_issued_word shows
+the model finding that race without it.
 """
 import random
 
@@ -42,8 +52,11 @@ def ready(bar, parity, phase_needed):
     return ok
 
 
-def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed):
+def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
     rnd = random.Random(seed)
+    in_flight = []                                              # copies issued, not landed: (kind, slot, barrier)
+    a_landed, c_landed, s_landed = [False] * SA, [False] * SC, [False] * 2
+    c_issued = [-1] * SC                                        # the kernel's cfill words
     afull = [Barrier(f"afull{s}", 1) for s in range(SA)]
     aempty = [Barrier(f"aempty{s}", 1) for s in range(SA)]
     cfull = [Barrier(f"cfull{s}", 1) for s in range(SC)]
@@ -77,12 +90,14 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed):
                         yield from wait(sempty[m & 1], ((m - 2) >> 1) & 1, (m - 2) // 2 + 1)
                         assert box_left[m - 2] == 0, "scale box overwritten before both groups released it"
                     s_box[m & 1] = m
+                    s_landed[m & 1] = False
                     span_len = min(span, ksteps - i)
                     box_left[m] = 2 if span_len >= 2 else 1
-                    sfull[m & 1].arrive()
+                    in_flight.append(("s", m & 1, sfull[m & 1]))
                 assert c_used[s], "code slot overwritten before it was dequantised"
-                c_slot[s], c_used[s] = it, False
-                cfull[s].arrive()
+                c_slot[s], c_used[s], c_landed[s] = it, False, False
+                c_issued[s] = it
+                in_flight.append(("c", s, cfull[s]))
 
     def act_producer():
         for j in range(works):
@@ -91,8 +106,16 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed):
                 s = it % SA
                 yield from wait(aempty[s], ((it // SA) & 1) ^ 1, it // SA)
                 assert a_used[s], "activation slot overwritten before the MMAs read it"
-                a_slot[s], a_used[s] = it, False
-                afull[s].arrive()
+                a_slot[s], a_used[s], a_landed[s] = it, False, False
+                in_flight.append(("a", s, afull[s]))
+
+    def copy_engine():
+        while True:
+            if in_flight:
+                kind, slot, bar = in_flight.pop(rnd.randrange(len(in_flight)))
+                {"a": a_landed, "c": c_landed, "s": s_landed}[kind][slot] = True
+                bar.arrive()
+            yield
 
     def mma():
         for j in range(works):
@@ -107,6 +130,7 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed):
                 yield from wait(afull[sa], (it // SA) & 1, it // SA + 1)
                 yield from wait(bready[sb], (it // SB) & 1, it // SB + 1)
                 assert a_slot[sa] == it and b_slot[sb] == it, "MMA read the wrong stage"
+                assert a_landed[sa], "MMA read an activation tile still in flight"
                 a_used[sa] = b_used[sb] = True
                 aempty[sa].arrive()
                 bempty[sb].arrive()
@@ -121,13 +145,18 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed):
                 if (it & 1) != grp:
                     continue
                 cs, bs = it % SC, it % SB
+                if issued_word and SC % 2 == 1:
+                    while c_issued[cs] != it:
+                        yield
                 yield from wait(cfull[cs], (it // SC) & 1, it // SC + 1)
                 assert c_slot[cs] == it, "dequantiser read the wrong code stage"
+                assert c_landed[cs], "dequantiser read a code tile still in flight"
                 m_cur = j * nbox + i // span
                 if tsc and m_cur != box_seen:
                     box_seen = m_cur
                     yield from wait(sfull[m_cur & 1], (m_cur >> 1) & 1, (m_cur >> 1) + 1)
                     assert s_box[m_cur & 1] == m_cur, "dequantiser read the wrong scale box"
+                    assert s_landed[m_cur & 1], "dequantiser read a scale box still in flight"
                 yield from wait(bempty[bs], ((it // SB) & 1) ^ 1, it // SB)
                 assert b_used[bs], "B slot overwritten before the MMAs read it"
                 b_slot[bs], b_used[bs] = it, False
@@ -151,12 +180,16 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed):
 
     roles = [code_producer(), act_producer(), mma(), dequant(0), dequant(1), epilogue()]
     live = list(roles)
+    engine = copy_engine()
     steps = 0
     last = None
     while live:
         steps += 1
         assert steps < 10_000_000, "model did not finish"
-        r = rnd.choice(live)
+        r = rnd.choice(live + [engine])
+        if r is engine:
+            next(engine)
+            continue
         try:
             next(r)
         except StopIteration:
@@ -189,3 +222,16 @@ CONFIGS = [
 def test_pipeline_protocol(cfg):
     for seed in range(6):
         simulate(*cfg, seed=seed)
+
+
+def test_odd_code_ring_needs_the_issued_word():
+    """Without the issued-stage word, some interleaving lets a dequantisation
+    group pass its parity wait on a three-slot code ring while the other group's
+    copy into that slot is still in flight."""
+    failures = 0
+    for seed in range(40):
+        try:
+            simulate(32, 3, 3, 3, 3, 1, True, 4, seed=seed, issued_word=False)
+        except AssertionError:
+            failures += 1
+    assert failures > 0

@@ -2,11 +2,14 @@
 library's own fixed device array (no allocation in the call).
 
 The CPU tests check the host-side rejections, which come before any CUDA call.
-The GPU test calls the entry point through the C ABI twice in a row, on two
-different decode layers, and compares each output with qmoe_forward's on the
-same inputs within the parity tolerance of the other GPU tests. This file is
-collected last, so the GPU test also runs after the rest of the suite has used
-the library in the same process.
+The GPU test calls the entry point through the C ABI several times in a row, on
+layers of different sizes (T = 8 with 128 experts and top-8, then T = 1 with 4
+experts and top-2, then T = 5), with no synchronisation between the calls, so a
+value one call leaves in the shared array would reach the next. Each output is
+compared with qmoe_forward's on the same inputs bit for bit (the same kernels
+run) and with the oracle within the parity tolerance of the other GPU tests.
+This file is collected last, so the GPU test also runs after the rest of the
+suite has used the library in the same process.
 """
 import os
 
@@ -62,22 +65,33 @@ def test_source_allocates_nothing():
 
 
 @pytest.mark.gpu
-def test_static_matches_forward_two_calls_in_a_row(L):
+def test_static_matches_forward_and_oracle_calls_in_a_row(L):
     import torch
 
+    import oracle
+    from synthetic import BF16, FP16, Recipe, Shape
+
+    layers = [synthetic.decode_layer(8, 0),
+              (Shape(T=1, H=256, inter=256, E=4, k=2, bits=4, block=32, dtype=BF16),
+               Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 91),
+              (Shape(T=5, H=512, inter=384, E=16, k=4, bits=4, block=32, dtype=FP16),
+               Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 92),
+              synthetic.decode_layer(8, 1)]
     cases = []
-    for layer in (0, 1):
-        shape, recipe, seed = synthetic.decode_layer(8, layer)
+    for shape, recipe, seed in layers:
         inp = synthetic.make_numpy(shape, recipe, seed)
         d = gu.device_inputs(inp)
         ref = gu.gpu_forward(shape, inp, d=d)
         out = torch.full((shape.T, shape.H), -1, dtype=torch.int16, device="cuda")
-        cases.append((shape, d, ref, out))
+        cases.append((shape, inp, d, ref, out))
     torch.cuda.synchronize()
-    for shape, d, _, out in cases:        # two calls in a row, no synchronisation between them
+    for shape, _, d, _, out in cases:      # calls in a row, no synchronisation between them
         qm.qmoe_forward_decode_static(gu.problem(shape), d["x"], d["logits"], d["fc1_q"], d["fc1_s"],
                                       d.get("fc1_zp"), d["fc2_q"], d["fc2_s"], d.get("fc2_zp"), out)
     torch.cuda.synchronize()
-    for i, (shape, _, ref, out) in enumerate(cases):
+    for i, (shape, inp, _, ref, out) in enumerate(cases):
         got = out.cpu().numpy().view(np.uint16)
-        gu.assert_parity(got, ref, shape.dtype, f"static call {i}")
+        assert np.array_equal(got, ref), f"static call {i} differs from qmoe_forward"
+        want, _ = oracle.forward(oracle.Problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits,
+                                                shape.block, shape.dtype), inp)
+        gu.assert_parity(got, want, shape.dtype, f"static call {i} against the oracle")
