@@ -151,16 +151,25 @@ qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* route
  *   rounding).
  * Bias pointers are caller-owned device memory, 16-byte aligned
  * (QMOE_ERR_MISALIGNED otherwise), and only read.
+ * decode_layer_kernel: 0 -- one kernel per stage; 1 -- on the decode path
+ *   with INT4, block 32, no zero points and hidden, inter multiples of 256,
+ *   FC1 and FC2 run as one persistent kernel (the decode layer kernel, whose
+ *   warps stream fc1 and fc2 units from one queue); elsewhere the same as 0.
+ *   Both give results within the same error bound of the pages' definition;
+ *   the layer kernel's result does not depend on the batch a token is packed
+ *   into. Other values: QMOE_ERR_INVALID_ARGUMENT.
  */
 typedef struct {
   int32_t full_softmax;
   const void* fc1_bias;
   const void* fc2_bias;
+  int32_t decode_layer_kernel;
 } qmoe_options;
 
 /*
  * qmoe_forward with options (opt may be NULL: the defaults). Extra errors:
- * QMOE_ERR_INVALID_ARGUMENT if opt->full_softmax is not 0 or 1. The pages
+ * QMOE_ERR_INVALID_ARGUMENT if opt->full_softmax or opt->decode_layer_kernel
+ * is not 0 or 1. The pages
  * define no separate entry point for these options; this one carries them so
  * that qmoe_forward keeps its signature.
  */
@@ -174,11 +183,8 @@ qmoe_status qmoe_forward_ex(const qmoe_problem* p, const qmoe_options* opt, cons
  * Stages of qmoe_forward: ROUTE (top-k routing, grouping by expert and the
  * activations' FP16 conversion), FC1 (fc1 dequant-matmul with the SwiGLU
  * epilogue), FC2 (fc2 dequant-matmul, weighted by the routing weight) and
- * COMBINE (sum over each token's routes, rounded once). On the decode path
- * with INT4, block 32, no zero points and hidden, inter multiples of 256, a
- * range that runs FC1 through COMBINE runs them as one kernel (the decode
- * layer kernel); a range that stops earlier, or starts later, uses the
- * separate kernels of each stage.
+ * COMBINE (sum over each token's routes, rounded once). Each stage runs its
+ * own kernels (qmoe_options.decode_layer_kernel = 0).
  */
 typedef enum {
   QMOE_STAGE_ROUTE = 0,

@@ -68,7 +68,8 @@ class qmoe_problem(ctypes.Structure):
 
 
 class qmoe_options(ctypes.Structure):
-    _fields_ = [("full_softmax", ctypes.c_int32), ("fc1_bias", ctypes.c_void_p), ("fc2_bias", ctypes.c_void_p)]
+    _fields_ = [("full_softmax", ctypes.c_int32), ("fc1_bias", ctypes.c_void_p), ("fc2_bias", ctypes.c_void_p),
+                ("decode_layer_kernel", ctypes.c_int32)]
 
 
 def problem(T, hidden, inter, num_experts, top_k, bits, block_size, dtype, path=QMOE_PATH_AUTO):
@@ -164,8 +165,9 @@ def qmoe_forward(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, f
 
 
 def qmoe_forward_ex(p: qmoe_problem, full_softmax: int, fc1_bias, fc2_bias, x, router_logits, fc1_q,
-                    fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, stream=None) -> None:
-    opt = qmoe_options(int(full_softmax), _addr(fc1_bias), _addr(fc2_bias))
+                    fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, stream=None,
+                    decode_layer_kernel: int = 0) -> None:
+    opt = qmoe_options(int(full_softmax), _addr(fc1_bias), _addr(fc2_bias), int(decode_layer_kernel))
     st = lib().qmoe_forward_ex(ctypes.byref(p), ctypes.byref(opt), _addr(x), _addr(router_logits),
                                _addr(fc1_q), _addr(fc1_scales), _addr(fc1_zp), _addr(fc2_q),
                                _addr(fc2_scales), _addr(fc2_zp), _addr(out), _addr(workspace),

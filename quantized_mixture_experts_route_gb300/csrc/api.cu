@@ -16,10 +16,6 @@ namespace {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// The decode layer kernel (decode_layer.cu) replaces the separate fc1, fc2 and
-// combine launches once it is the faster of the two on the decode stack.
-constexpr bool kUseDecodeLayerKernel = false;
-
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
 int resolve_path(const qmoe_problem& p) {
@@ -131,6 +127,7 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
   const qmoe_status st = check_problem(p);
   if (st != QMOE_OK) return st;
   if (opt && opt->full_softmax != 0 && opt->full_softmax != 1) return QMOE_ERR_INVALID_ARGUMENT;
+  if (opt && opt->decode_layer_kernel != 0 && opt->decode_layer_kernel != 1) return QMOE_ERR_INVALID_ARGUMENT;
   if (p->T == 0) return QMOE_OK;
   if (!x || !router_logits || !fc1_q || !fc1_scales || !fc2_q || !fc2_scales || !out || !workspace)
     return QMOE_ERR_INVALID_ARGUMENT;
@@ -159,10 +156,11 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
     if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
     if (err == cudaSuccess && grouped) err = launch_gather(ip, ws, s);
   }
-  // FC1 through COMBINE of the decode path in one kernel where it applies
-  if (err == cudaSuccess && kUseDecodeLayerKernel && in_range(QMOE_STAGE_FC1) &&
-      last_stage == QMOE_STAGE_COMBINE && decode_layer_applies(ip, fc1_zp || fc2_zp)) {
-    err = launch_decode_layer(ip, fc1_q, fc1_scales, fc2_q, fc2_scales, ws, out, s);
+  // FC1 and FC2 of the decode path in one kernel, where asked for and where it applies
+  if (err == cudaSuccess && opt && opt->decode_layer_kernel && in_range(QMOE_STAGE_FC1) &&
+      in_range(QMOE_STAGE_FC2) && decode_layer_applies(ip, fc1_zp || fc2_zp)) {
+    err = launch_decode_layer(ip, fc1_q, fc1_scales, fc2_q, fc2_scales, ws, s);
+    if (err == cudaSuccess && in_range(QMOE_STAGE_COMBINE)) err = launch_combine(ip, ws, out, s);
     if (err == cudaErrorNotSupported) return QMOE_ERR_UNSUPPORTED;
     return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
   }

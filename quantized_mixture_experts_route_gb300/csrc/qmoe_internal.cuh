@@ -48,10 +48,9 @@ struct Workspace {
   float* y;               // [R][H]   weighted fc2 output per route id (FP32)
   float* dsplit;           // decode split-K partials [work items][4][32] (FP32)
   int32_t* dticket;        // [decode units] arrival counters of the split-K partials
-  int32_t* dsync;          // decode-layer kernel: [0] unit claims, [1] finished blocks,
-                           //   [kSyncHeader ..] fc1 completions per decode-table entry [kDtabMax],
-                           //   then combine arrivals per (token, 32-row group of H) [T][H/32];
-                           //   zeroed by the routing kernel of every decode-path call
+  int32_t* dsync;          // decode layer kernel: [0] unit claims, [kSyncHeader ..] fc1
+                           //   completions per decode-table entry [kDtabMax]; zeroed by the
+                           //   routing kernel of every decode-path call
   int64_t dsync_ints;      // capacity of dsync
   int64_t dunits_max;      // capacity of dticket
   int64_t dsplit_items;    // capacity of dsplit in work items
@@ -75,9 +74,7 @@ int64_t decode_split_items_max(const Problem& p);
 
 // Synchronisation words of the decode-layer kernel (see Workspace::dsync).
 constexpr int kSyncHeader = 4;
-__host__ __device__ inline int64_t decode_sync_ints(const Problem& p) {
-  return kSyncHeader + kDtabMax + p.T * (int64_t)(p.H / 32);
-}
+__host__ __device__ inline int64_t decode_sync_ints(const Problem&) { return kSyncHeader + kDtabMax; }
 
 // Byte size of the workspace for problem p and the pointers inside `base`
 // (base may be null when only the size is wanted).
@@ -112,13 +109,13 @@ cudaError_t launch_decode(const Problem& p, bool fc1, const uint8_t* q, const vo
 cudaError_t launch_grouped(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
                            const uint8_t* zp, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cudaStream_t s);
-// The whole decode layer after routing (fc1 + SwiGLU, fc2, combine) as one
-// persistent kernel; applies to INT4 block 32 without zero points, H and inter
-// multiples of 256 (decode.cu's decode_layer_applies).
+// The decode layer's two expert matmuls (fc1 + SwiGLU, fc2) as one persistent
+// kernel (decode_layer.cu); applies to INT4 block 32 without zero points, H and
+// inter multiples of 256.
 bool decode_layer_applies(const Problem& p, bool has_zp);
 cudaError_t launch_decode_layer(const Problem& p, const uint8_t* fc1_q, const void* fc1_scales,
                                 const uint8_t* fc2_q, const void* fc2_scales, const Workspace& ws,
-                                void* out, cudaStream_t s);
+                                cudaStream_t s);
 
 // Per-device launch facts (launch_cache.cu), keyed by device and context and
 // safe to call from several host threads.

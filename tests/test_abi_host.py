@@ -134,6 +134,30 @@ def test_workspace_too_small(L):
         qm.QMOE_ERR_WORKSPACE_TOO_SMALL
 
 
+@pytest.mark.parametrize("field,value", [("full_softmax", 2), ("full_softmax", -1),
+                                         ("decode_layer_kernel", 2), ("decode_layer_kernel", -1)])
+def test_invalid_option_rejected(L, field, value):
+    """Option values other than 0 and 1 are refused before anything is read or launched."""
+    opt = qm.qmoe_options(0, None, None, 0)
+    setattr(opt, field, value)
+    args = [FAKE] * 10
+    assert L.qmoe_forward_ex(ctypes.byref(P()), ctypes.byref(opt), *args[:9], args[9], 1 << 40, None) == \
+        qm.QMOE_ERR_INVALID_ARGUMENT
+
+
+def test_options_struct_matches_the_header():
+    """The binding's qmoe_options has the header's fields, in order."""
+    import os
+    import re
+
+    from tests.conftest import ROOT
+
+    hdr = open(os.path.join(ROOT, "include", "qmoe.h")).read()
+    body = re.search(r"typedef struct \{([^}]*)\} qmoe_options;", hdr).group(1)
+    names = re.findall(r"(\w+);", body)
+    assert names == [f[0] for f in qm.qmoe_options._fields_]
+
+
 def test_empty_input_is_noop(L):
     # T == 0: OK with no launch, even with null buffers
     p = P(T=0)

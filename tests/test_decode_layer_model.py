@@ -1,200 +1,211 @@
-"""A host model of the decode layer kernel's shared-memory protocol.
+"""A host model of the decode layer kernel's scheduling protocol.
 
-csrc/decode_layer.cu runs one producer warp and four consumer warps per block
-around a ring of slots. The producer claims units (first fc1, then fc2) and, for
-each group of four consecutive 256-wide chunks of a unit, waits until all four
-consumers have handed the slot back, writes the slot's unit, first chunk and
-unit sequence number, arms the slot's mbarrier with the copies' byte count and
-issues the copies, which land later. Consumer warp w multiplies chunk w of
-every slot (and hands back a slot with no chunk for it at once). A warp sums its
-chunks of a unit, then leaves its sum in the unit's partial slot (one of four,
-reused every fourth unit once the unit four earlier has been finished) and
-counts itself; the last warp of the unit adds the sums in warp-position order
-and frees the partial slot. After the last unit the producer arms one slot
-without copies, which stops every consumer.
+csrc/decode_layer.cu runs independent warps. Each warp claims units (an entry's
+32-row group of fc1 or fc2, all of K) from one counter, in the order of the
+kernel's unit queue: the fc1 units of the first L entries, then rounds of one
+entry's fc1 units followed by the fc2 units of the entry L places earlier,
+then the fc2 units of the last L entries. A warp streams a unit's K chunks
+through its own ring of kLStages stages: it issues a chunk's copies as one
+committed group while fewer than kLStages chunks are in flight, claims its next
+unit when it issues the copies of the current unit's last two chunks, and
+multiplies its oldest chunk after waiting until at most (in flight - 1) of its
+groups are pending. The copy engine lands groups in any order. An fc2 chunk's
+activations (the entry's SwiGLU outputs) are copied only once every fc1 unit of
+the entry has finished; a warp that finds them not finished stops issuing,
+multiplies what it has in flight, and only then waits. A block's warps share the
+set of entries already seen finished.
 
-This test replays the kernel's slot indices, parity waits, arrival counts and
-unit bookkeeping with random interleavings and copies that land in random
-order, and checks on every wait that the parity selects exactly the phase the
-role needs, that no warp reads a slot before its copies land or after its
-reuse, that each unit's sum adds exactly its chunks in K order, that no partial
-slot is overwritten before it is read, and that every role finishes. Because
-every consumer waits on every phase of every slot, a parity wait can never pass
-on a phase that is two behind. The ring depth, the consumer count and the
-number of partial slots are read from the CUDA source, so the model follows the
-kernel's constants.
+This test replays that protocol with random interleavings and random landing
+order and checks, at every step, that a chunk is multiplied only after its
+copies landed, that no stage is refilled before it was multiplied, that a
+unit's chunks are multiplied in K order by the warp that claimed it, that an
+fc2 chunk's activations are copied only after all fc1 units of its entry
+finished, that every unit is finished exactly once, and that the warps never
+deadlock (the wait for an entry always ends). The ring depth and the queue
+are read from the CUDA source, so the model follows the kernel.
 """
+import os
 import random
+import re
 
 import pytest
 
-import os
-import re
-
 from tests.conftest import ROOT
+
+SRC = open(os.path.join(ROOT, "quantized_mixture_experts_route_gb300", "csrc", "decode_layer.cu")).read()
 
 
 def _kernel_constant(name):
-    src = open(os.path.join(ROOT, "quantized_mixture_experts_route_gb300", "csrc", "decode_layer.cu")).read()
-    consts = dict(re.findall(r"constexpr int (kL\w+) = (\w+);", src))
+    consts = dict(re.findall(r"constexpr int (kL\w+) = (\w+);", SRC))
     v = consts[name]
     while not v.isdigit():
         v = consts[v]
     return int(v)
 
 
-NC = _kernel_constant("kLConsumers")          # consumer warps, chunks per slot
-RING = _kernel_constant("kLRing")             # slots per block
-UNIT_SLOTS = _kernel_constant("kLUnitSlots")  # partial-sum slots
+STAGES = _kernel_constant("kLStages")
 
 
-class Barrier:
-    def __init__(self, name, count):
-        self.name, self.count, self.arrived, self.completed = name, count, 0, 0
-
-    def arrive(self):
-        self.arrived += 1
-        assert self.arrived <= self.count, f"{self.name}: too many arrivals in one phase"
-        if self.arrived == self.count:
-            self.completed += 1
-            self.arrived = 0
-
-
-def ready(bar, parity, phase_needed):
-    """mbarrier try_wait.parity; it must select exactly completion `phase_needed`."""
-    ok = (bar.completed & 1) != parity
-    if ok:
-        assert bar.completed == phase_needed, (
-            f"{bar.name}: parity wait passed with {bar.completed} completions, needed {phase_needed}")
-    return ok
+def unit_queue(entries, a, b, L):
+    """The kernel's UnitQueue::decode for every position: (fc1?, entry, row group)."""
+    out = []
+    p1, p2 = L * a, L * a + (entries - L) * (a + b)
+    for q in range(entries * (a + b)):
+        if q < p1:
+            out.append((True, q // a, q % a))
+        elif q < p2:
+            r, o = divmod(q - p1, a + b)
+            out.append((True, L + r, o) if o < a else (False, r, o - a))
+        else:
+            r, o = divmod(q - p2, b)
+            out.append((False, entries - L + r, o))
+    return out
 
 
-def simulate(unit_chunks, R, seed):
-    """unit_chunks: chunks per unit of the block's stream, in claim order."""
+def test_queue_is_a_permutation_with_fc1_first():
+    for entries, a, b, L in [(5, 3, 4, 2), (7, 2, 3, 7), (4, 6, 2, 1), (1, 3, 3, 1), (9, 48, 64, 4)]:
+        q = unit_queue(entries, a, b, L)
+        assert sorted(q) == sorted([(True, e, r) for e in range(entries) for r in range(a)] +
+                                   [(False, e, r) for e in range(entries) for r in range(b)])
+        last_fc1 = {e: max(i for i, u in enumerate(q) if u[0] and u[1] == e) for e in range(entries)}
+        first_fc2 = {e: min(i for i, u in enumerate(q) if not u[0] and u[1] == e) for e in range(entries)}
+        assert all(last_fc1[e] < first_fc2[e] for e in range(entries))
+
+
+def test_kernel_queue_matches_the_model():
+    """The model's queue is the kernel's: the same three ranges in the same order."""
+    body = SRC[SRC.index("struct UnitQueue"):SRC.index("template <bool BF16S>")]
+    assert "const int p1 = L * a, p2 = p1 + (entries - L) * (a + b);" in body
+    assert "ei = f1 ? L + r : r;" in body and "ei = entries - L + r;" in body
+
+
+def simulate(entries, a, b, nst1, nst2, warps, per_block, L, seed):
     rnd = random.Random(seed)
-    full = [Barrier(f"full{s}", 1) for s in range(R)]
-    empty = [Barrier(f"empty{s}", NC) for s in range(R)]
-    meta = [None] * R                 # (unit seq, first chunk, chunks) or "end"
-    landed = [False] * R
-    in_flight = []
-    part = {}                         # (partial slot, position) -> (unit seq, chunks summed)
-    u_arrive = [0] * UNIT_SLOTS
-    u_done = [s - UNIT_SLOTS for s in range(UNIT_SLOTS)]
+    queue = unit_queue(entries, a, b, L)
+    nunits = len(queue)
+    claim = [0]
+    fc1_done = [0] * entries
     finished = {}
+    ready = [set() for _ in range((warps + per_block - 1) // per_block)]
 
-    def wait(bar, parity, need):
-        while not ready(bar, parity, need):
-            yield
+    def take():
+        q = claim[0]
+        claim[0] += 1
+        return q
 
-    def producer():
-        i = 0
-        for useq, nst in enumerate(unit_chunks):
-            for j0 in range(0, nst, NC):
-                slot, ph = i % R, (i // R) & 1
-                yield from wait(empty[slot], ph ^ 1, i // R)
-                assert i < R or landed[slot], "slot refilled while its copies were in flight"
-                meta[slot], landed[slot] = (useq, j0, nst), False
-                in_flight.append(slot)
-                i += 1
-        slot, ph = i % R, (i // R) & 1
-        yield from wait(empty[slot], ph ^ 1, i // R)
-        meta[slot], landed[slot] = "end", True
-        full[slot].arrive()
-
-    def copy_engine():
+    def warp(w):
+        blk = ready[w // per_block]
+        ring = [None] * STAGES                 # per stage: (unit, chunk) it holds
+        groups = []                            # per issued group: landed?
+        issued = computed = 0
+        iu = take()
+        nxt = nunits
+        ij = 0
+        chunks_seen = {}
         while True:
-            if in_flight:
-                slot = in_flight.pop(rnd.randrange(len(in_flight)))
-                landed[slot] = True
-                full[slot].arrive()
-            yield
-
-    def consumer(w):
-        i = 0
-        acc = None
-        while True:
-            slot, ph = i % R, (i // R) & 1
-            yield from wait(full[slot], ph, i // R + 1)
-            m = meta[slot]
-            if m == "end":
+            # issue
+            while iu < nunits and issued - computed < STAGES:
+                f1, ei, _ = queue[iu]
+                inst = nst1 if f1 else nst2
+                if not f1 and ij == 0 and ei not in blk:
+                    if fc1_done[ei] < a:
+                        if issued != computed:
+                            break              # drain first
+                        while fc1_done[ei] < a:
+                            yield "wait"
+                    blk.add(ei)
+                if not f1:
+                    assert fc1_done[ei] == a, "fc2 activations copied before the entry's fc1 finished"
+                st = issued % STAGES
+                assert ring[st] is None, "stage refilled before it was multiplied"
+                ring[st] = (iu, ij)
+                groups.append(False)
+                issued += 1
+                if ij == max(inst - 2, 0):
+                    nxt = take()
+                ij += 1
+                if ij == inst:
+                    iu, ij = nxt, 0
+                yield "issue"
+            if issued == computed:
                 return
-            assert landed[slot], f"warp {w} read slot use {i} before its copies landed"
-            useq, j0, nst = m
-            j = j0 + w
-            i += 1
-            if j >= nst:
-                empty[slot].arrive()
-                yield
-                continue
-            if j < NC:
-                acc = []
-            acc.append(j)             # this warp's chunks of the unit, in K order
-            empty[slot].arrive()
-            yield
-            if j + NC < nst:
-                continue
-            us = useq % UNIT_SLOTS
-            while u_done[us] != useq - UNIT_SLOTS:
-                yield
-            assert (us, w) not in part, "partial slot overwritten before it was read"
-            part[(us, w)] = (useq, list(acc))
-            u_arrive[us] += 1
-            if u_arrive[us] != min(nst, NC):
-                continue
-            sums = []
-            for q in range(min(nst, NC)):
-                owner, chunks = part.pop((us, q))
-                assert owner == useq, "partial sum of another unit"
-                sums.append(chunks)
-            u_arrive[us] = 0
-            u_done[us] = useq
-            # warp position q holds chunks q, q + NC, ...: together every chunk once, in order
-            assert all(ch == list(range(q, nst, NC)) for q, ch in enumerate(sums))
-            finished[useq] = True
+            # wait until at most (in flight - 1) groups are pending: all older ones landed
+            while not all(groups[: computed + 1]):
+                yield "copy"
+            st = computed % STAGES
+            u, j = ring[st]
+            f1, ei, _ = queue[u]
+            inst = nst1 if f1 else nst2
+            assert chunks_seen.get(u, 0) == j, "chunks out of K order"
+            chunks_seen[u] = j + 1
+            ring[st] = None
+            computed += 1
+            if j + 1 == inst:
+                assert u not in finished, "unit finished twice"
+                finished[u] = w
+                if f1:
+                    fc1_done[ei] += 1
+            yield "compute"
 
-    roles = [producer()] + [consumer(w) for w in range(NC)]
-    engine = copy_engine()
+    roles = {w: warp(w) for w in range(warps)}
+    # the copy engine reaches each warp's group list through the generator's frame
     live = list(roles)
     steps = 0
-    last = None
+    stalled = 0
     while live:
         steps += 1
-        assert steps < 5_000_000, "model did not finish"
-        r = rnd.choice(live + [engine])
-        if r is engine:
-            next(engine)
-            continue
+        assert steps < 2_000_000, "model did not finish"
+        if rnd.random() < 0.3:
+            # land one random pending group of one random warp
+            cands = [w for w in live if any(not x for x in roles[w].gi_frame.f_locals.get("groups", []))]
+            if cands:
+                w = rnd.choice(cands)
+                gs = roles[w].gi_frame.f_locals["groups"]
+                i = rnd.choice([i for i, x in enumerate(gs) if not x])
+                gs[i] = True
+                stalled = 0
+                continue
+        w = rnd.choice(live)
         try:
-            next(r)
+            r = next(roles[w])
         except StopIteration:
-            live.remove(r)
+            live.remove(w)
+            stalled = 0
             continue
-        if steps % 20000 == 0:
-            snap = (len(live), [(b.completed, b.arrived) for b in full + empty], len(finished))
-            assert snap != last, "deadlock: no role moved in 20000 scheduling steps"
-            last = snap
-    assert len(finished) == len(unit_chunks), "a unit was not finished"
+        stalled = 0 if r in ("issue", "compute") else stalled + 1
+        if stalled > 200_000:
+            raise AssertionError("deadlock: no warp issued or multiplied for 200000 steps")
+    assert sorted(finished) == list(range(nunits)), "a unit was not finished"
 
 
-# chunks per unit: fc1 units of the decode stack (K = 2048: 8 chunks), fc2 units
-# (K = 768: 3 chunks), one-chunk units, and a long-K fc1 (K = 8192: 32 chunks)
-STREAMS = [
-    [8] * 6 + [3] * 9,
-    [3] * 20,
-    [1, 2, 3, 4, 5, 8, 1, 1, 3],
-    [32, 32, 3, 3],
-    [],
-]
+CASES = {
+    # entries, fc1 units per entry, fc2 units per entry, fc1 chunks, fc2 chunks, warps, warps per block
+    "decode_stack_scaled": (9, 6, 8, 8, 3, 10, 4),
+    "few_warps": (5, 3, 4, 8, 3, 2, 2),
+    "one_warp": (3, 2, 2, 4, 2, 1, 1),
+    "one_chunk_units": (6, 2, 3, 1, 1, 7, 3),
+    "many_warps": (4, 2, 2, 3, 2, 16, 4),
+}
 
 
-@pytest.mark.parametrize("stream", STREAMS, ids=["fc1_then_fc2", "fc2_only", "mixed", "long_k", "no_units"])
-def test_layer_protocol(stream):
-    for seed in range(8):
-        simulate(stream, R=RING, seed=seed)
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_layer_protocol(name):
+    entries, a, b, nst1, nst2, warps, per_block = CASES[name]
+    for seed in range(6):
+        # the kernel's lag: one wave of claims (one unit per warp) in fc1-unit lists, plus 2
+        L = min(warps // a + 2, entries)
+        simulate(entries, a, b, nst1, nst2, warps, per_block, L, seed)
 
 
-@pytest.mark.parametrize("R", [1, 2, 5])
-def test_layer_protocol_other_ring_depths(R):
-    """The protocol does not depend on the ring depth (every consumer sees every phase)."""
+@pytest.mark.parametrize("L", [1, 2, "all"])
+def test_layer_protocol_any_lag(L):
+    """The wait always ends whatever the lag: fc1 units precede their fc2 units."""
+    entries, a, b = 6, 3, 4
     for seed in range(4):
-        simulate([8] * 5 + [3] * 7, R=R, seed=seed)
+        simulate(entries, a, b, 4, 2, 5, 2, entries if L == "all" else L, seed)
+
+
+def test_kernel_lag_and_claim_rule_match_the_model():
+    assert "int lag = (int)(gridDim.x * kLWarps) / rg1 + 2;" in SRC
+    assert "if (ij == (inst > 2 ? inst - 2 : 0)) next = atomicAdd(claim, 1);" in SRC
+    assert "if (issued != computed) break;" in SRC

@@ -1,11 +1,11 @@
-"""The decode layer kernel (fc1 + SwiGLU, fc2 and the combine in one persistent
-launch) against the oracle and against the separate stage kernels; the
-workspace's failure word and the NaN output it causes; guard bands.
+"""The decode layer kernel (fc1 + SwiGLU and fc2 in one persistent launch,
+qmoe_options.decode_layer_kernel = 1) against the oracle and against the
+separate stage kernels (the default); the workspace's failure word and the NaN
+output it causes; guard bands.
 
 CPU test: the failure word's offset from the C ABI. GPU tests (-m gpu): the
-kernel runs whenever a decode-path call covers FC1 through COMBINE with INT4,
-block 32, no zero points and hidden, inter multiples of 256; the separate
-kernels run when the stages are enqueued one by one.
+kernel runs when asked for on a decode-path call with INT4, block 32, no zero
+points and hidden, inter multiples of 256; the separate kernels run otherwise.
 """
 import numpy as np
 import pytest
@@ -19,17 +19,20 @@ qm = pytest.importorskip("quantized_mixture_experts_route_gb300")
 from quantized_mixture_experts_route_gb300 import build as qbuild  # noqa: E402
 
 
-def layer_kernel_dispatched():
-    """Whether qmoe_forward runs the decode layer kernel (csrc/api.cu's switch)."""
-    import os
-    import re
+def layer_forward(shape, inp, d=None, ws=None, out=None):
+    """qmoe_forward_ex with the decode layer kernel."""
+    import torch
 
-    from tests.conftest import ROOT
-
-    src = open(os.path.join(ROOT, "quantized_mixture_experts_route_gb300", "csrc", "api.cu")).read()
-    m = re.search(r"constexpr bool kUseDecodeLayerKernel = (true|false);", src)
-    assert m, "dispatch switch not found"
-    return m.group(1) == "true"
+    p = gu.problem(shape)
+    d = d or gu.device_inputs(inp)
+    if ws is None:
+        ws = torch.empty(qm.qmoe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    if out is None:
+        out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+    qm.qmoe_forward_ex(p, 0, None, None, d["x"], d["logits"], d["fc1_q"], d["fc1_s"], d.get("fc1_zp"),
+                       d["fc2_q"], d["fc2_s"], d.get("fc2_zp"), out, ws, decode_layer_kernel=1)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().view(np.uint16)
 
 
 def oproblem(shape):
@@ -85,7 +88,7 @@ def test_layer_kernel_parity_and_stage_kernels(name):
     shape, recipe, seed = CASES[name]
     inp = synthetic.make_numpy(shape, recipe, seed)
     d = gu.device_inputs(inp)
-    fused = gu.gpu_forward(shape, inp, d=d)
+    fused = layer_forward(shape, inp, d=d)
     staged = staged_forward(shape, inp, d=d)
     ref, _ = oracle.forward(oproblem(shape), inp)
     gu.assert_parity(fused, ref, shape.dtype, f"{name} (layer kernel)")
@@ -99,19 +102,17 @@ def test_layer_kernel_is_batch_independent():
     """Each route's sums run over all of K in one warp in a fixed order, so a
     token's output does not depend on the batch it is packed into: packed and
     per-sequence calls agree bit for bit, and so do repeated calls."""
-    if not layer_kernel_dispatched():
-        pytest.skip("qmoe_forward does not dispatch the decode layer kernel")
     shape, recipe, seed = synthetic.decode_layer(8)
     inp = synthetic.make_numpy(shape, recipe, seed)
-    whole = gu.gpu_forward(shape, inp)
-    assert np.array_equal(whole, gu.gpu_forward(shape, inp))
+    whole = layer_forward(shape, inp)
+    assert np.array_equal(whole, layer_forward(shape, inp))
     d = gu.device_inputs(inp)
     parts, start = [], 0
     for L in (3, 1, 4):
         sub_shape = Shape(**{**shape.__dict__, "T": L})
         sub = dict(inp, x=inp["x"][start:start + L], logits=inp["logits"][start:start + L])
         dd = dict(d, x=gu.dev(sub["x"]), logits=gu.dev(sub["logits"]))
-        parts.append(gu.gpu_forward(sub_shape, sub, d=dd))
+        parts.append(layer_forward(sub_shape, sub, d=dd))
         start += L
     assert np.array_equal(np.concatenate(parts), whole)
 
@@ -125,7 +126,7 @@ def test_layer_kernel_zero_weight_route_is_skipped():
     s = inp["fc2_s"].copy()
     s[2:] = 0x7E00  # NaN scales in the experts that only receive zero-weight routes
     inp["fc2_s"] = s
-    got = gu.gpu_forward(shape, inp)
+    got = layer_forward(shape, inp)
     ref, _ = oracle.forward(oproblem(shape), inp)
     gu.assert_parity(got, ref, shape.dtype, "zero-weight")
 
@@ -136,11 +137,11 @@ def _nan(bits, dtype):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("last_stages", ["combine_kernel", "layer_kernel"])
-def test_failure_word_turns_the_output_into_nan(last_stages):
+def test_failure_word_turns_the_output_into_nan():
     """No wait is made to run out: the failure word is written from the host
-    between the routing stage and the rest, as a kernel that gave up would
-    leave it, and the call's last step must then write NaN everywhere."""
+    between the stages, as a kernel that gave up would leave it, and the
+    call's last step (the combine kernel, which follows the separate matmul
+    kernels and the decode layer kernel alike) must then write NaN everywhere."""
     import torch
 
     shape, recipe, seed = synthetic.decode_layer(4)
@@ -156,19 +157,14 @@ def test_failure_word_turns_the_output_into_nan(last_stages):
     torch.cuda.synchronize()
     assert int(ws[off:off + 4].view(torch.int32).item()) == 0
     assert not _nan(out.cpu().numpy().view(np.uint16), shape.dtype).any()
-    if last_stages == "combine_kernel":
+    for code in (2, 3):
         for st in range(3):
             qm.qmoe_forward_stages(p, st, st, *args)
         torch.cuda.synchronize()
-        ws[off:off + 4].view(torch.int32).fill_(2)
+        ws[off:off + 4].view(torch.int32).fill_(code)
         qm.qmoe_forward_stages(p, 3, 3, *args)
-    else:
-        qm.qmoe_forward_stages(p, 0, 0, *args)
         torch.cuda.synchronize()
-        ws[off:off + 4].view(torch.int32).fill_(3)
-        qm.qmoe_forward_stages(p, 1, 3, *args)
-    torch.cuda.synchronize()
-    assert _nan(out.cpu().numpy().view(np.uint16), shape.dtype).all()
+        assert _nan(out.cpu().numpy().view(np.uint16), shape.dtype).all()
     # the next complete call resets the word and computes normally again
     qm.qmoe_forward(p, *args)
     torch.cuda.synchronize()
@@ -206,7 +202,7 @@ def test_outputs_stay_inside_their_buffers(name):
     out_big = torch.full((shape.T * shape.H + G,), 0x3C3C, dtype=torch.int16, device="cuda")
     ws = ws_big[G:G + n_ws]
     out = out_big[G // 2:G // 2 + shape.T * shape.H].view(shape.T, shape.H)
-    got = gu.gpu_forward(shape, inp, ws=ws, out=out)
+    got = (layer_forward if name == "layer_kernel" else gu.gpu_forward)(shape, inp, ws=ws, out=out)
     wb = ws_big.cpu().numpy()
     ob = out_big.cpu().numpy()
     assert (wb[:G] == 0x5A).all() and (wb[G + n_ws:] == 0x5A).all()
