@@ -3,14 +3,20 @@
 
 Default workload: the decode stack -- 48 independent QMoE layers of shape
 H=2048, inter=768, E=128, top-k=8, INT4 block 32, BF16, run back to back on
-T=8 packed tokens, layer l+1 consuming layer l's output. One step is one pass
-through the 48 layers (every step of the method: routing, grouping, fc1 +
-SwiGLU, fc2, combine). Weights total 16.3 GB, far larger than L2, so no flush
-is needed between steps. The 48 layer calls are captured once in a CUDA graph
-through the public C ABI and replayed.
+T=8 packed tokens, layer l+1 consuming layer l's output. One step is 12 passes
+through the 48 layers (576 layer calls, each with its own router logits; every
+step of the method: routing, grouping, fc1 + SwiGLU, fc2, combine), about
+28 ms, so the default 20 steps time more than half a second. Weights total
+16.3 GB, far larger than L2, so no flush is needed between steps. The calls are
+captured once in a CUDA graph through the public C ABI and replayed.
 
---workload prefill: one layer of the same shape on T=8192 packed tokens
-(16 sequences of lengths ~U[128,1024]), the grouped tcgen05 path.
+The same line carries the prefill half of the metric (`prefill`): the same 48
+layers' weights on T=8192 packed tokens (16 sequences of lengths
+~U[128,1024]), the grouped tcgen05 path, one step = one pass through the 48
+layers, with its own roofline (grouped fc1 and the whole layer against the
+measured dense BF16 peak), e2e and CPU baseline.
+
+--workload prefill / int3 / int2: one layer of the named shape.
 
 Prints one JSON line (rank 0). --impl reference times the CPU oracle on the
 host cores on a bounded sample of the same workload.
@@ -49,10 +55,19 @@ def parse():
     ap.add_argument("--block", type=int, default=64, help="INT3 block size (64 or 128)")
     ap.add_argument("--T", type=int, default=None, help="tokens per step (decode default 8)")
     ap.add_argument("--layers", type=int, default=LAYERS)
-    ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
+    ap.add_argument("--passes", type=int, default=12,
+                    help="decode: passes through the layer stack per step (a step of about 28 ms, so "
+                         "that the default 20 steps time more than 0.5 s)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode: leave out the prefill half of the line")
+    ap.add_argument("--prefill-steps", type=int, default=None, help="prefill steps (default: --steps)")
+    ap.add_argument("--cpu-sample-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--options", action="store_true",
                     help="run qmoe_forward_ex with FC1/FC2 biases and full-softmax routing weights")
+    ap.add_argument("--decode-layer-kernel", action="store_true",
+                    help="decode: qmoe_forward_ex with the decode layer kernel (fc1 and fc2 in one "
+                         "persistent kernel) instead of one kernel per stage")
     ap.add_argument("--clock-log", default=None,
                     help="CSV file for the nvidia-smi clock samples (default: a file in the temp directory)")
     return ap.parse_args()
@@ -60,15 +75,24 @@ def parse():
 
 # --------------------------------------------------------------------------- common
 
+def pass_count(args):
+    return args.passes if args.workload == "decode" else 1
+
+
 def workload_config(args, shape, layers, world):
     """The `config` object of the bench line (the same for both arms)."""
+    passes = pass_count(args)
+    step = (f"one step = {passes} passes through the {layers} layers (call c runs layer c mod {layers} "
+            f"on call c-1's output, with its own router logits)" if passes > 1 else
+            f"one step = one pass through the {layers} layer(s)")
     return {"workload": (f"{args.workload}: {layers} QMoE layers H={shape.H} inter={shape.inter} "
                          f"E={shape.E} k={shape.k} INT{shape.bits} b{shape.block} "
                          f"{'BF16' if shape.dtype == 0 else 'FP16'} T={shape.T} per rank"),
-            "T": shape.T, "layers": layers, "parallelism": f"replicas x{world}",
+            "T": shape.T, "layers": layers, "passes": passes, "step": step, "parallelism": f"replicas x{world}",
             "l2": "weights 16.3 GB >> L2, no flush" if args.workload == "decode" else "inputs > L2 per step",
             **({"options": "fc1/fc2 biases N(0, 0.5), full-softmax routing weights"}
-               if getattr(args, "options", False) else {})}
+               if getattr(args, "options", False) else {}),
+            **({"decode_layer_kernel": 1} if getattr(args, "decode_layer_kernel", False) else {})}
 
 
 def reduce_max(v, device):
@@ -290,6 +314,14 @@ def run_reference(args):
         res = oracle_rate(shape, recipe, args, 0, budget)
         per_step.append(res["value"])
     value = statistics.median(per_step)
+    prefill = None
+    if args.workload == "decode" and not args.no_prefill:
+        pshape, precipe, _ = synthetic.prefill_8k()
+        pargs = argparse.Namespace(**{**vars(args), "workload": "prefill"})
+        pres = oracle_rate(pshape, precipe, pargs, 0, args.cpu_sample_seconds)
+        prefill = {"value": pres["value"], "unit": "layer-tokens/s", "cpu_baseline": pres,
+                   "e2e": {"value": pres["value"], "unit": "layer-tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}}
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "layer-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -299,6 +331,7 @@ def run_reference(args):
         "cpu_baseline": {**res, "value": value},
         "e2e": {"value": value, "unit": "layer-tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        **({"prefill": prefill} if prefill else {}),
     }
     print(json.dumps(line), flush=True)
 
@@ -324,13 +357,185 @@ def p_path(shape):
     return "decode" if shape.T <= 8 else "grouped"
 
 
-def launches_per_layer(path, shape):
-    """Kernels one qmoe_forward call launches (see csrc/api.cu and csrc/route.cu)."""
+def launches_per_layer(path, shape, layer_kernel=False):
+    """Kernels one qmoe_forward call launches (csrc/api.cu and csrc/route.cu)."""
     small = shape.T * shape.k <= 512
     route = 1 if small else 4            # fused route+group, or route, count, scan, scatter
     if path == "decode":
-        return route + 3                 # fc1, fc2, combine
+        return route + (2 if layer_kernel else 3)   # (layer kernel or fc1, fc2), combine
     return route + 1 + 3                 # gather, fc1, fc2, combine
+
+
+class Stack:
+    """`passes` passes through `layers` QMoE layers (weights W[l]) on T tokens, through
+    the public C ABI: call c runs layer c mod layers on the previous call's output
+    (call 0 on x) with its own router logits. Inputs are copied from pinned host
+    memory; the calls are captured in CUDA graphs."""
+
+    def __init__(self, qm, shape, W, x_h, logits_h, passes, device, options=None):
+        import torch
+
+        self.qm, self.shape, self.W, self.options = qm, shape, W, options
+        self.layers, self.passes = len(W), passes
+        self.calls = passes * self.layers
+        assert logits_h.shape[0] == self.calls
+        self.p = qm.problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
+                            shape.dtype, qm.QMOE_PATH_AUTO)
+        self.x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
+        self.lg_pin = torch.from_numpy(logits_h.view(np.int16)).pin_memory()
+        self.x_d = self.x_pin.to(device)
+        self.lg_d = self.lg_pin.to(device)
+        self.bufs = [torch.empty((shape.T, shape.H), dtype=torch.int16, device=device) for _ in range(2)]
+        self.ws = torch.empty(qm.qmoe_workspace_bytes(self.p), dtype=torch.uint8, device=device)
+        self.out_pin = torch.empty((shape.T, shape.H), dtype=torch.int16).pin_memory()
+        self.final = self.bufs[(self.calls - 1) % 2]
+
+    def args(self, c):
+        src = self.x_d if c == 0 else self.bufs[(c - 1) % 2]
+        w = self.W[c % self.layers]
+        return (src, self.lg_d[c], w["fc1_q"], w["fc1_s"], None, w["fc2_q"], w["fc2_s"], None,
+                self.bufs[c % 2], self.ws)
+
+    def step(self):
+        o = self.options
+        for c in range(self.calls):
+            if o is not None:
+                l = c % self.layers
+                self.qm.qmoe_forward_ex(self.p, o["full_softmax"], o["b1"][l] if o["b1"] else None,
+                                        o["b2"][l] if o["b2"] else None, *self.args(c),
+                                        decode_layer_kernel=o["layer_kernel"])
+            else:
+                self.qm.qmoe_forward(self.p, *self.args(c))
+
+    def capture(self, stream):
+        import torch
+
+        with torch.cuda.stream(stream):
+            self.step()                   # eager warm-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.step()
+        return g
+
+    def stage_graphs(self, stream):
+        """Per stage, one graph of that stage alone for the last pass's calls (the
+        workspace holds a valid previous state): the stage kernels' own durations."""
+        import torch
+
+        out = []
+        for st in range(4):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in range(self.calls - self.layers, self.calls):
+                    self.qm.qmoe_forward_stages(self.p, st, st, *self.args(c))
+            out.append(g)
+        return out
+
+    def h2d_bytes(self):
+        return int(self.x_pin.numel() * 2 + self.lg_pin.numel() * 2)
+
+    def d2h_bytes(self):
+        return int(self.out_pin.numel() * 2)
+
+
+def device_uuid(device):
+    import torch
+
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        return None
+
+
+def time_graph(g, stream, steps, warmup, device, clock_path, world):
+    """Warm-up replays, then exactly `steps` replays between events on the launching
+    stream, with a barrier and a synchronize on both sides: (per-step ms list,
+    mean ms per step over the slowest rank, clock summary)."""
+    import torch
+    import torch.distributed as dist
+
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(device_uuid(device), clock_path) as clocks:
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            marks[0].record()
+            for i in range(steps):
+                g.replay()
+                marks[i + 1].record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
+    ms = reduce_max(marks[0].elapsed_time(marks[-1]) / steps, device)
+    return step_ms, ms, clocks.summary()
+
+
+def time_stages(graphs, stream, steps, launches):
+    """ms per launch of each stage: events around `steps` replays of its graph."""
+    import torch
+
+    out = np.zeros(len(graphs))
+    for st, gst in enumerate(graphs):
+        gst.replay()   # warm
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record()
+            for _ in range(steps):
+                gst.replay()
+            b.record()
+        torch.cuda.synchronize()
+        out[st] = a.elapsed_time(b) / (steps * launches)
+    return out
+
+
+def time_e2e(stack, g, stream, steps, device):
+    """Seconds per step, end to end: pinned host inputs -> device, the step's calls,
+    the result -> pinned host memory, every step."""
+    import torch
+
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            stack.x_d.copy_(stack.x_pin, non_blocking=True)
+            stack.lg_d.copy_(stack.lg_pin, non_blocking=True)
+            g.replay()
+            stack.out_pin.copy_(stack.final, non_blocking=True)
+        stream.synchronize()
+    return reduce_max((time.perf_counter() - t0) / steps, device)
+
+
+def stage_us(stage_ms):
+    return {"route_group": round(stage_ms[0] * 1e3, 2), "fc1": round(stage_ms[1] * 1e3, 2),
+            "fc2": round(stage_ms[2] * 1e3, 2), "combine": round(stage_ms[3] * 1e3, 2)}
+
+
+def tensor_roofline(shape, fc1_ms, peaks, traffic):
+    """The grouped fc1 launch against the measured dense BF16 peak (FP16 operands run
+    at the same rate): 2 x routes x 2I x H FLOPs per launch."""
+    flops = 2.0 * shape.T * shape.k * (2 * shape.inter * shape.H)
+    tf = peaks.get("bf16_tflops")
+    peak = tf if tf else 1900.0
+    achieved = flops / (fc1_ms / 1e3) / 1e12
+    out = {"bound": "tensor", "kernel": "grouped fc1 dequant-GEMM + SwiGLU (tcgen05, FP16 operands)",
+           "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+           "peak_source": "measured burst" if tf else "fallback", "algorithmic_flops_per_launch": flops,
+           "traffic": traffic, "traffic_unit": "bytes per launch (ncu)"}
+    if peaks.get("bf16_tflops_sustained"):
+        out["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+    return out
+
+
+def layer_flops(shape):
+    return 2.0 * shape.T * shape.k * (2 * shape.inter * shape.H + shape.H * shape.inter)
+
 
 def run_ours(args):
     import torch
@@ -352,29 +557,10 @@ def run_ours(args):
 
     shape, recipe = workload_shape(args)
     layers = layer_count(args)
-    path = qm.QMOE_PATH_AUTO
-    p = qm.problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
-                   shape.dtype, path)
+    passes = pass_count(args)
     W = [synthetic.make_torch_weights(shape, recipe, 1000 + l, device) for l in range(layers)]
-    x_h, logits_h = host_inputs(shape, recipe, layers, rank)
-    x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
-    lg_pin = torch.from_numpy(logits_h.view(np.int16)).pin_memory()
-    x_d = x_pin.to(device)
-    lg_d = lg_pin.to(device)
-    bufs = [torch.empty((shape.T, shape.H), dtype=torch.int16, device=device) for _ in range(2)]
-    ws = torch.empty(qm.qmoe_workspace_bytes(p), dtype=torch.uint8, device=device)
-    out_pin = torch.empty((shape.T, shape.H), dtype=torch.int16).pin_memory()
-
-    def layer_io(l):
-        src = x_d if l == 0 else bufs[(l - 1) % 2]
-        return src, bufs[l % 2]
-
-    def layer_args(l):
-        src, dst = layer_io(l)
-        w = W[l]
-        return (src, lg_d[l], w["fc1_q"], w["fc1_s"], None, w["fc2_q"], w["fc2_s"], None, dst, ws)
-
-    B1 = B2 = None
+    x_h, logits_h = host_inputs(shape, recipe, layers * passes, rank)
+    options = None
     if args.options:
         gb = torch.Generator(device=device)
         gb.manual_seed(7)
@@ -383,88 +569,37 @@ def run_ours(args):
               .view(torch.int16) for _ in range(layers)]
         B2 = [(torch.randn((shape.E, shape.H), generator=gb, device=device) * 0.5).to(tdt)
               .view(torch.int16) for _ in range(layers)]
-
-    def step():
-        for l in range(layers):
-            if args.options:
-                qm.qmoe_forward_ex(p, 1, B1[l], B2[l], *layer_args(l))
-            else:
-                qm.qmoe_forward(p, *layer_args(l))
-
-    def stage_only(st):
-        # one stage of every layer, back to back: its kernels' own durations, with no
-        # timing nodes between them (the workspace holds a valid previous state)
-        for l in range(layers):
-            qm.qmoe_forward_stages(p, st, st, *layer_args(l))
-
-    final = bufs[(layers - 1) % 2]
+        options = dict(full_softmax=1, b1=B1, b2=B2, layer_kernel=0)
+    if args.decode_layer_kernel:
+        options = dict(options or dict(full_softmax=0, b1=None, b2=None), layer_kernel=1)
+    stack = Stack(qm, shape, W, x_h, logits_h, passes, device, options)
     s = torch.cuda.Stream(device)
     torch.cuda.synchronize()
-    with torch.cuda.stream(s):
-        step()  # eager warm-up outside capture
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        step()
-    gs = []
-    for st in range(4):
-        gst = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gst, stream=s):
-            stage_only(st)
-        gs.append(gst)
+    g = stack.capture(s)
+    gs = stack.stage_graphs(s)
     torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        g.replay()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        uuid = None
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    with ClockSampler(uuid, args.clock_log) as clocks:
-        torch.cuda.synchronize()
-        with torch.cuda.stream(s):
-            marks[0].record()
-            for i in range(args.steps):
-                g.replay()
-                marks[i + 1].record()
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
-    ms = reduce_max(marks[0].elapsed_time(marks[-1]) / args.steps, device)
-
-    # stage durations: CUDA events on the launching stream around `steps` replays of
-    # each single-stage graph (every layer's launch of that stage)
-    stage_ms = np.zeros(4)
+    step_ms, ms, clocks = time_graph(g, s, args.steps, args.warmup, device, args.clock_log, world)
     g.replay()
-    for st in range(4):
-        gs[st].replay()   # warm
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s):
-            a.record()
-            for _ in range(args.steps):
-                gs[st].replay()
-            b.record()
-        torch.cuda.synchronize()
-        stage_ms[st] = a.elapsed_time(b) / (args.steps * layers)  # ms per launch of each stage
+    stage_ms = time_stages(gs, s, args.steps, layers)
+    e2e_s = time_e2e(stack, g, s, args.steps, device)
 
-    # end to end: pinned host inputs -> device, 48 layers, result -> host, every step
-    torch.cuda.synchronize()
-    e2e_t0 = time.perf_counter()
-    for _ in range(args.steps):
-        with torch.cuda.stream(s):
-            x_d.copy_(x_pin, non_blocking=True)
-            lg_d.copy_(lg_pin, non_blocking=True)
-            g.replay()
-            out_pin.copy_(final, non_blocking=True)
-        s.synchronize()
-    e2e_s = reduce_max((time.perf_counter() - e2e_t0) / args.steps, device)
+    # the prefill half of the metric: the same 48 layers' weights on 8192 packed tokens
+    prefill = None
+    if args.workload == "decode" and not args.options and not args.decode_layer_kernel and not args.no_prefill:
+        pshape, precipe, _ = synthetic.prefill_8k()
+        px_h, plg_h = host_inputs(pshape, precipe, layers, rank)
+        pstack = Stack(qm, pshape, W, px_h, plg_h, 1, device)
+        pg = pstack.capture(s)
+        pgs = pstack.stage_graphs(s)
+        psteps = args.prefill_steps or args.steps
+        pclock = (args.clock_log + ".prefill") if args.clock_log else None
+        pstep_ms, pms, pclocks = time_graph(pg, s, psteps, args.warmup, device, pclock, world)
+        pg.replay()
+        pstage_ms = time_stages(pgs, s, psteps, layers)
+        pe2e_s = time_e2e(pstack, pg, s, psteps, device)
+        prefill = dict(shape=pshape, recipe=precipe, stack=pstack, step_ms=pstep_ms, ms=pms, clocks=pclocks,
+                       stage_ms=pstage_ms, e2e_s=pe2e_s, steps=psteps, logits=plg_h)
 
     if rank != 0:
         if world > 1:
@@ -472,8 +607,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    tokens_per_step = shape.T * layers * world
-    value = job_rate(shape.T * layers, world, ms / 1e3)
+    value = job_rate(shape.T * layers * passes, world, ms / 1e3)
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -481,57 +615,96 @@ def run_ours(args):
         pass
     fc1_b, fc2_b = expert_bytes(shape)
     # the captured kernels' workloads (traffic figures hold for the plain call only)
-    default_kernel = args.workload in ("decode", "prefill") and not args.options
+    default_kernel = args.workload in ("decode", "prefill") and not args.options and not args.decode_layer_kernel
+    nact = distinct_experts(logits_h, shape.dtype, shape.k)
     if shape.T <= 8:
-        nact = distinct_experts(logits_h, shape.dtype, shape.k)
-        # the single-stage graphs run on the routing of the last layer
+        # the single-stage graphs run on the routing of the last call
         bytes_fc1 = float(nact[-1]) * fc1_b
         hbm = peaks.get("hbm_gbs")
+        peak = hbm if hbm else 6800.0
         achieved = bytes_fc1 / (stage_ms[1] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": "decode fc1 dequant-GEMV + SwiGLU",
-                "achieved": round(achieved, 1), "peak": hbm if hbm else 6800.0, "unit": "GB/s",
-                "frac": round(achieved / (hbm if hbm else 6800.0), 4),
-                "peak_source": "measured" if hbm else "fallback",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": "measured" if hbm else "fallback",
                 "algorithmic_bytes_per_launch": int(bytes_fc1),
                 "traffic": kernel_traffic("decode_fc1") if default_kernel else None,
                 "traffic_unit": "bytes per launch (ncu)"}
+        per_call_ms = ms / (layers * passes)
+        if args.decode_layer_kernel:
+            # the stage calls run the separate kernels: the layer kernel is read through the whole call
+            lb = float(np.mean(nact)) * (fc1_b + fc2_b)
+            achieved = lb / (per_call_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "kernel": "decode layer kernel (whole call: routing, layer kernel, combine)",
+                    "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "peak_source": "measured" if hbm else "fallback",
+                    "algorithmic_bytes_per_launch": int(lb), "traffic": None,
+                    "traffic_unit": "bytes per launch (ncu)"}
         extra = {"distinct_experts_per_layer_mean": float(np.mean(nact)),
                  "fc2_GBps": round(float(nact[-1]) * fc2_b / (stage_ms[2] / 1e3) / 1e9, 1),
-                 "layer_GBps": round(float(np.mean(nact)) * (fc1_b + fc2_b) / (ms / layers / 1e3) / 1e9, 1)}
+                 "layer_GBps": round(float(np.mean(nact)) * (fc1_b + fc2_b) / (per_call_ms / 1e3) / 1e9, 1),
+                 "layer_frac_of_hbm": round(float(np.mean(nact)) * (fc1_b + fc2_b) / (per_call_ms / 1e3) / 1e9
+                                            / peak, 4)}
     else:
-        flops = 2.0 * shape.T * shape.k * (2 * shape.inter * shape.H)
-        tf = peaks.get("bf16_tflops")
-        achieved = flops / (stage_ms[1] / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": "grouped fc1 dequant-GEMM + SwiGLU (tcgen05, FP16 operands)",
-                "achieved": round(achieved, 1), "peak": tf if tf else 1900.0, "unit": "TFLOP/s",
-                "frac": round(achieved / (tf if tf else 1900.0), 4),
-                "peak_source": "measured" if tf else "fallback", "algorithmic_flops_per_launch": flops,
-                "traffic": kernel_traffic("prefill_fc1") if default_kernel else None,
-                "traffic_unit": "bytes per launch (ncu)"}
-        # the same launch read as a byte stream: the selected experts' fc1 codes + scales
-        nact = distinct_experts(logits_h, shape.dtype, shape.k)
+        roof = tensor_roofline(shape, stage_ms[1], peaks,
+                               kernel_traffic("prefill_fc1") if default_kernel else None)
+        lt = layer_flops(shape) / (ms / layers / 1e3) / 1e12
         extra = {"fc1_GBps": round(float(nact[-1]) * fc1_b / (stage_ms[1] / 1e3) / 1e9, 1),
-                 "distinct_experts_per_layer_mean": float(np.mean(nact))}
+                 "distinct_experts_per_layer_mean": float(np.mean(nact)),
+                 "layer_tflops": round(lt, 1), "layer_frac": round(lt / roof["peak"], 4)}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "layer-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "ms_per_step_stats": {"median": round(float(np.median(step_ms)), 4),
                               "min": round(float(np.min(step_ms)), 4), "max": round(float(np.max(step_ms)), 4)},
+        "timed_region_s": round(ms * args.steps / 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32-acc",
         "data": "synthetic",
         "config": workload_config(args, shape, layers, world),
         "roofline": roof,
-        "stage_us": {"route_group": round(stage_ms[0] * 1e3, 2), "fc1": round(stage_ms[1] * 1e3, 2),
-                     "fc2": round(stage_ms[2] * 1e3, 2), "combine": round(stage_ms[3] * 1e3, 2)},
-        "e2e": {"value": round(tokens_per_step / e2e_s, 1), "unit": "layer-tokens/s",
-                "h2d_bytes_per_step": int(x_pin.numel() * 2 + lg_pin.numel() * 2),
-                "d2h_bytes_per_step": int(out_pin.numel() * 2)},
-        "gpu_launches": int(launches_per_layer(p_path(shape), shape) * layers * args.steps),
-        "clocks": clocks.summary(),
+        "stage_us": stage_us(stage_ms),
+        "e2e": {"value": round(shape.T * layers * passes * world / e2e_s, 1), "unit": "layer-tokens/s",
+                "h2d_bytes_per_step": stack.h2d_bytes(), "d2h_bytes_per_step": stack.d2h_bytes()},
+        "gpu_launches": int(launches_per_layer(p_path(shape), shape, args.decode_layer_kernel) * layers * passes
+                            * args.steps),
+        "clocks": clocks,
         **extra,
     }
+    if prefill is not None:
+        ps = prefill["shape"]
+        pms = prefill["ms"]
+        proof = tensor_roofline(ps, prefill["stage_ms"][1], peaks, kernel_traffic("prefill_fc1"))
+        lt = layer_flops(ps) / (pms / layers / 1e3) / 1e12
+        pn = distinct_experts(prefill["logits"], ps.dtype, ps.k)
+        line["prefill"] = {
+            "workload": (f"prefill: {layers} QMoE layers (the decode stack's weights) on T={ps.T} packed "
+                         f"tokens from {len(prefill['recipe'].seq_lens)} sequences ~U[128,1024]; "
+                         f"one step = one pass through the {layers} layers"),
+            "value": round(job_rate(ps.T * layers, world, pms / 1e3), 1), "unit": "layer-tokens/s",
+            "steps": prefill["steps"], "ms_per_step": round(pms, 4),
+            "ms_per_layer": round(pms / layers, 4),
+            "ms_per_step_stats": {"median": round(float(np.median(prefill["step_ms"])), 4),
+                                  "min": round(float(np.min(prefill["step_ms"])), 4),
+                                  "max": round(float(np.max(prefill["step_ms"])), 4)},
+            "timed_region_s": round(pms * prefill["steps"] / 1e3, 3),
+            "roofline": proof,
+            "layer_roofline": {"bound": "tensor", "algorithmic_flops_per_layer": layer_flops(ps),
+                               "achieved": round(lt, 1), "peak": proof["peak"], "unit": "TFLOP/s",
+                               "frac": round(lt / proof["peak"], 4)},
+            "stage_us": stage_us(prefill["stage_ms"]),
+            "distinct_experts_per_layer_mean": float(np.mean(pn)),
+            "e2e": {"value": round(ps.T * layers * world / prefill["e2e_s"], 1), "unit": "layer-tokens/s",
+                    "h2d_bytes_per_step": prefill["stack"].h2d_bytes(),
+                    "d2h_bytes_per_step": prefill["stack"].d2h_bytes()},
+            "gpu_launches": int(launches_per_layer("grouped", ps) * layers * prefill["steps"]),
+            "clocks": prefill["clocks"],
+            "l2": "weights 16.3 GB and activations > L2, no flush",
+        }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_rate(shape, recipe, args, 0, args.cpu_sample_seconds)
+        if prefill is not None:
+            line["prefill"]["cpu_baseline"] = oracle_rate(prefill["shape"], prefill["recipe"],
+                                                          argparse.Namespace(**{**vars(args), "workload": "prefill"}),
+                                                          0, args.cpu_sample_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

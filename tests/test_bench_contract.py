@@ -27,6 +27,10 @@ def test_reference_arm_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["config"]["workload"].startswith("decode: 48 QMoE layers H=2048 inter=768 E=128 k=8 INT4 b32")
+    assert d["config"]["passes"] == 12
+    # the prefill half of the metric: the oracle on a sample of the 8K prefill tokens
+    pf = d["prefill"]
+    assert pf["value"] > 0 and pf["cpu_baseline"]["kind"] == "oracle" and "prefill tokens" in pf["cpu_baseline"]["sample"]
 
 
 def test_reference_arm_rejects_options():
@@ -40,7 +44,10 @@ def test_workload_config_names_options():
     import synthetic
 
     shape, _, _ = synthetic.decode_layer(8)
-    base = bench.workload_config(SimpleNamespace(workload="decode", options=False), shape, 48, 1)
-    opt = bench.workload_config(SimpleNamespace(workload="decode", options=True), shape, 48, 1)
+    base = bench.workload_config(SimpleNamespace(workload="decode", options=False, passes=12), shape, 48, 1)
+    opt = bench.workload_config(SimpleNamespace(workload="decode", options=True, passes=12), shape, 48, 1)
     assert "options" not in base and "biases" in opt["options"]
     assert base["parallelism"] == "replicas x1" and base["T"] == 8 and base["layers"] == 48
+    assert base["passes"] == 12 and "12 passes" in base["step"]
+    one = bench.workload_config(SimpleNamespace(workload="prefill", options=False, passes=12), shape, 1, 1)
+    assert one["passes"] == 1
