@@ -46,10 +46,16 @@
  * Precision. Routing compares raw logits exactly; weights use FP32 expf. The
  * expert matmuls run on tensor cores with FP16 operands and FP32 accumulation:
  * dequantised weights (code - zp) * scale are exact in FP16 for BF16 scales in
- * [2^-14, 2^12] and round once for FP16 scales; each token's activations are
- * scaled by a power of two so that their largest magnitude lies in [1, 2)
- * before the FP16 conversion, and the SwiGLU output is stored in FP16 with the
- * square of that power of two. The combine sums in FP32 and rounds once.
+ * [2^-17, 2^12] (where FP16 scales apply after the MMA, in FP32, any finite
+ * scale) and round once for FP16 scales; each token's activations are scaled
+ * by a power of two so that their largest magnitude lies in [1, 2) before the
+ * FP16 conversion, and the SwiGLU output is stored in FP16 times the square of
+ * that power of two and times a power of two set by the expert's first fc1
+ * block scale, so that its magnitude does not move with the scale range of the
+ * model (parity is tested with BF16 scales from 2^-15 to 2^12, activations with
+ * +-1e4 outliers and SwiGLU outputs beyond the FP16 range; an expert whose
+ * scales span more than about 2^12 can still leave that range). The combine
+ * sums in FP32 and rounds once.
  *
  * Threading and ordering. Every call only enqueues kernels on `stream` (a
  * cudaStream_t; NULL is the legacy default stream) and returns; it never

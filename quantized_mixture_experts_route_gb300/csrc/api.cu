@@ -143,6 +143,7 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
     ip.b1 = static_cast<const uint16_t*>(opt->fc1_bias);
     ip.b2 = static_cast<const uint16_t*>(opt->fc2_bias);
   }
+  ip.s1 = static_cast<const uint16_t*>(fc1_scales);
   const bool grouped = ip.path == QMOE_PATH_GROUPED;
   Workspace ws;
   if (workspace_layout(ip, grouped, workspace, &ws) > workspace_bytes)

@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
                 const float inv = 1.0f / sigma;
                 const int j = (r & 2) ? j_hi : j_lo;
                 const float2 bj = fc1_bias_pair(p, cur.e, j);
-                const float h = silu(tot[r] * inv + bj.x) * (up[r] * inv + bj.y) * sigma * sigma;
+                const float h = silu(tot[r] * inv + bj.x) * (up[r] * inv + bj.y) * (sigma * sigma * h_norm(p, cur.e));
                 ws.h16[(int64_t)(begin + n) * p.I + permuted_pos(j, G)] = __half_as_ushort(__float2half_rn(h));
               }
             }
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
               const int rid = ws.sorted_route[begin + n];
               const float inv = 1.0f / ws.tok_scale[rid / p.k];
               const int row = row0 + g + ((r & 2) ? 8 : 0);
-              ws.y[(int64_t)rid * p.H + row] = tot[r] * inv * inv * ws.topk_w[rid];
+              ws.y[(int64_t)rid * p.H + row] = tot[r] * (inv * inv / h_norm(p, cur.e)) * ws.topk_w[rid];
             }
           }
         }
@@ -727,14 +727,15 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
           const float sigma = ws.tok_scale[n ? tok1 : tok0];
           const float inv = 1.0f / sigma;
           const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+          const int ex = __ldg(ws.dtab + (item / rgroups) * kDtabInts);
           float2 b_lo = make_float2(0.0f, 0.0f), b_hi = b_lo;
           if (p.b1) {
-            const int ex = __ldg(ws.dtab + (item / rgroups) * kDtabInts);
             b_lo = fc1_bias_pair(p, ex, j_lo);
             b_hi = fc1_bias_pair(p, ex, j_hi);
           }
-          const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * sigma * sigma;
-          const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * sigma * sigma;
+          const float hs = sigma * sigma * h_norm(p, ex);
+          const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
+          const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
           // fc2 reads these as activations: odd K positions carry 1/16
           ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
               __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
@@ -745,7 +746,8 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
         if ((c & 1) == 0 && n < cnt) {
           const int rid = ws.sorted_route[pos0 + n];
           const float inv = 1.0f / ws.tok_scale[rid / p.k];
-          const float fct = inv * inv * ws.topk_w[rid];
+          const int ex = __ldg(ws.dtab + (item / rgroups) * kDtabInts);
+          const float fct = inv * inv / h_norm(p, ex) * ws.topk_w[rid];
           ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * fct;
           ws.y[(int64_t)rid * p.H + row0 + g + 8] = v_hi * fct;
         }
@@ -1165,14 +1167,15 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
           const float sigma = e_scale;
           const float inv = 1.0f / sigma;
           const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+          const int ex = __ldg(ws.dtab + ei * kDtabInts);
           float2 b_lo = make_float2(0.0f, 0.0f), b_hi = b_lo;
           if (p.b1) {
-            const int ex = __ldg(ws.dtab + ei * kDtabInts);
             b_lo = fc1_bias_pair(p, ex, j_lo);
             b_hi = fc1_bias_pair(p, ex, j_hi);
           }
-          const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * sigma * sigma;
-          const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * sigma * sigma;
+          const float hs = sigma * sigma * h_norm(p, ex);
+          const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
+          const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
           // fc2 reads these as activations: odd K positions carry 1/16
           ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 8)] =
               __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
@@ -1182,7 +1185,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       } else {
         if ((c & 1) == 0 && n < cnt) {
           const float inv = 1.0f / e_scale;
-          const float fct = inv * inv * e_w;
+          const float fct = inv * inv / h_norm(p, __ldg(ws.dtab + ei * kDtabInts)) * e_w;
           ws.y[(int64_t)e_rid * p.H + row0 + g] = v_lo * fct;
           ws.y[(int64_t)e_rid * p.H + row0 + g + 8] = v_hi * fct;
         }

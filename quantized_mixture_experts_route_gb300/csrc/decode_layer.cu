@@ -455,8 +455,9 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
             b_lo = fc1_bias_pair(p, ex, j_lo);
             b_hi = fc1_bias_pair(p, ex, j_hi);
           }
-          const float h_lo = silu(v[rh][0] * inv + b_lo.x) * (up_lo * inv + b_lo.y) * sigma * sigma;
-          const float h_hi = silu(v[rh][1] * inv + b_hi.x) * (up_hi * inv + b_hi.y) * sigma * sigma;
+          const float hs = sigma * sigma * h_norm(p, ex);
+          const float h_lo = silu(v[rh][0] * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
+          const float h_hi = silu(v[rh][1] * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
           // fc2 reads these as activations: K-order permuted, odd K positions carry 1/16
           const int pj0 = (j_lo & ~7) + ((j_lo & 7) < 4 ? 2 * (j_lo & 7) : 2 * (j_lo & 7) - 7);
           const int pj1 = (j_hi & ~7) + ((j_hi & 7) < 4 ? 2 * (j_hi & 7) : 2 * (j_hi & 7) - 7);
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
       if (lane == 0) red_add_release(fc1_done + ei, 1);
     } else {
       const float inv = 1.0f / e_scale;
-      const float fct = inv * inv * e_w;
+      const float fct = inv * inv / h_norm(p, ex) * e_w;
       if ((c & 1) == 0 && n < cnt) {
 #pragma unroll
         for (int rh = 0; rh < 2; ++rh) {

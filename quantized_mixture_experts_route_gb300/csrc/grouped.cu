@@ -693,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase =
           tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * 2 * C::BN + half * C::BN);
       const float inv = 1.0f / sigma;
+      const float hn = h_norm(p, e);
       for (int c0 = 32 * cpart; c0 < C::BN; c0 += 32 * (kEpiWarps / 4)) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)c0, v);
@@ -701,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // columns are W1 rows n0 + c0 .. +31: gate/up pairs -> 16 outputs h_j
           const int j0 = (n0 + c0) / 2;
           constexpr int G = BITS == 4 ? 8 : 16;
-          const float ss = sigma * sigma;
+          const float ss = sigma * sigma * hn;
           uint16_t hv[16];
           // SwiGLU with CUDA's fast exp and divide; the result is rounded to FP16
           if (p.b1) {
@@ -730,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        ov[8] | ((uint32_t)ov[9] << 16), ov[10] | ((uint32_t)ov[11] << 16),
                        ov[12] | ((uint32_t)ov[13] << 16), ov[14] | ((uint32_t)ov[15] << 16));
         } else {
-          const float f = inv * inv * wr;
+          const float f = inv * inv / hn * wr;
           float* dst = ws.y + (int64_t)rid * p.H + n0 + c0;
 #pragma unroll
           for (int q = 0; q < 4; ++q)

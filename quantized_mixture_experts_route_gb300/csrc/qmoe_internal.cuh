@@ -64,6 +64,7 @@ struct Problem {
   int full_softmax;               // routing weights under the softmax over all E logits
   const uint16_t* b1;             // [E][2I] fc1 bias in dtype, or null
   const uint16_t* b2;             // [E][H]  fc2 bias in dtype, or null
+  const uint16_t* s1;             // fc1 block scales [E][2I][H/block] in dtype (read by h_norm)
   __host__ __device__ int64_t R() const { return T * (int64_t)k; }
 };
 
@@ -145,6 +146,28 @@ __device__ __forceinline__ float2 fc1_bias_pair(const Problem& p, int e, int j) 
   const uint32_t v = __ldg(reinterpret_cast<const unsigned int*>(p.b1 + ((int64_t)e * p.I + j) * 2));
   return make_float2(half_bits_to_float((uint16_t)(v & 0xFFFFu), p.dtype),
                      half_bits_to_float((uint16_t)(v >> 16), p.dtype));
+}
+
+// The SwiGLU output h is stored in FP16 as h * sigma_t^2 * rho_e (sigma_t: the
+// token's activation scale) and the fc2 epilogue divides by the same product.
+// h grows with the square of the fc1 weights, so rho_e is the power of two
+// 2^(-2 (E + 7)) with 2^E <= |s| < 2^(E+1) for the expert's first fc1 block
+// scale s: the stored values keep the magnitude that block scales near 2^-7
+// give, whatever the scale range of the model (BF16 scales from 2^-40 to 2^40
+// keep the FP16 intermediate inside its normal range as long as an expert's
+// scales stay within about 2^6 of its first one). A zero, subnormal, infinite
+// or NaN first scale gives rho_e = 1. With an fc1 bias, h also holds the
+// bias's own contribution, so rho_e is capped at 1 there. rho_e is a power of
+// two: the scaling is exact.
+__device__ __forceinline__ float h_norm(const Problem& p, int e) {
+  if (!p.s1) return 1.0f;
+  const uint16_t b = __ldg(p.s1 + (int64_t)e * (2 * p.I) * (p.H / p.block));
+  const float s = fabsf(half_bits_to_float(b, p.dtype));
+  if (!(s >= 1.17549435e-38f) || s > 3.0e38f) return 1.0f;  // zero, subnormal, inf, NaN
+  int ex = (int)((__float_as_uint(s) >> 23) & 0xFF) - 127;   // floor(log2 s)
+  ex = min(max(ex, -40), 40);
+  const float rho = ldexpf(1.0f, -2 * (ex + 7));
+  return p.b1 ? fminf(rho, 1.0f) : rho;
 }
 
 // Round to nearest even; NaN stays NaN (the CUDA conversion intrinsics).
