@@ -68,6 +68,9 @@ def parse():
     ap.add_argument("--decode-layer-kernel", action="store_true",
                     help="decode: qmoe_forward_ex with the decode layer kernel (fc1 and fc2 in one "
                          "persistent kernel) instead of one kernel per stage")
+    ap.add_argument("--path", choices=["auto", "decode", "grouped"], default="auto",
+                    help="kernel path of every call (auto: decode for T <= 8 and for mid-size batches "
+                         "with few routes per expert, grouped otherwise)")
     ap.add_argument("--clock-log", default=None,
                     help="CSV file for the nvidia-smi clock samples (default: a file in the temp directory)")
     return ap.parse_args()
@@ -92,7 +95,8 @@ def workload_config(args, shape, layers, world):
             "l2": "weights 16.3 GB >> L2, no flush" if args.workload == "decode" else "inputs > L2 per step",
             **({"options": "fc1/fc2 biases N(0, 0.5), full-softmax routing weights"}
                if getattr(args, "options", False) else {}),
-            **({"decode_layer_kernel": 1} if getattr(args, "decode_layer_kernel", False) else {})}
+            **({"decode_layer_kernel": 1} if getattr(args, "decode_layer_kernel", False) else {}),
+            **({"path": args.path} if getattr(args, "path", "auto") != "auto" else {})}
 
 
 def reduce_max(v, device):
@@ -353,8 +357,15 @@ def kernel_traffic(key):
     return int(ent["dram_bytes_per_launch"]) if h.hexdigest() == ent["source_sha256"] else None
 
 
-def p_path(shape):
-    return "decode" if shape.T <= 8 else "grouped"
+def p_path(shape, forced="auto"):
+    """The kernel path of a call (csrc/api.cu, resolve_path)."""
+    if forced != "auto":
+        return forced
+    R = shape.T * shape.k
+    if shape.T <= 8:
+        return "decode"
+    few = R < 64 or R < 4 * shape.E
+    return "decode" if few and shape.T <= 64 and R <= 512 else "grouped"
 
 
 def launches_per_layer(path, shape, layer_kernel=False):
@@ -372,7 +383,7 @@ class Stack:
     (call 0 on x) with its own router logits. Inputs are copied from pinned host
     memory; the calls are captured in CUDA graphs."""
 
-    def __init__(self, qm, shape, W, x_h, logits_h, passes, device, options=None):
+    def __init__(self, qm, shape, W, x_h, logits_h, passes, device, options=None, path=0):
         import torch
 
         self.qm, self.shape, self.W, self.options = qm, shape, W, options
@@ -380,7 +391,7 @@ class Stack:
         self.calls = passes * self.layers
         assert logits_h.shape[0] == self.calls
         self.p = qm.problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
-                            shape.dtype, qm.QMOE_PATH_AUTO)
+                            shape.dtype, path)
         self.x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
         self.lg_pin = torch.from_numpy(logits_h.view(np.int16)).pin_memory()
         self.x_d = self.x_pin.to(device)
@@ -572,7 +583,8 @@ def run_ours(args):
         options = dict(full_softmax=1, b1=B1, b2=B2, layer_kernel=0)
     if args.decode_layer_kernel:
         options = dict(options or dict(full_softmax=0, b1=None, b2=None), layer_kernel=1)
-    stack = Stack(qm, shape, W, x_h, logits_h, passes, device, options)
+    path = {"auto": qm.QMOE_PATH_AUTO, "decode": qm.QMOE_PATH_DECODE, "grouped": qm.QMOE_PATH_GROUPED}[args.path]
+    stack = Stack(qm, shape, W, x_h, logits_h, passes, device, options, path)
     s = torch.cuda.Stream(device)
     torch.cuda.synchronize()
     g = stack.capture(s)
@@ -617,7 +629,7 @@ def run_ours(args):
     # the captured kernels' workloads (traffic figures hold for the plain call only)
     default_kernel = args.workload in ("decode", "prefill") and not args.options and not args.decode_layer_kernel
     nact = distinct_experts(logits_h, shape.dtype, shape.k)
-    if shape.T <= 8:
+    if p_path(shape, args.path) == "decode":
         # the single-stage graphs run on the routing of the last call
         bytes_fc1 = float(nact[-1]) * fc1_b
         hbm = peaks.get("hbm_gbs")
@@ -664,7 +676,7 @@ def run_ours(args):
         "stage_us": stage_us(stage_ms),
         "e2e": {"value": round(shape.T * layers * passes * world / e2e_s, 1), "unit": "layer-tokens/s",
                 "h2d_bytes_per_step": stack.h2d_bytes(), "d2h_bytes_per_step": stack.d2h_bytes()},
-        "gpu_launches": int(launches_per_layer(p_path(shape), shape, args.decode_layer_kernel) * layers * passes
+        "gpu_launches": int(launches_per_layer(p_path(shape, args.path), shape, args.decode_layer_kernel) * layers * passes
                             * args.steps),
         "clocks": clocks,
         **extra,

@@ -18,10 +18,18 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
+}  // namespace
+
 int resolve_path(const qmoe_problem& p) {
-  if (p.path == QMOE_PATH_AUTO) return p.T <= kDecodeMaxT ? QMOE_PATH_DECODE : QMOE_PATH_GROUPED;
-  return p.path;
+  if (p.path != QMOE_PATH_AUTO) return p.path;
+  const int64_t R = p.T * (int64_t)p.top_k;
+  if (p.T <= 8) return QMOE_PATH_DECODE;
+  // mid-size batches: the decode path while the routes are few per expert
+  const bool few = R < 64 || R < 4 * (int64_t)p.num_experts;
+  return (few && p.T <= kDecodeMaxT && R <= kPermuteChunk) ? QMOE_PATH_DECODE : QMOE_PATH_GROUPED;
 }
+
+namespace {
 
 // Shape and attribute checks shared by every entry point.
 qmoe_status check_problem(const qmoe_problem* p) {
@@ -39,7 +47,7 @@ qmoe_status check_problem(const qmoe_problem* p) {
   if ((int64_t)p->T * p->top_k > (int64_t)INT32_MAX / 2) return QMOE_ERR_UNSUPPORTED;
   const int path = resolve_path(*p);
   if (path == QMOE_PATH_DECODE) {
-    if (p->T > kDecodeMaxT) return QMOE_ERR_UNSUPPORTED;
+    if (p->T > kDecodeMaxT || p->T * (int64_t)p->top_k > kPermuteChunk) return QMOE_ERR_UNSUPPORTED;
     if (p->hidden > 8192 || p->inter > 8192) return QMOE_ERR_UNSUPPORTED;
   } else {
     const int m = p->bits == 3 ? 128 : 64;
@@ -80,7 +88,7 @@ size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* w
   w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * p.T * p.H));
   w.offsets = static_cast<int32_t*>(take(sizeof(int32_t) * (p.E + 1)));
   w.sorted_route = static_cast<int32_t*>(take(sizeof(int32_t) * R));
-  w.active = static_cast<int32_t*>(take(sizeof(int32_t) * p.E));
+  w.active = static_cast<int32_t*>(take(sizeof(int32_t) * (p.E + kPermuteChunk / kDecodeChunk)));
   w.counters = static_cast<int32_t*>(take(sizeof(int32_t) * 4));
   w.max_tiles = (R + kTileM - 1) / kTileM + p.E;
   w.tiles = static_cast<int32_t*>(take(sizeof(int32_t) * 2 * w.max_tiles));

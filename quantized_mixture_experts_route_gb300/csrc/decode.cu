@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   const int K = a.K, N = a.N;
   const int nq = (K + kChunkK - 1) / kChunkK;
   const int rgroups = N / kRowsPerGroup;
-  const int items = ws.counters[0] * rgroups;   // (active expert, 16-row group) pairs
+  const int items = ws.counters[0] * rgroups;   // (expert's chunk of <= 8 routes, 16-row group) pairs
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -235,9 +235,12 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   auto meta_of = [&](int it) {
     ItemMeta m{0, 0, 0, 0};
     if (it < items) {
-      m.e = ws.active[it / rgroups];
-      m.begin = ws.offsets[m.e];
-      m.n_e = ws.offsets[m.e + 1] - m.begin;
+      // the chunks of one expert are consecutive, so the items that read the same
+      // weight rows run at about the same time and the repeats hit L2
+      const int a = ws.active[it / rgroups];
+      m.e = a & 0xFFFF;
+      m.begin = ws.offsets[m.e] + (a >> 16) * kDecodeChunk;
+      m.n_e = min(kDecodeChunk, ws.offsets[m.e + 1] - m.begin);
       m.tok = g < m.n_e ? ws.sorted_route[m.begin + g] / p.k : 0;
     }
     return m;

@@ -66,7 +66,7 @@ extern "C" qmoe_status qmoe_forward_decode_static(const qmoe_problem* p, const v
   if (need == 0 || p->T == 0)
     return qmoe_forward(p, x, router_logits, fc1_q, fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp,
                         out, nullptr, 0, stream);
-  const bool decode = p->path == QMOE_PATH_DECODE || (p->path == QMOE_PATH_AUTO && p->T <= kDecodeMaxT);
+  const bool decode = resolve_path(*p) == QMOE_PATH_DECODE;
   if (!decode) return QMOE_ERR_UNSUPPORTED;
   if (need > QMOE_STATIC_WORKSPACE_BYTES) return QMOE_ERR_WORKSPACE_TOO_SMALL;
 

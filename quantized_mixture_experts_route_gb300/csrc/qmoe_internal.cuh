@@ -17,11 +17,18 @@ namespace qmoe {
 
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
-constexpr int kDecodeMaxT = 8;        // decode GEMV: at most 8 routes per expert (one MMA N-fragment)
 constexpr int kPermuteChunk = 512;    // routes per block in the grouping kernels
+// The decode path (expert weights streamed once, the routes of an expert on the
+// MMA's N side) takes batches of up to 64 tokens and kPermuteChunk routes: the
+// one-block routing kernel groups them and builds the decode table. AUTO picks
+// it for T <= 8 and, above that, while the routes number fewer than 4 per
+// expert (below 64 routes in all, always): the pages switch from their
+// tensor-core GEMV to the grouped GEMM at num_r >= 64 && num_r >= 4 E.
+constexpr int kDecodeMaxT = 64;
+constexpr int kDecodeChunk = 8;       // routes of one expert per MMA N-fragment (generic decode kernel)
 constexpr int kTileM = 256;           // rows (routes) per grouped-GEMM tile
 constexpr int kDtabInts = 8;          // ints per decode-table entry
-constexpr int kDtabMax = kDecodeMaxT * kMaxTopK;  // entries: at most one per route
+constexpr int kDtabMax = kPermuteChunk;  // entries: at most one per route
 
 // ---------------------------------------------------------------------------
 // Workspace: every scratch buffer of one forward call, carved from the
@@ -34,8 +41,11 @@ struct Workspace {
   uint16_t* x16;          // [T][H]   FP16 bits of x_t * tok_scale[t], K-order permuted
   int32_t* offsets;       // [E+1]    exclusive prefix of per-expert route counts
   int32_t* sorted_route;  // [R]      route ids grouped by expert, stable
-  int32_t* active;        // [E]      experts with at least one route, ascending
-  int32_t* counters;      // [4]      [0] active experts, [1] grouped tiles, [2] error flag,
+  int32_t* active;        // [E + R/8] experts with at least one route, ascending; on the
+                          //   decode path one word per (expert, chunk of up to 8 of its
+                          //   routes): expert | chunk << 16
+  int32_t* counters;      // [4]      [0] active experts (decode path: chunks), [1] grouped
+                          //   tiles, [2] error flag,
                           //          [3] decode-table entries
   int32_t* tiles;         // [2*max_tiles] (expert, first sorted row) of each kTileM-row tile
   int32_t* chunk_hist;    // [nchunks][E] per-chunk expert counts, then chunk bases
@@ -67,6 +77,9 @@ struct Problem {
   const uint16_t* s1;             // fc1 block scales [E][2I][H/block] in dtype (read by h_norm)
   __host__ __device__ int64_t R() const { return T * (int64_t)k; }
 };
+
+// The path a problem runs on (QMOE_PATH_DECODE or QMOE_PATH_GROUPED; AUTO resolved).
+int resolve_path(const qmoe_problem& p);
 
 // Decode work units (decode-table entries x 16-row groups of the larger matmul)
 // and split-K work items the workspace is sized for.

@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   __shared__ int s_idx[kPermuteChunk];
   __shared__ float s_w[kPermuteChunk];
   __shared__ int s_sorted[kPermuteChunk];
-  __shared__ int s_act[kMaxExperts];
+  __shared__ int s_act[kMaxExperts + kPermuteChunk / kDecodeChunk];
   const int warps = blockDim.x >> 5;
   const int R = (int)p.R();
   const int e = threadIdx.x;
@@ -415,19 +415,23 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   __syncthreads();
   int R_total, n_active, n_tiles = 0;
   const int off = block_exclusive_scan(total, sh, &R_total);
-  const int apos = block_exclusive_scan(total > 0 ? 1 : 0, sh, &n_active);
+  // active list: on the decode path one word per (expert, chunk of up to
+  // kDecodeChunk of its routes), expert | chunk << 16, so that the generic decode
+  // kernel puts each chunk on one MMA N-fragment; otherwise one per expert
+  const bool dec = p.path == QMOE_PATH_DECODE;  // (block-uniform) R <= kDtabMax on this path
+  const int n_act_e = dec ? (total + kDecodeChunk - 1) / kDecodeChunk : (total > 0 ? 1 : 0);
+  const int apos = block_exclusive_scan(n_act_e, sh, &n_active);
   const int nt = (total + kTileM - 1) / kTileM;
   const int tpos = want_tiles ? block_exclusive_scan(nt, sh, &n_tiles) : 0;
   if (e < p.E) {
     hist[e] = off;                   // scatter bases
-    if (total > 0) s_act[apos] = e;
+    for (int i = 0; i < n_act_e; ++i) s_act[apos + i] = e | (i << 16);
   }
   __syncthreads();
   scatter_routes(s_idx, 0, R, p.E, hist, warp_cnt, s_sorted);   // ends with a block barrier
   // decode table: one entry per (active expert, pair of its routes), in expert
   // order, so that a decode work unit reaches its expert's rows and its tokens
   // with one independent load and always multiplies exactly one MMA column pair
-  const bool dec = p.path == QMOE_PATH_DECODE;  // (block-uniform) R <= kDtabMax on this path
   int n_entries = 0;
   if (dec) {
     const int first = block_exclusive_scan((total + 1) / 2, sh, &n_entries);

@@ -78,9 +78,10 @@ BAD = [
     (dict(num_experts=64, top_k=33), qm.QMOE_ERR_UNSUPPORTED),
     (dict(dtype=2), qm.QMOE_ERR_UNSUPPORTED),
     (dict(path=3), qm.QMOE_ERR_UNSUPPORTED),
-    (dict(path=qm.QMOE_PATH_DECODE, T=9), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=qm.QMOE_PATH_DECODE, T=65), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=qm.QMOE_PATH_DECODE, T=64, top_k=16), qm.QMOE_ERR_UNSUPPORTED),   # 1024 routes
     (dict(path=qm.QMOE_PATH_GROUPED, bits=3, block_size=64, hidden=2048, inter=704), qm.QMOE_ERR_UNSUPPORTED),
-    (dict(T=9, hidden=96, inter=64), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(T=64, hidden=96, inter=64), qm.QMOE_ERR_UNSUPPORTED),   # grouped path: multiples of 64
 ]
 
 FAKE = 1 << 20  # an aligned address that is never dereferenced: every call below fails its checks first
@@ -156,6 +157,28 @@ def test_options_struct_matches_the_header():
     body = re.search(r"typedef struct \{([^}]*)\} qmoe_options;", hdr).group(1)
     names = re.findall(r"(\w+);", body)
     assert names == [f[0] for f in qm.qmoe_options._fields_]
+
+
+@pytest.mark.parametrize("kw,path", [
+    (dict(T=8), "decode"),
+    (dict(T=16), "decode"),                            # 128 routes < 4 E = 512
+    (dict(T=63), "decode"),                            # 504 routes
+    (dict(T=64), "grouped"),                           # 512 routes = 4 E: the pages' switch
+    (dict(T=9, num_experts=4, top_k=2), "decode"),     # 18 routes < 64
+    (dict(T=40, num_experts=8, top_k=2), "grouped"),   # 80 routes >= 64 and >= 4 E
+    (dict(T=64, num_experts=512, top_k=8), "decode"),  # 512 routes < 4 E
+    (dict(T=48, num_experts=512, top_k=16), "grouped"),  # 768 routes: above one grouping block
+])
+def test_auto_path_follows_the_route_count(L, kw, path):
+    """AUTO takes the decode path for T <= 8 and, up to 64 tokens and 512 routes, while
+    the routes number fewer than 64 or fewer than 4 per expert; the path shows in the
+    workspace size (the grouped path adds the gathered activation rows)."""
+    auto = L.qmoe_workspace_bytes(ctypes.byref(P(**kw)))
+    want = L.qmoe_workspace_bytes(ctypes.byref(P(**kw, path=qm.QMOE_PATH_DECODE if path == "decode"
+                                                       else qm.QMOE_PATH_GROUPED)))
+    other = L.qmoe_workspace_bytes(ctypes.byref(P(**kw, path=qm.QMOE_PATH_GROUPED if path == "decode"
+                                                        else qm.QMOE_PATH_DECODE)))
+    assert auto == want > 0 and auto != other
 
 
 def test_empty_input_is_noop(L):
