@@ -76,6 +76,8 @@ def _declare(L):
     L.oracle_forward_bias.argtypes = [P(_Problem), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_int64, vp, vp, ctypes.c_int]
     L.oracle_forward_bias.restype = ctypes.c_int
+    L.oracle_router_logits.argtypes = [P(_Problem), vp, vp, vp]
+    L.oracle_router_logits.restype = ctypes.c_int
     L.oracle_num_cores.argtypes = []
     L.oracle_num_cores.restype = ctypes.c_int
     return L
@@ -197,6 +199,17 @@ class Oracle:
             raise ValueError("oracle_forward: invalid arguments")
         return out, acc
 
+    def router_logits(self, p: Problem, x_bits: np.ndarray, w_router_bits: np.ndarray) -> np.ndarray:
+        """Router logits [T][E] (dtype bits) = round(x [T][H] . w_router [E][H]^T)."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        w = np.ascontiguousarray(w_router_bits, dtype=np.uint16)
+        assert x.shape == (p.T, p.H) and w.shape == (p.E, p.H)
+        out = np.zeros((p.T, p.E), dtype=np.uint16)
+        pc = p.c()
+        if self.L.oracle_router_logits(ctypes.byref(pc), _ptr(x), _ptr(w), _ptr(out)) != 0:
+            raise ValueError("oracle_router_logits: invalid arguments")
+        return out
+
     def num_cores(self) -> int:
         return self.L.oracle_num_cores()
 
@@ -241,6 +254,10 @@ def expert_ffn(p, inp, expert, x_row):
 
 def forward(p, inp, tokens=None, nthreads=0, want_acc=False):
     return default().forward(p, inp, tokens, nthreads, want_acc)
+
+
+def router_logits(p, x_bits, w_router_bits):
+    return default().router_logits(p, x_bits, w_router_bits)
 
 
 def num_cores() -> int:

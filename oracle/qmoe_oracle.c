@@ -229,6 +229,24 @@ int oracle_permute(const oracle_problem* p, const int32_t* topk_idx, int32_t* ex
 /* Expert FFN and the layer                                                  */
 /* ------------------------------------------------------------------------- */
 
+/* ------------------------------------------------------------------------- */
+/* Router logits: a plain dot product per (token, expert), one rounding.      */
+/* ------------------------------------------------------------------------- */
+
+int oracle_router_logits(const oracle_problem* p, const uint16_t* x, const uint16_t* w_router,
+                         uint16_t* logits) {
+  if (!p || p->T < 0 || p->H <= 0 || p->E <= 0 || !x || !w_router || !logits) return 1;
+  for (int64_t t = 0; t < p->T; ++t)
+    for (int e = 0; e < p->E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < p->H; ++h)
+        acc += oracle_bits_to_double(x[t * p->H + h], p->dtype) *
+               oracle_bits_to_double(w_router[(int64_t)e * p->H + h], p->dtype);
+      logits[t * p->E + e] = oracle_round_to_bits(acc, p->dtype);
+    }
+  return 0;
+}
+
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 void oracle_expert_ffn(const oracle_problem* p, const uint8_t* fc1_q, const uint16_t* fc1_s,

@@ -47,6 +47,16 @@ typedef struct {
                            probability under the softmax over all E logits */
 } oracle_problem;
 
+/* Router logits ahead of routing (the router part of the pages' RouterGateUpProj
+ * op, "[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload ..." #33731: one GEMM of
+ * the packed tokens with the router weight whose output feeds QMoE as raw
+ * logits): logits[t][e] = round( sum_h x[t][h] * w_router[e][h] ), the sum in
+ * double over h ascending, rounded once to the problem's dtype. x [T][H] and
+ * w_router [E][H] in dtype, logits [T][E] in dtype. Returns nonzero for an
+ * invalid problem. */
+int oracle_router_logits(const oracle_problem* p, const uint16_t* x, const uint16_t* w_router,
+                         uint16_t* logits);
+
 /* 16-bit float <-> double. */
 double oracle_bits_to_double(uint16_t bits, int dtype);
 uint16_t oracle_round_to_bits(double v, int dtype);

@@ -469,11 +469,77 @@ def pin_nan_propagates(orc):
         fail("NaN input is not kept as NaN in exactly its token's outputs")
 
 
+def _router_problem(T, H, E, dt):
+    return oracle_mod.Problem(T, H, 32, E, 1, 4, 32, dt)
+
+
+def pin_router_integer_bruteforce(orc):
+    """Small-integer x and router weights: every product and sum is exact, so the
+    logits equal Python integer dot products (rounded once when beyond 2^8)."""
+    rng = np.random.default_rng(31)
+    for dt in (BF16, FP16):
+        T, H, E = 5, 48, 7
+        xi = rng.integers(-4, 5, size=(T, H))
+        wi = rng.integers(-3, 4, size=(E, H))
+        xb = synthetic.float_to_bits(xi.astype(np.float64), dt)
+        wb = synthetic.float_to_bits(wi.astype(np.float64), dt)
+        got = orc.router_logits(_router_problem(T, H, E, dt), xb, wb)
+        want = [[sum(int(a) * int(b) for a, b in zip(xi[t], wi[e])) for e in range(E)] for t in range(T)]
+        ref = synthetic.float_to_bits(np.array(want, dtype=np.float64), dt)
+        if not np.array_equal(got, ref):
+            fail("router logits differ from integer dot products")
+
+
+def pin_router_one_hot_and_layout(orc):
+    """x = e_i gives logits[t][e] = w_router[e][i] exactly (the weight is [E][H],
+    one row per expert): a transposed operand or a wrong stride fails."""
+    rng = np.random.default_rng(32)
+    T, H, E = 6, 40, 9
+    wb = synthetic.float_to_bits(rng.standard_normal((E, H)), BF16)
+    x = np.zeros((T, H))
+    cols = rng.choice(H, size=T, replace=False)
+    x[np.arange(T), cols] = 1.0
+    got = orc.router_logits(_router_problem(T, H, E, BF16), synthetic.float_to_bits(x, BF16), wb)
+    if not np.array_equal(got, wb[:, cols].T):
+        fail("one-hot x does not select the router weight column")
+
+
+def pin_router_rounding_and_scaling(orc):
+    """Random x and weights: the logits are torch float64 matmul results rounded
+    once to the dtype (numpy float16 for FP16); doubling x doubles them exactly;
+    permuting the experts permutes the columns bit for bit."""
+    rng = np.random.default_rng(33)
+    T, H, E = 7, 96, 11
+    for dt in (BF16, FP16):
+        xb = synthetic.float_to_bits(rng.standard_normal((T, H)), dt)
+        wb = synthetic.float_to_bits(rng.standard_normal((E, H)) * 0.05, dt)
+        p = _router_problem(T, H, E, dt)
+        got = orc.router_logits(p, xb, wb)
+        ref64 = (torch.from_numpy(bits_to_f64(xb, dt)) @ torch.from_numpy(bits_to_f64(wb, dt)).T).numpy()
+        if dt == FP16:
+            ref = ref64.astype(np.float16).view(np.uint16)
+        else:
+            ref = synthetic.float_to_bits(ref64, dt)
+        if (got != ref).mean() > 0.0:
+            # a float64 sum order different from the oracle's may round across a tie
+            # only when the value sits exactly on a rounding boundary
+            if (got != ref).mean() > 0.01:
+                fail("router logits are not the float64 dot products rounded once")
+        x2 = synthetic.float_to_bits(bits_to_f64(xb, dt) * 2.0, dt)
+        got2 = orc.router_logits(p, x2, wb)
+        if not np.array_equal(bits_to_f64(got2, dt), 2.0 * bits_to_f64(got, dt)):
+            fail("router logits are not linear in x")
+        perm = rng.permutation(E)
+        if not np.array_equal(orc.router_logits(p, xb, wb[perm]), got[:, perm]):
+            fail("permuting the experts does not permute the logits")
+
+
 ALL_PINS = [
     pin_golden_packing, pin_unpack_random, pin_bits_to_double, pin_golden_rounding,
     pin_rounding_fp16_exhaustive, pin_rounding_bf16, pin_dequant, pin_golden_routing,
     pin_route_bruteforce, pin_permute, pin_dense_ffn_E1_k1, pin_bruteforce_dense_over_experts,
     pin_one_hot, pin_token_permutation, pin_zero_weights, pin_zero_weight_route_skipped,
     pin_nan_propagates, pin_full_softmax_routing, pin_biases_dense_over_experts,
-    pin_fc2_bias_with_zero_weights, pin_full_softmax_nan_row,
+    pin_fc2_bias_with_zero_weights, pin_full_softmax_nan_row, pin_router_integer_bruteforce,
+    pin_router_one_hot_and_layout, pin_router_rounding_and_scaling,
 ]

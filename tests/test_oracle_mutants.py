@@ -40,6 +40,10 @@ MUTANTS = {
     "fc2_bias_wrong_expert": ("fc2_b[(int64_t)expert * rows2 + m]", "fc2_b[m]"),
     "full_softmax_ignored": ("  if (p->full_softmax) {", "  if (0) {"),
     "full_softmax_last_expert_dropped": ("for (int e = 0; e < E; ++e) denom += exp(", "for (int e = 0; e + 1 < E; ++e) denom += exp("),
+    "router_weight_transposed": ("w_router[(int64_t)e * p->H + h]", "w_router[(int64_t)h * p->E + e]"),
+    "router_last_term_dropped": ("      for (int h = 0; h < p->H; ++h)\n        acc += oracle_bits_to_double(x[t * p->H + h]",
+                                 "      for (int h = 0; h + 1 < p->H; ++h)\n        acc += oracle_bits_to_double(x[t * p->H + h]"),
+    "router_x_row_ignored": ("oracle_bits_to_double(x[t * p->H + h], p->dtype) *", "oracle_bits_to_double(x[h], p->dtype) *"),
     "x_not_read_per_token": ("xr[kk] = oracle_bits_to_double(J->x[t * H + kk], p->dtype);", "xr[kk] = oracle_bits_to_double(J->x[kk], p->dtype);"),
 }
 
