@@ -164,12 +164,19 @@ qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* route
  *   Both give results within the same error bound of the pages' definition;
  *   the layer kernel's result does not depend on the batch a token is packed
  *   into. Other values: QMOE_ERR_INVALID_ARGUMENT.
+ * router_weight: [E][hidden] in dtype, caller-owned device memory, 16-byte
+ *   aligned, or NULL. When set, the call first computes the router logits from
+ *   x (qmoe_router_logits, into the workspace) and routes on them; the
+ *   router_logits argument is then not read and may be NULL. The pages run this
+ *   GEMM ahead of QMoE as the router part of their RouterGateUpProj op
+ *   ("[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload ..." #33731).
  */
 typedef struct {
   int32_t full_softmax;
   const void* fc1_bias;
   const void* fc2_bias;
   int32_t decode_layer_kernel;
+  const void* router_weight;
 } qmoe_options;
 
 /*
@@ -215,6 +222,23 @@ qmoe_status qmoe_forward_stages(const qmoe_problem* p, int first_stage, int last
                                 const uint8_t* fc2_q, const void* fc2_scales,
                                 const uint8_t* fc2_zp, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Router logits ahead of routing: logits[t][e] = round( sum_h x[t][h] *
+ * router_weight[e][h] ), products and sums in FP32 on the tensor cores (BF16 or
+ * FP16 operands as given), each logit rounded once to the problem's dtype
+ * (nearest even, NaN kept). x [T][hidden], router_weight [E][hidden], logits
+ * [T][E], all in dtype, caller-owned device memory, 16-byte aligned. This is
+ * the router part of the pages' RouterGateUpProj op, which feeds QMoE its raw
+ * logits ("[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload ..." #33731); its
+ * gate/up projection belongs to layers outside QMoE and is not computed here.
+ * The FP32 sum may differ from an exact one by a unit in the last place of the
+ * rounded logit. Uses only the problem's T, hidden, num_experts and dtype (the
+ * whole problem is validated as for qmoe_forward). Errors: as qmoe_forward;
+ * T == 0 returns QMOE_OK with no launch. Asynchronous on `stream`.
+ */
+qmoe_status qmoe_router_logits(const qmoe_problem* p, const void* x, const void* router_weight,
+                               void* logits, void* stream);
 
 /*
  * Routing and grouping only (the first two steps of qmoe_forward), for

@@ -44,7 +44,7 @@ QMOE_PATH_GROUPED = 2
 # every symbol the header declares
 EXPORTED = ("qmoe_workspace_bytes", "qmoe_forward", "qmoe_forward_stages", "qmoe_route",
             "qmoe_status_string", "qmoe_forward_decode_static", "qmoe_forward_ex",
-            "qmoe_workspace_error_offset")
+            "qmoe_workspace_error_offset", "qmoe_router_logits")
 
 QMOE_STATIC_WORKSPACE_BYTES = 8 << 20
 
@@ -69,7 +69,7 @@ class qmoe_problem(ctypes.Structure):
 
 class qmoe_options(ctypes.Structure):
     _fields_ = [("full_softmax", ctypes.c_int32), ("fc1_bias", ctypes.c_void_p), ("fc2_bias", ctypes.c_void_p),
-                ("decode_layer_kernel", ctypes.c_int32)]
+                ("decode_layer_kernel", ctypes.c_int32), ("router_weight", ctypes.c_void_p)]
 
 
 def problem(T, hidden, inter, num_experts, top_k, bits, block_size, dtype, path=QMOE_PATH_AUTO):
@@ -104,6 +104,8 @@ def lib():
         L.qmoe_forward_ex.argtypes = [P, ctypes.POINTER(qmoe_options), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_size_t, vp]
         L.qmoe_forward_ex.restype = ctypes.c_int
+        L.qmoe_router_logits.argtypes = [P, vp, vp, vp, vp]
+        L.qmoe_router_logits.restype = ctypes.c_int
         L.qmoe_workspace_error_offset.argtypes = [P]
         L.qmoe_workspace_error_offset.restype = ctypes.c_size_t
         L.qmoe_status_string.argtypes = [ctypes.c_int]
@@ -166,8 +168,9 @@ def qmoe_forward(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, f
 
 def qmoe_forward_ex(p: qmoe_problem, full_softmax: int, fc1_bias, fc2_bias, x, router_logits, fc1_q,
                     fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, stream=None,
-                    decode_layer_kernel: int = 0) -> None:
-    opt = qmoe_options(int(full_softmax), _addr(fc1_bias), _addr(fc2_bias), int(decode_layer_kernel))
+                    decode_layer_kernel: int = 0, router_weight=None) -> None:
+    opt = qmoe_options(int(full_softmax), _addr(fc1_bias), _addr(fc2_bias), int(decode_layer_kernel),
+                       _addr(router_weight))
     st = lib().qmoe_forward_ex(ctypes.byref(p), ctypes.byref(opt), _addr(x), _addr(router_logits),
                                _addr(fc1_q), _addr(fc1_scales), _addr(fc1_zp), _addr(fc2_q),
                                _addr(fc2_scales), _addr(fc2_zp), _addr(out), _addr(workspace),
@@ -198,6 +201,14 @@ def qmoe_forward_stages(p: qmoe_problem, first_stage: int, last_stage: int, x, r
                                    _stream(stream))
     if st != QMOE_OK:
         raise QMoEError(st, "qmoe_forward_stages")
+
+
+def qmoe_router_logits(p: qmoe_problem, x, router_weight, logits, stream=None) -> None:
+    """Router logits [T][E] = x [T][H] . router_weight [E][H]^T, rounded once to the dtype."""
+    st = lib().qmoe_router_logits(ctypes.byref(p), _addr(x), _addr(router_weight), _addr(logits),
+                                  _stream(stream))
+    if st != QMOE_OK:
+        raise QMoEError(st, "qmoe_router_logits")
 
 
 def qmoe_route(p: qmoe_problem, router_logits, topk_idx, topk_w, expert_offsets, sorted_route,

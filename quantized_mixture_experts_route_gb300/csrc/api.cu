@@ -105,6 +105,7 @@ size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* w
   w.x16s = grouped ? static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.H)) : nullptr;
   w.h16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * R * p.I));
   w.y = static_cast<float*>(take(sizeof(float) * R * p.H));
+  w.rlogits = static_cast<uint16_t*>(take(sizeof(uint16_t) * p.T * p.E));
   if (ws) *ws = w;
   return off;
 }
@@ -137,6 +138,9 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
   if (opt && opt->full_softmax != 0 && opt->full_softmax != 1) return QMOE_ERR_INVALID_ARGUMENT;
   if (opt && opt->decode_layer_kernel != 0 && opt->decode_layer_kernel != 1) return QMOE_ERR_INVALID_ARGUMENT;
   if (p->T == 0) return QMOE_OK;
+  // with a router weight the logits are computed from x and the argument is not read
+  const void* w_router = opt ? opt->router_weight : nullptr;
+  if (w_router) router_logits = w_router;
   if (!x || !router_logits || !fc1_q || !fc1_scales || !fc2_q || !fc2_scales || !out || !workspace)
     return QMOE_ERR_INVALID_ARGUMENT;
   const void* ptrs[] = {x, router_logits, fc1_q, fc1_scales, fc2_q, fc2_scales, out, workspace};
@@ -160,7 +164,13 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
   auto in_range = [&](int stage) { return first_stage <= stage && stage <= last_stage; };
   cudaError_t err = cudaSuccess;
   if (in_range(QMOE_STAGE_ROUTE)) {
-    err = launch_route(ip, x, router_logits, ws,
+    if (w_router) {
+      err = launch_router_logits(ip, x, w_router, ws.rlogits, s);
+      router_logits = ws.rlogits;
+      ip.logits_after_wait = 1;
+    }
+    if (err == cudaSuccess)
+      err = launch_route(ip, x, router_logits, ws,
                        decode_int4_blockscaled(ip) ? kX16OddSixteenth : kX16Plain, s);
     if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
     if (err == cudaSuccess && grouped) err = launch_gather(ip, ws, s);
@@ -214,6 +224,18 @@ qmoe_status qmoe_forward_ex(const qmoe_problem* p, const qmoe_options* opt, cons
                             void* stream) {
   return forward_impl(p, opt, QMOE_STAGE_ROUTE, QMOE_STAGE_COMBINE, x, router_logits, fc1_q, fc1_scales,
                       fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, workspace_bytes, stream);
+}
+
+qmoe_status qmoe_router_logits(const qmoe_problem* p, const void* x, const void* router_weight, void* logits,
+                               void* stream) {
+  const qmoe_status st = check_problem(p);
+  if (st != QMOE_OK) return st;
+  if (p->T == 0) return QMOE_OK;
+  if (!x || !router_weight || !logits) return QMOE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(router_weight) || !aligned16(logits)) return QMOE_ERR_MISALIGNED;
+  const Problem ip = to_internal(*p);
+  const cudaError_t err = launch_router_logits(ip, x, router_weight, logits, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }
 
 qmoe_status qmoe_route(const qmoe_problem* p, const void* router_logits, int32_t* topk_idx,

@@ -56,6 +56,7 @@ struct Workspace {
   uint16_t* x16s;         // [R][H]   x16 rows gathered into sorted-route order (grouped)
   uint16_t* h16;          // [R][I]   SwiGLU output, FP16, sorted-route order, K-order permuted
   float* y;               // [R][H]   weighted fc2 output per route id (FP32)
+  uint16_t* rlogits;      // [T][E]   router logits computed from x (qmoe_options.router_weight)
   float* dsplit;           // decode split-K partials [work items][4][32] (FP32)
   int32_t* dticket;        // [decode units] arrival counters of the split-K partials
   int32_t* dsync;          // decode layer kernel: [0] unit claims, [kSyncHeader ..] fc1
@@ -75,6 +76,8 @@ struct Problem {
   const uint16_t* b1;             // [E][2I] fc1 bias in dtype, or null
   const uint16_t* b2;             // [E][H]  fc2 bias in dtype, or null
   const uint16_t* s1;             // fc1 block scales [E][2I][H/block] in dtype (read by h_norm)
+  int logits_after_wait;          // the router logits are the previous kernel's output: read
+                                  //   them only after pdl_wait()
   __host__ __device__ int64_t R() const { return T * (int64_t)k; }
 };
 
@@ -123,6 +126,9 @@ cudaError_t launch_decode(const Problem& p, bool fc1, const uint8_t* q, const vo
 cudaError_t launch_grouped(const Problem& p, bool fc1, const uint8_t* q, const void* scales,
                            const uint8_t* zp, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_combine(const Problem& p, const Workspace& ws, void* out, cudaStream_t s);
+// Router logits [T][E] = x [T][H] . w_router [E][H]^T, rounded once to the dtype (router.cu).
+cudaError_t launch_router_logits(const Problem& p, const void* x, const void* w_router, void* logits,
+                                 cudaStream_t s);
 // The decode layer's two expert matmuls (fc1 + SwiGLU, fc2) as one persistent
 // kernel (decode_layer.cu); applies to INT4 block 32 without zero points, H and
 // inter multiples of 256.

@@ -393,6 +393,8 @@ template <int PER_LANE>
 __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
     Problem p, const uint16_t* __restrict__ x, const uint16_t* __restrict__ logits, Workspace ws,
     int x16_mode, int want_tiles) {
+  // logits computed by the previous kernel (the router GEMM) are read after its end
+  if (p.logits_after_wait) pdl_wait();
   extern __shared__ int smem[];
   int* hist = smem;                  // [E]
   int* warp_cnt = smem + p.E;        // [16][E]

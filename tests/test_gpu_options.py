@@ -82,10 +82,10 @@ def test_empty_batch_with_options(L):
 
 
 def test_options_struct_layout():
-    # int32, two pointers, int32: offsets 0, 8, 16, 24 and 32 bytes in all on LP64 hosts
+    # int32, two pointers, int32, pointer: offsets 0, 8, 16, 24, 32 and 40 bytes in all on LP64 hosts
     assert qm.qmoe_options.fc1_bias.offset == 8 and qm.qmoe_options.fc2_bias.offset == 16
-    assert qm.qmoe_options.decode_layer_kernel.offset == 24
-    assert ctypes.sizeof(qm.qmoe_options) == 32
+    assert qm.qmoe_options.decode_layer_kernel.offset == 24 and qm.qmoe_options.router_weight.offset == 32
+    assert ctypes.sizeof(qm.qmoe_options) == 40
 
 
 @pytest.mark.gpu
