@@ -44,7 +44,8 @@ def build(force: bool = False) -> str:
 class _Problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("bits", ctypes.c_int32),
-                ("block", ctypes.c_int32), ("dtype", ctypes.c_int32), ("full_softmax", ctypes.c_int32)]
+                ("block", ctypes.c_int32), ("dtype", ctypes.c_int32), ("full_softmax", ctypes.c_int32),
+                ("format", ctypes.c_int32), ("g1", ctypes.c_void_p), ("g2", ctypes.c_void_p)]
 
 
 
@@ -76,6 +77,9 @@ def _declare(L):
     L.oracle_forward_bias.argtypes = [P(_Problem), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_int64, vp, vp, ctypes.c_int]
     L.oracle_forward_bias.restype = ctypes.c_int
+    for f in ("oracle_e2m1", "oracle_e8m0", "oracle_e4m3"):
+        getattr(L, f).argtypes = [ctypes.c_uint]
+        getattr(L, f).restype = ctypes.c_double
     L.oracle_router_logits.argtypes = [P(_Problem), vp, vp, vp]
     L.oracle_router_logits.restype = ctypes.c_int
     L.oracle_num_cores.argtypes = []
@@ -94,10 +98,14 @@ class Problem:
     block: int
     dtype: int
     full_softmax: int = 0   # 1: normalize_routing_weights = 0 (weights under the softmax over all E)
+    format: int = 0         # 0 integer codes, 1 MXFP4, 2 NVFP4 (see qmoe_oracle.h)
+    g1: np.ndarray | None = None   # NVFP4 per-expert FP32 global scales of fc1 / fc2, or None (1.0)
+    g2: np.ndarray | None = None
 
     def c(self) -> _Problem:
+        self._g = [None if g is None else np.ascontiguousarray(g, dtype=np.float32) for g in (self.g1, self.g2)]
         return _Problem(self.T, self.H, self.inter, self.E, self.k, self.bits, self.block, self.dtype,
-                        self.full_softmax)
+                        self.full_softmax, self.format, *[None if g is None else g.ctypes.data for g in self._g])
 
 
 def _ptr(a):
@@ -109,8 +117,10 @@ def _ptr(a):
 
 def _weights(inp):
     c = lambda a, dt: None if a is None else np.ascontiguousarray(a, dtype=dt)
-    return (c(inp["fc1_q"], np.uint8), c(inp["fc1_s"], np.uint16), c(inp.get("fc1_zp"), np.uint8),
-            c(inp["fc2_q"], np.uint8), c(inp["fc2_s"], np.uint16), c(inp.get("fc2_zp"), np.uint8))
+    # block scales: 16-bit floats of the dtype, or the FP4 formats' 8-bit scales (uint8 arrays)
+    sc = lambda a: np.ascontiguousarray(a, dtype=np.uint8 if np.asarray(a).dtype == np.uint8 else np.uint16)
+    return (c(inp["fc1_q"], np.uint8), sc(inp["fc1_s"]), c(inp.get("fc1_zp"), np.uint8),
+            c(inp["fc2_q"], np.uint8), sc(inp["fc2_s"]), c(inp.get("fc2_zp"), np.uint8))
 
 
 def _biases(inp):
@@ -210,6 +220,12 @@ class Oracle:
             raise ValueError("oracle_router_logits: invalid arguments")
         return out
 
+    def fp4_tables(self):
+        """(E2M1 values of the 16 codes, E8M0 values of the 256 bytes, E4M3 values of the 256 bytes)."""
+        return (np.array([self.L.oracle_e2m1(c) for c in range(16)]),
+                np.array([self.L.oracle_e8m0(b) for b in range(256)]),
+                np.array([self.L.oracle_e4m3(b) for b in range(256)]))
+
     def num_cores(self) -> int:
         return self.L.oracle_num_cores()
 
@@ -258,6 +274,10 @@ def forward(p, inp, tokens=None, nthreads=0, want_acc=False):
 
 def router_logits(p, x_bits, w_router_bits):
     return default().router_logits(p, x_bits, w_router_bits)
+
+
+def fp4_tables():
+    return default().fp4_tables()
 
 
 def num_cores() -> int:

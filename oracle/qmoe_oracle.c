@@ -136,6 +136,49 @@ void oracle_dequant_row(const uint8_t* q, const uint16_t* scales, const uint8_t*
 }
 
 /* ------------------------------------------------------------------------- */
+/* FP4 expert formats (see qmoe_oracle.h).                                   */
+/* ------------------------------------------------------------------------- */
+
+double oracle_e2m1(unsigned code) {
+  const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -v : v;
+}
+
+double oracle_e8m0(unsigned bits) {
+  bits &= 0xFF;
+  return bits == 0xFF ? NAN : ldexp(1.0, (int)bits - 127);
+}
+
+double oracle_e4m3(unsigned bits) {
+  bits &= 0xFF;
+  const int sign = bits >> 7, e = (bits >> 3) & 0xF, m = bits & 7;
+  if (e == 0xF && m == 7) return NAN;
+  const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* One weight row of an expert matrix in the problem's format: integer codes
+ * through oracle_dequant_row, FP4 codes times their block scale (and, NVFP4,
+ * the expert's global scale g; NULL means 1). */
+static void dequant_row_fmt(const oracle_problem* p, const uint8_t* q, const void* scales, const uint8_t* zp,
+                            const float* g, int expert, int K, int64_t row, double* out) {
+  if (p->format == ORACLE_INT) {
+    oracle_dequant_row(q, (const uint16_t*)scales, zp, p->bits, p->block, p->dtype, K, row, out);
+    return;
+  }
+  const uint8_t* qrow = q + row * ((int64_t)K / 2);
+  const uint8_t* s8 = (const uint8_t*)scales;
+  const int nblk = K / p->block;
+  const double gs = (p->format == ORACLE_NVFP4 && g) ? (double)g[expert] : 1.0;
+  for (int kk = 0; kk < K; ++kk) {
+    const unsigned sb = s8[row * nblk + kk / p->block];
+    const double s = p->format == ORACLE_MXFP4 ? oracle_e8m0(sb) : oracle_e4m3(sb);
+    out[kk] = oracle_e2m1(code_at(qrow, 4, kk)) * s * gs;
+  }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Routing                                                                   */
 /* ------------------------------------------------------------------------- */
 
@@ -191,6 +234,8 @@ static int valid_problem(const oracle_problem* p) {
   if (p->H % 8 || p->inter % 8) return 0;
   if (p->dtype != ORACLE_BF16 && p->dtype != ORACLE_FP16) return 0;
   if (p->full_softmax != 0 && p->full_softmax != 1) return 0;
+  if (p->format != ORACLE_INT && p->format != ORACLE_MXFP4 && p->format != ORACLE_NVFP4) return 0;
+  if (p->format != ORACLE_INT && p->bits != 4) return 0;
   return 1;
 }
 
@@ -266,8 +311,7 @@ void oracle_expert_ffn_bias(const oracle_problem* p, const uint8_t* fc1_q, const
   double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
   /* fc1: 2I rows of length H; row 2i is gate_i, row 2i+1 is up_i */
   for (int64_t n = 0; n < rows1; ++n) {
-    oracle_dequant_row(fc1_q, fc1_s, fc1_zp, p->bits, p->block, p->dtype, H,
-                       (int64_t)expert * rows1 + n, wrow);
+    dequant_row_fmt(p, fc1_q, fc1_s, fc1_zp, p->g1, expert, H, (int64_t)expert * rows1 + n, wrow);
     double acc = 0.0;
     for (int kk = 0; kk < H; ++kk) acc += wrow[kk] * x_row[kk];
     if (fc1_b) acc += oracle_bits_to_double(fc1_b[(int64_t)expert * rows1 + n], p->dtype);
@@ -276,8 +320,7 @@ void oracle_expert_ffn_bias(const oracle_problem* p, const uint8_t* fc1_q, const
   for (int i = 0; i < I; ++i) h[i] = silu(gu[2 * i]) * gu[2 * i + 1];
   /* fc2: H rows of length I */
   for (int64_t m = 0; m < rows2; ++m) {
-    oracle_dequant_row(fc2_q, fc2_s, fc2_zp, p->bits, p->block, p->dtype, I,
-                       (int64_t)expert * rows2 + m, wrow);
+    dequant_row_fmt(p, fc2_q, fc2_s, fc2_zp, p->g2, expert, I, (int64_t)expert * rows2 + m, wrow);
     double acc = 0.0;
     for (int i = 0; i < I; ++i) acc += wrow[i] * h[i];
     if (fc2_b) acc += oracle_bits_to_double(fc2_b[(int64_t)expert * rows2 + m], p->dtype);

@@ -45,7 +45,30 @@ typedef struct {
   int32_t full_softmax; /* 0: weights = softmax over the k selected logits (renormalised);
                            1: normalize_routing_weights = 0, each selected expert's
                            probability under the softmax over all E logits */
+  int32_t format;  /* ORACLE_INT: integer codes (code - zp) * scale, scales in dtype;
+                      ORACLE_MXFP4 / ORACLE_NVFP4: 4-bit E2M1 codes, 8-bit block scales
+                      [N][K/block] (E8M0, block 32 / E4M3, block 16), no zero point */
+  const float* g1; /* NVFP4: per-expert FP32 global scale of fc1 [E], or NULL (1.0) */
+  const float* g2; /* NVFP4: the same for fc2 */
 } oracle_problem;
+
+enum { ORACLE_INT = 0, ORACLE_MXFP4 = 1, ORACLE_NVFP4 = 2 };
+
+/* The FP4 expert formats ("NVFP4 block/global scale semantics", "Execution plan
+ * to offload export on CPU for a MoE" review; NVFP4 / MXFP4 QMoE weights in
+ * "[CUDA] Add INT4 and INT3 QMoE CPU/GPU offload support" #33575), from the
+ * published format definitions:
+ *   E2M1 element: sign bit 3, exponent bits 2-1 (bias 1), mantissa bit 0; an
+ *     exponent field of 0 is subnormal (mantissa * 0.5);
+ *   E8M0 scale (MXFP4, one per 32 elements): 2^(b - 127), b = 255 is NaN;
+ *   E4M3 scale (NVFP4, one per 16 elements): sign bit 7, exponent bits 6-3
+ *     (bias 7), mantissa bits 2-0, subnormal below, the all-ones pattern NaN,
+ *     no infinities; NVFP4 weights are also multiplied by an FP32 global scale
+ *     (here one per expert and matmul).
+ * w = element * block scale (* global scale). */
+double oracle_e2m1(unsigned code);
+double oracle_e8m0(unsigned bits);
+double oracle_e4m3(unsigned bits);
 
 /* Router logits ahead of routing (the router part of the pages' RouterGateUpProj
  * op, "[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload ..." #33731: one GEMM of

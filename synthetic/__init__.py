@@ -42,6 +42,7 @@ class Shape:
     bits: int
     block: int
     dtype: int
+    format: int = 0   # 0 integer codes, 1 MXFP4 (E8M0 scales, block 32), 2 NVFP4 (E4M3, block 16)
 
     def code_bytes_per_row(self, K: int) -> int:
         return K * self.bits // 8
@@ -124,11 +125,18 @@ def make_numpy(shape: Shape, recipe: Recipe, seed: int) -> dict:
         return rng.integers(0, 256, size=nbytes, dtype=np.uint8).reshape(E, rows // E, K * shape.bits // 8)
 
     def scales(rows: int, K: int) -> np.ndarray:
-        v = rng.uniform(recipe.scale_lo, recipe.scale_hi, size=(E, rows // E, K // shape.block))
+        size = (E, rows // E, K // shape.block)
+        if shape.format == 1:
+            # E8M0 bytes 118..122: block scales 2^-9 .. 2^-5
+            return rng.integers(118, 123, size=size, dtype=np.uint8)
+        if shape.format == 2:
+            # E4M3 bytes 0x18..0x3F: exponent fields 3..7 (2^-4 .. 2^0), any mantissa
+            return rng.integers(0x18, 0x40, size=size, dtype=np.uint8)
+        v = rng.uniform(recipe.scale_lo, recipe.scale_hi, size=size)
         return float_to_bits(v, dt)
 
     def zps(rows: int, K: int):
-        if not recipe.explicit_zp:
+        if not recipe.explicit_zp or shape.format != 0:
             return None
         return rng.integers(0, 1 << shape.bits, size=(E, rows // E, K // shape.block), dtype=np.uint8)
 
@@ -143,8 +151,13 @@ def make_numpy(shape: Shape, recipe: Recipe, seed: int) -> dict:
     if recipe.bias_std is not None:
         fc1_b = float_to_bits(rng.standard_normal((E, 2 * I)) * recipe.bias_std, dt)
         fc2_b = float_to_bits(rng.standard_normal((E, H)) * recipe.bias_std, dt)
-    return dict(x=x, logits=logits, fc1_q=fc1_q, fc1_s=fc1_s, fc1_zp=fc1_zp,
-                fc2_q=fc2_q, fc2_s=fc2_s, fc2_zp=fc2_zp, fc1_b=fc1_b, fc2_b=fc2_b)
+    out = dict(x=x, logits=logits, fc1_q=fc1_q, fc1_s=fc1_s, fc1_zp=fc1_zp,
+               fc2_q=fc2_q, fc2_s=fc2_s, fc2_zp=fc2_zp, fc1_b=fc1_b, fc2_b=fc2_b)
+    if shape.format == 2:
+        # NVFP4 per-expert FP32 global scales of fc1 and fc2, drawn last
+        out["g1"] = rng.uniform(0.25, 1.0, size=E).astype(np.float32)
+        out["g2"] = rng.uniform(0.25, 1.0, size=E).astype(np.float32)
+    return out
 
 
 def make_torch_weights(shape: Shape, recipe: Recipe, seed: int, device):

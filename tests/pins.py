@@ -534,6 +534,67 @@ def pin_router_rounding_and_scaling(orc):
             fail("permuting the experts does not permute the logits")
 
 
+def pin_fp4_element_and_scale_tables(orc):
+    """E2M1: the closed set {0, 0.5, 1, 1.5, 2, 3, 4, 6}, increasing in the code's
+    low three bits, bit 3 the sign; E4M3 against torch's float8_e4m3fn and E8M0
+    against float8_e8m0fnu, every byte (NaN where torch has NaN)."""
+    e2, e8, e4 = orc.fp4_tables()
+    if not np.array_equal(e2[:8], [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]):
+        fail("E2M1 magnitudes")
+    if not np.array_equal(e2[8:], -e2[:8]) or not np.signbit(e2[8]):
+        fail("E2M1 sign bit")
+    b = torch.arange(256, dtype=torch.uint8)
+    r4 = b.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    r8 = b.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    for got, ref, name in ((e4, r4, "E4M3"), (e8, r8, "E8M0")):
+        if not np.array_equal(np.isnan(got), np.isnan(ref)) or not np.array_equal(got[~np.isnan(ref)],
+                                                                               ref[~np.isnan(ref)]):
+            fail(f"{name} scale values")
+
+
+def _fp4_dense_expert(inp, shape, e, xrow):
+    """y of expert e from torch float64 with the weights decoded through torch's
+    float8 dtypes (scales) and the E2M1 set (elements)."""
+    e2m1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+    def mat(q, s8, rows, K, g):
+        codes = lsb_first_codes(q, 4, rows * K).reshape(rows, K)
+        sb = torch.from_numpy(np.ascontiguousarray(s8, dtype=np.uint8).reshape(rows, K // shape.block))
+        fdt = torch.float8_e8m0fnu if shape.format == 1 else torch.float8_e4m3fn
+        scale = np.repeat(sb.view(fdt).to(torch.float64).numpy(), shape.block, axis=1)
+        return torch.from_numpy(e2m1[codes] * scale * g)
+
+    H, I = shape.H, shape.inter
+    g1 = float(inp["g1"][e]) if shape.format == 2 else 1.0
+    g2 = float(inp["g2"][e]) if shape.format == 2 else 1.0
+    W1 = mat(inp["fc1_q"][e], inp["fc1_s"][e], 2 * I, H, g1)
+    W2 = mat(inp["fc2_q"][e], inp["fc2_s"][e], H, I, g2)
+    gu = W1 @ torch.from_numpy(xrow)
+    h = torch.nn.functional.silu(gu[0::2]) * gu[1::2]
+    return (W2 @ h).numpy()
+
+
+def pin_fp4_dense_over_experts(orc):
+    """MXFP4 and NVFP4 layers: the oracle's forward against every expert computed
+    densely in torch float64 from the format definitions and weighted by the
+    routing (brute force over experts), before the one rounding."""
+    for fmt in (1, 2):
+        shape = synthetic.Shape(T=3, H=64, inter=32, E=4, k=2, bits=4, block=32 if fmt == 1 else 16,
+                                dtype=BF16, format=fmt)
+        inp = synthetic.make_numpy(shape, synthetic.Recipe(logit_std=1.0), 40 + fmt)
+        p = oracle_mod.Problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
+                               shape.dtype, 0, fmt, inp.get("g1"), inp.get("g2"))
+        _, acc = orc.forward(p, inp, nthreads=1, want_acc=True)
+        x = bits_to_f64(inp["x"], shape.dtype)
+        lg = bits_to_f64(inp["logits"], shape.dtype)
+        for t in range(shape.T):
+            order = sorted(range(shape.E), key=lambda e: (-lg[t, e], e))[:shape.k]
+            w = scipy.special.softmax(lg[t, order])
+            ref = sum(w[j] * _fp4_dense_expert(inp, shape, order[j], x[t]) for j in range(shape.k))
+            if not np.allclose(acc[t], ref, rtol=1e-9, atol=1e-12):
+                fail(f"FP4 format {fmt}: forward differs from the dense torch reference")
+
+
 ALL_PINS = [
     pin_golden_packing, pin_unpack_random, pin_bits_to_double, pin_golden_rounding,
     pin_rounding_fp16_exhaustive, pin_rounding_bf16, pin_dequant, pin_golden_routing,
@@ -541,5 +602,6 @@ ALL_PINS = [
     pin_one_hot, pin_token_permutation, pin_zero_weights, pin_zero_weight_route_skipped,
     pin_nan_propagates, pin_full_softmax_routing, pin_biases_dense_over_experts,
     pin_fc2_bias_with_zero_weights, pin_full_softmax_nan_row, pin_router_integer_bruteforce,
-    pin_router_one_hot_and_layout, pin_router_rounding_and_scaling,
+    pin_router_one_hot_and_layout, pin_router_rounding_and_scaling, pin_fp4_element_and_scale_tables,
+    pin_fp4_dense_over_experts,
 ]

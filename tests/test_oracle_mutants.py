@@ -44,6 +44,12 @@ MUTANTS = {
     "router_last_term_dropped": ("      for (int h = 0; h < p->H; ++h)\n        acc += oracle_bits_to_double(x[t * p->H + h]",
                                  "      for (int h = 0; h + 1 < p->H; ++h)\n        acc += oracle_bits_to_double(x[t * p->H + h]"),
     "router_x_row_ignored": ("oracle_bits_to_double(x[t * p->H + h], p->dtype) *", "oracle_bits_to_double(x[h], p->dtype) *"),
+    "e2m1_exponent_bias": ("ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)"),
+    "e2m1_subnormal": ("e == 0 ? 0.5 * m :", "e == 0 ? 1.0 * m :"),
+    "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e8m0_bias": ("ldexp(1.0, (int)bits - 127)", "ldexp(1.0, (int)bits - 128)"),
+    "nvfp4_global_scale_dropped": ("(double)g[expert] : 1.0;", "1.0 : 1.0;"),
+    "fp4_scale_block_index": ("s8[row * nblk + kk / p->block]", "s8[row * nblk + kk / 32]"),
     "x_not_read_per_token": ("xr[kk] = oracle_bits_to_double(J->x[t * H + kk], p->dtype);", "xr[kk] = oracle_bits_to_double(J->x[kk], p->dtype);"),
 }
 
