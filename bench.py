@@ -49,9 +49,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill", "int3", "int2"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "prefill", "int3", "int2", "router"], default="decode",
                     help="decode: 48-layer stack; prefill: one 8K layer; int3: one INT3 Zipf layer "
-                         "(--T, --block); int2: one INT2 32K layer")
+                         "(--T, --block); int2: one INT2 32K layer; router: the router-logit GEMM "
+                         "alone (qmoe_router_logits, --T tokens, default 8192)")
     ap.add_argument("--block", type=int, default=64, help="INT3 block size (64 or 128)")
     ap.add_argument("--T", type=int, default=None, help="tokens per step (decode default 8)")
     ap.add_argument("--layers", type=int, default=LAYERS)
@@ -68,6 +69,9 @@ def parse():
     ap.add_argument("--decode-layer-kernel", action="store_true",
                     help="decode: qmoe_forward_ex with the decode layer kernel (fc1 and fc2 in one "
                          "persistent kernel) instead of one kernel per stage")
+    ap.add_argument("--format", choices=["int", "mxfp4", "nvfp4"], default="int",
+                    help="decode: expert weight format (the FP4 formats: E2M1 codes with E8M0 block-32 "
+                         "or E4M3 block-16 scales; NVFP4 with per-expert global scales)")
     ap.add_argument("--path", choices=["auto", "decode", "grouped"], default="auto",
                     help="kernel path of every call (auto: decode for T <= 8 and for mid-size batches "
                          "with few routes per expert, grouped otherwise)")
@@ -89,14 +93,16 @@ def workload_config(args, shape, layers, world):
             f"on call c-1's output, with its own router logits)" if passes > 1 else
             f"one step = one pass through the {layers} layer(s)")
     return {"workload": (f"{args.workload}: {layers} QMoE layers H={shape.H} inter={shape.inter} "
-                         f"E={shape.E} k={shape.k} INT{shape.bits} b{shape.block} "
+                         f"E={shape.E} k={shape.k} {['INT%d' % shape.bits, 'MXFP4', 'NVFP4'][shape.format]} "
+                         f"b{shape.block} "
                          f"{'BF16' if shape.dtype == 0 else 'FP16'} T={shape.T} per rank"),
             "T": shape.T, "layers": layers, "passes": passes, "step": step, "parallelism": f"replicas x{world}",
             "l2": "weights 16.3 GB >> L2, no flush" if args.workload == "decode" else "inputs > L2 per step",
             **({"options": "fc1/fc2 biases N(0, 0.5), full-softmax routing weights"}
                if getattr(args, "options", False) else {}),
             **({"decode_layer_kernel": 1} if getattr(args, "decode_layer_kernel", False) else {}),
-            **({"path": args.path} if getattr(args, "path", "auto") != "auto" else {})}
+            **({"path": args.path} if getattr(args, "path", "auto") != "auto" else {}),
+            **({"format": args.format} if getattr(args, "format", "int") != "int" else {})}
 
 
 def reduce_max(v, device):
@@ -128,6 +134,9 @@ def workload_shape(args):
     if args.workload == "decode":
         T = args.T or 8
         shape, recipe, _ = synthetic.decode_layer(T)
+        fmt = {"int": 0, "mxfp4": 1, "nvfp4": 2}[getattr(args, "format", "int")]
+        if fmt:
+            shape.format, shape.block = fmt, 32 if fmt == 1 else 16
         return shape, recipe
     if args.workload == "int3":
         shape, recipe, _ = synthetic.int3_zipf(args.T or 512, args.block)
@@ -171,8 +180,9 @@ def distinct_experts(logits_bits, dtype, k):
 def expert_bytes(shape):
     """Packed codes + scales of one expert: (fc1, fc2)."""
     H, I, b, B = shape.H, shape.inter, shape.bits, shape.block
-    fc1 = 2 * I * (H * b // 8 + (H // B) * 2)
-    fc2 = H * (I * b // 8 + (I // B) * 2)
+    sb = 1 if shape.format else 2      # FP4 formats: 8-bit block scales
+    fc1 = 2 * I * (H * b // 8 + (H // B) * sb)
+    fc2 = H * (I * b // 8 + (I // B) * sb)
     return fc1, fc2
 
 
@@ -256,8 +266,10 @@ def oracle_rate(shape, recipe, args, rank, budget_s):
             weights_cache[l] = full
         return weights_cache[l]
 
-    op = oracle.Problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
-                        shape.dtype)
+    def op_of(w):
+        return oracle.Problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
+                              shape.dtype, 0, shape.format, w.get("g1"), w.get("g2"))
+
     done_tokens = 0
     spent = 0.0
     if args.workload == "decode":
@@ -267,7 +279,7 @@ def oracle_rate(shape, recipe, args, rank, budget_s):
             w = weights(l)
             inp = dict(w, x=cur, logits=logits[l])
             t0 = time.perf_counter()
-            cur, _ = oracle.forward(op, inp, nthreads=cores)
+            cur, _ = oracle.forward(op_of(w), inp, nthreads=cores)
             spent += time.perf_counter() - t0
             done_tokens += shape.T
             l += 1
@@ -280,7 +292,7 @@ def oracle_rate(shape, recipe, args, rank, budget_s):
         while spent < budget_s and start < shape.T:
             toks = np.arange(start, min(start + batch, shape.T))
             t0 = time.perf_counter()
-            oracle.forward(op, inp, tokens=toks, nthreads=cores)
+            oracle.forward(op_of(w), inp, tokens=toks, nthreads=cores)
             spent += time.perf_counter() - t0
             done_tokens += len(toks)
             start += batch
@@ -289,14 +301,14 @@ def oracle_rate(shape, recipe, args, rank, budget_s):
     if args.workload == "decode":
         inp1 = dict(weights(0), x=x, logits=logits[0])
         t0 = time.perf_counter()
-        oracle.forward(op, inp1, nthreads=1)
+        oracle.forward(op_of(inp1), inp1, nthreads=1)
         one = shape.T / (time.perf_counter() - t0)
         one_sample = f"one decode layer x {shape.T} tokens"
     else:
         inp1 = dict(weights(0), x=x, logits=logits[0])
         toks = np.arange(0, min(16, shape.T))
         t0 = time.perf_counter()
-        oracle.forward(op, inp1, tokens=toks, nthreads=1)
+        oracle.forward(op_of(inp1), inp1, tokens=toks, nthreads=1)
         one = len(toks) / (time.perf_counter() - t0)
         one_sample = f"{len(toks)} tokens of one layer"
     return {"value": done_tokens / spent, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
@@ -391,7 +403,7 @@ class Stack:
         self.calls = passes * self.layers
         assert logits_h.shape[0] == self.calls
         self.p = qm.problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
-                            shape.dtype, path)
+                            shape.dtype, path, shape.format)
         self.x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
         self.lg_pin = torch.from_numpy(logits_h.view(np.int16)).pin_memory()
         self.x_d = self.x_pin.to(device)
@@ -410,7 +422,11 @@ class Stack:
     def step(self):
         o = self.options
         for c in range(self.calls):
-            if o is not None:
+            if self.shape.format:
+                w = self.W[c % self.layers]
+                self.qm.qmoe_forward_ex(self.p, 0, None, None, *self.args(c), fc1_global_scale=w.get("g1"),
+                                        fc2_global_scale=w.get("g2"))
+            elif o is not None:
                 l = c % self.layers
                 self.qm.qmoe_forward_ex(self.p, o["full_softmax"], o["b1"][l] if o["b1"] else None,
                                         o["b2"][l] if o["b2"] else None, *self.args(c),
@@ -598,7 +614,8 @@ def run_ours(args):
 
     # the prefill half of the metric: the same 48 layers' weights on 8192 packed tokens
     prefill = None
-    if args.workload == "decode" and not args.options and not args.decode_layer_kernel and not args.no_prefill:
+    if (args.workload == "decode" and not args.options and not args.decode_layer_kernel and not args.no_prefill
+            and args.format == "int"):
         pshape, precipe, _ = synthetic.prefill_8k()
         px_h, plg_h = host_inputs(pshape, precipe, layers, rank)
         pstack = Stack(qm, pshape, W, px_h, plg_h, 1, device)
@@ -627,7 +644,8 @@ def run_ours(args):
         pass
     fc1_b, fc2_b = expert_bytes(shape)
     # the captured kernels' workloads (traffic figures hold for the plain call only)
-    default_kernel = args.workload in ("decode", "prefill") and not args.options and not args.decode_layer_kernel
+    default_kernel = (args.workload in ("decode", "prefill") and not args.options and not args.decode_layer_kernel
+                      and args.format == "int")
     nact = distinct_experts(logits_h, shape.dtype, shape.k)
     if p_path(shape, args.path) == "decode":
         # the single-stage graphs run on the routing of the last call
@@ -723,11 +741,65 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_router(args):
+    """qmoe_router_logits alone: logits [T][128] = x [T][2048] . W_router^T, BF16, timed
+    with CUDA events over `steps` calls on one stream (inputs resident in HBM)."""
+    import torch
+
+    from quantized_mixture_experts_route_gb300 import build as qbuild
+
+    qbuild.build()
+    import quantized_mixture_experts_route_gb300 as qm
+
+    T, H, E = args.T or 8192, 2048, 128
+    dev = torch.device("cuda", 0)
+    p = qm.problem(T, H, 768, E, 8, 4, 32, synthetic.BF16)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    x = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16).view(torch.int16)
+    w = (torch.randn((E, H), generator=gen, device=dev) * 0.05).to(torch.bfloat16).view(torch.int16)
+    out = torch.empty((T, E), dtype=torch.int16, device=dev)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            qm.qmoe_router_logits(p, x, w, out, stream=s)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        a.record()
+        for _ in range(args.steps):
+            qm.qmoe_router_logits(p, x, w, out, stream=s)
+        b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    flops = 2.0 * T * H * E
+    peak = peaks.get("bf16_tflops") or 1900.0
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({
+        "metric": "router-logit GEMM tokens/s", "value": round(T / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "dtype": "bf16-mma/fp32-acc", "data": "synthetic",
+        "config": {"workload": f"router: logits [{T}][{E}] = x [{T}][{H}] . W_router [{E}][{H}]^T, BF16"},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4), "algorithmic_flops_per_launch": flops,
+                     "peak_source": "measured burst" if peaks.get("bf16_tflops") else "fallback"},
+        "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     args = parse()
     if args.options and args.impl == "reference":
         raise SystemExit("--options applies to the CUDA arm only")
-    if args.impl == "reference":
+    if args.workload == "router":
+        if args.impl == "reference":
+            raise SystemExit("--workload router applies to the CUDA arm only")
+        run_router(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

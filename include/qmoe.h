@@ -114,7 +114,28 @@ typedef struct {
   int32_t block_size;  /* 32, 64 or 128 weights per scale along K */
   int32_t dtype;       /* qmoe_dtype of x, logits, scales and out */
   int32_t path;        /* qmoe_path */
+  int32_t format;      /* qmoe_format of the expert weights (0: integer codes) */
 } qmoe_problem;
+
+/*
+ * Expert weight formats. QMOE_FORMAT_INT: bits-wide unsigned codes, w = (code -
+ * zp) * scale, scales in dtype. The FP4 formats (NVFP4 / MXFP4 QMoE weights,
+ * "[CUDA] Add INT4 and INT3 QMoE CPU/GPU offload support" #33575 and the
+ * "Execution plan to offload export on CPU for a MoE" review on NVFP4
+ * block/global scale semantics) hold 4-bit E2M1 codes (sign bit 3, exponent
+ * bits 2-1 with bias 1, mantissa bit 0; values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+ * their negatives), packed like INT4, with one 8-bit block scale per block
+ * along K ([E][N][K/block] uint8) and no zero point:
+ *   QMOE_FORMAT_MXFP4: block_size 32, E8M0 scales (2^(b - 127); b = 255 is NaN);
+ *   QMOE_FORMAT_NVFP4: block_size 16, E4M3 scales (sign, 4 exponent bits with
+ *     bias 7, 3 mantissa bits; no infinities, 0x7F / 0xFF NaN), times an FP32
+ *     global scale per expert and matmul (qmoe_options.fc1_global_scale /
+ *     fc2_global_scale; NULL means 1).
+ * w = element * block scale (* global scale). bits must be 4 and the zero-point
+ * pointers NULL. The FP4 formats run on the decode path (T <= 64 and at most
+ * 512 routes); larger batches return QMOE_ERR_UNSUPPORTED.
+ */
+typedef enum { QMOE_FORMAT_INT = 0, QMOE_FORMAT_MXFP4 = 1, QMOE_FORMAT_NVFP4 = 2 } qmoe_format;
 
 /* Bytes of device workspace that qmoe_forward / qmoe_route need for *p
  * (0 if *p is invalid). The same value serves both calls. */
@@ -170,6 +191,9 @@ qmoe_status qmoe_forward(const qmoe_problem* p, const void* x, const void* route
  *   router_logits argument is then not read and may be NULL. The pages run this
  *   GEMM ahead of QMoE as the router part of their RouterGateUpProj op
  *   ("[CUDA] Enable Tensor-Core INT3/INT4 QMoE offload ..." #33731).
+ * fc1_global_scale, fc2_global_scale: QMOE_FORMAT_NVFP4 only: FP32 [E] device
+ *   arrays (16-byte aligned), the global scale of each expert's fc1 and fc2
+ *   weights; NULL means 1. Ignored for the other formats.
  */
 typedef struct {
   int32_t full_softmax;
@@ -177,6 +201,8 @@ typedef struct {
   const void* fc2_bias;
   int32_t decode_layer_kernel;
   const void* router_weight;
+  const float* fc1_global_scale;
+  const float* fc2_global_scale;
 } qmoe_options;
 
 /*

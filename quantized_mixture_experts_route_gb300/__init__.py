@@ -40,6 +40,9 @@ QMOE_ERR_CUDA = 5
 QMOE_PATH_AUTO = 0
 QMOE_PATH_DECODE = 1
 QMOE_PATH_GROUPED = 2
+QMOE_FORMAT_INT = 0
+QMOE_FORMAT_MXFP4 = 1
+QMOE_FORMAT_NVFP4 = 2
 
 # every symbol the header declares
 EXPORTED = ("qmoe_workspace_bytes", "qmoe_forward", "qmoe_forward_stages", "qmoe_route",
@@ -64,17 +67,18 @@ class qmoe_problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("bits", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("path", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("path", ctypes.c_int32), ("format", ctypes.c_int32)]
 
 
 class qmoe_options(ctypes.Structure):
     _fields_ = [("full_softmax", ctypes.c_int32), ("fc1_bias", ctypes.c_void_p), ("fc2_bias", ctypes.c_void_p),
-                ("decode_layer_kernel", ctypes.c_int32), ("router_weight", ctypes.c_void_p)]
+                ("decode_layer_kernel", ctypes.c_int32), ("router_weight", ctypes.c_void_p),
+                ("fc1_global_scale", ctypes.c_void_p), ("fc2_global_scale", ctypes.c_void_p)]
 
 
-def problem(T, hidden, inter, num_experts, top_k, bits, block_size, dtype, path=QMOE_PATH_AUTO):
+def problem(T, hidden, inter, num_experts, top_k, bits, block_size, dtype, path=QMOE_PATH_AUTO, fmt=0):
     return qmoe_problem(int(T), int(hidden), int(inter), int(num_experts), int(top_k), int(bits),
-                        int(block_size), int(dtype), int(path))
+                        int(block_size), int(dtype), int(path), int(fmt))
 
 
 _lib = None
@@ -168,9 +172,10 @@ def qmoe_forward(p: qmoe_problem, x, router_logits, fc1_q, fc1_scales, fc1_zp, f
 
 def qmoe_forward_ex(p: qmoe_problem, full_softmax: int, fc1_bias, fc2_bias, x, router_logits, fc1_q,
                     fc1_scales, fc1_zp, fc2_q, fc2_scales, fc2_zp, out, workspace, stream=None,
-                    decode_layer_kernel: int = 0, router_weight=None) -> None:
+                    decode_layer_kernel: int = 0, router_weight=None, fc1_global_scale=None,
+                    fc2_global_scale=None) -> None:
     opt = qmoe_options(int(full_softmax), _addr(fc1_bias), _addr(fc2_bias), int(decode_layer_kernel),
-                       _addr(router_weight))
+                       _addr(router_weight), _addr(fc1_global_scale), _addr(fc2_global_scale))
     st = lib().qmoe_forward_ex(ctypes.byref(p), ctypes.byref(opt), _addr(x), _addr(router_logits),
                                _addr(fc1_q), _addr(fc1_scales), _addr(fc1_zp), _addr(fc2_q),
                                _addr(fc2_scales), _addr(fc2_zp), _addr(out), _addr(workspace),

@@ -23,6 +23,8 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 int resolve_path(const qmoe_problem& p) {
   if (p.path != QMOE_PATH_AUTO) return p.path;
   const int64_t R = p.T * (int64_t)p.top_k;
+  // the FP4 formats run on the decode path only
+  if (p.format != QMOE_FORMAT_INT) return p.T <= kDecodeMaxT && R <= kPermuteChunk ? QMOE_PATH_DECODE : QMOE_PATH_GROUPED;
   if (p.T <= 8) return QMOE_PATH_DECODE;
   // mid-size batches: the decode path while the routes are few per expert
   const bool few = R < 64 || R < 4 * (int64_t)p.num_experts;
@@ -38,7 +40,14 @@ qmoe_status check_problem(const qmoe_problem* p) {
       p->hidden <= 0 || p->inter <= 0)
     return QMOE_ERR_INVALID_ARGUMENT;
   if (p->bits != 2 && p->bits != 3 && p->bits != 4) return QMOE_ERR_UNSUPPORTED;
-  if (p->block_size != 32 && p->block_size != 64 && p->block_size != 128) return QMOE_ERR_UNSUPPORTED;
+  if (p->format < QMOE_FORMAT_INT || p->format > QMOE_FORMAT_NVFP4) return QMOE_ERR_UNSUPPORTED;
+  if (p->format != QMOE_FORMAT_INT) {
+    // E2M1 codes with 8-bit block scales: 32 per E8M0 scale, 16 per E4M3 scale
+    if (p->bits != 4 || p->block_size != (p->format == QMOE_FORMAT_MXFP4 ? 32 : 16)) return QMOE_ERR_UNSUPPORTED;
+    if (resolve_path(*p) != QMOE_PATH_DECODE) return QMOE_ERR_UNSUPPORTED;
+  } else if (p->block_size != 32 && p->block_size != 64 && p->block_size != 128) {
+    return QMOE_ERR_UNSUPPORTED;
+  }
   if (p->hidden % p->block_size || p->inter % p->block_size) return QMOE_ERR_UNSUPPORTED;
   if (p->hidden % 32 || p->inter % 32) return QMOE_ERR_UNSUPPORTED;
   if (p->num_experts > kMaxExperts || p->top_k > kMaxTopK) return QMOE_ERR_UNSUPPORTED;
@@ -67,6 +76,7 @@ Problem to_internal(const qmoe_problem& q) {
   p.block = q.block_size;
   p.dtype = q.dtype;
   p.path = resolve_path(q);
+  p.format = q.format;
   return p;
 }
 
@@ -137,6 +147,7 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
   if (st != QMOE_OK) return st;
   if (opt && opt->full_softmax != 0 && opt->full_softmax != 1) return QMOE_ERR_INVALID_ARGUMENT;
   if (opt && opt->decode_layer_kernel != 0 && opt->decode_layer_kernel != 1) return QMOE_ERR_INVALID_ARGUMENT;
+  if (p->format != QMOE_FORMAT_INT && (fc1_zp || fc2_zp)) return QMOE_ERR_INVALID_ARGUMENT;
   if (p->T == 0) return QMOE_OK;
   // with a router weight the logits are computed from x and the argument is not read
   const void* w_router = opt ? opt->router_weight : nullptr;
@@ -149,13 +160,22 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
   if ((fc1_zp && !aligned16(fc1_zp)) || (fc2_zp && !aligned16(fc2_zp))) return QMOE_ERR_MISALIGNED;
   if (opt && ((opt->fc1_bias && !aligned16(opt->fc1_bias)) || (opt->fc2_bias && !aligned16(opt->fc2_bias))))
     return QMOE_ERR_MISALIGNED;
+  if (opt && ((opt->fc1_global_scale && !aligned16(opt->fc1_global_scale)) ||
+              (opt->fc2_global_scale && !aligned16(opt->fc2_global_scale))))
+    return QMOE_ERR_MISALIGNED;
   Problem ip = to_internal(*p);
   if (opt) {
     ip.full_softmax = opt->full_softmax;
     ip.b1 = static_cast<const uint16_t*>(opt->fc1_bias);
     ip.b2 = static_cast<const uint16_t*>(opt->fc2_bias);
   }
-  ip.s1 = static_cast<const uint16_t*>(fc1_scales);
+  if (opt && ip.format == QMOE_FORMAT_NVFP4) {
+    ip.g1 = opt->fc1_global_scale;
+    ip.g2 = opt->fc2_global_scale;
+  }
+  // the SwiGLU normalisation reads the expert's first fc1 block scale (h_norm)
+  ip.s1 = ip.format == QMOE_FORMAT_INT ? static_cast<const uint16_t*>(fc1_scales) : nullptr;
+  ip.s1b = ip.format == QMOE_FORMAT_INT ? nullptr : static_cast<const uint8_t*>(fc1_scales);
   const bool grouped = ip.path == QMOE_PATH_GROUPED;
   Workspace ws;
   if (workspace_layout(ip, grouped, workspace, &ws) > workspace_bytes)

@@ -27,6 +27,7 @@
 // token's power of two squared. fc2 epilogue: y = (W2 h) / scale^2 * w_route in
 // FP32, stored per route id for the combine.
 #include "tma.cuh"
+#include <cuda_fp8.h>
 
 namespace qmoe {
 namespace {
@@ -106,7 +107,33 @@ struct DecodeArgs {
   int ks;                  // warps per team (K split of one item), 1, 2, 4 or 8
   Problem p;
   Workspace ws;
+  const float* gsc;        // NVFP4: per-expert FP32 global scales of this matmul, or null
 };
+
+// ---- FP4 expert formats (E2M1 codes, 8-bit block scales; see qmoe.h)
+// FP16 high bytes of the E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (their low
+// bytes are 0): one byte permute turns two 3-bit magnitudes into an FP16 pair.
+constexpr uint32_t kE2m1Lo = 0x3E3C3800u, kE2m1Hi = 0x46444240u;
+
+// The FP16 pair of the codes at bits sh..sh+3 and 16+sh..19+sh of w.
+__device__ __forceinline__ uint32_t fp4_pair(uint32_t w, int sh) {
+  const uint32_t c0 = (w >> sh) & 0xFu, c1 = (w >> (16 + sh)) & 0xFu;
+  // result bytes: 0 (byte 0 of the table), value of c0, 0, value of c1
+  const uint32_t v = __byte_perm(kE2m1Lo, kE2m1Hi, ((c0 & 7u) << 4) | ((c1 & 7u) << 12));
+  return v | ((c0 & 8u) << 12) | ((c1 & 8u) << 28);     // signs into bits 15 and 31
+}
+
+// FP16 bits of a block scale: E8M0 times 2^-ref (ref: the expert's reference
+// exponent, taken back in FP32 by the epilogue), or E4M3 as it is (exact in FP16).
+template <int FMT>
+__device__ __forceinline__ uint32_t fp4_scale_half(uint32_t b, int ref) {
+  if constexpr (FMT == QMOE_FORMAT_MXFP4) {
+    if (b == 0xFFu) return 0x7E00u;
+    return __half_as_ushort(__float2half_rn(ldexpf(1.0f, (int)b - 127 - ref)));
+  } else {
+    return __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3).x;
+  }
+}
 
 // Index of h_j in the permuted FP16 row layout.
 __device__ __forceinline__ int permuted_pos(int j, int G) {
@@ -195,9 +222,10 @@ constexpr int kRing = 8;        // chunks in flight per warp (shared-memory ring
 // Per-item data of the decode table entry of one active expert.
 struct ItemMeta {
   int e, begin, n_e, tok;       // tok: token of route slot g (this lane's activation row)
+  int ref;                      // MXFP4: exponent of the expert's first block scale
 };
 
-template <int BITS, bool FC1>
+template <int BITS, bool FC1, int FMT>
 __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -233,15 +261,21 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   float* tred = red + (size_t)team * kSlices * 32 * 4;
 
   auto meta_of = [&](int it) {
-    ItemMeta m{0, 0, 0, 0};
+    ItemMeta m{0, 0, 0, 0, 0};
     if (it < items) {
       // the chunks of one expert are consecutive, so the items that read the same
       // weight rows run at about the same time and the repeats hit L2
-      const int a = ws.active[it / rgroups];
-      m.e = a & 0xFFFF;
-      m.begin = ws.offsets[m.e] + (a >> 16) * kDecodeChunk;
+      const int act = ws.active[it / rgroups];
+      m.e = act & 0xFFFF;
+      m.begin = ws.offsets[m.e] + (act >> 16) * kDecodeChunk;
       m.n_e = min(kDecodeChunk, ws.offsets[m.e + 1] - m.begin);
       m.tok = g < m.n_e ? ws.sorted_route[m.begin + g] / p.k : 0;
+      if constexpr (FMT == QMOE_FORMAT_MXFP4) {
+        // E8M0 block scales span 2^-127 .. 2^127: the FP16 operands carry them
+        // relative to the expert's first one, whose power of two the epilogue applies
+        const uint8_t b0 = __ldg(reinterpret_cast<const uint8_t*>(a.s) + (int64_t)m.e * N * (K / p.block));
+        m.ref = b0 == 0xFF ? 0 : min(max((int)b0 - 127, -100), 100);
+      }
     }
     return m;
   };
@@ -252,6 +286,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   const uint8_t* pq = nullptr;
   const uint16_t* ps = nullptr;
   const uint8_t* pz = nullptr;
+  int64_t pso = 0;               // FP4 formats: element offset of the chunk's first 8-bit scale
   int pkk = 0;
   uint32_t sring[kRing], zring[kRing];
   auto issue = [&](int slot_u) {
@@ -263,15 +298,27 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
       pkk = cb * kChunkK + 32 * c;
       pq = a.q + row * pitch + (int64_t)pkk * BITS / 8;
       ps = a.s + row * nblk + (pkk >> lb);
+      pso = row * nblk + (pkk >> lb);
       pz = a.zp ? a.zp + row * nblk + (pkk >> lb) : nullptr;
     }
     const uint32_t dst = ring_base + slot_u * (2 * 32 * 16) + lane * 16;
     if (pkk < K) {
       copy_codes<BITS>(dst, pq);
       copy_codes<BITS>(dst + 32 * 16, pq + 8 * pitch);
-      sring[slot_u] = (uint32_t)__ldg(ps) | ((uint32_t)__ldg(ps + 8 * nblk) << 16);
-      zring[slot_u] = pz ? ((uint32_t)__ldg(pz) | ((uint32_t)__ldg(pz + 8 * nblk) << 16))
-                         : ((1u << (BITS - 1)) * 0x00010001u);
+      if constexpr (FMT == QMOE_FORMAT_INT) {
+        sring[slot_u] = (uint32_t)__ldg(ps) | ((uint32_t)__ldg(ps + 8 * nblk) << 16);
+        zring[slot_u] = pz ? ((uint32_t)__ldg(pz) | ((uint32_t)__ldg(pz + 8 * nblk) << 16))
+                           : ((1u << (BITS - 1)) * 0x00010001u);
+      } else {
+        // 8-bit scales of rows g and g + 8: one each per 32 codes (MXFP4), two (NVFP4)
+        const uint8_t* s8 = reinterpret_cast<const uint8_t*>(a.s) + pso;
+        if constexpr (FMT == QMOE_FORMAT_MXFP4)
+          sring[slot_u] = (uint32_t)__ldg(s8) | ((uint32_t)__ldg(s8 + 8 * nblk) << 16);
+        else
+          sring[slot_u] = (uint32_t)__ldg(s8) | ((uint32_t)__ldg(s8 + 1) << 8) |
+                          ((uint32_t)__ldg(s8 + 8 * nblk) << 16) | ((uint32_t)__ldg(s8 + 8 * nblk + 1) << 24);
+        zring[slot_u] = 0u;
+      }
     } else {
       sring[slot_u] = 0u;   // zero scale: stale codes in the slot contribute exact zeros
       zring[slot_u] = 0u;
@@ -279,6 +326,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
     cp_async_commit();
     pq += kChunkBytes;
     ps += chunk_scales;
+    pso += chunk_scales;
     if (pz) pz += chunk_scales;
     pkk += kChunkK;
     if (++pf_cc == cpi) { pf_cc = 0; pf_item += teams_total; }
@@ -372,13 +420,34 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
         }
       }
       const uint32_t sp = sring[u], zp2 = zring[u];
-      ra.s2 = scale_half2((uint16_t)(sp & 0xFFFFu), p.dtype);
-      rb.s2 = scale_half2((uint16_t)(sp >> 16), p.dtype);
-      ra.z2 = (0x6400u + (zp2 & 0xFFFFu)) * 0x00010001u;
-      rb.z2 = (0x6400u + (zp2 >> 16)) * 0x00010001u;
       uint32_t pa[16], pb[16];
-      dequant_chunk<BITS>(ra, pa);
-      dequant_chunk<BITS>(rb, pb);
+      if constexpr (FMT == QMOE_FORMAT_INT) {
+        ra.s2 = scale_half2((uint16_t)(sp & 0xFFFFu), p.dtype);
+        rb.s2 = scale_half2((uint16_t)(sp >> 16), p.dtype);
+        ra.z2 = (0x6400u + (zp2 & 0xFFFFu)) * 0x00010001u;
+        rb.z2 = (0x6400u + (zp2 >> 16)) * 0x00010001u;
+        dequant_chunk<BITS>(ra, pa);
+        dequant_chunk<BITS>(rb, pb);
+      } else {
+        // E2M1 pairs times the block scale: pair q holds codes (8i + m, 8i + m + 4)
+        // of word i = q / 4, the first 16 codes (words 0, 1) in the first NVFP4 block
+        uint32_t sa[2], sb[2];
+        if constexpr (FMT == QMOE_FORMAT_MXFP4) {
+          sa[0] = sa[1] = fp4_scale_half<FMT>(sp & 0xFFu, cur.ref) * 0x00010001u;
+          sb[0] = sb[1] = fp4_scale_half<FMT>((sp >> 16) & 0xFFu, cur.ref) * 0x00010001u;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            sa[h] = fp4_scale_half<FMT>((sp >> (8 * h)) & 0xFFu, 0) * 0x00010001u;
+            sb[h] = fp4_scale_half<FMT>((sp >> (16 + 8 * h)) & 0xFFu, 0) * 0x00010001u;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          pa[q] = h2_mul(fp4_pair(ra.w[q >> 2], 4 * (q & 3)), sa[q >> 3]);
+          pb[q] = h2_mul(fp4_pair(rb.w[q >> 2], 4 * (q & 3)), sb[q >> 3]);
+        }
+      }
 #pragma unroll
       for (int s = 0; s < 8; s += 2) {
         mma16816(acc0, pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1], bw[2 * s], bw[2 * s + 1]);
@@ -402,6 +471,13 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
       if (ksi == 0) {
         const int n0 = 2 * c, n1 = 2 * c + 1;
         const int begin = cur.begin, n_e = cur.n_e;
+        if constexpr (FMT != QMOE_FORMAT_INT) {
+          // the factor the FP16 operands left out: the MXFP4 reference power of
+          // two, or the NVFP4 global scale of the expert's matrix
+          const float ef = FMT == QMOE_FORMAT_MXFP4 ? ldexpf(1.0f, cur.ref) : (a.gsc ? __ldg(a.gsc + cur.e) : 1.0f);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) tot[r] *= ef;
+        }
         if constexpr (FC1) {
           // gate rows are even, up rows odd: lane g+1 (lane + 4) holds the up rows of lane g
           float up[4];
@@ -1280,7 +1356,7 @@ cudaError_t launch_int4_bs(DecodeArgs a, cudaStream_t s) {
 
 int sm_count() { return device_sm_count(); }
 
-template <int BITS, bool FC1>
+template <int BITS, bool FC1, int FMT>
 cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
   const int rgroups = a.N / kRowsPerGroup;
   const int64_t items = (int64_t)active_max * rgroups;
@@ -1298,9 +1374,9 @@ cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
   if (blocks > cap) blocks = cap;
   const size_t smem = (size_t)kWarps * kRing * 2 * 32 * 16 +
                       (ks > 1 ? (size_t)(kWarps / ks) * kSlices * 32 * 4 * sizeof(float) : 0);
-  const cudaError_t err = ensure_smem_optin(decode_gemv_kernel<BITS, FC1>, 100 * 1024);
+  const cudaError_t err = ensure_smem_optin(decode_gemv_kernel<BITS, FC1, FMT>, 100 * 1024);
   if (err != cudaSuccess) return err;
-  return launch_pdl(decode_gemv_kernel<BITS, FC1>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
+  return launch_pdl(decode_gemv_kernel<BITS, FC1, FMT>, dim3((unsigned)blocks), dim3(32 * kWarps), smem, s, a);
 }
 
 template <int BITS>
@@ -1317,8 +1393,17 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
     return fc1 ? launch_int4_bs<true>(a, s) : launch_int4_bs<false>(a, s);
   }
   DecodeArgs a{q, static_cast<const uint16_t*>(scales), zp, fc1 ? ws.x16 : ws.h16,
-               fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws};
-  return fc1 ? launch_one<BITS, true>(a, active_max, s) : launch_one<BITS, false>(a, active_max, s);
+               fc1 ? 2 * p.I : p.H, fc1 ? p.H : p.I, 1, p, ws, fc1 ? p.g1 : p.g2};
+  if constexpr (BITS == 4) {
+    if (p.format == QMOE_FORMAT_MXFP4)
+      return fc1 ? launch_one<4, true, QMOE_FORMAT_MXFP4>(a, active_max, s)
+                 : launch_one<4, false, QMOE_FORMAT_MXFP4>(a, active_max, s);
+    if (p.format == QMOE_FORMAT_NVFP4)
+      return fc1 ? launch_one<4, true, QMOE_FORMAT_NVFP4>(a, active_max, s)
+                 : launch_one<4, false, QMOE_FORMAT_NVFP4>(a, active_max, s);
+  }
+  return fc1 ? launch_one<BITS, true, QMOE_FORMAT_INT>(a, active_max, s)
+             : launch_one<BITS, false, QMOE_FORMAT_INT>(a, active_max, s);
 }
 
 }  // namespace

@@ -490,7 +490,8 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
 }  // namespace
 
 bool decode_layer_applies(const Problem& p, bool has_zp) {
-  return !has_zp && p.path == QMOE_PATH_DECODE && p.bits == 4 && p.block == 32 && p.T <= kDecodeMaxT &&
+  return !has_zp && p.path == QMOE_PATH_DECODE && p.format == QMOE_FORMAT_INT && p.bits == 4 && p.block == 32 &&
+         p.T <= kDecodeMaxT &&
          p.H % kLChunk == 0 && p.I % kLChunk == 0;
 }
 

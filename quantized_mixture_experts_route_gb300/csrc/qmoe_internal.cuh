@@ -6,6 +6,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -76,6 +77,10 @@ struct Problem {
   const uint16_t* b1;             // [E][2I] fc1 bias in dtype, or null
   const uint16_t* b2;             // [E][H]  fc2 bias in dtype, or null
   const uint16_t* s1;             // fc1 block scales [E][2I][H/block] in dtype (read by h_norm)
+  const uint8_t* s1b;             // the same for the FP4 formats (8-bit scales)
+  int format;                     // qmoe_format of the expert weights
+  const float* g1;                // NVFP4: per-expert FP32 global scales of fc1 / fc2, or null
+  const float* g2;
   int logits_after_wait;          // the router logits are the previous kernel's output: read
                                   //   them only after pdl_wait()
   __host__ __device__ int64_t R() const { return T * (int64_t)k; }
@@ -106,7 +111,8 @@ __host__ __device__ inline int perm_group(int bits) { return bits == 4 ? 8 : 16;
 // K a multiple of 128 for both matmuls). It reads activations whose odd K
 // positions are pre-divided by 16 (see decode.cu).
 __host__ __device__ inline bool decode_int4_blockscaled(const Problem& p) {
-  return p.path == QMOE_PATH_DECODE && p.bits == 4 && p.block == 32 && p.H % 128 == 0 && p.I % 128 == 0;
+  return p.path == QMOE_PATH_DECODE && p.format == QMOE_FORMAT_INT && p.bits == 4 && p.block == 32 &&
+         p.H % 128 == 0 && p.I % 128 == 0;
 }
 
 // How the routing kernel writes x16: not at all, plain, or with the odd K
@@ -171,7 +177,8 @@ __device__ __forceinline__ float2 fc1_bias_pair(const Problem& p, int e, int j) 
 // token's activation scale) and the fc2 epilogue divides by the same product.
 // h grows with the square of the fc1 weights, so rho_e is the power of two
 // 2^(-2 (E + 7)) with 2^E <= |s| < 2^(E+1) for the expert's first fc1 block
-// scale s: the stored values keep the magnitude that block scales near 2^-7
+// scale s (FP4 formats: its E8M0 value, or its E4M3 value times the expert's
+// NVFP4 global scale): the stored values keep the magnitude that block scales near 2^-7
 // give, whatever the scale range of the model (BF16 scales from 2^-40 to 2^40
 // keep the FP16 intermediate inside its normal range as long as an expert's
 // scales stay within about 2^6 of its first one). A zero, subnormal, infinite
@@ -179,9 +186,23 @@ __device__ __forceinline__ float2 fc1_bias_pair(const Problem& p, int e, int j) 
 // bias's own contribution, so rho_e is capped at 1 there. rho_e is a power of
 // two: the scaling is exact.
 __device__ __forceinline__ float h_norm(const Problem& p, int e) {
-  if (!p.s1) return 1.0f;
-  const uint16_t b = __ldg(p.s1 + (int64_t)e * (2 * p.I) * (p.H / p.block));
-  const float s = fabsf(half_bits_to_float(b, p.dtype));
+  float s;
+  const int64_t first = (int64_t)e * (2 * p.I) * (p.H / p.block);
+  if (p.format == QMOE_FORMAT_INT) {
+    if (!p.s1) return 1.0f;
+    s = fabsf(half_bits_to_float(__ldg(p.s1 + first), p.dtype));
+  } else {
+    // FP4 formats: the E8M0 scale, or the E4M3 scale times the expert's global scale
+    if (!p.s1b) return 1.0f;
+    const uint32_t b = __ldg(p.s1b + first);
+    if (p.format == QMOE_FORMAT_MXFP4) {
+      if (b == 0xFFu) return 1.0f;
+      s = ldexpf(1.0f, (int)b - 127);
+    } else {
+      s = fabsf(__half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3))));
+      if (p.g1) s *= fabsf(__ldg(p.g1 + e));
+    }
+  }
   if (!(s >= 1.17549435e-38f) || s > 3.0e38f) return 1.0f;  // zero, subnormal, inf, NaN
   int ex = (int)((__float_as_uint(s) >> 23) & 0xFF) - 127;   // floor(log2 s)
   ex = min(max(ex, -40), 40);

@@ -178,7 +178,12 @@ def make_torch_weights(shape: Shape, recipe: Recipe, seed: int, device):
         return torch.randint(0, 256, (n,), generator=g, device=device, dtype=torch.uint8).view(E, rows // E, -1)
 
     def scales(rows, K):
-        v = torch.rand((E, rows // E, K // shape.block), generator=g, device=device, dtype=torch.float32)
+        size = (E, rows // E, K // shape.block)
+        if shape.format == 1:    # E8M0 bytes 118..122
+            return torch.randint(118, 123, size, generator=g, device=device, dtype=torch.uint8)
+        if shape.format == 2:    # E4M3 bytes 0x18..0x3F
+            return torch.randint(0x18, 0x40, size, generator=g, device=device, dtype=torch.uint8)
+        v = torch.rand(size, generator=g, device=device, dtype=torch.float32)
         v = v * (recipe.scale_hi - recipe.scale_lo) + recipe.scale_lo
         return v.to(tdt)
 
@@ -186,7 +191,11 @@ def make_torch_weights(shape: Shape, recipe: Recipe, seed: int, device):
     fc1_s = scales(E * 2 * I, H)
     fc2_q = codes(E * H, I)
     fc2_s = scales(E * H, I)
-    return dict(fc1_q=fc1_q, fc1_s=fc1_s, fc1_zp=None, fc2_q=fc2_q, fc2_s=fc2_s, fc2_zp=None)
+    out = dict(fc1_q=fc1_q, fc1_s=fc1_s, fc1_zp=None, fc2_q=fc2_q, fc2_s=fc2_s, fc2_zp=None)
+    if shape.format == 2:
+        out["g1"] = torch.rand(E, generator=g, device=device) * 0.75 + 0.25
+        out["g2"] = torch.rand(E, generator=g, device=device) * 0.75 + 0.25
+    return out
 
 
 def make_activations(shape: Shape, recipe: Recipe, seed: int) -> dict:

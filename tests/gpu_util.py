@@ -24,7 +24,7 @@ def problem(shape, path=0):
     import quantized_mixture_experts_route_gb300 as qm
 
     return qm.problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
-                      shape.dtype, path)
+                      shape.dtype, path, getattr(shape, "format", 0))
 
 
 def device_inputs(inp):

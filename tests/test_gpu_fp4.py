@@ -1,0 +1,118 @@
+"""MXFP4 and NVFP4 experts (qmoe_problem.format) against the oracle.
+
+The E2M1 codes become FP16 pairs through a byte-permute table, times the block
+scale in FP16: E4M3 scales are exact in FP16; E8M0 scales are carried relative
+to the expert's first one and that power of two, like the NVFP4 global scale,
+is applied in FP32 by the epilogue. Both formats run on the decode path's
+generic kernel (an expert's routes in chunks of 8 on the MMA N side).
+
+CPU tests: the host checks of the formats. GPU tests (-m gpu): decode and
+mid-size batches, both dtypes, the decode-stack shape, E8M0 scales far from 1
+and spread over a few powers of two, NVFP4 with and without global scales.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from synthetic import BF16, FP16, Recipe, Shape
+from tests import gpu_util as gu
+
+qm = pytest.importorskip("quantized_mixture_experts_route_gb300")
+from quantized_mixture_experts_route_gb300 import build as qbuild  # noqa: E402
+
+MX, NV = qm.QMOE_FORMAT_MXFP4, qm.QMOE_FORMAT_NVFP4
+
+
+def P(T=8, fmt=MX, block=None, path=0, bits=4):
+    block = block or (32 if fmt == MX else 16)
+    return qm.problem(T, 512, 256, 16, 4, bits, block, BF16, path, fmt)
+
+
+def test_fp4_host_checks():
+    qbuild.build()
+    L = qm.lib()
+    ws = lambda p: L.qmoe_workspace_bytes(ctypes.byref(p))
+    assert ws(P(fmt=MX)) > 0 and ws(P(fmt=NV)) > 0
+    assert ws(P(fmt=MX, block=16)) == 0 and ws(P(fmt=NV, block=32)) == 0   # the formats fix the block
+    assert ws(P(fmt=MX, bits=3)) == 0
+    assert ws(P(fmt=MX, path=qm.QMOE_PATH_GROUPED)) == 0                   # decode path only
+    assert ws(P(T=200, fmt=NV)) == 0                                        # above the decode path's batch
+    assert ws(qm.problem(8, 512, 256, 16, 4, 4, 32, BF16, 0, 3)) == 0       # unknown format
+    # a zero point with an FP4 format is an argument error, found before any launch
+    F = 1 << 20
+    args = [F] * 10
+    args[2] = F  # fc1_zp
+    p = P(fmt=MX)
+    assert L.qmoe_forward(ctypes.byref(p), F, F, F, F, F, F, F, None, F, F, 1 << 40, None) == \
+        qm.QMOE_ERR_INVALID_ARGUMENT
+
+
+def oproblem(shape, inp):
+    return oracle.Problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block,
+                          shape.dtype, 0, shape.format, inp.get("g1"), inp.get("g2"))
+
+
+def fp4_forward(shape, inp, use_global=True):
+    import torch
+
+    p = gu.problem(shape)
+    d = gu.device_inputs(inp)
+    ws = torch.empty(qm.qmoe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+    g1 = d.get("g1") if use_global else None
+    g2 = d.get("g2") if use_global else None
+    qm.qmoe_forward_ex(p, 0, None, None, d["x"], d["logits"], d["fc1_q"], d["fc1_s"], None, d["fc2_q"],
+                       d["fc2_s"], None, out, ws, fc1_global_scale=g1, fc2_global_scale=g2)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().view(np.uint16)
+
+
+CASES = {
+    "mx_T8": (Shape(T=8, H=512, inter=256, E=16, k=4, bits=4, block=32, dtype=BF16, format=1), 101),
+    "mx_T1_fp16": (Shape(T=1, H=256, inter=512, E=8, k=2, bits=4, block=32, dtype=FP16, format=1), 102),
+    "mx_T33_mid": (Shape(T=33, H=512, inter=256, E=12, k=3, bits=4, block=32, dtype=BF16, format=1), 103),
+    "nv_T8": (Shape(T=8, H=512, inter=256, E=16, k=4, bits=4, block=16, dtype=BF16, format=2), 104),
+    "nv_T5_fp16": (Shape(T=5, H=384, inter=128, E=6, k=2, bits=4, block=16, dtype=FP16, format=2), 105),
+    "nv_T40_mid": (Shape(T=40, H=256, inter=256, E=8, k=2, bits=4, block=16, dtype=BF16, format=2), 106),
+    "mx_decode_stack": (Shape(T=8, H=2048, inter=768, E=128, k=8, bits=4, block=32, dtype=BF16, format=1), 107),
+    "nv_decode_stack": (Shape(T=8, H=2048, inter=768, E=128, k=8, bits=4, block=16, dtype=BF16, format=2), 108),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_fp4_parity(name):
+    shape, seed = CASES[name]
+    inp = synthetic.make_numpy(shape, Recipe(logit_std=1.0), seed)
+    got = fp4_forward(shape, inp)
+    ref, _ = oracle.forward(oproblem(shape, inp), inp)
+    gu.assert_parity(got, ref, shape.dtype, name)
+
+
+@pytest.mark.gpu
+def test_nvfp4_without_global_scales():
+    """NULL global scale pointers mean 1 on both sides."""
+    shape, seed = CASES["nv_T8"]
+    inp = synthetic.make_numpy(shape, Recipe(logit_std=1.0), seed)
+    got = fp4_forward(shape, inp, use_global=False)
+    ref, _ = oracle.forward(oproblem(shape, dict(inp, g1=None, g2=None)), dict(inp, g1=None, g2=None))
+    gu.assert_parity(got, ref, shape.dtype, "NVFP4 without global scales")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("lo,hi", [(127 - 40, 127 - 36), (127 + 20, 127 + 24)])
+def test_mxfp4_scales_far_from_one(lo, hi):
+    """E8M0 scales of 2^-40 .. 2^-36 or 2^20 .. 2^24, spread over four powers of
+    two inside an expert (outside the FP16 range as such); activations scaled so
+    that the outputs stay finite."""
+    shape, seed = CASES["mx_T8"]
+    rng = np.random.default_rng(7)
+    inp = synthetic.make_numpy(shape, Recipe(logit_std=1.0, x_std=1.0 if lo < 127 else 2.0 ** -40), seed)
+    for key in ("fc1_s", "fc2_s"):
+        inp[key] = rng.integers(lo, hi + 1, size=inp[key].shape, dtype=np.uint8)
+    got = fp4_forward(shape, inp)
+    ref, _ = oracle.forward(oproblem(shape, inp), inp)
+    gu.assert_parity(got, ref, shape.dtype, f"MXFP4 scales 2^{lo - 127}..2^{hi - 127}")

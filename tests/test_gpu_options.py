@@ -82,10 +82,13 @@ def test_empty_batch_with_options(L):
 
 
 def test_options_struct_layout():
-    # int32, two pointers, int32, pointer: offsets 0, 8, 16, 24, 32 and 40 bytes in all on LP64 hosts
+    # int32, two pointers, int32, three pointers: offsets 0, 8, 16, 24, 32, 40, 48; 56 bytes on LP64 hosts
     assert qm.qmoe_options.fc1_bias.offset == 8 and qm.qmoe_options.fc2_bias.offset == 16
     assert qm.qmoe_options.decode_layer_kernel.offset == 24 and qm.qmoe_options.router_weight.offset == 32
-    assert ctypes.sizeof(qm.qmoe_options) == 40
+    assert qm.qmoe_options.fc1_global_scale.offset == 40 and qm.qmoe_options.fc2_global_scale.offset == 48
+    assert ctypes.sizeof(qm.qmoe_options) == 56
+    # the problem: int64, nine int32 (the last the weight format)
+    assert qm.qmoe_problem.format.offset == 40 and ctypes.sizeof(qm.qmoe_problem) == 48
 
 
 @pytest.mark.gpu
