@@ -257,7 +257,11 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   extern __shared__ __align__(16) uint8_t smem[];
   // per warp: [kRing][2 rows][32 lanes][16 B] of codes; then the split-K buffers
   const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(smem) + warp * (kRing * 2 * 32 * 16);
-  float* red = reinterpret_cast<float*>(smem + kWarps * kRing * 2 * 32 * 16);
+  // per warp, after the code rings: [kRing][32 lanes] scale words and zero-point words
+  // (each lane reads back only what it wrote), then the split-K buffers
+  uint32_t* const sring = reinterpret_cast<uint32_t*>(smem + kWarps * kRing * 2 * 32 * 16) + warp * (2 * kRing * 32);
+  uint32_t* const zring = sring + kRing * 32;
+  float* red = reinterpret_cast<float*>(smem + kWarps * kRing * 2 * 32 * 16 + kWarps * 2 * kRing * 32 * 4);
   float* tred = red + (size_t)team * kSlices * 32 * 4;
 
   auto meta_of = [&](int it) {
@@ -288,7 +292,6 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   const uint8_t* pz = nullptr;
   int64_t pso = 0;               // FP4 formats: element offset of the chunk's first 8-bit scale
   int pkk = 0;
-  uint32_t sring[kRing], zring[kRing];
   auto issue = [&](int slot_u) {
     if (pf_cc == 0) {
       const ItemMeta m = pf_next;
@@ -306,22 +309,22 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
       copy_codes<BITS>(dst, pq);
       copy_codes<BITS>(dst + 32 * 16, pq + 8 * pitch);
       if constexpr (FMT == QMOE_FORMAT_INT) {
-        sring[slot_u] = (uint32_t)__ldg(ps) | ((uint32_t)__ldg(ps + 8 * nblk) << 16);
-        zring[slot_u] = pz ? ((uint32_t)__ldg(pz) | ((uint32_t)__ldg(pz + 8 * nblk) << 16))
+        sring[slot_u * 32 + lane] = (uint32_t)__ldg(ps) | ((uint32_t)__ldg(ps + 8 * nblk) << 16);
+        zring[slot_u * 32 + lane] = pz ? ((uint32_t)__ldg(pz) | ((uint32_t)__ldg(pz + 8 * nblk) << 16))
                            : ((1u << (BITS - 1)) * 0x00010001u);
       } else {
         // 8-bit scales of rows g and g + 8: one each per 32 codes (MXFP4), two (NVFP4)
         const uint8_t* s8 = reinterpret_cast<const uint8_t*>(a.s) + pso;
         if constexpr (FMT == QMOE_FORMAT_MXFP4)
-          sring[slot_u] = (uint32_t)__ldg(s8) | ((uint32_t)__ldg(s8 + 8 * nblk) << 16);
+          sring[slot_u * 32 + lane] = (uint32_t)__ldg(s8) | ((uint32_t)__ldg(s8 + 8 * nblk) << 16);
         else
-          sring[slot_u] = (uint32_t)__ldg(s8) | ((uint32_t)__ldg(s8 + 1) << 8) |
+          sring[slot_u * 32 + lane] = (uint32_t)__ldg(s8) | ((uint32_t)__ldg(s8 + 1) << 8) |
                           ((uint32_t)__ldg(s8 + 8 * nblk) << 16) | ((uint32_t)__ldg(s8 + 8 * nblk + 1) << 24);
-        zring[slot_u] = 0u;
+        zring[slot_u * 32 + lane] = 0u;
       }
     } else {
-      sring[slot_u] = 0u;   // zero scale: stale codes in the slot contribute exact zeros
-      zring[slot_u] = 0u;
+      sring[slot_u * 32 + lane] = 0u;   // zero scale: stale codes in the slot contribute exact zeros
+      zring[slot_u * 32 + lane] = 0u;
     }
     cp_async_commit();
     pq += kChunkBytes;
@@ -381,11 +384,13 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
     }
   };
 
-  for (int f0 = 0; f0 < total; f0 += kRing) {
-#pragma unroll
-    for (int u = 0; u < kRing; ++u) {
-      const int f = f0 + u;
-      if (f >= total) break;
+  // one rolled loop over the warp's chunks (its body once in the instruction
+  // stream: unrolled over the ring, the body with its epilogue overflowed the
+  // instruction cache)
+#pragma unroll 1
+  for (int f = 0; f < total; ++f) {
+    {
+      const int u = f % kRing;
       // keep kRing chunks in flight: issue f + kRing - 1 into the slot freed last iteration
       if (f + kRing - 1 < total) issue((u + kRing - 1) % kRing);
       else cp_async_commit();
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
           rb.w[i] = reinterpret_cast<const uint32_t*>(slotp + 32 * 16)[i];
         }
       }
-      const uint32_t sp = sring[u], zp2 = zring[u];
+      const uint32_t sp = sring[u * 32 + lane], zp2 = zring[u * 32 + lane];
       uint32_t pa[16], pb[16];
       if constexpr (FMT == QMOE_FORMAT_INT) {
         ra.s2 = scale_half2((uint16_t)(sp & 0xFFFFu), p.dtype);
@@ -1372,7 +1377,7 @@ cudaError_t launch_one(DecodeArgs a, int active_max, cudaStream_t s) {
   int64_t blocks = (teams_needed + (kWarps / ks) - 1) / (kWarps / ks);
   const int64_t cap = (int64_t)sm_count() * kBlocksPerSm;
   if (blocks > cap) blocks = cap;
-  const size_t smem = (size_t)kWarps * kRing * 2 * 32 * 16 +
+  const size_t smem = (size_t)kWarps * kRing * 2 * 32 * 16 + (size_t)kWarps * 2 * kRing * 32 * 4 +
                       (ks > 1 ? (size_t)(kWarps / ks) * kSlices * 32 * 4 * sizeof(float) : 0);
   const cudaError_t err = ensure_smem_optin(decode_gemv_kernel<BITS, FC1, FMT>, 100 * 1024);
   if (err != cudaSuccess) return err;
