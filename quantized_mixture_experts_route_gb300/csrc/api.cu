@@ -195,8 +195,11 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
     if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
     if (err == cudaSuccess && grouped) err = launch_gather(ip, ws, s);
   }
-  // FC1 and FC2 of the decode path in one kernel, where asked for and where it applies
-  if (err == cudaSuccess && opt && opt->decode_layer_kernel && in_range(QMOE_STAGE_FC1) &&
+  // FC1 and FC2 of the decode path in one kernel, where it applies: when asked
+  // for, and always for the FP4 formats (whose other decode kernel, the generic
+  // one, is three times slower)
+  const bool layer_kernel = (opt && opt->decode_layer_kernel) || ip.format != QMOE_FORMAT_INT;
+  if (err == cudaSuccess && layer_kernel && in_range(QMOE_STAGE_FC1) &&
       in_range(QMOE_STAGE_FC2) && decode_layer_applies(ip, fc1_zp || fc2_zp)) {
     err = launch_decode_layer(ip, fc1_q, fc1_scales, fc2_q, fc2_scales, ws, s);
     if (err == cudaSuccess && in_range(QMOE_STAGE_COMBINE)) err = launch_combine(ip, ws, out, s);

@@ -49,6 +49,7 @@
 // workspace counters, which makes the combine kernel write NaN to the output,
 // lets its copies in flight land and stops.
 #include "tma.cuh"
+#include <cuda_fp8.h>
 
 namespace qmoe {
 namespace {
@@ -128,6 +129,39 @@ __device__ __forceinline__ uint32_t ready_get(const uint32_t* word) {
   return v;
 }
 
+// ---- FP4 expert formats (E2M1 codes, 8-bit block scales; see qmoe.h)
+// FP16 high bytes of the E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (low bytes 0).
+constexpr uint32_t kLE2m1Lo = 0x3E3C3800u, kLE2m1Hi = 0x46444240u;
+
+// The FP16 pair of the codes at bits sh..sh+3 and 16+sh..19+sh of w: exact
+// element values (no offset to remove, no power of 16 in the activations).
+__device__ __forceinline__ uint32_t e2m1_pair(uint32_t w, int sh) {
+  const uint32_t c0 = (w >> sh) & 0xFu, c1 = (w >> (16 + sh)) & 0xFu;
+  const uint32_t v = __byte_perm(kLE2m1Lo, kLE2m1Hi, ((c0 & 7u) << 4) | ((c1 & 7u) << 12));
+  return v | ((c0 & 8u) << 12) | ((c1 & 8u) << 28);
+}
+
+// E8M0 block scale 2^(b - 127) as an FP32 value (exact; 255 is NaN).
+__device__ __forceinline__ float e8m0_value(uint32_t b) {
+  if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
+  return b == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// E4M3 block scale as an FP16 pair (exact in FP16).
+__device__ __forceinline__ uint32_t e4m3_half2(uint32_t b) {
+  const uint32_t h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3).x;
+  return h | (h << 16);
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Unit q of the queue: the fc1 units (a per entry) of entries 0 .. L-1, then
 // rounds r = L .. entries-1 of entry r's fc1 units followed by entry r-L's fc2
 // units (b per entry), then the fc2 units of the last L entries.
@@ -153,8 +187,9 @@ struct UnitQueue {
   }
 };
 
-template <bool BF16S>
+template <bool BF16S, int FMT>
 __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(LayerArgs a) {
+  constexpr bool kFp4 = FMT != QMOE_FORMAT_INT;
   const Problem& p = a.p;
   const Workspace& ws = a.ws;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -214,7 +249,9 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
     inst = if1 ? nst1 : nst2;
     iK = if1 ? p.H : p.I;
     iq = (if1 ? a.q1 : a.q2) + (int64_t)row0 * (iK / 2);
-    is = reinterpret_cast<const uint8_t*>((if1 ? a.s1 : a.s2) + (int64_t)row0 * (iK / 32));
+    // a row's scales: K/32 16-bit ones (INT4), K/32 E8M0 bytes, K/16 E4M3 bytes
+    is = reinterpret_cast<const uint8_t*>(if1 ? a.s1 : a.s2) +
+         (int64_t)row0 * (FMT == QMOE_FORMAT_MXFP4 ? iK / 32 : iK / 16);
     iact = reinterpret_cast<const uint8_t*>(if1 ? ws.x16 : ws.h16);
     ij = 0;
     iready = if1;
@@ -288,8 +325,12 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
 #pragma unroll
         for (int i = 0; i < kLRows / 4; ++i) cp_async16(dst + i * 512, src + (int64_t)i * 4 * (iK / 2));
       }
-      // scales: row `lane`'s 8 scales of the chunk
-      cp_async16(sb + kLScale + lane * 16, is + (int64_t)lane * (iK / 16) + ij * 16);
+      // scales: row `lane`'s scales of the chunk: 8 16-bit ones, 8 E8M0 bytes
+      // (MXFP4) or 16 E4M3 bytes (NVFP4)
+      if constexpr (FMT == QMOE_FORMAT_MXFP4)
+        cp_async8(sb + kLScale + lane * 16, is + (int64_t)lane * (iK / 32) + ij * 8);
+      else
+        cp_async16(sb + kLScale + lane * 16, is + (int64_t)lane * (iK / 16) + ij * 16);
       // activations: [route][256] FP16
       cp_async16(sb + kLAct + lane * 16, iact + (int64_t)ia0 * iK * 2 + ij * 512 + lane * 16);
       if (icnt > 1) cp_async16(sb + kLAct + 512 + lane * 16, iact + (int64_t)ia1 * iK * 2 + ij * 512 + lane * 16);
@@ -356,13 +397,15 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
         for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int e = 0; e < 4; ++e) tb[sub][q][e] = 0.f;
+      if constexpr (!kFp4) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          mma16816(tb[sub][0], ne_def, ne_def, no_def, no_def, bw[sub][4 * i], bw[sub][4 * i + 1]);
-          mma16816(tb[sub][1], ne_def, ne_def, no_def, no_def, bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
-        }
+          for (int sub = 0; sub < 2; ++sub) {
+            mma16816(tb[sub][0], ne_def, ne_def, no_def, no_def, bw[sub][4 * i], bw[sub][4 * i + 1]);
+            mma16816(tb[sub][1], ne_def, ne_def, no_def, no_def, bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+          }
+      }
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
         // rows 16 rh + g and 16 rh + 8 + g share the swizzle term, so the second
@@ -381,10 +424,23 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
                      : "=r"(cw[1][0].x), "=r"(cw[1][0].y), "=r"(cw[1][0].z), "=r"(cw[1][0].w) : "r"(cb1));
         asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+1024];\n"
                      : "=r"(cw[1][1].x), "=r"(cw[1][1].y), "=r"(cw[1][1].z), "=r"(cw[1][1].w) : "r"(cb1));
-        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sw[0][0]) : "r"(sr));
-        asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(sw[0][1]) : "r"(sr));
-        asm volatile("ld.shared.u32 %0, [%1+8];\n" : "=r"(sw[1][0]) : "r"(sr));
-        asm volatile("ld.shared.u32 %0, [%1+136];\n" : "=r"(sw[1][1]) : "r"(sr));
+        if constexpr (FMT == QMOE_FORMAT_INT) {
+          asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sw[0][0]) : "r"(sr));
+          asm volatile("ld.shared.u32 %0, [%1+128];\n" : "=r"(sw[0][1]) : "r"(sr));
+          asm volatile("ld.shared.u32 %0, [%1+8];\n" : "=r"(sw[1][0]) : "r"(sr));
+          asm volatile("ld.shared.u32 %0, [%1+136];\n" : "=r"(sw[1][1]) : "r"(sr));
+        } else {
+          // MXFP4: the E8M0 bytes of this lane's two block columns (blocks 2 (c & 1)
+          // and +1 of each half); NVFP4: the E4M3 bytes of the two 16-wide blocks of
+          // each of the lane's code pieces (pieces c and c + 4)
+          const uint32_t srow = sb + kLScale + (uint32_t)(rh * 16 + g) * 16;
+          const uint32_t o0 = FMT == QMOE_FORMAT_MXFP4 ? 2u * (c & 1) : 2u * c;
+          const uint32_t o1 = FMT == QMOE_FORMAT_MXFP4 ? 4u + 2u * (c & 1) : 8u + 2u * c;
+          asm volatile("ld.shared.u16 %0, [%1];\n" : "=r"(sw[0][0]) : "r"(srow + o0));
+          asm volatile("ld.shared.u16 %0, [%1];\n" : "=r"(sw[0][1]) : "r"(srow + 8 * 16 + o0));
+          asm volatile("ld.shared.u16 %0, [%1];\n" : "=r"(sw[1][0]) : "r"(srow + o1));
+          asm volatile("ld.shared.u16 %0, [%1];\n" : "=r"(sw[1][1]) : "r"(srow + 8 * 16 + o1));
+        }
         float t[2][2][4];
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub)
@@ -392,24 +448,52 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
           for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int e = 0; e < 4; ++e) t[sub][q][e] = 0.f;
+        if constexpr (!kFp4) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            const uint32_t wa = (&cw[sub][0].x)[i], wb = (&cw[sub][1].x)[i];
-            const uint32_t va8 = wa >> 8, vb8 = wb >> 8;
-            mma16816(t[sub][0], lop3_and_or(wa, 0x000F000Fu, kMagic), lop3_and_or(wb, 0x000F000Fu, kMagic),
-                     lop3_and_or(wa, 0x00F000F0u, kMagic), lop3_and_or(wb, 0x00F000F0u, kMagic),
-                     bw[sub][4 * i], bw[sub][4 * i + 1]);
-            mma16816(t[sub][1], lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
-                     lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
-                     bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
-          }
+            for (int sub = 0; sub < 2; ++sub) {
+              const uint32_t wa = (&cw[sub][0].x)[i], wb = (&cw[sub][1].x)[i];
+              const uint32_t va8 = wa >> 8, vb8 = wb >> 8;
+              mma16816(t[sub][0], lop3_and_or(wa, 0x000F000Fu, kMagic), lop3_and_or(wb, 0x000F000Fu, kMagic),
+                       lop3_and_or(wa, 0x00F000F0u, kMagic), lop3_and_or(wb, 0x00F000F0u, kMagic),
+                       bw[sub][4 * i], bw[sub][4 * i + 1]);
+              mma16816(t[sub][1], lop3_and_or(va8, 0x000F000Fu, kMagic), lop3_and_or(vb8, 0x000F000Fu, kMagic),
+                       lop3_and_or(va8, 0x00F000F0u, kMagic), lop3_and_or(vb8, 0x00F000F0u, kMagic),
+                       bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+            }
+        } else {
+          // E2M1 values straight from the codes (nibbles m and m + 4 of a word form
+          // a pair, in the same order as the INT4 path); NVFP4 multiplies each
+          // word's pairs by the E4M3 scale of its 16-wide block (words 0-1 and
+          // 2-3 of a piece) before the MMA
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+              const uint32_t wa = (&cw[sub][0].x)[i], wb = (&cw[sub][1].x)[i];
+              uint32_t a0 = e2m1_pair(wa, 0), a1 = e2m1_pair(wb, 0), a2 = e2m1_pair(wa, 4), a3 = e2m1_pair(wb, 4);
+              uint32_t a4 = e2m1_pair(wa, 8), a5 = e2m1_pair(wb, 8), a6 = e2m1_pair(wa, 12), a7 = e2m1_pair(wb, 12);
+              if constexpr (FMT == QMOE_FORMAT_NVFP4) {
+                const uint32_t sa = e4m3_half2((sw[sub][0] >> (8 * (i >> 1))) & 0xFFu);
+                const uint32_t sbv = e4m3_half2((sw[sub][1] >> (8 * (i >> 1))) & 0xFFu);
+                a0 = hmul2_bits(a0, sa); a2 = hmul2_bits(a2, sa); a4 = hmul2_bits(a4, sa); a6 = hmul2_bits(a6, sa);
+                a1 = hmul2_bits(a1, sbv); a3 = hmul2_bits(a3, sbv); a5 = hmul2_bits(a5, sbv); a7 = hmul2_bits(a7, sbv);
+              }
+              mma16816(t[sub][0], a0, a1, a2, a3, bw[sub][4 * i], bw[sub][4 * i + 1]);
+              mma16816(t[sub][1], a4, a5, a6, a7, bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
+            }
+        }
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
           float s_a0, s_a1, s_b0, s_b1;
           const uint32_t swa = sw[sub][0], swb = sw[sub][1];
-          if constexpr (BF16S) {
+          if constexpr (FMT == QMOE_FORMAT_MXFP4) {
+            s_a0 = e8m0_value(swa & 0xFFu); s_a1 = e8m0_value((swa >> 8) & 0xFFu);
+            s_b0 = e8m0_value(swb & 0xFFu); s_b1 = e8m0_value((swb >> 8) & 0xFFu);
+          } else if constexpr (FMT == QMOE_FORMAT_NVFP4) {
+            s_a0 = s_a1 = s_b0 = s_b1 = 1.0f;       // applied before the MMA
+          } else if constexpr (BF16S) {
             s_a0 = __uint_as_float(swa << 16); s_a1 = __uint_as_float(swa & 0xFFFF0000u);
             s_b0 = __uint_as_float(swb << 16); s_b1 = __uint_as_float(swb & 0xFFFF0000u);
           } else {
@@ -432,12 +516,17 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
 
     // ---- the unit's last chunk: its epilogue
     float v[2][2];                               // [row half][row g, row g + 8], route n
+    // NVFP4: the expert's global scale of this matmul
+    const float* gsc = f1 ? p.g1 : p.g2;
+    const float gf = (FMT == QMOE_FORMAT_NVFP4 && gsc) ? __ldg(gsc + ex) : 1.0f;
 #pragma unroll
     for (int rh = 0; rh < 2; ++rh) {
       v[rh][0] = acc[rh][0] + acc[rh][1];
       v[rh][1] = acc[rh][2] + acc[rh][3];
       v[rh][0] += __shfl_xor_sync(0xffffffffu, v[rh][0], 1);
       v[rh][1] += __shfl_xor_sync(0xffffffffu, v[rh][1], 1);
+      v[rh][0] *= gf;
+      v[rh][1] *= gf;
     }
     if (f1) {
 #pragma unroll
@@ -458,11 +547,13 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
           const float hs = sigma * sigma * h_norm(p, ex);
           const float h_lo = silu(v[rh][0] * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
           const float h_hi = silu(v[rh][1] * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
-          // fc2 reads these as activations: K-order permuted, odd K positions carry 1/16
+          // fc2 reads these as activations: K-order permuted, odd K positions carry
+          // 1/16 for the INT4 codes (the FP4 pairs hold exact values)
           const int pj0 = (j_lo & ~7) + ((j_lo & 7) < 4 ? 2 * (j_lo & 7) : 2 * (j_lo & 7) - 7);
           const int pj1 = (j_hi & ~7) + ((j_hi & 7) < 4 ? 2 * (j_hi & 7) : 2 * (j_hi & 7) - 7);
-          ws.h16[(int64_t)hp * p.I + pj0] = __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
-          ws.h16[(int64_t)hp * p.I + pj1] = __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * 0.0625f : h_hi));
+          const float odd = kFp4 ? 1.0f : 0.0625f;
+          ws.h16[(int64_t)hp * p.I + pj0] = __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * odd : h_lo));
+          ws.h16[(int64_t)hp * p.I + pj1] = __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * odd : h_hi));
         }
       }
       // publish: the unit's h16 values are stored (the release orders the
@@ -490,8 +581,10 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
 }  // namespace
 
 bool decode_layer_applies(const Problem& p, bool has_zp) {
-  return !has_zp && p.path == QMOE_PATH_DECODE && p.format == QMOE_FORMAT_INT && p.bits == 4 && p.block == 32 &&
-         p.T <= kDecodeMaxT &&
+  const bool fmt_ok = (p.format == QMOE_FORMAT_INT && p.block == 32) ||
+                      (p.format == QMOE_FORMAT_MXFP4 && p.block == 32) ||
+                      (p.format == QMOE_FORMAT_NVFP4 && p.block == 16);
+  return !has_zp && p.path == QMOE_PATH_DECODE && fmt_ok && p.bits == 4 && p.T <= kDecodeMaxT &&
          p.H % kLChunk == 0 && p.I % kLChunk == 0;
 }
 
@@ -511,14 +604,16 @@ cudaError_t launch_decode_layer(const Problem& p, const uint8_t* fc1_q, const vo
   // single block with little shared memory) finds room at once and routes while
   // this kernel runs
   const int blocks = device_sm_count() * per_sm - 1;
-  if (p.dtype == QMOE_BF16) {
-    const cudaError_t err = ensure_smem_optin(decode_layer_kernel<true>, (int)smem);
+  auto go = [&](auto kernel) -> cudaError_t {
+    const cudaError_t err = ensure_smem_optin(kernel, (int)smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(decode_layer_kernel<true>, dim3(blocks), dim3(kLThreads), smem, s, a);
-  }
-  const cudaError_t err = ensure_smem_optin(decode_layer_kernel<false>, (int)smem);
-  if (err != cudaSuccess) return err;
-  return launch_pdl(decode_layer_kernel<false>, dim3(blocks), dim3(kLThreads), smem, s, a);
+    return launch_pdl(kernel, dim3(blocks), dim3(kLThreads), smem, s, a);
+  };
+  // the FP4 formats' scales are 8-bit, so the activation dtype plays no part there
+  if (p.format == QMOE_FORMAT_MXFP4) return go(decode_layer_kernel<false, QMOE_FORMAT_MXFP4>);
+  if (p.format == QMOE_FORMAT_NVFP4) return go(decode_layer_kernel<false, QMOE_FORMAT_NVFP4>);
+  if (p.dtype == QMOE_BF16) return go(decode_layer_kernel<true, QMOE_FORMAT_INT>);
+  return go(decode_layer_kernel<false, QMOE_FORMAT_INT>);
 }
 
 }  // namespace qmoe

@@ -116,3 +116,28 @@ def test_mxfp4_scales_far_from_one(lo, hi):
     got = fp4_forward(shape, inp)
     ref, _ = oracle.forward(oproblem(shape, inp), inp)
     gu.assert_parity(got, ref, shape.dtype, f"MXFP4 scales 2^{lo - 127}..2^{hi - 127}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["mx_T8", "nv_T8", "mx_T33_mid"])
+def test_fp4_generic_kernel_through_stages(name):
+    """The stages one by one run the generic decode kernel for fc1 and fc2 (the
+    whole call runs the decode layer kernel for these shapes); NVFP4 without
+    global scales there (the stage calls take no options)."""
+    import torch
+
+    shape, seed = CASES[name]
+    inp = dict(synthetic.make_numpy(shape, Recipe(logit_std=1.0), seed), g1=None, g2=None)
+    p = gu.problem(shape)
+    d = gu.device_inputs(inp)
+    ws = torch.empty(qm.qmoe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+    for st in range(4):
+        qm.qmoe_forward_stages(p, st, st, d["x"], d["logits"], d["fc1_q"], d["fc1_s"], None, d["fc2_q"],
+                               d["fc2_s"], None, out, ws)
+    torch.cuda.synchronize()
+    staged = out.cpu().numpy().view(np.uint16)
+    ref, _ = oracle.forward(oproblem(shape, inp), inp)
+    gu.assert_parity(staged, ref, shape.dtype, f"{name} (generic kernel)")
+    whole = fp4_forward(shape, inp, use_global=False)
+    gu.assert_parity(whole, ref, shape.dtype, f"{name} (layer kernel)")
