@@ -223,6 +223,7 @@ constexpr int kRing = 8;        // chunks in flight per warp (shared-memory ring
 struct ItemMeta {
   int e, begin, n_e, tok;       // tok: token of route slot g (this lane's activation row)
   int ref;                      // MXFP4: exponent of the expert's first block scale
+  float hn;                     // the expert's SwiGLU normalisation (h_norm), read one item ahead
 };
 
 template <int BITS, bool FC1, int FMT>
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
   float* tred = red + (size_t)team * kSlices * 32 * 4;
 
   auto meta_of = [&](int it) {
-    ItemMeta m{0, 0, 0, 0, 0};
+    ItemMeta m{0, 0, 0, 0, 0, 1.0f};
     if (it < items) {
       // the chunks of one expert are consecutive, so the items that read the same
       // weight rows run at about the same time and the repeats hit L2
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
       m.begin = ws.offsets[m.e] + (act >> 16) * kDecodeChunk;
       m.n_e = min(kDecodeChunk, ws.offsets[m.e + 1] - m.begin);
       m.tok = g < m.n_e ? ws.sorted_route[m.begin + g] / p.k : 0;
+      m.hn = h_norm(p, m.e);
       if constexpr (FMT == QMOE_FORMAT_MXFP4) {
         // E8M0 block scales span 2^-127 .. 2^127: the FP16 operands carry them
         // relative to the expert's first one, whose power of two the epilogue applies
@@ -499,7 +501,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
                 const float inv = 1.0f / sigma;
                 const int j = (r & 2) ? j_hi : j_lo;
                 const float2 bj = fc1_bias_pair(p, cur.e, j);
-                const float h = silu(tot[r] * inv + bj.x) * (up[r] * inv + bj.y) * (sigma * sigma * h_norm(p, cur.e));
+                const float h = silu(tot[r] * inv + bj.x) * (up[r] * inv + bj.y) * (sigma * sigma * cur.hn);
                 ws.h16[(int64_t)(begin + n) * p.I + permuted_pos(j, G)] = __half_as_ushort(__float2half_rn(h));
               }
             }
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
               const int rid = ws.sorted_route[begin + n];
               const float inv = 1.0f / ws.tok_scale[rid / p.k];
               const int row = row0 + g + ((r & 2) ? 8 : 0);
-              ws.y[(int64_t)rid * p.H + row] = tot[r] * (inv * inv / h_norm(p, cur.e)) * ws.topk_w[rid];
+              ws.y[(int64_t)rid * p.H + row] = tot[r] * (inv * inv / cur.hn) * ws.topk_w[rid];
             }
           }
         }
@@ -817,7 +819,7 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
             b_lo = fc1_bias_pair(p, ex, j_lo);
             b_hi = fc1_bias_pair(p, ex, j_hi);
           }
-          const float hs = sigma * sigma * h_norm(p, ex);
+          const float hs = sigma * sigma * __int_as_float(__ldg(ws.dtab + (item / rgroups) * kDtabInts + 7));
           const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
           const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
           // fc2 reads these as activations: odd K positions carry 1/16
@@ -830,8 +832,8 @@ __global__ void __launch_bounds__(32 * kWarps, kBlocksPerSmB) decode_int4_bs_ker
         if ((c & 1) == 0 && n < cnt) {
           const int rid = ws.sorted_route[pos0 + n];
           const float inv = 1.0f / ws.tok_scale[rid / p.k];
-          const int ex = __ldg(ws.dtab + (item / rgroups) * kDtabInts);
-          const float fct = inv * inv / h_norm(p, ex) * ws.topk_w[rid];
+          const float hn = __int_as_float(__ldg(ws.dtab + (item / rgroups) * kDtabInts + 7));
+          const float fct = inv * inv / hn * ws.topk_w[rid];
           ws.y[(int64_t)rid * p.H + row0 + g] = v_lo * fct;
           ws.y[(int64_t)rid * p.H + row0 + g + 8] = v_hi * fct;
         }
@@ -1031,6 +1033,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   bool first_unit = true, fresh = true;
   int cnt = 0, pos0 = 0, e_rid = 0;
   float e_scale = 1.0f, e_w = 0.0f;              // epilogue operands of route n, loaded early
+  float e_hn = 1.0f;                             // the expert's SwiGLU normalisation (decode table)
   float acc[C::kHalves][4];                    // [row half][D fragment]
 #pragma unroll
   for (int rh = 0; rh < C::kHalves; ++rh)
@@ -1047,6 +1050,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + ei * kDtabInts + 4));
       pos0 = d0.y;
       cnt = d0.z;
+      e_hn = __int_as_float(d1.w);
       if (n < cnt) {
         if constexpr (FC1) {
           e_scale = __ldg(ws.tok_scale + (n ? d1.y : d1.x));
@@ -1257,7 +1261,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
             b_lo = fc1_bias_pair(p, ex, j_lo);
             b_hi = fc1_bias_pair(p, ex, j_hi);
           }
-          const float hs = sigma * sigma * h_norm(p, ex);
+          const float hs = sigma * sigma * e_hn;
           const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
           const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
           // fc2 reads these as activations: odd K positions carry 1/16
@@ -1269,7 +1273,7 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
       } else {
         if ((c & 1) == 0 && n < cnt) {
           const float inv = 1.0f / e_scale;
-          const float fct = inv * inv / h_norm(p, __ldg(ws.dtab + ei * kDtabInts)) * e_w;
+          const float fct = inv * inv / e_hn * e_w;
           ws.y[(int64_t)e_rid * p.H + row0 + g] = v_lo * fct;
           ws.y[(int64_t)e_rid * p.H + row0 + g + 8] = v_hi * fct;
         }

@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
   float acc[2][4];
   bool f1 = true;
   int ei = 0, rg = 0, cnt = 0, pos0 = 0, ex = 0, e_rid = 0;
-  float e_scale = 1.0f, e_w = 0.0f;
+  float e_scale = 1.0f, e_w = 0.0f, e_hn = 1.0f;
   int issued = 0, computed = 0;
   bool ok = true;
 
@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
       ex = d[0];
       pos0 = d[1];
       cnt = d[2];
+      e_hn = __int_as_float(d[7]);   // the expert's SwiGLU normalisation
       e_rid = n ? d[6] : d[3];
       if (n < cnt) {
         e_scale = __ldg(ws.tok_scale + (n ? d[5] : d[4]));
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
             b_lo = fc1_bias_pair(p, ex, j_lo);
             b_hi = fc1_bias_pair(p, ex, j_hi);
           }
-          const float hs = sigma * sigma * h_norm(p, ex);
+          const float hs = sigma * sigma * e_hn;
           const float h_lo = silu(v[rh][0] * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
           const float h_hi = silu(v[rh][1] * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
           // fc2 reads these as activations: K-order permuted, odd K positions carry
@@ -562,7 +563,7 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
       if (lane == 0) red_add_release(fc1_done + ei, 1);
     } else {
       const float inv = 1.0f / e_scale;
-      const float fct = inv * inv / h_norm(p, ex) * e_w;
+      const float fct = inv * inv / e_hn * e_w;
       if ((c & 1) == 0 && n < cnt) {
 #pragma unroll
         for (int rh = 0; rh < 2; ++rh) {

@@ -53,7 +53,8 @@ struct Workspace {
   int32_t* dtab;          // [kDtabMax][kDtabInts] decode table: one entry per (active expert,
                           //   pair of its routes): expert, first sorted row of the pair, routes in
                           //   the pair (1 or 2), route id of the first, token of each route, route
-                          //   id of the second (0 if none), 0; counters[3] entries
+                          //   id of the second (0 if none), the expert's h_norm (FP32 bits);
+                          //   counters[3] entries
   uint16_t* x16s;         // [R][H]   x16 rows gathered into sorted-route order (grouped)
   uint16_t* h16;          // [R][I]   SwiGLU output, FP16, sorted-route order, K-order permuted
   float* y;               // [R][H]   weighted fc2 output per route id (FP32)

@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
       d[4] = s_sorted[off + 2 * q] / p.k;
       d[5] = cnt > 1 ? s_sorted[off + 2 * q + 1] / p.k : 0;
       d[6] = cnt > 1 ? s_sorted[off + 2 * q + 1] : 0;
-      d[7] = 0;
+      d[7] = __float_as_int(h_norm(p, e));   // the expert's SwiGLU normalisation (fc1 scales are inputs)
     }
     __syncthreads();
   }
