@@ -110,30 +110,4 @@ inline bool make_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Row-major 3-D view: dims {d0, d1, d2} (d0 innermost, contiguous), strides in
-// bytes of dims 1 and 2; box b0 x b1 x b2 elements, landing in shared memory as
-// [b2][b1][b0]. Elements past a dimension's end read as zeros.
-inline bool make_map_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t d0,
-                        uint64_t d1, uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t b0,
-                        uint32_t b1, uint32_t b2, CUtensorMapSwizzle swizzle) {
-  auto fn = tensor_map_encoder();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {stride1, stride2};
-  const cuuint32_t box[3] = {b0, b1, b2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
-                                            int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4, %5}], [%2];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 }  // namespace qmoe
