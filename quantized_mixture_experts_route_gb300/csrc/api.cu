@@ -183,6 +183,12 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto in_range = [&](int stage) { return first_stage <= stage && stage <= last_stage; };
   cudaError_t err = cudaSuccess;
+  // FC1 and FC2 of the decode path in one kernel, where it applies: when asked
+  // for, and always for the FP4 formats (whose other decode kernel, the generic
+  // one, is slower)
+  const bool layer_kernel = ((opt && opt->decode_layer_kernel) || ip.format != QMOE_FORMAT_INT) &&
+                            in_range(QMOE_STAGE_FC1) && in_range(QMOE_STAGE_FC2) &&
+                            decode_layer_applies(ip, fc1_zp || fc2_zp);
   if (in_range(QMOE_STAGE_ROUTE)) {
     if (w_router) {
       err = launch_router_logits(ip, x, w_router, ws.rlogits, s);
@@ -191,16 +197,12 @@ qmoe_status forward_impl(const qmoe_problem* p, const qmoe_options* opt, int fir
     }
     if (err == cudaSuccess)
       err = launch_route(ip, x, router_logits, ws,
-                       decode_int4_blockscaled(ip) ? kX16OddSixteenth : kX16Plain, s);
+                         decode_int4_blockscaled(ip) ? kX16OddSixteenth
+                         : ip.format != QMOE_FORMAT_INT ? kX16Natural : kX16Plain, s);
     if (err == cudaSuccess) err = launch_group(ip, ws, grouped, s);
     if (err == cudaSuccess && grouped) err = launch_gather(ip, ws, s);
   }
-  // FC1 and FC2 of the decode path in one kernel, where it applies: when asked
-  // for, and always for the FP4 formats (whose other decode kernel, the generic
-  // one, is three times slower)
-  const bool layer_kernel = (opt && opt->decode_layer_kernel) || ip.format != QMOE_FORMAT_INT;
-  if (err == cudaSuccess && layer_kernel && in_range(QMOE_STAGE_FC1) &&
-      in_range(QMOE_STAGE_FC2) && decode_layer_applies(ip, fc1_zp || fc2_zp)) {
+  if (err == cudaSuccess && layer_kernel) {
     err = launch_decode_layer(ip, fc1_q, fc1_scales, fc2_q, fc2_scales, ws, s);
     if (err == cudaSuccess && in_range(QMOE_STAGE_COMBINE)) err = launch_combine(ip, ws, out, s);
     if (err == cudaErrorNotSupported) return QMOE_ERR_UNSUPPORTED;

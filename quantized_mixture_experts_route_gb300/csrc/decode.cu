@@ -111,16 +111,15 @@ struct DecodeArgs {
 };
 
 // ---- FP4 expert formats (E2M1 codes, 8-bit block scales; see qmoe.h)
-// FP16 high bytes of the E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (their low
-// bytes are 0): one byte permute turns two 3-bit magnitudes into an FP16 pair.
-constexpr uint32_t kE2m1Lo = 0x3E3C3800u, kE2m1Hi = 0x46444240u;
-
-// The FP16 pair of the codes at bits sh..sh+3 and 16+sh..19+sh of w.
-__device__ __forceinline__ uint32_t fp4_pair(uint32_t w, int sh) {
-  const uint32_t c0 = (w >> sh) & 0xFu, c1 = (w >> (16 + sh)) & 0xFu;
-  // result bytes: 0 (byte 0 of the table), value of c0, 0, value of c1
-  const uint32_t v = __byte_perm(kE2m1Lo, kE2m1Hi, ((c0 & 7u) << 4) | ((c1 & 7u) << 12));
-  return v | ((c0 & 8u) << 12) | ((c1 & 8u) << 28);     // signs into bits 15 and 31
+// Byte r of w (codes 2r and 2r + 1) as an FP16 pair, low half from the low
+// nibble (the hardware conversion, exact: every E2M1 value is an FP16 value).
+// The FP4 formats keep the activations in natural K order (kX16Natural), so
+// the pairs are adjacent codes.
+__device__ __forceinline__ uint32_t e2m1x2(uint32_t w, int r) {
+  const uint32_t b = (w >> (8 * r)) & 0xFFu;
+  uint32_t h;
+  asm("{\n .reg .b8 q;\n cvt.u8.u32 q, %1;\n cvt.rn.f16x2.e2m1x2 %0, q;\n}\n" : "=r"(h) : "r"(b));
+  return h;
 }
 
 // FP16 bits of a block scale: E8M0 times 2^-ref (ref: the expert's reference
@@ -436,8 +435,8 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
         dequant_chunk<BITS>(ra, pa);
         dequant_chunk<BITS>(rb, pb);
       } else {
-        // E2M1 pairs times the block scale: pair q holds codes (8i + m, 8i + m + 4)
-        // of word i = q / 4, the first 16 codes (words 0, 1) in the first NVFP4 block
+        // E2M1 pairs times the block scale: pair q holds codes 2q and 2q + 1 (byte
+        // q % 4 of word q / 4), the first 16 codes (words 0, 1) in the first NVFP4 block
         uint32_t sa[2], sb[2];
         if constexpr (FMT == QMOE_FORMAT_MXFP4) {
           sa[0] = sa[1] = fp4_scale_half<FMT>(sp & 0xFFu, cur.ref) * 0x00010001u;
@@ -451,8 +450,8 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          pa[q] = h2_mul(fp4_pair(ra.w[q >> 2], 4 * (q & 3)), sa[q >> 3]);
-          pb[q] = h2_mul(fp4_pair(rb.w[q >> 2], 4 * (q & 3)), sb[q >> 3]);
+          pa[q] = h2_mul(e2m1x2(ra.w[q >> 2], q & 3), sa[q >> 3]);
+          pb[q] = h2_mul(e2m1x2(rb.w[q >> 2], q & 3), sb[q >> 3]);
         }
       }
 #pragma unroll
@@ -502,7 +501,8 @@ __global__ void __launch_bounds__(32 * kWarps, 2) decode_gemv_kernel(DecodeArgs 
                 const int j = (r & 2) ? j_hi : j_lo;
                 const float2 bj = fc1_bias_pair(p, cur.e, j);
                 const float h = silu(tot[r] * inv + bj.x) * (up[r] * inv + bj.y) * (sigma * sigma * cur.hn);
-                ws.h16[(int64_t)(begin + n) * p.I + permuted_pos(j, G)] = __half_as_ushort(__float2half_rn(h));
+                const int pos = FMT == QMOE_FORMAT_INT ? permuted_pos(j, G) : j;   // FP4: natural order
+                ws.h16[(int64_t)(begin + n) * p.I + pos] = __half_as_ushort(__float2half_rn(h));
               }
             }
           }

@@ -130,15 +130,13 @@ __device__ __forceinline__ uint32_t ready_get(const uint32_t* word) {
 }
 
 // ---- FP4 expert formats (E2M1 codes, 8-bit block scales; see qmoe.h)
-// FP16 high bytes of the E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (low bytes 0).
-constexpr uint32_t kLE2m1Lo = 0x3E3C3800u, kLE2m1Hi = 0x46444240u;
-
-// The FP16 pair of the codes at bits sh..sh+3 and 16+sh..19+sh of w: exact
-// element values (no offset to remove, no power of 16 in the activations).
-__device__ __forceinline__ uint32_t e2m1_pair(uint32_t w, int sh) {
-  const uint32_t c0 = (w >> sh) & 0xFu, c1 = (w >> (16 + sh)) & 0xFu;
-  const uint32_t v = __byte_perm(kLE2m1Lo, kLE2m1Hi, ((c0 & 7u) << 4) | ((c1 & 7u) << 12));
-  return v | ((c0 & 8u) << 12) | ((c1 & 8u) << 28);
+// Byte r of w (codes 2r and 2r + 1) as an FP16 pair: the low half from the low
+// nibble (the hardware conversion, exact: every E2M1 value is an FP16 value).
+__device__ __forceinline__ uint32_t e2m1x2(uint32_t w, int r) {
+  const uint32_t b = (w >> (8 * r)) & 0xFFu;
+  uint32_t h;
+  asm("{\n .reg .b8 q;\n cvt.u8.u32 q, %1;\n cvt.rn.f16x2.e2m1x2 %0, q;\n}\n" : "=r"(h) : "r"(b));
+  return h;
 }
 
 // E8M0 block scale 2^(b - 127) as an FP32 value (exact; 255 is NaN).
@@ -464,17 +462,17 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
                        bw[sub][4 * i + 2], bw[sub][4 * i + 3]);
             }
         } else {
-          // E2M1 values straight from the codes (nibbles m and m + 4 of a word form
-          // a pair, in the same order as the INT4 path); NVFP4 multiplies each
-          // word's pairs by the E4M3 scale of its 16-wide block (words 0-1 and
-          // 2-3 of a piece) before the MMA
+          // E2M1 pairs straight from the codes: byte r of a word holds codes 2r and
+          // 2r + 1, which one conversion turns into an FP16 pair (activations in
+          // natural K order); NVFP4 multiplies each word's pairs by the E4M3 scale
+          // of its 16-wide block (words 0-1 and 2-3 of a piece) before the MMA
 #pragma unroll
           for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
               const uint32_t wa = (&cw[sub][0].x)[i], wb = (&cw[sub][1].x)[i];
-              uint32_t a0 = e2m1_pair(wa, 0), a1 = e2m1_pair(wb, 0), a2 = e2m1_pair(wa, 4), a3 = e2m1_pair(wb, 4);
-              uint32_t a4 = e2m1_pair(wa, 8), a5 = e2m1_pair(wb, 8), a6 = e2m1_pair(wa, 12), a7 = e2m1_pair(wb, 12);
+              uint32_t a0 = e2m1x2(wa, 0), a1 = e2m1x2(wb, 0), a2 = e2m1x2(wa, 1), a3 = e2m1x2(wb, 1);
+              uint32_t a4 = e2m1x2(wa, 2), a5 = e2m1x2(wb, 2), a6 = e2m1x2(wa, 3), a7 = e2m1x2(wb, 3);
               if constexpr (FMT == QMOE_FORMAT_NVFP4) {
                 const uint32_t sa = e4m3_half2((sw[sub][0] >> (8 * (i >> 1))) & 0xFFu);
                 const uint32_t sbv = e4m3_half2((sw[sub][1] >> (8 * (i >> 1))) & 0xFFu);
@@ -548,13 +546,18 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
           const float hs = sigma * sigma * e_hn;
           const float h_lo = silu(v[rh][0] * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
           const float h_hi = silu(v[rh][1] * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
-          // fc2 reads these as activations: K-order permuted, odd K positions carry
-          // 1/16 for the INT4 codes (the FP4 pairs hold exact values)
+          // fc2 reads these as activations: for INT4 K-order permuted, odd K
+          // positions carrying 1/16
           const int pj0 = (j_lo & ~7) + ((j_lo & 7) < 4 ? 2 * (j_lo & 7) : 2 * (j_lo & 7) - 7);
           const int pj1 = (j_hi & ~7) + ((j_hi & 7) < 4 ? 2 * (j_hi & 7) : 2 * (j_hi & 7) - 7);
-          const float odd = kFp4 ? 1.0f : 0.0625f;
-          ws.h16[(int64_t)hp * p.I + pj0] = __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * odd : h_lo));
-          ws.h16[(int64_t)hp * p.I + pj1] = __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * odd : h_hi));
+          if constexpr (kFp4) {
+            // natural K order, plain values (the FP4 operand pairs are adjacent codes)
+            ws.h16[(int64_t)hp * p.I + j_lo] = __half_as_ushort(__float2half_rn(h_lo));
+            ws.h16[(int64_t)hp * p.I + j_hi] = __half_as_ushort(__float2half_rn(h_hi));
+          } else {
+            ws.h16[(int64_t)hp * p.I + pj0] = __half_as_ushort(__float2half_rn((j_lo & 1) ? h_lo * 0.0625f : h_lo));
+            ws.h16[(int64_t)hp * p.I + pj1] = __half_as_ushort(__float2half_rn((j_hi & 1) ? h_hi * 0.0625f : h_hi));
+          }
         }
       }
       // publish: the unit's h16 values are stored (the release orders the

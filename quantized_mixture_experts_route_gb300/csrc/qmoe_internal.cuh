@@ -118,7 +118,9 @@ __host__ __device__ inline bool decode_int4_blockscaled(const Problem& p) {
 
 // How the routing kernel writes x16: not at all, plain, or with the odd K
 // positions divided by 16 (for decode_int4_blockscaled).
-enum X16Mode { kX16None = 0, kX16Plain = 1, kX16OddSixteenth = 2 };
+// kX16Natural: plain values in natural K order (the decode layer kernel's FP4
+// path, whose operand pairs are adjacent codes).
+enum X16Mode { kX16None = 0, kX16Plain = 1, kX16OddSixteenth = 2, kX16Natural = 3 };
 
 // ---------------------------------------------------------------------------
 // launchers (return the launch error, never synchronise)

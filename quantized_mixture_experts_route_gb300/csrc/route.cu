@@ -154,7 +154,10 @@ __device__ void convert_token(const Problem& p, const uint16_t* __restrict__ x, 
       in[2 * i] = __half_as_ushort(__float2half_rn(half_bits_to_float((uint16_t)(w[i] & 0xFFFF), p.dtype) * sigma));
       in[2 * i + 1] = __half_as_ushort(__float2half_rn(half_bits_to_float((uint16_t)(w[i] >> 16), p.dtype) * odd));
     }
-    if (G == 8) {
+    if (x16_mode == kX16Natural) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) out[i] = in[i];
+    } else if (G == 8) {
 #pragma unroll
       for (int g = 0; g < 2; ++g)
 #pragma unroll
