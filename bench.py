@@ -70,7 +70,7 @@ def parse():
                     help="decode: qmoe_forward_ex with the decode layer kernel (fc1 and fc2 in one "
                          "persistent kernel) instead of one kernel per stage")
     ap.add_argument("--format", choices=["int", "mxfp4", "nvfp4"], default="int",
-                    help="decode: expert weight format (the FP4 formats: E2M1 codes with E8M0 block-32 "
+                    help="decode / prefill: expert weight format (the FP4 formats: E2M1 codes with E8M0 block-32 "
                          "or E4M3 block-16 scales; NVFP4 with per-expert global scales)")
     ap.add_argument("--path", choices=["auto", "decode", "grouped"], default="auto",
                     help="kernel path of every call (auto: decode for T <= 8 and for mid-size batches "
@@ -149,6 +149,9 @@ def workload_shape(args):
     shape, recipe, _ = synthetic.prefill_8k()
     if args.T:
         shape.T = args.T
+    fmt = {"int": 0, "mxfp4": 1, "nvfp4": 2}[getattr(args, "format", "int")]
+    if fmt:
+        shape.format, shape.block = fmt, 32 if fmt == 1 else 16
     return shape, recipe
 
 

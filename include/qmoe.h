@@ -132,8 +132,7 @@ typedef struct {
  *     global scale per expert and matmul (qmoe_options.fc1_global_scale /
  *     fc2_global_scale; NULL means 1).
  * w = element * block scale (* global scale). bits must be 4 and the zero-point
- * pointers NULL. The FP4 formats run on the decode path (T <= 64 and at most
- * 512 routes); larger batches return QMOE_ERR_UNSUPPORTED. Where hidden and
+ * pointers NULL. The FP4 formats run on both paths. Where hidden and
  * inter are multiples of 256, a call that covers FC1 and FC2 runs them in the
  * decode layer kernel (see qmoe_options.decode_layer_kernel) whatever that
  * option says.

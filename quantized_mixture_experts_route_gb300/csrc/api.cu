@@ -23,8 +23,6 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 int resolve_path(const qmoe_problem& p) {
   if (p.path != QMOE_PATH_AUTO) return p.path;
   const int64_t R = p.T * (int64_t)p.top_k;
-  // the FP4 formats run on the decode path only
-  if (p.format != QMOE_FORMAT_INT) return p.T <= kDecodeMaxT && R <= kPermuteChunk ? QMOE_PATH_DECODE : QMOE_PATH_GROUPED;
   if (p.T <= 8) return QMOE_PATH_DECODE;
   // mid-size batches: the decode path while the routes are few per expert
   const bool few = R < 64 || R < 4 * (int64_t)p.num_experts;
@@ -44,7 +42,6 @@ qmoe_status check_problem(const qmoe_problem* p) {
   if (p->format != QMOE_FORMAT_INT) {
     // E2M1 codes with 8-bit block scales: 32 per E8M0 scale, 16 per E4M3 scale
     if (p->bits != 4 || p->block_size != (p->format == QMOE_FORMAT_MXFP4 ? 32 : 16)) return QMOE_ERR_UNSUPPORTED;
-    if (resolve_path(*p) != QMOE_PATH_DECODE) return QMOE_ERR_UNSUPPORTED;
   } else if (p->block_size != 32 && p->block_size != 64 && p->block_size != 128) {
     return QMOE_ERR_UNSUPPORTED;
   }

@@ -35,6 +35,7 @@
 // error code in the workspace, drains its copies and MMAs in flight, frees its
 // TMEM and returns.
 #include "tma.cuh"
+#include <cuda_fp8.h>
 
 namespace qmoe {
 namespace {
@@ -254,6 +255,34 @@ __device__ __forceinline__ void dequant_unit(const uint32_t* w, uint32_t z2, uin
 }
 
 
+// FP4 formats (see qmoe.h): byte r of w (codes 2r and 2r + 1) as an FP16 pair,
+// low half from the low nibble (the hardware conversion; exact). The FP4
+// activations are in natural K order, so pair p is codes 2p and 2p + 1.
+__device__ __forceinline__ uint32_t e2m1x2(uint32_t w, int r) {
+  const uint32_t b = (w >> (8 * r)) & 0xFFu;
+  uint32_t h;
+  asm("{\n .reg .b8 q;\n cvt.u8.u32 q, %1;\n cvt.rn.f16x2.e2m1x2 %0, q;\n}\n" : "=r"(h) : "r"(b));
+  return h;
+}
+
+// FP16 bits of an FP4 block scale: E8M0 relative to 2^ref (the epilogue applies
+// 2^ref in FP32), or E4M3 as it is (exact in FP16).
+__device__ __forceinline__ uint16_t fp4_scale_bits(int fmt, uint32_t b, int ref) {
+  if (fmt == QMOE_FORMAT_MXFP4) {
+    if (b == 0xFFu) return (uint16_t)0x7E00u;
+    const int e16 = (int)b - 127 - ref + 15;     // FP16 exponent field of 2^(b - 127 - ref)
+    if (e16 >= 1 && e16 <= 30) return (uint16_t)(e16 << 10);
+    return __half_as_ushort(__float2half_rn(ldexpf(1.0f, (int)b - 127 - ref)));
+  }
+  return __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3).x;
+}
+
+// MXFP4: the exponent of the first E8M0 scale of expert e's matrix (N rows).
+__device__ __forceinline__ int mx_ref(const void* scales, int e, int N, int nblk) {
+  const uint8_t b = __ldg(static_cast<const uint8_t*>(scales) + (int64_t)e * N * nblk);
+  return b == 0xFF ? 0 : min(max((int)b - 127, -100), 100);
+}
+
 __device__ __forceinline__ int permuted_pos(int j, int G) {
   const int base = j - j % G, i = j % G;
   return base + (i < G / 2 ? 2 * i : 2 * (i - G / 2) + 1);
@@ -448,6 +477,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int PER_LANE = C::UNITS / 32;
         constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;
         static_assert(PER_LANE % BATCH == 0, "scale batches");
+        if (BITS == 4 && p.format != QMOE_FORMAT_INT) {
+          // FP4: the 8-bit scales of each unit of 32 codes (one E8M0, or two E4M3 for
+          // the 16-wide NVFP4 blocks) as two FP16 words, the first 16 codes' low
+          const uint8_t* s8 = reinterpret_cast<const uint8_t*>(g.scales);
+          const bool nv = p.format == QMOE_FORMAT_NVFP4;
+#pragma unroll 1
+          for (int q0 = 0; q0 < PER_LANE; q0 += BATCH) {
+            // the batch's loads first (independent), then convert and store
+            uint32_t b0[BATCH], b1[BATCH];
+#pragma unroll
+            for (int q = 0; q < BATCH; ++q) {
+              const int u = lane + 32 * (q0 + q);
+              const int r = u / C::UNITS_PER_ROW, jj = u % C::UNITS_PER_ROW;
+              const int64_t wr = min(wrow_base + r, wrow_end - 1);
+              const int64_t idx = wr * nblk + (k0 + 32 * jj) / p.block;
+              b0[q] = __ldg(s8 + idx);
+              b1[q] = nv ? __ldg(s8 + idx + 1) : 0u;
+            }
+#pragma unroll
+            for (int q = 0; q < BATCH; ++q) {
+              const int u = lane + 32 * (q0 + q);
+              const int r = u / C::UNITS_PER_ROW;
+              // the raw scale bytes; the dequantisers convert them (rows past the
+              // array: a zero E4M3 / the smallest E8M0 with no rows to scale)
+              st[u] = wrow_base + r < wrow_end ? (b0[q] | ((nv ? b1[q] : b0[q]) << 8)) : 0u;
+            }
+          }
+          mbar_arrive(bar_cfull(s));
+          continue;
+        }
 #pragma unroll 1
         for (int q0 = 0; q0 < PER_LANE; q0 += BATCH) {
           uint16_t sv[BATCH];
@@ -580,6 +639,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nbox = (ksteps + span - 1) / span; // scale boxes per tile (TSC)
     const uint32_t zdef = (uint32_t)(1u << (BITS - 1)) << 16;
     for (int j = 0; j < my_works && go; ++j) {
+      // MXFP4: the tile's expert's reference exponent (its E8M0 scales become FP16 relative to it)
+      int fref = 0;
+      if (BITS == 4 && !TSC && p.format == QMOE_FORMAT_MXFP4) {
+        int e, row0, n0;
+        tile_of(j, e, row0, n0);
+        fref = mx_ref(g.scales, e, N, nblk);
+      }
       for (int i = 0; i < ksteps; ++i) {
         const int it = j * ksteps + i;
         if ((it & 1) != grp) continue;
@@ -637,7 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t s2 = (sz & 0xFFFFu) * 0x00010001u;
           uint32_t pr[16];
-          dequant_unit_fast<BITS>(w, sz >> 16, s2, pr);
+          if (BITS == 4 && p.format != QMOE_FORMAT_INT) {
+            // FP4: E2M1 pairs (natural order) times the scale of their 16 codes
+            const uint32_t sa = fp4_scale_bits(p.format, sz & 0xFFu, fref) * 0x00010001u;
+            const uint32_t sb2 = fp4_scale_bits(p.format, (sz >> 8) & 0xFFu, fref) * 0x00010001u;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) pr[q] = h2_mul(e2m1x2(w[q >> 2], q & 3), q < 8 ? sa : sb2);
+          } else {
+            dequant_unit_fast<BITS>(w, sz >> 16, s2, pr);
+          }
           uint8_t* rowp = bt + (jj >> 1) * (C::BN * 128) + r * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -692,7 +766,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = ok_h[half];
       const uint32_t tbase =
           tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * 2 * C::BN + half * C::BN);
-      const float inv = 1.0f / sigma;
+      // FP4: the factor the FP16 operands left out (MXFP4 2^ref, NVFP4 global scale)
+      float ef = 1.0f;
+      if constexpr (BITS == 4) {
+        if (p.format == QMOE_FORMAT_MXFP4) ef = ldexpf(1.0f, mx_ref(g.scales, e, N, g.K / p.block));
+        if (p.format == QMOE_FORMAT_NVFP4 && (FC1 ? p.g1 : p.g2)) ef = __ldg((FC1 ? p.g1 : p.g2) + e);
+      }
+      const float inv1 = 1.0f / sigma;
+      const float inv = ef * inv1;
       const float hn = h_norm(p, e);
       for (int c0 = 32 * cpart; c0 < C::BN; c0 += 32 * (kEpiWarps / 4)) {
         uint32_t v[32];
@@ -722,8 +803,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           uint16_t ov[16];
+          if (BITS == 4 && p.format != QMOE_FORMAT_INT) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) ov[permuted_pos(q, G)] = hv[q];
+            for (int q = 0; q < 16; ++q) ov[q] = hv[q];     // FP4: natural K order
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) ov[permuted_pos(q, G)] = hv[q];
+          }
           // one 32-byte store: a whole sector per lane
           st_global_v8(ws.h16 + (int64_t)pos * p.I + j0,
                        ov[0] | ((uint32_t)ov[1] << 16), ov[2] | ((uint32_t)ov[3] << 16),
@@ -731,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        ov[8] | ((uint32_t)ov[9] << 16), ov[10] | ((uint32_t)ov[11] << 16),
                        ov[12] | ((uint32_t)ov[13] << 16), ov[14] | ((uint32_t)ov[15] << 16));
         } else {
-          const float f = inv * inv / hn * wr;
+          const float f = inv * inv1 / hn * wr;
           float* dst = ws.y + (int64_t)rid * p.H + n0 + c0;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -802,7 +888,8 @@ template <int BITS, bool FC1>
 cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
                         const Workspace& ws, cudaStream_t s) {
   const int K = FC1 ? p.H : p.I;
-  if (!zp && (K / p.block) % 8 == 0) return launch_gemm_t<BITS, FC1, true>(p, q, scales, zp, ws, s);
+  if (!zp && p.format == QMOE_FORMAT_INT && (K / p.block) % 8 == 0)
+    return launch_gemm_t<BITS, FC1, true>(p, q, scales, zp, ws, s);
   return launch_gemm_t<BITS, FC1, false>(p, q, scales, zp, ws, s);
 }
 

@@ -130,8 +130,8 @@ def make_numpy(shape: Shape, recipe: Recipe, seed: int) -> dict:
             # E8M0 bytes 118..122: block scales 2^-9 .. 2^-5
             return rng.integers(118, 123, size=size, dtype=np.uint8)
         if shape.format == 2:
-            # E4M3 bytes 0x18..0x3F: exponent fields 3..7 (2^-4 .. 2^0), any mantissa
-            return rng.integers(0x18, 0x40, size=size, dtype=np.uint8)
+            # E4M3 bytes 0x08..0x1F: exponent fields 1..3 (2^-6 .. 2^-4), any mantissa
+            return rng.integers(0x08, 0x20, size=size, dtype=np.uint8)
         v = rng.uniform(recipe.scale_lo, recipe.scale_hi, size=size)
         return float_to_bits(v, dt)
 
@@ -181,8 +181,8 @@ def make_torch_weights(shape: Shape, recipe: Recipe, seed: int, device):
         size = (E, rows // E, K // shape.block)
         if shape.format == 1:    # E8M0 bytes 118..122
             return torch.randint(118, 123, size, generator=g, device=device, dtype=torch.uint8)
-        if shape.format == 2:    # E4M3 bytes 0x18..0x3F
-            return torch.randint(0x18, 0x40, size, generator=g, device=device, dtype=torch.uint8)
+        if shape.format == 2:    # E4M3 bytes 0x08..0x1F
+            return torch.randint(0x08, 0x20, size, generator=g, device=device, dtype=torch.uint8)
         v = torch.rand(size, generator=g, device=device, dtype=torch.float32)
         v = v * (recipe.scale_hi - recipe.scale_lo) + recipe.scale_lo
         return v.to(tdt)

@@ -1,10 +1,12 @@
-"""MXFP4 and NVFP4 experts (qmoe_problem.format) against the oracle.
+"""MXFP4 and NVFP4 experts (qmoe_problem.format) against the oracle, on the
+decode path and on the grouped tcgen05 path.
 
 The E2M1 codes become FP16 pairs through a byte-permute table, times the block
 scale in FP16: E4M3 scales are exact in FP16; E8M0 scales are carried relative
 to the expert's first one and that power of two, like the NVFP4 global scale,
-is applied in FP32 by the epilogue. Both formats run on the decode path's
-generic kernel (an expert's routes in chunks of 8 on the MMA N side).
+is applied in FP32 by the epilogue. On the decode path they run on the decode
+layer kernel (or the generic kernel through the stage calls); on the grouped
+path the dequantisers form the same FP16 pairs for tcgen05.
 
 CPU tests: the host checks of the formats. GPU tests (-m gpu): decode and
 mid-size batches, both dtypes, the decode-stack shape, E8M0 scales far from 1
@@ -38,8 +40,8 @@ def test_fp4_host_checks():
     assert ws(P(fmt=MX)) > 0 and ws(P(fmt=NV)) > 0
     assert ws(P(fmt=MX, block=16)) == 0 and ws(P(fmt=NV, block=32)) == 0   # the formats fix the block
     assert ws(P(fmt=MX, bits=3)) == 0
-    assert ws(P(fmt=MX, path=qm.QMOE_PATH_GROUPED)) == 0                   # decode path only
-    assert ws(P(T=200, fmt=NV)) == 0                                        # above the decode path's batch
+    assert ws(P(fmt=MX, path=qm.QMOE_PATH_GROUPED)) > 0                    # both paths
+    assert ws(P(T=200, fmt=NV)) > 0
     assert ws(qm.problem(8, 512, 256, 16, 4, 4, 32, BF16, 0, 3)) == 0       # unknown format
     # a zero point with an FP4 format is an argument error, found before any launch
     F = 1 << 20
@@ -77,6 +79,8 @@ CASES = {
     "nv_T8": (Shape(T=8, H=512, inter=256, E=16, k=4, bits=4, block=16, dtype=BF16, format=2), 104),
     "nv_T5_fp16": (Shape(T=5, H=384, inter=128, E=6, k=2, bits=4, block=16, dtype=FP16, format=2), 105),
     "nv_T40_mid": (Shape(T=40, H=256, inter=256, E=8, k=2, bits=4, block=16, dtype=BF16, format=2), 106),
+    "mx_grouped_T300": (Shape(T=300, H=512, inter=256, E=8, k=2, bits=4, block=32, dtype=BF16, format=1), 109),
+    "nv_grouped_T260_fp16": (Shape(T=260, H=256, inter=320, E=6, k=3, bits=4, block=16, dtype=FP16, format=2), 110),
     "mx_decode_stack": (Shape(T=8, H=2048, inter=768, E=128, k=8, bits=4, block=32, dtype=BF16, format=1), 107),
     "nv_decode_stack": (Shape(T=8, H=2048, inter=768, E=128, k=8, bits=4, block=16, dtype=BF16, format=2), 108),
 }
