@@ -145,3 +145,34 @@ def test_fp4_generic_kernel_through_stages(name):
     gu.assert_parity(staged, ref, shape.dtype, f"{name} (generic kernel)")
     whole = fp4_forward(shape, inp, use_global=False)
     gu.assert_parity(whole, ref, shape.dtype, f"{name} (layer kernel)")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["mx_T8", "nv_T8", "mx_grouped_T300"])
+def test_fp4_with_biases_full_softmax_and_router(name):
+    """The FP4 formats with the other options: FC1/FC2 biases, full-softmax
+    routing weights and router logits computed from a router weight; against
+    the oracle on the GPU's own logits (the routing decision taken from the same
+    values on both sides)."""
+    import torch
+
+    shape, seed = CASES[name]
+    inp = synthetic.make_numpy(shape, Recipe(logit_std=1.0, bias_std=0.5), seed)
+    rng = np.random.default_rng(seed + 7)
+    w_router = synthetic.float_to_bits(rng.standard_normal((shape.E, shape.H)) * 0.3, shape.dtype)
+    p = gu.problem(shape)
+    d = gu.device_inputs(inp)
+    logits = torch.empty((shape.T, shape.E), dtype=torch.int16, device="cuda")
+    qm.qmoe_router_logits(p, d["x"], gu.dev(w_router), logits)
+    ws = torch.empty(qm.qmoe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+    qm.qmoe_forward_ex(p, 1, d["fc1_b"], d["fc2_b"], d["x"], None, d["fc1_q"], d["fc1_s"], None, d["fc2_q"],
+                       d["fc2_s"], None, out, ws, router_weight=gu.dev(w_router),
+                       fc1_global_scale=d.get("g1"), fc2_global_scale=d.get("g2"))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16)
+    with_logits = dict(inp, logits=logits.cpu().numpy().view(np.uint16))
+    op = oracle.Problem(shape.T, shape.H, shape.inter, shape.E, shape.k, shape.bits, shape.block, shape.dtype, 1,
+                        shape.format, inp.get("g1"), inp.get("g2"))
+    ref, _ = oracle.forward(op, with_logits)
+    gu.assert_parity(got, ref, shape.dtype, f"{name} with options")
