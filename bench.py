@@ -72,9 +72,10 @@ def parse():
     ap.add_argument("--format", choices=["int", "mxfp4", "nvfp4"], default="int",
                     help="decode / prefill: expert weight format (the FP4 formats: E2M1 codes with E8M0 block-32 "
                          "or E4M3 block-16 scales; NVFP4 with per-expert global scales)")
-    ap.add_argument("--path", choices=["auto", "decode", "grouped"], default="auto",
+    ap.add_argument("--path", choices=["auto", "decode", "grouped", "tiles", "ws"], default="auto",
                     help="kernel path of every call (auto: decode for T <= 8 and for mid-size batches "
-                         "with few routes per expert, grouped otherwise)")
+                         "with few routes per expert, grouped otherwise; grouped: its kernel by the route "
+                         "count; tiles / ws: the grouped path's route-tile / weights-stationary kernel)")
     ap.add_argument("--clock-log", default=None,
                     help="CSV file for the nvidia-smi clock samples (default: a file in the temp directory)")
     return ap.parse_args()
@@ -373,7 +374,9 @@ def kernel_traffic(key):
 
 
 def p_path(shape, forced="auto"):
-    """The kernel path of a call (csrc/api.cu, resolve_path)."""
+    """The kernel path of a call (csrc/api.cu, resolve_path): "decode" or "grouped"."""
+    if forced in ("grouped", "tiles", "ws"):
+        return "grouped"
     if forced != "auto":
         return forced
     R = shape.T * shape.k
@@ -602,7 +605,8 @@ def run_ours(args):
         options = dict(full_softmax=1, b1=B1, b2=B2, layer_kernel=0)
     if args.decode_layer_kernel:
         options = dict(options or dict(full_softmax=0, b1=None, b2=None), layer_kernel=1)
-    path = {"auto": qm.QMOE_PATH_AUTO, "decode": qm.QMOE_PATH_DECODE, "grouped": qm.QMOE_PATH_GROUPED}[args.path]
+    path = {"auto": qm.QMOE_PATH_AUTO, "decode": qm.QMOE_PATH_DECODE, "grouped": qm.QMOE_PATH_GROUPED,
+            "tiles": qm.QMOE_PATH_GROUPED_ROUTE_TILES, "ws": qm.QMOE_PATH_GROUPED_WS}[args.path]
     stack = Stack(qm, shape, W, x_h, logits_h, passes, device, options, path)
     s = torch.cuda.Stream(device)
     torch.cuda.synchronize()

@@ -96,13 +96,34 @@ typedef enum {
 } qmoe_status;
 
 /*
- * Execution path. AUTO takes DECODE for T <= 8 and GROUPED otherwise.
- * DECODE: split-K dequant-GEMV kernels bound by HBM bandwidth; needs T <= 8.
- * GROUPED: per-expert dequant-GEMM tiles on tcgen05 tensor cores with TMEM
+ * Execution path. AUTO takes DECODE for T <= 8 and, up to T = 64 and 512
+ * routes (R = T * top_k), while R < 64 or R < 4 * E (the pages switch from their
+ * tensor-core GEMV to the grouped GEMM at num_r >= 64 && num_r >= 4 E); GROUPED
+ * otherwise.
+ * DECODE: weights-stationary dequant-GEMV kernels bound by HBM bandwidth; needs
+ * T <= 64, R <= 512 and hidden, inter <= 8192.
+ * GROUPED: per-expert dequant-GEMM on tcgen05 tensor cores with TMEM
  * accumulators; needs hidden and inter to be multiples of 64 (bits 2 and 4)
- * or 128 (bits 3). A path whose condition fails returns QMOE_ERR_UNSUPPORTED.
+ * or 128 (bits 3). It has two kernels, chosen by the route count: with few
+ * routes per expert (R <= 32 * E, and hidden, inter multiples of 256)
+ * GROUPED_WS, otherwise GROUPED_ROUTE_TILES.
+ * GROUPED_ROUTE_TILES: tiles of 256 sorted routes of one expert on the MMA's M
+ * side against 256 (INT3: 128) dequantised weight rows on N.
+ * GROUPED_WS (weights-stationary): 128 dequantised weight rows on M against up
+ * to 128 routes of one expert on N, in steps of 16; each expert's weights are
+ * dequantised once per 128 of its routes, and an expert with a few routes pays
+ * for 16-route MMA columns instead of a 128-row route tile. Needs hidden and
+ * inter to be multiples of 256 (GROUPED picks route tiles otherwise).
+ * The two grouped kernels give results within the same error bound. A path
+ * whose condition fails returns QMOE_ERR_UNSUPPORTED.
  */
-typedef enum { QMOE_PATH_AUTO = 0, QMOE_PATH_DECODE = 1, QMOE_PATH_GROUPED = 2 } qmoe_path;
+typedef enum {
+  QMOE_PATH_AUTO = 0,
+  QMOE_PATH_DECODE = 1,
+  QMOE_PATH_GROUPED = 2,
+  QMOE_PATH_GROUPED_ROUTE_TILES = 3,
+  QMOE_PATH_GROUPED_WS = 4
+} qmoe_path;
 
 typedef struct {
   int64_t T;           /* packed tokens (rows of x) */

@@ -40,6 +40,8 @@ QMOE_ERR_CUDA = 5
 QMOE_PATH_AUTO = 0
 QMOE_PATH_DECODE = 1
 QMOE_PATH_GROUPED = 2
+QMOE_PATH_GROUPED_ROUTE_TILES = 3
+QMOE_PATH_GROUPED_WS = 4
 QMOE_FORMAT_INT = 0
 QMOE_FORMAT_MXFP4 = 1
 QMOE_FORMAT_NVFP4 = 2

@@ -21,6 +21,7 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 }  // namespace
 
 int resolve_path(const qmoe_problem& p) {
+  if (p.path == QMOE_PATH_GROUPED_ROUTE_TILES || p.path == QMOE_PATH_GROUPED_WS) return QMOE_PATH_GROUPED;
   if (p.path != QMOE_PATH_AUTO) return p.path;
   const int64_t R = p.T * (int64_t)p.top_k;
   if (p.T <= 8) return QMOE_PATH_DECODE;
@@ -49,7 +50,7 @@ qmoe_status check_problem(const qmoe_problem* p) {
   if (p->hidden % 32 || p->inter % 32) return QMOE_ERR_UNSUPPORTED;
   if (p->num_experts > kMaxExperts || p->top_k > kMaxTopK) return QMOE_ERR_UNSUPPORTED;
   if (p->dtype != QMOE_BF16 && p->dtype != QMOE_FP16) return QMOE_ERR_UNSUPPORTED;
-  if (p->path < QMOE_PATH_AUTO || p->path > QMOE_PATH_GROUPED) return QMOE_ERR_UNSUPPORTED;
+  if (p->path < QMOE_PATH_AUTO || p->path > QMOE_PATH_GROUPED_WS) return QMOE_ERR_UNSUPPORTED;
   if ((int64_t)p->T * p->top_k > (int64_t)INT32_MAX / 2) return QMOE_ERR_UNSUPPORTED;
   const int path = resolve_path(*p);
   if (path == QMOE_PATH_DECODE) {
@@ -58,6 +59,7 @@ qmoe_status check_problem(const qmoe_problem* p) {
   } else {
     const int m = p->bits == 3 ? 128 : 64;
     if (p->hidden % m || p->inter % m) return QMOE_ERR_UNSUPPORTED;
+    if (p->path == QMOE_PATH_GROUPED_WS && !grouped_ws_applies(p->hidden, p->inter)) return QMOE_ERR_UNSUPPORTED;
   }
   return QMOE_OK;
 }
@@ -74,6 +76,9 @@ Problem to_internal(const qmoe_problem& q) {
   p.dtype = q.dtype;
   p.path = resolve_path(q);
   p.format = q.format;
+  // the grouped kernel: weights-stationary tiles of kTileWs routes, or route tiles of kTileM
+  const int force = q.path == QMOE_PATH_GROUPED_ROUTE_TILES ? 1 : q.path == QMOE_PATH_GROUPED_WS ? 2 : 0;
+  p.tile_m = p.path == QMOE_PATH_GROUPED && grouped_ws(p.R(), p.E, p.H, p.I, force) ? kTileWs : kTileM;
   return p;
 }
 
@@ -97,7 +102,7 @@ size_t workspace_layout(const Problem& p, bool grouped, void* base, Workspace* w
   w.sorted_route = static_cast<int32_t*>(take(sizeof(int32_t) * R));
   w.active = static_cast<int32_t*>(take(sizeof(int32_t) * (p.E + kPermuteChunk / kDecodeChunk)));
   w.counters = static_cast<int32_t*>(take(sizeof(int32_t) * 4));
-  w.max_tiles = (R + kTileM - 1) / kTileM + p.E;
+  w.max_tiles = (R + kTileWs - 1) / kTileWs + p.E;   // tiles of either size
   w.tiles = static_cast<int32_t*>(take(sizeof(int32_t) * 2 * w.max_tiles));
   w.nchunks = (R + kPermuteChunk - 1) / kPermuteChunk;
   w.chunk_hist = static_cast<int32_t*>(take(sizeof(int32_t) * w.nchunks * p.E));

@@ -31,6 +31,15 @@
 // FP16 store in the K-order permutation of the fc2 operand. fc2 epilogue: FP32
 // rows scaled by the routing weight, stored per route id for the combine.
 //
+// Weights-stationary works (WS; few routes per expert, e.g. a mid-size batch):
+// tiles of at most 128 sorted rows of one expert, and the operands trade
+// places. The dequantised tile of 128 weight rows is the MMA's A (M = 128) and
+// the tile's routes are B, N = the routes rounded up to 16, copied in boxes of
+// 16 rows; D holds weight rows on the TMEM lanes and routes on the columns. An
+// expert with a handful of routes then pays for 16-route MMA columns instead of
+// a 128-row route tile, the activation ring is a quarter the size, and the code
+// ring is deep enough to keep the weight stream in flight.
+//
 // Every mbarrier wait gives up after a bounded time: the CTA then records an
 // error code in the workspace, drains its copies and MMAs in flight, frees its
 // TMEM and returns.
@@ -58,28 +67,49 @@ static_assert(kBM == kTileM, "the grouping kernels cut tiles of kTileM sorted ro
 // scales a multiple of 16 bytes): one [BN rows][8 scales] box covers 8 blocks
 // along K (a "scale span" of 8*block/BK stages) in a ring of two; otherwise the
 // producer warp loads scales and zero points per stage and stores FP16 words.
-template <int BITS, bool TSC, bool FC1>
+// WS: the weights-stationary form (see the top of the file).
+template <int BITS, bool TSC, bool FC1, bool WS>
 struct Cfg {
-  static constexpr int BK = BITS == 3 ? 128 : 64;     // K per stage
-  // Weight rows per tile (MMA N). With 128 (INT3), a tile's two accumulators
-  // take 256 TMEM columns, so two tiles' accumulators fit (ACC = 2) and the
-  // epilogue of one tile overlaps the MMAs of the next. INT4 / INT2 keep 256 and
-  // one accumulator buffer: 128 there (double-buffered) measured slower for fc2,
-  // as every activation tile then feeds half as many MMAs.
+  // K per stage. INT3 takes 128 (a 32-code unit of INT3 is 12 bytes; a code copy
+  // must be a multiple of 16 bytes per row).
+  static constexpr int BK = BITS == 3 ? 128 : 64;
+  // Weight rows per tile (MMA N; WS: M, as two 128-row halves). With 128 (INT3
+  // route tiles), a tile's two accumulators take 256 TMEM columns, so two tiles'
+  // accumulators fit (ACC = 2) and the epilogue of one tile overlaps the MMAs of
+  // the next. INT4 / INT2 keep 256 and one accumulator buffer: 128 there
+  // (double-buffered) measured slower for fc2, as every activation tile then
+  // feeds half as many MMAs. WS: the same rows, as 128-row halves (M = 128 each)
+  // with accumulators of up to 128 route columns, double-buffered; every stage's
+  // fixed cost (its barrier hand-offs) is spread over 256 rows for INT4 / INT2,
+  // which measured worth more than the deeper rings 128 rows would leave room
+  // for.
   static constexpr int BN = BITS == 3 ? 128 : 256;
-  static constexpr int ACC = 4 * BN <= 512 ? 2 : 1;   // accumulator buffers
+  static constexpr int HALVES = BN / kSubM;           // WS: accumulators per tile
+  static constexpr int AROWS = WS ? kTileWs : kBM;    // activation rows per stage
+  static constexpr int ACC = WS ? 2 : (4 * BN <= 512 ? 2 : 1);   // accumulator buffers
   // Three rings: activation tiles (read by the MMAs), code tiles (read by the
   // dequantisers) and dequantised B tiles (written by the dequantisers, read by
   // the MMAs). The B ring only spans dequantisation to MMA; the two rings fed by
-  // copies are deeper, so that more copies are in flight per SM.
+  // copies are deeper, so that more copies are in flight per SM. WS: the small
+  // activation tiles leave room for a code ring of 8 (INT3) or 12 stages.
   static constexpr int SA = BITS == 3 ? 2 : 3;
-  static constexpr int SC = BITS == 3 ? 2 : (BITS == 4 ? 3 : 4);
+  static constexpr int SC = WS ? (BITS == 3 ? 4 : 2) : (BITS == 3 ? 2 : (BITS == 4 ? 3 : 4));
   static constexpr int SB = BITS == 3 ? 2 : 3;
   static constexpr int SUB = BK / 64;                 // 64-wide swizzle atoms per stage
-  static constexpr int A_BYTES = kBM * BK * 2;
+  // K per code copy. A weight row's codes are read in pieces of CK * BITS / 8
+  // bytes; WS copies 256 K at once (128 bytes of INT4, 96 of INT3, 64 of INT2 per
+  // row), which the dequantisers take as R = CK / BK stages, both groups sharing
+  // each copy. (Each expert's weights there come from DRAM once; pieces of 32
+  // bytes per row, spread over a whole tile's time, held its weight stream to a
+  // fraction of the bandwidth.) Route tiles re-read each weight tile from L2 and
+  // keep one copy per stage.
+  static constexpr int CK = WS ? kWsCodeK : BK;
+  static constexpr int R = CK / BK;
+  static constexpr int A_BYTES = AROWS * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int CODE_ROW = BK * BITS / 8;      // bytes of codes per weight row per stage
-  static constexpr int C_BYTES = BN * CODE_ROW;
+  static constexpr int CODE_ROW_C = CK * BITS / 8;    // bytes per weight row per code copy
+  static constexpr int C_BYTES = BN * CODE_ROW_C;
   static constexpr int UNIT_BYTES = 4 * BITS;         // 32 codes
   static constexpr int UNITS_PER_ROW = BK / 32;
   static constexpr int UNITS = BN * UNITS_PER_ROW;
@@ -90,11 +120,13 @@ struct Cfg {
   static constexpr int B_OFF = A_OFF + SA * A_BYTES;
   static constexpr int C_OFF = B_OFF + SB * B_BYTES;
   static constexpr int S_OFF = C_OFF + SC * C_BYTES;
-  static constexpr int BAR_OFF = S_OFF + (TSC ? 2 * SC_BYTES : SC * S_BYTES);
+  static constexpr int BAR_OFF = S_OFF + (TSC ? 2 * SC_BYTES : SC * R * S_BYTES);
   static constexpr int NBARS = 2 * (SA + SC + SB) + 2 * ACC + 4;
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;   // barriers + TMEM address + alignment slack
-  static_assert(8 * NBARS + 8 + 4 * SC <= 256, "barrier area");
-  static constexpr int TMEM_COLS = 2 * BN * ACC;      // two accumulators per tile
+  static constexpr int BAR_BYTES = WS ? 512 : 256;    // barriers, TMEM address, flags, fill words
+  static constexpr int SMEM = BAR_OFF + BAR_BYTES + 1024;   // + alignment slack
+  static_assert(8 * NBARS + 8 + 4 * SC <= BAR_BYTES, "barrier area");
+  // two accumulators per tile; WS: one per 128 weight rows, of kTileWs columns
+  static constexpr int TMEM_COLS = WS ? ACC * HALVES * kTileWs : 2 * BN * ACC;
   static_assert(UNITS % kDequantThreads == 0, "units must split evenly");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -336,14 +368,14 @@ __device__ __forceinline__ void dequant_unit_fast(const uint32_t* w, uint32_t zp
 }
 
 
-template <int BITS, bool FC1, bool TSC>
+template <int BITS, bool FC1, bool TSC, bool WS>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_s, GemmArgs g) {
   pdl_wait();
   pdl_trigger();
-  using C = Cfg<BITS, TSC, FC1>;
+  using C = Cfg<BITS, TSC, FC1, WS>;
   constexpr int SA = C::SA, SB = C::SB, SC = C::SC;
   const Workspace& ws = g.ws;
   const Problem& p = g.p;
@@ -388,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < SC; ++s) {
       mbar_init(bar_cfull(s), TSC ? 1 : 1 + 32);  // the copy issue [+ 32 scale writers]
-      mbar_init(bar_cempty(s), kDequantThreads);
+      mbar_init(bar_cempty(s), kDequantThreads * C::R);   // every stage of the copy
       cfill[s] = -1;
     }
     for (int s = 0; s < SB; ++s) {
@@ -422,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int nblk = K / p.block;
   const int span = 8 * p.block / C::BK;          // stages per scale box (TSC)
+  const int kcopies = ksteps / C::R;             // code copies per tile (K is a multiple of CK)
   auto tile_of = [&](int j, int& e, int& row0, int& n0) {
     const int w = blockIdx.x + j * gridDim.x;
     const int mt = w / n_tiles_n;
@@ -435,8 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto halves_of = [&](int e, int row0) { return ws.offsets[e + 1] - row0 > kSubM ? 2 : 1; };
 
   if (warp == 0) {
-    // ---------------- code producer: per stage the code tile (lane 0) and either a
-    // scale box every `span` stages (lane 0) or the stage's scales (all lanes)
+    // ---------------- code producer: per code copy (R stages) the code tile (lane 0)
+    // and either a scale box every `span` stages (lane 0) or the stages' scales
+    // (all lanes)
     int issued = 0, spans = 0;
     bool go = true;
     for (int j = 0; j < my_works && go; ++j) {
@@ -444,90 +478,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_of(j, e, row0, n0);
       const int64_t wrow_base = (int64_t)e * N + n0;
       const int64_t wrow_end = (int64_t)p.E * N;
-      for (int i = 0; i < ksteps; ++i) {
-        const int it = j * ksteps + i;           // stage sequence number across tiles
-        const int s = it % SC;
-        const uint32_t ph = (uint32_t)(it / SC) & 1u;
+      for (int ci = 0; ci < kcopies; ++ci) {
+        const int ic = j * kcopies + ci;         // copy sequence number across tiles
+        const int s = ic % SC;
+        const uint32_t ph = (uint32_t)(ic / SC) & 1u;
         int ok = 1;
         if (lane == 0) ok = mbar_wait(bar_cempty(s), ph ^ 1u, abort_flag, launch_err) ? 1 : 0;
-        const int k0 = i * C::BK;
-        if (TSC && i % span == 0) {
-          // next scale box, into the ring slot the dequantisers released
-          const int m = spans++;
-          if (lane == 0 && ok) {
-            if (m >= 2 && !mbar_wait(bar_sempty(m & 1), (uint32_t)((m - 2) >> 1) & 1u, abort_flag, launch_err))
-              ok = 0;
-            else {
-              mbar_expect_tx(bar_sfull(m & 1), C::SC_BYTES);
-              tma_load_2d(sbase + C::S_OFF + (m & 1) * C::SC_BYTES, &tmap_s, bar_sfull(m & 1), k0 / p.block,
-                          e * N + n0);
+        if constexpr (TSC) {
+          // the scale boxes of the copy's stages that start a span, into the ring
+          // slot the dequantisers released
+#pragma unroll
+          for (int sub = 0; sub < C::R; ++sub) {
+            const int i = ci * C::R + sub;
+            if (i % span != 0) continue;
+            const int m = spans++;
+            if (lane == 0 && ok) {
+              if (m >= 2 && !mbar_wait(bar_sempty(m & 1), (uint32_t)((m - 2) >> 1) & 1u, abort_flag, launch_err))
+                ok = 0;
+              else {
+                mbar_expect_tx(bar_sfull(m & 1), C::SC_BYTES);
+                tma_load_2d(sbase + C::S_OFF + (m & 1) * C::SC_BYTES, &tmap_s, bar_sfull(m & 1),
+                            i * C::BK / p.block, e * N + n0);
+              }
             }
           }
         }
         if (__shfl_sync(0xffffffffu, ok, 0) == 0) { go = false; break; }
         ++issued;
         if (lane == 0) {
-          cfill[s] = it;
+          cfill[s] = ic;
           mbar_expect_tx(bar_cfull(s), C::C_BYTES);
-          tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_cfull(s), k0 * BITS / 8, e * N + n0);
+          tma_load_2d(sbase + C::C_OFF + s * C::C_BYTES, &tmap_q, bar_cfull(s), ci * C::CODE_ROW_C, e * N + n0);
         }
         if constexpr (TSC) continue;
-        uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + s * C::S_BYTES);
-        // per batch of 8: all loads first (independent, no branches), then convert and store
-        constexpr int PER_LANE = C::UNITS / 32;
-        constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;
-        static_assert(PER_LANE % BATCH == 0, "scale batches");
-        if (BITS == 4 && p.format != QMOE_FORMAT_INT) {
-          // FP4: the 8-bit scales of each unit of 32 codes (one E8M0, or two E4M3 for
-          // the 16-wide NVFP4 blocks) as two FP16 words, the first 16 codes' low
-          const uint8_t* s8 = reinterpret_cast<const uint8_t*>(g.scales);
-          const bool nv = p.format == QMOE_FORMAT_NVFP4;
+#pragma unroll 1
+        for (int sub = 0; sub < C::R; ++sub) {
+          const int k0 = (ci * C::R + sub) * C::BK;
+          uint32_t* st = reinterpret_cast<uint32_t*>(smem + C::S_OFF + (s * C::R + sub) * C::S_BYTES);
+          // per batch of 8: all loads first (independent, no branches), then convert and store
+          constexpr int PER_LANE = C::UNITS / 32;
+          constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;
+          static_assert(PER_LANE % BATCH == 0, "scale batches");
+          if (BITS == 4 && p.format != QMOE_FORMAT_INT) {
+            // FP4: the 8-bit scales of each unit of 32 codes (one E8M0, or two E4M3 for
+            // the 16-wide NVFP4 blocks) as two FP16 words, the first 16 codes' low
+            const uint8_t* s8 = reinterpret_cast<const uint8_t*>(g.scales);
+            const bool nv = p.format == QMOE_FORMAT_NVFP4;
+#pragma unroll 1
+            for (int q0 = 0; q0 < PER_LANE; q0 += BATCH) {
+              // the batch's loads first (independent), then convert and store
+              uint32_t b0[BATCH], b1[BATCH];
+#pragma unroll
+              for (int q = 0; q < BATCH; ++q) {
+                const int u = lane + 32 * (q0 + q);
+                const int r = u / C::UNITS_PER_ROW, jj = u % C::UNITS_PER_ROW;
+                const int64_t wr = min(wrow_base + r, wrow_end - 1);
+                const int64_t idx = wr * nblk + (k0 + 32 * jj) / p.block;
+                b0[q] = __ldg(s8 + idx);
+                b1[q] = nv ? __ldg(s8 + idx + 1) : 0u;
+              }
+#pragma unroll
+              for (int q = 0; q < BATCH; ++q) {
+                const int u = lane + 32 * (q0 + q);
+                const int r = u / C::UNITS_PER_ROW;
+                // the raw scale bytes; the dequantisers convert them (rows past the
+                // array: a zero E4M3 / the smallest E8M0 with no rows to scale)
+                st[u] = wrow_base + r < wrow_end ? (b0[q] | ((nv ? b1[q] : b0[q]) << 8)) : 0u;
+              }
+            }
+            continue;
+          }
 #pragma unroll 1
           for (int q0 = 0; q0 < PER_LANE; q0 += BATCH) {
-            // the batch's loads first (independent), then convert and store
-            uint32_t b0[BATCH], b1[BATCH];
+            uint16_t sv[BATCH];
+            uint8_t zv[BATCH];
 #pragma unroll
             for (int q = 0; q < BATCH; ++q) {
               const int u = lane + 32 * (q0 + q);
               const int r = u / C::UNITS_PER_ROW, jj = u % C::UNITS_PER_ROW;
-              const int64_t wr = min(wrow_base + r, wrow_end - 1);
+              const int64_t wr = min(wrow_base + r, wrow_end - 1);   // rows past the array: masked below
               const int64_t idx = wr * nblk + (k0 + 32 * jj) / p.block;
-              b0[q] = __ldg(s8 + idx);
-              b1[q] = nv ? __ldg(s8 + idx + 1) : 0u;
+              sv[q] = __ldg(g.scales + idx);
+              zv[q] = g.zp ? __ldg(g.zp + idx) : (uint8_t)(1u << (BITS - 1));
             }
 #pragma unroll
             for (int q = 0; q < BATCH; ++q) {
               const int u = lane + 32 * (q0 + q);
               const int r = u / C::UNITS_PER_ROW;
-              // the raw scale bytes; the dequantisers convert them (rows past the
-              // array: a zero E4M3 / the smallest E8M0 with no rows to scale)
-              st[u] = wrow_base + r < wrow_end ? (b0[q] | ((nv ? b1[q] : b0[q]) << 8)) : 0u;
+              const uint16_t sh = p.dtype == QMOE_BF16
+                                      ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sv[q] << 16)))
+                                      : sv[q];
+              st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
             }
-          }
-          mbar_arrive(bar_cfull(s));
-          continue;
-        }
-#pragma unroll 1
-        for (int q0 = 0; q0 < PER_LANE; q0 += BATCH) {
-          uint16_t sv[BATCH];
-          uint8_t zv[BATCH];
-#pragma unroll
-          for (int q = 0; q < BATCH; ++q) {
-            const int u = lane + 32 * (q0 + q);
-            const int r = u / C::UNITS_PER_ROW, jj = u % C::UNITS_PER_ROW;
-            const int64_t wr = min(wrow_base + r, wrow_end - 1);   // rows past the array: masked below
-            const int64_t idx = wr * nblk + (k0 + 32 * jj) / p.block;
-            sv[q] = __ldg(g.scales + idx);
-            zv[q] = g.zp ? __ldg(g.zp + idx) : (uint8_t)(1u << (BITS - 1));
-          }
-#pragma unroll
-          for (int q = 0; q < BATCH; ++q) {
-            const int u = lane + 32 * (q0 + q);
-            const int r = u / C::UNITS_PER_ROW;
-            const uint16_t sh = p.dtype == QMOE_BF16
-                                    ? __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)sv[q] << 16)))
-                                    : sv[q];
-            st[u] = wrow_base + r < wrow_end ? ((uint32_t)sh | ((uint32_t)zv[q] << 16)) : 0u;
           }
         }
         mbar_arrive(bar_cfull(s));
@@ -550,7 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < my_works && go; ++j) {
         int e, row0, n0;
         tile_of(j, e, row0, n0);
-        const int nh = halves_of(e, row0);
+        const int nh = WS ? 0 : halves_of(e, row0);
+        // WS: the tile's routes in boxes of 16 rows (the MMA's N in steps of 16)
+        const int nb = WS ? (min(kTileWs, ws.offsets[e + 1] - row0) + 15) / 16 : 0;
         for (int i = 0; i < ksteps; ++i) {
           const int it = j * ksteps + i;
           const int s = it % SA;
@@ -558,14 +602,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_aempty(s), ph ^ 1u, abort_flag, launch_err)) { go = false; break; }
           ++issued;
           const int k0 = i * C::BK;
-          mbar_expect_tx(bar_afull(s), (uint32_t)(C::A_BYTES / 2 * nh));
+          if constexpr (WS) {
+            mbar_expect_tx(bar_afull(s), (uint32_t)(C::SUB * nb * 2048));
 #pragma unroll
-          for (int sub = 0; sub < C::SUB; ++sub)
+            for (int sub = 0; sub < C::SUB; ++sub)
+              for (int b = 0; b < nb; ++b)
+                tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (C::AROWS * 128) + b * 2048, &tmap_a,
+                            bar_afull(s), k0 + 64 * sub, row0 + 16 * b);
+          } else {
+            mbar_expect_tx(bar_afull(s), (uint32_t)(C::A_BYTES / 2 * nh));
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              if (h < nh)
-                tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
-                            bar_afull(s), k0 + 64 * sub, row0 + h * kSubM);
+            for (int sub = 0; sub < C::SUB; ++sub)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if (h < nh)
+                  tma_load_2d(sbase + C::A_OFF + s * C::A_BYTES + sub * (kBM * 128) + h * (kSubM * 128), &tmap_a,
+                              bar_afull(s), k0 + 64 * sub, row0 + h * kSubM);
+          }
         }
       }
       if (*abort_flag)
@@ -587,10 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait(bar_drained(buf), (uint32_t)(j / C::ACC - 1) & 1u, abort_flag, launch_err))
           break;
         tc_fence_after();
-        const uint32_t acc0 = tmem + (uint32_t)(buf * 2 * C::BN);
+        const uint32_t acc0 = tmem + (uint32_t)(WS ? buf * C::HALVES * kTileWs : buf * 2 * C::BN);
         int e_t, row0_t, n0_t;
         tile_of(j, e_t, row0_t, n0_t);
-        const int nh = halves_of(e_t, row0_t);
+        const int nh = WS ? 0 : halves_of(e_t, row0_t);
+        // WS: M = the 128 dequantised weight rows, N = the tile's routes rounded up to 16
+        const uint32_t idesc_ws =
+            WS ? idesc_f16(kSubM, 16 * ((min(kTileWs, ws.offsets[e_t + 1] - row0_t) + 15) / 16)) : 0u;
         for (int i = 0; i < ksteps; ++i) {
           const int it = j * ksteps + i;
           const int sa = it % SA, sb = it % SB;
@@ -603,11 +659,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             const int sub = kk / 4, off = (kk % 4) * 32;
             const uint64_t bdesc = sw128_desc(b_base + sub * (C::BN * 128) + off);
+            if constexpr (WS) {
+              // each 128-row half of the weight tile against the same routes
+              const uint64_t adesc = sw128_desc(a_base + sub * (C::AROWS * 128) + off);
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              if (h < nh)
-                tc_mma(acc0 + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
-                       idesc, (i | kk) != 0);
+              for (int h = 0; h < C::HALVES; ++h)
+                tc_mma(acc0 + h * kTileWs, sw128_desc(b_base + sub * (C::BN * 128) + h * (kSubM * 128) + off), adesc,
+                       idesc_ws, (i | kk) != 0);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if (h < nh)
+                  tc_mma(acc0 + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
+                         idesc, (i | kk) != 0);
+            }
           }
           pending = true;
           tc_commit(bar_aempty(sa));
@@ -649,13 +714,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < ksteps; ++i) {
         const int it = j * ksteps + i;
         if ((it & 1) != grp) continue;
-        const int cs = it % SC, bs = it % SB;
-        // With an odd ring the slot's previous stage belongs to the other group. A
-        // parity wait would also pass while that stage's copy is still open, so wait
-        // first until the producer has issued this stage's copy into the slot: it
-        // does so only after the previous stage was read, i.e. after its copy landed.
-        if (SC % 2 == 1 && !word_wait(cfill + cs, it, abort_flag, launch_err)) { go = false; break; }
-        if (!mbar_wait(bar_cfull(cs), (uint32_t)(it / SC) & 1u, abort_flag, launch_err)) { go = false; break; }
+        const int sub = i % C::R;                // stage within its code copy
+        const int ic = j * kcopies + i / C::R;   // the copy's sequence number
+        const int cs = ic % SC, bs = it % SB;
+        // With one stage per copy and an odd ring the slot's previous copy belongs
+        // to the other group. A parity wait would also pass while that copy is
+        // still open, so wait first until the producer has issued this copy into
+        // the slot: it does so only after the previous one was read, i.e. after it
+        // landed. With R >= 2 (even) both groups read every copy, so each has seen
+        // the slot's previous phase complete.
+        if (C::R == 1 && SC % 2 == 1 && !word_wait(cfill + cs, ic, abort_flag, launch_err)) { go = false; break; }
+        if (!mbar_wait(bar_cfull(cs), (uint32_t)(ic / SC) & 1u, abort_flag, launch_err)) { go = false; break; }
         const int m_cur = j * nbox + i / span;   // scale box of this stage (TSC), in issue order
         if (TSC && m_cur != box_seen) {
           box_seen = m_cur;
@@ -672,14 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [BN rows][8] scales of this box; this stage's first block within it
         const uint16_t* sbox = reinterpret_cast<const uint16_t*>(smem + C::S_OFF + (m_cur & 1) * C::SC_BYTES);
         const int b_first = (i % span) * C::BK / p.block;
-        const uint8_t* codes = smem + C::C_OFF + cs * C::C_BYTES;
-        const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + cs * C::S_BYTES);
+        const uint8_t* codes = smem + C::C_OFF + cs * C::C_BYTES + sub * C::CODE_ROW;
+        const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + C::S_OFF + (cs * C::R + sub) * C::S_BYTES);
         uint8_t* bt = smem + C::B_OFF + bs * C::B_BYTES;
 #pragma unroll
         for (int u = 0; u < C::UNITS_PER_THREAD; ++u) {
           const int unit = t + kDequantThreads * u;
           const int r = unit / C::UNITS_PER_ROW, jj = unit % C::UNITS_PER_ROW;
-          const uint8_t* src = codes + r * C::CODE_ROW + jj * C::UNIT_BYTES;
+          const uint8_t* src = codes + r * C::CODE_ROW_C + jj * C::UNIT_BYTES;
           uint32_t w[BITS];
           if constexpr (BITS == 4) {
             const uint4 v = *reinterpret_cast<const uint4*>(src);
@@ -731,6 +800,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i + 2 >= box_end) mbar_arrive_cnt(bar_sempty(m_cur & 1), box_end - box0 >= 2 ? 1u : 2u);
         }
       }
+    }
+  } else if constexpr (WS) {
+    // ---------------- epilogue (warps 18..21), weights-stationary: in accumulator
+    // h (of C::HALVES), TMEM lane 32 (w % 4) + lane holds weight row f = n0 +
+    // 128 h + 32 (w % 4) + lane of the tile, column c its route row0 + c. Each route's
+    // factors are loaded by one lane and handed to the others by shuffles.
+    const int quarter = warp & 3;
+    for (int j = 0; j < my_works; ++j) {
+      int e, row0, n0;
+      tile_of(j, e, row0, n0);
+      const int nr = min(kTileWs, ws.offsets[e + 1] - row0);
+      const int f0 = n0 + quarter * 32 + lane;   // this thread's weight row in half 0
+      // FP4: the factor the FP16 operands left out (MXFP4 2^ref, NVFP4 global scale)
+      float ef = 1.0f;
+      if constexpr (BITS == 4) {
+        if (p.format == QMOE_FORMAT_MXFP4) ef = ldexpf(1.0f, mx_ref(g.scales, e, N, g.K / p.block));
+        if (p.format == QMOE_FORMAT_NVFP4 && (FC1 ? p.g1 : p.g2)) ef = __ldg((FC1 ? p.g1 : p.g2) + e);
+      }
+      const float hn = h_norm(p, e);
+      float2 bq[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+      if (FC1 && p.b1)
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h)
+          if (f0 + kSubM * h < N) bq[h] = fc1_bias_pair(p, e, (f0 + kSubM * h) >> 1);
+      const int buf = j % C::ACC;
+      if (!mbar_wait(bar_accum(buf), (uint32_t)(j / C::ACC) & 1u, abort_flag, launch_err)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * C::HALVES * kTileWs);
+      for (int c0 = 0; c0 < nr; c0 += 32) {
+        const int c = c0 + lane;
+        const bool ok = c < nr;
+        const int rid_l = ok ? ws.sorted_route[row0 + c] : 0;
+        const float sig_l = ok ? ws.tok_scale[rid_l / p.k] : 1.0f;
+        const float inv1_l = 1.0f / sig_l;
+        const float inv_l = ef * inv1_l;
+#pragma unroll 1
+        for (int h = 0; h < C::HALVES; ++h) {
+          const int f = f0 + kSubM * h;
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(kTileWs * h + c0), v);
+          if constexpr (FC1) {
+            // rows 2m (gate) and 2m + 1 (up) of SwiGLU unit f / 2 sit in lanes 2m and
+            // 2m + 1: the even lane finishes routes c0 .. c0 + 15, the odd one the rest
+            const float ss_l = sig_l * sig_l * hn;
+            const bool odd = lane & 1;
+            const int jj = f >> 1;
+            constexpr int G = BITS == 4 ? 8 : 16;
+            const int col = (BITS == 4 && p.format != QMOE_FORMAT_INT) ? jj : permuted_pos(jj, G);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[16 + i], 1);
+              const int cc = odd ? 16 + i : i;
+              const float inv = __shfl_sync(0xffffffffu, inv_l, cc);
+              const float ss = __shfl_sync(0xffffffffu, ss_l, cc);
+              // SwiGLU with CUDA's fast exp and divide; the result is rounded to FP16
+              const float gt = __uint_as_float(odd ? got : v[i]) * inv + bq[h].x;
+              const float ut = __uint_as_float(odd ? v[16 + i] : got) * inv + bq[h].y;
+              if (c0 + cc < nr && f < N)
+                ws.h16[(int64_t)(row0 + c0 + cc) * p.I + col] =
+                    __half_as_ushort(__float2half_rn(__fdividef(gt, 1.0f + __expf(-gt)) * ut * ss));
+            }
+          } else {
+            const float fct_l = ok ? inv_l * inv1_l / hn * ws.topk_w[rid_l] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int rid = __shfl_sync(0xffffffffu, rid_l, i);
+              const float fct = __shfl_sync(0xffffffffu, fct_l, i);
+              if (c0 + i < nr && f < N) ws.y[(int64_t)rid * p.H + f] = __uint_as_float(v[i]) * fct;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_drained(buf));             // the accumulators may be overwritten
     }
   } else {
     // ---------------- epilogue (warps 18..21): warp w reads TMEM lanes 32 (w % 4) ..
@@ -847,21 +990,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-template <int BITS, bool FC1, bool TSC>
+template <int BITS, bool FC1, bool TSC, bool WS>
 cudaError_t launch_gemm_t(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
                           const Workspace& ws, cudaStream_t s) {
-  using C = Cfg<BITS, TSC, FC1>;
+  using C = Cfg<BITS, TSC, FC1, WS>;
   const int N = FC1 ? 2 * p.I : p.H;
   const int K = FC1 ? p.H : p.I;
   const int64_t R = p.R();
   const uint16_t* A = FC1 ? ws.x16s : ws.h16;
   CUtensorMap ta, tq, tsc;
+  // activation boxes: 64 K x 128 rows (a route tile's half), WS 64 K x 16 routes
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2,
-                   64, kSubM, CU_TENSOR_MAP_SWIZZLE_128B))
+                   64, WS ? 16 : kSubM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const uint64_t row_bytes = (uint64_t)K * BITS / 8;
   if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, row_bytes, (uint64_t)p.E * N, row_bytes,
-                   C::CODE_ROW, C::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   C::CODE_ROW_C, C::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (TSC) {
     // [E*N rows][K/block] 16-bit scales, boxes of 8 scales x BN rows
@@ -872,25 +1016,30 @@ cudaError_t launch_gemm_t(const Problem& p, const uint8_t* q, const void* scales
   } else {
     tsc = tq;                                    // not read
   }
-  const cudaError_t err = ensure_smem_optin(grouped_gemm_kernel<BITS, FC1, TSC>, C::SMEM);
+  const cudaError_t err = ensure_smem_optin(grouped_gemm_kernel<BITS, FC1, TSC, WS>, C::SMEM);
   if (err != cudaSuccess) return err;
   GemmArgs g{static_cast<const uint16_t*>(scales), zp, N, K, p, ws};
   // persistent: one CTA per SM, each walking its share of the (m-tile, n-tile) list
   const int sms = device_sm_count();
   const int64_t works_max = ws.max_tiles * ((N + C::BN - 1) / C::BN);
   dim3 grid((unsigned)(works_max < sms ? works_max : sms));
-  return launch_pdl(grouped_gemm_kernel<BITS, FC1, TSC>, grid, dim3(kThreads), C::SMEM, s, ta, tq, tsc, g);
+  return launch_pdl(grouped_gemm_kernel<BITS, FC1, TSC, WS>, grid, dim3(kThreads), C::SMEM, s, ta, tq, tsc, g);
 }
 
 // Scales by bulk tensor copies when there are no zero points and a row of
-// scales is a multiple of 16 bytes; the producer-warp path otherwise.
+// scales is a multiple of 16 bytes; the producer-warp path otherwise. The
+// weights-stationary kernel where the routing step cut tiles of kTileWs rows.
 template <int BITS, bool FC1>
 cudaError_t launch_gemm(const Problem& p, const uint8_t* q, const void* scales, const uint8_t* zp,
                         const Workspace& ws, cudaStream_t s) {
   const int K = FC1 ? p.H : p.I;
-  if (!zp && p.format == QMOE_FORMAT_INT && (K / p.block) % 8 == 0)
-    return launch_gemm_t<BITS, FC1, true>(p, q, scales, zp, ws, s);
-  return launch_gemm_t<BITS, FC1, false>(p, q, scales, zp, ws, s);
+  const bool tsc = !zp && p.format == QMOE_FORMAT_INT && (K / p.block) % 8 == 0;
+  if (p.tile_m == kTileWs)
+    return tsc ? launch_gemm_t<BITS, FC1, true, true>(p, q, scales, zp, ws, s)
+               : launch_gemm_t<BITS, FC1, false, true>(p, q, scales, zp, ws, s);
+  if (p.tile_m != kTileM) return cudaErrorInvalidValue;
+  return tsc ? launch_gemm_t<BITS, FC1, true, false>(p, q, scales, zp, ws, s)
+             : launch_gemm_t<BITS, FC1, false, false>(p, q, scales, zp, ws, s);
 }
 
 }  // namespace

@@ -28,6 +28,7 @@ constexpr int kPermuteChunk = 512;    // routes per block in the grouping kernel
 constexpr int kDecodeMaxT = 64;
 constexpr int kDecodeChunk = 8;       // routes of one expert per MMA N-fragment (generic decode kernel)
 constexpr int kTileM = 256;           // rows (routes) per grouped-GEMM tile
+constexpr int kTileWs = 128;          // rows per tile of the weights-stationary grouped GEMM
 constexpr int kDtabInts = 8;          // ints per decode-table entry
 constexpr int kDtabMax = kPermuteChunk;  // entries: at most one per route
 
@@ -48,7 +49,7 @@ struct Workspace {
   int32_t* counters;      // [4]      [0] active experts (decode path: chunks), [1] grouped
                           //   tiles, [2] error flag,
                           //          [3] decode-table entries
-  int32_t* tiles;         // [2*max_tiles] (expert, first sorted row) of each kTileM-row tile
+  int32_t* tiles;         // [2*max_tiles] (expert, first sorted row) of each tile (Problem::tile_m rows)
   int32_t* chunk_hist;    // [nchunks][E] per-chunk expert counts, then chunk bases
   int32_t* dtab;          // [kDtabMax][kDtabInts] decode table: one entry per (active expert,
                           //   pair of its routes): expert, first sorted row of the pair, routes in
@@ -84,11 +85,28 @@ struct Problem {
   const float* g2;
   int logits_after_wait;          // the router logits are the previous kernel's output: read
                                   //   them only after pdl_wait()
+  int tile_m;                     // grouped path: sorted rows per tile, kTileM (route tiles) or
+                                  //   kTileWs (weights-stationary kernel; grouped_ws)
   __host__ __device__ int64_t R() const { return T * (int64_t)k; }
 };
 
 // The path a problem runs on (QMOE_PATH_DECODE or QMOE_PATH_GROUPED; AUTO resolved).
 int resolve_path(const qmoe_problem& p);
+
+// Whether the grouped path runs the weights-stationary kernel (an expert's
+// routes on the MMA N side) rather than route tiles: when the routes per expert
+// are few on average (R <= kWsRoutesPerExpert * E), or as `force` asks
+// (0 automatic, 1 route tiles, 2 weights-stationary: QMOE_PATH_GROUPED_ROUTE_TILES
+// and QMOE_PATH_GROUPED_WS). It reads codes in copies of kWsCodeK along K, so
+// hidden and inter must be multiples of kWsCodeK.
+constexpr int kWsRoutesPerExpert = 32;
+constexpr int kWsCodeK = 256;
+__host__ __device__ inline bool grouped_ws_applies(int H, int I) { return H % kWsCodeK == 0 && I % kWsCodeK == 0; }
+__host__ __device__ inline bool grouped_ws(int64_t R, int E, int H, int I, int force) {
+  if (force == 1 || !grouped_ws_applies(H, I)) return false;
+  if (force == 2) return true;
+  return R <= (int64_t)kWsRoutesPerExpert * E;
+}
 
 // Decode work units (decode-table entries x 16-row groups of the larger matmul)
 // and split-K work items the workspace is sized for.

@@ -268,9 +268,9 @@ __device__ void scatter_routes(const int32_t* __restrict__ idx, int64_t r0, int6
   }
 }
 
-// Offsets, active-expert list and 128-row tile list from per-expert totals held
-// one per thread (thread e < E holds total[e]).
-__device__ void finish_groups(int E, int total_e, const Workspace& ws, bool want_tiles, int* sh,
+// Offsets, active-expert list and the tile list (tiles of tile_m sorted rows)
+// from per-expert totals held one per thread (thread e < E holds total[e]).
+__device__ void finish_groups(int E, int total_e, const Workspace& ws, bool want_tiles, int tile_m, int* sh,
                               int* expert_base_out) {
   const int e = threadIdx.x;
   const int v = e < E ? total_e : 0;
@@ -287,12 +287,12 @@ __device__ void finish_groups(int E, int total_e, const Workspace& ws, bool want
     ws.counters[2] = 0;  // error flag of the grouped GEMM (set on a timed-out wait)
   }
   if (want_tiles) {
-    const int nt = (v + kTileM - 1) / kTileM;
+    const int nt = (v + tile_m - 1) / tile_m;
     int n_tiles;
     const int tpos = block_exclusive_scan(nt, sh, &n_tiles);
     for (int i = 0; i < nt; ++i) {
       ws.tiles[2 * (tpos + i)] = e;
-      ws.tiles[2 * (tpos + i) + 1] = off + i * kTileM;
+      ws.tiles[2 * (tpos + i) + 1] = off + i * tile_m;
     }
     if (e == 0) ws.counters[1] = n_tiles;
   }
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(Problem p, Wor
       total += v;
     }
   __syncthreads();
-  finish_groups(E, total, ws, want_tiles != 0, sh, expert_base);
+  finish_groups(E, total, ws, want_tiles != 0, p.tile_m, sh, expert_base);
   __syncthreads();
   if (active) {
     int run = expert_base[e] + part_sum[tid];
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   const bool dec = p.path == QMOE_PATH_DECODE;  // (block-uniform) R <= kDtabMax on this path
   const int n_act_e = dec ? (total + kDecodeChunk - 1) / kDecodeChunk : (total > 0 ? 1 : 0);
   const int apos = block_exclusive_scan(n_act_e, sh, &n_active);
-  const int nt = (total + kTileM - 1) / kTileM;
+  const int nt = (total + p.tile_m - 1) / p.tile_m;
   const int tpos = want_tiles ? block_exclusive_scan(nt, sh, &n_tiles) : 0;
   if (e < p.E) {
     hist[e] = off;                   // scatter bases
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kGroupThreads) route_group_small_kernel(
   if (want_tiles && e < p.E)
     for (int i = 0; i < nt; ++i) {
       ws.tiles[2 * (tpos + i)] = e;
-      ws.tiles[2 * (tpos + i) + 1] = off + i * kTileM;
+      ws.tiles[2 * (tpos + i) + 1] = off + i * p.tile_m;
     }
   if (dec) {
     for (int64_t i = threadIdx.x; i < ws.dunits_max; i += blockDim.x) ws.dticket[i] = 0;

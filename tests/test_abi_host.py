@@ -77,7 +77,9 @@ BAD = [
     (dict(num_experts=1024, top_k=8), qm.QMOE_ERR_UNSUPPORTED),
     (dict(num_experts=64, top_k=33), qm.QMOE_ERR_UNSUPPORTED),
     (dict(dtype=2), qm.QMOE_ERR_UNSUPPORTED),
-    (dict(path=3), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=5), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=qm.QMOE_PATH_GROUPED_WS, T=64, hidden=96, inter=64), qm.QMOE_ERR_UNSUPPORTED),
+    (dict(path=qm.QMOE_PATH_GROUPED_WS, T=64, hidden=320, inter=256), qm.QMOE_ERR_UNSUPPORTED),   # 256 | H
     (dict(path=qm.QMOE_PATH_DECODE, T=65), qm.QMOE_ERR_UNSUPPORTED),
     (dict(path=qm.QMOE_PATH_DECODE, T=64, top_k=16), qm.QMOE_ERR_UNSUPPORTED),   # 1024 routes
     (dict(path=qm.QMOE_PATH_GROUPED, bits=3, block_size=64, hidden=2048, inter=704), qm.QMOE_ERR_UNSUPPORTED),

@@ -74,7 +74,7 @@ def test_queue_is_a_permutation_with_fc1_first():
 
 def test_kernel_queue_matches_the_model():
     """The model's queue is the kernel's: the same three ranges in the same order."""
-    body = SRC[SRC.index("struct UnitQueue"):SRC.index("template <bool BF16S>")]
+    body = SRC[SRC.index("struct UnitQueue"):SRC.index("template <bool BF16S, int FMT>")]
     assert "const int p1 = L * a, p2 = p1 + (entries - L) * (a + b);" in body
     assert "ei = f1 ? L + r : r;" in body and "ei = entries - L + r;" in body
 
