@@ -653,24 +653,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_afull(sa), (uint32_t)(it / SA) & 1u, abort_flag, launch_err) ||
               !mbar_wait(bar_bready(sb), (uint32_t)(it / SB) & 1u, abort_flag, launch_err)) { go = false; break; }
           tc_fence_after();
-          const uint32_t a_base = sbase + C::A_OFF + sa * C::A_BYTES;
-          const uint32_t b_base = sbase + C::B_OFF + sb * C::B_BYTES;
+          // one descriptor per slot; the others add their byte offset / 16 to its
+          // start-address field (offsets within 2^18 bytes of shared memory: no
+          // carry out of the field), so that each MMA issues after two additions
+          const uint64_t a0 = sw128_desc(sbase + C::A_OFF + sa * C::A_BYTES);
+          const uint64_t b0 = sw128_desc(sbase + C::B_OFF + sb * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             const int sub = kk / 4, off = (kk % 4) * 32;
-            const uint64_t bdesc = sw128_desc(b_base + sub * (C::BN * 128) + off);
+            const uint64_t bdesc = b0 + (uint64_t)((sub * (C::BN * 128) + off) >> 4);
             if constexpr (WS) {
               // each 128-row half of the weight tile against the same routes
-              const uint64_t adesc = sw128_desc(a_base + sub * (C::AROWS * 128) + off);
+              const uint64_t adesc = a0 + (uint64_t)((sub * (C::AROWS * 128) + off) >> 4);
 #pragma unroll
               for (int h = 0; h < C::HALVES; ++h)
-                tc_mma(acc0 + h * kTileWs, sw128_desc(b_base + sub * (C::BN * 128) + h * (kSubM * 128) + off), adesc,
-                       idesc_ws, (i | kk) != 0);
+                tc_mma(acc0 + h * kTileWs, bdesc + (uint64_t)((h * (kSubM * 128)) >> 4), adesc, idesc_ws,
+                       (i | kk) != 0);
             } else {
 #pragma unroll
               for (int h = 0; h < 2; ++h)
                 if (h < nh)
-                  tc_mma(acc0 + h * C::BN, sw128_desc(a_base + sub * (kBM * 128) + h * (kSubM * 128) + off), bdesc,
+                  tc_mma(acc0 + h * C::BN, a0 + (uint64_t)((sub * (kBM * 128) + h * (kSubM * 128) + off) >> 4), bdesc,
                          idesc, (i | kk) != 0);
             }
           }
