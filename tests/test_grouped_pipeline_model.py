@@ -15,7 +15,9 @@ the copy engine, completes the copies in flight in random order, so a copy can
 land after later ones. Configurations cover one and several tiles, K stage
 counts below, equal to and above the ring depths, odd stage counts (the
 dequantisation groups swap stages between tiles), scale boxes of one stage, and
-the INT3 ring depths with double-buffered accumulators. The model has to follow
+the INT3 ring depths with double-buffered accumulators, and the
+weights-stationary rings, whose code copies hold R stages each (both groups
+read every copy; its slot is free after all R stages). The model has to follow
 the kernel: change both together.
 
 With an odd code ring (INT4: three slots) a slot's consecutive stages belong
@@ -52,7 +54,9 @@ def ready(bar, parity, phase_needed):
     return ok
 
 
-def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
+def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True, R=1):
+    assert ksteps % R == 0
+    kcopies = ksteps // R                                       # code copies per tile
     rnd = random.Random(seed)
     in_flight = []                                              # copies issued, not landed: (kind, slot, barrier)
     a_landed, c_landed, s_landed = [False] * SA, [False] * SC, [False] * 2
@@ -60,7 +64,7 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
     afull = [Barrier(f"afull{s}", 1) for s in range(SA)]
     aempty = [Barrier(f"aempty{s}", 1) for s in range(SA)]
     cfull = [Barrier(f"cfull{s}", 1) for s in range(SC)]
-    cempty = [Barrier(f"cempty{s}", 1) for s in range(SC)]      # one group's arrival per stage
+    cempty = [Barrier(f"cempty{s}", R) for s in range(SC)]      # one group's arrival per stage of the copy
     bready = [Barrier(f"bready{s}", 1) for s in range(SB)]
     bempty = [Barrier(f"bempty{s}", 1) for s in range(SB)]
     accum = [Barrier(f"accum{b}", 1) for b in range(ACC)]
@@ -69,6 +73,7 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
     sempty = [Barrier(f"sempty{b}", 2) for b in range(2)]       # both groups, or one group twice
     a_slot, b_slot, c_slot, s_box, acc_buf = [None] * SA, [None] * SB, [None] * SC, [None] * 2, [None] * ACC
     a_used, b_used, c_used = [True] * SA, [True] * SB, [True] * SC
+    c_left = [0] * SC                                           # stages of the copy not yet dequantised
     nbox = (ksteps + span - 1) // span
     box_left = {}                                               # arrivals still due per scale box
 
@@ -79,24 +84,26 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
     def code_producer():
         spans = 0
         for j in range(works):
-            for i in range(ksteps):
-                it = j * ksteps + i
-                s = it % SC
-                yield from wait(cempty[s], ((it // SC) & 1) ^ 1, it // SC)
-                if tsc and i % span == 0:
-                    m = spans
-                    spans += 1
-                    if m >= 2:
-                        yield from wait(sempty[m & 1], ((m - 2) >> 1) & 1, (m - 2) // 2 + 1)
-                        assert box_left[m - 2] == 0, "scale box overwritten before both groups released it"
-                    s_box[m & 1] = m
-                    s_landed[m & 1] = False
-                    span_len = min(span, ksteps - i)
-                    box_left[m] = 2 if span_len >= 2 else 1
-                    in_flight.append(("s", m & 1, sfull[m & 1]))
+            for ci in range(kcopies):
+                ic = j * kcopies + ci
+                s = ic % SC
+                yield from wait(cempty[s], ((ic // SC) & 1) ^ 1, ic // SC)
+                for sub in range(R):
+                    i = ci * R + sub
+                    if tsc and i % span == 0:
+                        m = spans
+                        spans += 1
+                        if m >= 2:
+                            yield from wait(sempty[m & 1], ((m - 2) >> 1) & 1, (m - 2) // 2 + 1)
+                            assert box_left[m - 2] == 0, "scale box overwritten before both groups released it"
+                        s_box[m & 1] = m
+                        s_landed[m & 1] = False
+                        span_len = min(span, ksteps - i)
+                        box_left[m] = 2 if span_len >= 2 else 1
+                        in_flight.append(("s", m & 1, sfull[m & 1]))
                 assert c_used[s], "code slot overwritten before it was dequantised"
-                c_slot[s], c_used[s], c_landed[s] = it, False, False
-                c_issued[s] = it
+                c_slot[s], c_used[s], c_landed[s], c_left[s] = ic, False, False, R
+                c_issued[s] = ic
                 in_flight.append(("c", s, cfull[s]))
 
     def act_producer():
@@ -144,12 +151,13 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
                 it = j * ksteps + i
                 if (it & 1) != grp:
                     continue
-                cs, bs = it % SC, it % SB
-                if issued_word and SC % 2 == 1:
-                    while c_issued[cs] != it:
+                ic = j * kcopies + i // R
+                cs, bs = ic % SC, it % SB
+                if issued_word and R == 1 and SC % 2 == 1:
+                    while c_issued[cs] != ic:
                         yield
-                yield from wait(cfull[cs], (it // SC) & 1, it // SC + 1)
-                assert c_slot[cs] == it, "dequantiser read the wrong code stage"
+                yield from wait(cfull[cs], (ic // SC) & 1, ic // SC + 1)
+                assert c_slot[cs] == ic, "dequantiser read the wrong code copy"
                 assert c_landed[cs], "dequantiser read a code tile still in flight"
                 m_cur = j * nbox + i // span
                 if tsc and m_cur != box_seen:
@@ -161,7 +169,9 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
                 assert b_used[bs], "B slot overwritten before the MMAs read it"
                 b_slot[bs], b_used[bs] = it, False
                 bready[bs].arrive()
-                c_used[cs] = True
+                c_left[cs] -= 1
+                if c_left[cs] == 0:
+                    c_used[cs] = True
                 cempty[cs].arrive()
                 if tsc:
                     box0 = (i // span) * span
@@ -204,7 +214,7 @@ def simulate(ksteps, works, SA, SB, SC, ACC, tsc, span, seed, issued_word=True):
     assert all(v == 0 for v in box_left.values()), "a scale box was not released by every group"
 
 
-# (ksteps, works, SA, SB, SC, ACC, scales by tensor copy, stages per scale box)
+# (ksteps, works, SA, SB, SC, ACC, scales by tensor copy, stages per scale box[, stages per code copy])
 CONFIGS = [
     (32, 3, 3, 3, 3, 1, True, 4),     # INT4 block 32, fc1 K = 2048
     (12, 4, 3, 3, 3, 1, True, 4),     # INT4 block 32, fc2 K = 768
@@ -215,13 +225,20 @@ CONFIGS = [
     (1, 6, 3, 3, 3, 1, True, 4),      # one stage per tile
     (16, 4, 2, 2, 2, 2, True, 2),     # INT3 block 32 (K stage 128): double-buffered accumulators
     (3, 5, 2, 2, 2, 2, True, 4),      # INT3, short K
+    # weights-stationary: 256-K code copies
+    (32, 4, 3, 3, 2, 2, True, 4, 4),  # INT4 block 32, fc1 K = 2048: 4 stages per copy
+    (12, 5, 3, 3, 2, 2, False, 4, 4), # INT4 / INT2 fc2 K = 768, scales by the producer
+    (16, 4, 2, 2, 4, 2, True, 4, 2),  # INT3 block 64, fc1 K = 2048 (K stage 128): 2 stages per copy
+    (6, 5, 2, 2, 4, 2, False, 4, 2),  # INT3 fc2 K = 768
+    (4, 6, 3, 3, 2, 2, True, 16, 4),  # one copy per tile, block 128
 ]
 
 
 @pytest.mark.parametrize("cfg", CONFIGS)
 def test_pipeline_protocol(cfg):
+    R = cfg[8] if len(cfg) > 8 else 1
     for seed in range(6):
-        simulate(*cfg, seed=seed)
+        simulate(*cfg[:8], seed=seed, R=R)
 
 
 def test_odd_code_ring_needs_the_issued_word():
