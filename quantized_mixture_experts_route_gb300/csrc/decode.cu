@@ -871,7 +871,7 @@ int64_t decode_grid_blocks() { return (int64_t)sm_count() * kBlocksPerSmB; }
 constexpr int kTWarps = 8;
 constexpr int kTChunkK = 256;
 constexpr int kTBlocksPerSm = 2;
-constexpr int kTMinPiece = 4;                      // chunks per warp at least
+constexpr int kTMinPiece = 2;                      // chunks per warp at least
 constexpr int kTZero = 512;                        // zero bytes read by non-supplying lanes
 constexpr uint64_t kTWaitNs = 1000000000ull;      // 1 s: far beyond any legitimate wait
 constexpr uint64_t kTDrainNs = 100000000ull;
@@ -1342,12 +1342,14 @@ cudaError_t launch_int4_tma_rows(const uint8_t* q, const uint16_t* scales, const
 }
 
 // 32-row units where a unit has at least four chunks (long enough that few of
-// them are cut between warps), 16-row units otherwise.
+// them are cut between warps), 16-row units otherwise, and for one or two
+// tokens: there the work is a few chunks per warp, and 16-row units give twice
+// the warps, each with two chunks in flight (T = 2: 30.9 -> 26.6 us per layer).
 template <bool FC1>
 cudaError_t launch_int4_tma(const uint8_t* q, const uint16_t* scales, const uint8_t* zp, const Problem& p,
                             const Workspace& ws, cudaStream_t s) {
   const int K = FC1 ? p.H : p.I, N = FC1 ? 2 * p.I : p.H;
-  if (K / kTChunkK >= 4 && N % 32 == 0) return launch_int4_tma_rows<32, FC1>(q, scales, zp, p, ws, s);
+  if (p.T > 2 && K / kTChunkK >= 4 && N % 32 == 0) return launch_int4_tma_rows<32, FC1>(q, scales, zp, p, ws, s);
   return launch_int4_tma_rows<16, FC1>(q, scales, zp, p, ws, s);
 }
 
