@@ -74,5 +74,30 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(lib_path: str, defines: dict[str, str]) -> str:
+    """Build a copy of the library with extra preprocessor definitions (e.g. a
+    test build with QMOE_WAIT_LIMIT_NS=0) at lib_path; objects go next to it."""
+    nvcc = _nvcc()
+    obj_dir = lib_path + ".objs"
+    os.makedirs(obj_dir, exist_ok=True)
+    dflags = [f"-D{k}={v}" for k, v in defines.items()]
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
+        cmd = [nvcc, *ARCH, *[f for f in NVCC_FLAGS if f not in ("-Xptxas", "-v")], *dflags, "-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
+        return obj
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, sources()))
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", lib_path, *objs, "-cudart", "static"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stderr}")
+    return lib_path
+
+
 if __name__ == "__main__":
     print(build(force=True, verbose=True))

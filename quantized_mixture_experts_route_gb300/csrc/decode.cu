@@ -873,7 +873,7 @@ constexpr int kTChunkK = 256;
 constexpr int kTBlocksPerSm = 2;
 constexpr int kTMinPiece = 2;                      // chunks per warp at least
 constexpr int kTZero = 512;                        // zero bytes read by non-supplying lanes
-constexpr uint64_t kTWaitNs = 1000000000ull;      // 1 s: far beyond any legitimate wait
+constexpr uint64_t kTWaitNs = QMOE_WAIT_LIMIT_NS;
 constexpr uint64_t kTDrainNs = 100000000ull;
 constexpr int kErrDecodeTimeout = 2;
 

@@ -71,7 +71,7 @@ constexpr int kLMetaOff = kLZeroOff + kLZero + 96;   // [warp][stage] int4, 16-b
 constexpr int kLReadyOff = kLMetaOff + kLWarps * kLStages * 16;   // [kDtabMax / 32] entries whose fc1 is done
 constexpr int kLDtabOff = kLReadyOff + kDtabMax / 8;              // the decode table, [entries][kDtabInts]
 constexpr int kLSmemFixed = 128 + kLDtabOff;                      // + the decode table's bytes
-constexpr uint64_t kLWaitNs = 1000000000ull;         // 1 s: far beyond any legitimate wait
+constexpr uint64_t kLWaitNs = QMOE_WAIT_LIMIT_NS;
 constexpr int kErrLayerTimeout = 3;
 static_assert(kLStage % 128 == 0, "stages keep the code rows 128-byte aligned");
 static_assert(kLZeroOff % 128 == 32, "the zero area must not share banks with the activation tiles");
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kLThreads, kLBlocksPerSm) decode_layer_kernel(
             if (lane == 0) {
               const uint64_t t0 = globaltimer_ns();
               while (ld_acquire(fc1_done + iei) < rg1) {
-                if (globaltimer_ns() - t0 > kLWaitNs) { good = 0; break; }
+                if (globaltimer_ns() - t0 >= kLWaitNs) { good = 0; break; }
                 __nanosleep(128);
               }
             }

@@ -58,7 +58,7 @@ constexpr int kEpiWarps = 4;           // warps 18..21: one per TMEM lane quarte
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kAProdWarp = 2 + kDequantWarps + kEpiWarps;   // warp 22
 constexpr int kThreads = 32 * (kAProdWarp + 1);
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
+constexpr uint64_t kWaitLimitNs = QMOE_WAIT_LIMIT_NS;
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
 constexpr int kErrTimeout = 1;
 static_assert(kBM == kTileM, "the grouping kernels cut tiles of kTileM sorted rows");
@@ -153,12 +153,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((i & 255u) == 0) {
+    if ((i & 255u) == 0 || kWaitLimitNs == 0) {
       if (*launch_err) {
         *abort_flag = 1;
         return false;
       }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 >= kWaitLimitNs) {
         *abort_flag = 1;
         *launch_err = kErrTimeout;
         return false;
@@ -175,12 +175,12 @@ __device__ __forceinline__ bool word_wait(const volatile int* word, int want, vo
   for (uint32_t i = 1;; ++i) {
     if (*word == want) return true;
     if (*abort_flag) return false;
-    if ((i & 255u) == 0) {
+    if ((i & 255u) == 0 || kWaitLimitNs == 0) {
       if (*launch_err) {
         *abort_flag = 1;
         return false;
       }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 >= kWaitLimitNs) {
         *abort_flag = 1;
         *launch_err = kErrTimeout;
         return false;

@@ -25,6 +25,13 @@ constexpr int kPermuteChunk = 512;    // routes per block in the grouping kernel
 // it for T <= 8 and, above that, while the routes number fewer than 4 per
 // expert (below 64 routes in all, always): the pages switch from their
 // tensor-core GEMV to the grouped GEMM at num_r >= 64 && num_r >= 4 E.
+// Wall-time limit of every bounded wait in the matmul kernels (1 s: far beyond
+// any legitimate wait). A test build sets it to 0, so that waits run out and
+// the kernels' give-up paths run (tests/test_gpu_wait_timeouts.py).
+#ifndef QMOE_WAIT_LIMIT_NS
+#define QMOE_WAIT_LIMIT_NS 1000000000ull
+#endif
+
 constexpr int kDecodeMaxT = 64;
 constexpr int kDecodeChunk = 8;       // routes of one expert per MMA N-fragment (generic decode kernel)
 constexpr int kTileM = 256;           // rows (routes) per grouped-GEMM tile

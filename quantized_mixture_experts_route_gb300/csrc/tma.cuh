@@ -42,12 +42,23 @@ __device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#if QMOE_WAIT_LIMIT_NS == 0
+  // the test build with zero wait limits polls without suspending, so that a
+  // wait gives up as soon as it finds its phase open
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+#else
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 
@@ -57,13 +68,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Wait for phase `parity` of an mbarrier for at most limit_ns; false on timeout.
+// Wait for phase `parity` of an mbarrier for at most limit_ns; false on timeout
+// (with a zero limit, at the first poll that finds the phase open).
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    if (((i & 255u) == 0 || limit_ns == 0) && globaltimer_ns() - t0 >= limit_ns) return false;
   }
 }
 
