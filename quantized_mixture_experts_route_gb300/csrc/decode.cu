@@ -1294,6 +1294,431 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
   }
 }
 
+// ---------------------------------------------------------------------------
+// INT3 (implicit zero point 4), blocks of 32, 64 or 128, K a multiple of 256:
+// the tensor-copy kernel's walk, tickets and epilogues with 3-bit codes. A
+// chunk's codes are one [rows][96 B] box; lane c takes its 32 codes of a
+// 128-wide half as 12 bytes, byte permutes put two 8-code groups in the two
+// 16-bit halves, and one shift and one AND/OR per pair give 1024 + code in
+// FP16, in the same 16-group K permutation as the activations. One bias MMA
+// per K step (operand -(1024 + 4)) is shared by all row halves. The block
+// scales come by one 16-, 8- or 4-byte load per lane and row, stored into the
+// slot one chunk later (scale rows need not be a multiple of 16 bytes, as a
+// tensor copy would require); each D column takes the scale of the block its
+// owner lane's codes fall in.
+// ---------------------------------------------------------------------------
+template <int ROWS>
+struct T3Cfg {
+  static constexpr int kRows = ROWS;
+  static constexpr int kHalves = ROWS / 16;
+  static constexpr int kRing = 3;                     // chunks per warp: two in flight, one in use
+  static constexpr int kCode = 0;                     // [ROWS][96 B]
+  static constexpr int kScale = ROWS * 96;            // [ROWS][8] 16-bit scales (the first 8, 4 or 2 used)
+  static constexpr int kAct0 = kScale + ROWS * 16;
+  static constexpr int kAct1 = kAct0 + 512;
+  static constexpr int kSlot = kAct1 + 512;
+  static constexpr int kPart = kHalves * 4 * 32;
+  static constexpr size_t kSmem = (size_t)kTWarps * kRing * kSlot + kTZero + kTWarps * kRing * 8 + 128;
+  static_assert(kScale % 128 == 0 && kAct0 % 128 == 0 && kSlot % 128 == 0, "copies land on 128-byte boundaries");
+};
+
+struct Tma3Args {
+  int N, K;
+  Problem p;
+  Workspace ws;
+  const uint16_t* s;       // [E][N][K/block] block scales in dtype
+  int lb;                  // log2(block)
+};
+
+template <int ROWS, bool FC1, bool BF16S>
+__global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int3_tma_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ta, Tma3Args a) {
+  using C = T3Cfg<ROWS>;
+  // fc1 needs the routing kernel's results at once. fc2 reads only the routing
+  // results (complete: fc1 let fc2 be scheduled only after waiting for routing)
+  // and its own weights before it waits for fc1, so its first weight copies
+  // overlap the end of fc1.
+  if constexpr (FC1) {
+    pdl_wait();
+    pdl_trigger();
+  } else {
+    pdl_trigger();
+  }
+  const Problem& p = a.p;
+  const Workspace& ws = a.ws;
+  const int K = a.K, N = a.N;
+  const int nq = K / kTChunkK;                   // chunks per unit
+  const int rgroups = N / C::kRows;
+  const int cfull = ws.counters[3] * rgroups * nq;   // < 2^31: <= 256 entries x 512 groups x 32 chunks
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int gw = gridDim.x * kTWarps;
+  const int wg = blockIdx.x * kTWarps + warp;
+  // equal pieces of L chunks (the last one shorter, none empty)
+  int L = (cfull + gw - 1) / gw;
+  if (L < kTMinPiece) L = kTMinPiece;
+  const int nw = (cfull + L - 1) / L;
+  const int x_begin = wg < nw ? wg * L : 0;
+  const int total = wg < nw ? min(x_begin + L, cfull) - x_begin : 0;
+  const bool owner = (g & 3) == c;               // supplies activations for column g
+  const int on = g >> 2;                         // owner lane's route within the pair
+  const int n = c >> 1;                          // route within the pair of this lane's D columns
+
+  extern __shared__ __align__(16) uint8_t smem[];
+  // bulk tensor copies land on 128-byte boundaries
+  uint8_t* base = smem + ((128u - (smem_u32(smem) & 127u)) & 127u);
+  const uint32_t ring_s = smem_u32(base) + warp * (C::kRing * C::kSlot);
+  const uint32_t zero_s = smem_u32(base) + kTWarps * C::kRing * C::kSlot;
+  const uint32_t bar_s = zero_s + kTZero + warp * (C::kRing * 8);
+  if (threadIdx.x < kTZero / 4) reinterpret_cast<uint32_t*>(base + kTWarps * C::kRing * C::kSlot)[threadIdx.x] = 0u;
+  if (lane == 0)
+    for (int s = 0; s < C::kRing; ++s) mbar_init(bar_s + 8 * s, 1);
+  mbar_init_fence();
+  __syncthreads();
+  if (total == 0) {
+    if constexpr (!FC1) pdl_wait();
+    return;
+  }
+
+  // unit = (decode-table entry ei, 32-row group rg); walked without divisions
+  const int item0 = x_begin / nq;
+  const int cic0 = x_begin - item0 * nq;
+  const int ei0 = item0 / rgroups, rg0 = item0 - ei0 * rgroups;
+
+  // ---- issue side: lane 0 copies chunk f of the piece into slot f % C::kRing:
+  // the weights (codes, scales, zero points; announced without arriving) and the
+  // activations of the entry's tokens (announced with the arrival)
+  int p_ei = ei0, p_rg = rg0, p_cic = cic0, p_row = 0, p_t0 = 0, p_t1 = 0, p_cnt = 0;
+  bool p_new = true;
+  uint32_t p_slot_s = ring_s, p_bar = bar_s;
+  // block scales: lane L < ROWS loads row L's scales of the chunk (16, 8 or 4
+  // bytes for blocks of 32, 64 or 128) when the chunk is issued and stores them
+  // into the slot one chunk later, so that the load's latency is hidden
+  const int lb = a.lb;
+  const int nblk = K >> lb;
+  uint4 s_pend = make_uint4(0u, 0u, 0u, 0u);
+  uint32_t s_pend_dst = 0;
+  bool s_have = false;
+  auto scale_store = [&]() {
+    if (s_have && lane < ROWS) {
+      if (lb == 5)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(s_pend_dst), "r"(s_pend.x), "r"(s_pend.y),
+                     "r"(s_pend.z), "r"(s_pend.w) : "memory");
+      else if (lb == 6)
+        asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s_pend_dst), "r"(s_pend.x), "r"(s_pend.y) : "memory");
+      else
+        asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(s_pend_dst), "r"(s_pend.x) : "memory");
+    }
+    s_have = false;
+  };
+  auto issue_act = [&](uint32_t slot_s, uint32_t bar, int kx, int t0, int t1, int cnt) {
+    if (lane == 0) {
+      mbar_expect_tx(bar, cnt > 1 ? 1024 : 512);
+      tma_load_2d(slot_s + C::kAct0, &ta, bar, kx, t0);
+      if (cnt > 1) tma_load_2d(slot_s + C::kAct1, &ta, bar, kx, t1);
+    }
+  };
+  // deferred activation copies of the first slots (fc2: issued after the wait)
+  uint32_t q_slot[C::kRing - 1], q_bar[C::kRing - 1];
+  int q_kx[C::kRing - 1], q_t0[C::kRing - 1], q_t1[C::kRing - 1], q_cnt[C::kRing - 1];
+  auto issue = [&](bool with_act, int q) {
+    if (p_new) {
+      p_new = false;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + p_ei * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + p_ei * kDtabInts + 4));
+      p_row = d0.x * N + p_rg * C::kRows;
+      p_cnt = d0.z;
+      p_t0 = FC1 ? d1.x : d0.y;
+      p_t1 = FC1 ? d1.y : d0.y + 1;
+    }
+    const int kx = p_cic * kTChunkK;
+    if (lane == 0) {
+      mbar_expect_tx_only(p_bar, ROWS * 96);
+      tma_load_2d(p_slot_s + C::kCode, &tq, p_bar, kx / 8 * 3, p_row);
+    }
+    // the previous chunk's scales go to its slot; this chunk's are loaded
+    scale_store();
+    if (lane < ROWS) {
+      const uint16_t* src = a.s + (int64_t)(p_row + lane) * nblk + (kx >> lb);
+      if (lb == 5) s_pend = __ldg(reinterpret_cast<const uint4*>(src));
+      else if (lb == 6) { const uint2 v = __ldg(reinterpret_cast<const uint2*>(src)); s_pend.x = v.x; s_pend.y = v.y; }
+      else s_pend.x = __ldg(reinterpret_cast<const uint32_t*>(src));
+    }
+    s_pend_dst = p_slot_s + C::kScale + lane * 16;
+    s_have = true;
+    if (with_act) {
+      issue_act(p_slot_s, p_bar, kx, p_t0, p_t1, p_cnt);
+    } else {
+      q_slot[q] = p_slot_s; q_bar[q] = p_bar; q_kx[q] = kx; q_t0[q] = p_t0; q_t1[q] = p_t1; q_cnt[q] = p_cnt;
+    }
+    if (p_bar == bar_s + 8 * (C::kRing - 1)) { p_bar = bar_s; p_slot_s = ring_s; }
+    else { p_bar += 8; p_slot_s += C::kSlot; }
+    if (++p_cic == nq) {
+      p_cic = 0;
+      p_new = true;
+      if (++p_rg == rgroups) { p_rg = 0; ++p_ei; }
+    }
+  };
+  const int pre = total < C::kRing - 1 ? total : C::kRing - 1;
+#pragma unroll
+  for (int u = 0; u < C::kRing - 1; ++u)
+    if (u < pre) issue(FC1, u);
+  if constexpr (!FC1) {
+    pdl_wait();                                  // h16 (fc1's output) is complete from here on
+#pragma unroll
+    for (int u = 0; u < C::kRing - 1; ++u)
+      if (u < pre) issue_act(q_slot[u], q_bar[u], q_kx[u], q_t0[u], q_t1[u], q_cnt[u]);
+  }
+
+  // the implicit zero point 4 of every code: -(1024 + 4) in every FP16 operand
+  const __half2 nb_d = __float2half2_rn(-(1024.0f + 4.0f));
+  const uint32_t nb_def = *reinterpret_cast<const uint32_t*>(&nb_d);
+  // per-lane shared-memory offsets within a slot
+  const uint32_t code_off = g * 96 + c * 12;    // row g of the [rows][96 B] code tile, lane c's 32 codes
+  // the blocks of this lane's two D columns (owner lanes 2c & 3 and (2c + 1) & 3) in each 128-wide half
+  // of the chunk, as byte offsets into a row's scales
+  uint32_t blk_off[2][2];
+#pragma unroll
+  for (int sub = 0; sub < 2; ++sub) {
+    blk_off[sub][0] = 2u * (uint32_t)((sub * 128 + ((2 * c) & 3) * 32) >> lb);
+    blk_off[sub][1] = 2u * (uint32_t)((sub * 128 + ((2 * c + 1) & 3) * 32) >> lb);
+  }
+  // activation words: owners read their token's tile, the other lanes the zero area
+  const uint32_t act_base = owner ? ring_s + (on ? C::kAct1 : C::kAct0) + 64 * c : zero_s;
+  const uint32_t act_slot_stride = owner ? C::kSlot : 0;
+
+  // ---- compute side
+  int ei = ei0, rg = rg0, cic = cic0, first_cic = cic0;
+  bool first_unit = true, fresh = true;
+  int cnt = 0, pos0 = 0, e_rid = 0;
+  float e_scale = 1.0f, e_w = 0.0f;              // epilogue operands of route n, loaded early
+  float e_hn = 1.0f;                             // the expert's SwiGLU normalisation (decode table)
+  float acc[C::kHalves][4];                    // [row half][D fragment]
+#pragma unroll
+  for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[rh][r] = 0.f;
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int f = 0; f < total; ++f) {
+    __syncwarp();                                // every lane is done with the slot refilled next
+    if (f + C::kRing - 1 < total) issue(true, 0);
+    else scale_store();
+    __syncwarp();                                // chunk f's scales are in its slot
+    if (fresh) {
+      fresh = false;
+      const int4 d0 = __ldg(reinterpret_cast<const int4*>(ws.dtab + ei * kDtabInts));
+      const int4 d1 = __ldg(reinterpret_cast<const int4*>(ws.dtab + ei * kDtabInts + 4));
+      pos0 = d0.y;
+      cnt = d0.z;
+      e_hn = __int_as_float(d1.w);
+      if (n < cnt) {
+        if constexpr (FC1) {
+          e_scale = __ldg(ws.tok_scale + (n ? d1.y : d1.x));
+        } else {
+          e_rid = __ldg(ws.sorted_route + pos0 + n);
+          e_scale = __ldg(ws.tok_scale + e_rid / p.k);
+          e_w = __ldg(ws.topk_w + e_rid);
+        }
+      }
+    }
+    const uint32_t bar = bar_s + 8 * slot;
+    if (!mbar_wait_for(bar, phase, kTWaitNs)) {
+      // record the failure, let this warp's copies in flight land, and stop
+      if (lane == 0) atomicExch(ws.counters + 2, kErrDecodeTimeout);
+      int s2 = slot;
+      uint32_t ph2 = phase;
+      const int inflight = total - f < C::kRing ? total - f : C::kRing;   // chunks f .. f + C::kRing - 1
+      for (int u = 0; u < inflight; ++u) {
+        mbar_wait_for(bar_s + 8 * s2, ph2, kTDrainNs);
+        if (++s2 == C::kRing) { s2 = 0; ph2 ^= 1u; }
+      }
+      return;
+    }
+    const uint32_t sb = ring_s + slot * C::kSlot;
+    const uint32_t ab = act_base + slot * act_slot_stride;
+    // the activations (B fragments) of both sub-chunks serve both 16-row halves
+    uint32_t bw[2][16];
+#define QMOE_LDS_ACT(SUB, J, OFF)                                                                  \
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+" #OFF "];\n"                                 \
+               : "=r"(bw[SUB][4 * J]), "=r"(bw[SUB][4 * J + 1]), "=r"(bw[SUB][4 * J + 2]),         \
+                 "=r"(bw[SUB][4 * J + 3])                                                          \
+               : "r"(ab))
+    QMOE_LDS_ACT(0, 0, 0);
+    QMOE_LDS_ACT(0, 1, 16);
+    QMOE_LDS_ACT(0, 2, 32);
+    QMOE_LDS_ACT(0, 3, 48);
+    QMOE_LDS_ACT(1, 0, 256);
+    QMOE_LDS_ACT(1, 1, 272);
+    QMOE_LDS_ACT(1, 2, 288);
+    QMOE_LDS_ACT(1, 3, 304);
+#undef QMOE_LDS_ACT
+    // Every weight row has the same bias operand (the implicit zero point), so
+    // the bias MMAs are computed once per chunk and start each row half's sums:
+    // stream q takes the K steps j with j % 2 == q.
+    float tb[2][2][4];
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tb[sub][q][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub)
+        mma16816(tb[sub][j & 1], nb_def, nb_def, nb_def, nb_def, bw[sub][2 * j], bw[sub][2 * j + 1]);
+#pragma unroll
+    for (int rh = 0; rh < C::kHalves; ++rh) {
+      const uint32_t cb_ = sb + code_off + rh * (16 * 96);                 // rows 16 rh + g and + 8
+      const uint32_t sr = sb + C::kScale + (rh * 16 + g) * 16;
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        // lane c's 32 codes of rows g and g + 8 in this 128-wide half: 12 bytes each
+        uint32_t wa[3], wb[3];
+        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(wa[0]) : "r"(cb_ + sub * 48));
+        asm volatile("ld.shared.u32 %0, [%1+4];\n" : "=r"(wa[1]) : "r"(cb_ + sub * 48));
+        asm volatile("ld.shared.u32 %0, [%1+8];\n" : "=r"(wa[2]) : "r"(cb_ + sub * 48));
+        asm volatile("ld.shared.u32 %0, [%1+768];\n" : "=r"(wb[0]) : "r"(cb_ + sub * 48));
+        asm volatile("ld.shared.u32 %0, [%1+772];\n" : "=r"(wb[1]) : "r"(cb_ + sub * 48));
+        asm volatile("ld.shared.u32 %0, [%1+776];\n" : "=r"(wb[2]) : "r"(cb_ + sub * 48));
+        // byte permutes: the two 8-code groups of each 16 in the two 16-bit halves
+        const uint32_t va[4] = {__byte_perm(wa[0], wa[1], 0x4310), __byte_perm(wa[0], wa[1], 0x5421),
+                                __byte_perm(wa[1], wa[2], 0x6532), __byte_perm(wa[1], wa[2], 0x7643)};
+        const uint32_t vb[4] = {__byte_perm(wb[0], wb[1], 0x4310), __byte_perm(wb[0], wb[1], 0x5421),
+                                __byte_perm(wb[1], wb[2], 0x6532), __byte_perm(wb[1], wb[2], 0x7643)};
+        // pair p: codes (16 (p / 8) + m, 16 (p / 8) + m + 8), m = p % 8, as 1024 + code
+        constexpr uint32_t kMagic = 0x64006400u;
+        auto pair = [&](const uint32_t* v, int p) -> uint32_t {
+          const int gq = p >> 3, m = p & 7;
+          const uint32_t w = m < 5 ? v[2 * gq] >> (3 * m) : v[2 * gq + 1] >> (3 * m - 8);
+          return lop3_and_or(w, 0x00070007u, kMagic);
+        };
+        float t[2][4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) t[q][e] = tb[sub][q][e];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          mma16816(t[j & 1], pair(va, 2 * j), pair(vb, 2 * j), pair(va, 2 * j + 1), pair(vb, 2 * j + 1),
+                   bw[sub][2 * j], bw[sub][2 * j + 1]);
+        // the scales of this lane's two D columns for rows g and g + 8
+        uint32_t h[4];
+        asm volatile("ld.shared.u16 %0, [%1];\n" : "=r"(h[0]) : "r"(sr + blk_off[sub][0]));
+        asm volatile("ld.shared.u16 %0, [%1];\n" : "=r"(h[1]) : "r"(sr + blk_off[sub][1]));
+        asm volatile("ld.shared.u16 %0, [%1+128];\n" : "=r"(h[2]) : "r"(sr + blk_off[sub][0]));
+        asm volatile("ld.shared.u16 %0, [%1+128];\n" : "=r"(h[3]) : "r"(sr + blk_off[sub][1]));
+        float sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sc[e] = BF16S ? __uint_as_float(h[e] << 16) : __half2float(__ushort_as_half((uint16_t)h[e]));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[rh][e] = fmaf(sc[e], t[0][e] + t[1][e], acc[rh][e]);
+      }
+    }
+    if (++slot == C::kRing) { slot = 0; phase ^= 1u; }
+    if (++cic < nq && f + 1 < total) continue;
+
+    // ---- this warp's part of the unit is done
+    const bool whole = first_cic == 0 && cic == nq;
+    bool last = true;
+    if (!whole) {
+      // parts of this unit: the warps owning its first and last chunk, and those between
+      const int item = ei * rgroups + rg;
+      const int ux = item * nq;
+      const int w0 = ux / L, w1 = (ux + nq - 1) / L;
+      // partial slot 0: the piece's first unit; slot 1: its last unit
+      float* part = ws.dsplit + ((size_t)wg * 2 + (first_unit ? 0 : 1)) * C::kPart;
+#pragma unroll
+      for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) part[(rh * 4 + r) * 32 + lane] = acc[rh][r];
+      __syncwarp();
+      int old = 0;
+      if (lane == 0) {
+        // release: the warp's partial tile is visible before the ticket moves;
+        // acquire: the other parts' tiles are visible to the last arriver
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(ws.dticket + item) : "memory");
+      }
+      old = __shfl_sync(0xffffffffu, old, 0);
+      last = old == w1 - w0;
+      if (last) {
+        if (lane == 0) ws.dticket[item] = 0;    // free again for fc2 and the next call
+        __syncwarp();
+        // parts added in chunk order: warps w0 .. w1. Warp w0's piece may begin
+        // before the unit (the unit is then its last, slot 1); every later
+        // warp's piece begins inside it (slot 0).
+        const int hs0 = w0 * L < ux ? 1 : 0;
+#pragma unroll
+        for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            float v = 0.f;
+            for (int wk = w0; wk <= w1; ++wk) {
+              const int hs = wk == w0 ? hs0 : 0;
+              const float pk = wk == wg ? acc[rh][r]
+                                        : __ldcg(ws.dsplit + ((size_t)wk * 2 + hs) * C::kPart + (rh * 4 + r) * 32 + lane);
+              v = wk == w0 ? pk : v + pk;
+            }
+            acc[rh][r] = v;
+          }
+      }
+    }
+    if (last) {
+#pragma unroll
+      for (int rh = 0; rh < C::kHalves; ++rh) {
+      const int row0 = rg * C::kRows + rh * kRowsPerGroup;
+      float v_lo = acc[rh][0] + acc[rh][1];
+      float v_hi = acc[rh][2] + acc[rh][3];
+      v_lo += __shfl_xor_sync(0xffffffffu, v_lo, 1);
+      v_hi += __shfl_xor_sync(0xffffffffu, v_hi, 1);
+      if constexpr (FC1) {
+        const float up_lo = __shfl_down_sync(0xffffffffu, v_lo, 4);
+        const float up_hi = __shfl_down_sync(0xffffffffu, v_hi, 4);
+        if ((g & 1) == 0 && (c & 1) == 0 && n < cnt) {
+          const int pos = pos0 + n;
+          const float sigma = e_scale;
+          const float inv = 1.0f / sigma;
+          const int j_lo = row0 / 2 + g / 2, j_hi = j_lo + 4;
+          const int ex = __ldg(ws.dtab + ei * kDtabInts);
+          float2 b_lo = make_float2(0.0f, 0.0f), b_hi = b_lo;
+          if (p.b1) {
+            b_lo = fc1_bias_pair(p, ex, j_lo);
+            b_hi = fc1_bias_pair(p, ex, j_hi);
+          }
+          const float hs = sigma * sigma * e_hn;
+          const float h_lo = silu(v_lo * inv + b_lo.x) * (up_lo * inv + b_lo.y) * hs;
+          const float h_hi = silu(v_hi * inv + b_hi.x) * (up_hi * inv + b_hi.y) * hs;
+          // fc2 reads these as activations (the 3-bit codes' 16-group permutation)
+          ws.h16[(int64_t)pos * p.I + permuted_pos(j_lo, 16)] = __half_as_ushort(__float2half_rn(h_lo));
+          ws.h16[(int64_t)pos * p.I + permuted_pos(j_hi, 16)] = __half_as_ushort(__float2half_rn(h_hi));
+        }
+      } else {
+        if ((c & 1) == 0 && n < cnt) {
+          const float inv = 1.0f / e_scale;
+          const float fct = inv * inv / e_hn * e_w;
+          ws.y[(int64_t)e_rid * p.H + row0 + g] = v_lo * fct;
+          ws.y[(int64_t)e_rid * p.H + row0 + g + 8] = v_hi * fct;
+        }
+      }
+      }
+    }
+#pragma unroll
+    for (int rh = 0; rh < C::kHalves; ++rh)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[rh][r] = 0.f;
+    if (cic == nq) {
+      cic = 0;
+      if (++rg == rgroups) { rg = 0; ++ei; }
+    }
+    first_cic = cic;
+    first_unit = false;
+    fresh = true;
+  }
+}
+
 template <int ROWS, bool FC1, bool BF16S, bool HAS_ZP>
 cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, const CUtensorMap& tz,
                               const CUtensorMap& ta, TmaDecodeArgs a, cudaStream_t s) {
@@ -1306,6 +1731,12 @@ cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, cons
 
 // The tensor-copy variant applies when both matmuls' K are multiples of 256 and
 // the zero-point rows (if any) are a multiple of 16 bytes long.
+// The INT3 tensor-copy kernel: implicit zero point, K of both matmuls a multiple of 256.
+bool decode_tma3_applies(const Problem& p, bool has_zp) {
+  return p.path == QMOE_PATH_DECODE && p.format == QMOE_FORMAT_INT && p.bits == 3 && !has_zp &&
+         p.H % kTChunkK == 0 && p.I % kTChunkK == 0;
+}
+
 bool decode_tma_applies(const Problem& p, bool has_zp) {
   if (!decode_int4_blockscaled(p) || p.H % kTChunkK || p.I % kTChunkK) return false;
   return !has_zp || ((p.H / 32) % 16 == 0 && (p.I / 32) % 16 == 0);
@@ -1354,6 +1785,42 @@ cudaError_t launch_int4_tma(const uint8_t* q, const uint16_t* scales, const uint
 }
 
 
+template <int ROWS, bool FC1>
+cudaError_t launch_int3_tma_rows(const uint8_t* q, const uint16_t* scales, const Problem& p, const Workspace& ws,
+                                 cudaStream_t s) {
+  using C = T3Cfg<ROWS>;
+  const int N = FC1 ? 2 * p.I : p.H, K = FC1 ? p.H : p.I;
+  const uint64_t rows = (uint64_t)p.E * N;
+  const uint16_t* act = FC1 ? ws.x16 : ws.h16;
+  const uint64_t arows = FC1 ? (uint64_t)p.T : (uint64_t)p.R();
+  CUtensorMap tq, ta;
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K * 3 / 8, rows, (uint64_t)K * 3 / 8, 96,
+                   ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT16, act, (uint64_t)K, arows, (uint64_t)K * 2, kTChunkK, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  Tma3Args a{N, K, p, ws, scales, 31 - __builtin_clz((unsigned)p.block)};
+  const bool bf16 = p.dtype == QMOE_BF16;
+  const cudaError_t err = bf16 ? ensure_smem_optin(decode_int3_tma_kernel<ROWS, FC1, true>, (int)C::kSmem)
+                               : ensure_smem_optin(decode_int3_tma_kernel<ROWS, FC1, false>, (int)C::kSmem);
+  if (err != cudaSuccess) return err;
+  const int64_t blocks = (int64_t)sm_count() * kTBlocksPerSm;
+  if (bf16)
+    return launch_pdl(decode_int3_tma_kernel<ROWS, FC1, true>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem,
+                      s, tq, ta, a);
+  return launch_pdl(decode_int3_tma_kernel<ROWS, FC1, false>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem,
+                    s, tq, ta, a);
+}
+
+// Unit height as for INT4.
+template <bool FC1>
+cudaError_t launch_int3_tma(const uint8_t* q, const uint16_t* scales, const Problem& p, const Workspace& ws,
+                            cudaStream_t s) {
+  const int K = FC1 ? p.H : p.I, N = FC1 ? 2 * p.I : p.H;
+  if (p.T > 2 && K / kTChunkK >= 4 && N % 32 == 0) return launch_int3_tma_rows<32, FC1>(q, scales, p, ws, s);
+  return launch_int3_tma_rows<16, FC1>(q, scales, p, ws, s);
+}
+
 template <bool FC1>
 cudaError_t launch_int4_bs(DecodeArgs a, cudaStream_t s) {
   const int64_t blocks = decode_grid_blocks();
@@ -1395,6 +1862,9 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
                         const uint8_t* zp, const Workspace& ws, cudaStream_t s) {
   const int64_t R = p.R();
   const int active_max = (int)(R < p.E ? R : p.E);
+  if (BITS == 3 && decode_tma3_applies(p, zp != nullptr))
+    return fc1 ? launch_int3_tma<true>(q, static_cast<const uint16_t*>(scales), p, ws, s)
+               : launch_int3_tma<false>(q, static_cast<const uint16_t*>(scales), p, ws, s);
   if (BITS == 4 && decode_tma_applies(p, zp != nullptr))
     return fc1 ? launch_int4_tma<true>(q, static_cast<const uint16_t*>(scales), zp, p, ws, s)
                : launch_int4_tma<false>(q, static_cast<const uint16_t*>(scales), zp, p, ws, s);
@@ -1430,7 +1900,7 @@ int64_t decode_split_items_max(const Problem& p) {
   // two partial tiles (the piece's first and last unit) per warp of the grid, in
   // items of 128 floats: one per warp of the cp.async kernel, two (32 rows) per
   // warp of the tensor-copy kernel
-  if (!decode_int4_blockscaled(p)) return 0;
+  if (!decode_int4_blockscaled(p) && !decode_tma3_applies(p, false)) return 0;
   const int64_t bs = decode_grid_blocks() * kWarps * 2;
   const int64_t tma = (int64_t)sm_count() * kTBlocksPerSm * kTWarps * 2 * (kTPartMax / 128);
   return bs > tma ? bs : tma;
