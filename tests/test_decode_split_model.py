@@ -2,7 +2,7 @@
 decode_int4_tma_kernel).
 
 The flattened range of (work unit, 256-wide K chunk) pairs is cut into equal
-pieces of L chunks, one per warp of the persistent grid (L at least 4). A unit
+pieces of L chunks, one per warp of the persistent grid (L at least 2). A unit
 cut between warps is finished by its last arriving part: each part stores its
 FP32 partial tile in one of the warp's two slots of the workspace (slot 0 for
 the piece's first unit, slot 1 for its last), takes a ticket, and the warp that
@@ -20,7 +20,7 @@ import itertools
 
 import pytest
 
-K_MIN_PIECE = 4
+K_MIN_PIECE = 2
 
 
 def split(units, nq, gw):
@@ -80,3 +80,13 @@ def test_split_of_the_decode_layer():
     L, nw = split(28 * 48, 8, 152 * 16)
     assert L >= K_MIN_PIECE and nw <= 152 * 16
     split(28 * 128, 3, 152 * 16)
+
+
+def test_model_constant_matches_the_kernel():
+    """The minimum piece the model uses is the kernel's."""
+    import os
+    import re
+
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "quantized_mixture_experts_route_gb300", "csrc", "decode.cu")).read()
+    assert int(re.search(r"constexpr int kTMinPiece = (\d+);", src).group(1)) == K_MIN_PIECE
