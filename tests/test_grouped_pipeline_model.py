@@ -27,6 +27,7 @@ dequantisers therefore first wait until the producer has issued their stage
 into the slot (`issued_word`). test_odd_code_ring_needs_the_issued_word shows
 the model finding that race without it.
 """
+import os
 import random
 
 import pytest
@@ -252,3 +253,56 @@ def test_odd_code_ring_needs_the_issued_word():
         except AssertionError:
             failures += 1
     assert failures > 0
+
+
+# ---- ties to the CUDA source: the model's rings are the kernel's
+
+_CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                     "quantized_mixture_experts_route_gb300", "csrc")
+_GROUPED = open(os.path.join(_CSRC, "grouped.cu")).read()
+_INTERNAL = open(os.path.join(_CSRC, "qmoe_internal.cuh")).read()
+
+# the kernel's ring configuration, restated (the lines below are asserted verbatim)
+_CFG_LINES = [
+    "static constexpr int BK = BITS == 3 ? 128 : 64;",
+    "static constexpr int BN = BITS == 3 ? 128 : 256;",
+    "static constexpr int ACC = WS ? 2 : (4 * BN <= 512 ? 2 : 1);",
+    "static constexpr int SA = BITS == 3 ? 2 : 3;",
+    "static constexpr int SC = WS ? (BITS == 3 ? 4 : 2) : (BITS == 3 ? 2 : (BITS == 4 ? 3 : 4));",
+    "static constexpr int SB = BITS == 3 ? 2 : 3;",
+    "static constexpr int CK = WS ? kWsCodeK : BK;",
+    "static constexpr int R = CK / BK;",
+]
+
+
+def _cfg(bits, ws):
+    bk = 128 if bits == 3 else 64
+    bn = 128 if bits == 3 else 256
+    acc = 2 if ws else (2 if 4 * bn <= 512 else 1)
+    sa = 2 if bits == 3 else 3
+    sc = (4 if bits == 3 else 2) if ws else (2 if bits == 3 else (3 if bits == 4 else 4))
+    sb = 2 if bits == 3 else 3
+    r = (256 if ws else bk) // bk
+    return sa, sb, sc, acc, r
+
+
+def test_kernel_rings_are_the_models():
+    for line in _CFG_LINES:
+        assert line in _GROUPED, line
+    assert "constexpr int kWsCodeK = 256;" in _INTERNAL
+    covered = {(c[2], c[3], c[4], c[5], c[8] if len(c) > 8 else 1) for c in CONFIGS}
+    for bits in (2, 3, 4):
+        for ws in (False, True):
+            assert _cfg(bits, ws) in covered, (bits, ws, _cfg(bits, ws))
+
+
+def test_kernel_protocol_lines_are_the_models():
+    """The arrival counts, the copy numbering, the issued-stage guard and the
+    scale-box release rule that the model replays."""
+    for line in ["mbar_init(bar_cempty(s), kDequantThreads * C::R);",
+                 "const int ic = j * kcopies + i / C::R;",
+                 "if (C::R == 1 && SC % 2 == 1 && !word_wait(cfill + cs, ic, abort_flag, launch_err))",
+                 "if (i + 2 >= box_end) mbar_arrive_cnt(bar_sempty(m_cur & 1), box_end - box0 >= 2 ? 1u : 2u);",
+                 "mbar_init(bar_sempty(b), 2 * kDequantThreads);",
+                 "if ((it & 1) != grp) continue;"]:
+        assert line in _GROUPED, line
