@@ -1295,25 +1295,27 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int4_tma_k
 }
 
 // ---------------------------------------------------------------------------
-// INT3 (implicit zero point 4), blocks of 32, 64 or 128, K a multiple of 256:
-// the tensor-copy kernel's walk, tickets and epilogues with 3-bit codes. A
-// chunk's codes are one [rows][96 B] box; lane c takes its 32 codes of a
-// 128-wide half as 12 bytes, byte permutes put two 8-code groups in the two
-// 16-bit halves, and one shift and one AND/OR per pair give 1024 + code in
-// FP16, in the same 16-group K permutation as the activations. One bias MMA
-// per K step (operand -(1024 + 4)) is shared by all row halves. The block
+// INT3 and INT2 (implicit zero points 4 and 2), blocks of 32, 64 or 128, K a
+// multiple of 256: the tensor-copy kernel's walk, tickets and epilogues with
+// 3- or 2-bit codes. A chunk's codes are one [rows][32 * BITS bytes] box; lane
+// c takes its 32 codes of a 128-wide half as 4 * BITS bytes (INT3: byte permutes
+// put two 8-code groups in the two 16-bit halves), and one shift and one
+// AND/OR per pair give 1024 + code in FP16, in the same 16-group K permutation
+// as the activations. One bias MMA per K step (operand -(1024 + zp)) is shared
+// by all row halves. The block
 // scales come by one 16-, 8- or 4-byte load per lane and row, stored into the
 // slot one chunk later (scale rows need not be a multiple of 16 bytes, as a
 // tensor copy would require); each D column takes the scale of the block its
 // owner lane's codes fall in.
 // ---------------------------------------------------------------------------
-template <int ROWS>
-struct T3Cfg {
+template <int BITS, int ROWS>
+struct T23Cfg {
   static constexpr int kRows = ROWS;
   static constexpr int kHalves = ROWS / 16;
   static constexpr int kRing = 3;                     // chunks per warp: two in flight, one in use
-  static constexpr int kCode = 0;                     // [ROWS][96 B]
-  static constexpr int kScale = ROWS * 96;            // [ROWS][8] 16-bit scales (the first 8, 4 or 2 used)
+  static constexpr int kCodeRow = 32 * BITS;          // code bytes of a row in a 256-wide chunk
+  static constexpr int kCode = 0;                     // [ROWS][kCodeRow]
+  static constexpr int kScale = ROWS * kCodeRow;      // [ROWS][8] 16-bit scales (the first 8, 4 or 2 used)
   static constexpr int kAct0 = kScale + ROWS * 16;
   static constexpr int kAct1 = kAct0 + 512;
   static constexpr int kSlot = kAct1 + 512;
@@ -1322,7 +1324,7 @@ struct T3Cfg {
   static_assert(kScale % 128 == 0 && kAct0 % 128 == 0 && kSlot % 128 == 0, "copies land on 128-byte boundaries");
 };
 
-struct Tma3Args {
+struct Tma23Args {
   int N, K;
   Problem p;
   Workspace ws;
@@ -1330,10 +1332,11 @@ struct Tma3Args {
   int lb;                  // log2(block)
 };
 
-template <int ROWS, bool FC1, bool BF16S>
-__global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int3_tma_kernel(
-    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ta, Tma3Args a) {
-  using C = T3Cfg<ROWS>;
+template <int BITS, int ROWS, bool FC1, bool BF16S>
+__global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int23_tma_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ta, Tma23Args a) {
+  static_assert(BITS == 2 || BITS == 3, "3- or 2-bit codes");
+  using C = T23Cfg<BITS, ROWS>;
   // fc1 needs the routing kernel's results at once. fc2 reads only the routing
   // results (complete: fc1 let fc2 be scheduled only after waiting for routing)
   // and its own weights before it waits for fc1, so its first weight copies
@@ -1434,8 +1437,8 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int3_tma_k
     }
     const int kx = p_cic * kTChunkK;
     if (lane == 0) {
-      mbar_expect_tx_only(p_bar, ROWS * 96);
-      tma_load_2d(p_slot_s + C::kCode, &tq, p_bar, kx / 8 * 3, p_row);
+      mbar_expect_tx_only(p_bar, ROWS * C::kCodeRow);
+      tma_load_2d(p_slot_s + C::kCode, &tq, p_bar, kx / 8 * BITS, p_row);
     }
     // the previous chunk's scales go to its slot; this chunk's are loaded
     scale_store();
@@ -1471,11 +1474,11 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int3_tma_k
       if (u < pre) issue_act(q_slot[u], q_bar[u], q_kx[u], q_t0[u], q_t1[u], q_cnt[u]);
   }
 
-  // the implicit zero point 4 of every code: -(1024 + 4) in every FP16 operand
-  const __half2 nb_d = __float2half2_rn(-(1024.0f + 4.0f));
+  // the implicit zero point 2^(BITS-1) of every code: -(1024 + zp) in every FP16 operand
+  const __half2 nb_d = __float2half2_rn(-(1024.0f + (float)(1 << (BITS - 1))));
   const uint32_t nb_def = *reinterpret_cast<const uint32_t*>(&nb_d);
   // per-lane shared-memory offsets within a slot
-  const uint32_t code_off = g * 96 + c * 12;    // row g of the [rows][96 B] code tile, lane c's 32 codes
+  const uint32_t code_off = g * C::kCodeRow + c * (4 * BITS);   // row g of the code tile, lane c's 32 codes
   // the blocks of this lane's two D columns (owner lanes 2c & 3 and (2c + 1) & 3) in each 128-wide half
   // of the chunk, as byte offsets into a row's scales
   uint32_t blk_off[2][2];
@@ -1571,29 +1574,41 @@ __global__ void __launch_bounds__(32 * kTWarps, kTBlocksPerSm) decode_int3_tma_k
         mma16816(tb[sub][j & 1], nb_def, nb_def, nb_def, nb_def, bw[sub][2 * j], bw[sub][2 * j + 1]);
 #pragma unroll
     for (int rh = 0; rh < C::kHalves; ++rh) {
-      const uint32_t cb_ = sb + code_off + rh * (16 * 96);                 // rows 16 rh + g and + 8
+      const uint32_t cb_ = sb + code_off + rh * (16 * C::kCodeRow);        // rows 16 rh + g and + 8
       const uint32_t sr = sb + C::kScale + (rh * 16 + g) * 16;
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
-        // lane c's 32 codes of rows g and g + 8 in this 128-wide half: 12 bytes each
-        uint32_t wa[3], wb[3];
-        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(wa[0]) : "r"(cb_ + sub * 48));
-        asm volatile("ld.shared.u32 %0, [%1+4];\n" : "=r"(wa[1]) : "r"(cb_ + sub * 48));
-        asm volatile("ld.shared.u32 %0, [%1+8];\n" : "=r"(wa[2]) : "r"(cb_ + sub * 48));
-        asm volatile("ld.shared.u32 %0, [%1+768];\n" : "=r"(wb[0]) : "r"(cb_ + sub * 48));
-        asm volatile("ld.shared.u32 %0, [%1+772];\n" : "=r"(wb[1]) : "r"(cb_ + sub * 48));
-        asm volatile("ld.shared.u32 %0, [%1+776];\n" : "=r"(wb[2]) : "r"(cb_ + sub * 48));
-        // byte permutes: the two 8-code groups of each 16 in the two 16-bit halves
-        const uint32_t va[4] = {__byte_perm(wa[0], wa[1], 0x4310), __byte_perm(wa[0], wa[1], 0x5421),
-                                __byte_perm(wa[1], wa[2], 0x6532), __byte_perm(wa[1], wa[2], 0x7643)};
-        const uint32_t vb[4] = {__byte_perm(wb[0], wb[1], 0x4310), __byte_perm(wb[0], wb[1], 0x5421),
-                                __byte_perm(wb[1], wb[2], 0x6532), __byte_perm(wb[1], wb[2], 0x7643)};
-        // pair p: codes (16 (p / 8) + m, 16 (p / 8) + m + 8), m = p % 8, as 1024 + code
+        // lane c's 32 codes of rows g and g + 8 in this 128-wide half: 4 * BITS bytes each
         constexpr uint32_t kMagic = 0x64006400u;
+        uint32_t va[4], vb[4];
+        const uint32_t ra = cb_ + sub * (16 * BITS), rb = ra + 8 * C::kCodeRow;
+        if constexpr (BITS == 3) {
+          uint32_t wa[3], wb[3];
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(wa[q]) : "r"(ra + 4 * q));
+            asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(wb[q]) : "r"(rb + 4 * q));
+          }
+          // byte permutes: the two 8-code groups of each 16 in the two 16-bit halves
+          va[0] = __byte_perm(wa[0], wa[1], 0x4310); va[1] = __byte_perm(wa[0], wa[1], 0x5421);
+          va[2] = __byte_perm(wa[1], wa[2], 0x6532); va[3] = __byte_perm(wa[1], wa[2], 0x7643);
+          vb[0] = __byte_perm(wb[0], wb[1], 0x4310); vb[1] = __byte_perm(wb[0], wb[1], 0x5421);
+          vb[2] = __byte_perm(wb[1], wb[2], 0x6532); vb[3] = __byte_perm(wb[1], wb[2], 0x7643);
+        } else {
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(va[0]), "=r"(va[1]) : "r"(ra));
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(vb[0]), "=r"(vb[1]) : "r"(rb));
+          va[2] = va[3] = vb[2] = vb[3] = 0u;
+        }
+        // pair p as 1024 + code: INT3 codes (16 (p / 8) + m, 16 (p / 8) + m + 8), m = p % 8;
+        // INT2 codes (16 (p / 8) + m, + 8) of word p / 8
         auto pair = [&](const uint32_t* v, int p) -> uint32_t {
           const int gq = p >> 3, m = p & 7;
-          const uint32_t w = m < 5 ? v[2 * gq] >> (3 * m) : v[2 * gq + 1] >> (3 * m - 8);
-          return lop3_and_or(w, 0x00070007u, kMagic);
+          if constexpr (BITS == 3) {
+            const uint32_t w = m < 5 ? v[2 * gq] >> (3 * m) : v[2 * gq + 1] >> (3 * m - 8);
+            return lop3_and_or(w, 0x00070007u, kMagic);
+          } else {
+            return lop3_and_or(v[gq] >> (2 * m), 0x00030003u, kMagic);
+          }
         };
         float t[2][4];
 #pragma unroll
@@ -1731,9 +1746,9 @@ cudaError_t launch_int4_tma_t(const CUtensorMap& tq, const CUtensorMap& ts, cons
 
 // The tensor-copy variant applies when both matmuls' K are multiples of 256 and
 // the zero-point rows (if any) are a multiple of 16 bytes long.
-// The INT3 tensor-copy kernel: implicit zero point, K of both matmuls a multiple of 256.
-bool decode_tma3_applies(const Problem& p, bool has_zp) {
-  return p.path == QMOE_PATH_DECODE && p.format == QMOE_FORMAT_INT && p.bits == 3 && !has_zp &&
+// The INT3 / INT2 tensor-copy kernel: implicit zero point, K of both matmuls a multiple of 256.
+bool decode_tma23_applies(const Problem& p, bool has_zp) {
+  return p.path == QMOE_PATH_DECODE && p.format == QMOE_FORMAT_INT && (p.bits == 3 || p.bits == 2) && !has_zp &&
          p.H % kTChunkK == 0 && p.I % kTChunkK == 0;
 }
 
@@ -1785,40 +1800,40 @@ cudaError_t launch_int4_tma(const uint8_t* q, const uint16_t* scales, const uint
 }
 
 
-template <int ROWS, bool FC1>
-cudaError_t launch_int3_tma_rows(const uint8_t* q, const uint16_t* scales, const Problem& p, const Workspace& ws,
-                                 cudaStream_t s) {
-  using C = T3Cfg<ROWS>;
+template <int BITS, int ROWS, bool FC1>
+cudaError_t launch_int23_tma_rows(const uint8_t* q, const uint16_t* scales, const Problem& p, const Workspace& ws,
+                                  cudaStream_t s) {
+  using C = T23Cfg<BITS, ROWS>;
   const int N = FC1 ? 2 * p.I : p.H, K = FC1 ? p.H : p.I;
   const uint64_t rows = (uint64_t)p.E * N;
   const uint16_t* act = FC1 ? ws.x16 : ws.h16;
   const uint64_t arows = FC1 ? (uint64_t)p.T : (uint64_t)p.R();
   CUtensorMap tq, ta;
-  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K * 3 / 8, rows, (uint64_t)K * 3 / 8, 96,
-                   ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+  if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K * BITS / 8, rows, (uint64_t)K * BITS / 8,
+                   C::kCodeRow, ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT16, act, (uint64_t)K, arows, (uint64_t)K * 2, kTChunkK, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  Tma3Args a{N, K, p, ws, scales, 31 - __builtin_clz((unsigned)p.block)};
+  Tma23Args a{N, K, p, ws, scales, 31 - __builtin_clz((unsigned)p.block)};
   const bool bf16 = p.dtype == QMOE_BF16;
-  const cudaError_t err = bf16 ? ensure_smem_optin(decode_int3_tma_kernel<ROWS, FC1, true>, (int)C::kSmem)
-                               : ensure_smem_optin(decode_int3_tma_kernel<ROWS, FC1, false>, (int)C::kSmem);
+  const cudaError_t err = bf16 ? ensure_smem_optin(decode_int23_tma_kernel<BITS, ROWS, FC1, true>, (int)C::kSmem)
+                               : ensure_smem_optin(decode_int23_tma_kernel<BITS, ROWS, FC1, false>, (int)C::kSmem);
   if (err != cudaSuccess) return err;
   const int64_t blocks = (int64_t)sm_count() * kTBlocksPerSm;
   if (bf16)
-    return launch_pdl(decode_int3_tma_kernel<ROWS, FC1, true>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem,
-                      s, tq, ta, a);
-  return launch_pdl(decode_int3_tma_kernel<ROWS, FC1, false>, dim3((unsigned)blocks), dim3(32 * kTWarps), C::kSmem,
-                    s, tq, ta, a);
+    return launch_pdl(decode_int23_tma_kernel<BITS, ROWS, FC1, true>, dim3((unsigned)blocks), dim3(32 * kTWarps),
+                      C::kSmem, s, tq, ta, a);
+  return launch_pdl(decode_int23_tma_kernel<BITS, ROWS, FC1, false>, dim3((unsigned)blocks), dim3(32 * kTWarps),
+                    C::kSmem, s, tq, ta, a);
 }
 
 // Unit height as for INT4.
-template <bool FC1>
-cudaError_t launch_int3_tma(const uint8_t* q, const uint16_t* scales, const Problem& p, const Workspace& ws,
-                            cudaStream_t s) {
+template <int BITS, bool FC1>
+cudaError_t launch_int23_tma(const uint8_t* q, const uint16_t* scales, const Problem& p, const Workspace& ws,
+                             cudaStream_t s) {
   const int K = FC1 ? p.H : p.I, N = FC1 ? 2 * p.I : p.H;
-  if (p.T > 2 && K / kTChunkK >= 4 && N % 32 == 0) return launch_int3_tma_rows<32, FC1>(q, scales, p, ws, s);
-  return launch_int3_tma_rows<16, FC1>(q, scales, p, ws, s);
+  if (p.T > 2 && K / kTChunkK >= 4 && N % 32 == 0) return launch_int23_tma_rows<BITS, 32, FC1>(q, scales, p, ws, s);
+  return launch_int23_tma_rows<BITS, 16, FC1>(q, scales, p, ws, s);
 }
 
 template <bool FC1>
@@ -1862,9 +1877,10 @@ cudaError_t launch_bits(const Problem& p, bool fc1, const uint8_t* q, const void
                         const uint8_t* zp, const Workspace& ws, cudaStream_t s) {
   const int64_t R = p.R();
   const int active_max = (int)(R < p.E ? R : p.E);
-  if (BITS == 3 && decode_tma3_applies(p, zp != nullptr))
-    return fc1 ? launch_int3_tma<true>(q, static_cast<const uint16_t*>(scales), p, ws, s)
-               : launch_int3_tma<false>(q, static_cast<const uint16_t*>(scales), p, ws, s);
+  if constexpr (BITS == 2 || BITS == 3)
+    if (decode_tma23_applies(p, zp != nullptr))
+      return fc1 ? launch_int23_tma<BITS, true>(q, static_cast<const uint16_t*>(scales), p, ws, s)
+                 : launch_int23_tma<BITS, false>(q, static_cast<const uint16_t*>(scales), p, ws, s);
   if (BITS == 4 && decode_tma_applies(p, zp != nullptr))
     return fc1 ? launch_int4_tma<true>(q, static_cast<const uint16_t*>(scales), zp, p, ws, s)
                : launch_int4_tma<false>(q, static_cast<const uint16_t*>(scales), zp, p, ws, s);
@@ -1900,7 +1916,7 @@ int64_t decode_split_items_max(const Problem& p) {
   // two partial tiles (the piece's first and last unit) per warp of the grid, in
   // items of 128 floats: one per warp of the cp.async kernel, two (32 rows) per
   // warp of the tensor-copy kernel
-  if (!decode_int4_blockscaled(p) && !decode_tma3_applies(p, false)) return 0;
+  if (!decode_int4_blockscaled(p) && !decode_tma23_applies(p, false)) return 0;
   const int64_t bs = decode_grid_blocks() * kWarps * 2;
   const int64_t tma = (int64_t)sm_count() * kTBlocksPerSm * kTWarps * 2 * (kTPartMax / 128);
   return bs > tma ? bs : tma;

@@ -1,5 +1,5 @@
-"""A host model of the INT3 decode kernel's block-scale staging
-(csrc/decode.cu, decode_int3_tma_kernel).
+"""A host model of the INT3 / INT2 decode kernel's block-scale staging
+(csrc/decode.cu, decode_int23_tma_kernel).
 
 Each warp walks its piece of `total` chunks through a ring of kRing shared-
 memory slots. Issuing chunk i (in the prologue for i < kRing - 1, otherwise
@@ -22,7 +22,7 @@ SRC = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__
 
 
 def kernel_ring():
-    body = SRC[SRC.index("struct T3Cfg {"):SRC.index("struct Tma3Args {")]
+    body = SRC[SRC.index("struct T23Cfg {"):SRC.index("struct Tma23Args {")]
     return int(re.search(r"static constexpr int kRing = (\d+);", body).group(1))
 
 
@@ -71,7 +71,7 @@ def test_scales_in_place_before_use(total):
 
 def test_the_kernel_follows_the_model():
     """The issue lambda stores before it loads, and an iteration without an issue stores."""
-    body = SRC[SRC.index("decode_int3_tma_kernel("):]
+    body = SRC[SRC.index("decode_int23_tma_kernel("):]
     i_store = body.index("    scale_store();\n    if (lane < ROWS) {")
     i_load = body.index("s_pend = __ldg(")
     assert i_store < i_load
