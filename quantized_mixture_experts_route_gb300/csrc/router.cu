@@ -140,7 +140,10 @@ __global__ void __launch_bounds__(kRThreads) router_logits_kernel(Problem p, con
 // 16-byte asynchronous copies (rows past T or E are filled with zeros), and each
 // of the 8 warps multiplies 16 or 32 tokens x 32 experts from fragments read
 // with ldmatrix. Rows are padded to 144 bytes so that the eight 16-byte rows an
-// ldmatrix phase reads fall in distinct bank groups.
+// ldmatrix phase reads fall in distinct bank groups. The block's time is the
+// SM's mma.sync throughput over its K loop (about 2 TFLOP/s per SM); 128-wide K
+// steps halved the steps but not the time (8K tokens 22.6 us, 32K slower with
+// one block per SM).
 constexpr int kGN = 128, kGK = 64, kGStages = 4, kGPitch = 72;   // pitch in 16-bit elements
 constexpr int kGThreads = 256;
 
@@ -260,9 +263,10 @@ cudaError_t launch_gemm(const Problem& p, const uint16_t* x, const uint16_t* w, 
 
 template <bool BF16>
 cudaError_t launch_dtype(const Problem& p, const uint16_t* x, const uint16_t* w, uint16_t* out, cudaStream_t s) {
-  if (p.T <= 64) {
-    // decode-sized batches: 8 experts per block, K split 16 ways, so that the
-    // router weight streams through E / 8 blocks of 16 warps
+  if (p.T <= 64 || p.H % kGK != 0) {
+    // decode-sized batches (and hidden sizes the tiled GEMM's K steps do not
+    // divide): 8 experts per block, K split 16 ways, so that the router weight
+    // streams through E / 8 blocks of 16 warps
     constexpr int KS = 16;
     const int64_t tiles = (p.T + 15) / 16;
     const dim3 grid((p.E + 7) / 8, (unsigned)tiles);

@@ -86,6 +86,10 @@ SHAPES = {
     "mid_T33_E100": (Shape(T=33, H=1024, inter=256, E=100, k=6, bits=4, block=32, dtype=BF16), 93),
     "prefill_T1000": (Shape(T=1000, H=2048, inter=768, E=128, k=8, bits=4, block=32, dtype=BF16), 94),
     "tiny_E8": (Shape(T=5, H=64, inter=32, E=8, k=2, bits=4, block=32, dtype=FP16), 95),
+    # the tiled GEMM with 32-token tiles, H not a multiple of 128
+    "gemm_k64_T200": (Shape(T=200, H=320, inter=128, E=64, k=4, bits=4, block=32, dtype=BF16), 96),
+    # 64-token tiles, a ragged token tail and E above one 128-expert block
+    "gemm_T4100_E160": (Shape(T=4100, H=1024, inter=256, E=160, k=8, bits=4, block=32, dtype=BF16), 98),
 }
 
 
