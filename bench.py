@@ -488,8 +488,9 @@ def time_graph(g, stream, steps, warmup, device, clock_path, world):
     import torch
     import torch.distributed as dist
 
-    for _ in range(warmup):
-        g.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -509,13 +510,25 @@ def time_graph(g, stream, steps, warmup, device, clock_path, world):
     return step_ms, ms, clocks.summary()
 
 
+def replay_synchronised(g, stream):
+    """One replay on `stream` (the stage graphs read the workspace state it leaves),
+    finished before anything else is timed."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+
+
 def time_stages(graphs, stream, steps, launches):
     """ms per launch of each stage: events around `steps` replays of its graph."""
     import torch
 
     out = np.zeros(len(graphs))
     for st, gst in enumerate(graphs):
-        gst.replay()   # warm
+        with torch.cuda.stream(stream):
+            gst.replay()   # warm, on the timed stream, finished before the timed region
+        torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -615,7 +628,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     step_ms, ms, clocks = time_graph(g, s, args.steps, args.warmup, device, args.clock_log, world)
-    g.replay()
+    replay_synchronised(g, s)
     stage_ms = time_stages(gs, s, args.steps, layers)
     e2e_s = time_e2e(stack, g, s, args.steps, device)
 
@@ -631,7 +644,7 @@ def run_ours(args):
         psteps = args.prefill_steps or args.steps
         pclock = (args.clock_log + ".prefill") if args.clock_log else None
         pstep_ms, pms, pclocks = time_graph(pg, s, psteps, args.warmup, device, pclock, world)
-        pg.replay()
+        replay_synchronised(pg, s)
         pstage_ms = time_stages(pgs, s, psteps, layers)
         pe2e_s = time_e2e(pstack, pg, s, psteps, device)
         prefill = dict(shape=pshape, recipe=precipe, stack=pstack, step_ms=pstep_ms, ms=pms, clocks=pclocks,
