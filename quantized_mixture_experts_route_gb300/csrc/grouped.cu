@@ -899,6 +899,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sigma_h[half] = ok_h[half] ? ws.tok_scale[rid_h[half] / p.k] : 1.0f;
         wr_h[half] = FC1 ? 0.f : (ok_h[half] ? ws.topk_w[rid_h[half]] : 0.f);
       }
+      // fc1 biases of the tile's BN weight rows, loaded before the accumulators are
+      // waited for: lane l holds rows n0 + 8 l .. + 7 (four gate/up pairs); the
+      // column loop takes its 16 pairs from the lanes by shuffles
+      uint4 bias_v = make_uint4(0u, 0u, 0u, 0u);
+      if (FC1 && p.b1 && 8 * lane < C::BN && n0 + 8 * lane < N)
+        bias_v = __ldg(reinterpret_cast<const uint4*>(p.b1 + (int64_t)e * N + n0 + 8 * lane));
       const int buf = j % C::ACC;
       if (!mbar_wait(bar_accum(buf), (uint32_t)(j / C::ACC) & 1u, abort_flag, launch_err)) break;
       tc_fence_after();
@@ -924,8 +930,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 32 * cpart; c0 < C::BN; c0 += 32 * (kEpiWarps / 4)) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)c0, v);
-        if (!row_ok || n0 + c0 >= N) continue;
+        if (n0 + c0 >= N) continue;              // the same for the whole warp
         if constexpr (FC1) {
+          // every lane takes part in the bias shuffles; rows past the tile's routes
+          // (row_ok false) compute and store nothing
           // columns are W1 rows n0 + c0 .. +31: gate/up pairs -> 16 outputs h_j
           const int j0 = (n0 + c0) / 2;
           constexpr int G = BITS == 4 ? 8 : 16;
@@ -935,7 +943,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.b1) {
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-              const float2 bq = fc1_bias_pair(p, e, j0 + q);
+              // pair j0 + q = the tile's pair c0 / 2 + q: lane c0 / 8 + q / 4, element q % 4
+              const uint32_t src = (q & 3) == 0 ? bias_v.x : (q & 3) == 1 ? bias_v.y : (q & 3) == 2 ? bias_v.z : bias_v.w;
+              const uint32_t braw = __shfl_sync(0xffffffffu, src, (c0 >> 3) + (q >> 2));
+              const float2 bq = make_float2(half_bits_to_float((uint16_t)(braw & 0xFFFFu), p.dtype),
+                                            half_bits_to_float((uint16_t)(braw >> 16), p.dtype));
               const float gt = __uint_as_float(v[2 * q]) * inv + bq.x;
               const float ut = __uint_as_float(v[2 * q + 1]) * inv + bq.y;
               hv[q] = __half_as_ushort(__float2half_rn(__fdividef(gt, 1.0f + __expf(-gt)) * ut * ss));
@@ -957,12 +969,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 16; ++q) ov[permuted_pos(q, G)] = hv[q];
           }
           // one 32-byte store: a whole sector per lane
+          if (row_ok)
           st_global_v8(ws.h16 + (int64_t)pos * p.I + j0,
                        ov[0] | ((uint32_t)ov[1] << 16), ov[2] | ((uint32_t)ov[3] << 16),
                        ov[4] | ((uint32_t)ov[5] << 16), ov[6] | ((uint32_t)ov[7] << 16),
                        ov[8] | ((uint32_t)ov[9] << 16), ov[10] | ((uint32_t)ov[11] << 16),
                        ov[12] | ((uint32_t)ov[13] << 16), ov[14] | ((uint32_t)ov[15] << 16));
         } else {
+          if (!row_ok) continue;
           const float f = inv * inv1 / hn * wr;
           float* dst = ws.y + (int64_t)rid * p.H + n0 + c0;
 #pragma unroll
