@@ -34,8 +34,13 @@ __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
     for (int j0 = 0; j0 < p.k; j0 += 8) {
       float w[8];
       float4 a[8], b[8];
+      int ex[8];
+      uint4 bbv[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[j] = j0 + j < p.k ? ws.topk_w[t * p.k + j0 + j] : 0.0f;
+      if (p.b2)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ex[j] = ws.topk_idx[t * p.k + (j0 + j < p.k ? j0 + j : j0)];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int64_t r = t * p.k + (j0 + j < p.k ? j0 + j : j0);
@@ -43,12 +48,16 @@ __global__ void __launch_bounds__(256) combine_kernel(Problem p, Workspace ws,
         a[j] = src[0];
         b[j] = src[1];
       }
+      // the batch's FC2 bias rows, all issued before the first is used (each waits
+      // for its route's expert only)
+      if (p.b2)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) bbv[j] = *reinterpret_cast<const uint4*>(p.b2 + (int64_t)ex[j] * p.H + h0);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (w[j] == 0.0f) continue;   // also the batch's padding past k
         if (p.b2) {
-          const int e = ws.topk_idx[t * p.k + j0 + j];
-          const uint4 bb = *reinterpret_cast<const uint4*>(p.b2 + (int64_t)e * p.H + h0);
+          const uint4 bb = bbv[j];
           const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
           float bv[8];
 #pragma unroll
