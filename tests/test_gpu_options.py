@@ -43,6 +43,13 @@ CASES = {
                                Recipe(logit_std=1.0, scale_lo=0.01, scale_hi=0.04, bias_std=0.5), 77, 2, 1),
     "grouped_int3_full": (Shape(T=260, H=256, inter=256, E=5, k=2, bits=3, block=32, dtype=BF16),
                           Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02), 78, 2, 1),
+    # route tiles with fc1 biases: the epilogue takes a tile's biases from the lanes of
+    # one per-tile load; fc1 N = 640 and fc2 N = 448 end in part-filled 256-row tiles
+    "tiles_int4_bias_fp16_tail": (Shape(T=250, H=448, inter=320, E=6, k=3, bits=4, block=32, dtype=FP16),
+                                  Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, bias_std=0.5), 79, 3, 0),
+    # INT3 route tiles: 128-row weight tiles (lanes 0-15 hold the tile's biases)
+    "tiles_int3_bias_full": (Shape(T=260, H=384, inter=384, E=5, k=2, bits=3, block=128, dtype=BF16),
+                             Recipe(logit_std=1.0, scale_lo=0.005, scale_hi=0.02, bias_std=0.5), 80, 3, 1),
 }
 
 
